@@ -1,0 +1,166 @@
+/*
+ * ssd.h -- C ABI of the GB300 (sm_103a) Mamba-2 SSD chunked forward pass.
+ *
+ * Per head h (group g = h / (nheads / ngroups)) and token t the library
+ * computes the selective state-space recurrence
+ *
+ *     hs_t = exp(dt_t * A_h) * hs_{t-1} + B_t (dt_t * x_t)^T      (N x P state)
+ *     y_t  = C_t . hs_t + D_h * x_t
+ *
+ * in chunks of Q = chunk_size tokens, as three stages:
+ *   chunk_cumsum   -- in-chunk cumulative sum of dt*A in log2 units;
+ *   fwd_pass_state -- per-chunk states B^T (decay * dt * X) (ssd_chunk_state)
+ *                     then the sequential jump across chunks (ssd_state_passing);
+ *   compute_out    -- carried-state term, causally masked decayed C B^T X term
+ *                     and D skip, fused (ssd_chunk_scan).
+ * Sources (web pages, by title and section):
+ *   "Jane Street ML Engineers Map Mamba-2 Recurrent State Computation to
+ *   Tensor Cores with cuTile" (disconfirmai.com) -- three-kernel paragraph and
+ *   jump-formula paragraph; devotd.net page on the Mamba-2 cuTile forward
+ *   kernels, section 2 (the three kernels and the chunk_cumsum listing) and
+ *   section 3 (transposed dA_cumsum / dt layout for contiguous reads).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  * All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never frees or retains them.  Layouts are dense row-major:
+ *        x, y        (batch, seqlen, nheads, headdim)      bfloat16
+ *        dt          (batch, seqlen, nheads)               float32, dt > 0
+ *        A, D        (nheads,)                             float32
+ *        B, C        (batch, seqlen, ngroups, dstate)      bfloat16
+ *        dA_cumsum   (batch, nheads, nchunks, chunk_size)  float32, log2 units
+ *        dt_t        (batch, nheads, nchunks, chunk_size)  float32
+ *        chunk_states, states (batch, nchunks, nheads, headdim, dstate) float32
+ *        init_state, final_state (batch, nheads, headdim, dstate)        float32
+ *    A state is stored as state[p][n] = hs[n][p] (headdim-major, dstate
+ *    contiguous).  nchunks = ceil(seqlen / chunk_size); positions past the
+ *    end of the sequence behave as dt = 0 (zero padding).
+ *  * bfloat16 tensors are passed as void pointers; each element is an IEEE
+ *    bfloat16 (the upper 16 bits of a float32).
+ *  * Every call is asynchronous on `stream` (0 = legacy default stream) and
+ *    never synchronizes the host.  The return value reports argument
+ *    validation and launch errors only; a failed validation launches nothing
+ *    and leaves every output untouched.  Device-side errors surface at the
+ *    caller's next synchronization; a bounded device wait that gave up is
+ *    reported by ssd_get_device_error().
+ *  * Supported shapes: headdim == 64; dstate in {64, 128, 256, 512};
+ *    chunk_size in {64, 128, 256}; nheads % ngroups == 0; x, B, C, y and the
+ *    float32 tensors 16-byte aligned.  Other shapes return
+ *    SSD_ERR_UNSUPPORTED (valid but not implemented) or SSD_ERR_INVALID_ARG.
+ *  * No C++ exception crosses this boundary.  The library keeps no state
+ *    between calls other than the optional profiling counters below; calls
+ *    on different streams may run concurrently.
+ */
+#ifndef SSD_GB300_H
+#define SSD_GB300_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1, /* null required pointer, non-positive size, misalignment, bad grouping */
+    SSD_ERR_UNSUPPORTED = 2, /* well-formed shape outside the implemented set */
+    SSD_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    SSD_ERR_NO_MEMORY = 4,   /* workspace allocation failed (ssd_forward) */
+    SSD_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (see ssd_get_device_error) */
+} ssd_status;
+
+/* Static, never-NULL description of a status code. */
+const char* ssd_status_string(int status);
+
+/*
+ * ssd_chunk_cumsum -- the chunk_cumsum stage (devotd.net page, section 2 and
+ * its listing: dt tile times A, cumulative sum along the chunk, times log2 e;
+ * section 3: the result and dt stored chunk-contiguous).
+ *   dA_cumsum[b,h,c,i] = log2(e) * sum_{j<=i} dt[b, c*Q+j, h] * A[h]
+ *   dt_t[b,h,c,i]      = dt[b, c*Q+i, h]          (0 past the sequence end)
+ * dt: (batch, seqlen, nheads); A: (nheads); outputs (batch, nheads, nchunks, Q).
+ */
+int ssd_chunk_cumsum(const float* dt, const float* A, int batch, int seqlen, int nheads,
+                     int chunk_size, float* dA_cumsum, float* dt_t, cudaStream_t stream);
+
+/*
+ * ssd_chunk_state -- first half of fwd_pass_state: every chunk's own state
+ * contribution (the jump formula h(t+T) = h(t) + B X^T with X's rows
+ * pre-scaled by the decay to the chunk end and by dt; disconfirmai.com page,
+ * jump-formula paragraph):
+ *   chunk_states[b,c,h][p][n] = sum_{i in chunk c} B[b,t_i,g,n] * w_i * x[b,t_i,h,p],
+ *   w_i = 2^(dA_cumsum[b,h,c,Q-1] - dA_cumsum[b,h,c,i]) * dt_t[b,h,c,i].
+ * dt_t and dA_cumsum are ssd_chunk_cumsum's outputs.
+ */
+int ssd_chunk_state(const void* x, const void* B, const float* dt_t, const float* dA_cumsum,
+                    int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                    int chunk_size, float* chunk_states, cudaStream_t stream);
+
+/*
+ * ssd_state_passing -- second half of fwd_pass_state: the sequential jump
+ * across chunks, parallel over the independent (p, n) state entries
+ * (devotd.net page, section 2: chunk order kept, independent parts of the
+ * state processed in parallel):
+ *   h_0 = init_state (zeros if NULL);  states[c] = h_c;
+ *   h_{c+1} = 2^(dA_cumsum[b,h,c,Q-1]) * h_c + chunk_states[c];
+ *   final_state = h_nchunks (not written if NULL).
+ * `states` may alias `chunk_states` (in-place update is supported).
+ */
+int ssd_state_passing(const float* chunk_states, const float* dA_cumsum, const float* init_state,
+                      int batch, int nchunks, int nheads, int headdim, int dstate, int chunk_size,
+                      float* states, float* final_state, cudaStream_t stream);
+
+/*
+ * ssd_chunk_scan -- compute_out: output of every chunk from its chunk-start
+ * state, fused so that the Q x Q interaction matrix never leaves the chip
+ * (disconfirmai.com page, three-kernel paragraph; devotd.net page, section 2):
+ *   y[t_i] = 2^(cs_i) * (C_i . h_c)
+ *          + sum_{j<=i} (C_i . B_j) * 2^(cs_i - cs_j) * dt_j * x_j
+ *          + D[h] * x_i,          cs = dA_cumsum[b,h,c,:],  h_c = states[b,c,h]
+ * D may be NULL (no skip term).  y: (batch, seqlen, nheads, headdim) bfloat16.
+ */
+int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_t,
+                   const float* dA_cumsum, const float* D, const float* states, int batch,
+                   int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk_size,
+                   void* y, cudaStream_t stream);
+
+/*
+ * ssd_forward -- the whole chunked forward pass: y and the final state from
+ * the raw inputs.  D, init_state and final_state may be NULL.  Allocates its
+ * workspace stream-ordered on `stream` (cudaMallocAsync / cudaFreeAsync) and
+ * returns SSD_ERR_NO_MEMORY if that fails.  The result equals the recurrence
+ * above for any chunk_size; chunk_size only sets the internal tiling.
+ */
+int ssd_forward(const void* x, const float* dt, const float* A, const void* B, const void* C,
+                const float* D, const float* init_state, int batch, int seqlen, int nheads,
+                int headdim, int ngroups, int dstate, int chunk_size, void* y,
+                float* final_state, cudaStream_t stream);
+
+/*
+ * ssd_get_device_error -- reads and clears the library's device error word
+ * on the current device (synchronizes with the device).  Returns SSD_OK, or
+ * SSD_ERR_TIMEOUT if a kernel's bounded wait gave up since the last read, or
+ * SSD_ERR_CUDA if the read itself failed.
+ */
+int ssd_get_device_error(void);
+
+/*
+ * Profiling counters (host side, process-wide, not thread-safe).
+ * ssd_profile_enable(1) makes every later launch record a CUDA event pair
+ * around itself on the launch stream; ssd_profile_read() waits for those
+ * events and returns, per kernel kind (see ssd_kernel_name), the summed
+ * device time in milliseconds and the launch count since the last reset.
+ * ssd_launch_count() counts every kernel the library has launched since load
+ * (profiling enabled or not).
+ */
+int ssd_profile_enable(int enable);
+int ssd_profile_reset(void);
+int ssd_profile_read(float* total_ms, int* launches, int max_kinds, int* n_kinds);
+const char* ssd_kernel_name(int kind);
+long long ssd_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_GB300_H */

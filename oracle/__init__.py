@@ -1,0 +1,189 @@
+"""CPU oracle for the Mamba-2 SSD forward pass -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports, loads or calls anything here, and this
+package imports nothing from the product.
+
+Two independent implementations live here:
+
+* ``ssd_oracle.c`` -- the token-by-token fp64 recurrence (the definition), in
+  plain C, threaded over (batch, head) units.  Wrapped below via ctypes.
+* ``closed_form.py`` -- numpy fp64 closed forms (brute-force quadratic form,
+  naive chunked form, jump formula with A = 0) used only to pin the C oracle.
+
+Array conventions (all numpy, C-contiguous):
+    x  (batch, L, H, P)   uint16 bfloat16 bit patterns
+    dt (batch, L, H)      float32
+    A  (H,)               float32
+    B, C (batch, L, G, N) uint16 bfloat16 bit patterns
+    D  (H,)               float32 or None
+    init (batch, H, P, N) float32 or None
+    states / chunk states (batch, nc, H, P, N); dA_cumsum (batch, H, nc, Q)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssd_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libssd_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ssd_oracle.c with gcc into oracle/_build/libssd_oracle.so."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm", "-lpthread"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            lib.ssd_oracle_forward.argtypes = [p] * 7 + [i64] * 7 + [p, i64, p, p, p, i32]
+            lib.ssd_oracle_chunk_states.argtypes = [p] * 4 + [i64] * 7 + [p, i64, p, i32]
+            lib.ssd_oracle_chunk_scan.argtypes = [p] * 7 + [i64] * 7 + [p, i64, p, i32]
+            lib.ssd_oracle_dA_cumsum.argtypes = [p, p, i64, i64, i64, i64, p, p]
+            lib.ssd_oracle_state_passing.argtypes = [p, p, p] + [i64] * 6 + [p, p]
+            for f in ("ssd_oracle_forward", "ssd_oracle_chunk_states", "ssd_oracle_chunk_scan",
+                      "ssd_oracle_dA_cumsum", "ssd_oracle_state_passing"):
+                getattr(lib, f).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {a.dtype}")
+    return a
+
+
+def _units(batch, nheads, units):
+    if units is None:
+        units = np.arange(batch * nheads, dtype=np.int64)
+    units = np.ascontiguousarray(np.asarray(units, dtype=np.int64))
+    if units.ndim != 1 or units.size == 0 or units.min() < 0 or units.max() >= batch * nheads:
+        raise ValueError("units must be a non-empty list of b * H + h indices")
+    return units
+
+
+def last_threads_used() -> int:
+    return _last_threads[0]
+
+
+_last_threads = [0]
+
+
+def forward(x, dt, A, B, C, D, init, chunk_size, units=None, want_chunk_starts=False, nthreads=0):
+    """Token-by-token fp64 recurrence.
+
+    Returns dict with ``y`` (nunits, L, P), ``final`` (nunits, P, N) and,
+    if requested, ``chunk_starts`` (nunits, nc, P, N): the state before each
+    chunk of ``chunk_size`` tokens.  ``units`` lists b * H + h indices
+    (default: all units, in order).
+    """
+    x, B, C = _c(x, np.uint16), _c(B, np.uint16), _c(C, np.uint16)
+    dt, A = _c(dt, np.float32), _c(A, np.float32)
+    D, init = _c(D, np.float32), _c(init, np.float32)
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    nc = -(-L // chunk_size)
+    u = _units(b, H, units)
+    y = np.empty((u.size, L, P), np.float64)
+    fin = np.empty((u.size, P, N), np.float64)
+    cst = np.empty((u.size, nc, P, N), np.float64) if want_chunk_starts else None
+    r = _load().ssd_oracle_forward(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init),
+                                   b, L, H, P, G, N, chunk_size, _ptr(u), u.size,
+                                   _ptr(y), _ptr(fin), _ptr(cst), nthreads)
+    if r < 0:
+        raise ValueError("ssd_oracle_forward: bad arguments")
+    _last_threads[0] = r
+    out = {"y": y, "final": fin}
+    if want_chunk_starts:
+        out["chunk_starts"] = cst
+    return out
+
+
+def chunk_states(x, dt, A, B, chunk_size, units=None, nthreads=0):
+    """Per chunk, the state reached from zero over that chunk alone: (nunits, nc, P, N)."""
+    x, B = _c(x, np.uint16), _c(B, np.uint16)
+    dt, A = _c(dt, np.float32), _c(A, np.float32)
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    nc = -(-L // chunk_size)
+    u = _units(b, H, units)
+    S = np.empty((u.size, nc, P, N), np.float64)
+    r = _load().ssd_oracle_chunk_states(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), b, L, H, P, G, N,
+                                        chunk_size, _ptr(u), u.size, _ptr(S), nthreads)
+    if r < 0:
+        raise ValueError("ssd_oracle_chunk_states: bad arguments")
+    return S
+
+
+def chunk_scan(x, dt, A, B, C, D, states, chunk_size, units=None, nthreads=0):
+    """Outputs with every chunk restarted from ``states`` (batch, nc, H, P, N) f32: (nunits, L, P)."""
+    x, B, C = _c(x, np.uint16), _c(B, np.uint16), _c(C, np.uint16)
+    dt, A, D = _c(dt, np.float32), _c(A, np.float32), _c(D, np.float32)
+    states = _c(states, np.float32)
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    u = _units(b, H, units)
+    y = np.empty((u.size, L, P), np.float64)
+    r = _load().ssd_oracle_chunk_scan(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(states),
+                                      b, L, H, P, G, N, chunk_size, _ptr(u), u.size, _ptr(y), nthreads)
+    if r < 0:
+        raise ValueError("ssd_oracle_chunk_scan: bad arguments")
+    return y
+
+
+def dA_cumsum(dt, A, chunk_size):
+    """Inclusive in-chunk cumsum of dt*A times log2(e), and dt, both (batch, H, nc, Q) f64."""
+    dt, A = _c(dt, np.float32), _c(A, np.float32)
+    b, L, H = dt.shape
+    nc = -(-L // chunk_size)
+    cs = np.empty((b, H, nc, chunk_size), np.float64)
+    dtt = np.empty((b, H, nc, chunk_size), np.float64)
+    r = _load().ssd_oracle_dA_cumsum(_ptr(dt), _ptr(A), b, L, H, chunk_size, _ptr(cs), _ptr(dtt))
+    if r < 0:
+        raise ValueError("ssd_oracle_dA_cumsum: bad arguments")
+    return cs, dtt
+
+
+def state_passing(S, cs, init, chunk_size):
+    """Sequential chunk hop. S (batch, nc, H, P, N) f32, cs (batch, H, nc, Q) f32, init f32 or None.
+
+    Returns (states (batch, nc, H, P, N), final (batch, H, P, N)) in f64.
+    """
+    S, cs, init = _c(S, np.float32), _c(cs, np.float32), _c(init, np.float32)
+    b, nc, H, P, N = S.shape
+    states = np.empty(S.shape, np.float64)
+    fin = np.empty((b, H, P, N), np.float64)
+    r = _load().ssd_oracle_state_passing(_ptr(S), _ptr(cs), _ptr(init), b, nc, H, P, N, chunk_size,
+                                         _ptr(states), _ptr(fin))
+    if r < 0:
+        raise ValueError("ssd_oracle_state_passing: bad arguments")
+    return states, fin
