@@ -1,0 +1,403 @@
+"""Benchmark of the SSD chunked forward pass on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one ssd_forward over one batch of the workload (all stages:
+chunk_cumsum, fwd_pass_state, compute_out) with inputs resident in HBM.
+L2 is flushed (256 MB memset) between timed steps, outside the timed events.
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from state_space_sequence_ssd_gb300 import inputs as I  # noqa: E402
+
+METRIC = "SSD forward tokens/s and TFLOP/s at L=64K, N=128; % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------ work model
+
+def alg_flops(w: I.Workload) -> float:
+    """Algorithmic FLOPs of one forward: per chunk G*Q(Q+1)*N (causal C.B^T once per group)
+    + H*(4*Q*N*P (chunk state + C.h) + Q(Q+1)*P (causal M.X)), per batch row."""
+    Q, N, P, H, G = w.chunk_size, w.dstate, w.headdim, w.nheads, w.ngroups
+    return float(w.batch * w.nchunks * (G * Q * (Q + 1) * N + H * (4 * Q * N * P + Q * (Q + 1) * P)))
+
+
+def compulsory_bytes(w: I.Workload) -> float:
+    """x read + y write (bf16), B and C (bf16), dt (f32), init/final state (f32), A and D."""
+    b, L, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    by = 2 * b * L * H * P * 2 + 2 * b * L * G * N * 2 + b * L * H * 4 + 2 * H * 4
+    by += b * H * P * N * 4  # final state write
+    if w.nonzero_init:
+        by += b * H * P * N * 4
+    return float(by)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ oracle leg
+
+def oracle_sample(w: I.Workload, inp: dict, tokens: int):
+    """Time the fp64 oracle (as it stands) on the first `tokens` tokens of every (batch, head)."""
+    import oracle
+    n = I.as_numpy(inp)
+    T = min(tokens, w.seqlen)
+    sl = {k: (None if v is None else (np.ascontiguousarray(v[:, :T]) if k in ("x", "dt", "B", "C") else v))
+          for k, v in n.items()}
+    t0 = time.perf_counter()
+    oracle.forward(sl["x"], sl["dt"], sl["A"], sl["B"], sl["C"], sl["D"], sl["init"], w.chunk_size)
+    dt = time.perf_counter() - t0
+    return w.batch * T / dt, oracle.last_threads_used(), T, dt
+
+
+# ------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=I.HEADLINE, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--oracle-tokens", type=int, default=0, help="tokens per head for the CPU oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: --warmup raised to 3 (minimum)", file=sys.stderr)
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = I.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        run_reference(args, w)
+        return 0
+
+    import torch
+    import state_space_sequence_ssd_gb300 as ssd
+    from state_space_sequence_ssd_gb300 import _ffi
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = _ffi.lib()
+
+    inp = I.make_inputs(w, seed=rank)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), device=dev, dtype=torch.float32)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ssd.ssd_forward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"], w.chunk_size, y=y,
+                        final_state=fin, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    lib.ssd_profile_reset()
+    lib.ssd_profile_enable(1)
+    launches0 = lib.ssd_launch_count()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    launches = lib.ssd_launch_count() - launches0
+    lib.ssd_profile_enable(0)
+    clk = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(step_ms))
+    import ctypes
+    kms = (ctypes.c_float * 16)()
+    kcnt = (ctypes.c_int * 16)()
+    nk = ctypes.c_int(0)
+    lib.ssd_profile_read(kms, kcnt, 16, ctypes.byref(nk))
+    kernels = {lib.ssd_kernel_name(k).decode(): {"ms_total": float(kms[k]), "launches": int(kcnt[k])}
+               for k in range(nk.value) if kcnt[k] > 0}
+    err = ssd.ssd_get_device_error()
+
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- end to end through the public call with host buffers
+    e2e = e2e_measure(w, inp, dev, stream, args, ssd, dist)
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    ms_per_step = total_ms / args.steps
+    tokens = w.batch * w.seqlen * world
+    value = tokens / (ms_per_step / 1e3)
+    flops = alg_flops(w)
+    cbytes = compulsory_bytes(w)
+    peaks, peaks_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    tflops_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    t_roof_us = max(flops / (tflops_peak * 1e12), cbytes / (hbm * 1e9)) * 1e6
+
+    # dominant kernel and its algorithmic bytes per launch
+    dom = max(kernels.items(), key=lambda kv: kv[1]["ms_total"]) if kernels else (None, None)
+    roof = None
+    if dom[0] is not None:
+        name, st = dom
+        avg_ms = st["ms_total"] / max(1, st["launches"])
+        kb = kernel_alg_bytes(name, w)
+        achieved = kb / (avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "peak_source": f"{peaks_src} hbm_gbs (copy)",
+                "alg_bytes_per_launch": kb, "avg_launch_us": round(avg_ms * 1e3, 2),
+                "traffic": kernel_traffic(name, w)}
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; x,B,C ~N(0,1) bf16, dt=softplus(N(0,1)-4), A=-exp(U(0,ln16)), D~N(0,1))",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk_size": w.chunk_size,
+                   "nonzero_init": w.nonzero_init, "l2": "flushed between steps (256 MB memset, untimed)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tflops": round(flops / (ms_per_step / 1e3) / 1e12, 2),
+        "pass_roofline": {"t_roofline_us": round(t_roof_us, 2), "t_measured_us": round(ms_per_step * 1e3, 2),
+                          "frac": round(t_roof_us / (ms_per_step * 1e3), 4),
+                          "alg_gflop": round(flops / 1e9, 3), "compulsory_mb": round(cbytes / 1e6, 2),
+                          "peaks": f"{peaks_src}: {hbm} GB/s, {tflops_peak} TFLOP/s bf16"},
+        "roofline": roof,
+        "kernels": kernels,
+        "gpu_launches": int(launches),
+        "e2e": e2e,
+        "clocks": clk,
+        "device_error": int(err),
+    }
+    if not args.no_cpu_baseline:
+        tok = args.oracle_tokens or default_oracle_tokens(w)
+        v, cores, T, secs = oracle_sample(w, inp, tok)
+        line["cpu_baseline"] = {"value": round(v, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"first {T} of {w.seqlen} tokens, all {w.batch * w.nheads} (batch, head) "
+                                          f"units, fp64 recurrence, {secs:.1f} s wall"}
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def default_oracle_tokens(w: I.Workload) -> int:
+    # about 10 s of host work on 16 cores for the headline workload
+    per_tok = w.batch * w.nheads * w.dstate * w.headdim * 4.0  # fp64 flops per token (update + output)
+    return int(max(256, min(w.seqlen, 6.0e10 / per_tok)))
+
+
+def kernel_alg_bytes(name: str, w: I.Workload) -> float:
+    """Algorithmic bytes one launch of `name` must move at ssd_forward's tiling (stated per unit in the design doc)."""
+    b, L, H, P, N, G, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk_size
+    nc = w.nchunks
+    ncq = b * H * nc * Q
+    st = b * nc * H * P * N * 4
+    if name == "chunk_cumsum":
+        return float(b * L * H * 4 + 2 * ncq * 4)
+    if name == "chunk_state":
+        return float(b * L * H * P * 2 + b * L * G * N * 2 + 2 * ncq * 4 + st)
+    if name == "state_passing":
+        return float(2 * st + b * H * nc * 4 + 2 * b * H * P * N * 4)
+    if name == "chunk_scan":
+        return float(2 * b * L * H * P * 2 + 2 * b * L * G * N * 2 + 2 * ncq * 4 + st)
+    return float("nan")
+
+
+def kernel_traffic(name: str, w: I.Workload):
+    """DRAM bytes per launch from the committed ncu capture, if one matches this kernel build."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        t = json.load(f)
+    ent = t.get(w.name, {}).get(name)
+    return None if ent is None else ent.get("dram_bytes_per_launch")
+
+
+def e2e_measure(w, inp, dev, stream, args, ssd, dist):
+    """Same metric through ssd_forward with host buffers: H2D of inputs and D2H of y + final inside the timing."""
+    import torch
+    host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+    devb = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in inp.items()}
+    y = torch.empty_like(devb["x"])
+    fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), device=dev, dtype=torch.float32)
+    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    fin_h = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = y.numel() * y.element_size() + fin.numel() * fin.element_size()
+
+    def once():
+        for k, v in host.items():
+            if v is not None:
+                devb[k].copy_(v, non_blocking=True)
+        ssd.ssd_forward(devb["x"], devb["dt"], devb["A"], devb["B"], devb["C"], devb["D"], devb["init"],
+                        w.chunk_size, y=y, final_state=fin, stream=stream)
+        y_h.copy_(y, non_blocking=True)
+        fin_h.copy_(fin, non_blocking=True)
+
+    for _ in range(2):
+        once()
+    torch.cuda.synchronize()
+    n = max(3, args.steps // 2)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    s.record(stream)
+    for _ in range(n):
+        once()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    world = dist.get_world_size() if dist is not None else 1
+    return {"value": round(w.batch * w.seqlen * world / (ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4)}
+
+
+def run_reference(args, w):
+    """The oracle as it stands, on the host cores: each step a bounded sample of the workload."""
+    inp = I.make_inputs(w, seed=0)
+    tok = args.oracle_tokens or max(256, default_oracle_tokens(w) // 8)
+    for _ in range(max(0, args.warmup)):
+        oracle_sample(w, inp, tok)
+    vals, secs_all, cores, T = [], 0.0, 0, 0
+    for _ in range(args.steps):
+        v, cores, T, secs = oracle_sample(w, inp, tok)
+        vals.append(v)
+        secs_all += secs
+    value = args.steps * w.batch * T / secs_all
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs_all / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, same recipe)",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk_size": w.chunk_size},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: first {T} of {w.seqlen} tokens of all {w.batch * w.nheads} units"},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -56,6 +56,12 @@
 
 #include <cuda_runtime_api.h>
 
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -70,7 +76,7 @@ typedef enum {
 } ssd_status;
 
 /* Static, never-NULL description of a status code. */
-const char* ssd_status_string(int status);
+SSD_API const char* ssd_status_string(int status);
 
 /*
  * ssd_chunk_cumsum -- the chunk_cumsum stage (devotd.net page, section 2 and
@@ -80,7 +86,7 @@ const char* ssd_status_string(int status);
  *   dt_t[b,h,c,i]      = dt[b, c*Q+i, h]          (0 past the sequence end)
  * dt: (batch, seqlen, nheads); A: (nheads); outputs (batch, nheads, nchunks, Q).
  */
-int ssd_chunk_cumsum(const float* dt, const float* A, int batch, int seqlen, int nheads,
+SSD_API int ssd_chunk_cumsum(const float* dt, const float* A, int batch, int seqlen, int nheads,
                      int chunk_size, float* dA_cumsum, float* dt_t, cudaStream_t stream);
 
 /*
@@ -92,7 +98,7 @@ int ssd_chunk_cumsum(const float* dt, const float* A, int batch, int seqlen, int
  *   w_i = 2^(dA_cumsum[b,h,c,Q-1] - dA_cumsum[b,h,c,i]) * dt_t[b,h,c,i].
  * dt_t and dA_cumsum are ssd_chunk_cumsum's outputs.
  */
-int ssd_chunk_state(const void* x, const void* B, const float* dt_t, const float* dA_cumsum,
+SSD_API int ssd_chunk_state(const void* x, const void* B, const float* dt_t, const float* dA_cumsum,
                     int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
                     int chunk_size, float* chunk_states, cudaStream_t stream);
 
@@ -106,7 +112,7 @@ int ssd_chunk_state(const void* x, const void* B, const float* dt_t, const float
  *   final_state = h_nchunks (not written if NULL).
  * `states` may alias `chunk_states` (in-place update is supported).
  */
-int ssd_state_passing(const float* chunk_states, const float* dA_cumsum, const float* init_state,
+SSD_API int ssd_state_passing(const float* chunk_states, const float* dA_cumsum, const float* init_state,
                       int batch, int nchunks, int nheads, int headdim, int dstate, int chunk_size,
                       float* states, float* final_state, cudaStream_t stream);
 
@@ -119,7 +125,7 @@ int ssd_state_passing(const float* chunk_states, const float* dA_cumsum, const f
  *          + D[h] * x_i,          cs = dA_cumsum[b,h,c,:],  h_c = states[b,c,h]
  * D may be NULL (no skip term).  y: (batch, seqlen, nheads, headdim) bfloat16.
  */
-int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_t,
+SSD_API int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_t,
                    const float* dA_cumsum, const float* D, const float* states, int batch,
                    int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk_size,
                    void* y, cudaStream_t stream);
@@ -131,7 +137,7 @@ int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_
  * returns SSD_ERR_NO_MEMORY if that fails.  The result equals the recurrence
  * above for any chunk_size; chunk_size only sets the internal tiling.
  */
-int ssd_forward(const void* x, const float* dt, const float* A, const void* B, const void* C,
+SSD_API int ssd_forward(const void* x, const float* dt, const float* A, const void* B, const void* C,
                 const float* D, const float* init_state, int batch, int seqlen, int nheads,
                 int headdim, int ngroups, int dstate, int chunk_size, void* y,
                 float* final_state, cudaStream_t stream);
@@ -142,7 +148,7 @@ int ssd_forward(const void* x, const float* dt, const float* A, const void* B, c
  * SSD_ERR_TIMEOUT if a kernel's bounded wait gave up since the last read, or
  * SSD_ERR_CUDA if the read itself failed.
  */
-int ssd_get_device_error(void);
+SSD_API int ssd_get_device_error(void);
 
 /*
  * Profiling counters (host side, process-wide, not thread-safe).
@@ -153,11 +159,11 @@ int ssd_get_device_error(void);
  * ssd_launch_count() counts every kernel the library has launched since load
  * (profiling enabled or not).
  */
-int ssd_profile_enable(int enable);
-int ssd_profile_reset(void);
-int ssd_profile_read(float* total_ms, int* launches, int max_kinds, int* n_kinds);
-const char* ssd_kernel_name(int kind);
-long long ssd_launch_count(void);
+SSD_API int ssd_profile_enable(int enable);
+SSD_API int ssd_profile_reset(void);
+SSD_API int ssd_profile_read(float* total_ms, int* launches, int max_kinds, int* n_kinds);
+SSD_API const char* ssd_kernel_name(int kind);
+SSD_API long long ssd_launch_count(void);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,166 @@
+"""GB300 (sm_103a) Mamba-2 SSD chunked forward pass.
+
+Thin Python binding over the C ABI of include/ssd.h.  Each function has the
+name of its C entry point and only marshals arguments: torch supplies device
+memory and the stream, every step of the computation runs in the library's
+CUDA kernels.  Inputs must be contiguous CUDA tensors:
+
+    x (batch, L, H, P) bf16, dt (batch, L, H) f32, A (H,) f32,
+    B, C (batch, L, G, N) bf16, D (H,) f32 or None,
+    init_state / final_state (batch, H, P, N) f32,
+    dA_cumsum / dt_t (batch, H, nchunks, chunk_size) f32,
+    chunk_states / states (batch, nchunks, H, P, N) f32.
+
+``stream`` is a torch.cuda.Stream (default: the current stream).
+"""
+from __future__ import annotations
+
+from . import _ffi
+
+__all__ = ["ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_forward",
+           "ssd_get_device_error", "SSDError", "library_path"]
+
+SSDError = _ffi.SSDError
+library_path = _ffi.LIB_PATH
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _need(t, name, dtype, ndim=None):
+    torch = _torch()
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return t
+
+
+def _opt(t, name, dtype, ndim=None):
+    return None if t is None else _need(t, name, dtype, ndim)
+
+
+def ssd_chunk_cumsum(dt, A, chunk_size, dA_cumsum=None, dt_t=None, stream=None):
+    """chunk_cumsum stage -> (dA_cumsum, dt_t), both (batch, H, nchunks, chunk_size) f32."""
+    torch = _torch()
+    _need(dt, "dt", torch.float32, 3)
+    _need(A, "A", torch.float32, 1)
+    b, L, H = dt.shape
+    nc = -(-L // chunk_size)
+    if dA_cumsum is None:
+        dA_cumsum = torch.empty((b, H, nc, chunk_size), device=dt.device, dtype=torch.float32)
+    if dt_t is None:
+        dt_t = torch.empty((b, H, nc, chunk_size), device=dt.device, dtype=torch.float32)
+    _need(dA_cumsum, "dA_cumsum", torch.float32, 4)
+    _need(dt_t, "dt_t", torch.float32, 4)
+    _ffi.check("ssd_chunk_cumsum", _ffi.lib().ssd_chunk_cumsum(
+        _ptr(dt), _ptr(A), b, L, H, chunk_size, _ptr(dA_cumsum), _ptr(dt_t), _stream(stream)))
+    return dA_cumsum, dt_t
+
+
+def ssd_chunk_state(x, B, dt_t, dA_cumsum, chunk_size, chunk_states=None, stream=None):
+    """First half of fwd_pass_state -> chunk_states (batch, nchunks, H, P, N) f32."""
+    torch = _torch()
+    _need(x, "x", torch.bfloat16, 4)
+    _need(B, "B", torch.bfloat16, 4)
+    _need(dt_t, "dt_t", torch.float32, 4)
+    _need(dA_cumsum, "dA_cumsum", torch.float32, 4)
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    nc = -(-L // chunk_size)
+    if chunk_states is None:
+        chunk_states = torch.empty((b, nc, H, P, N), device=x.device, dtype=torch.float32)
+    _need(chunk_states, "chunk_states", torch.float32, 5)
+    _ffi.check("ssd_chunk_state", _ffi.lib().ssd_chunk_state(
+        _ptr(x), _ptr(B), _ptr(dt_t), _ptr(dA_cumsum), b, L, H, P, G, N, chunk_size,
+        _ptr(chunk_states), _stream(stream)))
+    return chunk_states
+
+
+def ssd_state_passing(chunk_states, dA_cumsum, init_state, chunk_size, states=None, final_state=None,
+                      want_final=True, stream=None):
+    """Second half of fwd_pass_state -> (states, final_state or None)."""
+    torch = _torch()
+    _need(chunk_states, "chunk_states", torch.float32, 5)
+    _need(dA_cumsum, "dA_cumsum", torch.float32, 4)
+    _opt(init_state, "init_state", torch.float32, 4)
+    b, nc, H, P, N = chunk_states.shape
+    if states is None:
+        states = torch.empty_like(chunk_states)
+    if final_state is None and want_final:
+        final_state = torch.empty((b, H, P, N), device=chunk_states.device, dtype=torch.float32)
+    _need(states, "states", torch.float32, 5)
+    _opt(final_state, "final_state", torch.float32, 4)
+    _ffi.check("ssd_state_passing", _ffi.lib().ssd_state_passing(
+        _ptr(chunk_states), _ptr(dA_cumsum), _ptr(init_state), b, nc, H, P, N, chunk_size,
+        _ptr(states), _ptr(final_state), _stream(stream)))
+    return states, final_state
+
+
+def ssd_chunk_scan(x, B, C, dt_t, dA_cumsum, D, states, chunk_size, y=None, stream=None):
+    """compute_out stage -> y (batch, L, H, P) bf16."""
+    torch = _torch()
+    _need(x, "x", torch.bfloat16, 4)
+    _need(B, "B", torch.bfloat16, 4)
+    _need(C, "C", torch.bfloat16, 4)
+    _need(dt_t, "dt_t", torch.float32, 4)
+    _need(dA_cumsum, "dA_cumsum", torch.float32, 4)
+    _opt(D, "D", torch.float32, 1)
+    _need(states, "states", torch.float32, 5)
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", torch.bfloat16, 4)
+    _ffi.check("ssd_chunk_scan", _ffi.lib().ssd_chunk_scan(
+        _ptr(x), _ptr(B), _ptr(C), _ptr(dt_t), _ptr(dA_cumsum), _ptr(D), _ptr(states),
+        b, L, H, P, G, N, chunk_size, _ptr(y), _stream(stream)))
+    return y
+
+
+def ssd_forward(x, dt, A, B, C, D, init_state, chunk_size, y=None, final_state=None, want_final=True,
+                stream=None):
+    """Whole chunked forward pass -> (y, final_state or None)."""
+    torch = _torch()
+    _need(x, "x", torch.bfloat16, 4)
+    _need(dt, "dt", torch.float32, 3)
+    _need(A, "A", torch.float32, 1)
+    _need(B, "B", torch.bfloat16, 4)
+    _need(C, "C", torch.bfloat16, 4)
+    _opt(D, "D", torch.float32, 1)
+    _opt(init_state, "init_state", torch.float32, 4)
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and want_final:
+        final_state = torch.empty((b, H, P, N), device=x.device, dtype=torch.float32)
+    _need(y, "y", torch.bfloat16, 4)
+    _opt(final_state, "final_state", torch.float32, 4)
+    _ffi.check("ssd_forward", _ffi.lib().ssd_forward(
+        _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
+        b, L, H, P, G, N, chunk_size, _ptr(y), _ptr(final_state), _stream(stream)))
+    return y, final_state
+
+
+def ssd_get_device_error():
+    """SSD_OK (0) or SSD_ERR_TIMEOUT (5) if a bounded device wait gave up since the last read."""
+    return _ffi.lib().ssd_get_device_error()

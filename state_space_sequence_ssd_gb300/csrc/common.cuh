@@ -1,0 +1,47 @@
+// common.cuh -- shared host/device definitions of the SSD library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/ssd.h"
+
+namespace ssd {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Problem dimensions shared by every launch.
+struct Dims {
+    int batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nchunks;
+};
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Kernel kinds, for the profiling counters (names in ssd_api.cu).
+enum KernelKind {
+    kKindCumsum = 0,
+    kKindChunkState = 1,
+    kKindStatePassing = 2,
+    kKindChunkScan = 3,
+    kNumKinds = 4
+};
+
+// Launch bookkeeping implemented in ssd_api.cu: opens/closes the optional
+// profiling event pair around one launch and counts it.
+void launch_begin(int kind, cudaStream_t s);
+int launch_end(int kind, cudaStream_t s);  // returns SSD_OK or SSD_ERR_CUDA
+
+// Stage launchers (one .cu file each).  Arguments are validated by the caller.
+int launch_chunk_cumsum(const float* dt, const float* A, const Dims& d, float* cs, float* dtt,
+                        cudaStream_t s);
+int launch_chunk_state(const __nv_bfloat16* x, const __nv_bfloat16* B, const float* dtt,
+                       const float* cs, const Dims& d, float* S, cudaStream_t s);
+int launch_state_passing(const float* S, const float* cs, const float* init, const Dims& d,
+                         float* states, float* final_state, cudaStream_t s);
+int launch_chunk_scan(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfloat16* C,
+                      const float* dtt, const float* cs, const float* D, const float* states,
+                      const Dims& d, __nv_bfloat16* y, cudaStream_t s);
+
+}  // namespace ssd

@@ -1,0 +1,78 @@
+// k_state_passing.cu -- second half of fwd_pass_state: the sequential hop
+// across chunks.
+//
+// devotd.net page on the Mamba-2 cuTile forward kernels, section 2
+// (fwd_pass_state keeps chunk order but processes independent parts of the
+// state in parallel); disconfirmai.com page "Jane Street ML Engineers Map
+// Mamba-2 Recurrent State Computation to Tensor Cores with cuTile",
+// jump-formula paragraph (the decay re-enters as an exponential of the
+// log-space chunk sum).
+//
+//   h_0 = init;  states[c] = h_c;  h_{c+1} = 2^(cs[b,h,c,Q-1]) h_c + S[c];  final = h_nc
+//
+// Every (b, h, p, n) entry is an independent lane of a serial fp32 recurrence.
+// Each thread owns 4 consecutive entries (one float4); the loop over chunks
+// loads kUnroll chunk states ahead of the dependent FMAs so the memory
+// system always has independent requests in flight (the loads of S do not
+// depend on the carried state).  `states` may alias `S`: every element is
+// read before the same element is written.
+#include "common.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 8;
+
+__global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S, const float* __restrict__ cs,
+                                                                 const float* __restrict__ init, Dims d,
+                                                                 int64_t span_stride_q, float* states,
+                                                                 float* __restrict__ final_state) {
+    const int64_t PN = (int64_t)d.headdim * d.dstate;
+    const int64_t e = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * 4;
+    const int h = blockIdx.y, b = blockIdx.z;
+    if (e >= PN) return;
+    const int nc = d.nchunks;
+    float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (init != nullptr) hv = *reinterpret_cast<const float4*>(init + ((int64_t)b * d.nheads + h) * PN + e);
+    // decay of chunk c: 2^(cs[b, h, c, Q-1])
+    const float* csl = cs + ((int64_t)b * d.nheads + h) * nc * span_stride_q + (span_stride_q - 1);
+    const int64_t cstride = (int64_t)d.nheads * PN;  // distance between consecutive chunks
+    const int64_t base = ((int64_t)b * nc * d.nheads + h) * PN + e;
+    for (int c0 = 0; c0 < nc; c0 += kUnroll) {
+        float4 sv[kUnroll];
+        float dec[kUnroll];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            if (c0 + k < nc) {
+                sv[k] = *reinterpret_cast<const float4*>(S + base + (int64_t)(c0 + k) * cstride);
+                dec[k] = exp2f(__ldg(csl + (int64_t)(c0 + k) * span_stride_q));
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            if (c0 + k < nc) {
+                *reinterpret_cast<float4*>(states + base + (int64_t)(c0 + k) * cstride) = hv;
+                hv.x = fmaf(dec[k], hv.x, sv[k].x);
+                hv.y = fmaf(dec[k], hv.y, sv[k].y);
+                hv.z = fmaf(dec[k], hv.z, sv[k].z);
+                hv.w = fmaf(dec[k], hv.w, sv[k].w);
+            }
+        }
+    }
+    if (final_state != nullptr)
+        *reinterpret_cast<float4*>(final_state + ((int64_t)b * d.nheads + h) * PN + e) = hv;
+}
+
+}  // namespace
+
+int launch_state_passing(const float* S, const float* cs, const float* init, const Dims& d,
+                         float* states, float* final_state, cudaStream_t s) {
+    const int64_t PN = (int64_t)d.headdim * d.dstate;
+    dim3 grid((unsigned)ceil_div64(PN, (int64_t)kThreads * 4), d.nheads, d.batch);
+    launch_begin(kKindStatePassing, s);
+    state_passing_kernel<<<grid, kThreads, 0, s>>>(S, cs, init, d, d.chunk_size, states, final_state);
+    return launch_end(kKindStatePassing, s);
+}
+
+}  // namespace ssd

@@ -1,0 +1,272 @@
+// ssd_api.cu -- the C ABI: argument validation, workspace, launch sequencing,
+// device error word and profiling counters.  Every exported function is
+// declared (and documented) in include/ssd.h.
+#include <stdint.h>
+
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+
+namespace ssd {
+
+// ------------------------------------------------------------ profiling
+namespace {
+
+struct EventPair {
+    int kind;
+    cudaEvent_t start, stop;
+};
+
+std::mutex g_prof_mu;
+bool g_prof_enabled = false;
+std::vector<EventPair> g_prof_open;   // recorded, not yet read
+std::vector<cudaEvent_t> g_prof_free; // reusable events
+double g_prof_ms[kNumKinds];
+int g_prof_count[kNumKinds];
+long long g_launches = 0;
+EventPair g_pending = {-1, nullptr, nullptr};
+
+cudaEvent_t take_event() {
+    if (!g_prof_free.empty()) {
+        cudaEvent_t e = g_prof_free.back();
+        g_prof_free.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+const char* const kKindNames[kNumKinds] = {"chunk_cumsum", "chunk_state", "state_passing", "chunk_scan"};
+
+}  // namespace
+
+void launch_begin(int kind, cudaStream_t s) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_pending.kind = -1;
+    if (!g_prof_enabled) return;
+    cudaEvent_t a = take_event(), b = take_event();
+    if (a == nullptr || b == nullptr) return;
+    cudaEventRecord(a, s);
+    g_pending = {kind, a, b};
+}
+
+int launch_end(int kind, cudaStream_t s) {
+    const cudaError_t e = cudaGetLastError();
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    ++g_launches;
+    if (g_pending.kind == kind) {
+        cudaEventRecord(g_pending.stop, s);
+        g_prof_open.push_back(g_pending);
+        g_pending.kind = -1;
+    }
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // namespace ssd
+
+using namespace ssd;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_dstate(int n) { return n == 64 || n == 128 || n == 256 || n == 512; }
+bool supported_chunk(int q) { return q == 64 || q == 128 || q == 256; }
+
+// Shape validation shared by the entry points.  Returns SSD_OK or an error.
+int check_dims(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk_size) {
+    if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0 ||
+        chunk_size <= 0)
+        return SSD_ERR_INVALID_ARG;
+    if (nheads % ngroups != 0) return SSD_ERR_INVALID_ARG;
+    if (headdim != 64 || !supported_dstate(dstate) || !supported_chunk(chunk_size)) return SSD_ERR_UNSUPPORTED;
+    // element counts must fit the kernels' 64-bit offsets and grid limits
+    const int64_t nchunks = ((int64_t)seqlen + chunk_size - 1) / chunk_size;
+    if (nchunks > 65535 * 64 || batch > 65535 || nheads > 4096) return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+Dims make_dims(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk_size) {
+    Dims d;
+    d.batch = batch;
+    d.seqlen = seqlen;
+    d.nheads = nheads;
+    d.headdim = headdim;
+    d.ngroups = ngroups;
+    d.dstate = dstate;
+    d.chunk_size = chunk_size;
+    d.nchunks = (seqlen + chunk_size - 1) / chunk_size;
+    return d;
+}
+
+}  // namespace
+
+// device error word (bounded waits that gave up set it)
+__device__ int g_ssd_device_error = 0;
+
+extern "C" {
+
+const char* ssd_status_string(int status) {
+    switch (status) {
+        case SSD_OK: return "SSD_OK: success";
+        case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG: null pointer, non-positive size, misalignment or bad grouping";
+        case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: shape outside the implemented set";
+        case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA call or kernel launch failed";
+        case SSD_ERR_NO_MEMORY: return "SSD_ERR_NO_MEMORY: workspace allocation failed";
+        case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT: a bounded device-side wait gave up";
+        default: return "unknown ssd status";
+    }
+}
+
+int ssd_chunk_cumsum(const float* dt, const float* A, int batch, int seqlen, int nheads, int chunk_size,
+                     float* dA_cumsum, float* dt_t, cudaStream_t stream) {
+    if (!dt || !A || !dA_cumsum || !dt_t) return SSD_ERR_INVALID_ARG;
+    if (batch <= 0 || seqlen <= 0 || nheads <= 0 || chunk_size <= 0) return SSD_ERR_INVALID_ARG;
+    if (!aligned16(dA_cumsum) || !aligned16(dt_t) || ((uintptr_t)dt & 3u) || ((uintptr_t)A & 3u))
+        return SSD_ERR_INVALID_ARG;
+    if (!supported_chunk(chunk_size)) return SSD_ERR_UNSUPPORTED;
+    const int64_t nchunks = ((int64_t)seqlen + chunk_size - 1) / chunk_size;
+    if (nchunks > 2147483647LL || batch > 65535 || nheads > 65535 * 32) return SSD_ERR_UNSUPPORTED;
+    Dims d = make_dims(batch, seqlen, nheads, 64, 1, 64, chunk_size);
+    return launch_chunk_cumsum(dt, A, d, dA_cumsum, dt_t, stream);
+}
+
+int ssd_chunk_state(const void* x, const void* B, const float* dt_t, const float* dA_cumsum, int batch,
+                    int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk_size,
+                    float* chunk_states, cudaStream_t stream) {
+    if (!x || !B || !dt_t || !dA_cumsum || !chunk_states) return SSD_ERR_INVALID_ARG;
+    int r = check_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    if (r != SSD_OK) return r;
+    if (!aligned16(x) || !aligned16(B) || !aligned16(dt_t) || !aligned16(dA_cumsum) || !aligned16(chunk_states))
+        return SSD_ERR_INVALID_ARG;
+    Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    return launch_chunk_state(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(B), dt_t,
+                              dA_cumsum, d, chunk_states, stream);
+}
+
+int ssd_state_passing(const float* chunk_states, const float* dA_cumsum, const float* init_state, int batch,
+                      int nchunks, int nheads, int headdim, int dstate, int chunk_size, float* states,
+                      float* final_state, cudaStream_t stream) {
+    if (!chunk_states || !dA_cumsum || !states) return SSD_ERR_INVALID_ARG;
+    if (batch <= 0 || nchunks <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 || chunk_size <= 0)
+        return SSD_ERR_INVALID_ARG;
+    if (headdim != 64 || !supported_dstate(dstate) || !supported_chunk(chunk_size)) return SSD_ERR_UNSUPPORTED;
+    if (batch > 65535 || nheads > 65535) return SSD_ERR_UNSUPPORTED;
+    if (!aligned16(chunk_states) || !aligned16(states) || ((uintptr_t)dA_cumsum & 3u) ||
+        (init_state && !aligned16(init_state)) || (final_state && !aligned16(final_state)))
+        return SSD_ERR_INVALID_ARG;
+    Dims d = make_dims(batch, nchunks * chunk_size, nheads, headdim, 1, dstate, chunk_size);
+    d.nchunks = nchunks;
+    return launch_state_passing(chunk_states, dA_cumsum, init_state, d, states, final_state, stream);
+}
+
+int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_t, const float* dA_cumsum,
+                   const float* D, const float* states, int batch, int seqlen, int nheads, int headdim,
+                   int ngroups, int dstate, int chunk_size, void* y, cudaStream_t stream) {
+    if (!x || !B || !C || !dt_t || !dA_cumsum || !states || !y) return SSD_ERR_INVALID_ARG;
+    int r = check_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    if (r != SSD_OK) return r;
+    if (!aligned16(x) || !aligned16(B) || !aligned16(C) || !aligned16(y) || !aligned16(dt_t) ||
+        !aligned16(dA_cumsum) || !aligned16(states) || (D && ((uintptr_t)D & 3u)))
+        return SSD_ERR_INVALID_ARG;
+    Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    return launch_chunk_scan(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(B),
+                             static_cast<const __nv_bfloat16*>(C), dt_t, dA_cumsum, D, states, d,
+                             static_cast<__nv_bfloat16*>(y), stream);
+}
+
+int ssd_forward(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,
+                const float* init_state, int batch, int seqlen, int nheads, int headdim, int ngroups,
+                int dstate, int chunk_size, void* y, float* final_state, cudaStream_t stream) {
+    if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    int r = check_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    if (r != SSD_OK) return r;
+    if (!aligned16(x) || !aligned16(B) || !aligned16(C) || !aligned16(y) || ((uintptr_t)dt & 3u) ||
+        ((uintptr_t)A & 3u) || (D && ((uintptr_t)D & 3u)) || (init_state && !aligned16(init_state)) ||
+        (final_state && !aligned16(final_state)))
+        return SSD_ERR_INVALID_ARG;
+    Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    const size_t ncq = (size_t)d.batch * d.nheads * d.nchunks * d.chunk_size;
+    const size_t nst = (size_t)d.batch * d.nchunks * d.nheads * d.headdim * d.dstate;
+    const size_t bytes = (2 * ncq + nst) * sizeof(float);
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SSD_ERR_NO_MEMORY;
+    }
+    float* cs = static_cast<float*>(ws);
+    float* dtt = cs + ncq;
+    float* S = dtt + ncq;
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    const __nv_bfloat16* Bb = static_cast<const __nv_bfloat16*>(B);
+    const __nv_bfloat16* Cb = static_cast<const __nv_bfloat16*>(C);
+    r = launch_chunk_cumsum(dt, A, d, cs, dtt, stream);
+    if (r == SSD_OK) r = launch_chunk_state(xb, Bb, dtt, cs, d, S, stream);
+    if (r == SSD_OK) r = launch_state_passing(S, cs, init_state, d, S, final_state, stream);
+    if (r == SSD_OK) r = launch_chunk_scan(xb, Bb, Cb, dtt, cs, D, S, d, static_cast<__nv_bfloat16*>(y), stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
+    return r;
+}
+
+int ssd_get_device_error(void) {
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_ssd_device_error, sizeof(int)) != cudaSuccess) return SSD_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_ssd_device_error, &zero, sizeof(int)) != cudaSuccess) return SSD_ERR_CUDA;
+    return v == 0 ? SSD_OK : SSD_ERR_TIMEOUT;
+}
+
+int ssd_profile_enable(int enable) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_enabled = enable != 0;
+    return SSD_OK;
+}
+
+int ssd_profile_reset(void) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (auto& p : g_prof_open) {
+        cudaEventSynchronize(p.stop);
+        g_prof_free.push_back(p.start);
+        g_prof_free.push_back(p.stop);
+    }
+    g_prof_open.clear();
+    for (int k = 0; k < kNumKinds; ++k) {
+        g_prof_ms[k] = 0.0;
+        g_prof_count[k] = 0;
+    }
+    return SSD_OK;
+}
+
+int ssd_profile_read(float* total_ms, int* launches, int max_kinds, int* n_kinds) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    int status = SSD_OK;
+    for (auto& p : g_prof_open) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(p.stop) != cudaSuccess || cudaEventElapsedTime(&ms, p.start, p.stop) != cudaSuccess)
+            status = SSD_ERR_CUDA;
+        g_prof_ms[p.kind] += ms;
+        g_prof_count[p.kind] += 1;
+        g_prof_free.push_back(p.start);
+        g_prof_free.push_back(p.stop);
+    }
+    g_prof_open.clear();
+    const int n = max_kinds < kNumKinds ? max_kinds : kNumKinds;
+    for (int k = 0; k < n; ++k) {
+        if (total_ms) total_ms[k] = (float)g_prof_ms[k];
+        if (launches) launches[k] = g_prof_count[k];
+    }
+    if (n_kinds) *n_kinds = kNumKinds;
+    return status;
+}
+
+const char* ssd_kernel_name(int kind) {
+    return (kind >= 0 && kind < kNumKinds) ? kKindNames[kind] : "unknown";
+}
+
+long long ssd_launch_count(void) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    return g_launches;
+}
+
+}  // extern "C"

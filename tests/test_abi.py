@@ -1,0 +1,104 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+include/ssd.h declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from state_space_sequence_ssd_gb300 import _ffi, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _ffi.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"SSD_API\s+[\w\s\*]+?\b(ssd_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_symbols())
+    for required in ("ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
+                     "ssd_forward", "ssd_status_string", "ssd_get_device_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in _ffi.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    for s in range(0, 7):
+        msg = lib.ssd_status_string(s)
+        assert msg is not None and len(msg) > 0
+    assert b"INVALID_ARG" in lib.ssd_status_string(1)
+
+
+FAKE = 4096  # a 16-byte aligned non-null address: validation must fail before it is used
+
+
+def fwd(lib, **kw):
+    a = dict(x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, D=FAKE, init=FAKE, batch=1, seqlen=512, nheads=4,
+             headdim=64, ngroups=1, dstate=64, chunk_size=64, y=FAKE, final=FAKE)
+    a.update(kw)
+    return lib.ssd_forward(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["init"], a["batch"], a["seqlen"],
+                           a["nheads"], a["headdim"], a["ngroups"], a["dstate"], a["chunk_size"], a["y"],
+                           a["final"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(x=None), dict(dt=None), dict(A=None), dict(B=None), dict(C=None),
+                                dict(y=None), dict(batch=0), dict(seqlen=0), dict(nheads=-1), dict(dstate=0),
+                                dict(chunk_size=0), dict(ngroups=3), dict(x=FAKE + 2), dict(y=FAKE + 8),
+                                dict(init=FAKE + 4), dict(final=FAKE + 4)])
+def test_forward_rejects_invalid(lib, kw):
+    assert fwd(lib, **kw) == _ffi.SSD_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(headdim=128), dict(dstate=96), dict(dstate=1024), dict(chunk_size=32),
+                                dict(chunk_size=512)])
+def test_forward_rejects_unsupported(lib, kw):
+    assert fwd(lib, **kw) == _ffi.SSD_ERR_UNSUPPORTED
+
+
+def test_stage_entry_points_validate(lib):
+    assert lib.ssd_chunk_cumsum(None, FAKE, 1, 64, 4, 64, FAKE, FAKE, None) == _ffi.SSD_ERR_INVALID_ARG
+    assert lib.ssd_chunk_cumsum(FAKE, FAKE, 1, 64, 4, 96, FAKE, FAKE, None) == _ffi.SSD_ERR_UNSUPPORTED
+    assert lib.ssd_chunk_state(FAKE, FAKE, FAKE, FAKE, 1, 64, 4, 64, 1, 64, 64, None, None) == _ffi.SSD_ERR_INVALID_ARG
+    assert lib.ssd_chunk_state(FAKE, FAKE, FAKE, FAKE, 1, 64, 4, 32, 1, 64, 64, FAKE, None) == _ffi.SSD_ERR_UNSUPPORTED
+    assert lib.ssd_state_passing(FAKE, FAKE, None, 1, 0, 4, 64, 64, 64, FAKE, None, None) == _ffi.SSD_ERR_INVALID_ARG
+    assert lib.ssd_state_passing(FAKE, FAKE, None, 1, 4, 4, 64, 64, 64, FAKE + 4, None, None) == _ffi.SSD_ERR_INVALID_ARG
+    assert lib.ssd_chunk_scan(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 1, 64, 4, 64, 1, 64, 64, FAKE, None) \
+        == _ffi.SSD_ERR_INVALID_ARG
+    assert lib.ssd_chunk_scan(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1, 64, 6, 64, 4, 64, 64, FAKE, None) \
+        == _ffi.SSD_ERR_INVALID_ARG
+
+
+def test_profiling_counters_without_launches(lib):
+    assert lib.ssd_profile_reset() == 0
+    ms = (ctypes.c_float * 8)()
+    cnt = (ctypes.c_int * 8)()
+    n = ctypes.c_int(0)
+    assert lib.ssd_profile_read(ms, cnt, 8, ctypes.byref(n)) == 0
+    assert n.value >= 4
+    assert all(cnt[k] == 0 for k in range(n.value))
+    assert lib.ssd_kernel_name(3) == b"chunk_scan"
+    assert lib.ssd_launch_count() >= 0
+
+
+def test_binding_requires_cuda_tensors():
+    import torch
+
+    import state_space_sequence_ssd_gb300 as ssd
+    x = torch.zeros((1, 64, 4, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        ssd.ssd_forward(x, torch.zeros((1, 64, 4)), torch.zeros(4), torch.zeros((1, 64, 1, 64), dtype=torch.bfloat16),
+                        torch.zeros((1, 64, 1, 64), dtype=torch.bfloat16), None, None, 64)
