@@ -293,6 +293,9 @@ def main():
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
+    if err != 0:
+        print("bench: the library's device error word was set (a bounded wait gave up)", file=sys.stderr)
+        return 3
     return 0
 
 

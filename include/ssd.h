@@ -43,6 +43,10 @@
  *    and leaves every output untouched.  Device-side errors surface at the
  *    caller's next synchronization; a bounded device wait that gave up is
  *    reported by ssd_get_device_error().
+ *  * Value domain: A <= 0 (decay rates) and dt >= 0, so every in-chunk decay
+ *    factor 2^(dA_cumsum[i] - dA_cumsum[j]), j <= i, is at most 1; the
+ *    kernels exponentiate only such differences and never overflow.  Other
+ *    values of A or dt are outside the supported domain.
  *  * Supported shapes: headdim == 64; dstate in {64, 128, 256, 512};
  *    chunk_size in {64, 128, 256}; nheads % ngroups == 0; x, B, C, y and the
  *    float32 tensors 16-byte aligned.  Other shapes return

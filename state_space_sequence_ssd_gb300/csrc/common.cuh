@@ -34,14 +34,20 @@ void launch_begin(int kind, cudaStream_t s);
 int launch_end(int kind, cudaStream_t s);  // returns SSD_OK or SSD_ERR_CUDA
 
 // Stage launchers (one .cu file each).  Arguments are validated by the caller.
+// A "span" is a run of `span_chunks` whole chunks; the stage entry points use
+// one-chunk spans, ssd_forward uses longer ones.  `err` is the device error word.
 int launch_chunk_cumsum(const float* dt, const float* A, const Dims& d, float* cs, float* dtt,
                         cudaStream_t s);
-int launch_chunk_state(const __nv_bfloat16* x, const __nv_bfloat16* B, const float* dtt,
-                       const float* cs, const Dims& d, float* S, cudaStream_t s);
+int launch_chunk_state_span(const __nv_bfloat16* x, const __nv_bfloat16* B, const float* dtt, const float* cs,
+                            int span_chunks, const Dims& d, float* S, float* span_decay, int* err,
+                            cudaStream_t s);
 int launch_state_passing(const float* S, const float* cs, const float* init, const Dims& d,
                          float* states, float* final_state, cudaStream_t s);
-int launch_chunk_scan(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfloat16* C,
-                      const float* dtt, const float* cs, const float* D, const float* states,
-                      const Dims& d, __nv_bfloat16* y, cudaStream_t s);
+int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_step, int64_t dec_row,
+                               const float* init, const Dims& d, int nsteps, float* states, float* final_state,
+                               cudaStream_t s);
+int launch_chunk_scan_span(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfloat16* C,
+                           const float* dtt, const float* cs, const float* D, const float* span_states,
+                           int span_chunks, const Dims& d, __nv_bfloat16* y, int* err, cudaStream_t s);
 
 }  // namespace ssd

@@ -1,183 +1,634 @@
-// k_chunk_scan.cu -- compute_out: the chunk's output from its start state.
+// k_chunk_scan.cu -- compute_out on tcgen05 tensor cores, carrying the state
+// through 128-token sub-blocks of a span.
 //
 // disconfirmai.com page "Jane Street ML Engineers Map Mamba-2 Recurrent State
-// Computation to Tensor Cores with cuTile", three-kernel paragraph
-// (carried-state term + decayed, causally masked interaction matrix + skip
-// connection, fused in one tiled kernel); devotd.net page, section 2 (the
-// intermediate matrix stays on chip instead of going to global memory).
+// Computation to Tensor Cores with cuTile": three-kernel paragraph
+// (compute_out fuses the carried-state term, the decayed causally masked
+// interaction matrix and the skip connection into one tiled kernel) and the
+// jump-formula paragraph (state advance B^T (w * X) as one matrix product);
+// devotd.net page, section 2 (the intermediate matrix stays on chip) and
+// section 3 (operand order chosen for the tensor-core input layout, bank
+// conflicts avoided -- here by 128-byte swizzled tiles).
 //
-//   y_i = 2^(cs_i) (C_i . h_c) + sum_{j<=i} (C_i . B_j) 2^(cs_i - cs_j) dt_j x_j + D x_i
+// One CTA per (head h, span s, batch b).  A span is a run of whole chunks
+// that starts from a known state (its chunk-start state).  The span is walked
+// in sub-blocks of 128 tokens.  With u_i the in-sub-block inclusive log2
+// decay (u_i = log2(e) * sum_{k<=i} dt_k A) and the state h at the
+// sub-block start:
 //
-// SIMT formulation: one CTA per (chunk, head, batch, 64-row tile).  The
-// 64 x 64 interaction tiles are built in shared memory (never in global
-// memory); each thread owns a 4 (row) x 4 (p) output tile.
+//   S    : h   <- 2^(u_last) h + B^T (w X),   w_j = 2^(u_last - u_j) dt_j
+//   YS   : Yst  = C h                          -> y_i += 2^(u_i) Yst_i
+//   CB   : CB   = C B^T                        (128 x 128, f32 in TMEM)
+//   mask : M    = CB * 2^(u_i - u_j) dt_j [j <= i]   (bf16, back into TMEM)
+//   MX   : Y    = M X                          (A operand read from TMEM)
+//   y_i  = Y_i + 2^(u_i) Yst_i + D x_i
+//
+// The mask never exponentiates more than a 32 x 32 diagonal block per row:
+// for a column block q strictly below the row's block, with r the block's
+// last position, 2^(u_i - u_j) = 2^(u_i - u_r) * 2^(u_r - u_j), both factors
+// <= 1 (u is non-increasing), so no factor overflows.
+//
+// Roles (448 threads):
+//   warps 0-3   mask warpgroup: CB -> M (one row per thread)
+//   warps 4-7   state warpgroup: u/dt, scaled X' = w X, the bf16 copy of the
+//               state for C h and the decay of the state in TMEM
+//   warps 8-11  epilogue warpgroup: y = Y + 2^u Yst + D x, written over the
+//               x tile in shared memory, then stored by TMA
+//   warp 12     TMA producer
+//   warp 13     TMEM owner and single-thread MMA issuer
+// The MMA issue order is software-pipelined by one sub-block:
+//   S(0) YS(0) CB(0) | S(1) YS(1) CB(1) MX(0) | S(2) YS(2) CB(2) MX(1) | ...
+// with two TMEM buffer sets {CB/M/Y, Yst} so the mask and epilogue of one
+// sub-block overlap the MMAs of the next.  Every wait is bounded (1 s); a
+// role that gives up sets the CTA abort flag and the device error word, and
+// all roles fall through to teardown.
 #include "common.cuh"
+#include "sm100.cuh"
+#include "tmap.cuh"
 
 namespace ssd {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kRows = 64;
-constexpr int kP = 64;
-constexpr int kNB = 32;  // n block for the state term
+using namespace sm100;
 
-struct ScanSmem {
-    // dynamic layout: Cs[kRows][N] bf16, Bs[kRows][N] bf16, Xs[64][68] f32,
-    // Ms[64][68] f32, Ss[kNB][68] f32, csv[Q], dtv[Q]
-    static size_t bytes(int N, int Q) {
-        return (size_t)kRows * N * 2 * 2 + 64 * 68 * 4 * 2 + kNB * 68 * 4 + 2 * (size_t)Q * 4;
-    }
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr int kThreads = 448;
+constexpr int kTile = 16384;  // 128 rows x 128 B
+constexpr int kWarpTma = 12, kWarpMma = 13;
+
+template <int N>
+struct Cfg {
+    static constexpr int NB = N < 128 ? N : 128;  // state rows per n-block
+    static constexpr int NBLK = N / NB;
+    static constexpr int BOXES = NB / 64;        // 64-column TMA boxes per n-block
+    static constexpr int NST = (N == 512) ? 1 : 2;
+    static constexpr bool S_FIRST = NBLK <= NST;  // all n-blocks resident: issue every S before YS/CB
+    static constexpr int NBUF = (N == 512) ? 1 : 2;
+    static constexpr int NH = (N <= 128) ? 2 : 1;  // bf16 state copies
+    static constexpr int NX = 2;
+    // TMEM columns
+    static constexpr int T_H = 0;
+    static constexpr int HC = NBLK * 64;
+    static constexpr int T_SET = HC;  // set k at T_SET + k * SET: [CB/M, Y in cols 64..127][Yst]
+    static constexpr int SET = 192;
+    static constexpr int TCOLS = 512;
+    static_assert(HC + NBUF * SET <= TCOLS, "TMEM budget");
+    // shared memory (offsets from a 1024-aligned base)
+    static constexpr int OFF_X = 0;  // NX x tiles (y is written over them)
+    static constexpr int OFF_XS = OFF_X + NX * kTile;
+    static constexpr int OFF_H = OFF_XS + kTile;
+    static constexpr int SZ_H = N * 128;
+    static constexpr int OFF_BC = OFF_H + NH * SZ_H;
+    static constexpr int SZ_C = BOXES * kTile;
+    static constexpr int SZ_STAGE = 2 * SZ_C;  // C then B
+    static constexpr int OFF_ZERO = OFF_BC + NST * SZ_STAGE;
+    static constexpr int SZ_ZERO = (N == 64) ? kTile : 0;
+    static constexpr int OFF_U = OFF_ZERO + SZ_ZERO;  // 3 x {u[128], dt[128], bcol[128]}
+    static constexpr int OFF_BAR = OFF_U + 3 * 1536;
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + alignment slack
+    static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-__global__ void __launch_bounds__(kThreads) chunk_scan_simt_kernel(
-    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ B,
-    const __nv_bfloat16* __restrict__ C, const float* __restrict__ dtt, const float* __restrict__ cs,
-    const float* __restrict__ D, const float* __restrict__ states, Dims d,
-    __nv_bfloat16* __restrict__ y) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    const int Q = d.chunk_size, N = d.dstate, H = d.nheads, G = d.ngroups;
-    const int rtiles = Q / kRows;
-    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z / rtiles, rt = blockIdx.z % rtiles;
+constexpr uint32_t kIdescCB = idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescYS = idesc_bf16(128, 64, false, true);
+constexpr uint32_t kIdescS = idesc_bf16(128, 64, true, true);
+constexpr uint32_t kIdescMX = idesc_bf16(128, 64, false, true);
+
+struct ScanArgs {
+    Dims d;
+    int span_chunks;  // chunks per span
+    int nspans;
+    const float* cs;    // (b, H, nc, Q)
+    const float* dtt;   // (b, H, nc, Q)
+    const float* D;     // (H) or null
+    const float* init;  // (b, nspans, H, P, N) span-start states
+    int* err;
+};
+
+struct Bars {
+    uint64_t x_full[2], x_empty[2];
+    uint64_t bc_full[2], bc_empty[2];
+    uint64_t uv_ready[3], u_free[3];
+    uint64_t cb_full[2], y_free[2];
+    uint64_t xs_ready, xs_free, h_ready, state_done, m_ready, y_full, final_mma;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+template <int N>
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
+                         const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y,
+                         ScanArgs a) {
+    using K = Cfg<N>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Bars* bar = reinterpret_cast<Bars*>(smem + K::OFF_BAR);
+    float* sU = reinterpret_cast<float*>(smem + K::OFF_U);  // buffer k: u at k*384, dt at +128, bcol at +256
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_sh;
+
+    const Dims& d = a.d;
+    const int h = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
+    const int H = d.nheads, G = d.ngroups, Q = d.chunk_size;
     const int g = h / (H / G);
-    __nv_bfloat16* Cs = reinterpret_cast<__nv_bfloat16*>(smem);
-    __nv_bfloat16* Bs = Cs + kRows * N;
-    float* Xs = reinterpret_cast<float*>(Bs + kRows * N);
-    float* Ms = Xs + 64 * 68;
-    float* Ss = Ms + 64 * 68;
-    float* csv = Ss + kNB * 68;
-    float* dtv = csv + Q;
-    const int tid = threadIdx.x;
-    const int rg = tid / 16, pg = tid % 16;  // rows rg*4..+3, p (or j) pg*4..+3
-    const int r0 = rt * kRows;                // first row of this tile inside the chunk
-    const int64_t tchunk = (int64_t)c * Q;
-    const int64_t rowbase = ((int64_t)b * H + h) * d.nchunks + c;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t ts = (int64_t)s * a.span_chunks * Q;
+    const int64_t te = min((int64_t)d.seqlen, ts + (int64_t)a.span_chunks * Q);
+    const int nsb = (int)((te - ts + 127) / 128);
 
-    for (int i = tid; i < Q; i += kThreads) {
-        csv[i] = cs[rowbase * Q + i];
-        dtv[i] = dtt[rowbase * Q + i];
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar->x_full[i], 1);
+            mbar_init(&bar->x_empty[i], 2);  // MX commit + epilogue after its TMA store read the tile
+            mbar_init(&bar->bc_full[i], 1);
+            mbar_init(&bar->bc_empty[i], 1);
+            mbar_init(&bar->cb_full[i], 1);
+            mbar_init(&bar->y_free[i], 128);
+        }
+        for (int i = 0; i < 3; ++i) {
+            mbar_init(&bar->uv_ready[i], 128);
+            mbar_init(&bar->u_free[i], 128);  // the epilogue has read u of this buffer
+        }
+        mbar_init(&bar->xs_ready, 128);
+        mbar_init(&bar->xs_free, 1);
+        mbar_init(&bar->h_ready, 128);
+        mbar_init(&bar->state_done, 1);
+        mbar_init(&bar->m_ready, 128);
+        mbar_init(&bar->y_full, 1);
+        mbar_init(&bar->final_mma, 1);
+        abort_sh = 0;
+        fence_barrier_init();
     }
-    // C rows of this tile
-    for (int e = tid; e < kRows * N; e += kThreads) {
-        const int i = e / N, n = e % N;
-        const int64_t t = tchunk + r0 + i;
-        Cs[e] = (t < d.seqlen) ? C[(((int64_t)b * d.seqlen + t) * G + g) * N + n] : __float2bfloat16(0.f);
+    if (K::SZ_ZERO > 0) {  // rows that pad the state-update A operand to 128 (N = 64)
+        uint4* z = reinterpret_cast<uint4*>(smem + K::OFF_ZERO);
+        for (int i = threadIdx.x; i < K::SZ_ZERO / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
     }
+    if (warp == kWarpMma) {
+        tmem_alloc(&tmem_base_sh, K::TCOLS);
+        tmem_relinquish();
+    }
+    if (warp == kWarpTma && lane == 0) {
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_B);
+        tma_prefetch_desc(&tm_C);
+        tma_prefetch_desc(&tm_y);
+    }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_base_sh;
+    volatile int* abort_flag = &abort_sh;
 
-    float acc[4][4];
+    if (warp == kWarpTma) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            int issued_x[2] = {0, 0};
+            int issued_bc[2] = {0, 0};
+            for (int sb = 0; sb < nsb && ok; ++sb) {
+                const int t0 = (int)(ts + sb * 128);
+                const int xb = sb % K::NX;
+                ok = mbar_wait_bounded(&bar->x_empty[xb], ((sb / K::NX) & 1) ^ 1, abort_flag, a.err, 1, kWaitNs);
+                if (!ok) break;
+                mbar_arrive_expect_tx(&bar->x_full[xb], kTile);
+                tma_load_4d(smem + K::OFF_X + xb * kTile, &tm_x, &bar->x_full[xb], 0, h, t0, b);
+                ++issued_x[xb];
+                for (int nb = 0; nb < K::NBLK && ok; ++nb, ++it) {
+                    const int st = it % K::NST;
+                    ok = mbar_wait_bounded(&bar->bc_empty[st], ((it / K::NST) & 1) ^ 1, abort_flag, a.err, 2,
+                                           kWaitNs);
+                    if (!ok) break;
+                    uint8_t* sC = smem + K::OFF_BC + st * K::SZ_STAGE;
+                    uint8_t* sB = sC + K::SZ_C;
+                    mbar_arrive_expect_tx(&bar->bc_full[st], K::SZ_STAGE);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-
-    // carried-state term: sum_n C[i,n] * state[p][n]
-    const float* st = states + (((int64_t)b * d.nchunks + c) * H + h) * (int64_t)kP * N;
-    for (int n0 = 0; n0 < N; n0 += kNB) {
-        __syncthreads();
-        for (int e = tid; e < kNB * kP; e += kThreads) {
-            const int p = e / kNB, k = e % kNB;
-            Ss[k * 68 + p] = st[(int64_t)p * N + n0 + k];
-        }
-        __syncthreads();
-        for (int k = 0; k < kNB; ++k) {
-            float cv[4], sv[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) cv[i] = __bfloat162float(Cs[(rg * 4 + i) * N + n0 + k]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) sv[j] = Ss[k * 68 + pg * 4 + j];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(cv[i], sv[j], acc[i][j]);
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float e = exp2f(csv[r0 + rg * 4 + i]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] *= e;
-    }
-
-    // intra-chunk term over column tiles j0 <= r0 (causal)
-    for (int j0 = 0; j0 <= r0; j0 += kRows) {
-        __syncthreads();
-        for (int e = tid; e < kRows * N; e += kThreads) {
-            const int j = e / N, n = e % N;
-            const int64_t t = tchunk + j0 + j;
-            Bs[e] = (t < d.seqlen) ? B[(((int64_t)b * d.seqlen + t) * G + g) * N + n] : __float2bfloat16(0.f);
-        }
-        for (int e = tid; e < 64 * kP; e += kThreads) {
-            const int j = e / kP, p = e % kP;
-            const int64_t t = tchunk + j0 + j;
-            Xs[j * 68 + p] = (t < d.seqlen) ? __bfloat162float(x[(((int64_t)b * d.seqlen + t) * H + h) * kP + p]) : 0.f;
-        }
-        __syncthreads();
-        // CB tile: rows rg*4.., cols pg*4..
-        float cb[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) cb[i][j] = 0.f;
-        for (int n = 0; n < N; ++n) {
-            float cv[4], bv[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) cv[i] = __bfloat162float(Cs[(rg * 4 + i) * N + n]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) bv[j] = __bfloat162float(Bs[(pg * 4 + j) * N + n]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) cb[i][j] = fmaf(cv[i], bv[j], cb[i][j]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int ri = r0 + rg * 4 + i;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int cj = j0 + pg * 4 + j;
-                const bool valid = (cj <= ri) && (tchunk + cj < d.seqlen);
-                Ms[(rg * 4 + i) * 68 + pg * 4 + j] = valid ? cb[i][j] * exp2f(csv[ri] - csv[cj]) * dtv[cj] : 0.f;
+                    for (int bx = 0; bx < K::BOXES; ++bx) {
+                        tma_load_4d(sC + bx * kTile, &tm_C, &bar->bc_full[st], nb * K::NB + bx * 64, g, t0, b);
+                        tma_load_4d(sB + bx * kTile, &tm_B, &bar->bc_full[st], nb * K::NB + bx * 64, g, t0, b);
+                    }
+                    ++issued_bc[st];
+                }
+            }
+            // no load may still be landing in shared memory at teardown
+            for (int i = 0; i < 2; ++i) {
+                if (issued_x[i] > 0)
+                    mbar_wait_bounded(&bar->x_full[i], (issued_x[i] - 1) & 1, abort_flag, a.err, 3, kWaitNs);
+                if (issued_bc[i] > 0)
+                    mbar_wait_bounded(&bar->bc_full[i], (issued_bc[i] - 1) & 1, abort_flag, a.err, 3, kWaitNs);
             }
         }
-        __syncthreads();
-        for (int j = 0; j < 64; ++j) {
-            float mv[4], xv[4];
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int it = 0;  // n-block ring position
+            bool ok = true;
+            const uint32_t sXs = smem_u32(smem + K::OFF_XS);
+            const uint32_t sZero = smem_u32(smem + K::OFF_ZERO);
+            // Y = M X for sub-block q (A = M from TMEM, B = the x tile, MN-major)
+            auto issue_mx = [&](int q) -> bool {
+                const int k = q % K::NBUF;
+                if (!mbar_wait_bounded(&bar->m_ready, q & 1, abort_flag, a.err, 9, kWaitNs)) return false;
+                tc_fence_after();
+                const uint32_t sX = smem_u32(smem + K::OFF_X + (q % K::NX) * kTile);
+                const uint32_t set = tm + K::T_SET + k * K::SET;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) mv[i] = Ms[(rg * 4 + i) * 68 + j];
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(set + 64, set + kk * 8, desc_sw128(sX + kk * 2048, 16, 1024), kIdescMX, kk > 0);
+                mma_commit(&bar->y_full);
+                mma_commit(&bar->x_empty[q % K::NX]);
+                return true;
+            };
+            // h[nb] += B_nb^T X'  (K = tokens; A MN-major over two 64-row n boxes)
+            auto issue_s = [&](int nb, uint32_t sB) {
+                const uint32_t lbo = (K::BOXES == 2) ? (uint32_t)kTile : (sZero - sB);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) xv[q] = Xs[j * 68 + pg * 4 + q];
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tm + K::T_H + nb * 64, desc_sw128(sB + kk * 2048, lbo, 1024),
+                           desc_sw128(sXs + kk * 2048, 16, 1024), kIdescS, 1);
+            };
+            // Yst += C_nb h_nb ; CB += C_nb B_nb^T   (K = n, 16 per step)
+            auto issue_ys_cb = [&](int nb, uint32_t set, uint32_t sH, uint32_t sC, uint32_t sB) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[i][q] = fmaf(mv[i], xv[q], acc[i][q]);
+                for (int kk = 0; kk < K::NB / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kTile + (kk & 3) * 32;
+                    const uint64_t ad = desc_sw128(sC + off, 16, 1024);
+                    mma_ss(set + 128, ad, desc_sw128(sH + (nb * K::NB + kk * 16) * 128, 16, 1024), kIdescYS,
+                           (nb | kk) != 0);
+                    mma_ss(set, ad, desc_sw128(sB + off, 16, 1024), kIdescCB, (nb | kk) != 0);
+                }
+            };
+            for (int sb = 0; sb < nsb && ok; ++sb) {
+                const bool need_S = sb + 1 < nsb;
+                const int k = sb % K::NBUF;
+                const uint32_t set = tm + K::T_SET + k * K::SET;
+                const uint32_t sH = smem_u32(smem + K::OFF_H + (sb % K::NH) * K::SZ_H);
+                ok = mbar_wait_bounded(&bar->xs_ready, sb & 1, abort_flag, a.err, 5, kWaitNs) &&
+                     mbar_wait_bounded(&bar->h_ready, sb & 1, abort_flag, a.err, 6, kWaitNs);
+                if (!ok) break;
+                tc_fence_after();
+                if (K::S_FIRST) {
+                    // every n-block of this sub-block is resident: the state (critical path) goes first
+                    for (int nb = 0; nb < K::NBLK && ok; ++nb)
+                        ok = mbar_wait_bounded(&bar->bc_full[(it + nb) % K::NST], ((it + nb) / K::NST) & 1,
+                                               abort_flag, a.err, 8, kWaitNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (need_S)
+                        for (int nb = 0; nb < K::NBLK; ++nb)
+                            issue_s(nb, smem_u32(smem + K::OFF_BC + ((it + nb) % K::NST) * K::SZ_STAGE) + K::SZ_C);
+                    mma_commit(&bar->xs_free);
+                    if (K::NH == 2) mma_commit(&bar->state_done);
+                    if (sb >= K::NBUF) {
+                        ok = mbar_wait_bounded(&bar->y_free[k], ((sb / K::NBUF) - 1) & 1, abort_flag, a.err, 7,
+                                               kWaitNs);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    for (int nb = 0; nb < K::NBLK; ++nb, ++it) {
+                        const int st = it % K::NST;
+                        const uint32_t sC = smem_u32(smem + K::OFF_BC + st * K::SZ_STAGE);
+                        issue_ys_cb(nb, set, sH, sC, sC + K::SZ_C);
+                        mma_commit(&bar->bc_empty[st]);
+                    }
+                } else {
+                    // n-blocks streamed one stage at a time (single buffer set)
+                    if (sb >= K::NBUF) {
+                        ok = mbar_wait_bounded(&bar->y_free[k], ((sb / K::NBUF) - 1) & 1, abort_flag, a.err, 7,
+                                               kWaitNs);
+                        if (!ok) break;
+                    }
+                    for (int nb = 0; nb < K::NBLK && ok; ++nb, ++it) {
+                        const int st = it % K::NST;
+                        ok = mbar_wait_bounded(&bar->bc_full[st], (it / K::NST) & 1, abort_flag, a.err, 8, kWaitNs);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t sC = smem_u32(smem + K::OFF_BC + st * K::SZ_STAGE);
+                        if (need_S) issue_s(nb, sC + K::SZ_C);
+                        issue_ys_cb(nb, set, sH, sC, sC + K::SZ_C);
+                        mma_commit(&bar->bc_empty[st]);
+                    }
+                    if (!ok) break;
+                    mma_commit(&bar->xs_free);
+                }
+                if (K::NH == 1) mma_commit(&bar->state_done);
+                mma_commit(&bar->cb_full[k]);
+                // software pipeline: the previous sub-block's M X goes after this front
+                if (K::NBUF == 2) {
+                    if (sb > 0) ok = issue_mx(sb - 1);
+                } else {
+                    ok = issue_mx(sb);
+                }
+            }
+            if (ok && K::NBUF == 2 && nsb > 0) issue_mx(nsb - 1);
+            // every MMA retired before TMEM is released
+            mma_commit(&bar->final_mma);
+            mbar_wait_bounded(&bar->final_mma, 0, abort_flag, a.err, 10, kWaitNs);
         }
+    } else if (warp < 4) {
+        // ------------------------------------------------------ mask warpgroup: CB -> M
+        const int r = threadIdx.x;  // TMEM lane == row
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        for (int sb = 0; sb < nsb; ++sb) {
+            const int k = sb % K::NBUF;
+            const int ub = sb % 3;
+            bool ok = mbar_wait_bounded(&bar->uv_ready[ub], (sb / 3) & 1, abort_flag, a.err, 11, kWaitNs) &&
+                      mbar_wait_bounded(&bar->cb_full[k], (sb / K::NBUF) & 1, abort_flag, a.err, 12, kWaitNs);
+            ok = __all_sync(0xffffffffu, ok);  // TMEM loads/stores below are warp-collective
+            if (!ok) break;
+            tc_fence_after();
+            const float* su = sU + ub * 384;
+            const float* sdt = su + 128;
+            const float* sbc = su + 256;
+            const int nv = (int)min((int64_t)128, te - (ts + sb * 128));
+            const float ui = su[r];
+            const uint32_t set = tm + lane_base + K::T_SET + k * K::SET;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                uint32_t o[16];
+                if (q > warp) {  // above the diagonal
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) o[e] = 0u;
+                } else {
+                    uint32_t v[32];
+                    tmem_ld32(set + q * 32, v);
+                    tmem_ld_wait();
+                    if (q < warp) {  // strictly below: factorized decay
+                        const float ar = exp2f(fminf(ui - su[q * 32 + 31], 0.f));
+#pragma unroll
+                        for (int jj = 0; jj < 32; jj += 2) {
+                            const int j = q * 32 + jj;
+                            o[jj >> 1] = pack_bf16x2(__uint_as_float(v[jj]) * ar * sbc[j],
+                                                     __uint_as_float(v[jj + 1]) * ar * sbc[j + 1]);
+                        }
+                    } else {  // diagonal block: exact per-element decay
+#pragma unroll
+                        for (int jj = 0; jj < 32; jj += 2) {
+                            const int j0 = q * 32 + jj, j1 = j0 + 1;
+                            const float m0 = (j0 <= r && j0 < nv)
+                                                 ? __uint_as_float(v[jj]) * exp2f(fminf(ui - su[j0], 0.f)) * sdt[j0]
+                                                 : 0.f;
+                            const float m1 = (j1 <= r && j1 < nv)
+                                                 ? __uint_as_float(v[jj + 1]) * exp2f(fminf(ui - su[j1], 0.f)) * sdt[j1]
+                                                 : 0.f;
+                            o[jj >> 1] = pack_bf16x2(m0, m1);
+                        }
+                    }
+                }
+                tmem_st16(set + q * 16, o);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bar->m_ready);
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------ state warpgroup
+        // Failures never break this loop: named barriers need all 128 threads,
+        // so a failed wait only turns the remaining work into no-ops.
+        const int r = threadIdx.x - 128;  // TMEM lane (warp % 4 == warp - 4)
+        const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+        const int64_t row = (int64_t)b * H + h;
+        const float* csr = a.cs + row * d.nchunks * Q;
+        const float* dtr = a.dtt + row * d.nchunks * Q;
+        const int64_t PN = (int64_t)d.headdim * N;
+        const float* init = a.init + (((int64_t)b * a.nspans + s) * H + h) * PN;
+        bool ok = true;
+        for (int sb = 0; sb < nsb; ++sb) {
+            const int64_t t0 = ts + sb * 128;
+            const int nv = (int)min((int64_t)128, te - t0);
+            const int xb = sb % K::NX;
+            const int ub = sb % 3;
+            float* su = sU + ub * 384;
+            float* sdt = su + 128;
+            float* sbc = su + 256;
+            // 1. in-sub-block inclusive log2 decay u, dt, and the factorized column weights
+            const int64_t t = t0 + r;
+            const bool valid = r < nv;
+            float u = 0.f, dtv = 0.f;
+            if (valid) {
+                const int64_t c0 = t0 / Q;
+                const int64_t p0 = t0 - c0 * Q;
+                const float prev = (p0 > 0) ? csr[t0 - 1] : 0.f;
+                const int64_t c = t / Q;
+                u = (c == c0) ? (csr[t] - prev) : ((csr[c0 * Q + Q - 1] - prev) + csr[t]);
+                dtv = dtr[t];
+            }
+            if (sb >= 3) {  // the epilogue of sub-block sb-3 (the last reader of this buffer) is done with it
+                ok = ok && mbar_wait_bounded(&bar->u_free[ub], ((sb / 3) - 1) & 1, abort_flag, a.err, 17, kWaitNs);
+                ok = __all_sync(0xffffffffu, ok);
+            }
+            su[r] = u;
+            sdt[r] = dtv;
+            named_sync(1, 128);
+            const float ulast = su[nv - 1];
+            if (!valid) u = ulast;
+            // column weight of the factorized mask: 2^(u_end - u_j) dt_j, end = last position of j's 32-block
+            // (positions past nv hold ulast, so the block end is clamped to the last valid position)
+            const int bend = min(r | 31, nv - 1);
+            const float uend = su[bend];
+            named_sync(1, 128);  // every thread has read su before padded rows are rewritten
+            if (!valid) su[r] = ulast;
+            sbc[r] = valid ? exp2f(fminf(uend - u, 0.f)) * dtv : 0.f;
+            mbar_arrive(&bar->uv_ready[ub]);
+            const float dsb = exp2f(ulast);
+            // 2. X' = w X  (row r of the token tile, same swizzle)
+            ok = ok && mbar_wait_bounded(&bar->x_full[xb], (sb / K::NX) & 1, abort_flag, a.err, 13, kWaitNs);
+            ok = ok && (sb == 0 || mbar_wait_bounded(&bar->xs_free, (sb - 1) & 1, abort_flag, a.err, 14, kWaitNs));
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                const float w = valid ? exp2f(ulast - u) * dtv : 0.f;
+                const uint8_t* xrow = smem + K::OFF_X + xb * kTile;
+                uint8_t* xsrow = smem + K::OFF_XS;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint32_t off = sw128_offset(r, ch);
+                    uint4 v = *reinterpret_cast<const uint4*>(xrow + off);
+                    __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float2 f = __bfloat1622float2(p2[e]);
+                        p2[e] = __floats2bfloat162_rn(f.x * w, f.y * w);
+                    }
+                    *reinterpret_cast<uint4*>(xsrow + off) = v;
+                }
+                fence_proxy_async_smem();
+            }
+            mbar_arrive(&bar->xs_ready);
+            // 3. state h_sb -> bf16 copy for C h, and h <- 2^(u_last) h in TMEM
+            if (sb > 0) {
+                ok = ok && mbar_wait_bounded(&bar->state_done, (sb - 1) & 1, abort_flag, a.err, 15, kWaitNs);
+                ok = __all_sync(0xffffffffu, ok);
+                tc_fence_after();
+            }
+            if (ok) {
+                uint8_t* hbase = smem + K::OFF_H + (sb % K::NH) * K::SZ_H;
+#pragma unroll 1
+                for (int nb = 0; nb < K::NBLK; ++nb) {
+                    const int n = nb * K::NB + (r % K::NB);
+                    const bool real = r < K::NB;  // N = 64: lanes 64..127 are padding
+                    float hv[64];
+                    if (sb == 0) {
+#pragma unroll
+                        for (int p = 0; p < 64; ++p) hv[p] = real ? init[(int64_t)p * N + n] : 0.f;
+                    } else {
+                        uint32_t v[32];
+                        tmem_ld32(tm + lane_base + K::T_H + nb * 64, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int p = 0; p < 32; ++p) hv[p] = __uint_as_float(v[p]);
+                        tmem_ld32(tm + lane_base + K::T_H + nb * 64 + 32, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int p = 0; p < 32; ++p) hv[32 + p] = __uint_as_float(v[p]);
+                    }
+                    if (real) {
+                        const int hr = nb * K::NB + r;  // smem row (state index n)
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            uint4 v;
+                            v.x = pack_bf16x2(hv[ch * 8 + 0], hv[ch * 8 + 1]);
+                            v.y = pack_bf16x2(hv[ch * 8 + 2], hv[ch * 8 + 3]);
+                            v.z = pack_bf16x2(hv[ch * 8 + 4], hv[ch * 8 + 5]);
+                            v.w = pack_bf16x2(hv[ch * 8 + 6], hv[ch * 8 + 7]);
+                            *reinterpret_cast<uint4*>(hbase + sw128_offset(hr, ch)) = v;
+                        }
+                    }
+                    uint32_t o[16];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+                        for (int p = 0; p < 16; ++p) o[p] = __float_as_uint(hv[q4 * 16 + p] * dsb);
+                        tmem_st16(tm + lane_base + K::T_H + nb * 64 + q4 * 16, o);
+                    }
+                }
+                tmem_st_wait();
+                fence_proxy_async_smem();
+                tc_fence_before();
+            }
+            mbar_arrive(&bar->h_ready);
+        }
+    } else if (warp < 12) {
+        // ------------------------------------------------------ epilogue warpgroup
+        const int r = threadIdx.x - 256;  // TMEM lane (warp % 4 == warp - 8)
+        const uint32_t lane_base = (uint32_t)((warp - 8) * 32) << 16;
+        const float Dh = (a.D != nullptr) ? a.D[h] : 0.f;
+        bool ok = true;
+        for (int sb = 0; sb < nsb; ++sb) {
+            const int64_t t0 = ts + sb * 128;
+            const int nv = (int)min((int64_t)128, te - t0);
+            const int xb = sb % K::NX;
+            const int k = sb % K::NBUF;
+            ok = ok && mbar_wait_bounded(&bar->y_full, sb & 1, abort_flag, a.err, 16, kWaitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+            uint8_t* xrow = smem + K::OFF_X + xb * kTile;
+            const float e = exp2f(sU[(sb % 3) * 384 + r]);
+            mbar_arrive(&bar->u_free[sb % 3]);
+            if (ok) {
+                const uint32_t set = tm + lane_base + K::T_SET + k * K::SET;
+                uint32_t yv[2][32], sv[2][32];
+                tmem_ld32(set + 64, yv[0]);
+                tmem_ld32(set + 96, yv[1]);
+                tmem_ld32(set + 128, sv[0]);
+                tmem_ld32(set + 160, sv[1]);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&bar->y_free[k]);  // this TMEM set may be reused
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint32_t off = sw128_offset(r, ch);
+                    uint4 xv = *reinterpret_cast<const uint4*>(xrow + off);
+                    const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
+                    uint4 ov;
+                    uint32_t* o4 = reinterpret_cast<uint32_t*>(&ov);
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const float2 xf = __bfloat1622float2(x2[e2]);
+                        const int c = ch * 8 + e2 * 2;
+                        const float y0 = __uint_as_float(yv[c >> 5][c & 31]) +
+                                         e * __uint_as_float(sv[c >> 5][c & 31]) + Dh * xf.x;
+                        const float y1 = __uint_as_float(yv[c >> 5][(c + 1) & 31]) +
+                                         e * __uint_as_float(sv[c >> 5][(c + 1) & 31]) + Dh * xf.y;
+                        o4[e2] = pack_bf16x2(y0, y1);
+                    }
+                    *reinterpret_cast<uint4*>(xrow + off) = ov;  // y overwrites its own x row
+                }
+            } else {
+                mbar_arrive(&bar->y_free[k]);
+            }
+            fence_proxy_async_smem();
+            named_sync(2, 128);
+            if (r == 0) {
+                if (ok) {
+                    tma_store_4d(&tm_y, xrow, 0, h, (int)t0, b);
+                    if (nv > 64) tma_store_4d(&tm_y, xrow + 64 * 128, 0, h, (int)t0 + 64, b);
+                    tma_store_commit();
+                    tma_store_wait_read0();  // the tile is reloaded only after the store has read it
+                }
+                mbar_arrive(&bar->x_empty[xb]);
+            }
+        }
+        if (r == 0) tma_store_wait_all0();
     }
 
-    const float Dh = (D != nullptr) ? D[h] : 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int64_t t = tchunk + r0 + rg * 4 + i;
-        if (t >= d.seqlen) continue;
-        const int64_t o = (((int64_t)b * d.seqlen + t) * H + h) * kP + pg * 4;
-        __nv_bfloat16 out[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) out[q] = __float2bfloat16_rn(acc[i][q] + Dh * __bfloat162float(x[o + q]));
-        *reinterpret_cast<uint2*>(y + o) = *reinterpret_cast<uint2*>(out);
-    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma) tmem_dealloc(tm, K::TCOLS);
+}
+
+template <int N>
+int launch_scan_n(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfloat16* C, __nv_bfloat16* y,
+                  const ScanArgs& a, cudaStream_t s) {
+    const Dims& d = a.d;
+    CUtensorMap tx, tb, tc, ty;
+    const uint64_t dx[4] = {(uint64_t)d.headdim, (uint64_t)d.nheads, (uint64_t)d.seqlen, (uint64_t)d.batch};
+    const uint64_t dbc[4] = {(uint64_t)d.dstate, (uint64_t)d.ngroups, (uint64_t)d.seqlen, (uint64_t)d.batch};
+    const uint32_t box_in[4] = {64, 1, 128, 1};
+    const uint32_t box_out[4] = {64, 1, 64, 1};
+    if (!make_tmap_bf16_4d(&tx, x, dx, box_in) || !make_tmap_bf16_4d(&tb, B, dbc, box_in) ||
+        !make_tmap_bf16_4d(&tc, C, dbc, box_in) || !make_tmap_bf16_4d(&ty, y, dx, box_out))
+        return SSD_ERR_CUDA;
+    const int smem = Cfg<N>::SMEM;
+    if (cudaFuncSetAttribute(chunk_scan_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return SSD_ERR_CUDA;
+    dim3 grid(d.nheads, a.nspans, d.batch);
+    launch_begin(kKindChunkScan, s);
+    chunk_scan_tc_kernel<N><<<grid, kThreads, smem, s>>>(tx, tb, tc, ty, a);
+    return launch_end(kKindChunkScan, s);
 }
 
 }  // namespace
 
-int launch_chunk_scan(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfloat16* C,
-                      const float* dtt, const float* cs, const float* D, const float* states,
-                      const Dims& d, __nv_bfloat16* y, cudaStream_t s) {
-    const size_t smem = ScanSmem::bytes(d.dstate, d.chunk_size);
-    cudaError_t e = cudaFuncSetAttribute(chunk_scan_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return SSD_ERR_CUDA;
-    dim3 grid(d.nchunks, d.nheads, d.batch * (d.chunk_size / kRows));
-    launch_begin(kKindChunkScan, s);
-    chunk_scan_simt_kernel<<<grid, kThreads, smem, s>>>(x, B, C, dtt, cs, D, states, d, y);
-    return launch_end(kKindChunkScan, s);
+int launch_chunk_scan_span(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfloat16* C,
+                           const float* dtt, const float* cs, const float* D, const float* span_states,
+                           int span_chunks, const Dims& d, __nv_bfloat16* y, int* err, cudaStream_t s) {
+    ScanArgs a;
+    a.d = d;
+    a.span_chunks = span_chunks;
+    a.nspans = ceil_div(d.nchunks, span_chunks);
+    a.cs = cs;
+    a.dtt = dtt;
+    a.D = D;
+    a.init = span_states;
+    a.err = err;
+    switch (d.dstate) {
+        case 64: return launch_scan_n<64>(x, B, C, y, a, s);
+        case 128: return launch_scan_n<128>(x, B, C, y, a, s);
+        case 256: return launch_scan_n<256>(x, B, C, y, a, s);
+        case 512: return launch_scan_n<512>(x, B, C, y, a, s);
+        default: return SSD_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace ssd

@@ -1,101 +1,272 @@
-// k_chunk_state.cu -- first half of fwd_pass_state: each chunk's own state.
+// k_chunk_state.cu -- first half of fwd_pass_state on tcgen05 tensor cores.
 //
 // disconfirmai.com page "Jane Street ML Engineers Map Mamba-2 Recurrent State
-// Computation to Tensor Cores with cuTile", jump-formula paragraph: without
-// decay the state advances by B X^T over a chunk (B, X the stacked per-token
-// vectors); with decay, X's rows are pre-multiplied by exponentials of the
-// log-space sums, which keeps the matrix-product form:
+// Computation to Tensor Cores with cuTile", jump-formula paragraph: with no
+// decay a run of tokens advances the state by B^T X (B, X the stacked
+// per-token vectors); with decay, X's rows are pre-scaled by exponentials of
+// the log-space sums, which keeps one matrix product:
 //
-//   S[b,c,h][p][n] = sum_i B[t_i, g, n] * w_i * x[t_i, h, p],
-//   w_i = 2^(cs[Q-1] - cs[i]) * dt_i            (cs, dt from chunk_cumsum)
+//   S_span[p][n] = sum_{t in span} B[t, n] * w_t * x[t, p],
+//   w_t = 2^(cs_span_end - cs_span(t)) * dt_t
 //
-// SIMT formulation: one CTA per (chunk, head, batch, 128-wide n tile); each
-// thread accumulates an 8 (p) x 4 (n) fp32 tile over the chunk's tokens,
-// staged 32 tokens at a time through shared memory.
+// A span is a run of whole chunks (one chunk for ssd_chunk_state).  With
+// per-chunk cumsums cs[c][i] (chunk_cumsum's output), the exponent is
+//   R_c + cs[c][Q-1] - cs[c][i],   R_c = sum of cs[c'][Q-1] over the span's chunks after c,
+// every term <= 0, so no intermediate overflows.  The span's total exponent
+// sum_c cs[c][Q-1] is also written (log2 decay of the whole span).
+//
+// One CTA per (head, span, batch); 192 threads: warps 0-3 scale X rows in
+// shared memory (one token per thread) and store the result; warp 4 issues
+// TMA loads; warp 5 owns TMEM and issues the MMAs
+//   acc[mb] (128 n x 64 p, f32 in TMEM) += B_tile^T (MN-major) * X'_tile (MN-major).
 #include "common.cuh"
+#include "sm100.cuh"
+#include "tmap.cuh"
 
 namespace ssd {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kTok = 32;     // tokens per shared-memory stage
-constexpr int kNTile = 128;  // n columns per CTA
-constexpr int kP = 64;       // headdim
+using namespace sm100;
 
-__global__ void __launch_bounds__(kThreads) chunk_state_simt_kernel(
-    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ B,
-    const float* __restrict__ dtt, const float* __restrict__ cs, Dims d, float* __restrict__ S) {
-    __shared__ float xs[kTok][kP + 4];
-    __shared__ float bs[kTok][kNTile + 4];
-    const int c = blockIdx.x, h = blockIdx.y % d.nheads, ntile = blockIdx.y / d.nheads, b = blockIdx.z;
-    const int Q = d.chunk_size, N = d.dstate, H = d.nheads, G = d.ngroups;
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr int kThreads = 192;
+constexpr int kMaxSpanChunks = 256;
+
+template <int N>
+struct StCfg {
+    static constexpr int TB = (N == 512) ? 64 : 128;   // tokens per stage
+    static constexpr int BOX = TB * 128;               // one 64-column box, TB rows
+    static constexpr int NBOX = N / 64;                // boxes of B per stage
+    static constexpr int MB = (N + 127) / 128;         // 128-row accumulator blocks
+    static constexpr int NST = (N == 64) ? 4 : (N == 128 ? 3 : 2);
+    static constexpr int SZ_STAGE = BOX + NBOX * BOX;  // X then B
+    static constexpr int OFF_ZERO = NST * SZ_STAGE;
+    static constexpr int SZ_ZERO = (N == 64) ? BOX : 0;
+    static constexpr int OFF_R = OFF_ZERO + SZ_ZERO;   // R_c suffix sums
+    static constexpr int OFF_BAR = OFF_R + kMaxSpanChunks * 4;
+    static constexpr int SMEM = OFF_BAR + 256 + 1024;
+    static constexpr int TCOLS = (MB * 64 < 32) ? 32 : MB * 64;
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct StateArgs {
+    Dims d;
+    int span_chunks;
+    int nspans;
+    const float* cs;    // (b, H, nc, Q)
+    const float* dtt;   // (b, H, nc, Q)
+    float* S;           // (b, nspans, H, P, N)
+    float* span_decay;  // (b, H, nspans) log2 units, or null
+    int* err;
+};
+
+template <int N>
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
+                          StateArgs a) {
+    using K = StCfg<N>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
+    uint64_t* xs_ready = full + K::NST;
+    uint64_t* empty = xs_ready + K::NST;
+    uint64_t* acc_done = empty + K::NST;
+    float* Rs = reinterpret_cast<float*>(smem + K::OFF_R);
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_sh;
+
+    const Dims& d = a.d;
+    const int h = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
+    const int H = d.nheads, G = d.ngroups, Q = d.chunk_size;
     const int g = h / (H / G);
-    const int n0 = ntile * kNTile;
-    const int ncols = min(kNTile, N - n0);
-    const int tid = threadIdx.x;
-    const int pg = tid / 32, ng = tid % 32;  // p rows pg*8..+7, n cols ng*4..+3
-    const float* csr = cs + (((int64_t)b * H + h) * d.nchunks + c) * Q;
-    const float* dtr = dtt + (((int64_t)b * H + h) * d.nchunks + c) * Q;
-    const float cs_last = csr[Q - 1];
-    float acc[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t ts = (int64_t)s * a.span_chunks * Q;
+    const int64_t te = min((int64_t)d.seqlen, ts + (int64_t)a.span_chunks * Q);
+    const int nblk = (int)((te - ts + K::TB - 1) / K::TB);
+    const int64_t c_first = ts / Q;
+    const int nchk = (int)((te - ts + Q - 1) / Q);
+    const int64_t row = (int64_t)b * H + h;
+    const float* csr = a.cs + row * d.nchunks * Q;
+    const float* dtr = a.dtt + row * d.nchunks * Q;
 
-    for (int k0 = 0; k0 < Q; k0 += kTok) {
-        __syncthreads();
-        // x tile, scaled by w
-        for (int e = tid; e < kTok * kP; e += kThreads) {
-            const int k = e / kP, p = e % kP;
-            const int64_t t = (int64_t)c * Q + k0 + k;
-            float v = 0.f;
-            if (t < d.seqlen) {
-                const float w = exp2f(cs_last - csr[k0 + k]) * dtr[k0 + k];
-                v = w * __bfloat162float(x[(((int64_t)b * d.seqlen + t) * H + h) * kP + p]);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < K::NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&xs_ready[i], 128);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(acc_done, 1);
+        abort_sh = 0;
+        fence_barrier_init();
+        // R_c: sum of the chunk totals after chunk c inside this span
+        float run = 0.f;
+        for (int c = nchk - 1; c >= 0; --c) {
+            Rs[c] = run;
+            run += csr[(c_first + c) * Q + Q - 1];
+        }
+        if (a.span_decay != nullptr) a.span_decay[row * a.nspans + s] = run;
+    }
+    if (K::SZ_ZERO > 0) {
+        uint4* z = reinterpret_cast<uint4*>(smem + K::OFF_ZERO);
+        for (int i = threadIdx.x; i < K::SZ_ZERO / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    if (warp == 5) {
+        tmem_alloc(&tmem_base_sh, K::TCOLS);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_B);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_base_sh;
+    volatile int* abort_flag = &abort_sh;
+
+    if (warp == 4) {
+        // TMA producer
+        if (lane == 0) {
+            int issued[K::NST];
+            for (int i = 0; i < K::NST; ++i) issued[i] = 0;
+            for (int kb = 0; kb < nblk; ++kb) {
+                const int st = kb % K::NST;
+                if (!mbar_wait_bounded(&empty[st], ((kb / K::NST) & 1) ^ 1, abort_flag, a.err, 21, kWaitNs)) break;
+                uint8_t* sX = smem + st * K::SZ_STAGE;
+                uint8_t* sB = sX + K::BOX;
+                const int t0 = (int)(ts + (int64_t)kb * K::TB);
+                mbar_arrive_expect_tx(&full[st], K::SZ_STAGE);
+                tma_load_4d(sX, &tm_x, &full[st], 0, h, t0, b);
+#pragma unroll
+                for (int bx = 0; bx < K::NBOX; ++bx) tma_load_4d(sB + bx * K::BOX, &tm_B, &full[st], bx * 64, g, t0, b);
+                ++issued[st];
             }
-            xs[k][p] = v;
+            for (int i = 0; i < K::NST; ++i)
+                if (issued[i] > 0) mbar_wait_bounded(&full[i], (issued[i] - 1) & 1, abort_flag, a.err, 22, kWaitNs);
         }
-        for (int e = tid; e < kTok * kNTile; e += kThreads) {
-            const int k = e / kNTile, n = e % kNTile;
-            const int64_t t = (int64_t)c * Q + k0 + k;
-            float v = 0.f;
-            if (t < d.seqlen && n < ncols) v = __bfloat162float(B[(((int64_t)b * d.seqlen + t) * G + g) * N + n0 + n]);
-            bs[k][n] = v;
+    } else if (warp == 5) {
+        // MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(128, 64, true, true);
+            for (int kb = 0; kb < nblk; ++kb) {
+                const int st = kb % K::NST;
+                if (!mbar_wait_bounded(&xs_ready[st], (kb / K::NST) & 1, abort_flag, a.err, 23, kWaitNs)) break;
+                tc_fence_after();
+                const uint32_t sX = smem_u32(smem + st * K::SZ_STAGE);
+                const uint32_t sB = sX + K::BOX;
+#pragma unroll
+                for (int mb = 0; mb < K::MB; ++mb) {
+                    const uint32_t a0 = sB + 2 * mb * K::BOX;
+                    const uint32_t lbo = (N == 64) ? (uint32_t)(smem_u32(smem + K::OFF_ZERO) - a0) : (uint32_t)K::BOX;
+#pragma unroll
+                    for (int k = 0; k < K::TB / 16; ++k)
+                        mma_ss(tm + mb * 64, desc_sw128(a0 + k * 2048, lbo, 1024), desc_sw128(sX + k * 2048, 16, 1024),
+                               idesc, (kb | k) != 0);
+                }
+                mma_commit(&empty[st]);
+            }
+            mma_commit(acc_done);
         }
-        __syncthreads();
-#pragma unroll 4
-        for (int k = 0; k < kTok; ++k) {
-            float xv[8], bv[4];
+    } else {
+        // warps 0-3: scale X rows, then store the accumulator
+        const int r = threadIdx.x;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        bool ok = true;
+        for (int kb = 0; kb < nblk; ++kb) {
+            const int st = kb % K::NST;
+            ok = ok && mbar_wait_bounded(&full[st], (kb / K::NST) & 1, abort_flag, a.err, 24, kWaitNs);
+            if (ok && r < K::TB) {
+                const int64_t t = ts + (int64_t)kb * K::TB + r;
+                float w = 0.f;
+                if (t < te) {
+                    const int64_t c = t / Q;
+                    w = exp2f(Rs[c - c_first] + csr[c * Q + Q - 1] - csr[t]) * dtr[t];
+                }
+                uint8_t* xrow = smem + st * K::SZ_STAGE;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) xv[i] = xs[k][pg * 8 + i];
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint32_t off = sw128_offset(r, ch);
+                    uint4 v = *reinterpret_cast<const uint4*>(xrow + off);
+                    __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&v);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) bv[j] = bs[k][ng * 4 + j];
+                    for (int e = 0; e < 4; ++e) {
+                        float2 f = __bfloat1622float2(p2[e]);
+                        p2[e] = __floats2bfloat162_rn(f.x * w, f.y * w);
+                    }
+                    *reinterpret_cast<uint4*>(xrow + off) = v;
+                }
+                fence_proxy_async_smem();
+            }
+            mbar_arrive(&xs_ready[st]);
+        }
+        ok = ok && mbar_wait_bounded(acc_done, 0, abort_flag, a.err, 25, kWaitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+        if (ok) {
+            const int64_t PN = (int64_t)d.headdim * N;
+            float* out = a.S + (((int64_t)b * a.nspans + s) * H + h) * PN;
+#pragma unroll 1
+            for (int mb = 0; mb < K::MB; ++mb) {
+                const int n = mb * 128 + r;
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32];
+                    tmem_ld32(tm + lane_base + mb * 64 + half * 32, v);
+                    tmem_ld_wait();
+                    if (n < N) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], bv[j], acc[i][j]);
+                        for (int p = 0; p < 32; ++p) out[(int64_t)(half * 32 + p) * N + n] = __uint_as_float(v[p]);
+                    }
+                }
+            }
         }
     }
-    if (ng * 4 < ncols) {
-        float* out = S + (((int64_t)b * d.nchunks + c) * H + h) * kP * N;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int p = pg * 8 + i;
-            *reinterpret_cast<float4*>(out + (int64_t)p * N + n0 + ng * 4) =
-                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        }
-    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tm, K::TCOLS);
+}
+
+template <int N>
+int launch_state_n(const __nv_bfloat16* x, const __nv_bfloat16* B, const StateArgs& a, cudaStream_t s) {
+    using K = StCfg<N>;
+    const Dims& d = a.d;
+    CUtensorMap tx, tb;
+    const uint64_t dx[4] = {(uint64_t)d.headdim, (uint64_t)d.nheads, (uint64_t)d.seqlen, (uint64_t)d.batch};
+    const uint64_t db[4] = {(uint64_t)d.dstate, (uint64_t)d.ngroups, (uint64_t)d.seqlen, (uint64_t)d.batch};
+    const uint32_t box[4] = {64, 1, (uint32_t)K::TB, 1};
+    if (!make_tmap_bf16_4d(&tx, x, dx, box) || !make_tmap_bf16_4d(&tb, B, db, box)) return SSD_ERR_CUDA;
+    if (cudaFuncSetAttribute(chunk_state_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM) !=
+        cudaSuccess)
+        return SSD_ERR_CUDA;
+    dim3 grid(d.nheads, a.nspans, d.batch);
+    launch_begin(kKindChunkState, s);
+    chunk_state_tc_kernel<N><<<grid, kThreads, K::SMEM, s>>>(tx, tb, a);
+    return launch_end(kKindChunkState, s);
 }
 
 }  // namespace
 
-int launch_chunk_state(const __nv_bfloat16* x, const __nv_bfloat16* B, const float* dtt,
-                       const float* cs, const Dims& d, float* S, cudaStream_t s) {
-    dim3 grid(d.nchunks, d.nheads * ceil_div(d.dstate, kNTile), d.batch);
-    launch_begin(kKindChunkState, s);
-    chunk_state_simt_kernel<<<grid, kThreads, 0, s>>>(x, B, dtt, cs, d, S);
-    return launch_end(kKindChunkState, s);
+int launch_chunk_state_span(const __nv_bfloat16* x, const __nv_bfloat16* B, const float* dtt, const float* cs,
+                            int span_chunks, const Dims& d, float* S, float* span_decay, int* err, cudaStream_t s) {
+    if (span_chunks < 1 || span_chunks > kMaxSpanChunks) return SSD_ERR_UNSUPPORTED;
+    StateArgs a;
+    a.d = d;
+    a.span_chunks = span_chunks;
+    a.nspans = ceil_div(d.nchunks, span_chunks);
+    a.cs = cs;
+    a.dtt = dtt;
+    a.S = S;
+    a.span_decay = span_decay;
+    a.err = err;
+    switch (d.dstate) {
+        case 64: return launch_state_n<64>(x, B, a, s);
+        case 128: return launch_state_n<128>(x, B, a, s);
+        case 256: return launch_state_n<256>(x, B, a, s);
+        case 512: return launch_state_n<512>(x, B, a, s);
+        default: return SSD_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace ssd

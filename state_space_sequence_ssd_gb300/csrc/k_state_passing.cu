@@ -24,10 +24,11 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 8;
 
-__global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S, const float* __restrict__ cs,
+// dec: log2 decay of step c for row (b, h) at dec[row * dec_row + c * dec_step]
+__global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S, const float* __restrict__ dec,
+                                                                 int64_t dec_step, int64_t dec_row,
                                                                  const float* __restrict__ init, Dims d,
-                                                                 int64_t span_stride_q, float* states,
-                                                                 float* __restrict__ final_state) {
+                                                                 float* states, float* __restrict__ final_state) {
     const int64_t PN = (int64_t)d.headdim * d.dstate;
     const int64_t e = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * 4;
     const int h = blockIdx.y, b = blockIdx.z;
@@ -35,28 +36,27 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
     const int nc = d.nchunks;
     float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
     if (init != nullptr) hv = *reinterpret_cast<const float4*>(init + ((int64_t)b * d.nheads + h) * PN + e);
-    // decay of chunk c: 2^(cs[b, h, c, Q-1])
-    const float* csl = cs + ((int64_t)b * d.nheads + h) * nc * span_stride_q + (span_stride_q - 1);
+    const float* csl = dec + ((int64_t)b * d.nheads + h) * dec_row;
     const int64_t cstride = (int64_t)d.nheads * PN;  // distance between consecutive chunks
     const int64_t base = ((int64_t)b * nc * d.nheads + h) * PN + e;
     for (int c0 = 0; c0 < nc; c0 += kUnroll) {
         float4 sv[kUnroll];
-        float dec[kUnroll];
+        float dk[kUnroll];
 #pragma unroll
         for (int k = 0; k < kUnroll; ++k) {
             if (c0 + k < nc) {
                 sv[k] = *reinterpret_cast<const float4*>(S + base + (int64_t)(c0 + k) * cstride);
-                dec[k] = exp2f(__ldg(csl + (int64_t)(c0 + k) * span_stride_q));
+                dk[k] = exp2f(__ldg(csl + (int64_t)(c0 + k) * dec_step));
             }
         }
 #pragma unroll
         for (int k = 0; k < kUnroll; ++k) {
             if (c0 + k < nc) {
                 *reinterpret_cast<float4*>(states + base + (int64_t)(c0 + k) * cstride) = hv;
-                hv.x = fmaf(dec[k], hv.x, sv[k].x);
-                hv.y = fmaf(dec[k], hv.y, sv[k].y);
-                hv.z = fmaf(dec[k], hv.z, sv[k].z);
-                hv.w = fmaf(dec[k], hv.w, sv[k].w);
+                hv.x = fmaf(dk[k], hv.x, sv[k].x);
+                hv.y = fmaf(dk[k], hv.y, sv[k].y);
+                hv.z = fmaf(dk[k], hv.z, sv[k].z);
+                hv.w = fmaf(dk[k], hv.w, sv[k].w);
             }
         }
     }
@@ -68,10 +68,20 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
 
 int launch_state_passing(const float* S, const float* cs, const float* init, const Dims& d,
                          float* states, float* final_state, cudaStream_t s) {
+    // per-chunk decay: cs[b, h, c, Q-1]
+    return launch_state_passing_steps(S, cs + (d.chunk_size - 1), d.chunk_size, (int64_t)d.nchunks * d.chunk_size,
+                                      init, d, d.nchunks, states, final_state, s);
+}
+
+int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_step, int64_t dec_row,
+                               const float* init, const Dims& d, int nsteps, float* states, float* final_state,
+                               cudaStream_t s) {
+    Dims dd = d;
+    dd.nchunks = nsteps;
     const int64_t PN = (int64_t)d.headdim * d.dstate;
     dim3 grid((unsigned)ceil_div64(PN, (int64_t)kThreads * 4), d.nheads, d.batch);
     launch_begin(kKindStatePassing, s);
-    state_passing_kernel<<<grid, kThreads, 0, s>>>(S, cs, init, d, d.chunk_size, states, final_state);
+    state_passing_kernel<<<grid, kThreads, 0, s>>>(S, dec, dec_step, dec_row, init, dd, states, final_state);
     return launch_end(kKindStatePassing, s);
 }
 

@@ -106,6 +106,36 @@ Dims make_dims(int batch, int seqlen, int nheads, int headdim, int ngroups, int 
 // device error word (bounded waits that gave up set it)
 __device__ int g_ssd_device_error = 0;
 
+namespace {
+
+// Device address of g_ssd_device_error on the current device (cached per device).
+int* device_error_ptr() {
+    static std::mutex mu;
+    static int* cache[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 64 && cache[dev] != nullptr) return cache[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ssd_device_error) != cudaSuccess) return nullptr;
+    if (dev < 64) cache[dev] = static_cast<int*>(p);
+    return static_cast<int*>(p);
+}
+
+// Chunks per span for ssd_forward: about eight waves of 152 CTAs over
+// (batch, head, span), so the span-level intermediates stay small while
+// every SM stays busy.
+int forward_span_chunks(const Dims& d) {
+    const int64_t units = (int64_t)d.batch * d.nheads * d.nchunks;
+    int64_t k = (units + 1215) / 1216;
+    if (k < 1) k = 1;
+    if (k > 64) k = 64;
+    if (k > d.nchunks) k = d.nchunks;
+    return (int)k;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* ssd_status_string(int status) {
@@ -142,8 +172,10 @@ int ssd_chunk_state(const void* x, const void* B, const float* dt_t, const float
     if (!aligned16(x) || !aligned16(B) || !aligned16(dt_t) || !aligned16(dA_cumsum) || !aligned16(chunk_states))
         return SSD_ERR_INVALID_ARG;
     Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
-    return launch_chunk_state(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(B), dt_t,
-                              dA_cumsum, d, chunk_states, stream);
+    int* err = device_error_ptr();
+    if (err == nullptr) return SSD_ERR_CUDA;
+    return launch_chunk_state_span(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(B), dt_t,
+                                   dA_cumsum, 1, d, chunk_states, nullptr, err, stream);
 }
 
 int ssd_state_passing(const float* chunk_states, const float* dA_cumsum, const float* init_state, int batch,
@@ -172,9 +204,11 @@ int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_
         !aligned16(dA_cumsum) || !aligned16(states) || (D && ((uintptr_t)D & 3u)))
         return SSD_ERR_INVALID_ARG;
     Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
-    return launch_chunk_scan(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(B),
-                             static_cast<const __nv_bfloat16*>(C), dt_t, dA_cumsum, D, states, d,
-                             static_cast<__nv_bfloat16*>(y), stream);
+    int* err = device_error_ptr();
+    if (err == nullptr) return SSD_ERR_CUDA;
+    return launch_chunk_scan_span(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(B),
+                                  static_cast<const __nv_bfloat16*>(C), dt_t, dA_cumsum, D, states, 1, d,
+                                  static_cast<__nv_bfloat16*>(y), err, stream);
 }
 
 int ssd_forward(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,
@@ -188,9 +222,14 @@ int ssd_forward(const void* x, const float* dt, const float* A, const void* B, c
         (final_state && !aligned16(final_state)))
         return SSD_ERR_INVALID_ARG;
     Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    int* err = device_error_ptr();
+    if (err == nullptr) return SSD_ERR_CUDA;
+    const int span = forward_span_chunks(d);
+    const int nspans = ceil_div(d.nchunks, span);
     const size_t ncq = (size_t)d.batch * d.nheads * d.nchunks * d.chunk_size;
-    const size_t nst = (size_t)d.batch * d.nchunks * d.nheads * d.headdim * d.dstate;
-    const size_t bytes = (2 * ncq + nst) * sizeof(float);
+    const size_t nst = (size_t)d.batch * nspans * d.nheads * d.headdim * d.dstate;
+    const size_t ndec = ((size_t)d.batch * d.nheads * nspans + 3) & ~(size_t)3;
+    const size_t bytes = (2 * ncq + nst + ndec) * sizeof(float);
     void* ws = nullptr;
     if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
         cudaGetLastError();
@@ -199,13 +238,16 @@ int ssd_forward(const void* x, const float* dt, const float* A, const void* B, c
     float* cs = static_cast<float*>(ws);
     float* dtt = cs + ncq;
     float* S = dtt + ncq;
+    float* dec = S + nst;
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     const __nv_bfloat16* Bb = static_cast<const __nv_bfloat16*>(B);
     const __nv_bfloat16* Cb = static_cast<const __nv_bfloat16*>(C);
     r = launch_chunk_cumsum(dt, A, d, cs, dtt, stream);
-    if (r == SSD_OK) r = launch_chunk_state(xb, Bb, dtt, cs, d, S, stream);
-    if (r == SSD_OK) r = launch_state_passing(S, cs, init_state, d, S, final_state, stream);
-    if (r == SSD_OK) r = launch_chunk_scan(xb, Bb, Cb, dtt, cs, D, S, d, static_cast<__nv_bfloat16*>(y), stream);
+    if (r == SSD_OK) r = launch_chunk_state_span(xb, Bb, dtt, cs, span, d, S, dec, err, stream);
+    // span-level hop, in place: S becomes the span-start states
+    if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
+    if (r == SSD_OK)
+        r = launch_chunk_scan_span(xb, Bb, Cb, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
     return r;
 }
