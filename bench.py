@@ -50,6 +50,16 @@ def compulsory_bytes(w: I.Workload) -> float:
     return float(by)
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The slowest rank's value (timed regions are reported as the max over ranks)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -220,10 +230,7 @@ def main():
                for k in range(nk.value) if kcnt[k] > 0}
     err = ssd.ssd_get_device_error()
 
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
 
     # ---- end to end through the public call with host buffers
     e2e = e2e_measure(w, inp, dev, stream, args, ssd, dist)
@@ -367,10 +374,7 @@ def e2e_measure(w, inp, dev, stream, args, ssd, dist):
     e.record(stream)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / n
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     world = dist.get_world_size() if dist is not None else 1
     return {"value": round(w.batch * w.seqlen * world / (ms / 1e3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4)}

@@ -51,6 +51,12 @@
  *    chunk_size in {64, 128, 256}; nheads % ngroups == 0; x, B, C, y and the
  *    float32 tensors 16-byte aligned.  Other shapes return
  *    SSD_ERR_UNSUPPORTED (valid but not implemented) or SSD_ERR_INVALID_ARG.
+ *  * Precision: the tensor-core products run on float16 operands with float32
+ *    accumulation.  B and C are copied to float16 (exact for magnitudes in
+ *    [2^-14, 65504]; larger magnitudes saturate), x is converted the same way
+ *    on chip, and the derived operands (decayed masked C B^T, carried state,
+ *    decay-scaled x) are rounded once to float16.  Inputs are expected to lie
+ *    in float16's range.
  *  * No C++ exception crosses this boundary.  The library keeps no state
  *    between calls other than the optional profiling counters below; calls
  *    on different streams may run concurrently.
@@ -100,7 +106,9 @@ SSD_API int ssd_chunk_cumsum(const float* dt, const float* A, int batch, int seq
  * jump-formula paragraph):
  *   chunk_states[b,c,h][p][n] = sum_{i in chunk c} B[b,t_i,g,n] * w_i * x[b,t_i,h,p],
  *   w_i = 2^(dA_cumsum[b,h,c,Q-1] - dA_cumsum[b,h,c,i]) * dt_t[b,h,c,i].
- * dt_t and dA_cumsum are ssd_chunk_cumsum's outputs.
+ * dt_t and dA_cumsum are ssd_chunk_cumsum's outputs.  Allocates a
+ * stream-ordered float16 copy of B (cudaMallocAsync / cudaFreeAsync on
+ * `stream`); returns SSD_ERR_NO_MEMORY if that fails.
  */
 SSD_API int ssd_chunk_state(const void* x, const void* B, const float* dt_t, const float* dA_cumsum,
                     int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
@@ -128,6 +136,8 @@ SSD_API int ssd_state_passing(const float* chunk_states, const float* dA_cumsum,
  *          + sum_{j<=i} (C_i . B_j) * 2^(cs_i - cs_j) * dt_j * x_j
  *          + D[h] * x_i,          cs = dA_cumsum[b,h,c,:],  h_c = states[b,c,h]
  * D may be NULL (no skip term).  y: (batch, seqlen, nheads, headdim) bfloat16.
+ * Allocates stream-ordered float16 copies of B and C (cudaMallocAsync /
+ * cudaFreeAsync on `stream`); returns SSD_ERR_NO_MEMORY if that fails.
  */
 SSD_API int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_t,
                    const float* dA_cumsum, const float* D, const float* states, int batch,

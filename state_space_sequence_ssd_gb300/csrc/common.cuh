@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "../../include/ssd.h"
@@ -25,7 +26,8 @@ enum KernelKind {
     kKindChunkState = 1,
     kKindStatePassing = 2,
     kKindChunkScan = 3,
-    kNumKinds = 4
+    kKindConvert = 4,
+    kNumKinds = 5
 };
 
 // Launch bookkeeping implemented in ssd_api.cu: opens/closes the optional
@@ -38,7 +40,11 @@ int launch_end(int kind, cudaStream_t s);  // returns SSD_OK or SSD_ERR_CUDA
 // one-chunk spans, ssd_forward uses longer ones.  `err` is the device error word.
 int launch_chunk_cumsum(const float* dt, const float* A, const Dims& d, float* cs, float* dtt,
                         cudaStream_t s);
-int launch_chunk_state_span(const __nv_bfloat16* x, const __nv_bfloat16* B, const float* dtt, const float* cs,
+// B, C (bf16) -> float16 copies for the tensor-core products (see k_convert.cu)
+int launch_bc_to_f16(const __nv_bfloat16* B, const __nv_bfloat16* C, const Dims& d, __half* B16, __half* C16,
+                     cudaStream_t s);
+// B and C below are the float16 copies; x stays bfloat16.
+int launch_chunk_state_span(const __nv_bfloat16* x, const __half* B, const float* dtt, const float* cs,
                             int span_chunks, const Dims& d, float* S, float* span_decay, int* err,
                             cudaStream_t s);
 int launch_state_passing(const float* S, const float* cs, const float* init, const Dims& d,
@@ -46,7 +52,7 @@ int launch_state_passing(const float* S, const float* cs, const float* init, con
 int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_step, int64_t dec_row,
                                const float* init, const Dims& d, int nsteps, float* states, float* final_state,
                                cudaStream_t s);
-int launch_chunk_scan_span(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfloat16* C,
+int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C,
                            const float* dtt, const float* cs, const float* D, const float* span_states,
                            int span_chunks, const Dims& d, __nv_bfloat16* y, int* err, cudaStream_t s);
 

@@ -19,7 +19,7 @@
 //   S    : h   <- 2^(u_last) h + B^T (w X),   w_j = 2^(u_last - u_j) dt_j
 //   YS   : Yst  = C h                          -> y_i += 2^(u_i) Yst_i
 //   CB   : CB   = C B^T                        (128 x 128, f32 in TMEM)
-//   mask : M    = CB * 2^(u_i - u_j) dt_j [j <= i]   (bf16, back into TMEM)
+//   mask : M    = CB * 2^(u_i - u_j) dt_j [j <= i]   (float16, back into TMEM)
 //   MX   : Y    = M X                          (A operand read from TMEM)
 //   y_i  = Y_i + 2^(u_i) Yst_i + D x_i
 //
@@ -30,7 +30,7 @@
 //
 // Roles (448 threads):
 //   warps 0-3   mask warpgroup: CB -> M (one row per thread)
-//   warps 4-7   state warpgroup: u/dt, scaled X' = w X, the bf16 copy of the
+//   warps 4-7   state warpgroup: u/dt, scaled X' = w X, the float16 copy of the
 //               state for C h and the decay of the state in TMEM
 //   warps 8-11  epilogue warpgroup: y = Y + 2^u Yst + D x, written over the
 //               x tile in shared memory, then stored by TMA
@@ -39,7 +39,13 @@
 // The MMA issue order is software-pipelined by one sub-block:
 //   S(0) YS(0) CB(0) | S(1) YS(1) CB(1) MX(0) | S(2) YS(2) CB(2) MX(1) | ...
 // with two TMEM buffer sets {CB/M/Y, Yst} so the mask and epilogue of one
-// sub-block overlap the MMAs of the next.  Every wait is bounded (1 s); a
+// sub-block overlap the MMAs of the next.
+//
+// Precision: all four products run in float16 (kind::f16, f32 accumulate).
+// B and C are exact float16 copies of the inputs; the x tile is converted to
+// float16 in place (exact for normal-range bfloat16); the derived operands M,
+// h and w x are rounded once to float16 (11 significant bits), which keeps
+// every output within 1e-2 + 1e-2 |y| where bfloat16 operands do not.  Every wait is bounded (1 s); a
 // role that gives up sets the CTA abort flag and the device error word, and
 // all roles fall through to teardown.
 #include "common.cuh"
@@ -64,7 +70,7 @@ struct Cfg {
     static constexpr int NST = (N == 512) ? 1 : 2;
     static constexpr bool S_FIRST = NBLK <= NST;  // all n-blocks resident: issue every S before YS/CB
     static constexpr int NBUF = (N == 512) ? 1 : 2;
-    static constexpr int NH = (N <= 128) ? 2 : 1;  // bf16 state copies
+    static constexpr int NH = (N <= 128) ? 2 : 1;  // float16 state copies
     static constexpr int NX = 2;
     // TMEM columns
     static constexpr int T_H = 0;
@@ -89,10 +95,10 @@ struct Cfg {
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-constexpr uint32_t kIdescCB = idesc_bf16(128, 128, false, false);
-constexpr uint32_t kIdescYS = idesc_bf16(128, 64, false, true);
-constexpr uint32_t kIdescS = idesc_bf16(128, 64, true, true);
-constexpr uint32_t kIdescMX = idesc_bf16(128, 64, false, true);
+constexpr uint32_t kIdescCB = idesc_fp16(128, 128, false, false);
+constexpr uint32_t kIdescYS = idesc_fp16(128, 64, false, true);
+constexpr uint32_t kIdescS = idesc_fp16(128, 64, true, true);
+constexpr uint32_t kIdescMX = idesc_fp16(128, 64, false, true);
 
 struct ScanArgs {
     Dims d;
@@ -115,6 +121,11 @@ struct Bars {
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
@@ -367,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int jj = 0; jj < 32; jj += 2) {
                             const int j = q * 32 + jj;
-                            o[jj >> 1] = pack_bf16x2(__uint_as_float(v[jj]) * ar * sbc[j],
-                                                     __uint_as_float(v[jj + 1]) * ar * sbc[j + 1]);
+                            o[jj >> 1] = pack_f16x2(__uint_as_float(v[jj]) * ar * sbc[j],
+                                                    __uint_as_float(v[jj + 1]) * ar * sbc[j + 1]);
                         }
                     } else {  // diagonal block: exact per-element decay
 #pragma unroll
@@ -380,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float m1 = (j1 <= r && j1 < nv)
                                                  ? __uint_as_float(v[jj + 1]) * exp2f(fminf(ui - su[j1], 0.f)) * sdt[j1]
                                                  : 0.f;
-                            o[jj >> 1] = pack_bf16x2(m0, m1);
+                            o[jj >> 1] = pack_f16x2(m0, m1);
                         }
                     }
                 }
@@ -445,25 +456,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = ok && (sb == 0 || mbar_wait_bounded(&bar->xs_free, (sb - 1) & 1, abort_flag, a.err, 14, kWaitNs));
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
+                // x row -> float16 in place (exact in range) and w x -> the X' tile (float16)
                 const float w = valid ? exp2f(ulast - u) * dtv : 0.f;
-                const uint8_t* xrow = smem + K::OFF_X + xb * kTile;
+                uint8_t* xrow = smem + K::OFF_X + xb * kTile;
                 uint8_t* xsrow = smem + K::OFF_XS;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     const uint32_t off = sw128_offset(r, ch);
-                    uint4 v = *reinterpret_cast<const uint4*>(xrow + off);
-                    __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&v);
+                    const uint4 v = *reinterpret_cast<const uint4*>(xrow + off);
+                    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+                    uint4 xo, wo;
+                    uint32_t* x4 = reinterpret_cast<uint32_t*>(&xo);
+                    uint32_t* w4 = reinterpret_cast<uint32_t*>(&wo);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        float2 f = __bfloat1622float2(p2[e]);
-                        p2[e] = __floats2bfloat162_rn(f.x * w, f.y * w);
+                        const float2 f = __bfloat1622float2(p2[e]);
+                        x4[e] = pack_f16x2(f.x, f.y);
+                        w4[e] = pack_f16x2(f.x * w, f.y * w);
                     }
-                    *reinterpret_cast<uint4*>(xsrow + off) = v;
+                    *reinterpret_cast<uint4*>(xrow + off) = xo;
+                    *reinterpret_cast<uint4*>(xsrow + off) = wo;
                 }
                 fence_proxy_async_smem();
             }
             mbar_arrive(&bar->xs_ready);
-            // 3. state h_sb -> bf16 copy for C h, and h <- 2^(u_last) h in TMEM
+            // 3. state h_sb -> float16 copy for C h, and h <- 2^(u_last) h in TMEM
             if (sb > 0) {
                 ok = ok && mbar_wait_bounded(&bar->state_done, (sb - 1) & 1, abort_flag, a.err, 15, kWaitNs);
                 ok = __all_sync(0xffffffffu, ok);
@@ -495,10 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int ch = 0; ch < 8; ++ch) {
                             uint4 v;
-                            v.x = pack_bf16x2(hv[ch * 8 + 0], hv[ch * 8 + 1]);
-                            v.y = pack_bf16x2(hv[ch * 8 + 2], hv[ch * 8 + 3]);
-                            v.z = pack_bf16x2(hv[ch * 8 + 4], hv[ch * 8 + 5]);
-                            v.w = pack_bf16x2(hv[ch * 8 + 6], hv[ch * 8 + 7]);
+                            v.x = pack_f16x2(hv[ch * 8 + 0], hv[ch * 8 + 1]);
+                            v.y = pack_f16x2(hv[ch * 8 + 2], hv[ch * 8 + 3]);
+                            v.z = pack_f16x2(hv[ch * 8 + 4], hv[ch * 8 + 5]);
+                            v.w = pack_f16x2(hv[ch * 8 + 6], hv[ch * 8 + 7]);
                             *reinterpret_cast<uint4*>(hbase + sw128_offset(hr, ch)) = v;
                         }
                     }
@@ -546,13 +563,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     const uint32_t off = sw128_offset(r, ch);
-                    uint4 xv = *reinterpret_cast<const uint4*>(xrow + off);
-                    const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
+                    uint4 xv = *reinterpret_cast<const uint4*>(xrow + off);  // float16 since the X' step
+                    const __half2* x2 = reinterpret_cast<const __half2*>(&xv);
                     uint4 ov;
                     uint32_t* o4 = reinterpret_cast<uint32_t*>(&ov);
 #pragma unroll
                     for (int e2 = 0; e2 < 4; ++e2) {
-                        const float2 xf = __bfloat1622float2(x2[e2]);
+                        const float2 xf = __half22float2(x2[e2]);
                         const int c = ch * 8 + e2 * 2;
                         const float y0 = __uint_as_float(yv[c >> 5][c & 31]) +
                                          e * __uint_as_float(sv[c >> 5][c & 31]) + Dh * xf.x;
@@ -587,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int N>
-int launch_scan_n(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfloat16* C, __nv_bfloat16* y,
+int launch_scan_n(const __nv_bfloat16* x, const __half* B, const __half* C, __nv_bfloat16* y,
                   const ScanArgs& a, cudaStream_t s) {
     const Dims& d = a.d;
     CUtensorMap tx, tb, tc, ty;
@@ -595,8 +612,8 @@ int launch_scan_n(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfl
     const uint64_t dbc[4] = {(uint64_t)d.dstate, (uint64_t)d.ngroups, (uint64_t)d.seqlen, (uint64_t)d.batch};
     const uint32_t box_in[4] = {64, 1, 128, 1};
     const uint32_t box_out[4] = {64, 1, 64, 1};
-    if (!make_tmap_bf16_4d(&tx, x, dx, box_in) || !make_tmap_bf16_4d(&tb, B, dbc, box_in) ||
-        !make_tmap_bf16_4d(&tc, C, dbc, box_in) || !make_tmap_bf16_4d(&ty, y, dx, box_out))
+    if (!make_tmap_16b_4d(&tx, x, dx, box_in) || !make_tmap_16b_4d(&tb, B, dbc, box_in) ||
+        !make_tmap_16b_4d(&tc, C, dbc, box_in) || !make_tmap_16b_4d(&ty, y, dx, box_out))
         return SSD_ERR_CUDA;
     const int smem = Cfg<N>::SMEM;
     if (cudaFuncSetAttribute(chunk_scan_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -610,7 +627,7 @@ int launch_scan_n(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfl
 
 }  // namespace
 
-int launch_chunk_scan_span(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfloat16* C,
+int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C,
                            const float* dtt, const float* cs, const float* D, const float* span_states,
                            int span_chunks, const Dims& d, __nv_bfloat16* y, int* err, cudaStream_t s) {
     ScanArgs a;

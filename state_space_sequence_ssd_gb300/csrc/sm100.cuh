@@ -150,7 +150,7 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D(tmem) (+)= A(smem desc) * B(smem desc), kind::f16 (bf16 inputs, f32 accumulate)
+// D(tmem) (+)= A(smem desc) * B(smem desc), kind::f16 (16-bit inputs, f32 accumulate)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
     asm volatile(
@@ -177,15 +177,21 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and f32 D.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+// Instruction descriptor, kind::f16 with f32 D; A/B both float16 (fmt 0) or both bfloat16 (fmt 1).
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool a_mn_major, bool b_mn_major, uint32_t fmt) {
     return (1u << 4)                                  // D format: f32
-           | (1u << 7)                                // A format: bf16
-           | (1u << 10)                               // B format: bf16
+           | (fmt << 7)                               // A format
+           | (fmt << 10)                              // B format
            | ((a_mn_major ? 1u : 0u) << 15)           // A major-ness
            | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
            | ((uint32_t)(N >> 3) << 17)               // N / 8
            | ((uint32_t)(M >> 4) << 24);              // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return idesc_f16kind(M, N, a_mn_major, b_mn_major, 1u);
+}
+__host__ __device__ constexpr uint32_t idesc_fp16(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return idesc_f16kind(M, N, a_mn_major, b_mn_major, 0u);
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled tile.

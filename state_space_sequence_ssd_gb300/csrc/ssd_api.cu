@@ -38,7 +38,8 @@ cudaEvent_t take_event() {
     return e;
 }
 
-const char* const kKindNames[kNumKinds] = {"chunk_cumsum", "chunk_state", "state_passing", "chunk_scan"};
+const char* const kKindNames[kNumKinds] = {"chunk_cumsum", "chunk_state", "state_passing", "chunk_scan",
+                                           "bc_to_f16"};
 
 }  // namespace
 
@@ -174,8 +175,20 @@ int ssd_chunk_state(const void* x, const void* B, const float* dt_t, const float
     Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
     int* err = device_error_ptr();
     if (err == nullptr) return SSD_ERR_CUDA;
-    return launch_chunk_state_span(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(B), dt_t,
-                                   dA_cumsum, 1, d, chunk_states, nullptr, err, stream);
+    // stream-ordered float16 copy of B for the tensor-core products
+    const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, nbc * sizeof(__half), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SSD_ERR_NO_MEMORY;
+    }
+    __half* B16 = static_cast<__half*>(ws);
+    r = launch_bc_to_f16(static_cast<const __nv_bfloat16*>(B), nullptr, d, B16, nullptr, stream);
+    if (r == SSD_OK)
+        r = launch_chunk_state_span(static_cast<const __nv_bfloat16*>(x), B16, dt_t, dA_cumsum, 1, d, chunk_states,
+                                    nullptr, err, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
+    return r;
 }
 
 int ssd_state_passing(const float* chunk_states, const float* dA_cumsum, const float* init_state, int batch,
@@ -206,9 +219,22 @@ int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_
     Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
     int* err = device_error_ptr();
     if (err == nullptr) return SSD_ERR_CUDA;
-    return launch_chunk_scan_span(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(B),
-                                  static_cast<const __nv_bfloat16*>(C), dt_t, dA_cumsum, D, states, 1, d,
-                                  static_cast<__nv_bfloat16*>(y), err, stream);
+    // stream-ordered float16 copies of B and C for the tensor-core products
+    const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, 2 * nbc * sizeof(__half), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SSD_ERR_NO_MEMORY;
+    }
+    __half* B16 = static_cast<__half*>(ws);
+    __half* C16 = B16 + nbc;
+    r = launch_bc_to_f16(static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), d, B16, C16,
+                         stream);
+    if (r == SSD_OK)
+        r = launch_chunk_scan_span(static_cast<const __nv_bfloat16*>(x), B16, C16, dt_t, dA_cumsum, D, states, 1, d,
+                                   static_cast<__nv_bfloat16*>(y), err, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
+    return r;
 }
 
 int ssd_forward(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,
@@ -229,7 +255,8 @@ int ssd_forward(const void* x, const float* dt, const float* A, const void* B, c
     const size_t ncq = (size_t)d.batch * d.nheads * d.nchunks * d.chunk_size;
     const size_t nst = (size_t)d.batch * nspans * d.nheads * d.headdim * d.dstate;
     const size_t ndec = ((size_t)d.batch * d.nheads * nspans + 3) & ~(size_t)3;
-    const size_t bytes = (2 * ncq + nst + ndec) * sizeof(float);
+    const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;  // multiple of 64
+    const size_t bytes = (2 * ncq + nst + ndec) * sizeof(float) + 2 * nbc * sizeof(__half);
     void* ws = nullptr;
     if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
         cudaGetLastError();
@@ -239,15 +266,18 @@ int ssd_forward(const void* x, const float* dt, const float* A, const void* B, c
     float* dtt = cs + ncq;
     float* S = dtt + ncq;
     float* dec = S + nst;
+    __half* B16 = reinterpret_cast<__half*>(dec + ndec);
+    __half* C16 = B16 + nbc;
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-    const __nv_bfloat16* Bb = static_cast<const __nv_bfloat16*>(B);
-    const __nv_bfloat16* Cb = static_cast<const __nv_bfloat16*>(C);
     r = launch_chunk_cumsum(dt, A, d, cs, dtt, stream);
-    if (r == SSD_OK) r = launch_chunk_state_span(xb, Bb, dtt, cs, span, d, S, dec, err, stream);
+    if (r == SSD_OK)
+        r = launch_bc_to_f16(static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), d, B16, C16,
+                             stream);
+    if (r == SSD_OK) r = launch_chunk_state_span(xb, B16, dtt, cs, span, d, S, dec, err, stream);
     // span-level hop, in place: S becomes the span-start states
     if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
     if (r == SSD_OK)
-        r = launch_chunk_scan_span(xb, Bb, Cb, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream);
+        r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
     return r;
 }

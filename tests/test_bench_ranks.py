@@ -1,0 +1,47 @@
+"""bench.py's multi-rank host logic on CPU: world size 2 over gloo.
+
+Every rank times its own replica; the reported time is the slowest rank's,
+so `max_over_ranks` must return the maximum on every rank."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, values, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    out[rank] = bench.max_over_ranks(values[rank], dist, torch.device("cpu"))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_world2():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    values = [3.5, 7.25]
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, values, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    assert out[0] == pytest.approx(7.25) and out[1] == pytest.approx(7.25)
+
+
+def test_max_over_ranks_single_process():
+    import bench
+    assert bench.max_over_ranks(2.0, None, torch.device("cpu")) == 2.0
