@@ -107,7 +107,7 @@ SSD_API int ssd_chunk_cumsum(const float* dt, const float* A, int batch, int seq
  *   chunk_states[b,c,h][p][n] = sum_{i in chunk c} B[b,t_i,g,n] * w_i * x[b,t_i,h,p],
  *   w_i = 2^(dA_cumsum[b,h,c,Q-1] - dA_cumsum[b,h,c,i]) * dt_t[b,h,c,i].
  * dt_t and dA_cumsum are ssd_chunk_cumsum's outputs.  Allocates a
- * stream-ordered float16 copy of B (cudaMallocAsync / cudaFreeAsync on
+ * stream-ordered float16 copy of B from the library's memory pool (freed on
  * `stream`); returns SSD_ERR_NO_MEMORY if that fails.
  */
 SSD_API int ssd_chunk_state(const void* x, const void* B, const float* dt_t, const float* dA_cumsum,
@@ -136,8 +136,8 @@ SSD_API int ssd_state_passing(const float* chunk_states, const float* dA_cumsum,
  *          + sum_{j<=i} (C_i . B_j) * 2^(cs_i - cs_j) * dt_j * x_j
  *          + D[h] * x_i,          cs = dA_cumsum[b,h,c,:],  h_c = states[b,c,h]
  * D may be NULL (no skip term).  y: (batch, seqlen, nheads, headdim) bfloat16.
- * Allocates stream-ordered float16 copies of B and C (cudaMallocAsync /
- * cudaFreeAsync on `stream`); returns SSD_ERR_NO_MEMORY if that fails.
+ * Allocates stream-ordered float16 copies of B and C from the library's
+ * memory pool (freed on `stream`); returns SSD_ERR_NO_MEMORY if that fails.
  */
 SSD_API int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_t,
                    const float* dA_cumsum, const float* D, const float* states, int batch,
@@ -147,8 +147,10 @@ SSD_API int ssd_chunk_scan(const void* x, const void* B, const void* C, const fl
 /*
  * ssd_forward -- the whole chunked forward pass: y and the final state from
  * the raw inputs.  D, init_state and final_state may be NULL.  Allocates its
- * workspace stream-ordered on `stream` (cudaMallocAsync / cudaFreeAsync) and
- * returns SSD_ERR_NO_MEMORY if that fails.  The result equals the recurrence
+ * workspace stream-ordered on `stream` from a library-owned memory pool per
+ * device that keeps freed memory cached for the next call
+ * (cudaMallocFromPoolAsync / cudaFreeAsync), and returns SSD_ERR_NO_MEMORY if
+ * that fails.  The result equals the recurrence
  * above for any chunk_size; chunk_size only sets the internal tiling.
  */
 SSD_API int ssd_forward(const void* x, const float* dt, const float* A, const void* B, const void* C,

@@ -30,6 +30,9 @@ enum KernelKind {
     kNumKinds = 5
 };
 
+// Sets a kernel's dynamic shared-memory limit once per (kernel, device).
+int ensure_smem_limit(const void* kernel, int bytes);
+
 // Launch bookkeeping implemented in ssd_api.cu: opens/closes the optional
 // profiling event pair around one launch and counts it.
 void launch_begin(int kind, cudaStream_t s);
@@ -40,6 +43,9 @@ int launch_end(int kind, cudaStream_t s);  // returns SSD_OK or SSD_ERR_CUDA
 // one-chunk spans, ssd_forward uses longer ones.  `err` is the device error word.
 int launch_chunk_cumsum(const float* dt, const float* A, const Dims& d, float* cs, float* dtt,
                         cudaStream_t s);
+// chunk_cumsum plus, in the same launch, the float16 copies of B and C
+int launch_chunk_cumsum_bc(const float* dt, const float* A, const Dims& d, float* cs, float* dtt,
+                           const __nv_bfloat16* B, const __nv_bfloat16* C, __half* B16, __half* C16, cudaStream_t s);
 // B, C (bf16) -> float16 copies for the tensor-core products (see k_convert.cu)
 int launch_bc_to_f16(const __nv_bfloat16* B, const __nv_bfloat16* C, const Dims& d, __half* B16, __half* C16,
                      cudaStream_t s);

@@ -19,35 +19,39 @@
 //   S    : h   <- 2^(u_last) h + B^T (w X),   w_j = 2^(u_last - u_j) dt_j
 //   YS   : Yst  = C h                          -> y_i += 2^(u_i) Yst_i
 //   CB   : CB   = C B^T                        (128 x 128, f32 in TMEM)
-//   mask : M    = CB * 2^(u_i - u_j) dt_j [j <= i]   (float16, back into TMEM)
-//   MX   : Y    = M X                          (A operand read from TMEM)
-//   y_i  = Y_i + 2^(u_i) Yst_i + D x_i
+//   mask : M    = CB * 2^(u_i - u_j) dt_j [j <= i] + D [j == i]   (float16, back into TMEM)
+//   MX   : Y    = M X                          (A operand read from TMEM; includes the D skip)
+//   y_i  = Y_i + 2^(u_i) Yst_i
 //
 // The mask never exponentiates more than a 32 x 32 diagonal block per row:
 // for a column block q strictly below the row's block, with r the block's
 // last position, 2^(u_i - u_j) = 2^(u_i - u_r) * 2^(u_r - u_j), both factors
 // <= 1 (u is non-increasing), so no factor overflows.
 //
-// Roles (448 threads):
+// Roles (480 threads):
 //   warps 0-3   mask warpgroup: CB -> M (one row per thread)
-//   warps 4-7   state warpgroup: u/dt, scaled X' = w X, the float16 copy of the
-//               state for C h and the decay of the state in TMEM
-//   warps 8-11  epilogue warpgroup: y = Y + 2^u Yst + D x, written over the
-//               x tile in shared memory, then stored by TMA
-//   warp 12     TMA producer
+//   warps 4-7   state warpgroup: u/dt/column weights of each sub-block, the
+//               x tile converted to float16 in place with X' = w X, the
+//               float16 copy of the state for C h and the decay of the state
+//               held in TMEM
+//   warps 8-11  epilogue warpgroup: y = Y + 2^u Yst, each thread storing its
+//               128-byte row of y straight from registers
+//   warp 12     producer of the x tiles and dA_cumsum/dt rows (TMA)
 //   warp 13     TMEM owner and single-thread MMA issuer
-// The MMA issue order is software-pipelined by one sub-block:
-//   S(0) YS(0) CB(0) | S(1) YS(1) CB(1) MX(0) | S(2) YS(2) CB(2) MX(1) | ...
-// with two TMEM buffer sets {CB/M/Y, Yst} so the mask and epilogue of one
-// sub-block overlap the MMAs of the next.
+//   warp 14     producer of the C and B tiles (TMA), running ahead independently
+// The MMA issuer polls readiness and issues whichever is ready: the "front"
+// of the next sub-block (S, YS, CB) or the M X of a finished mask, keeping at
+// most two sub-blocks in flight over two TMEM buffer sets {CB/M/Y, Yst}.  The
+// x tile is released as soon as its M X retires.
 //
 // Precision: all four products run in float16 (kind::f16, f32 accumulate).
 // B and C are exact float16 copies of the inputs; the x tile is converted to
 // float16 in place (exact for normal-range bfloat16); the derived operands M,
 // h and w x are rounded once to float16 (11 significant bits), which keeps
-// every output within 1e-2 + 1e-2 |y| where bfloat16 operands do not.  Every wait is bounded (1 s); a
-// role that gives up sets the CTA abort flag and the device error word, and
-// all roles fall through to teardown.
+// every output within 1e-2 + 1e-2 |y| where bfloat16 operands do not.
+//
+// Every wait is bounded (1 s); a role that gives up sets the CTA abort flag
+// and the device error word, and all roles fall through to teardown.
 #include "common.cuh"
 #include "sm100.cuh"
 #include "tmap.cuh"
@@ -58,9 +62,9 @@ namespace {
 using namespace sm100;
 
 constexpr uint64_t kWaitNs = 1000000000ull;
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
 constexpr int kTile = 16384;  // 128 rows x 128 B
-constexpr int kWarpTma = 12, kWarpMma = 13;
+constexpr int kWarpTma = 12, kWarpMma = 13, kWarpTmaBC = 14;
 
 template <int N>
 struct Cfg {
@@ -70,8 +74,7 @@ struct Cfg {
     static constexpr int NST = (N == 512) ? 1 : 2;
     static constexpr bool S_FIRST = NBLK <= NST;  // all n-blocks resident: issue every S before YS/CB
     static constexpr int NBUF = (N == 512) ? 1 : 2;
-    static constexpr int NH = (N <= 128) ? 2 : 1;  // float16 state copies
-    static constexpr int NX = 2;
+    static constexpr int NX = (N == 256) ? 2 : 3;  // x tiles in flight
     // TMEM columns
     static constexpr int T_H = 0;
     static constexpr int HC = NBLK * 64;
@@ -80,17 +83,18 @@ struct Cfg {
     static constexpr int TCOLS = 512;
     static_assert(HC + NBUF * SET <= TCOLS, "TMEM budget");
     // shared memory (offsets from a 1024-aligned base)
-    static constexpr int OFF_X = 0;  // NX x tiles (y is written over them)
+    static constexpr int OFF_X = 0;  // NX x tiles
     static constexpr int OFF_XS = OFF_X + NX * kTile;
     static constexpr int OFF_H = OFF_XS + kTile;
     static constexpr int SZ_H = N * 128;
-    static constexpr int OFF_BC = OFF_H + NH * SZ_H;
+    static constexpr int OFF_BC = OFF_H + SZ_H;
     static constexpr int SZ_C = BOXES * kTile;
     static constexpr int SZ_STAGE = 2 * SZ_C;  // C then B
     static constexpr int OFF_ZERO = OFF_BC + NST * SZ_STAGE;
     static constexpr int SZ_ZERO = (N == 64) ? kTile : 0;
     static constexpr int OFF_U = OFF_ZERO + SZ_ZERO;  // 3 x {u[128], dt[128], bcol[128]}
-    static constexpr int OFF_BAR = OFF_U + 3 * 1536;
+    static constexpr int OFF_CD = OFF_U + 3 * 1536;   // NX x {cs[128], dt[128]} rows, bulk-copied with x
+    static constexpr int OFF_BAR = OFF_CD + NX * 1024;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + alignment slack
     static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -108,15 +112,16 @@ struct ScanArgs {
     const float* dtt;   // (b, H, nc, Q)
     const float* D;     // (H) or null
     const float* init;  // (b, nspans, H, P, N) span-start states
+    __nv_bfloat16* y;   // (b, L, H, P)
     int* err;
 };
 
 struct Bars {
-    uint64_t x_full[2], x_empty[2];
+    uint64_t x_full[3], x_empty[3];
     uint64_t bc_full[2], bc_empty[2];
     uint64_t uv_ready[3], u_free[3];
-    uint64_t cb_full[2], y_free[2];
-    uint64_t xs_ready, xs_free, h_ready, state_done, m_ready, y_full, final_mma;
+    uint64_t cb_full[2], m_ready[2], y_full[2], y_free[2];
+    uint64_t xs_ready, xs_free, h_ready, state_done, final_mma;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -129,15 +134,17 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ void named_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+// In-sub-block inclusive log2 decay of position i (raw per-chunk cumsums in
+// scs, the raw value before the sub-block in prev when it starts inside a
+// chunk; a 64-token chunk boundary may fall inside the sub-block).
+__device__ __forceinline__ float sub_block_decay(const float* scs, float prev, int p0, int Q, int i) {
+    return ((p0 + i) / Q == 0) ? (scs[i] - prev) : ((scs[Q - 1 - p0] - prev) + scs[i]);
 }
 
 template <int N>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
-                         const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y,
-                         ScanArgs a) {
+                         const __grid_constant__ CUtensorMap tm_C, ScanArgs a) {
     using K = Cfg<N>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -156,24 +163,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nsb = (int)((te - ts + 127) / 128);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 3; ++i) {
             mbar_init(&bar->x_full[i], 1);
-            mbar_init(&bar->x_empty[i], 2);  // MX commit + epilogue after its TMA store read the tile
+            mbar_init(&bar->x_empty[i], 1);   // the M X product that read the tile has retired
+            mbar_init(&bar->uv_ready[i], 128);
+            mbar_init(&bar->u_free[i], 256);  // mask and epilogue are done with this u buffer
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&bar->bc_full[i], 1);
             mbar_init(&bar->bc_empty[i], 1);
             mbar_init(&bar->cb_full[i], 1);
+            mbar_init(&bar->m_ready[i], 128);
+            mbar_init(&bar->y_full[i], 1);
             mbar_init(&bar->y_free[i], 128);
-        }
-        for (int i = 0; i < 3; ++i) {
-            mbar_init(&bar->uv_ready[i], 128);
-            mbar_init(&bar->u_free[i], 128);  // the epilogue has read u of this buffer
         }
         mbar_init(&bar->xs_ready, 128);
         mbar_init(&bar->xs_free, 1);
         mbar_init(&bar->h_ready, 128);
         mbar_init(&bar->state_done, 1);
-        mbar_init(&bar->m_ready, 128);
-        mbar_init(&bar->y_full, 1);
         mbar_init(&bar->final_mma, 1);
         abort_sh = 0;
         fence_barrier_init();
@@ -191,7 +198,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_x);
         tma_prefetch_desc(&tm_B);
         tma_prefetch_desc(&tm_C);
-        tma_prefetch_desc(&tm_y);
     }
     tc_fence_before();
     __syncthreads();
@@ -200,20 +206,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = &abort_sh;
 
     if (warp == kWarpTma) {
-        // ------------------------------------------------------ TMA producer
+        // ------------------------------------------------------ x / dA_cumsum / dt producer
+        if (lane == 0) {
+            int issued[3] = {0, 0, 0};
+            const int64_t rowlen = (int64_t)d.nchunks * Q;
+            for (int sb = 0; sb < nsb; ++sb) {
+                const int t0 = (int)(ts + sb * 128);
+                const int xb = sb % K::NX;
+                if (!mbar_wait_bounded(&bar->x_empty[xb], ((sb / K::NX) & 1) ^ 1, abort_flag, a.err, 1, kWaitNs))
+                    break;
+                // this sub-block's rows of dA_cumsum and dt (contiguous per (b, h); at most 128)
+                const uint32_t cdb = (uint32_t)min((int64_t)128, rowlen - t0) * 4u;
+                float* scd = reinterpret_cast<float*>(smem + K::OFF_CD + xb * 1024);
+                mbar_arrive_expect_tx(&bar->x_full[xb], kTile + 2 * cdb);
+                tma_load_4d(smem + K::OFF_X + xb * kTile, &tm_x, &bar->x_full[xb], 0, h, t0, b);
+                bulk_load(scd, a.cs + ((int64_t)b * H + h) * rowlen + t0, cdb, &bar->x_full[xb]);
+                bulk_load(scd + 128, a.dtt + ((int64_t)b * H + h) * rowlen + t0, cdb, &bar->x_full[xb]);
+                ++issued[xb];
+            }
+            // no load may still be landing in shared memory at teardown
+            for (int i = 0; i < K::NX; ++i)
+                if (issued[i] > 0)
+                    mbar_wait_bounded(&bar->x_full[i], (issued[i] - 1) & 1, abort_flag, a.err, 3, kWaitNs);
+        }
+    } else if (warp == kWarpTmaBC) {
+        // ------------------------------------------------------ C / B producer
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            int issued_x[2] = {0, 0};
-            int issued_bc[2] = {0, 0};
+            int issued[2] = {0, 0};
             for (int sb = 0; sb < nsb && ok; ++sb) {
                 const int t0 = (int)(ts + sb * 128);
-                const int xb = sb % K::NX;
-                ok = mbar_wait_bounded(&bar->x_empty[xb], ((sb / K::NX) & 1) ^ 1, abort_flag, a.err, 1, kWaitNs);
-                if (!ok) break;
-                mbar_arrive_expect_tx(&bar->x_full[xb], kTile);
-                tma_load_4d(smem + K::OFF_X + xb * kTile, &tm_x, &bar->x_full[xb], 0, h, t0, b);
-                ++issued_x[xb];
                 for (int nb = 0; nb < K::NBLK && ok; ++nb, ++it) {
                     const int st = it % K::NST;
                     ok = mbar_wait_bounded(&bar->bc_empty[st], ((it / K::NST) & 1) ^ 1, abort_flag, a.err, 2,
@@ -227,38 +250,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_4d(sC + bx * kTile, &tm_C, &bar->bc_full[st], nb * K::NB + bx * 64, g, t0, b);
                         tma_load_4d(sB + bx * kTile, &tm_B, &bar->bc_full[st], nb * K::NB + bx * 64, g, t0, b);
                     }
-                    ++issued_bc[st];
+                    ++issued[st];
                 }
             }
-            // no load may still be landing in shared memory at teardown
-            for (int i = 0; i < 2; ++i) {
-                if (issued_x[i] > 0)
-                    mbar_wait_bounded(&bar->x_full[i], (issued_x[i] - 1) & 1, abort_flag, a.err, 3, kWaitNs);
-                if (issued_bc[i] > 0)
-                    mbar_wait_bounded(&bar->bc_full[i], (issued_bc[i] - 1) & 1, abort_flag, a.err, 3, kWaitNs);
-            }
+            for (int i = 0; i < 2; ++i)
+                if (issued[i] > 0)
+                    mbar_wait_bounded(&bar->bc_full[i], (issued[i] - 1) & 1, abort_flag, a.err, 3, kWaitNs);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int it = 0;  // n-block ring position
-            bool ok = true;
             const uint32_t sXs = smem_u32(smem + K::OFF_XS);
             const uint32_t sZero = smem_u32(smem + K::OFF_ZERO);
-            // Y = M X for sub-block q (A = M from TMEM, B = the x tile, MN-major)
-            auto issue_mx = [&](int q) -> bool {
-                const int k = q % K::NBUF;
-                if (!mbar_wait_bounded(&bar->m_ready, q & 1, abort_flag, a.err, 9, kWaitNs)) return false;
-                tc_fence_after();
-                const uint32_t sX = smem_u32(smem + K::OFF_X + (q % K::NX) * kTile);
-                const uint32_t set = tm + K::T_SET + k * K::SET;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(set + 64, set + kk * 8, desc_sw128(sX + kk * 2048, 16, 1024), kIdescMX, kk > 0);
-                mma_commit(&bar->y_full);
-                mma_commit(&bar->x_empty[q % K::NX]);
-                return true;
-            };
+            const uint32_t sH = smem_u32(smem + K::OFF_H);
+            auto stage_c = [&](int st) -> uint32_t { return smem_u32(smem + K::OFF_BC + st * K::SZ_STAGE); };
             // h[nb] += B_nb^T X'  (K = tokens; A MN-major over two 64-row n boxes)
             auto issue_s = [&](int nb, uint32_t sB) {
                 const uint32_t lbo = (K::BOXES == 2) ? (uint32_t)kTile : (sZero - sB);
@@ -267,80 +272,107 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ss(tm + K::T_H + nb * 64, desc_sw128(sB + kk * 2048, lbo, 1024),
                            desc_sw128(sXs + kk * 2048, 16, 1024), kIdescS, 1);
             };
-            // Yst += C_nb h_nb ; CB += C_nb B_nb^T   (K = n, 16 per step)
-            auto issue_ys_cb = [&](int nb, uint32_t set, uint32_t sH, uint32_t sC, uint32_t sB) {
+            // Yst += C_nb h_nb   (K = n, 16 per step)
+            auto issue_ys = [&](int nb, uint32_t set, uint32_t sC) {
 #pragma unroll
                 for (int kk = 0; kk < K::NB / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kTile + (kk & 3) * 32;
-                    const uint64_t ad = desc_sw128(sC + off, 16, 1024);
-                    mma_ss(set + 128, ad, desc_sw128(sH + (nb * K::NB + kk * 16) * 128, 16, 1024), kIdescYS,
-                           (nb | kk) != 0);
-                    mma_ss(set, ad, desc_sw128(sB + off, 16, 1024), kIdescCB, (nb | kk) != 0);
+                    mma_ss(set + 128, desc_sw128(sC + off, 16, 1024),
+                           desc_sw128(sH + (nb * K::NB + kk * 16) * 128, 16, 1024), kIdescYS, (nb | kk) != 0);
                 }
             };
-            for (int sb = 0; sb < nsb && ok; ++sb) {
-                const bool need_S = sb + 1 < nsb;
-                const int k = sb % K::NBUF;
+            // CB += C_nb B_nb^T   (K = n, 16 per step)
+            auto issue_cb = [&](int nb, uint32_t set, uint32_t sC, uint32_t sB) {
+#pragma unroll
+                for (int kk = 0; kk < K::NB / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kTile + (kk & 3) * 32;
+                    mma_ss(set, desc_sw128(sC + off, 16, 1024), desc_sw128(sB + off, 16, 1024), kIdescCB,
+                           (nb | kk) != 0);
+                }
+            };
+            // Y = M X for sub-block q (A = M from TMEM, B = the float16 x tile, MN-major)
+            auto issue_mx = [&](int q) {
+                const int k = q % K::NBUF;
+                const uint32_t sX = smem_u32(smem + K::OFF_X + (q % K::NX) * kTile);
                 const uint32_t set = tm + K::T_SET + k * K::SET;
-                const uint32_t sH = smem_u32(smem + K::OFF_H + (sb % K::NH) * K::SZ_H);
-                ok = mbar_wait_bounded(&bar->xs_ready, sb & 1, abort_flag, a.err, 5, kWaitNs) &&
-                     mbar_wait_bounded(&bar->h_ready, sb & 1, abort_flag, a.err, 6, kWaitNs);
-                if (!ok) break;
-                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(set + 64, set + kk * 8, desc_sw128(sX + kk * 2048, 16, 1024), kIdescMX, kk > 0);
+                mma_commit(&bar->y_full[k]);
+                mma_commit(&bar->x_empty[q % K::NX]);
+            };
+            // front(f): S (state update), then C h, then C B^T; false on a failed wait
+            int it = 0;
+            auto issue_front = [&](int f) -> bool {
+                const bool need_S = f + 1 < nsb;
+                const int k = f % K::NBUF;
+                const uint32_t set = tm + K::T_SET + k * K::SET;
                 if (K::S_FIRST) {
-                    // every n-block of this sub-block is resident: the state (critical path) goes first
-                    for (int nb = 0; nb < K::NBLK && ok; ++nb)
-                        ok = mbar_wait_bounded(&bar->bc_full[(it + nb) % K::NST], ((it + nb) / K::NST) & 1,
-                                               abort_flag, a.err, 8, kWaitNs);
-                    if (!ok) break;
-                    tc_fence_after();
                     if (need_S)
-                        for (int nb = 0; nb < K::NBLK; ++nb)
-                            issue_s(nb, smem_u32(smem + K::OFF_BC + ((it + nb) % K::NST) * K::SZ_STAGE) + K::SZ_C);
+                        for (int nb = 0; nb < K::NBLK; ++nb) issue_s(nb, stage_c((it + nb) % K::NST) + K::SZ_C);
                     mma_commit(&bar->xs_free);
-                    if (K::NH == 2) mma_commit(&bar->state_done);
-                    if (sb >= K::NBUF) {
-                        ok = mbar_wait_bounded(&bar->y_free[k], ((sb / K::NBUF) - 1) & 1, abort_flag, a.err, 7,
-                                               kWaitNs);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
+                    for (int nb = 0; nb < K::NBLK; ++nb) issue_ys(nb, set, stage_c((it + nb) % K::NST));
+                    mma_commit(&bar->state_done);
                     for (int nb = 0; nb < K::NBLK; ++nb, ++it) {
                         const int st = it % K::NST;
-                        const uint32_t sC = smem_u32(smem + K::OFF_BC + st * K::SZ_STAGE);
-                        issue_ys_cb(nb, set, sH, sC, sC + K::SZ_C);
+                        issue_cb(nb, set, stage_c(st), stage_c(st) + K::SZ_C);
                         mma_commit(&bar->bc_empty[st]);
                     }
                 } else {
-                    // n-blocks streamed one stage at a time (single buffer set)
-                    if (sb >= K::NBUF) {
-                        ok = mbar_wait_bounded(&bar->y_free[k], ((sb / K::NBUF) - 1) & 1, abort_flag, a.err, 7,
-                                               kWaitNs);
-                        if (!ok) break;
-                    }
-                    for (int nb = 0; nb < K::NBLK && ok; ++nb, ++it) {
+                    // n-blocks streamed one stage at a time
+                    for (int nb = 0; nb < K::NBLK; ++nb, ++it) {
                         const int st = it % K::NST;
-                        ok = mbar_wait_bounded(&bar->bc_full[st], (it / K::NST) & 1, abort_flag, a.err, 8, kWaitNs);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const uint32_t sC = smem_u32(smem + K::OFF_BC + st * K::SZ_STAGE);
-                        if (need_S) issue_s(nb, sC + K::SZ_C);
-                        issue_ys_cb(nb, set, sH, sC, sC + K::SZ_C);
+                        if (nb > 0) {
+                            if (!mbar_wait_bounded(&bar->bc_full[st], (it / K::NST) & 1, abort_flag, a.err, 8,
+                                                   kWaitNs))
+                                return false;
+                            tc_fence_after();
+                        }
+                        if (need_S) issue_s(nb, stage_c(st) + K::SZ_C);
+                        issue_ys(nb, set, stage_c(st));
+                        issue_cb(nb, set, stage_c(st), stage_c(st) + K::SZ_C);
                         mma_commit(&bar->bc_empty[st]);
                     }
-                    if (!ok) break;
                     mma_commit(&bar->xs_free);
+                    mma_commit(&bar->state_done);
                 }
-                if (K::NH == 1) mma_commit(&bar->state_done);
                 mma_commit(&bar->cb_full[k]);
-                // software pipeline: the previous sub-block's M X goes after this front
-                if (K::NBUF == 2) {
-                    if (sb > 0) ok = issue_mx(sb - 1);
+                return true;
+            };
+            auto front_ready = [&](int f) -> bool {
+                if (!mbar_test_wait(&bar->xs_ready, f & 1) || !mbar_test_wait(&bar->h_ready, f & 1)) return false;
+                const int nres = K::S_FIRST ? K::NBLK : 1;  // stages that must be resident to start
+                for (int nb = 0; nb < nres; ++nb)
+                    if (!mbar_test_wait(&bar->bc_full[(it + nb) % K::NST], ((it + nb) / K::NST) & 1)) return false;
+                if (f >= K::NBUF && !mbar_test_wait(&bar->y_free[f % K::NBUF], ((f / K::NBUF) - 1) & 1))
+                    return false;
+                return true;
+            };
+            int f = 0, m = 0;
+            bool ok = true;
+            uint64_t last = globaltimer_ns();
+            while (m < nsb && ok) {
+                bool did = false;
+                if (m < f && mbar_test_wait(&bar->m_ready[m % K::NBUF], (m / K::NBUF) & 1)) {
+                    tc_fence_after();
+                    issue_mx(m++);
+                    did = true;
+                } else if (f < nsb && f - m < K::NBUF && front_ready(f)) {
+                    tc_fence_after();
+                    ok = issue_front(f++);
+                    did = true;
+                }
+                if (did) {
+                    last = globaltimer_ns();
                 } else {
-                    ok = issue_mx(sb);
+                    if (*abort_flag) break;
+                    if (globaltimer_ns() - last > kWaitNs) {
+                        *abort_flag = 1;
+                        atomicExch(a.err, 4);
+                        break;
+                    }
                 }
             }
-            if (ok && K::NBUF == 2 && nsb > 0) issue_mx(nsb - 1);
             // every MMA retired before TMEM is released
             mma_commit(&bar->final_mma);
             mbar_wait_bounded(&bar->final_mma, 0, abort_flag, a.err, 10, kWaitNs);
@@ -349,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ mask warpgroup: CB -> M
         const int r = threadIdx.x;  // TMEM lane == row
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const float Dh = (a.D != nullptr) ? a.D[h] : 0.f;  // the skip term rides on M's diagonal
         for (int sb = 0; sb < nsb; ++sb) {
             const int k = sb % K::NBUF;
             const int ub = sb % 3;
@@ -372,25 +405,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     uint32_t v[32];
                     tmem_ld32(set + q * 32, v);
-                    tmem_ld_wait();
+                    tmem_ld_wait(v);
                     if (q < warp) {  // strictly below: factorized decay
-                        const float ar = exp2f(fminf(ui - su[q * 32 + 31], 0.f));
+                        const float ar = fast_exp2(fminf(ui - su[q * 32 + 31], 0.f));
 #pragma unroll
                         for (int jj = 0; jj < 32; jj += 2) {
                             const int j = q * 32 + jj;
-                            o[jj >> 1] = pack_f16x2(__uint_as_float(v[jj]) * ar * sbc[j],
-                                                    __uint_as_float(v[jj + 1]) * ar * sbc[j + 1]);
+                            o[jj >> 1] = pack_f16x2(__uint_as_float(v[jj]) * (ar * sbc[j]),
+                                                    __uint_as_float(v[jj + 1]) * (ar * sbc[j + 1]));
                         }
-                    } else {  // diagonal block: exact per-element decay
+                    } else {  // diagonal block: exact per-element decay, D on the diagonal
 #pragma unroll
                         for (int jj = 0; jj < 32; jj += 2) {
                             const int j0 = q * 32 + jj, j1 = j0 + 1;
-                            const float m0 = (j0 <= r && j0 < nv)
-                                                 ? __uint_as_float(v[jj]) * exp2f(fminf(ui - su[j0], 0.f)) * sdt[j0]
-                                                 : 0.f;
-                            const float m1 = (j1 <= r && j1 < nv)
-                                                 ? __uint_as_float(v[jj + 1]) * exp2f(fminf(ui - su[j1], 0.f)) * sdt[j1]
-                                                 : 0.f;
+                            float m0 = (j0 <= r && j0 < nv)
+                                           ? __uint_as_float(v[jj]) * fast_exp2(fminf(ui - su[j0], 0.f)) * sdt[j0]
+                                           : 0.f;
+                            float m1 = (j1 <= r && j1 < nv)
+                                           ? __uint_as_float(v[jj + 1]) * fast_exp2(fminf(ui - su[j1], 0.f)) * sdt[j1]
+                                           : 0.f;
+                            if (j0 == r) m0 += Dh;
+                            if (j1 == r) m1 += Dh;
                             o[jj >> 1] = pack_f16x2(m0, m1);
                         }
                     }
@@ -399,65 +434,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&bar->m_ready);
+            mbar_arrive(&bar->m_ready[k]);
+            mbar_arrive(&bar->u_free[ub]);
         }
     } else if (warp < 8) {
         // ------------------------------------------------------ state warpgroup
-        // Failures never break this loop: named barriers need all 128 threads,
-        // so a failed wait only turns the remaining work into no-ops.
+        // A failed wait turns the remaining work into no-ops but keeps every arrival.
         const int r = threadIdx.x - 128;  // TMEM lane (warp % 4 == warp - 4)
         const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
-        const int64_t row = (int64_t)b * H + h;
-        const float* csr = a.cs + row * d.nchunks * Q;
-        const float* dtr = a.dtt + row * d.nchunks * Q;
         const int64_t PN = (int64_t)d.headdim * N;
         const float* init = a.init + (((int64_t)b * a.nspans + s) * H + h) * PN;
         bool ok = true;
+        float prev_raw = 0.f;  // raw dA_cumsum of the token before this sub-block (same chunk)
         for (int sb = 0; sb < nsb; ++sb) {
             const int64_t t0 = ts + sb * 128;
             const int nv = (int)min((int64_t)128, te - t0);
             const int xb = sb % K::NX;
             const int ub = sb % 3;
             float* su = sU + ub * 384;
-            float* sdt = su + 128;
-            float* sbc = su + 256;
-            // 1. in-sub-block inclusive log2 decay u, dt, and the factorized column weights
-            const int64_t t = t0 + r;
-            const bool valid = r < nv;
-            float u = 0.f, dtv = 0.f;
-            if (valid) {
-                const int64_t c0 = t0 / Q;
-                const int64_t p0 = t0 - c0 * Q;
-                const float prev = (p0 > 0) ? csr[t0 - 1] : 0.f;
-                const int64_t c = t / Q;
-                u = (c == c0) ? (csr[t] - prev) : ((csr[c0 * Q + Q - 1] - prev) + csr[t]);
-                dtv = dtr[t];
-            }
-            if (sb >= 3) {  // the epilogue of sub-block sb-3 (the last reader of this buffer) is done with it
+            // 1. u, dt and the factorized column weights of this sub-block, each computed by its
+            //    own thread from the dA_cumsum/dt rows that arrived with the x tile
+            if (sb >= 3)
                 ok = ok && mbar_wait_bounded(&bar->u_free[ub], ((sb / 3) - 1) & 1, abort_flag, a.err, 17, kWaitNs);
-                ok = __all_sync(0xffffffffu, ok);
+            ok = ok && mbar_wait_bounded(&bar->x_full[xb], (sb / K::NX) & 1, abort_flag, a.err, 13, kWaitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            const float* scs = reinterpret_cast<const float*>(smem + K::OFF_CD + xb * 1024);
+            const int p0 = (int)(t0 % Q);
+            const float prev = (p0 > 0) ? prev_raw : 0.f;
+            const bool valid = r < nv;
+            float u = 0.f, ulast = 0.f, dtv = 0.f, bcol = 0.f;
+            if (ok) {
+                ulast = sub_block_decay(scs, prev, p0, Q, nv - 1);
+                if (valid) {
+                    u = sub_block_decay(scs, prev, p0, Q, r);
+                    dtv = scs[128 + r];
+                    // weight for the factorized mask: 2^(u_end - u_r) dt_r, end = last valid
+                    // position of r's 32-block
+                    const float uend = sub_block_decay(scs, prev, p0, Q, min(r | 31, nv - 1));
+                    bcol = fast_exp2(fminf(uend - u, 0.f)) * dtv;
+                } else {
+                    u = ulast;
+                }
+                prev_raw = scs[nv - 1];
             }
             su[r] = u;
-            sdt[r] = dtv;
-            named_sync(1, 128);
-            const float ulast = su[nv - 1];
-            if (!valid) u = ulast;
-            // column weight of the factorized mask: 2^(u_end - u_j) dt_j, end = last position of j's 32-block
-            // (positions past nv hold ulast, so the block end is clamped to the last valid position)
-            const int bend = min(r | 31, nv - 1);
-            const float uend = su[bend];
-            named_sync(1, 128);  // every thread has read su before padded rows are rewritten
-            if (!valid) su[r] = ulast;
-            sbc[r] = valid ? exp2f(fminf(uend - u, 0.f)) * dtv : 0.f;
+            su[128 + r] = dtv;
+            su[256 + r] = bcol;
             mbar_arrive(&bar->uv_ready[ub]);
             const float dsb = exp2f(ulast);
-            // 2. X' = w X  (row r of the token tile, same swizzle)
-            ok = ok && mbar_wait_bounded(&bar->x_full[xb], (sb / K::NX) & 1, abort_flag, a.err, 13, kWaitNs);
-            ok = ok && (sb == 0 || mbar_wait_bounded(&bar->xs_free, (sb - 1) & 1, abort_flag, a.err, 14, kWaitNs));
+            // 2. x tile -> float16 in place, and X' = w x into the single X' buffer once the
+            //    previous sub-block's state update has read it
+            if (sb > 0) ok = ok && mbar_wait_bounded(&bar->xs_free, (sb - 1) & 1, abort_flag, a.err, 14, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
-                // x row -> float16 in place (exact in range) and w x -> the X' tile (float16)
-                const float w = valid ? exp2f(ulast - u) * dtv : 0.f;
+                const float w = valid ? fast_exp2(fminf(ulast - u, 0.f)) * dtv : 0.f;
                 uint8_t* xrow = smem + K::OFF_X + xb * kTile;
                 uint8_t* xsrow = smem + K::OFF_XS;
 #pragma unroll
@@ -470,9 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t* w4 = reinterpret_cast<uint32_t*>(&wo);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 f = __bfloat1622float2(p2[e]);
-                        x4[e] = pack_f16x2(f.x, f.y);
-                        w4[e] = pack_f16x2(f.x * w, f.y * w);
+                        const float2 fv = __bfloat1622float2(p2[e]);
+                        x4[e] = pack_f16x2(fv.x, fv.y);
+                        w4[e] = pack_f16x2(fv.x * w, fv.y * w);
                     }
                     *reinterpret_cast<uint4*>(xrow + off) = xo;
                     *reinterpret_cast<uint4*>(xsrow + off) = wo;
@@ -487,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
             }
             if (ok) {
-                uint8_t* hbase = smem + K::OFF_H + (sb % K::NH) * K::SZ_H;
+                uint8_t* hbase = smem + K::OFF_H;
 #pragma unroll 1
                 for (int nb = 0; nb < K::NBLK; ++nb) {
                     const int n = nb * K::NB + (r % K::NB);
@@ -499,11 +529,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         uint32_t v[32];
                         tmem_ld32(tm + lane_base + K::T_H + nb * 64, v);
-                        tmem_ld_wait();
+                        tmem_ld_wait(v);
 #pragma unroll
                         for (int p = 0; p < 32; ++p) hv[p] = __uint_as_float(v[p]);
                         tmem_ld32(tm + lane_base + K::T_H + nb * 64 + 32, v);
-                        tmem_ld_wait();
+                        tmem_ld_wait(v);
 #pragma unroll
                         for (int p = 0; p < 32; ++p) hv[32 + p] = __uint_as_float(v[p]);
                     }
@@ -537,64 +567,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ epilogue warpgroup
         const int r = threadIdx.x - 256;  // TMEM lane (warp % 4 == warp - 8)
         const uint32_t lane_base = (uint32_t)((warp - 8) * 32) << 16;
-        const float Dh = (a.D != nullptr) ? a.D[h] : 0.f;
         bool ok = true;
         for (int sb = 0; sb < nsb; ++sb) {
             const int64_t t0 = ts + sb * 128;
             const int nv = (int)min((int64_t)128, te - t0);
-            const int xb = sb % K::NX;
             const int k = sb % K::NBUF;
-            ok = ok && mbar_wait_bounded(&bar->y_full, sb & 1, abort_flag, a.err, 16, kWaitNs);
+            const int ub = sb % 3;
+            ok = ok && mbar_wait_bounded(&bar->y_full[k], (sb / K::NBUF) & 1, abort_flag, a.err, 16, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
-            uint8_t* xrow = smem + K::OFF_X + xb * kTile;
-            const float e = exp2f(sU[(sb % 3) * 384 + r]);
-            mbar_arrive(&bar->u_free[sb % 3]);
+            const float e = fast_exp2(fminf(sU[ub * 384 + r], 0.f));
+            mbar_arrive(&bar->u_free[ub]);
             if (ok) {
                 const uint32_t set = tm + lane_base + K::T_SET + k * K::SET;
-                uint32_t yv[2][32], sv[2][32];
-                tmem_ld32(set + 64, yv[0]);
-                tmem_ld32(set + 96, yv[1]);
-                tmem_ld32(set + 128, sv[0]);
-                tmem_ld32(set + 160, sv[1]);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&bar->y_free[k]);  // this TMEM set may be reused
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint32_t off = sw128_offset(r, ch);
-                    uint4 xv = *reinterpret_cast<const uint4*>(xrow + off);  // float16 since the X' step
-                    const __half2* x2 = reinterpret_cast<const __half2*>(&xv);
-                    uint4 ov;
-                    uint32_t* o4 = reinterpret_cast<uint32_t*>(&ov);
-#pragma unroll
-                    for (int e2 = 0; e2 < 4; ++e2) {
-                        const float2 xf = __half22float2(x2[e2]);
-                        const int c = ch * 8 + e2 * 2;
-                        const float y0 = __uint_as_float(yv[c >> 5][c & 31]) +
-                                         e * __uint_as_float(sv[c >> 5][c & 31]) + Dh * xf.x;
-                        const float y1 = __uint_as_float(yv[c >> 5][(c + 1) & 31]) +
-                                         e * __uint_as_float(sv[c >> 5][(c + 1) & 31]) + Dh * xf.y;
-                        o4[e2] = pack_bf16x2(y0, y1);
+                uint4* yrow = reinterpret_cast<uint4*>(a.y + (((int64_t)b * d.seqlen + t0 + r) * H + h) * 64);
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t yv[32], sv[32];
+                    tmem_ld32(set + 64 + half * 32, yv);
+                    tmem_ld32(set + 128 + half * 32, sv);
+                    tmem_ld_wait(sv);
+                    tmem_ld_wait(yv);
+                    if (half == 1) {
+                        tc_fence_before();
+                        mbar_arrive(&bar->y_free[k]);  // this TMEM set may be reused
                     }
-                    *reinterpret_cast<uint4*>(xrow + off) = ov;  // y overwrites its own x row
+                    if (r < nv) {
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch) {
+                            uint4 ov;
+                            uint32_t* o4 = reinterpret_cast<uint32_t*>(&ov);
+#pragma unroll
+                            for (int e2 = 0; e2 < 4; ++e2) {
+                                const int c = ch * 8 + e2 * 2;
+                                o4[e2] = pack_bf16x2(__uint_as_float(yv[c]) + e * __uint_as_float(sv[c]),
+                                                     __uint_as_float(yv[c + 1]) + e * __uint_as_float(sv[c + 1]));
+                            }
+                            yrow[half * 4 + ch] = ov;
+                        }
+                    }
                 }
             } else {
                 mbar_arrive(&bar->y_free[k]);
             }
-            fence_proxy_async_smem();
-            named_sync(2, 128);
-            if (r == 0) {
-                if (ok) {
-                    tma_store_4d(&tm_y, xrow, 0, h, (int)t0, b);
-                    if (nv > 64) tma_store_4d(&tm_y, xrow + 64 * 128, 0, h, (int)t0 + 64, b);
-                    tma_store_commit();
-                    tma_store_wait_read0();  // the tile is reloaded only after the store has read it
-                }
-                mbar_arrive(&bar->x_empty[xb]);
-            }
         }
-        if (r == 0) tma_store_wait_all0();
     }
 
     tc_fence_before();
@@ -604,32 +620,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int N>
-int launch_scan_n(const __nv_bfloat16* x, const __half* B, const __half* C, __nv_bfloat16* y,
-                  const ScanArgs& a, cudaStream_t s) {
+int launch_scan_n(const __nv_bfloat16* x, const __half* B, const __half* C, const ScanArgs& a, cudaStream_t s) {
     const Dims& d = a.d;
-    CUtensorMap tx, tb, tc, ty;
+    CUtensorMap tx, tb, tc;
     const uint64_t dx[4] = {(uint64_t)d.headdim, (uint64_t)d.nheads, (uint64_t)d.seqlen, (uint64_t)d.batch};
     const uint64_t dbc[4] = {(uint64_t)d.dstate, (uint64_t)d.ngroups, (uint64_t)d.seqlen, (uint64_t)d.batch};
     const uint32_t box_in[4] = {64, 1, 128, 1};
-    const uint32_t box_out[4] = {64, 1, 64, 1};
     if (!make_tmap_16b_4d(&tx, x, dx, box_in) || !make_tmap_16b_4d(&tb, B, dbc, box_in) ||
-        !make_tmap_16b_4d(&tc, C, dbc, box_in) || !make_tmap_16b_4d(&ty, y, dx, box_out))
+        !make_tmap_16b_4d(&tc, C, dbc, box_in))
         return SSD_ERR_CUDA;
     const int smem = Cfg<N>::SMEM;
-    if (cudaFuncSetAttribute(chunk_scan_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
+    if (ensure_smem_limit(reinterpret_cast<const void*>(chunk_scan_tc_kernel<N>), smem) != SSD_OK)
         return SSD_ERR_CUDA;
     dim3 grid(d.nheads, a.nspans, d.batch);
     launch_begin(kKindChunkScan, s);
-    chunk_scan_tc_kernel<N><<<grid, kThreads, smem, s>>>(tx, tb, tc, ty, a);
+    chunk_scan_tc_kernel<N><<<grid, kThreads, smem, s>>>(tx, tb, tc, a);
     return launch_end(kKindChunkScan, s);
 }
 
 }  // namespace
 
-int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C,
-                           const float* dtt, const float* cs, const float* D, const float* span_states,
-                           int span_chunks, const Dims& d, __nv_bfloat16* y, int* err, cudaStream_t s) {
+int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C, const float* dtt,
+                           const float* cs, const float* D, const float* span_states, int span_chunks, const Dims& d,
+                           __nv_bfloat16* y, int* err, cudaStream_t s) {
     ScanArgs a;
     a.d = d;
     a.span_chunks = span_chunks;
@@ -638,12 +651,13 @@ int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half
     a.dtt = dtt;
     a.D = D;
     a.init = span_states;
+    a.y = y;
     a.err = err;
     switch (d.dstate) {
-        case 64: return launch_scan_n<64>(x, B, C, y, a, s);
-        case 128: return launch_scan_n<128>(x, B, C, y, a, s);
-        case 256: return launch_scan_n<256>(x, B, C, y, a, s);
-        case 512: return launch_scan_n<512>(x, B, C, y, a, s);
+        case 64: return launch_scan_n<64>(x, B, C, a, s);
+        case 128: return launch_scan_n<128>(x, B, C, a, s);
+        case 256: return launch_scan_n<256>(x, B, C, a, s);
+        case 512: return launch_scan_n<512>(x, B, C, a, s);
         default: return SSD_ERR_UNSUPPORTED;
     }
 }

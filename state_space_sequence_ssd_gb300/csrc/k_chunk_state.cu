@@ -41,13 +41,16 @@ struct StCfg {
     static constexpr int BOX = TB * 128;               // one 64-column box, TB rows
     static constexpr int NBOX = N / 64;                // boxes of B per stage
     static constexpr int MB = (N + 127) / 128;         // 128-row accumulator blocks
-    static constexpr int NST = (N == 64) ? 4 : (N == 128 ? 3 : 2);
-    static constexpr int SZ_STAGE = BOX + NBOX * BOX;  // X then B
+    static constexpr int NST = 2;
+    // X, B, then the cs and dt rows; stages stay 1024-byte aligned for the 128-byte swizzle
+    static constexpr int SZ_STAGE = (BOX + NBOX * BOX + 2 * TB * 4 + 1023) / 1024 * 1024;
+    static constexpr int OFF_CD = BOX + NBOX * BOX;                 // within a stage
     static constexpr int OFF_ZERO = NST * SZ_STAGE;
     static constexpr int SZ_ZERO = (N == 64) ? BOX : 0;
-    static constexpr int OFF_R = OFF_ZERO + SZ_ZERO;   // R_c suffix sums
+    static constexpr int OFF_R = OFF_ZERO + SZ_ZERO;  // per chunk of the span: R_c + cs[c][Q-1]
     static constexpr int OFF_BAR = OFF_R + kMaxSpanChunks * 4;
     static constexpr int SMEM = OFF_BAR + 256 + 1024;
+    static constexpr int CTAS_PER_SM = (SMEM <= 113 * 1024) ? 2 : 1;
     static constexpr int TCOLS = (MB * 64 < 32) ? 32 : MB * 64;
     static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -64,7 +67,7 @@ struct StateArgs {
 };
 
 template <int N>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, StCfg<N>::CTAS_PER_SM)
     chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
                           StateArgs a) {
     using K = StCfg<N>;
@@ -101,11 +104,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(acc_done, 1);
         abort_sh = 0;
         fence_barrier_init();
-        // R_c: sum of the chunk totals after chunk c inside this span
+        // per chunk c of the span: R_c + cs[c][Q-1], R_c = sum of the chunk totals after c
         float run = 0.f;
         for (int c = nchk - 1; c >= 0; --c) {
-            Rs[c] = run;
-            run += csr[(c_first + c) * Q + Q - 1];
+            const float last = csr[(c_first + c) * Q + Q - 1];
+            Rs[c] = run + last;
+            run += last;
         }
         if (a.span_decay != nullptr) a.span_decay[row * a.nspans + s] = run;
     }
@@ -139,8 +143,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* sX = smem + st * K::SZ_STAGE;
                 uint8_t* sB = sX + K::BOX;
                 const int t0 = (int)(ts + (int64_t)kb * K::TB);
-                mbar_arrive_expect_tx(&full[st], K::SZ_STAGE);
+                // the block's dA_cumsum and dt rows (contiguous per (b, h)), at most TB values each
+                const uint32_t cdb = (uint32_t)min((int64_t)K::TB, (int64_t)d.nchunks * Q - t0) * 4u;
+                float* scd = reinterpret_cast<float*>(sX + K::OFF_CD);
+                mbar_arrive_expect_tx(&full[st], K::BOX + K::NBOX * K::BOX + 2 * cdb);
                 tma_load_4d(sX, &tm_x, &full[st], 0, h, t0, b);
+                bulk_load(scd, csr + t0, cdb, &full[st]);
+                bulk_load(scd + K::TB, dtr + t0, cdb, &full[st]);
 #pragma unroll
                 for (int bx = 0; bx < K::NBOX; ++bx) tma_load_4d(sB + bx * K::BOX, &tm_B, &full[st], bx * 64, g, t0, b);
                 ++issued[st];
@@ -181,12 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = ok && mbar_wait_bounded(&full[st], (kb / K::NST) & 1, abort_flag, a.err, 24, kWaitNs);
             if (ok && r < K::TB) {
                 const int64_t t = ts + (int64_t)kb * K::TB + r;
-                float w = 0.f;
-                if (t < te) {
-                    const int64_t c = t / Q;
-                    w = exp2f(Rs[c - c_first] + csr[c * Q + Q - 1] - csr[t]) * dtr[t];
-                }
                 uint8_t* xrow = smem + st * K::SZ_STAGE;
+                const float* scd = reinterpret_cast<const float*>(xrow + K::OFF_CD);
+                float w = 0.f;
+                if (t < te) w = exp2f(Rs[t / Q - c_first] - scd[r]) * scd[K::TB + r];
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     const uint32_t off = sw128_offset(r, ch);
@@ -218,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int half = 0; half < 2; ++half) {
                     uint32_t v[32];
                     tmem_ld32(tm + lane_base + mb * 64 + half * 32, v);
-                    tmem_ld_wait();
+                    tmem_ld_wait(v);
                     if (n < N) {
 #pragma unroll
                         for (int p = 0; p < 32; ++p) out[(int64_t)(half * 32 + p) * N + n] = __uint_as_float(v[p]);
@@ -242,8 +249,7 @@ int launch_state_n(const __nv_bfloat16* x, const __half* B, const StateArgs& a, 
     const uint64_t db[4] = {(uint64_t)d.dstate, (uint64_t)d.ngroups, (uint64_t)d.seqlen, (uint64_t)d.batch};
     const uint32_t box[4] = {64, 1, (uint32_t)K::TB, 1};
     if (!make_tmap_16b_4d(&tx, x, dx, box) || !make_tmap_16b_4d(&tb, B, db, box)) return SSD_ERR_CUDA;
-    if (cudaFuncSetAttribute(chunk_state_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM) !=
-        cudaSuccess)
+    if (ensure_smem_limit(reinterpret_cast<const void*>(chunk_state_tc_kernel<N>), K::SMEM) != SSD_OK)
         return SSD_ERR_CUDA;
     dim3 grid(d.nheads, a.nspans, d.batch);
     launch_begin(kKindChunkState, s);

@@ -5,78 +5,134 @@
 // (BLOCK_H,) tile of A, cumulative sum of A*dt along the chunk, times log2 e)
 // and section 3 (dA_cumsum and dt re-laid out for contiguous reads).
 //
-// One CTA per (chunk, 32-head tile, batch).  The (Q x 32) dt tile of a chunk
-// is a run of Q rows of 32 contiguous floats, read coalesced into shared
-// memory; each warp then scans 4 heads along the chunk (each lane owns Q/32
-// consecutive positions: serial in-lane prefix + warp-shuffle scan of the
-// lane totals) and writes the (batch, H, nchunks, Q) rows contiguously.
+// One CTA per (chunk, 8-head tile, batch).  The (Q x 8) dt tile is read with
+// one pair of 16-byte loads per token row into shared memory; each warp then
+// scans one head along the chunk (each lane owns Q/32 consecutive positions:
+// serial in-lane prefix + warp-shuffle scan of the lane totals) and writes
+// its (batch, H, nchunks, Q) rows with 16-byte stores.
+//
+// Optionally the same launch also writes the float16 copies of B and C that
+// the tensor-core stages use (k_convert.cu explains why): the B/C elements
+// are split evenly over all CTAs of the grid.
 #include "common.cuh"
 
 namespace ssd {
 namespace {
 
-constexpr int kHeadsPerCta = 32;
+constexpr int kHeads = 8;
 constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t v) {
+    const float lo = __uint_as_float(v << 16);
+    const float hi = __uint_as_float(v & 0xffff0000u);
+    const __half2 h = __floats2half2_rn(fminf(fmaxf(lo, -65504.f), 65504.f), fminf(fmaxf(hi, -65504.f), 65504.f));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
 
 template <int Q>
 __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __restrict__ dt,
                                                                 const float* __restrict__ A, Dims d,
-                                                                float* __restrict__ cs,
-                                                                float* __restrict__ dtt) {
-    __shared__ float tile[Q][kHeadsPerCta + 1];
-    const int c = blockIdx.x, h0 = blockIdx.y * kHeadsPerCta, b = blockIdx.z;
+                                                                float* __restrict__ cs, float* __restrict__ dtt,
+                                                                const uint4* __restrict__ bsrc,
+                                                                const uint4* __restrict__ csrc, uint4* __restrict__ bdst,
+                                                                uint4* __restrict__ cdst, int64_t bc16) {
+    __shared__ float tile[Q][kHeads + 1];
+    const int c = blockIdx.x, h0 = blockIdx.y * kHeads, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // coalesced load: row i (token c*Q+i), column hh (head h0+hh)
-    for (int i = tid >> 5; i < Q; i += kThreads / 32) {
-        const int64_t t = (int64_t)c * Q + i;
-        const int h = h0 + lane;
-        float v = 0.f;
-        if (t < d.seqlen && h < d.nheads) v = __ldg(dt + ((int64_t)b * d.seqlen + t) * d.nheads + h);
-        tile[i][lane] = v;
+    // token row tid: 8 heads h0..h0+7
+    if (tid < Q) {
+        const int64_t t = (int64_t)c * Q + tid;
+        float v[kHeads];
+        if (t < d.seqlen) {
+            const float* src = dt + ((int64_t)b * d.seqlen + t) * d.nheads + h0;
+            if (h0 + kHeads <= d.nheads && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+                const float4 a0 = __ldg(reinterpret_cast<const float4*>(src));
+                const float4 a1 = __ldg(reinterpret_cast<const float4*>(src) + 1);
+                v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+                v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+            } else {
+#pragma unroll
+                for (int k = 0; k < kHeads; ++k) v[k] = (h0 + k < d.nheads) ? __ldg(src + k) : 0.f;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < kHeads; ++k) v[k] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kHeads; ++k) tile[tid][k] = v[k];
+    }
+    // share of the B / C float16 copies (16-byte chunks), independent of the scan
+    if (bc16 > 0) {
+        const int64_t nblk = (int64_t)gridDim.x * gridDim.y * gridDim.z;
+        const int64_t blk = ((int64_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        const int64_t per = (bc16 + nblk - 1) / nblk;
+        const int64_t lo = blk * per, hi = min(bc16, lo + per);
+        for (int64_t i = lo + tid; i < hi; i += kThreads) {
+            uint4 v = __ldg(bsrc + i);
+            v.x = bf16x2_to_f16x2_sat(v.x);
+            v.y = bf16x2_to_f16x2_sat(v.y);
+            v.z = bf16x2_to_f16x2_sat(v.z);
+            v.w = bf16x2_to_f16x2_sat(v.w);
+            bdst[i] = v;
+            uint4 w = __ldg(csrc + i);
+            w.x = bf16x2_to_f16x2_sat(w.x);
+            w.y = bf16x2_to_f16x2_sat(w.y);
+            w.z = bf16x2_to_f16x2_sat(w.z);
+            w.w = bf16x2_to_f16x2_sat(w.w);
+            cdst[i] = w;
+        }
     }
     __syncthreads();
+    const int h = h0 + warp;
+    if (h >= d.nheads) return;
     constexpr int kPer = Q / 32;  // positions per lane
-    for (int hh = warp; hh < kHeadsPerCta; hh += kThreads / 32) {
-        const int h = h0 + hh;
-        if (h >= d.nheads) break;
-        const float a = __ldg(A + h);
-        float v[kPer], run = 0.f;
+    const float a = __ldg(A + h);
+    float v[kPer], run = 0.f;
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            v[k] = tile[lane * kPer + k][hh];
-            run += a * v[k];
-            v[k] = run;  // in-lane inclusive prefix of a*dt
-        }
-        // inclusive warp scan of the lane totals
-        float tot = run;
+    for (int k = 0; k < kPer; ++k) {
+        const float x = tile[lane * kPer + k][warp];
+        run += a * x;
+        v[k] = run;  // in-lane inclusive prefix of a*dt
+    }
+    // inclusive warp scan of the lane totals
+    float tot = run;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float o = __shfl_up_sync(0xffffffffu, tot, off);
-            if (lane >= off) tot += o;
-        }
-        const float excl = tot - run;
-        const int64_t row = (((int64_t)b * d.nheads + h) * d.nchunks + c) * Q + lane * kPer;
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, tot, off);
+        if (lane >= off) tot += o;
+    }
+    const float excl = tot - run;
+    const int64_t row = (((int64_t)b * d.nheads + h) * d.nchunks + c) * Q + lane * kPer;
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            cs[row + k] = (v[k] + excl) * kLog2e;
-            dtt[row + k] = tile[lane * kPer + k][hh];
-        }
+    for (int k = 0; k < kPer; k += 2) {
+        *reinterpret_cast<float2*>(cs + row + k) = make_float2((v[k] + excl) * kLog2e, (v[k + 1] + excl) * kLog2e);
+        *reinterpret_cast<float2*>(dtt + row + k) =
+            make_float2(tile[lane * kPer + k][warp], tile[lane * kPer + k + 1][warp]);
     }
 }
 
 }  // namespace
 
-int launch_chunk_cumsum(const float* dt, const float* A, const Dims& d, float* cs, float* dtt,
-                        cudaStream_t s) {
-    dim3 grid(d.nchunks, ceil_div(d.nheads, kHeadsPerCta), d.batch);
+int launch_chunk_cumsum_bc(const float* dt, const float* A, const Dims& d, float* cs, float* dtt,
+                           const __nv_bfloat16* B, const __nv_bfloat16* C, __half* B16, __half* C16, cudaStream_t s) {
+    dim3 grid(d.nchunks, ceil_div(d.nheads, kHeads), d.batch);
+    const int64_t bc16 = (B != nullptr) ? (int64_t)d.batch * d.seqlen * d.ngroups * d.dstate / 8 : 0;
+    const uint4* bs = reinterpret_cast<const uint4*>(B);
+    const uint4* cs16 = reinterpret_cast<const uint4*>(C);
+    uint4* bd = reinterpret_cast<uint4*>(B16);
+    uint4* cd = reinterpret_cast<uint4*>(C16);
     launch_begin(kKindCumsum, s);
     switch (d.chunk_size) {
-        case 64: chunk_cumsum_kernel<64><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt); break;
-        case 128: chunk_cumsum_kernel<128><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt); break;
-        case 256: chunk_cumsum_kernel<256><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt); break;
+        case 64: chunk_cumsum_kernel<64><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16); break;
+        case 128: chunk_cumsum_kernel<128><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16); break;
+        case 256: chunk_cumsum_kernel<256><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16); break;
         default: return SSD_ERR_UNSUPPORTED;
     }
     return launch_end(kKindCumsum, s);
+}
+
+int launch_chunk_cumsum(const float* dt, const float* A, const Dims& d, float* cs, float* dtt, cudaStream_t s) {
+    return launch_chunk_cumsum_bc(dt, A, d, cs, dtt, nullptr, nullptr, nullptr, nullptr, s);
 }
 
 }  // namespace ssd

@@ -65,6 +65,20 @@ int launch_end(int kind, cudaStream_t s) {
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+int ensure_smem_limit(const void* kernel, int bytes) {
+    static std::mutex mu;
+    static std::vector<std::pair<const void*, int>> done;  // (kernel, device)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SSD_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(mu);
+    for (auto& e : done)
+        if (e.first == kernel && e.second == dev) return SSD_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    done.emplace_back(kernel, dev);
+    return SSD_OK;
+}
+
 }  // namespace ssd
 
 using namespace ssd;
@@ -123,6 +137,41 @@ int* device_error_ptr() {
     return static_cast<int*>(p);
 }
 
+// Stream-ordered workspace from a library-owned pool per device that keeps
+// freed memory cached (release threshold = max), so repeated calls neither
+// map nor unmap device memory.
+cudaMemPool_t workspace_pool() {
+    static std::mutex mu;
+    static cudaMemPool_t pools[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (pools[dev] == nullptr) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        if (cudaMemPoolCreate(&p, &props) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        uint64_t keep = UINT64_MAX;
+        cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+        pools[dev] = p;
+    }
+    return pools[dev];
+}
+
+int workspace_alloc(void** ptr, size_t bytes, cudaStream_t s) {
+    cudaMemPool_t p = workspace_pool();
+    if (p == nullptr || cudaMallocFromPoolAsync(ptr, bytes, p, s) != cudaSuccess) {
+        cudaGetLastError();
+        return SSD_ERR_NO_MEMORY;
+    }
+    return SSD_OK;
+}
+
 // Chunks per span for ssd_forward: about eight waves of 152 CTAs over
 // (batch, head, span), so the span-level intermediates stay small while
 // every SM stays busy.
@@ -159,7 +208,7 @@ int ssd_chunk_cumsum(const float* dt, const float* A, int batch, int seqlen, int
         return SSD_ERR_INVALID_ARG;
     if (!supported_chunk(chunk_size)) return SSD_ERR_UNSUPPORTED;
     const int64_t nchunks = ((int64_t)seqlen + chunk_size - 1) / chunk_size;
-    if (nchunks > 2147483647LL || batch > 65535 || nheads > 65535 * 32) return SSD_ERR_UNSUPPORTED;
+    if (nchunks > 2147483647LL || batch > 65535 || nheads > 65535 * 8) return SSD_ERR_UNSUPPORTED;
     Dims d = make_dims(batch, seqlen, nheads, 64, 1, 64, chunk_size);
     return launch_chunk_cumsum(dt, A, d, dA_cumsum, dt_t, stream);
 }
@@ -178,10 +227,7 @@ int ssd_chunk_state(const void* x, const void* B, const float* dt_t, const float
     // stream-ordered float16 copy of B for the tensor-core products
     const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, nbc * sizeof(__half), stream) != cudaSuccess) {
-        cudaGetLastError();
-        return SSD_ERR_NO_MEMORY;
-    }
+    if (workspace_alloc(&ws, nbc * sizeof(__half), stream) != SSD_OK) return SSD_ERR_NO_MEMORY;
     __half* B16 = static_cast<__half*>(ws);
     r = launch_bc_to_f16(static_cast<const __nv_bfloat16*>(B), nullptr, d, B16, nullptr, stream);
     if (r == SSD_OK)
@@ -222,10 +268,7 @@ int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_
     // stream-ordered float16 copies of B and C for the tensor-core products
     const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, 2 * nbc * sizeof(__half), stream) != cudaSuccess) {
-        cudaGetLastError();
-        return SSD_ERR_NO_MEMORY;
-    }
+    if (workspace_alloc(&ws, 2 * nbc * sizeof(__half), stream) != SSD_OK) return SSD_ERR_NO_MEMORY;
     __half* B16 = static_cast<__half*>(ws);
     __half* C16 = B16 + nbc;
     r = launch_bc_to_f16(static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), d, B16, C16,
@@ -258,10 +301,7 @@ int ssd_forward(const void* x, const float* dt, const float* A, const void* B, c
     const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;  // multiple of 64
     const size_t bytes = (2 * ncq + nst + ndec) * sizeof(float) + 2 * nbc * sizeof(__half);
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
-        cudaGetLastError();
-        return SSD_ERR_NO_MEMORY;
-    }
+    if (workspace_alloc(&ws, bytes, stream) != SSD_OK) return SSD_ERR_NO_MEMORY;
     float* cs = static_cast<float*>(ws);
     float* dtt = cs + ncq;
     float* S = dtt + ncq;
@@ -269,10 +309,8 @@ int ssd_forward(const void* x, const float* dt, const float* A, const void* B, c
     __half* B16 = reinterpret_cast<__half*>(dec + ndec);
     __half* C16 = B16 + nbc;
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-    r = launch_chunk_cumsum(dt, A, d, cs, dtt, stream);
-    if (r == SSD_OK)
-        r = launch_bc_to_f16(static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), d, B16, C16,
-                             stream);
+    r = launch_chunk_cumsum_bc(dt, A, d, cs, dtt, static_cast<const __nv_bfloat16*>(B),
+                               static_cast<const __nv_bfloat16*>(C), B16, C16, stream);
     if (r == SSD_OK) r = launch_chunk_state_span(xb, B16, dtt, cs, span, d, S, dec, err, stream);
     // span-level hop, in place: S becomes the span-start states
     if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
