@@ -104,14 +104,24 @@ __global__ void __launch_bounds__(kThreads, StCfg<N>::CTAS_PER_SM)
         mbar_init(acc_done, 1);
         abort_sh = 0;
         fence_barrier_init();
-        // per chunk c of the span: R_c + cs[c][Q-1], R_c = sum of the chunk totals after c
-        float run = 0.f;
-        for (int c = nchk - 1; c >= 0; --c) {
-            const float last = csr[(c_first + c) * Q + Q - 1];
-            Rs[c] = run + last;
-            run += last;
+    }
+    if (warp == 0) {
+        // per chunk c of the span: R_c + cs[c][Q-1] = sum of the chunk totals from c to the span
+        // end (an inclusive suffix sum), 32 chunks per round with one load per lane
+        float carry = 0.f;
+        for (int base = nchk - 32; base > -32; base -= 32) {
+            const int c = base + lane;
+            float v = (c >= 0) ? csr[(c_first + c) * Q + Q - 1] : 0.f;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {  // suffix scan: add the lanes above
+                const float o = __shfl_down_sync(0xffffffffu, v, off);
+                if (lane + off < 32) v += o;
+            }
+            v += carry;
+            if (c >= 0) Rs[c] = v;
+            carry = __shfl_sync(0xffffffffu, v, 0);
         }
-        if (a.span_decay != nullptr) a.span_decay[row * a.nspans + s] = run;
+        if (lane == 0 && a.span_decay != nullptr) a.span_decay[row * a.nspans + s] = carry;
     }
     if (K::SZ_ZERO > 0) {
         uint4* z = reinterpret_cast<uint4*>(smem + K::OFF_ZERO);
