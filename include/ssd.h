@@ -59,7 +59,8 @@
  *    in float16's range.
  *  * No C++ exception crosses this boundary.  The library keeps no state
  *    between calls other than the optional profiling counters below; calls
- *    on different streams may run concurrently.
+ *    on different streams may run concurrently, except ssd_forward_noalloc,
+ *    whose calls on one device share one scratch array (see there).
  */
 #ifndef SSD_GB300_H
 #define SSD_GB300_H
@@ -82,8 +83,12 @@ typedef enum {
     SSD_ERR_UNSUPPORTED = 2, /* well-formed shape outside the implemented set */
     SSD_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
     SSD_ERR_NO_MEMORY = 4,   /* workspace allocation failed (ssd_forward) */
-    SSD_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (see ssd_get_device_error) */
+    SSD_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (see ssd_get_device_error) */
+    SSD_ERR_SCRATCH_TOO_SMALL = 6 /* ssd_forward_noalloc: workload larger than its fixed scratch */
 } ssd_status;
+
+/* Size in bytes of the fixed device scratch array used by ssd_forward_noalloc. */
+#define SSD_NOALLOC_SCRATCH_BYTES (64u << 20)
 
 /* Static, never-NULL description of a status code. */
 SSD_API const char* ssd_status_string(int status);
@@ -157,6 +162,46 @@ SSD_API int ssd_forward(const void* x, const float* dt, const float* A, const vo
                 const float* D, const float* init_state, int batch, int seqlen, int nheads,
                 int headdim, int ngroups, int dstate, int chunk_size, void* y,
                 float* final_state, cudaStream_t stream);
+
+/*
+ * ssd_forward_noalloc -- ssd_forward with no memory allocation of any kind.
+ * The pages describe no such variant; it exists for callers that must not
+ * have the library allocate device memory during a call: code that has
+ * already reserved the device's memory for its own allocator (so a pool of
+ * the library's could not grow, or would compete with it), code that
+ * accounts for every byte it places on the device, and latency-critical
+ * loops where a pool that has to grow would stall the call.
+ *
+ * Arguments, layouts, ownership, results and errors are those of
+ * ssd_forward.  Instead of a pool, the workspace lives in one fixed array of
+ * SSD_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library's device image on
+ * each device, so the library's footprint includes that array whether or not
+ * this function is called.  The workspace of a call is about
+ *     8 * batch * nheads * nchunks * chunk_size      (cumulative sums, dt)
+ *   + 4 * batch * nspans * nheads * headdim * dstate (span states)
+ *   + 4 * batch * seqlen * ngroups * dstate          (float16 B and C)
+ * bytes, each part rounded up to 256 bytes, where nspans is the number of
+ * chunk groups the library forms (about 1216 (batch, head, group) units);
+ * a call that would need more returns SSD_ERR_SCRATCH_TOO_SMALL and launches
+ * nothing -- use ssd_forward for such sizes.  For example batch 2,
+ * seqlen 4096, nheads 64, dstate 128, chunk 256 needs 40 MiB and fits;
+ * seqlen 65536, nheads 32, dstate 128 needs 85 MiB and does not.
+ *
+ * The first call on each device performs a one-time set-up with that device
+ * current: it looks up the device address of the scratch array (and, like
+ * every entry point, sets each kernel's shared-memory limit on first use).
+ * Make that first call outside any stream capture.
+ *
+ * All calls on one device share the one scratch array.  Calls issued on the
+ * same stream are ordered and safe; calls that may overlap on the device
+ * (different streams, or host threads on different streams) race on the
+ * scratch and give wrong results.  Nothing in the scratch needs to start at
+ * zero: every call writes each part before reading it.
+ */
+SSD_API int ssd_forward_noalloc(const void* x, const float* dt, const float* A, const void* B,
+                        const void* C, const float* D, const float* init_state, int batch,
+                        int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                        int chunk_size, void* y, float* final_state, cudaStream_t stream);
 
 /*
  * ssd_get_device_error -- reads and clears the library's device error word

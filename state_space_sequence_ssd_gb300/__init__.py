@@ -18,6 +18,7 @@ from __future__ import annotations
 from . import _ffi
 
 __all__ = ["ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_forward",
+           "ssd_forward_noalloc",
            "ssd_get_device_error", "SSDError", "library_path"]
 
 SSDError = _ffi.SSDError
@@ -156,6 +157,30 @@ def ssd_forward(x, dt, A, B, C, D, init_state, chunk_size, y=None, final_state=N
     _need(y, "y", torch.bfloat16, 4)
     _opt(final_state, "final_state", torch.float32, 4)
     _ffi.check("ssd_forward", _ffi.lib().ssd_forward(
+        _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
+        b, L, H, P, G, N, chunk_size, _ptr(y), _ptr(final_state), _stream(stream)))
+    return y, final_state
+
+
+def ssd_forward_noalloc(x, dt, A, B, C, D, init_state, chunk_size, y, final_state=None, stream=None):
+    """ssd_forward with no allocation: the library works in its fixed device
+    scratch array, and the caller supplies y (and final_state, or None to skip
+    it), so this call allocates nothing either.  Calls on one device share the
+    scratch: overlapping calls on different streams race.  Raises SSDError
+    with SSD_ERR_SCRATCH_TOO_SMALL when the workload does not fit."""
+    torch = _torch()
+    _need(x, "x", torch.bfloat16, 4)
+    _need(dt, "dt", torch.float32, 3)
+    _need(A, "A", torch.float32, 1)
+    _need(B, "B", torch.bfloat16, 4)
+    _need(C, "C", torch.bfloat16, 4)
+    _opt(D, "D", torch.float32, 1)
+    _opt(init_state, "init_state", torch.float32, 4)
+    _need(y, "y", torch.bfloat16, 4)
+    _opt(final_state, "final_state", torch.float32, 4)
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    _ffi.check("ssd_forward_noalloc", _ffi.lib().ssd_forward_noalloc(
         _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
         b, L, H, P, G, N, chunk_size, _ptr(y), _ptr(final_state), _stream(stream)))
     return y, final_state

@@ -18,6 +18,8 @@ SSD_ERR_UNSUPPORTED = 2
 SSD_ERR_CUDA = 3
 SSD_ERR_NO_MEMORY = 4
 SSD_ERR_TIMEOUT = 5
+SSD_ERR_SCRATCH_TOO_SMALL = 6
+SSD_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 # name -> (restype, argtypes); the exported surface of include/ssd.h
 _p, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
@@ -28,6 +30,7 @@ SIGNATURES = {
     "ssd_state_passing": (_i, [_p, _p, _p] + [_i] * 6 + [_p, _p, _p]),
     "ssd_chunk_scan": (_i, [_p] * 7 + [_i] * 7 + [_p, _p]),
     "ssd_forward": (_i, [_p] * 7 + [_i] * 7 + [_p, _p, _p]),
+    "ssd_forward_noalloc": (_i, [_p] * 7 + [_i] * 7 + [_p, _p, _p]),
     "ssd_get_device_error": (_i, []),
     "ssd_profile_enable": (_i, [_i]),
     "ssd_profile_reset": (_i, []),

@@ -186,6 +186,38 @@ int forward_span_chunks(const Dims& d) {
 
 }  // namespace
 
+// ---------------------------------------------------------------- fixed scratch
+// Scratch for ssd_forward_noalloc: a fixed array in the library's own device
+// image, so that call needs no allocation at all.  Every call on a device uses
+// the same bytes.  Nothing in it has to start at zero: each region is fully
+// written by an earlier kernel of the same call before any kernel reads it.
+static __device__ __align__(256) unsigned char g_ssd_noalloc_scratch[SSD_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of the fixed scratch on the current device, looked up once
+// per device (with that device current) and cached.
+unsigned char* noalloc_scratch_ptr() {
+    static std::mutex mu;
+    static unsigned char* cache[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev] == nullptr) {
+        unsigned char* p = nullptr;
+        if (cudaGetSymbolAddress((void**)&p, g_ssd_noalloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        cache[dev] = p;
+    }
+    return cache[dev];
+}
+
+size_t round256(size_t bytes) { return (bytes + 255) & ~(size_t)255; }
+
+}  // namespace
+
 extern "C" {
 
 const char* ssd_status_string(int status) {
@@ -196,6 +228,9 @@ const char* ssd_status_string(int status) {
         case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA call or kernel launch failed";
         case SSD_ERR_NO_MEMORY: return "SSD_ERR_NO_MEMORY: workspace allocation failed";
         case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT: a bounded device-side wait gave up";
+        case SSD_ERR_SCRATCH_TOO_SMALL:
+            return "SSD_ERR_SCRATCH_TOO_SMALL: the workload needs more than the fixed scratch of ssd_forward_noalloc "
+                   "(SSD_NOALLOC_SCRATCH_BYTES); use ssd_forward";
         default: return "unknown ssd status";
     }
 }
@@ -317,6 +352,50 @@ int ssd_forward(const void* x, const float* dt, const float* A, const void* B, c
     if (r == SSD_OK)
         r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
+    return r;
+}
+
+int ssd_forward_noalloc(const void* x, const float* dt, const float* A, const void* B, const void* C,
+                        const float* D, const float* init_state, int batch, int seqlen, int nheads, int headdim,
+                        int ngroups, int dstate, int chunk_size, void* y, float* final_state, cudaStream_t stream) {
+    if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    int r = check_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    if (r != SSD_OK) return r;
+    if (!aligned16(x) || !aligned16(B) || !aligned16(C) || !aligned16(y) || ((uintptr_t)dt & 3u) ||
+        ((uintptr_t)A & 3u) || (D && ((uintptr_t)D & 3u)) || (init_state && !aligned16(init_state)) ||
+        (final_state && !aligned16(final_state)))
+        return SSD_ERR_INVALID_ARG;
+    Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    const int span = forward_span_chunks(d);
+    const int nspans = ceil_div(d.nchunks, span);
+    const size_t ncq = (size_t)d.batch * d.nheads * d.nchunks * d.chunk_size;
+    const size_t nst = (size_t)d.batch * nspans * d.nheads * d.headdim * d.dstate;
+    const size_t ndec = (size_t)d.batch * d.nheads * nspans;
+    const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;
+    // the same regions as ssd_forward, each starting on a 256-byte boundary
+    const size_t off_dtt = round256(ncq * sizeof(float));
+    const size_t off_S = off_dtt + round256(ncq * sizeof(float));
+    const size_t off_dec = off_S + round256(nst * sizeof(float));
+    const size_t off_B16 = off_dec + round256(ndec * sizeof(float));
+    const size_t off_C16 = off_B16 + round256(nbc * sizeof(__half));
+    const size_t need = off_C16 + round256(nbc * sizeof(__half));
+    if (need > (size_t)SSD_NOALLOC_SCRATCH_BYTES) return SSD_ERR_SCRATCH_TOO_SMALL;
+    int* err = device_error_ptr();
+    unsigned char* ws = noalloc_scratch_ptr();
+    if (err == nullptr || ws == nullptr) return SSD_ERR_CUDA;
+    float* cs = reinterpret_cast<float*>(ws);
+    float* dtt = reinterpret_cast<float*>(ws + off_dtt);
+    float* S = reinterpret_cast<float*>(ws + off_S);
+    float* dec = reinterpret_cast<float*>(ws + off_dec);
+    __half* B16 = reinterpret_cast<__half*>(ws + off_B16);
+    __half* C16 = reinterpret_cast<__half*>(ws + off_C16);
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    r = launch_chunk_cumsum_bc(dt, A, d, cs, dtt, static_cast<const __nv_bfloat16*>(B),
+                               static_cast<const __nv_bfloat16*>(C), B16, C16, stream);
+    if (r == SSD_OK) r = launch_chunk_state_span(xb, B16, dtt, cs, span, d, S, dec, err, stream);
+    if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
+    if (r == SSD_OK)
+        r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream);
     return r;
 }
 

@@ -102,3 +102,22 @@ def test_binding_requires_cuda_tensors():
     with pytest.raises(ValueError, match="CUDA"):
         ssd.ssd_forward(x, torch.zeros((1, 64, 4)), torch.zeros(4), torch.zeros((1, 64, 1, 64), dtype=torch.bfloat16),
                         torch.zeros((1, 64, 1, 64), dtype=torch.bfloat16), None, None, 64)
+
+
+def fwd_noalloc(lib, **kw):
+    a = dict(x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, D=FAKE, init=FAKE, batch=1, seqlen=512, nheads=4,
+             headdim=64, ngroups=1, dstate=64, chunk_size=64, y=FAKE, final=FAKE)
+    a.update(kw)
+    return lib.ssd_forward_noalloc(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["init"], a["batch"],
+                                   a["seqlen"], a["nheads"], a["headdim"], a["ngroups"], a["dstate"],
+                                   a["chunk_size"], a["y"], a["final"], None)
+
+
+def test_noalloc_validates_before_the_device(lib):
+    """Bad arguments and workloads larger than the fixed scratch are refused
+    before any CUDA call (the fake pointers are never touched)."""
+    assert fwd_noalloc(lib, x=None) == _ffi.SSD_ERR_INVALID_ARG
+    assert fwd_noalloc(lib, y=FAKE + 8) == _ffi.SSD_ERR_INVALID_ARG
+    assert fwd_noalloc(lib, dstate=96) == _ffi.SSD_ERR_UNSUPPORTED
+    assert fwd_noalloc(lib, seqlen=65536, nheads=32, dstate=128, chunk_size=256) == _ffi.SSD_ERR_SCRATCH_TOO_SMALL
+    assert b"SCRATCH_TOO_SMALL" in lib.ssd_status_string(_ffi.SSD_ERR_SCRATCH_TOO_SMALL)
