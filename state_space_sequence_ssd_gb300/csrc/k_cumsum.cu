@@ -36,7 +36,9 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
                                                                 const uint4* __restrict__ bsrc,
                                                                 const uint4* __restrict__ csrc, uint4* __restrict__ bdst,
                                                                 uint4* __restrict__ cdst, int64_t bc16) {
-    __shared__ float tile[Q][kHeads + 1];
+    // tile[h][i + i / 8]: one padding word per 8 positions, so that lanes reading runs of
+    // consecutive positions spread over the banks
+    __shared__ float tile[kHeads][Q + Q / 8];
     const int c = blockIdx.x, h0 = blockIdx.y * kHeads, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // token row tid: 8 heads h0..h0+7
@@ -59,7 +61,7 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
             for (int k = 0; k < kHeads; ++k) v[k] = 0.f;
         }
 #pragma unroll
-        for (int k = 0; k < kHeads; ++k) tile[tid][k] = v[k];
+        for (int k = 0; k < kHeads; ++k) tile[k][tid + tid / 8] = v[k];
     }
     // share of the B / C float16 copies (16-byte chunks), independent of the scan
     if (bc16 > 0) {
@@ -67,19 +69,28 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
         const int64_t blk = ((int64_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
         const int64_t per = (bc16 + nblk - 1) / nblk;
         const int64_t lo = blk * per, hi = min(bc16, lo + per);
-        for (int64_t i = lo + tid; i < hi; i += kThreads) {
-            uint4 v = __ldg(bsrc + i);
-            v.x = bf16x2_to_f16x2_sat(v.x);
-            v.y = bf16x2_to_f16x2_sat(v.y);
-            v.z = bf16x2_to_f16x2_sat(v.z);
-            v.w = bf16x2_to_f16x2_sat(v.w);
-            bdst[i] = v;
-            uint4 w = __ldg(csrc + i);
-            w.x = bf16x2_to_f16x2_sat(w.x);
-            w.y = bf16x2_to_f16x2_sat(w.y);
-            w.z = bf16x2_to_f16x2_sat(w.z);
-            w.w = bf16x2_to_f16x2_sat(w.w);
-            cdst[i] = w;
+        int64_t i = lo + tid;
+        for (; i + 3 * kThreads < hi; i += 4 * kThreads) {  // four chunks of B and C in flight
+            uint4 vb[4], vc[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                vb[u] = __ldg(bsrc + i + u * kThreads);
+                vc[u] = __ldg(csrc + i + u * kThreads);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                bdst[i + u * kThreads] = make_uint4(bf16x2_to_f16x2_sat(vb[u].x), bf16x2_to_f16x2_sat(vb[u].y),
+                                                    bf16x2_to_f16x2_sat(vb[u].z), bf16x2_to_f16x2_sat(vb[u].w));
+                cdst[i + u * kThreads] = make_uint4(bf16x2_to_f16x2_sat(vc[u].x), bf16x2_to_f16x2_sat(vc[u].y),
+                                                    bf16x2_to_f16x2_sat(vc[u].z), bf16x2_to_f16x2_sat(vc[u].w));
+            }
+        }
+        for (; i < hi; i += kThreads) {
+            const uint4 vb = __ldg(bsrc + i), vc = __ldg(csrc + i);
+            bdst[i] = make_uint4(bf16x2_to_f16x2_sat(vb.x), bf16x2_to_f16x2_sat(vb.y), bf16x2_to_f16x2_sat(vb.z),
+                                 bf16x2_to_f16x2_sat(vb.w));
+            cdst[i] = make_uint4(bf16x2_to_f16x2_sat(vc.x), bf16x2_to_f16x2_sat(vc.y), bf16x2_to_f16x2_sat(vc.z),
+                                 bf16x2_to_f16x2_sat(vc.w));
         }
     }
     __syncthreads();
@@ -90,7 +101,8 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
     float v[kPer], run = 0.f;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-        const float x = tile[lane * kPer + k][warp];
+        const int pos = lane * kPer + k;
+        const float x = tile[warp][pos + (pos >> 3)];
         run += a * x;
         v[k] = run;  // in-lane inclusive prefix of a*dt
     }
@@ -105,9 +117,9 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
     const int64_t row = (((int64_t)b * d.nheads + h) * d.nchunks + c) * Q + lane * kPer;
 #pragma unroll
     for (int k = 0; k < kPer; k += 2) {
+        const int p0 = lane * kPer + k, p1 = p0 + 1;
         *reinterpret_cast<float2*>(cs + row + k) = make_float2((v[k] + excl) * kLog2e, (v[k + 1] + excl) * kLog2e);
-        *reinterpret_cast<float2*>(dtt + row + k) =
-            make_float2(tile[lane * kPer + k][warp], tile[lane * kPer + k + 1][warp]);
+        *reinterpret_cast<float2*>(dtt + row + k) = make_float2(tile[warp][p0 + (p0 >> 3)], tile[warp][p1 + (p1 >> 3)]);
     }
 }
 

@@ -12,9 +12,10 @@
 //
 // Every (b, h, p, n) entry is an independent lane of a serial fp32 recurrence.
 // Each thread owns 4 consecutive entries (one float4); the loop over chunks
-// loads kUnroll chunk states ahead of the dependent FMAs so the memory
-// system always has independent requests in flight (the loads of S do not
-// depend on the carried state).  `states` may alias `S`: every element is
+// keeps two groups of kUnroll chunk-state loads in flight -- the next group
+// is requested before the current one is folded -- so the memory system
+// always has independent requests outstanding (the loads of S do not depend
+// on the carried state).  `states` may alias `S`: every element is
 // read before the same element is written.
 #include "common.cuh"
 
@@ -39,24 +40,39 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
     const float* csl = dec + ((int64_t)b * d.nheads + h) * dec_row;
     const int64_t cstride = (int64_t)d.nheads * PN;  // distance between consecutive chunks
     const int64_t base = ((int64_t)b * nc * d.nheads + h) * PN + e;
+    // software pipeline: the next group of kUnroll steps is loaded before the current one is folded
+    float4 sv[kUnroll], nv[kUnroll];
+    float dk[kUnroll], nd[kUnroll];
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+        if (k < nc) {
+            nv[k] = *reinterpret_cast<const float4*>(S + base + (int64_t)k * cstride);
+            nd[k] = __ldg(csl + (int64_t)k * dec_step);
+        }
+    }
     for (int c0 = 0; c0 < nc; c0 += kUnroll) {
-        float4 sv[kUnroll];
-        float dk[kUnroll];
 #pragma unroll
         for (int k = 0; k < kUnroll; ++k) {
-            if (c0 + k < nc) {
-                sv[k] = *reinterpret_cast<const float4*>(S + base + (int64_t)(c0 + k) * cstride);
-                dk[k] = exp2f(__ldg(csl + (int64_t)(c0 + k) * dec_step));
+            sv[k] = nv[k];
+            dk[k] = nd[k];
+        }
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const int cn = c0 + kUnroll + k;
+            if (cn < nc) {
+                nv[k] = *reinterpret_cast<const float4*>(S + base + (int64_t)cn * cstride);
+                nd[k] = __ldg(csl + (int64_t)cn * dec_step);
             }
         }
 #pragma unroll
         for (int k = 0; k < kUnroll; ++k) {
             if (c0 + k < nc) {
+                const float dd = exp2f(dk[k]);
                 *reinterpret_cast<float4*>(states + base + (int64_t)(c0 + k) * cstride) = hv;
-                hv.x = fmaf(dk[k], hv.x, sv[k].x);
-                hv.y = fmaf(dk[k], hv.y, sv[k].y);
-                hv.z = fmaf(dk[k], hv.z, sv[k].z);
-                hv.w = fmaf(dk[k], hv.w, sv[k].w);
+                hv.x = fmaf(dd, hv.x, sv[k].x);
+                hv.y = fmaf(dd, hv.y, sv[k].y);
+                hv.z = fmaf(dd, hv.z, sv[k].z);
+                hv.w = fmaf(dd, hv.w, sv[k].w);
             }
         }
     }

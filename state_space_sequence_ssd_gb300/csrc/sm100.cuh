@@ -69,13 +69,10 @@ __device__ __forceinline__ uint32_t mbar_test_wait(uint64_t* bar, uint32_t parit
     return ok;
 }
 
-// Bounded wait on phase `parity` of `bar`.  Gives up after `limit_ns` of
-// global time, or as soon as *abort becomes non-zero (another role already
-// gave up).  On giving up it sets *abort and records `code` in *err, and
-// returns false; the caller then skips its remaining work.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                  int* err, int code, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait_bounded, kept out of line so that the many wait
+// sites of a kernel share one copy of the loop.
+static __device__ __noinline__ bool mbar_wait_bounded_slow(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
+                                                    int code, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
 #pragma unroll 1
@@ -88,6 +85,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
             return false;
         }
     }
+}
+
+// Bounded wait on phase `parity` of `bar`.  Gives up after `limit_ns` of
+// global time, or as soon as *abort becomes non-zero (another role already
+// gave up).  On giving up it sets *abort and records `code` in *err, and
+// returns false; the caller then skips its remaining work.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  int* err, int code, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_bounded_slow(bar, parity, abort, err, code, limit_ns);
 }
 
 // ------------------------------------------------------------------ TMA
@@ -263,6 +270,15 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
                    "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
                    "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
                    "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15])
                  :
                  : "memory");
 }
