@@ -15,10 +15,15 @@
 // every term <= 0, so no intermediate overflows.  The span's total exponent
 // sum_c cs[c][Q-1] is also written (log2 decay of the whole span).
 //
-// One CTA per (head, span, batch); 192 threads: warps 0-3 scale X rows in
-// shared memory (one token per thread) and store the result; warp 4 issues
-// TMA loads; warp 5 owns TMEM and issues the MMAs
-//   acc[mb] (128 n x 64 p, f32 in TMEM) += B_tile^T (MN-major) * X'_tile (MN-major).
+// One CTA per (HH heads of one B group, span, batch): the heads share the B
+// tile and one MMA per k-step, whose N = 64 HH columns hold the HH heads'
+// states side by side:
+//   acc[mb] (128 n x 64 HH, f32 in TMEM) += B_tile^T (MN-major) * [X'_0 .. X'_HH-1] (MN-major).
+// HH = 4 for N <= 128 and 2 for N >= 256 when the heads per group allow it
+// (fewer and wider MMAs, one B load per HH heads).  Roles: one or two
+// warpgroups scale the X rows in shared memory (one token row per thread)
+// and store the result; one warp issues the TMA loads; one warp owns TMEM
+// and issues the MMAs.
 // Operands are float16: B is the exact float16 copy of the input, and the
 // scaled rows w x (bfloat16 x times an f32 weight) are rounded once to
 // float16, whose 11 significant bits keep the state within tolerance.
@@ -32,26 +37,32 @@ namespace {
 using namespace sm100;
 
 constexpr uint64_t kWaitNs = 1000000000ull;
-constexpr int kThreads = 192;
 constexpr int kMaxSpanChunks = 256;
 
-template <int N>
+// HH heads of one B group per CTA: they share the B tile, and one MMA per
+// k-step covers all of them (N = 64 HH).  2 scaling warpgroups when HH > 1.
+template <int N, int HH>
 struct StCfg {
     static constexpr int TB = (N == 512) ? 64 : 128;   // tokens per stage
     static constexpr int BOX = TB * 128;               // one 64-column box, TB rows
     static constexpr int NBOX = N / 64;                // boxes of B per stage
     static constexpr int MB = (N + 127) / 128;         // 128-row accumulator blocks
     static constexpr int NST = 2;
-    // X, B, then the cs and dt rows; stages stay 1024-byte aligned for the 128-byte swizzle
-    static constexpr int SZ_STAGE = (BOX + NBOX * BOX + 2 * TB * 4 + 1023) / 1024 * 1024;
-    static constexpr int OFF_CD = BOX + NBOX * BOX;                 // within a stage
+    static constexpr int SW = (HH > 1) ? 2 : 1;        // scaling warpgroups
+    static constexpr int THREADS = 128 * SW + 64;      // + TMA warp + MMA warp
+    static constexpr int WARP_TMA = 4 * SW, WARP_MMA = 4 * SW + 1;
+    // per stage: HH x tiles, the B boxes, then HH x {cs[TB], dt[TB]}; 1024-byte aligned stages
+    static constexpr int OFF_B = HH * BOX;
+    static constexpr int OFF_CD = OFF_B + NBOX * BOX;
+    static constexpr int SZ_STAGE = (OFF_CD + HH * 2 * TB * 4 + 1023) / 1024 * 1024;
     static constexpr int OFF_ZERO = NST * SZ_STAGE;
-    static constexpr int SZ_ZERO = (N == 64) ? BOX : 0;
-    static constexpr int OFF_R = OFF_ZERO + SZ_ZERO;  // per chunk of the span: R_c + cs[c][Q-1]
-    static constexpr int OFF_BAR = OFF_R + kMaxSpanChunks * 4;
+    static constexpr int SZ_ZERO = (N == 64) ? BOX : 0;  // zero rows padding the A operand to 128
+    static constexpr int OFF_R = OFF_ZERO + SZ_ZERO;     // HH x per chunk of the span: R_c + cs[c][Q-1]
+    static constexpr int OFF_BAR = OFF_R + HH * kMaxSpanChunks * 4;
     static constexpr int SMEM = OFF_BAR + 256 + 1024;
     static constexpr int CTAS_PER_SM = (SMEM <= 113 * 1024) ? 2 : 1;
-    static constexpr int TCOLS = (MB * 64 < 32) ? 32 : MB * 64;
+    static constexpr int TCOLS = MB * HH * 64 <= 32 ? 32 : (MB * HH * 64 <= 64 ? 64 : (MB * HH * 64 <= 128 ? 128 : (MB * HH * 64 <= 256 ? 256 : 512)));
+    static_assert(MB * HH * 64 <= 512, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -66,48 +77,48 @@ struct StateArgs {
     int* err;
 };
 
-template <int N>
-__global__ void __launch_bounds__(kThreads, StCfg<N>::CTAS_PER_SM)
+template <int N, int HH>
+__global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_SM)
     chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
                           StateArgs a) {
-    using K = StCfg<N>;
+    using K = StCfg<N, HH>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
     uint64_t* xs_ready = full + K::NST;
     uint64_t* empty = xs_ready + K::NST;
     uint64_t* acc_done = empty + K::NST;
-    float* Rs = reinterpret_cast<float*>(smem + K::OFF_R);
+    float* Rs = reinterpret_cast<float*>(smem + K::OFF_R);  // head hh at hh * kMaxSpanChunks
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
 
     const Dims& d = a.d;
-    const int h = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
+    const int h0 = blockIdx.x * HH, s = blockIdx.y, b = blockIdx.z;
     const int H = d.nheads, G = d.ngroups, Q = d.chunk_size;
-    const int g = h / (H / G);
+    const int g = h0 / (H / G);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t ts = (int64_t)s * a.span_chunks * Q;
     const int64_t te = min((int64_t)d.seqlen, ts + (int64_t)a.span_chunks * Q);
     const int nblk = (int)((te - ts + K::TB - 1) / K::TB);
     const int64_t c_first = ts / Q;
     const int nchk = (int)((te - ts + Q - 1) / Q);
-    const int64_t row = (int64_t)b * H + h;
-    const float* csr = a.cs + row * d.nchunks * Q;
-    const float* dtr = a.dtt + row * d.nchunks * Q;
+    const int64_t rowlen = (int64_t)d.nchunks * Q;  // dA_cumsum / dt row length per (b, h)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < K::NST; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&xs_ready[i], 128);
+            mbar_init(&xs_ready[i], 128 * K::SW);
             mbar_init(&empty[i], 1);
         }
         mbar_init(acc_done, 1);
         abort_sh = 0;
         fence_barrier_init();
     }
-    if (warp == 0) {
-        // per chunk c of the span: R_c + cs[c][Q-1] = sum of the chunk totals from c to the span
-        // end (an inclusive suffix sum), 32 chunks per round with one load per lane
+    if (warp < HH) {
+        // head h0 + warp: per chunk c of the span, R_c + cs[c][Q-1] = sum of the chunk totals
+        // from c to the span end (an inclusive suffix sum), 32 chunks per round, one load per lane
+        const int64_t row = (int64_t)b * H + h0 + warp;
+        const float* csr = a.cs + row * rowlen;
         float carry = 0.f;
         for (int base = nchk - 32; base > -32; base -= 32) {
             const int c = base + lane;
@@ -118,21 +129,21 @@ __global__ void __launch_bounds__(kThreads, StCfg<N>::CTAS_PER_SM)
                 if (lane + off < 32) v += o;
             }
             v += carry;
-            if (c >= 0) Rs[c] = v;
+            if (c >= 0) Rs[warp * kMaxSpanChunks + c] = v;
             carry = __shfl_sync(0xffffffffu, v, 0);
         }
         if (lane == 0 && a.span_decay != nullptr) a.span_decay[row * a.nspans + s] = carry;
     }
     if (K::SZ_ZERO > 0) {
         uint4* z = reinterpret_cast<uint4*>(smem + K::OFF_ZERO);
-        for (int i = threadIdx.x; i < K::SZ_ZERO / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+        for (int i = threadIdx.x; i < K::SZ_ZERO / 16; i += K::THREADS) z[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
-    if (warp == 5) {
+    if (warp == K::WARP_MMA) {
         tmem_alloc(&tmem_base_sh, K::TCOLS);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == K::WARP_TMA && lane == 0) {
         tma_prefetch_desc(&tm_x);
         tma_prefetch_desc(&tm_B);
     }
@@ -142,8 +153,8 @@ __global__ void __launch_bounds__(kThreads, StCfg<N>::CTAS_PER_SM)
     const uint32_t tm = tmem_base_sh;
     volatile int* abort_flag = &abort_sh;
 
-    if (warp == 4) {
-        // TMA producer
+    if (warp == K::WARP_TMA) {
+        // TMA producer: per stage the HH x tiles, the B boxes and the heads' dA_cumsum / dt rows
         if (lane == 0) {
             int issued[K::NST];
             for (int i = 0; i < K::NST; ++i) issued[i] = 0;
@@ -151,72 +162,83 @@ __global__ void __launch_bounds__(kThreads, StCfg<N>::CTAS_PER_SM)
                 const int st = kb % K::NST;
                 if (!mbar_wait_bounded(&empty[st], ((kb / K::NST) & 1) ^ 1, abort_flag, a.err, 21, kWaitNs)) break;
                 uint8_t* sX = smem + st * K::SZ_STAGE;
-                uint8_t* sB = sX + K::BOX;
                 const int t0 = (int)(ts + (int64_t)kb * K::TB);
-                // the block's dA_cumsum and dt rows (contiguous per (b, h)), at most TB values each
-                const uint32_t cdb = (uint32_t)min((int64_t)K::TB, (int64_t)d.nchunks * Q - t0) * 4u;
+                const uint32_t cdb = (uint32_t)min((int64_t)K::TB, rowlen - t0) * 4u;
                 float* scd = reinterpret_cast<float*>(sX + K::OFF_CD);
-                mbar_arrive_expect_tx(&full[st], K::BOX + K::NBOX * K::BOX + 2 * cdb);
-                tma_load_4d(sX, &tm_x, &full[st], 0, h, t0, b);
-                bulk_load(scd, csr + t0, cdb, &full[st]);
-                bulk_load(scd + K::TB, dtr + t0, cdb, &full[st]);
+                mbar_arrive_expect_tx(&full[st], HH * K::BOX + K::NBOX * K::BOX + HH * 2 * cdb);
 #pragma unroll
-                for (int bx = 0; bx < K::NBOX; ++bx) tma_load_4d(sB + bx * K::BOX, &tm_B, &full[st], bx * 64, g, t0, b);
+                for (int hh = 0; hh < HH; ++hh) {
+                    const int64_t row = ((int64_t)b * H + h0 + hh) * rowlen + t0;
+                    tma_load_4d(sX + hh * K::BOX, &tm_x, &full[st], 0, h0 + hh, t0, b);
+                    bulk_load(scd + hh * 2 * K::TB, a.cs + row, cdb, &full[st]);
+                    bulk_load(scd + hh * 2 * K::TB + K::TB, a.dtt + row, cdb, &full[st]);
+                }
+#pragma unroll
+                for (int bx = 0; bx < K::NBOX; ++bx)
+                    tma_load_4d(sX + K::OFF_B + bx * K::BOX, &tm_B, &full[st], bx * 64, g, t0, b);
                 ++issued[st];
             }
             for (int i = 0; i < K::NST; ++i)
                 if (issued[i] > 0) mbar_wait_bounded(&full[i], (issued[i] - 1) & 1, abort_flag, a.err, 22, kWaitNs);
         }
-    } else if (warp == 5) {
-        // MMA issuer
+    } else if (warp == K::WARP_MMA) {
+        // MMA issuer: acc[mb] (128 n x 64 HH) += B_mb^T (MN-major) * [X'_0 .. X'_HH-1] (MN-major)
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_fp16(128, 64, true, true);
+            constexpr uint32_t idesc = idesc_fp16(128, 64 * HH, true, true);
             for (int kb = 0; kb < nblk; ++kb) {
                 const int st = kb % K::NST;
                 if (!mbar_wait_bounded(&xs_ready[st], (kb / K::NST) & 1, abort_flag, a.err, 23, kWaitNs)) break;
                 tc_fence_after();
                 const uint32_t sX = smem_u32(smem + st * K::SZ_STAGE);
-                const uint32_t sB = sX + K::BOX;
+                const uint32_t sB = sX + K::OFF_B;
 #pragma unroll
                 for (int mb = 0; mb < K::MB; ++mb) {
                     const uint32_t a0 = sB + 2 * mb * K::BOX;
                     const uint32_t lbo = (N == 64) ? (uint32_t)(smem_u32(smem + K::OFF_ZERO) - a0) : (uint32_t)K::BOX;
 #pragma unroll
                     for (int k = 0; k < K::TB / 16; ++k)
-                        mma_ss(tm + mb * 64, desc_sw128(a0 + k * 2048, lbo, 1024), desc_sw128(sX + k * 2048, 16, 1024),
-                               idesc, (kb | k) != 0);
+                        mma_ss(tm + mb * 64 * HH, desc_sw128(a0 + k * 2048, lbo, 1024),
+                               desc_sw128(sX + k * 2048, HH > 1 ? (uint32_t)K::BOX : 16u, 1024), idesc, (kb | k) != 0);
                 }
                 mma_commit(&empty[st]);
             }
             mma_commit(acc_done);
         }
     } else {
-        // warps 0-3: scale X rows, then store the accumulator
-        const int r = threadIdx.x;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        // scaling warpgroup(s): thread t scales token row r = t % 128 of the x tiles of heads
+        // hh = t / 128, t / 128 + SW, ... in place, then stores those heads' accumulators
+        const int r = threadIdx.x & 127;
+        const int hsel = threadIdx.x >> 7;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         bool ok = true;
         for (int kb = 0; kb < nblk; ++kb) {
             const int st = kb % K::NST;
             ok = ok && mbar_wait_bounded(&full[st], (kb / K::NST) & 1, abort_flag, a.err, 24, kWaitNs);
             if (ok && r < K::TB) {
                 const int64_t t = ts + (int64_t)kb * K::TB + r;
-                uint8_t* xrow = smem + st * K::SZ_STAGE;
-                const float* scd = reinterpret_cast<const float*>(xrow + K::OFF_CD);
-                float w = 0.f;
-                if (t < te) w = exp2f(Rs[t / Q - c_first] - scd[r]) * scd[K::TB + r];
+                uint8_t* stage = smem + st * K::SZ_STAGE;
+                const float* scd = reinterpret_cast<const float*>(stage + K::OFF_CD);
+#pragma unroll 1
+                for (int hh = hsel; hh < HH; hh += K::SW) {
+                    uint8_t* xrow = stage + hh * K::BOX;
+                    const float* cd = scd + hh * 2 * K::TB;
+                    float w = 0.f;
+                    if (t < te) w = exp2f(Rs[hh * kMaxSpanChunks + (int)(t / Q - c_first)] - cd[r]) * cd[K::TB + r];
+                    uint4 v[8];
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint32_t off = sw128_offset(r, ch);
-                    uint4 v = *reinterpret_cast<const uint4*>(xrow + off);
-                    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
-                    uint4 o;
-                    __half2* o2 = reinterpret_cast<__half2*>(&o);
+                    for (int ch = 0; ch < 8; ++ch) v[ch] = *reinterpret_cast<const uint4*>(xrow + sw128_offset(r, ch));
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = __bfloat1622float2(p2[e]);
-                        o2[e] = __floats2half2_rn(f.x * w, f.y * w);
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v[ch]);
+                        uint4 o;
+                        __half2* o2 = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(p2[e]);
+                            o2[e] = __floats2half2_rn(f.x * w, f.y * w);
+                        }
+                        *reinterpret_cast<uint4*>(xrow + sw128_offset(r, ch)) = o;
                     }
-                    *reinterpret_cast<uint4*>(xrow + off) = o;
                 }
                 fence_proxy_async_smem();
             }
@@ -227,18 +249,21 @@ __global__ void __launch_bounds__(kThreads, StCfg<N>::CTAS_PER_SM)
         tc_fence_after();
         if (ok) {
             const int64_t PN = (int64_t)d.headdim * N;
-            float* out = a.S + (((int64_t)b * a.nspans + s) * H + h) * PN;
 #pragma unroll 1
-            for (int mb = 0; mb < K::MB; ++mb) {
-                const int n = mb * 128 + r;
+            for (int hh = hsel; hh < HH; hh += K::SW) {
+                float* out = a.S + (((int64_t)b * a.nspans + s) * H + h0 + hh) * PN;
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t v[32];
-                    tmem_ld32(tm + lane_base + mb * 64 + half * 32, v);
-                    tmem_ld_wait(v);
-                    if (n < N) {
+                for (int mb = 0; mb < K::MB; ++mb) {
+                    const int n = mb * 128 + r;
+#pragma unroll 1
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t v[32];
+                        tmem_ld32(tm + lane_base + mb * 64 * HH + hh * 64 + half * 32, v);
+                        tmem_ld_wait(v);
+                        if (n < N) {
 #pragma unroll
-                        for (int p = 0; p < 32; ++p) out[(int64_t)(half * 32 + p) * N + n] = __uint_as_float(v[p]);
+                            for (int p = 0; p < 32; ++p) out[(int64_t)(half * 32 + p) * N + n] = __uint_as_float(v[p]);
+                        }
                     }
                 }
             }
@@ -247,24 +272,34 @@ __global__ void __launch_bounds__(kThreads, StCfg<N>::CTAS_PER_SM)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tm, K::TCOLS);
+    if (warp == K::WARP_MMA) tmem_dealloc(tm, K::TCOLS);
 }
 
-template <int N>
-int launch_state_n(const __nv_bfloat16* x, const __half* B, const StateArgs& a, cudaStream_t s) {
-    using K = StCfg<N>;
+template <int N, int HH>
+int launch_state_nh(const __nv_bfloat16* x, const __half* B, const StateArgs& a, cudaStream_t s) {
+    using K = StCfg<N, HH>;
     const Dims& d = a.d;
     CUtensorMap tx, tb;
     const uint64_t dx[4] = {(uint64_t)d.headdim, (uint64_t)d.nheads, (uint64_t)d.seqlen, (uint64_t)d.batch};
     const uint64_t db[4] = {(uint64_t)d.dstate, (uint64_t)d.ngroups, (uint64_t)d.seqlen, (uint64_t)d.batch};
     const uint32_t box[4] = {64, 1, (uint32_t)K::TB, 1};
     if (!make_tmap_16b_4d(&tx, x, dx, box) || !make_tmap_16b_4d(&tb, B, db, box)) return SSD_ERR_CUDA;
-    if (ensure_smem_limit(reinterpret_cast<const void*>(chunk_state_tc_kernel<N>), K::SMEM) != SSD_OK)
+    if (ensure_smem_limit(reinterpret_cast<const void*>(chunk_state_tc_kernel<N, HH>), K::SMEM) != SSD_OK)
         return SSD_ERR_CUDA;
-    dim3 grid(d.nheads, a.nspans, d.batch);
+    dim3 grid(d.nheads / HH, a.nspans, d.batch);
     launch_begin(kKindChunkState, s);
-    chunk_state_tc_kernel<N><<<grid, kThreads, K::SMEM, s>>>(tx, tb, a);
+    chunk_state_tc_kernel<N, HH><<<grid, K::THREADS, K::SMEM, s>>>(tx, tb, a);
     return launch_end(kKindChunkState, s);
+}
+
+// Heads per CTA: as many of one group as divide evenly, up to 4 (N <= 128) or 2 (N >= 256).
+template <int N>
+int launch_state_n(const __nv_bfloat16* x, const __half* B, const StateArgs& a, cudaStream_t s) {
+    const int hpg = a.d.nheads / a.d.ngroups;
+    constexpr int HMAX = (N <= 128) ? 4 : 2;
+    if (HMAX >= 4 && hpg % 4 == 0) return launch_state_nh<N, (HMAX >= 4 ? 4 : 2)>(x, B, a, s);
+    if (hpg % 2 == 0) return launch_state_nh<N, 2>(x, B, a, s);
+    return launch_state_nh<N, 1>(x, B, a, s);
 }
 
 }  // namespace
