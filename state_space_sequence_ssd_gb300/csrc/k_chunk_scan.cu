@@ -303,6 +303,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // front(f): S (state update), then C h, then C B^T; false on a failed wait
             int it = 0;
+            int f = 0, m = 0;  // next front to issue, next M X to issue
+            // a finished mask's M X goes ahead of the rest of a front (the tensor pipe runs
+            // instructions in issue order, and the epilogue and the next front wait on it);
+            // measured on GB300 to pay off for N >= 256 (two n-blocks per front) only
+            auto mx_if_ready = [&](int f) {
+                if (N >= 256 && m < f && mbar_test_wait(&bar->m_ready[m % K::NBUF], (m / K::NBUF) & 1)) {
+                    tc_fence_after();
+                    issue_mx(m++);
+                }
+            };
             auto issue_front = [&](int f) -> bool {
                 const bool need_S = f + 1 < nsb;
                 const int k = f % K::NBUF;
@@ -311,8 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (need_S)
                         for (int nb = 0; nb < K::NBLK; ++nb) issue_s(nb, stage_c((it + nb) % K::NST) + K::SZ_C);
                     mma_commit(&bar->xs_free);
+                    mx_if_ready(f);
                     for (int nb = 0; nb < K::NBLK; ++nb) issue_ys(nb, set, stage_c((it + nb) % K::NST));
                     mma_commit(&bar->state_done);
+                    mx_if_ready(f);
                     for (int nb = 0; nb < K::NBLK; ++nb, ++it) {
                         const int st = it % K::NST;
                         issue_cb(nb, set, stage_c(st), stage_c(st) + K::SZ_C);
@@ -348,7 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return false;
                 return true;
             };
-            int f = 0, m = 0;
             bool ok = true;
             uint64_t last = globaltimer_ns();
             while (m < nsb && ok) {
