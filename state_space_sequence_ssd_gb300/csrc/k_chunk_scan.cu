@@ -92,7 +92,7 @@ struct Cfg {
     static constexpr int SZ_STAGE = 2 * SZ_C;  // C then B
     static constexpr int OFF_ZERO = OFF_BC + NST * SZ_STAGE;
     static constexpr int SZ_ZERO = (N == 64) ? kTile : 0;
-    static constexpr int OFF_U = OFF_ZERO + SZ_ZERO;  // 3 x {u[128], dt[128], bcol[128], bdiag[128]}
+    static constexpr int OFF_U = OFF_ZERO + SZ_ZERO;  // 3 x {u[128], dt[128], bcol[128], -[128]}
     static constexpr int OFF_CD = OFF_U + 3 * 2048;   // NX x {cs[128], dt[128]} rows, bulk-copied with x
     static constexpr int OFF_BAR = OFF_CD + NX * 1024;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + alignment slack
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars* bar = reinterpret_cast<Bars*>(smem + K::OFF_BAR);
-    float* sU = reinterpret_cast<float*>(smem + K::OFF_U);  // buffer k at k*512: u, dt, bcol, bdiag
+    float* sU = reinterpret_cast<float*>(smem + K::OFF_U);  // buffer k at k*512: u, dt, bcol
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
 
@@ -405,8 +405,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* su = sU + ub * 512;
             const float* sdt = su + 128;
             const float* sbc = su + 256;
-            const float* sbd = su + 384;
-            const int nv = (int)min((int64_t)128, te - (ts + sb * 128));
             const float ui = su[r];
             const uint32_t set = tm + lane_base + K::T_SET + k * K::SET;
 #pragma unroll 1
@@ -427,31 +425,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             o[jj >> 1] = pack_f16x2(__uint_as_float(v[jj]) * (ar * sbc[j]),
                                                     __uint_as_float(v[jj + 1]) * (ar * sbc[j + 1]));
                         }
-                    } else if (su[q * 32] - su[q * 32 + 31] <= 100.f) {
-                        // diagonal block, factorized with the block's first position as reference:
-                        // the block decays by at most 2^100, so both factors stay normal floats
-                        const float ar = fast_exp2(fminf(ui - su[q * 32], 0.f));
+                    } else {
+                        // diagonal block: exact per-element exponent, causal mask, D on the diagonal
 #pragma unroll
                         for (int jj = 0; jj < 32; jj += 2) {
                             const int j0 = q * 32 + jj, j1 = j0 + 1;
-                            float m0 = (j0 <= r) ? __uint_as_float(v[jj]) * (ar * sbd[j0]) : 0.f;
-                            float m1 = (j1 <= r) ? __uint_as_float(v[jj + 1]) * (ar * sbd[j1]) : 0.f;
-                            if (j0 == r) m0 += Dh;
-                            if (j1 == r) m1 += Dh;
-                            o[jj >> 1] = pack_f16x2(m0, m1);
-                        }
-                    } else {  // diagonal block of extreme decay: exact per-element exponent
-#pragma unroll
-                        for (int jj = 0; jj < 32; jj += 2) {
-                            const int j0 = q * 32 + jj, j1 = j0 + 1;
-                            float m0 = (j0 <= r && j0 < nv)
-                                           ? __uint_as_float(v[jj]) * fast_exp2(fminf(ui - su[j0], 0.f)) * sdt[j0]
-                                           : 0.f;
-                            float m1 = (j1 <= r && j1 < nv)
-                                           ? __uint_as_float(v[jj + 1]) * fast_exp2(fminf(ui - su[j1], 0.f)) * sdt[j1]
-                                           : 0.f;
-                            if (j0 == r) m0 += Dh;
-                            if (j1 == r) m1 += Dh;
+                            const float2 uj = *reinterpret_cast<const float2*>(su + j0);
+                            const float2 dj = *reinterpret_cast<const float2*>(sdt + j0);
+                            float m0 = __uint_as_float(v[jj]) * fast_exp2(fminf(ui - uj.x, 0.f)) * dj.x;
+                            float m1 = __uint_as_float(v[jj + 1]) * fast_exp2(fminf(ui - uj.y, 0.f)) * dj.y;
+                            m0 = (j0 <= r) ? m0 : 0.f;
+                            m1 = (j1 <= r) ? m1 : 0.f;
+                            m0 += (j0 == r) ? Dh : 0.f;
+                            m1 += (j1 == r) ? Dh : 0.f;
                             o[jj >> 1] = pack_f16x2(m0, m1);
                         }
                     }
@@ -488,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int p0 = (int)(t0 % Q);
             const float prev = (p0 > 0) ? prev_raw : 0.f;
             const bool valid = r < nv;
-            float u = 0.f, ulast = 0.f, dtv = 0.f, bcol = 0.f, bdiag = 0.f;
+            float u = 0.f, ulast = 0.f, dtv = 0.f, bcol = 0.f;
             if (ok) {
                 ulast = sub_block_decay(scs, prev, p0, Q, nv - 1);
                 if (valid) {
@@ -498,9 +484,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // position of r's 32-block
                     const float uend = sub_block_decay(scs, prev, p0, Q, min(r | 31, nv - 1));
                     bcol = fast_exp2(fminf(uend - u, 0.f)) * dtv;
-                    // diagonal-block weight 2^(u_start - u_r) dt_r (used only where the block's
-                    // total decay is at most 2^100; invalid columns stay 0)
-                    bdiag = fast_exp2(fminf(sub_block_decay(scs, prev, p0, Q, r & ~31) - u, 100.f)) * dtv;
                 } else {
                     u = ulast;
                 }
@@ -509,7 +492,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             su[r] = u;
             su[128 + r] = dtv;
             su[256 + r] = bcol;
-            su[384 + r] = bdiag;
             mbar_arrive(&bar->uv_ready[ub]);
             const float dsb = exp2f(ulast);
             // 2. x tile -> float16 in place, and X' = w x into the single X' buffer once the
