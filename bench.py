@@ -378,43 +378,100 @@ def kernel_source_sha1(name: str) -> str:
 
 
 def e2e_measure(w, inp, dev, stream, args, ssd, dist):
-    """Same metric through ssd_forward with host buffers: H2D of inputs and D2H of y + final inside the timing."""
+    """Same metric through ssd_forward with host buffers: every step copies its inputs from pinned host
+    memory to the device and reads y and the final state back, inside the timing.
+
+    Steps run as a serving loop would: two device buffer sets and three streams (host-to-device copies,
+    ssd_forward, device-to-host copies), so step i+1's inputs travel while step i computes and step i-1's
+    result comes back.  The serial figure (copy, compute, copy on one stream) is reported beside it."""
     import torch
     host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
-    devb = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in inp.items()}
-    y = torch.empty_like(devb["x"])
-    fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), device=dev, dtype=torch.float32)
-    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
-    fin_h = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
-    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
-    d2h = y.numel() * y.element_size() + fin.numel() * fin.element_size()
-
-    def once():
-        for k, v in host.items():
-            if v is not None:
-                devb[k].copy_(v, non_blocking=True)
-        ssd.ssd_forward(devb["x"], devb["dt"], devb["A"], devb["B"], devb["C"], devb["D"], devb["init"],
-                        w.chunk_size, y=y, final_state=fin, stream=stream)
-        y_h.copy_(y, non_blocking=True)
-        fin_h.copy_(fin, non_blocking=True)
-
+    fshape = (w.batch, w.nheads, w.headdim, w.dstate)
+    sets = []
     for _ in range(2):
-        once()
+        devb = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in inp.items()}
+        devb["y"] = torch.empty_like(devb["x"])
+        devb["fin"] = torch.empty(fshape, device=dev, dtype=torch.float32)
+        devb["y_h"] = torch.empty(devb["y"].shape, dtype=devb["y"].dtype, pin_memory=True)
+        devb["fin_h"] = torch.empty(fshape, dtype=torch.float32, pin_memory=True)
+        sets.append(devb)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = sets[0]["y"].numel() * sets[0]["y"].element_size() + sets[0]["fin"].numel() * 4
+
+    def forward(db, st):
+        ssd.ssd_forward(db["x"], db["dt"], db["A"], db["B"], db["C"], db["D"], db["init"], w.chunk_size,
+                        y=db["y"], final_state=db["fin"], stream=st)
+
+    # serial: everything on one stream
+    def serial_once():
+        db = sets[0]
+        with torch.cuda.stream(stream):
+            for k, v in host.items():
+                if v is not None:
+                    db[k].copy_(v, non_blocking=True)
+            forward(db, stream)
+            db["y_h"].copy_(db["y"], non_blocking=True)
+            db["fin_h"].copy_(db["fin"], non_blocking=True)
+
+    # pipelined: stream hs copies inputs in, cs computes, ds copies results out
+    hs, cs, ds = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ev_h2d = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_d2h = [torch.cuda.Event() for _ in range(2)]
+
+    def pipelined_step(i):
+        k = i % 2
+        db = sets[k]
+        with torch.cuda.stream(hs):
+            if i >= 2:
+                hs.wait_event(ev_comp[k])  # step i-2 has consumed this set's inputs
+            for name, v in host.items():
+                if v is not None:
+                    db[name].copy_(v, non_blocking=True)
+            ev_h2d[k].record(hs)
+        with torch.cuda.stream(cs):
+            cs.wait_event(ev_h2d[k])
+            if i >= 2:
+                cs.wait_event(ev_d2h[k])  # step i-2's result has been read back
+            forward(db, cs)
+            ev_comp[k].record(cs)
+        with torch.cuda.stream(ds):
+            ds.wait_event(ev_comp[k])
+            db["y_h"].copy_(db["y"], non_blocking=True)
+            db["fin_h"].copy_(db["fin"], non_blocking=True)
+            ev_d2h[k].record(ds)
+
+    n = max(8, args.steps // 2)
+    for _ in range(2):
+        serial_once()
     torch.cuda.synchronize()
-    n = max(3, args.steps // 2)
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
-    s.record(stream)
+    s0.record(stream)
     for _ in range(n):
-        once()
-    e.record(stream)
+        serial_once()
+    s1.record(stream)
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / n
-    ms = max_over_ranks(ms, dist, dev)
+    serial_ms = max_over_ranks(s0.elapsed_time(s1) / n, dist, dev)
+
+    for i in range(4):
+        pipelined_step(i)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    t0.record(hs)
+    for i in range(n):
+        pipelined_step(i)
+    t1.record(ds)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1) / n, dist, dev)
     world = dist.get_world_size() if dist is not None else 1
     return {"value": round(w.batch * w.seqlen * world / (ms / 1e3), 1), "unit": "tokens/s",
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4),
+            "steps": n, "pipeline": "two buffer sets; H2D, compute and D2H on separate streams",
+            "serial_ms_per_step": round(serial_ms, 4)}
 
 
 def run_reference(args, w):
