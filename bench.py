@@ -235,6 +235,9 @@ def main():
     # ---- end to end through the public call with host buffers
     e2e = e2e_measure(w, inp, dev, stream, args, ssd, dist)
 
+    # ---- the recurrent decode step on a serving batch of the workload's model
+    decode = decode_measure(w, dev, stream, args, ssd, lib, flush)
+
     if rank != 0:
         dist.destroy_process_group()
         return 0
@@ -288,6 +291,7 @@ def main():
         "kernels": kernels,
         "gpu_launches": int(launches),
         "e2e": e2e,
+        "decode_step": decode,
         "clocks": clk,
         "device_error": int(err),
     }
@@ -349,7 +353,7 @@ def kernel_alg_bytes(name: str, w: I.Workload) -> float:
 
 
 KERNEL_SOURCES = {"chunk_cumsum": "k_cumsum.cu", "chunk_state": "k_chunk_state.cu",
-                  "state_passing": "k_state_passing.cu", "chunk_scan": "k_chunk_scan.cu"}
+                  "state_passing": "k_state_passing.cu", "chunk_scan": "k_chunk_scan.cu", "step": "k_step.cu"}
 
 
 def kernel_traffic(name: str, w: I.Workload):
@@ -472,6 +476,58 @@ def e2e_measure(w, inp, dev, stream, args, ssd, dist):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4),
             "steps": n, "pipeline": "two buffer sets; H2D, compute and D2H on separate streams",
             "serial_ms_per_step": round(serial_ms, 4)}
+
+
+DECODE_BATCH = 256
+
+
+def decode_step_bytes(b: int, H: int, P: int, N: int, G: int) -> float:
+    """Algorithmic bytes of one ssd_step: state read + write (f32), x read and y write (bf16),
+    dt (f32), B and C (bf16), A and D."""
+    return float(2 * b * H * P * N * 4 + 2 * b * H * P * 2 + b * H * 4 + 2 * b * G * N * 2 + 2 * H * 4)
+
+
+def decode_measure(w, dev, stream, args, ssd, lib, flush):
+    """ssd_step for DECODE_BATCH sequences of the workload's model (H, P, N, G), state resident in HBM.
+    One step = one new token of every sequence; L2 flushed between steps outside the events."""
+    import torch
+    dw = w.with_(name=f"decode_b{DECODE_BATCH}_{w.name}", batch=DECODE_BATCH, seqlen=1, nonzero_init=True)
+    inp = I.make_inputs(dw, seed=1)
+    d = {k: v.to(dev) for k, v in inp.items()}
+    x, dt, B, C = d["x"][:, 0].contiguous(), d["dt"][:, 0].contiguous(), d["B"][:, 0].contiguous(), \
+        d["C"][:, 0].contiguous()
+    state = d["init"]
+    y = torch.empty_like(x)
+
+    def step():
+        ssd.ssd_step(x, dt, d["A"], B, C, d["D"], state, y=y, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    steps = max(args.steps, 20)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    n0 = lib.ssd_launch_count()
+    for i in range(steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    launches = lib.ssd_launch_count() - n0
+    us = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / steps * 1e3
+    by = decode_step_bytes(dw.batch, dw.nheads, dw.headdim, dw.dstate, dw.ngroups)
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs = by / (us / 1e6) / 1e9
+    return {"workload": dw.name, "batch": dw.batch, "state_mb": round(dw.batch * dw.nheads * dw.headdim * dw.dstate * 4 / 1e6, 1),
+            "us_per_step": round(us, 2), "tokens_per_s": round(dw.batch / (us / 1e6), 1),
+            "roofline": {"bound": "hbm", "kernel": "step", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "peak_source": f"{src} hbm_gbs (copy)",
+                         "alg_bytes_per_launch": by, "traffic": kernel_traffic("step", dw)},
+            "steps": steps, "gpu_launches": int(launches)}
 
 
 def run_reference(args, w):

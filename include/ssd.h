@@ -204,6 +204,30 @@ SSD_API int ssd_forward_noalloc(const void* x, const float* dt, const float* A, 
                         int chunk_size, void* y, float* final_state, cudaStream_t stream);
 
 /*
+ * ssd_step -- one recurrent step of the selective state-space model for a
+ * single new token of every sequence: the fixed-size-state mode of the model
+ * (disconfirmai.com page, SSM/attention/RNN paragraph; readmex.ai page,
+ * English excerpt: constant memory per token).  Per batch row b and head h,
+ * g = h / (nheads / ngroups):
+ *     a = exp(dt[b,h] * A[h])
+ *     state[b,h,p,n] <- a * state[b,h,p,n] + dt[b,h] * B[b,g,n] * x[b,h,p]
+ *     y[b,h,p] = sum_n C[b,g,n] * state[b,h,p,n] + D[h] * x[b,h,p]
+ * i.e. ssd_forward over one token with init_state = final_state = state.
+ *   x, y      (batch, nheads, headdim)   bfloat16 (2-byte aligned)
+ *   dt        (batch, nheads)            float32
+ *   A, D      (nheads)                   float32; D may be NULL (no skip term)
+ *   B, C      (batch, ngroups, dstate)   bfloat16
+ *   state     (batch, nheads, headdim, dstate) float32, 16-byte aligned; read
+ *             and overwritten in place with the state after the token.
+ * fp32 arithmetic throughout (exp is the accurate expf).  Supported shapes as
+ * for ssd_forward (headdim 64, dstate 64/128/256/512).  Asynchronous on
+ * `stream`; the same error behaviour as the other entry points.
+ */
+SSD_API int ssd_step(const void* x, const float* dt, const float* A, const void* B, const void* C,
+                     const float* D, float* state, int batch, int nheads, int headdim, int ngroups, int dstate,
+                     void* y, cudaStream_t stream);
+
+/*
  * ssd_get_device_error -- reads and clears the library's device error word
  * on the current device (synchronizes with the device).  Returns SSD_OK, or
  * SSD_ERR_TIMEOUT if a kernel's bounded wait gave up since the last read, or

@@ -18,7 +18,7 @@ from __future__ import annotations
 from . import _ffi
 
 __all__ = ["ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_forward",
-           "ssd_forward_noalloc",
+           "ssd_forward_noalloc", "ssd_step",
            "ssd_get_device_error", "SSDError", "library_path"]
 
 SSDError = _ffi.SSDError
@@ -184,6 +184,34 @@ def ssd_forward_noalloc(x, dt, A, B, C, D, init_state, chunk_size, y, final_stat
         _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
         b, L, H, P, G, N, chunk_size, _ptr(y), _ptr(final_state), _stream(stream)))
     return y, final_state
+
+
+def ssd_step(x, dt, A, B, C, D, state, y=None, stream=None):
+    """One recurrent step for a single new token of every sequence.
+
+    x (batch, H, P) bf16, dt (batch, H) f32, A (H,) f32, B, C (batch, G, N) bf16,
+    D (H,) f32 or None, state (batch, H, P, N) f32 updated in place.  Returns y (batch, H, P) bf16."""
+    torch = _torch()
+    _need(x, "x", torch.bfloat16, 3)
+    _need(dt, "dt", torch.float32, 2)
+    _need(A, "A", torch.float32, 1)
+    _need(B, "B", torch.bfloat16, 3)
+    _need(C, "C", torch.bfloat16, 3)
+    _opt(D, "D", torch.float32, 1)
+    _need(state, "state", torch.float32, 4)
+    b, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", torch.bfloat16, 3)
+    for name, t, shape in (("dt", dt, (b, H)), ("A", A, (H,)), ("B", B, (b, G, N)), ("C", C, (b, G, N)),
+                           ("D", D, (H,)), ("state", state, (b, H, P, N)), ("y", y, (b, H, P))):
+        if t is not None and tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+    _ffi.check("ssd_step", _ffi.lib().ssd_step(
+        _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(state), b, H, P, G, N, _ptr(y),
+        _stream(stream)))
+    return y
 
 
 def ssd_get_device_error():

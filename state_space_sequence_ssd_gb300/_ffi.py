@@ -31,6 +31,7 @@ SIGNATURES = {
     "ssd_chunk_scan": (_i, [_p] * 7 + [_i] * 7 + [_p, _p]),
     "ssd_forward": (_i, [_p] * 7 + [_i] * 7 + [_p, _p, _p]),
     "ssd_forward_noalloc": (_i, [_p] * 7 + [_i] * 7 + [_p, _p, _p]),
+    "ssd_step": (_i, [_p] * 7 + [_i] * 5 + [_p, _p]),
     "ssd_get_device_error": (_i, []),
     "ssd_profile_enable": (_i, [_i]),
     "ssd_profile_reset": (_i, []),

@@ -27,7 +27,8 @@ enum KernelKind {
     kKindStatePassing = 2,
     kKindChunkScan = 3,
     kKindConvert = 4,
-    kNumKinds = 5
+    kKindStep = 5,
+    kNumKinds = 6
 };
 
 // Sets a kernel's dynamic shared-memory limit once per (kernel, device).
@@ -61,5 +62,10 @@ int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_ste
 int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C,
                            const float* dtt, const float* cs, const float* D, const float* span_states,
                            int span_chunks, const Dims& d, __nv_bfloat16* y, int* err, cudaStream_t s);
+
+// one recurrent step for every (batch, head): state updated in place, y for the token (k_step.cu)
+int launch_step(const __nv_bfloat16* x, const float* dt, const float* A, const __nv_bfloat16* B,
+                const __nv_bfloat16* C, const float* D, float* state, int batch, int nheads, int ngroups, int dstate,
+                __nv_bfloat16* y, cudaStream_t s);
 
 }  // namespace ssd

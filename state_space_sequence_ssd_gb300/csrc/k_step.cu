@@ -1,0 +1,147 @@
+// k_step.cu -- one recurrent step of the selective state-space model: the
+// constant-memory per-token update that the chunked forward pass computes in
+// bulk.
+//
+// disconfirmai.com page "Jane Street ML Engineers Map Mamba-2 Recurrent State
+// Computation to Tensor Cores with cuTile", SSM/attention/RNN paragraph (the
+// model can run as a recurrence with a fixed-size state) and readmex.ai page,
+// English excerpt (the sequence-model trade-off: constant memory per token).
+// Per batch row b and head h (group g = h / (H / G)), for the single token:
+//
+//   a              = exp(dt A_h)
+//   state[p][n]   <- a state[p][n] + dt B[n] x[p]
+//   y[p]           = sum_n C[n] state[p][n] + D_h x[p]
+//
+// One CTA per (b, h), 256 threads: warp w updates state rows p = w, w + 8, ...
+// (each lane four consecutive n per 128 n, one float4 load and store per 128 n)
+// and reduces the row's dot product with C by warp shuffles.  The state is
+// read and written once: the step is bound by HBM.  fp32 throughout.
+#include "common.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <int N>
+__global__ void __launch_bounds__(kThreads) ssd_step_kernel(const __nv_bfloat16* __restrict__ x,
+                                                            const float* __restrict__ dt,
+                                                            const float* __restrict__ A,
+                                                            const __nv_bfloat16* __restrict__ B,
+                                                            const __nv_bfloat16* __restrict__ C,
+                                                            const float* __restrict__ D, float* __restrict__ state,
+                                                            int nheads, int ngroups, __nv_bfloat16* __restrict__ y) {
+    constexpr int P = 64;
+    constexpr int NV = N / 128;  // float4 per lane per row
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int g = h / (nheads / ngroups);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t bh = (int64_t)b * nheads + h;
+    const float dtv = dt[bh];
+    const float a = expf(dtv * A[h]);
+    const float Dh = (D != nullptr) ? D[h] : 0.f;
+    // this lane's B and C entries: n = 128 v + 4 lane + e
+    float bv[NV][4], cv[NV][4];
+    const __nv_bfloat16* Bg = B + ((int64_t)b * ngroups + g) * N;
+    const __nv_bfloat16* Cg = C + ((int64_t)b * ngroups + g) * N;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int n = 128 * v + 4 * lane + e;
+            bv[v][e] = __bfloat162float(Bg[n]) * dtv;
+            cv[v][e] = __bfloat162float(Cg[n]);
+        }
+    }
+    const __nv_bfloat16* xr = x + bh * P;
+    float* st = state + bh * (int64_t)P * N;
+#pragma unroll 2
+    for (int p = warp; p < P; p += kThreads / 32) {
+        const float xp = __bfloat162float(xr[p]);
+        float acc = 0.f;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            float4* q = reinterpret_cast<float4*>(st + (int64_t)p * N + 128 * v + 4 * lane);
+            float4 s4 = *q;
+            s4.x = fmaf(a, s4.x, bv[v][0] * xp);
+            s4.y = fmaf(a, s4.y, bv[v][1] * xp);
+            s4.z = fmaf(a, s4.z, bv[v][2] * xp);
+            s4.w = fmaf(a, s4.w, bv[v][3] * xp);
+            *q = s4;
+            acc = fmaf(cv[v][0], s4.x, acc);
+            acc = fmaf(cv[v][1], s4.y, acc);
+            acc = fmaf(cv[v][2], s4.z, acc);
+            acc = fmaf(cv[v][3], s4.w, acc);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) y[bh * P + p] = __float2bfloat16_rn(acc + Dh * xp);
+    }
+}
+
+// N = 64: half a warp's lanes per row (each lane four n), two rows per warp at a time.
+__global__ void __launch_bounds__(kThreads) ssd_step_kernel_n64(const __nv_bfloat16* __restrict__ x,
+                                                                const float* __restrict__ dt,
+                                                                const float* __restrict__ A,
+                                                                const __nv_bfloat16* __restrict__ B,
+                                                                const __nv_bfloat16* __restrict__ C,
+                                                                const float* __restrict__ D, float* __restrict__ state,
+                                                                int nheads, int ngroups, __nv_bfloat16* __restrict__ y) {
+    constexpr int P = 64, N = 64;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int g = h / (nheads / ngroups);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = lane >> 4, l16 = lane & 15;
+    const int64_t bh = (int64_t)b * nheads + h;
+    const float dtv = dt[bh];
+    const float a = expf(dtv * A[h]);
+    const float Dh = (D != nullptr) ? D[h] : 0.f;
+    const __nv_bfloat16* Bg = B + ((int64_t)b * ngroups + g) * N;
+    const __nv_bfloat16* Cg = C + ((int64_t)b * ngroups + g) * N;
+    float bv[4], cv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        bv[e] = __bfloat162float(Bg[4 * l16 + e]) * dtv;
+        cv[e] = __bfloat162float(Cg[4 * l16 + e]);
+    }
+    const __nv_bfloat16* xr = x + bh * P;
+    float* st = state + bh * (int64_t)P * N;
+#pragma unroll 2
+    for (int p0 = 2 * warp; p0 < P; p0 += 2 * (kThreads / 32)) {
+        const int p = p0 + half;
+        const float xp = __bfloat162float(xr[p]);
+        float4* q = reinterpret_cast<float4*>(st + (int64_t)p * N + 4 * l16);
+        float4 s4 = *q;
+        s4.x = fmaf(a, s4.x, bv[0] * xp);
+        s4.y = fmaf(a, s4.y, bv[1] * xp);
+        s4.z = fmaf(a, s4.z, bv[2] * xp);
+        s4.w = fmaf(a, s4.w, bv[3] * xp);
+        *q = s4;
+        float acc = cv[0] * s4.x;
+        acc = fmaf(cv[1], s4.y, acc);
+        acc = fmaf(cv[2], s4.z, acc);
+        acc = fmaf(cv[3], s4.w, acc);
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (l16 == 0) y[bh * P + p] = __float2bfloat16_rn(acc + Dh * xp);
+    }
+}
+
+}  // namespace
+
+int launch_step(const __nv_bfloat16* x, const float* dt, const float* A, const __nv_bfloat16* B,
+                const __nv_bfloat16* C, const float* D, float* state, int batch, int nheads, int ngroups, int dstate,
+                __nv_bfloat16* y, cudaStream_t s) {
+    dim3 grid(nheads, batch);
+    launch_begin(kKindStep, s);
+    switch (dstate) {
+        case 64: ssd_step_kernel_n64<<<grid, kThreads, 0, s>>>(x, dt, A, B, C, D, state, nheads, ngroups, y); break;
+        case 128: ssd_step_kernel<128><<<grid, kThreads, 0, s>>>(x, dt, A, B, C, D, state, nheads, ngroups, y); break;
+        case 256: ssd_step_kernel<256><<<grid, kThreads, 0, s>>>(x, dt, A, B, C, D, state, nheads, ngroups, y); break;
+        case 512: ssd_step_kernel<512><<<grid, kThreads, 0, s>>>(x, dt, A, B, C, D, state, nheads, ngroups, y); break;
+        default: return SSD_ERR_UNSUPPORTED;
+    }
+    return launch_end(kKindStep, s);
+}
+
+}  // namespace ssd

@@ -39,7 +39,7 @@ cudaEvent_t take_event() {
 }
 
 const char* const kKindNames[kNumKinds] = {"chunk_cumsum", "chunk_state", "state_passing", "chunk_scan",
-                                           "bc_to_f16"};
+                                           "bc_to_f16", "step"};
 
 }  // namespace
 
@@ -397,6 +397,22 @@ int ssd_forward_noalloc(const void* x, const float* dt, const float* A, const vo
     if (r == SSD_OK)
         r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream);
     return r;
+}
+
+int ssd_step(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,
+             float* state, int batch, int nheads, int headdim, int ngroups, int dstate, void* y,
+             cudaStream_t stream) {
+    if (!x || !dt || !A || !B || !C || !state || !y) return SSD_ERR_INVALID_ARG;
+    if (batch <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0) return SSD_ERR_INVALID_ARG;
+    if (nheads % ngroups != 0) return SSD_ERR_INVALID_ARG;
+    if (headdim != 64 || !supported_dstate(dstate)) return SSD_ERR_UNSUPPORTED;
+    if (batch > 65535 || nheads > 2147483647 / 64) return SSD_ERR_UNSUPPORTED;
+    if (!aligned16(state) || ((uintptr_t)x & 1u) || ((uintptr_t)B & 1u) || ((uintptr_t)C & 1u) ||
+        ((uintptr_t)y & 1u) || ((uintptr_t)dt & 3u) || ((uintptr_t)A & 3u) || (D && ((uintptr_t)D & 3u)))
+        return SSD_ERR_INVALID_ARG;
+    return launch_step(static_cast<const __nv_bfloat16*>(x), dt, A, static_cast<const __nv_bfloat16*>(B),
+                       static_cast<const __nv_bfloat16*>(C), D, state, batch, nheads, ngroups, dstate,
+                       static_cast<__nv_bfloat16*>(y), stream);
 }
 
 int ssd_get_device_error(void) {

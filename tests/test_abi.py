@@ -121,3 +121,21 @@ def test_noalloc_validates_before_the_device(lib):
     assert fwd_noalloc(lib, dstate=96) == _ffi.SSD_ERR_UNSUPPORTED
     assert fwd_noalloc(lib, seqlen=65536, nheads=32, dstate=128, chunk_size=256) == _ffi.SSD_ERR_SCRATCH_TOO_SMALL
     assert b"SCRATCH_TOO_SMALL" in lib.ssd_status_string(_ffi.SSD_ERR_SCRATCH_TOO_SMALL)
+
+
+def test_step_validation(lib):
+    def step(**kw):
+        a = dict(x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, state=FAKE, batch=2, nheads=4, headdim=64,
+                 ngroups=1, dstate=128, y=FAKE)
+        a.update(kw)
+        return lib.ssd_step(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["state"], a["batch"], a["nheads"],
+                            a["headdim"], a["ngroups"], a["dstate"], a["y"], None)
+    assert step(x=None) == _ffi.SSD_ERR_INVALID_ARG
+    assert step(state=None) == _ffi.SSD_ERR_INVALID_ARG
+    assert step(y=None) == _ffi.SSD_ERR_INVALID_ARG
+    assert step(batch=0) == _ffi.SSD_ERR_INVALID_ARG
+    assert step(ngroups=3) == _ffi.SSD_ERR_INVALID_ARG
+    assert step(state=FAKE + 4) == _ffi.SSD_ERR_INVALID_ARG
+    assert step(x=FAKE + 1) == _ffi.SSD_ERR_INVALID_ARG
+    assert step(headdim=32) == _ffi.SSD_ERR_UNSUPPORTED
+    assert step(dstate=96) == _ffi.SSD_ERR_UNSUPPORTED
