@@ -58,11 +58,14 @@ def _load():
             lib = ctypes.CDLL(_LIB_PATH)
             p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
             lib.ssd_oracle_forward.argtypes = [p] * 7 + [i64] * 7 + [p, i64, p, p, p, i32]
+            f64 = ctypes.c_double
+            lib.ssd_oracle_forward_opts.argtypes = ([p] * 7 + [i64] * 7 + [p, i32, i32, f64, f64, i32, p] +
+                                                    [p, i64, p, p, p, i32])
             lib.ssd_oracle_chunk_states.argtypes = [p] * 4 + [i64] * 7 + [p, i64, p, i32]
             lib.ssd_oracle_chunk_scan.argtypes = [p] * 7 + [i64] * 7 + [p, i64, p, i32]
             lib.ssd_oracle_dA_cumsum.argtypes = [p, p, i64, i64, i64, i64, p, p]
             lib.ssd_oracle_state_passing.argtypes = [p, p, p] + [i64] * 6 + [p, p]
-            for f in ("ssd_oracle_forward", "ssd_oracle_chunk_states", "ssd_oracle_chunk_scan",
+            for f in ("ssd_oracle_forward", "ssd_oracle_forward_opts", "ssd_oracle_chunk_states", "ssd_oracle_chunk_scan",
                       "ssd_oracle_dA_cumsum", "ssd_oracle_state_passing"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -98,17 +101,24 @@ def last_threads_used() -> int:
 _last_threads = [0]
 
 
-def forward(x, dt, A, B, C, D, init, chunk_size, units=None, want_chunk_starts=False, nthreads=0):
+def forward(x, dt, A, B, C, D, init, chunk_size, units=None, want_chunk_starts=False, nthreads=0,
+            dt_bias=None, dt_softplus=False, dt_limit=None, z=None):
     """Token-by-token fp64 recurrence.
 
     Returns dict with ``y`` (nunits, L, P), ``final`` (nunits, P, N) and,
     if requested, ``chunk_starts`` (nunits, nc, P, N): the state before each
     chunk of ``chunk_size`` tokens.  ``units`` lists b * H + h indices
     (default: all units, in order).
+
+    Input-side options of a whole layer (none by default): ``dt_bias`` (H,)
+    f32 added to dt, ``dt_softplus`` (dt <- log(1 + exp(dt))), ``dt_limit``
+    = (lo, hi) clamp applied last; D of shape (H, P) gives one skip weight
+    per channel; ``z`` (batch, L, H, P) bf16 bits gates y <- y z sigmoid(z).
     """
     x, B, C = _c(x, np.uint16), _c(B, np.uint16), _c(C, np.uint16)
     dt, A = _c(dt, np.float32), _c(A, np.float32)
     D, init = _c(D, np.float32), _c(init, np.float32)
+    dt_bias, z = _c(dt_bias, np.float32), _c(z, np.uint16)
     b, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     nc = -(-L // chunk_size)
@@ -116,9 +126,24 @@ def forward(x, dt, A, B, C, D, init, chunk_size, units=None, want_chunk_starts=F
     y = np.empty((u.size, L, P), np.float64)
     fin = np.empty((u.size, P, N), np.float64)
     cst = np.empty((u.size, nc, P, N), np.float64) if want_chunk_starts else None
-    r = _load().ssd_oracle_forward(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init),
-                                   b, L, H, P, G, N, chunk_size, _ptr(u), u.size,
-                                   _ptr(y), _ptr(fin), _ptr(cst), nthreads)
+    if D is not None and D.shape not in ((H,), (H, P)):
+        raise ValueError("D must be (H,) or (H, P)")
+    if z is not None and z.shape != x.shape:
+        raise ValueError("z must have x's shape")
+    if dt_bias is not None and dt_bias.shape != (H,):
+        raise ValueError("dt_bias must be (H,)")
+    plain = dt_bias is None and not dt_softplus and dt_limit is None and z is None and (D is None or D.ndim == 1)
+    if plain:
+        r = _load().ssd_oracle_forward(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init),
+                                       b, L, H, P, G, N, chunk_size, _ptr(u), u.size,
+                                       _ptr(y), _ptr(fin), _ptr(cst), nthreads)
+    else:
+        lo, hi = (0.0, 0.0) if dt_limit is None else (float(dt_limit[0]), float(dt_limit[1]))
+        r = _load().ssd_oracle_forward_opts(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init),
+                                            b, L, H, P, G, N, chunk_size,
+                                            _ptr(dt_bias), int(bool(dt_softplus)), int(dt_limit is not None), lo, hi,
+                                            int(D is not None and D.ndim == 2), _ptr(z),
+                                            _ptr(u), u.size, _ptr(y), _ptr(fin), _ptr(cst), nthreads)
     if r < 0:
         raise ValueError("ssd_oracle_forward: bad arguments")
     _last_threads[0] = r

@@ -115,11 +115,44 @@ static int run_units(unit_fn fn, void* ctx, int64_t nunits, int nthreads) {
  * state hs (N x P, updated in place).  If y is non-NULL, writes y rows
  * y[(t - t0) * P + p].  C/D may be NULL when y is NULL.
  */
+/*
+ * Input-side options of a whole Mamba-2 layer around the scan.  The pages
+ * take dt as given and D as one weight per head; these are the plainest
+ * readings of the steps a layer adds on either side, applied per token:
+ *
+ *     dt <- dt + dt_bias[h]                      (dt_bias non-NULL)
+ *     dt <- log(1 + exp(dt))                     (dt_softplus)
+ *     dt <- min(max(dt, dt_min), dt_max)         (dt_limit)
+ *     skip term D[h][p] x[p]                     (D_per_channel: D is (H, P))
+ *     y  <- y * z / (1 + exp(-z))                (z non-NULL, x's layout, bf16)
+ */
+typedef struct {
+    const float* dt_bias;
+    int dt_softplus, dt_limit;
+    double dt_min, dt_max;
+    int D_per_channel;
+    const uint16_t* z;
+} opts_t;
+
 typedef struct {
     const dims_t* d;
     const uint16_t *x, *B, *C;
     const float *dt, *A, *D;
+    const opts_t* opt; /* NULL: dt, D and y as they are */
 } inputs_t;
+
+/* log(1 + exp(v)) without overflow: for v > 0 it is v + log(1 + exp(-v)). */
+static double softplus_d(double v) {
+    return v > 0.0 ? v + log1p(exp(-v)) : log1p(exp(v));
+}
+
+static double effective_dt(const opts_t* o, int64_t h, double v) {
+    if (o == NULL) return v;
+    if (o->dt_bias != NULL) v += (double)o->dt_bias[h];
+    if (o->dt_softplus) v = softplus_d(v);
+    if (o->dt_limit) v = fmin(fmax(v, o->dt_min), o->dt_max);
+    return v;
+}
 
 static void recur_tokens(const inputs_t* in, int64_t b, int64_t h, int64_t t0, int64_t t1,
                          double* hs, double* y) {
@@ -127,12 +160,14 @@ static void recur_tokens(const inputs_t* in, int64_t b, int64_t h, int64_t t0, i
     const int64_t H = d->nheads, P = d->headdim, N = d->dstate, G = d->ngroups;
     const int64_t g = h / (H / G);
     const double A = (double)in->A[h];
-    const double Dh = (in->D != NULL) ? (double)in->D[h] : 0.0;
+    const opts_t* opt = in->opt;
+    const int d_per_p = (opt != NULL && opt->D_per_channel);
+    const uint16_t* z = (opt != NULL) ? opt->z : NULL;
     double* xv = (double*)malloc(sizeof(double) * (size_t)P);
     double* bv = (double*)malloc(sizeof(double) * (size_t)N);
     double* cv = (double*)malloc(sizeof(double) * (size_t)N);
     for (int64_t t = t0; t < t1; ++t) {
-        const double dt = (double)in->dt[(b * d->seqlen + t) * H + h];
+        const double dt = effective_dt(opt, h, (double)in->dt[(b * d->seqlen + t) * H + h]);
         const double a = exp(dt * A);
         const uint16_t* xr = in->x + ((b * d->seqlen + t) * H + h) * P;
         const uint16_t* br = in->B + ((b * d->seqlen + t) * G + g) * N;
@@ -147,11 +182,21 @@ static void recur_tokens(const inputs_t* in, int64_t b, int64_t h, int64_t t0, i
             const uint16_t* cr = in->C + ((b * d->seqlen + t) * G + g) * N;
             for (int64_t n = 0; n < N; ++n) cv[n] = bf16_to_double(cr[n]);
             double* yr = y + (t - t0) * P;
-            for (int64_t p = 0; p < P; ++p) yr[p] = Dh * xv[p];
+            for (int64_t p = 0; p < P; ++p) {
+                const double Dp = (in->D == NULL) ? 0.0 : (double)in->D[d_per_p ? h * P + p : h];
+                yr[p] = Dp * xv[p];
+            }
             for (int64_t n = 0; n < N; ++n) {
                 const double c = cv[n];
                 const double* row = hs + n * P;
                 for (int64_t p = 0; p < P; ++p) yr[p] += c * row[p];
+            }
+            if (z != NULL) {
+                const uint16_t* zr = z + ((b * d->seqlen + t) * H + h) * P;
+                for (int64_t p = 0; p < P; ++p) {
+                    const double zv = bf16_to_double(zr[p]);
+                    yr[p] *= zv / (1.0 + exp(-zv));
+                }
             }
         }
     }
@@ -215,7 +260,31 @@ int ssd_oracle_forward(const uint16_t* x, const float* dt, const float* A, const
         chunk_size <= 0 || nheads % ngroups != 0 || nunits <= 0)
         return -1;
     dims_t d = {batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size};
-    fwd_ctx_t ctx = {{&d, x, B, C, dt, A, D}, init, units, y, final_state, chunk_starts};
+    fwd_ctx_t ctx = {{&d, x, B, C, dt, A, D, NULL}, init, units, y, final_state, chunk_starts};
+    return run_units(fwd_unit, &ctx, nunits, nthreads);
+}
+
+/*
+ * ssd_oracle_forward_opts: ssd_oracle_forward with the input-side options
+ * (see opts_t): dt_bias (H) or NULL, dt_softplus, dt_limit with [dt_min,
+ * dt_max], D_per_channel (D is (H, P)), z (x's layout, bf16) or NULL.
+ */
+int ssd_oracle_forward_opts(const uint16_t* x, const float* dt, const float* A, const uint16_t* B,
+                            const uint16_t* C, const float* D, const float* init,
+                            int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                            int64_t ngroups, int64_t dstate, int64_t chunk_size,
+                            const float* dt_bias, int dt_softplus, int dt_limit, double dt_min, double dt_max,
+                            int D_per_channel, const uint16_t* z,
+                            const int64_t* units, int64_t nunits,
+                            double* y, double* final_state, double* chunk_starts, int nthreads) {
+    if (!x || !dt || !A || !B || !C || !units || !y) return -1;
+    if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0 ||
+        chunk_size <= 0 || nheads % ngroups != 0 || nunits <= 0)
+        return -1;
+    if (dt_limit && !(dt_min <= dt_max)) return -1;
+    dims_t d = {batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size};
+    opts_t o = {dt_bias, dt_softplus, dt_limit, dt_min, dt_max, D_per_channel, z};
+    fwd_ctx_t ctx = {{&d, x, B, C, dt, A, D, &o}, init, units, y, final_state, chunk_starts};
     return run_units(fwd_unit, &ctx, nunits, nthreads);
 }
 
@@ -258,7 +327,7 @@ int ssd_oracle_chunk_states(const uint16_t* x, const float* dt, const float* A, 
         chunk_size <= 0 || nheads % ngroups != 0 || nunits <= 0)
         return -1;
     dims_t d = {batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size};
-    cst_ctx_t ctx = {{&d, x, B, NULL, dt, A, NULL}, units, S};
+    cst_ctx_t ctx = {{&d, x, B, NULL, dt, A, NULL, NULL}, units, S};
     return run_units(cst_unit, &ctx, nunits, nthreads);
 }
 
@@ -302,7 +371,7 @@ int ssd_oracle_chunk_scan(const uint16_t* x, const float* dt, const float* A, co
         chunk_size <= 0 || nheads % ngroups != 0 || nunits <= 0)
         return -1;
     dims_t d = {batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size};
-    csc_ctx_t ctx = {{&d, x, B, C, dt, A, D}, states, units, y};
+    csc_ctx_t ctx = {{&d, x, B, C, dt, A, D, NULL}, states, units, y};
     return run_units(csc_unit, &ctx, nunits, nthreads);
 }
 

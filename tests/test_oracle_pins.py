@@ -252,3 +252,99 @@ def test_unit_subset_matches_full_run():
     sub = oracle.forward(i["x"], i["dt"], i["A"], i["B"], i["C"], i["D"], i["init"], 16, units=units)
     np.testing.assert_array_equal(sub["y"], full["y"][units])
     np.testing.assert_array_equal(sub["final"], full["final"][units])
+
+
+# ---------------------------------------------------------------- input-side options
+# dt_bias / softplus / clamp, D per channel and the z gate are not on the pages;
+# the oracle takes their plainest reading.  Each pin ties one option to a
+# different routine or a closed form (never to a retyped copy of itself).
+
+def _f32_of_bits(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _plain(i, Q, **kw):
+    a = dict(i)
+    a.update(kw)
+    return oracle.forward(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["init"], Q)
+
+
+def test_options_that_change_nothing_reproduce_the_plain_path():
+    w, i = _small(L=29, H=4, P=8, N=6, G=2)
+    ref = _plain(i, 16)
+    D2 = np.repeat(i["D"][:, None], w.headdim, axis=1)  # one weight per channel, equal to the head's
+    o = oracle.forward(i["x"], i["dt"], i["A"], i["B"], i["C"], D2, i["init"], 16,
+                       dt_bias=np.zeros(w.nheads, np.float32), dt_limit=(0.0, 1e30))
+    np.testing.assert_array_equal(o["y"], ref["y"])
+    np.testing.assert_array_equal(o["final"], ref["final"])
+
+
+def test_softplus_and_bias_undo_their_inverse():
+    """raw = log(expm1(d)) - bias: softplus(raw + bias) gives d back (numpy's expm1/log, not log1p/exp)."""
+    w, i = _small(L=33, H=4, P=8, N=6, G=2)
+    d = i["dt"].astype(np.float64)
+    bias = (np.random.default_rng(3).standard_normal(w.nheads) * 0.5).astype(np.float32)
+    raw = (np.log(np.expm1(d)) - bias.astype(np.float64)).astype(np.float32)
+    o = oracle.forward(i["x"], raw, i["A"], i["B"], i["C"], i["D"], i["init"], 16,
+                       dt_bias=bias, dt_softplus=True)
+    ref = _plain(i, 16)
+    np.testing.assert_allclose(o["y"], ref["y"], rtol=1e-4, atol=1e-7)
+    np.testing.assert_allclose(o["final"], ref["final"], rtol=1e-4, atol=1e-7)
+    # a large pre-activation passes through (softplus(v) -> v), a very negative one gives ~0
+    big = np.full_like(i["dt"], 40.0)
+    o2 = oracle.forward(i["x"], big, i["A"], i["B"], i["C"], i["D"], None, 16, dt_softplus=True)
+    np.testing.assert_allclose(o2["y"], _plain(i, 16, dt=big, init=None)["y"], rtol=1e-12, atol=1e-14)
+    o3 = oracle.forward(i["x"], np.full_like(i["dt"], -800.0), i["A"], i["B"], i["C"], i["D"], None, 16,
+                        dt_softplus=True)
+    np.testing.assert_allclose(o3["final"], 0.0, atol=1e-300)
+
+
+def test_dt_limit_clamps_last():
+    w, i = _small(L=40, H=4, P=8, N=6, G=2)
+    d = i["dt"]
+    lo, hi = np.float32(np.quantile(d, 0.25)), np.float32(np.quantile(d, 0.75))
+    # equal bounds: a constant step
+    o = oracle.forward(i["x"], d, i["A"], i["B"], i["C"], i["D"], i["init"], 16, dt_limit=(float(lo), float(lo)))
+    ref = _plain(i, 16, dt=np.full_like(d, lo))
+    np.testing.assert_allclose(o["y"], ref["y"], rtol=1e-12, atol=1e-14)
+    # after the softplus, not before: softplus(log(expm1(d))) clamped equals d clamped
+    raw = np.log(np.expm1(d.astype(np.float64))).astype(np.float32)
+    o = oracle.forward(i["x"], raw, i["A"], i["B"], i["C"], i["D"], i["init"], 16, dt_softplus=True,
+                       dt_limit=(float(lo), float(hi)))
+    ref = _plain(i, 16, dt=np.clip(d, lo, hi))
+    np.testing.assert_allclose(o["y"], ref["y"], rtol=1e-4, atol=1e-7)
+    np.testing.assert_allclose(o["final"], ref["final"], rtol=1e-4, atol=1e-7)
+
+
+def test_D_per_channel_closed_form():
+    """With C = 0 the output is the skip term alone: y[b,t,h,p] = D[h,p] x[b,t,h,p] (H != P catches a transpose)."""
+    w, i = _small(L=21, H=4, P=8, N=6, G=2)
+    D2 = np.random.default_rng(5).standard_normal((w.nheads, w.headdim)).astype(np.float32)
+    C0 = np.zeros_like(i["C"])
+    o = oracle.forward(i["x"], i["dt"], i["A"], i["B"], C0, D2, i["init"], 16)
+    y = _by_unit(o["y"], w.batch, w.nheads)                   # (b, H, L, P)
+    x = _f32_of_bits(i["x"]).transpose(0, 2, 1, 3)            # (b, H, L, P)
+    np.testing.assert_allclose(y, D2[None, :, None, :].astype(np.float64) * x, rtol=1e-15, atol=0)
+    # and it adds to the state-space term exactly as the per-head weight does (linearity in D)
+    ref0 = _plain(i, 16, D=None)
+    o = oracle.forward(i["x"], i["dt"], i["A"], i["B"], i["C"], D2, i["init"], 16)
+    np.testing.assert_allclose(_by_unit(o["y"] - ref0["y"], w.batch, w.nheads),
+                               D2[None, :, None, :].astype(np.float64) * x, rtol=1e-12, atol=1e-12)
+
+
+def test_z_gate_is_silu():
+    """silu is pinned by two identities: g(z) - g(-z) = z and g(z) + g(-z) = z tanh(z/2)."""
+    w, i = _small(L=25, H=4, P=8, N=6, G=2)
+    y0 = _plain(i, 16)
+    zf = np.random.default_rng(7).standard_normal(i["x"].shape).astype(np.float32) * 3
+    z = _bits(zf)
+    zneg = z ^ np.uint16(0x8000)                               # exact negation of a bf16 value
+    op = oracle.forward(i["x"], i["dt"], i["A"], i["B"], i["C"], i["D"], i["init"], 16, z=z)
+    on = oracle.forward(i["x"], i["dt"], i["A"], i["B"], i["C"], i["D"], i["init"], 16, z=zneg)
+    zz = _f32_of_bits(z).transpose(0, 2, 1, 3).reshape(w.batch * w.nheads, w.seqlen, w.headdim)
+    np.testing.assert_allclose(op["y"] - on["y"], zz * y0["y"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(op["y"] + on["y"], zz * np.tanh(zz / 2) * y0["y"], rtol=1e-12, atol=1e-13)
+    # the gate touches the output only: the carried state is the ungated one
+    np.testing.assert_array_equal(op["final"], y0["final"])
+    oz = oracle.forward(i["x"], i["dt"], i["A"], i["B"], i["C"], i["D"], i["init"], 16, z=np.zeros_like(z))
+    np.testing.assert_array_equal(oz["y"], 0.0)
