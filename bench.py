@@ -238,6 +238,9 @@ def main():
     # ---- the recurrent decode step on a serving batch of the workload's model
     decode = decode_measure(w, dev, stream, args, ssd, lib, flush)
 
+    # ---- the same forward with a whole layer's input-side options (dt bias/softplus/clamp, D per channel, z gate)
+    layer = layer_options_measure(w, d, dev, stream, args, ssd, lib, flush)
+
     if rank != 0:
         dist.destroy_process_group()
         return 0
@@ -292,6 +295,7 @@ def main():
         "gpu_launches": int(launches),
         "e2e": e2e,
         "decode_step": decode,
+        "layer_options": layer,
         "clocks": clk,
         "device_error": int(err),
     }
@@ -476,6 +480,54 @@ def e2e_measure(w, inp, dev, stream, args, ssd, dist):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4),
             "steps": n, "pipeline": "two buffer sets; H2D, compute and D2H on separate streams",
             "serial_ms_per_step": round(serial_ms, 4)}
+
+
+def layer_options_measure(w, d, dev, stream, args, ssd, lib, flush):
+    """ssd_forward_ex with every input-side option on the workload (inputs resident, L2 flushed between
+    steps outside the events).  Extra algorithmic bytes over the plain pass: the z read (bf16, x's size)."""
+    import torch
+    lo = I.make_layer_options(w, seed=0)
+    dt_raw, dt_bias, D_hp, z = (lo[k].to(dev) for k in ("dt_raw", "dt_bias", "D_hp", "z"))
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), device=dev, dtype=torch.float32)
+
+    def step():
+        ssd.ssd_forward_ex(d["x"], dt_raw, d["A"], d["B"], d["C"], D_hp, d["init"], w.chunk_size, dt_bias=dt_bias,
+                           dt_softplus=True, dt_limit=lo["dt_limit"], z=z, y=y, final_state=fin, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    steps = max(args.steps, 10)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    lib.ssd_profile_reset()
+    lib.ssd_profile_enable(1)
+    n0 = lib.ssd_launch_count()
+    for i in range(steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    launches = lib.ssd_launch_count() - n0
+    lib.ssd_profile_enable(0)
+    import ctypes
+    kms = (ctypes.c_float * 16)()
+    kcnt = (ctypes.c_int * 16)()
+    nk = ctypes.c_int(0)
+    lib.ssd_profile_read(kms, kcnt, 16, ctypes.byref(nk))
+    scan_us = None
+    for k in range(nk.value):
+        if lib.ssd_kernel_name(k).decode() == "chunk_scan" and kcnt[k] > 0:
+            scan_us = float(kms[k]) / kcnt[k] * 1e3
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / steps
+    return {"options": "dt_bias + softplus + dt_limit (0.001, 0.1), D per channel (H, P), z gate",
+            "ms_per_step": round(ms, 4), "tokens_per_s": round(w.batch * w.seqlen / (ms / 1e3), 1),
+            "chunk_scan_us": None if scan_us is None else round(scan_us, 2),
+            "extra_alg_bytes": float(w.batch * w.seqlen * w.nheads * w.headdim * 2 + w.nheads * 4 * (1 + w.headdim)),
+            "steps": steps, "gpu_launches": int(launches)}
 
 
 DECODE_BATCH = 256

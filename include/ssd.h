@@ -228,6 +228,59 @@ SSD_API int ssd_step(const void* x, const float* dt, const float* A, const void*
                      void* y, cudaStream_t stream);
 
 /*
+ * Input-side options of a whole Mamba-2 layer around the scan.  The pages
+ * take dt as already positive and D as one weight per head; these are the
+ * plainest reading of the steps a layer adds on either side, applied per
+ * token and head in this order:
+ *     dt <- dt + dt_bias[h]                    if dt_bias != NULL
+ *     dt <- log(1 + exp(dt))                   if dt_softplus
+ *     dt <- min(max(dt, dt_min), dt_max)       if dt_limit
+ *     skip term D[h][p] * x[p]                 if D_per_channel (D is (nheads, headdim))
+ *     y  <- y * z * sigmoid(z)                 if z != NULL (after the skip term)
+ * z has x's layout, bfloat16, 16-byte aligned for ssd_forward_ex (2-byte for
+ * ssd_step_ex); a per-channel D is 16-byte aligned for ssd_forward_ex.
+ * dt_bias is (nheads) float32.  A zero-filled struct (or a
+ * NULL pointer) selects none of them.  The options change only the inputs
+ * and the output: the carried state is never gated.
+ */
+typedef struct ssd_input_options {
+    const float* dt_bias;
+    int dt_softplus;
+    int dt_limit;
+    float dt_min;
+    float dt_max;
+    int D_per_channel;
+    const void* z;
+} ssd_input_options;
+
+/*
+ * ssd_forward_ex -- ssd_forward with the input-side options above (options
+ * may be NULL: then it is ssd_forward).  The dt transform is applied where
+ * dt is first read (chunk_cumsum), so every later stage sees the effective
+ * dt.  A per-channel D enters compute_out as one more tensor-core product,
+ * Y += X diag(D), so D is rounded to float16 there (11 significant bits; D
+ * beyond the float16 range saturates); the z gate is applied in
+ * compute_out's epilogue, in fp32.
+ * Extra errors: SSD_ERR_INVALID_ARG if dt_limit is set with dt_min > dt_max
+ * or a NaN bound, if z or a per-channel D is not 16-byte aligned, or dt_bias
+ * not 4-byte aligned.
+ */
+SSD_API int ssd_forward_ex(const void* x, const float* dt, const float* A, const void* B, const void* C,
+                           const float* D, const float* init_state, int batch, int seqlen, int nheads,
+                           int headdim, int ngroups, int dstate, int chunk_size,
+                           const ssd_input_options* options, void* y, float* final_state,
+                           cudaStream_t stream);
+
+/*
+ * ssd_step_ex -- ssd_step with the input-side options (NULL: ssd_step).
+ * With D_per_channel, D is (nheads, headdim); z is (batch, nheads, headdim)
+ * bfloat16.  Errors as ssd_step plus those of ssd_forward_ex's options.
+ */
+SSD_API int ssd_step_ex(const void* x, const float* dt, const float* A, const void* B, const void* C,
+                        const float* D, float* state, int batch, int nheads, int headdim, int ngroups,
+                        int dstate, const ssd_input_options* options, void* y, cudaStream_t stream);
+
+/*
  * ssd_get_device_error -- reads and clears the library's device error word
  * on the current device (synchronizes with the device).  Returns SSD_OK, or
  * SSD_ERR_TIMEOUT if a kernel's bounded wait gave up since the last read, or

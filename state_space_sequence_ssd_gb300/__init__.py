@@ -18,7 +18,7 @@ from __future__ import annotations
 from . import _ffi
 
 __all__ = ["ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_forward",
-           "ssd_forward_noalloc", "ssd_step",
+           "ssd_forward_noalloc", "ssd_step", "ssd_forward_ex", "ssd_step_ex",
            "ssd_get_device_error", "SSDError", "library_path"]
 
 SSDError = _ffi.SSDError
@@ -160,6 +160,86 @@ def ssd_forward(x, dt, A, B, C, D, init_state, chunk_size, y=None, final_state=N
         _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
         b, L, H, P, G, N, chunk_size, _ptr(y), _ptr(final_state), _stream(stream)))
     return y, final_state
+
+
+def _options(x, D, dt_bias, dt_softplus, dt_limit, z, H, P):
+    """ssd_input_options from keyword arguments; D may be (H,) or (H, P) (one weight per channel)."""
+    torch = _torch()
+    _opt(dt_bias, "dt_bias", torch.float32, 1)
+    _opt(z, "z", torch.bfloat16, x.dim())
+    if dt_bias is not None and tuple(dt_bias.shape) != (H,):
+        raise ValueError(f"dt_bias must have shape {(H,)}, got {tuple(dt_bias.shape)}")
+    if z is not None and tuple(z.shape) != tuple(x.shape):
+        raise ValueError(f"z must have x's shape {tuple(x.shape)}, got {tuple(z.shape)}")
+    if D is not None:
+        _need(D, "D", torch.float32)
+        if tuple(D.shape) not in ((H,), (H, P)):
+            raise ValueError(f"D must have shape {(H,)} or {(H, P)}, got {tuple(D.shape)}")
+    o = _ffi.InputOptions()
+    o.dt_bias = _ptr(dt_bias)
+    o.dt_softplus = int(bool(dt_softplus))
+    if dt_limit is not None:
+        o.dt_limit = 1
+        o.dt_min, o.dt_max = float(dt_limit[0]), float(dt_limit[1])
+    o.D_per_channel = int(D is not None and D.dim() == 2)
+    o.z = _ptr(z)
+    return o
+
+
+def ssd_forward_ex(x, dt, A, B, C, D, init_state, chunk_size, dt_bias=None, dt_softplus=False, dt_limit=None,
+                   z=None, y=None, final_state=None, want_final=True, stream=None):
+    """ssd_forward with a whole layer's input-side options:
+    dt <- clamp(softplus(dt + dt_bias), *dt_limit) (each part optional), D of shape (H,) or (H, P)
+    (one skip weight per channel), and y <- y * z * sigmoid(z) with z shaped like x.
+    Returns (y, final_state or None); the state is never gated."""
+    import ctypes
+    torch = _torch()
+    _need(x, "x", torch.bfloat16, 4)
+    _need(dt, "dt", torch.float32, 3)
+    _need(A, "A", torch.float32, 1)
+    _need(B, "B", torch.bfloat16, 4)
+    _need(C, "C", torch.bfloat16, 4)
+    _opt(init_state, "init_state", torch.float32, 4)
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    opts = _options(x, D, dt_bias, dt_softplus, dt_limit, z, H, P)
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and want_final:
+        final_state = torch.empty((b, H, P, N), device=x.device, dtype=torch.float32)
+    _need(y, "y", torch.bfloat16, 4)
+    _opt(final_state, "final_state", torch.float32, 4)
+    _ffi.check("ssd_forward_ex", _ffi.lib().ssd_forward_ex(
+        _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
+        b, L, H, P, G, N, chunk_size, ctypes.addressof(opts), _ptr(y), _ptr(final_state), _stream(stream)))
+    return y, final_state
+
+
+def ssd_step_ex(x, dt, A, B, C, D, state, dt_bias=None, dt_softplus=False, dt_limit=None, z=None, y=None,
+                stream=None):
+    """ssd_step with the input-side options of ssd_forward_ex (z shaped like x: (batch, H, P))."""
+    import ctypes
+    torch = _torch()
+    _need(x, "x", torch.bfloat16, 3)
+    _need(dt, "dt", torch.float32, 2)
+    _need(A, "A", torch.float32, 1)
+    _need(B, "B", torch.bfloat16, 3)
+    _need(C, "C", torch.bfloat16, 3)
+    _need(state, "state", torch.float32, 4)
+    b, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    opts = _options(x, D, dt_bias, dt_softplus, dt_limit, z, H, P)
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", torch.bfloat16, 3)
+    for name, t, shape in (("dt", dt, (b, H)), ("A", A, (H,)), ("B", B, (b, G, N)), ("C", C, (b, G, N)),
+                           ("state", state, (b, H, P, N)), ("y", y, (b, H, P))):
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+    _ffi.check("ssd_step_ex", _ffi.lib().ssd_step_ex(
+        _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(state), b, H, P, G, N,
+        ctypes.addressof(opts), _ptr(y), _stream(stream)))
+    return y
 
 
 def ssd_forward_noalloc(x, dt, A, B, C, D, init_state, chunk_size, y, final_state=None, stream=None):

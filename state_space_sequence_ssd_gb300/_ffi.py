@@ -32,6 +32,8 @@ SIGNATURES = {
     "ssd_forward": (_i, [_p] * 7 + [_i] * 7 + [_p, _p, _p]),
     "ssd_forward_noalloc": (_i, [_p] * 7 + [_i] * 7 + [_p, _p, _p]),
     "ssd_step": (_i, [_p] * 7 + [_i] * 5 + [_p, _p]),
+    "ssd_forward_ex": (_i, [_p] * 7 + [_i] * 7 + [_p, _p, _p, _p]),
+    "ssd_step_ex": (_i, [_p] * 7 + [_i] * 5 + [_p, _p, _p]),
     "ssd_get_device_error": (_i, []),
     "ssd_profile_enable": (_i, [_i]),
     "ssd_profile_reset": (_i, []),
@@ -39,6 +41,15 @@ SIGNATURES = {
     "ssd_kernel_name": (ctypes.c_char_p, [_i]),
     "ssd_launch_count": (ctypes.c_longlong, []),
 }
+
+
+
+class InputOptions(ctypes.Structure):
+    """struct ssd_input_options (field order and types as in include/ssd.h)."""
+    _fields_ = [("dt_bias", ctypes.c_void_p), ("dt_softplus", ctypes.c_int), ("dt_limit", ctypes.c_int),
+                ("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float), ("D_per_channel", ctypes.c_int),
+                ("z", ctypes.c_void_p)]
+
 
 _lock = threading.Lock()
 _lib = None

@@ -20,6 +20,34 @@ struct Dims {
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// The dt transform of the input-side options (ssd_input_options): bias, then
+// softplus, then clamp; identity when nothing is set.
+struct DtOpts {
+    const float* bias = nullptr;  // (H) or nullptr
+    int softplus = 0;
+    int limit = 0;
+    float lo = 0.f, hi = 0.f;
+    __host__ __device__ bool active() const { return bias != nullptr || softplus != 0 || limit != 0; }
+};
+
+// log(1 + exp(v)) written as max(v, 0) + log(1 + exp(-|v|)), which never overflows.
+__device__ __forceinline__ float effective_dt(float v, int h, const DtOpts& o) {
+    if (o.bias != nullptr) v += __ldg(o.bias + h);
+    if (o.softplus) v = fmaxf(v, 0.f) + log1pf(expf(-fabsf(v)));
+    if (o.limit) v = fminf(fmaxf(v, o.lo), o.hi);
+    return v;
+}
+
+// Output-side options: one skip weight per channel (D is (H, P)) and the z gate.
+struct OutOpts {
+    const float* Dp = nullptr;            // (H, P) or nullptr
+    const __nv_bfloat16* z = nullptr;     // x's layout or nullptr
+};
+
+// z sigmoid(z) = z / (1 + exp(-z)), with the approximate division: for z < -87 the
+// denominator exceeds 2^126 and the quotient is 0, the function's limit.
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
+
 // Kernel kinds, for the profiling counters (names in ssd_api.cu).
 enum KernelKind {
     kKindCumsum = 0,
@@ -46,7 +74,8 @@ int launch_chunk_cumsum(const float* dt, const float* A, const Dims& d, float* c
                         cudaStream_t s);
 // chunk_cumsum plus, in the same launch, the float16 copies of B and C
 int launch_chunk_cumsum_bc(const float* dt, const float* A, const Dims& d, float* cs, float* dtt,
-                           const __nv_bfloat16* B, const __nv_bfloat16* C, __half* B16, __half* C16, cudaStream_t s);
+                           const __nv_bfloat16* B, const __nv_bfloat16* C, __half* B16, __half* C16, cudaStream_t s,
+                           const DtOpts& dto = DtOpts());
 // B, C (bf16) -> float16 copies for the tensor-core products (see k_convert.cu)
 int launch_bc_to_f16(const __nv_bfloat16* B, const __nv_bfloat16* C, const Dims& d, __half* B16, __half* C16,
                      cudaStream_t s);
@@ -61,11 +90,12 @@ int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_ste
                                cudaStream_t s);
 int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C,
                            const float* dtt, const float* cs, const float* D, const float* span_states,
-                           int span_chunks, const Dims& d, __nv_bfloat16* y, int* err, cudaStream_t s);
+                           int span_chunks, const Dims& d, __nv_bfloat16* y, int* err, cudaStream_t s,
+                           const OutOpts& oo = OutOpts());
 
 // one recurrent step for every (batch, head): state updated in place, y for the token (k_step.cu)
 int launch_step(const __nv_bfloat16* x, const float* dt, const float* A, const __nv_bfloat16* B,
                 const __nv_bfloat16* C, const float* D, float* state, int batch, int nheads, int ngroups, int dstate,
-                __nv_bfloat16* y, cudaStream_t s);
+                __nv_bfloat16* y, cudaStream_t s, const DtOpts& dto = DtOpts(), const OutOpts& oo = OutOpts());
 
 }  // namespace ssd

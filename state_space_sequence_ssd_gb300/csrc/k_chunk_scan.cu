@@ -21,6 +21,9 @@
 //   CB   : CB   = C B^T                        (128 x 128, f32 in TMEM)
 //   mask : M    = CB * 2^(u_i - u_j) dt_j [j <= i] + D [j == i]   (float16, back into TMEM)
 //   MX   : Y    = M X                          (A operand read from TMEM; includes the D skip)
+//   DX   : Y   += X diag(D)                    (only with one skip weight per channel: D is
+//                                               (H, P); X as a K-major A operand, diag(D) a
+//                                               float16 64 x 64 tile built once per CTA)
 //   y_i  = Y_i + 2^(u_i) Yst_i
 //
 // The mask never exponentiates more than a 32 x 32 diagonal block per row:
@@ -35,7 +38,9 @@
 //               float16 copy of the state for C h and the decay of the state
 //               held in TMEM
 //   warps 8-11  epilogue warpgroup: y = Y + 2^u Yst, each thread storing its
-//               128-byte row of y straight from registers
+//               128-byte row of y straight from registers; with the z gate
+//               it multiplies by z sigmoid(z), the thread's z row loaded into
+//               registers one sub-block ahead
 //   warp 12     producer of the x tiles and dA_cumsum/dt rows (TMA)
 //   warp 13     TMEM owner and single-thread MMA issuer
 //   warp 14     producer of the C and B tiles (TMA), running ahead independently
@@ -66,7 +71,7 @@ constexpr int kThreads = 480;
 constexpr int kTile = 16384;  // 128 rows x 128 B
 constexpr int kWarpTma = 12, kWarpMma = 13, kWarpTmaBC = 14;
 
-template <int N>
+template <int N, bool OPT>
 struct Cfg {
     static constexpr int NB = N < 128 ? N : 128;  // state rows per n-block
     static constexpr int NBLK = N / NB;
@@ -94,7 +99,8 @@ struct Cfg {
     static constexpr int SZ_ZERO = (N == 64) ? kTile : 0;
     static constexpr int OFF_U = OFF_ZERO + SZ_ZERO;  // 3 x {u[128], dt[128], bcol[128], -[128]}
     static constexpr int OFF_CD = OFF_U + 3 * 2048;   // NX x {cs[128], dt[128]} rows, bulk-copied with x
-    static constexpr int OFF_BAR = OFF_CD + NX * 1024;
+    static constexpr int OFF_DG = OFF_CD + NX * 1024;  // diag(D) 64 x 64 float16, K-major, 128B-swizzled
+    static constexpr int OFF_BAR = OFF_DG + (OPT ? 8192 : 0);
     static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + alignment slack
     static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -103,6 +109,7 @@ constexpr uint32_t kIdescCB = idesc_fp16(128, 128, false, false);
 constexpr uint32_t kIdescYS = idesc_fp16(128, 64, false, true);
 constexpr uint32_t kIdescS = idesc_fp16(128, 64, true, true);
 constexpr uint32_t kIdescMX = idesc_fp16(128, 64, false, true);
+constexpr uint32_t kIdescDX = idesc_fp16(128, 64, false, false);
 
 struct ScanArgs {
     Dims d;
@@ -110,10 +117,11 @@ struct ScanArgs {
     int nspans;
     const float* cs;    // (b, H, nc, Q)
     const float* dtt;   // (b, H, nc, Q)
-    const float* D;     // (H) or null
+    const float* D;     // (H) or null: the skip term on M's diagonal
     const float* init;  // (b, nspans, H, P, N) span-start states
     __nv_bfloat16* y;   // (b, L, H, P)
     int* err;
+    OutOpts oo;  // D per channel (then D is null: no diagonal skip) and the z gate
 };
 
 struct Bars {
@@ -123,6 +131,18 @@ struct Bars {
     uint64_t cb_full[2], m_ready[2], y_full[2], y_free[2];
     uint64_t xs_ready, xs_free, h_ready, state_done, final_mma;
 };
+
+static_assert(sizeof(Bars) <= 512, "barriers fit their shared-memory slot");
+
+// Eight consecutive channels of one output row times z sigmoid(z); zq holds the row's eight bf16 gate values.
+__device__ __forceinline__ void gate8(float (&o)[8], const uint4& zq) {
+    const uint32_t* zw = reinterpret_cast<const uint32_t*>(&zq);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t w = zw[i >> 1];
+        o[i] *= silu(__uint_as_float((i & 1) ? (w & 0xffff0000u) : (w << 16)));
+    }
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -141,11 +161,13 @@ __device__ __forceinline__ float sub_block_decay(const float* scs, float prev, i
     return ((p0 + i) / Q == 0) ? (scs[i] - prev) : ((scs[Q - 1 - p0] - prev) + scs[i]);
 }
 
-template <int N>
+// OPT: the layer's output options (D per channel, z gate) are compiled in; the plain
+// instantiation carries none of their code, registers or shared memory.
+template <int N, bool OPT>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
                          const __grid_constant__ CUtensorMap tm_C, ScanArgs a) {
-    using K = Cfg<N>;
+    using K = Cfg<N, OPT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars* bar = reinterpret_cast<Bars*>(smem + K::OFF_BAR);
@@ -188,6 +210,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (K::SZ_ZERO > 0) {  // rows that pad the state-update A operand to 128 (N = 64)
         uint4* z = reinterpret_cast<uint4*>(smem + K::OFF_ZERO);
         for (int i = threadIdx.x; i < K::SZ_ZERO / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    if (OPT && a.oo.Dp != nullptr) {
+        // diag(D[h, :]) as the B operand of DX: row n (output channel) holds D[h][n] at column k = n.
+        // 128B swizzle: row n at (n / 8) * 1024 + (n % 8) * 128, 16-byte chunk j stored at chunk j ^ (n % 8).
+        for (int c = threadIdx.x; c < 512; c += kThreads) {
+            const int n = (c >> 6) * 8 + ((c >> 3) & 7);
+            const int j = (c & 7) ^ (n & 7);  // logical chunk: columns 8j .. 8j+7
+            uint32_t v = 0u;  // the diagonal element, placed in its 32-bit word of the chunk
+            if (j == (n >> 3)) {
+                const __half dv = __float2half_rn(a.oo.Dp[h * 64 + n]);
+                const uint32_t bits = *reinterpret_cast<const uint16_t*>(&dv);
+                v = (n & 1) ? (bits << 16) : bits;
+            }
+            const int wi = (n & 7) >> 1;
+            reinterpret_cast<uint4*>(smem + K::OFF_DG)[c] =
+                make_uint4(wi == 0 ? v : 0u, wi == 1 ? v : 0u, wi == 2 ? v : 0u, wi == 3 ? v : 0u);
+        }
         fence_proxy_async_smem();
     }
     if (warp == kWarpMma) {
@@ -263,6 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sXs = smem_u32(smem + K::OFF_XS);
             const uint32_t sZero = smem_u32(smem + K::OFF_ZERO);
             const uint32_t sH = smem_u32(smem + K::OFF_H);
+            const uint32_t sDg = smem_u32(smem + K::OFF_DG);
+            const bool dx = OPT && a.oo.Dp != nullptr;
             auto stage_c = [&](int st) -> uint32_t { return smem_u32(smem + K::OFF_BC + st * K::SZ_STAGE); };
             // h[nb] += B_nb^T X'  (K = tokens; A MN-major over two 64-row n boxes)
             auto issue_s = [&](int nb, uint32_t sB) {
@@ -298,6 +340,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(set + 64, set + kk * 8, desc_sw128(sX + kk * 2048, 16, 1024), kIdescMX, kk > 0);
+                if (dx) {  // Y += X diag(D): the same tile read as a K-major A operand (K = channels)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(set + 64, desc_sw128(sX + kk * 32, 16, 1024), desc_sw128(sDg + kk * 32, 16, 1024),
+                               kIdescDX, 1);
+                }
                 mma_commit(&bar->y_full[k]);
                 mma_commit(&bar->x_empty[q % K::NX]);
             };
@@ -579,6 +627,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ epilogue warpgroup
         const int r = threadIdx.x - 256;  // TMEM lane (warp % 4 == warp - 8)
         const uint32_t lane_base = (uint32_t)((warp - 8) * 32) << 16;
+        const bool gate = OPT && a.oo.z != nullptr;  // uniform over the CTA
+        uint4 zq[8];                                 // this thread's z row of the coming sub-block
+        if (gate && r < min((int64_t)128, te - ts)) {
+            const uint4* zr = reinterpret_cast<const uint4*>(a.oo.z + (((int64_t)b * d.seqlen + ts + r) * H + h) * 64);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) zq[i] = __ldg(zr + i);
+        }
         bool ok = true;
         for (int sb = 0; sb < nsb; ++sb) {
             const int64_t t0 = ts + sb * 128;
@@ -592,7 +647,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&bar->u_free[ub]);
             if (ok) {
                 const uint32_t set = tm + lane_base + K::T_SET + k * K::SET;
-                uint4* yrow = reinterpret_cast<uint4*>(a.y + (((int64_t)b * d.seqlen + t0 + r) * H + h) * 64);
+                const int64_t row = (((int64_t)b * d.seqlen + t0 + r) * H + h) * 64;
+                uint4* yrow = reinterpret_cast<uint4*>(a.y + row);
 #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
                     uint32_t yv[32], sv[32];
@@ -607,20 +663,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (r < nv) {
 #pragma unroll
                         for (int ch = 0; ch < 4; ++ch) {
+                            float o[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                o[i] = __uint_as_float(yv[ch * 8 + i]) + e * __uint_as_float(sv[ch * 8 + i]);
+                            if (gate) gate8(o, zq[ch]);
                             uint4 ov;
                             uint32_t* o4 = reinterpret_cast<uint32_t*>(&ov);
 #pragma unroll
-                            for (int e2 = 0; e2 < 4; ++e2) {
-                                const int c = ch * 8 + e2 * 2;
-                                o4[e2] = pack_bf16x2(__uint_as_float(yv[c]) + e * __uint_as_float(sv[c]),
-                                                     __uint_as_float(yv[c + 1]) + e * __uint_as_float(sv[c + 1]));
-                            }
+                            for (int e2 = 0; e2 < 4; ++e2) o4[e2] = pack_bf16x2(o[2 * e2], o[2 * e2 + 1]);
                             yrow[half * 4 + ch] = ov;
                         }
                     }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) zq[i] = zq[i + 4];  // the row's second half moves down
                 }
             } else {
                 mbar_arrive(&bar->y_free[k]);
+            }
+            if (gate && t0 + 128 + r < te) {  // the next sub-block's z row, in flight during the next wait
+                const uint4* zr =
+                    reinterpret_cast<const uint4*>(a.oo.z + (((int64_t)b * d.seqlen + t0 + 128 + r) * H + h) * 64);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) zq[i] = __ldg(zr + i);
             }
         }
     }
@@ -631,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpMma) tmem_dealloc(tm, K::TCOLS);
 }
 
-template <int N>
+template <int N, bool OPT>
 int launch_scan_n(const __nv_bfloat16* x, const __half* B, const __half* C, const ScanArgs& a, cudaStream_t s) {
     const Dims& d = a.d;
     CUtensorMap tx, tb, tc;
@@ -641,12 +706,12 @@ int launch_scan_n(const __nv_bfloat16* x, const __half* B, const __half* C, cons
     if (!make_tmap_16b_4d(&tx, x, dx, box_in) || !make_tmap_16b_4d(&tb, B, dbc, box_in) ||
         !make_tmap_16b_4d(&tc, C, dbc, box_in))
         return SSD_ERR_CUDA;
-    const int smem = Cfg<N>::SMEM;
-    if (ensure_smem_limit(reinterpret_cast<const void*>(chunk_scan_tc_kernel<N>), smem) != SSD_OK)
+    const int smem = Cfg<N, OPT>::SMEM;
+    if (ensure_smem_limit(reinterpret_cast<const void*>(chunk_scan_tc_kernel<N, OPT>), smem) != SSD_OK)
         return SSD_ERR_CUDA;
     dim3 grid(d.nheads, a.nspans, d.batch);
     launch_begin(kKindChunkScan, s);
-    chunk_scan_tc_kernel<N><<<grid, kThreads, smem, s>>>(tx, tb, tc, a);
+    chunk_scan_tc_kernel<N, OPT><<<grid, kThreads, smem, s>>>(tx, tb, tc, a);
     return launch_end(kKindChunkScan, s);
 }
 
@@ -654,7 +719,7 @@ int launch_scan_n(const __nv_bfloat16* x, const __half* B, const __half* C, cons
 
 int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C, const float* dtt,
                            const float* cs, const float* D, const float* span_states, int span_chunks, const Dims& d,
-                           __nv_bfloat16* y, int* err, cudaStream_t s) {
+                           __nv_bfloat16* y, int* err, cudaStream_t s, const OutOpts& oo) {
     ScanArgs a;
     a.d = d;
     a.span_chunks = span_chunks;
@@ -665,11 +730,14 @@ int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half
     a.init = span_states;
     a.y = y;
     a.err = err;
+    a.oo = oo;
+    if (oo.Dp != nullptr) a.D = nullptr;  // the skip moves from M's diagonal to the X diag(D) product
+    const bool opt = oo.Dp != nullptr || oo.z != nullptr;
     switch (d.dstate) {
-        case 64: return launch_scan_n<64>(x, B, C, a, s);
-        case 128: return launch_scan_n<128>(x, B, C, a, s);
-        case 256: return launch_scan_n<256>(x, B, C, a, s);
-        case 512: return launch_scan_n<512>(x, B, C, a, s);
+        case 64: return opt ? launch_scan_n<64, true>(x, B, C, a, s) : launch_scan_n<64, false>(x, B, C, a, s);
+        case 128: return opt ? launch_scan_n<128, true>(x, B, C, a, s) : launch_scan_n<128, false>(x, B, C, a, s);
+        case 256: return opt ? launch_scan_n<256, true>(x, B, C, a, s) : launch_scan_n<256, false>(x, B, C, a, s);
+        case 512: return opt ? launch_scan_n<512, true>(x, B, C, a, s) : launch_scan_n<512, false>(x, B, C, a, s);
         default: return SSD_ERR_UNSUPPORTED;
     }
 }

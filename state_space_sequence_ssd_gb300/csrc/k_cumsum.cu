@@ -11,6 +11,9 @@
 // serial in-lane prefix + warp-shuffle scan of the lane totals) and writes
 // its (batch, H, nchunks, Q) rows with 16-byte stores.
 //
+// With a layer's input-side options the dt tile is transformed as it is read
+// (bias, softplus, clamp), so dt_t and every later stage see the effective dt.
+//
 // Optionally the same launch also writes the float16 copies of B and C that
 // the tensor-core stages use (k_convert.cu explains why): the B/C elements
 // are split evenly over all CTAs of the grid.
@@ -35,7 +38,8 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
                                                                 float* __restrict__ cs, float* __restrict__ dtt,
                                                                 const uint4* __restrict__ bsrc,
                                                                 const uint4* __restrict__ csrc, uint4* __restrict__ bdst,
-                                                                uint4* __restrict__ cdst, int64_t bc16) {
+                                                                uint4* __restrict__ cdst, int64_t bc16,
+                                                                DtOpts dto) {
     // tile[h][i + i / 8]: one padding word per 8 positions, so that lanes reading runs of
     // consecutive positions spread over the banks
     __shared__ float tile[kHeads][Q + Q / 8];
@@ -55,6 +59,11 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
             } else {
 #pragma unroll
                 for (int k = 0; k < kHeads; ++k) v[k] = (h0 + k < d.nheads) ? __ldg(src + k) : 0.f;
+            }
+            if (dto.active()) {  // the layer's dt transform, on real positions only (padding stays 0)
+#pragma unroll
+                for (int k = 0; k < kHeads; ++k)
+                    if (h0 + k < d.nheads) v[k] = effective_dt(v[k], h0 + k, dto);
             }
         } else {
 #pragma unroll
@@ -126,7 +135,8 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
 }  // namespace
 
 int launch_chunk_cumsum_bc(const float* dt, const float* A, const Dims& d, float* cs, float* dtt,
-                           const __nv_bfloat16* B, const __nv_bfloat16* C, __half* B16, __half* C16, cudaStream_t s) {
+                           const __nv_bfloat16* B, const __nv_bfloat16* C, __half* B16, __half* C16, cudaStream_t s,
+                           const DtOpts& dto) {
     dim3 grid(d.nchunks, ceil_div(d.nheads, kHeads), d.batch);
     const int64_t bc16 = (B != nullptr) ? (int64_t)d.batch * d.seqlen * d.ngroups * d.dstate / 8 : 0;
     const uint4* bs = reinterpret_cast<const uint4*>(B);
@@ -135,9 +145,9 @@ int launch_chunk_cumsum_bc(const float* dt, const float* A, const Dims& d, float
     uint4* cd = reinterpret_cast<uint4*>(C16);
     launch_begin(kKindCumsum, s);
     switch (d.chunk_size) {
-        case 64: chunk_cumsum_kernel<64><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16); break;
-        case 128: chunk_cumsum_kernel<128><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16); break;
-        case 256: chunk_cumsum_kernel<256><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16); break;
+        case 64: chunk_cumsum_kernel<64><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, dto); break;
+        case 128: chunk_cumsum_kernel<128><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, dto); break;
+        case 256: chunk_cumsum_kernel<256><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, dto); break;
         default: return SSD_ERR_UNSUPPORTED;
     }
     return launch_end(kKindCumsum, s);

@@ -16,12 +16,23 @@
 // (each lane four consecutive n per 128 n, one float4 load and store per 128 n)
 // and reduces the row's dot product with C by warp shuffles.  The state is
 // read and written once: the step is bound by HBM.  fp32 throughout.
+//
+// With a layer's input-side options, dt is transformed first (bias, softplus,
+// clamp), the skip weight may be one per channel (D is (H, P)) and y is gated
+// by z sigmoid(z); the state itself is never gated.
 #include "common.cuh"
 
 namespace ssd {
 namespace {
 
 constexpr int kThreads = 256;
+
+// y = C.state + D x, then the optional gate; hp indexes (H, P) weights, i the (batch, H, P) rows
+__device__ __forceinline__ float step_output(float acc, float xp, float Dh, int64_t hp, int64_t i, const OutOpts& oo) {
+    float v = acc + ((oo.Dp != nullptr) ? oo.Dp[hp] : Dh) * xp;
+    if (oo.z != nullptr) v *= silu(__bfloat162float(oo.z[i]));
+    return v;
+}
 
 template <int N>
 __global__ void __launch_bounds__(kThreads) ssd_step_kernel(const __nv_bfloat16* __restrict__ x,
@@ -30,14 +41,15 @@ __global__ void __launch_bounds__(kThreads) ssd_step_kernel(const __nv_bfloat16*
                                                             const __nv_bfloat16* __restrict__ B,
                                                             const __nv_bfloat16* __restrict__ C,
                                                             const float* __restrict__ D, float* __restrict__ state,
-                                                            int nheads, int ngroups, __nv_bfloat16* __restrict__ y) {
+                                                            int nheads, int ngroups, __nv_bfloat16* __restrict__ y,
+                                                            DtOpts dto, OutOpts oo) {
     constexpr int P = 64;
     constexpr int NV = N / 128;  // float4 per lane per row
     const int h = blockIdx.x, b = blockIdx.y;
     const int g = h / (nheads / ngroups);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t bh = (int64_t)b * nheads + h;
-    const float dtv = dt[bh];
+    const float dtv = dto.active() ? effective_dt(dt[bh], h, dto) : dt[bh];
     const float a = expf(dtv * A[h]);
     const float Dh = (D != nullptr) ? D[h] : 0.f;
     // this lane's B and C entries: n = 128 v + 4 lane + e
@@ -75,7 +87,7 @@ __global__ void __launch_bounds__(kThreads) ssd_step_kernel(const __nv_bfloat16*
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) y[bh * P + p] = __float2bfloat16_rn(acc + Dh * xp);
+        if (lane == 0) y[bh * P + p] = __float2bfloat16_rn(step_output(acc, xp, Dh, h * P + p, bh * P + p, oo));
     }
 }
 
@@ -86,14 +98,15 @@ __global__ void __launch_bounds__(kThreads) ssd_step_kernel_n64(const __nv_bfloa
                                                                 const __nv_bfloat16* __restrict__ B,
                                                                 const __nv_bfloat16* __restrict__ C,
                                                                 const float* __restrict__ D, float* __restrict__ state,
-                                                                int nheads, int ngroups, __nv_bfloat16* __restrict__ y) {
+                                                                int nheads, int ngroups, __nv_bfloat16* __restrict__ y,
+                                                                DtOpts dto, OutOpts oo) {
     constexpr int P = 64, N = 64;
     const int h = blockIdx.x, b = blockIdx.y;
     const int g = h / (nheads / ngroups);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int half = lane >> 4, l16 = lane & 15;
     const int64_t bh = (int64_t)b * nheads + h;
-    const float dtv = dt[bh];
+    const float dtv = dto.active() ? effective_dt(dt[bh], h, dto) : dt[bh];
     const float a = expf(dtv * A[h]);
     const float Dh = (D != nullptr) ? D[h] : 0.f;
     const __nv_bfloat16* Bg = B + ((int64_t)b * ngroups + g) * N;
@@ -123,7 +136,7 @@ __global__ void __launch_bounds__(kThreads) ssd_step_kernel_n64(const __nv_bfloa
         acc = fmaf(cv[3], s4.w, acc);
 #pragma unroll
         for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (l16 == 0) y[bh * P + p] = __float2bfloat16_rn(acc + Dh * xp);
+        if (l16 == 0) y[bh * P + p] = __float2bfloat16_rn(step_output(acc, xp, Dh, h * P + p, bh * P + p, oo));
     }
 }
 
@@ -131,14 +144,14 @@ __global__ void __launch_bounds__(kThreads) ssd_step_kernel_n64(const __nv_bfloa
 
 int launch_step(const __nv_bfloat16* x, const float* dt, const float* A, const __nv_bfloat16* B,
                 const __nv_bfloat16* C, const float* D, float* state, int batch, int nheads, int ngroups, int dstate,
-                __nv_bfloat16* y, cudaStream_t s) {
+                __nv_bfloat16* y, cudaStream_t s, const DtOpts& dto, const OutOpts& oo) {
     dim3 grid(nheads, batch);
     launch_begin(kKindStep, s);
     switch (dstate) {
-        case 64: ssd_step_kernel_n64<<<grid, kThreads, 0, s>>>(x, dt, A, B, C, D, state, nheads, ngroups, y); break;
-        case 128: ssd_step_kernel<128><<<grid, kThreads, 0, s>>>(x, dt, A, B, C, D, state, nheads, ngroups, y); break;
-        case 256: ssd_step_kernel<256><<<grid, kThreads, 0, s>>>(x, dt, A, B, C, D, state, nheads, ngroups, y); break;
-        case 512: ssd_step_kernel<512><<<grid, kThreads, 0, s>>>(x, dt, A, B, C, D, state, nheads, ngroups, y); break;
+        case 64: ssd_step_kernel_n64<<<grid, kThreads, 0, s>>>(x, dt, A, B, C, D, state, nheads, ngroups, y, dto, oo); break;
+        case 128: ssd_step_kernel<128><<<grid, kThreads, 0, s>>>(x, dt, A, B, C, D, state, nheads, ngroups, y, dto, oo); break;
+        case 256: ssd_step_kernel<256><<<grid, kThreads, 0, s>>>(x, dt, A, B, C, D, state, nheads, ngroups, y, dto, oo); break;
+        case 512: ssd_step_kernel<512><<<grid, kThreads, 0, s>>>(x, dt, A, B, C, D, state, nheads, ngroups, y, dto, oo); break;
         default: return SSD_ERR_UNSUPPORTED;
     }
     return launch_end(kKindStep, s);

@@ -103,6 +103,28 @@ int check_dims(int batch, int seqlen, int nheads, int headdim, int ngroups, int 
     return SSD_OK;
 }
 
+// Validates the input-side options and splits them into the dt transform
+// (chunk_cumsum / step) and the output options (compute_out's epilogue / step).
+// `rows16`: z and a per-channel D are read in 16-byte pieces (ssd_forward_ex).
+int read_options(const ssd_input_options* o, const float* D, bool rows16, DtOpts* dto, OutOpts* oo) {
+    *dto = DtOpts();
+    *oo = OutOpts();
+    if (o == nullptr) return SSD_OK;
+    if (o->dt_bias != nullptr && (reinterpret_cast<uintptr_t>(o->dt_bias) & 3u)) return SSD_ERR_INVALID_ARG;
+    if (o->dt_limit && !(o->dt_min <= o->dt_max)) return SSD_ERR_INVALID_ARG;  // also rejects a NaN bound
+    if (o->z != nullptr && (rows16 ? !aligned16(o->z) : (reinterpret_cast<uintptr_t>(o->z) & 1u)))
+        return SSD_ERR_INVALID_ARG;
+    if (o->D_per_channel && D != nullptr && rows16 && !aligned16(D)) return SSD_ERR_INVALID_ARG;
+    dto->bias = o->dt_bias;
+    dto->softplus = o->dt_softplus != 0;
+    dto->limit = o->dt_limit != 0;
+    dto->lo = o->dt_min;
+    dto->hi = o->dt_max;
+    if (o->D_per_channel) oo->Dp = D;
+    oo->z = static_cast<const __nv_bfloat16*>(o->z);
+    return SSD_OK;
+}
+
 Dims make_dims(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk_size) {
     Dims d;
     d.batch = batch;
@@ -318,6 +340,14 @@ int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_
 int ssd_forward(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,
                 const float* init_state, int batch, int seqlen, int nheads, int headdim, int ngroups,
                 int dstate, int chunk_size, void* y, float* final_state, cudaStream_t stream) {
+    return ssd_forward_ex(x, dt, A, B, C, D, init_state, batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size,
+                          nullptr, y, final_state, stream);
+}
+
+int ssd_forward_ex(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,
+                   const float* init_state, int batch, int seqlen, int nheads, int headdim, int ngroups,
+                   int dstate, int chunk_size, const ssd_input_options* options, void* y, float* final_state,
+                   cudaStream_t stream) {
     if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
     int r = check_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
     if (r != SSD_OK) return r;
@@ -325,6 +355,10 @@ int ssd_forward(const void* x, const float* dt, const float* A, const void* B, c
         ((uintptr_t)A & 3u) || (D && ((uintptr_t)D & 3u)) || (init_state && !aligned16(init_state)) ||
         (final_state && !aligned16(final_state)))
         return SSD_ERR_INVALID_ARG;
+    DtOpts dto;
+    OutOpts oo;
+    r = read_options(options, D, true, &dto, &oo);
+    if (r != SSD_OK) return r;
     Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
     int* err = device_error_ptr();
     if (err == nullptr) return SSD_ERR_CUDA;
@@ -345,12 +379,13 @@ int ssd_forward(const void* x, const float* dt, const float* A, const void* B, c
     __half* C16 = B16 + nbc;
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     r = launch_chunk_cumsum_bc(dt, A, d, cs, dtt, static_cast<const __nv_bfloat16*>(B),
-                               static_cast<const __nv_bfloat16*>(C), B16, C16, stream);
+                               static_cast<const __nv_bfloat16*>(C), B16, C16, stream, dto);
     if (r == SSD_OK) r = launch_chunk_state_span(xb, B16, dtt, cs, span, d, S, dec, err, stream);
     // span-level hop, in place: S becomes the span-start states
     if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
     if (r == SSD_OK)
-        r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream);
+        r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream,
+                                   oo);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
     return r;
 }
@@ -402,6 +437,12 @@ int ssd_forward_noalloc(const void* x, const float* dt, const float* A, const vo
 int ssd_step(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,
              float* state, int batch, int nheads, int headdim, int ngroups, int dstate, void* y,
              cudaStream_t stream) {
+    return ssd_step_ex(x, dt, A, B, C, D, state, batch, nheads, headdim, ngroups, dstate, nullptr, y, stream);
+}
+
+int ssd_step_ex(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,
+                float* state, int batch, int nheads, int headdim, int ngroups, int dstate,
+                const ssd_input_options* options, void* y, cudaStream_t stream) {
     if (!x || !dt || !A || !B || !C || !state || !y) return SSD_ERR_INVALID_ARG;
     if (batch <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0) return SSD_ERR_INVALID_ARG;
     if (nheads % ngroups != 0) return SSD_ERR_INVALID_ARG;
@@ -410,9 +451,13 @@ int ssd_step(const void* x, const float* dt, const float* A, const void* B, cons
     if (!aligned16(state) || ((uintptr_t)x & 1u) || ((uintptr_t)B & 1u) || ((uintptr_t)C & 1u) ||
         ((uintptr_t)y & 1u) || ((uintptr_t)dt & 3u) || ((uintptr_t)A & 3u) || (D && ((uintptr_t)D & 3u)))
         return SSD_ERR_INVALID_ARG;
+    DtOpts dto;
+    OutOpts oo;
+    const int r = read_options(options, D, false, &dto, &oo);
+    if (r != SSD_OK) return r;
     return launch_step(static_cast<const __nv_bfloat16*>(x), dt, A, static_cast<const __nv_bfloat16*>(B),
-                       static_cast<const __nv_bfloat16*>(C), D, state, batch, nheads, ngroups, dstate,
-                       static_cast<__nv_bfloat16*>(y), stream);
+                       static_cast<const __nv_bfloat16*>(C), oo.Dp != nullptr ? nullptr : D, state, batch, nheads,
+                       ngroups, dstate, static_cast<__nv_bfloat16*>(y), stream, dto, oo);
 }
 
 int ssd_get_device_error(void) {

@@ -76,6 +76,24 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
     return {"x": x, "dt": dt, "A": A, "B": B, "C": C, "D": D, "init": init}
 
 
+def make_layer_options(w: Workload, seed: int = 0) -> dict:
+    """Seeded inputs of a whole layer's input-side options for workload ``w`` (CPU torch tensors):
+        dt_raw  ~ N(0, 1)                    float32 (batch, L, H): the pre-activation dt
+        dt_bias ~ U(-6, -2)                  float32 (H,)
+        D_hp    ~ N(0, 1)                    float32 (H, P): one skip weight per channel
+        z       ~ N(0, 1) rounded to bf16    (batch, L, H, P): the output gate
+        dt_limit = (0.001, 0.1)
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(10_000 + seed)
+    b, L, H, P = w.batch, w.seqlen, w.nheads, w.headdim
+    dt_raw = torch.randn((b, L, H), generator=g, dtype=torch.float32)
+    dt_bias = torch.rand((H,), generator=g, dtype=torch.float32) * 4.0 - 6.0
+    D_hp = torch.randn((H, P), generator=g, dtype=torch.float32)
+    z = torch.randn((b, L, H, P), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return {"dt_raw": dt_raw, "dt_bias": dt_bias, "D_hp": D_hp, "z": z, "dt_limit": (0.001, 0.1)}
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """bfloat16 torch tensor -> numpy uint16 bit patterns (no copy of values' meaning)."""
     assert t.dtype == torch.bfloat16

@@ -139,3 +139,32 @@ def test_step_validation(lib):
     assert step(x=FAKE + 1) == _ffi.SSD_ERR_INVALID_ARG
     assert step(headdim=32) == _ffi.SSD_ERR_UNSUPPORTED
     assert step(dstate=96) == _ffi.SSD_ERR_UNSUPPORTED
+
+
+def test_options_validation(lib):
+    """Bad input-side options are rejected before any launch (each case keeps every other argument valid)."""
+    def fwd_ex(**kw):
+        o = _ffi.InputOptions()
+        for k, v in kw.items():
+            setattr(o, k, v)
+        return lib.ssd_forward_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 512, 4, 64, 1, 64, 64,
+                                  ctypes.addressof(o), FAKE, FAKE, None)
+
+    def step_ex(**kw):
+        o = _ffi.InputOptions()
+        for k, v in kw.items():
+            setattr(o, k, v)
+        return lib.ssd_step_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 64, 1, 128, ctypes.addressof(o),
+                               FAKE, None)
+    bad = _ffi.SSD_ERR_INVALID_ARG
+    assert fwd_ex(dt_limit=1, dt_min=0.5, dt_max=0.1) == bad
+    assert fwd_ex(dt_limit=1, dt_min=float("nan"), dt_max=0.1) == bad
+    assert fwd_ex(dt_bias=FAKE + 2) == bad
+    assert fwd_ex(z=FAKE + 8) == bad
+    assert step_ex(z=FAKE + 1) == bad
+    assert step_ex(dt_limit=1, dt_min=1.0, dt_max=0.0) == bad
+    # a per-channel D is read in 16-byte pieces by the forward pass
+    o = _ffi.InputOptions()
+    o.D_per_channel = 1
+    assert lib.ssd_forward_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 4, FAKE, 1, 512, 4, 64, 1, 64, 64,
+                              ctypes.addressof(o), FAKE, FAKE, None) == bad
