@@ -43,11 +43,10 @@ constexpr int kMaxSpanChunks = 256;
 // k-step covers all of them (N = 64 HH).  2 scaling warpgroups when HH > 1.
 template <int N, int HH>
 struct StCfg {
-    static constexpr int TB = (N == 512) ? 64 : 128;   // tokens per stage
+    static constexpr int TB = 64;                      // tokens per stage
     static constexpr int BOX = TB * 128;               // one 64-column box, TB rows
     static constexpr int NBOX = N / 64;                // boxes of B per stage
     static constexpr int MB = (N + 127) / 128;         // 128-row accumulator blocks
-    static constexpr int NST = 2;
     static constexpr int SW = (HH > 1) ? 2 : 1;        // scaling warpgroups
     static constexpr int THREADS = 128 * SW + 64;      // + TMA warp + MMA warp
     static constexpr int WARP_TMA = 4 * SW, WARP_MMA = 4 * SW + 1;
@@ -55,6 +54,10 @@ struct StCfg {
     static constexpr int OFF_B = HH * BOX;
     static constexpr int OFF_CD = OFF_B + NBOX * BOX;
     static constexpr int SZ_STAGE = (OFF_CD + HH * 2 * TB * 4 + 1023) / 1024 * 1024;
+    // as many stages as fit about 200 KB (2 to 4): a stage refills only after its MMAs retire,
+    // so more, smaller stages keep more of the x stream in flight
+    static constexpr int NST_FIT = (100 * 1024) / SZ_STAGE;
+    static constexpr int NST = NST_FIT < 2 ? 2 : (NST_FIT > 4 ? 4 : NST_FIT);
     static constexpr int OFF_ZERO = NST * SZ_STAGE;
     static constexpr int SZ_ZERO = (N == 64) ? BOX : 0;  // zero rows padding the A operand to 128
     static constexpr int OFF_R = OFF_ZERO + SZ_ZERO;     // HH x per chunk of the span: R_c + cs[c][Q-1]
@@ -205,28 +208,30 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
             mma_commit(acc_done);
         }
     } else {
-        // scaling warpgroup(s): thread t scales token row r = t % 128 of the x tiles of heads
-        // hh = t / 128, t / 128 + SW, ... in place, then stores those heads' accumulators
+        // scaling warpgroup(s): thread t scales token row t % TB of the x tiles of heads
+        // hh = t / TB, t / TB + 128 SW / TB, ... in place; afterwards thread t stores TMEM lane t % 128
         const int r = threadIdx.x & 127;
         const int hsel = threadIdx.x >> 7;
+        const int rr = threadIdx.x % K::TB;
+        constexpr int kHeadStep = 128 * K::SW / K::TB;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         bool ok = true;
         for (int kb = 0; kb < nblk; ++kb) {
             const int st = kb % K::NST;
             ok = ok && mbar_wait_bounded(&full[st], (kb / K::NST) & 1, abort_flag, a.err, 24, kWaitNs);
-            if (ok && r < K::TB) {
-                const int64_t t = ts + (int64_t)kb * K::TB + r;
+            if (ok) {
+                const int64_t t = ts + (int64_t)kb * K::TB + rr;
                 uint8_t* stage = smem + st * K::SZ_STAGE;
                 const float* scd = reinterpret_cast<const float*>(stage + K::OFF_CD);
 #pragma unroll 1
-                for (int hh = hsel; hh < HH; hh += K::SW) {
+                for (int hh = (int)(threadIdx.x / K::TB); hh < HH; hh += kHeadStep) {
                     uint8_t* xrow = stage + hh * K::BOX;
                     const float* cd = scd + hh * 2 * K::TB;
                     float w = 0.f;
-                    if (t < te) w = exp2f(Rs[hh * kMaxSpanChunks + (int)(t / Q - c_first)] - cd[r]) * cd[K::TB + r];
+                    if (t < te) w = exp2f(Rs[hh * kMaxSpanChunks + (int)(t / Q - c_first)] - cd[rr]) * cd[K::TB + rr];
                     uint4 v[8];
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) v[ch] = *reinterpret_cast<const uint4*>(xrow + sw128_offset(r, ch));
+                    for (int ch = 0; ch < 8; ++ch) v[ch] = *reinterpret_cast<const uint4*>(xrow + sw128_offset(rr, ch));
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
                         const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v[ch]);
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
                             const float2 f = __bfloat1622float2(p2[e]);
                             o2[e] = __floats2half2_rn(f.x * w, f.y * w);
                         }
-                        *reinterpret_cast<uint4*>(xrow + sw128_offset(r, ch)) = o;
+                        *reinterpret_cast<uint4*>(xrow + sw128_offset(rr, ch)) = o;
                     }
                 }
                 fence_proxy_async_smem();

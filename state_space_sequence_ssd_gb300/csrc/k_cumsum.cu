@@ -45,6 +45,27 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
     __shared__ float tile[kHeads][Q + Q / 8];
     const int c = blockIdx.x, h0 = blockIdx.y * kHeads, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // this CTA's share of the B / C float16 copies (16-byte chunks); the first round of loads
+    // is issued before the dt tile, so the two memory latencies overlap
+    int64_t i = 0, hi = 0;
+    uint4 vb[4], vc[4];
+    bool first = false;
+    if (bc16 > 0) {
+        const int64_t nblk = (int64_t)gridDim.x * gridDim.y * gridDim.z;
+        const int64_t blk = ((int64_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        const int64_t per = (bc16 + nblk - 1) / nblk;
+        const int64_t lo = blk * per;
+        hi = min(bc16, lo + per);
+        i = lo + tid;
+        if (i + 3 * kThreads < hi) {
+            first = true;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                vb[u] = __ldg(bsrc + i + u * kThreads);
+                vc[u] = __ldg(csrc + i + u * kThreads);
+            }
+        }
+    }
     // token row tid: 8 heads h0..h0+7
     if (tid < Q) {
         const int64_t t = (int64_t)c * Q + tid;
@@ -72,20 +93,17 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
 #pragma unroll
         for (int k = 0; k < kHeads; ++k) tile[k][tid + tid / 8] = v[k];
     }
-    // share of the B / C float16 copies (16-byte chunks), independent of the scan
+    // the rest of the B / C share, independent of the scan
     if (bc16 > 0) {
-        const int64_t nblk = (int64_t)gridDim.x * gridDim.y * gridDim.z;
-        const int64_t blk = ((int64_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-        const int64_t per = (bc16 + nblk - 1) / nblk;
-        const int64_t lo = blk * per, hi = min(bc16, lo + per);
-        int64_t i = lo + tid;
         for (; i + 3 * kThreads < hi; i += 4 * kThreads) {  // four chunks of B and C in flight
-            uint4 vb[4], vc[4];
+            if (!first) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                vb[u] = __ldg(bsrc + i + u * kThreads);
-                vc[u] = __ldg(csrc + i + u * kThreads);
+                for (int u = 0; u < 4; ++u) {
+                    vb[u] = __ldg(bsrc + i + u * kThreads);
+                    vc[u] = __ldg(csrc + i + u * kThreads);
+                }
             }
+            first = false;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 bdst[i + u * kThreads] = make_uint4(bf16x2_to_f16x2_sat(vb[u].x), bf16x2_to_f16x2_sat(vb[u].y),
