@@ -290,14 +290,18 @@ SSD_API int ssd_get_device_error(void);
 
 /*
  * Profiling counters (host side, process-wide, not thread-safe).
- * ssd_profile_enable(1) makes every later launch record a CUDA event pair
- * around itself on the launch stream; ssd_profile_read() waits for those
+ * ssd_profile_enable(kinds) makes every later launch of a selected kernel
+ * kind record a CUDA event pair around itself on the launch stream: `kinds`
+ * is a bit mask over the kinds of ssd_kernel_name (bit k selects kind k),
+ * -1 selects all and 0 turns profiling off.  Each event pair adds a few
+ * microseconds between launches, so a timed loop can select only the kernel
+ * it needs.  ssd_profile_read() waits for those
  * events and returns, per kernel kind (see ssd_kernel_name), the summed
  * device time in milliseconds and the launch count since the last reset.
  * ssd_launch_count() counts every kernel the library has launched since load
  * (profiling enabled or not).
  */
-SSD_API int ssd_profile_enable(int enable);
+SSD_API int ssd_profile_enable(int kinds);
 SSD_API int ssd_profile_reset(void);
 SSD_API int ssd_profile_read(float* total_ms, int* launches, int max_kinds, int* n_kinds);
 SSD_API const char* ssd_kernel_name(int kind);

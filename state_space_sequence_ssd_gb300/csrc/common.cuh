@@ -48,6 +48,32 @@ struct OutOpts {
 // denominator exceeds 2^126 and the quotient is 0, the function's limit.
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
+// Programmatic dependent launch.  A kernel launched with launch_dependent() may begin while
+// the previous kernel on the stream is still running; it must execute grid_dep_wait() before
+// it reads anything an earlier launch wrote (the wait returns once that kernel has completed
+// and its writes are visible).  grid_dep_launch_dependents() lets the next such launch begin.
+// Both are no-ops for a kernel launched without the attribute or followed by none.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Kernel kinds, for the profiling counters (names in ssd_api.cu).
 enum KernelKind {
     kKindCumsum = 0,

@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    grid_dep_wait();  // states, dA_cumsum, dt and the float16 B / C come from earlier launches
     const uint32_t tm = tmem_base_sh;
     volatile int* abort_flag = &abort_sh;
 
@@ -711,8 +712,9 @@ int launch_scan_n(const __nv_bfloat16* x, const __half* B, const __half* C, cons
         return SSD_ERR_CUDA;
     dim3 grid(d.nheads, a.nspans, d.batch);
     launch_begin(kKindChunkScan, s);
-    chunk_scan_tc_kernel<N, OPT><<<grid, kThreads, smem, s>>>(tx, tb, tc, a);
-    return launch_end(kKindChunkScan, s);
+    const cudaError_t le = launch_dependent(chunk_scan_tc_kernel<N, OPT>, grid, dim3(kThreads), smem, s, tx, tb, tc, a);
+    const int r = launch_end(kKindChunkScan, s);
+    return le != cudaSuccess ? SSD_ERR_CUDA : r;
 }
 
 }  // namespace

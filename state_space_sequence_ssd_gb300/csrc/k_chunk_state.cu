@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
         abort_sh = 0;
         fence_barrier_init();
     }
+    grid_dep_wait();  // dA_cumsum, dt and the float16 B come from the previous launch
+    grid_dep_launch_dependents();
     if (warp < HH) {
         // head h0 + warp: per chunk c of the span, R_c + cs[c][Q-1] = sum of the chunk totals
         // from c to the span end (an inclusive suffix sum), 32 chunks per round, one load per lane
@@ -293,8 +295,9 @@ int launch_state_nh(const __nv_bfloat16* x, const __half* B, const StateArgs& a,
         return SSD_ERR_CUDA;
     dim3 grid(d.nheads / HH, a.nspans, d.batch);
     launch_begin(kKindChunkState, s);
-    chunk_state_tc_kernel<N, HH><<<grid, K::THREADS, K::SMEM, s>>>(tx, tb, a);
-    return launch_end(kKindChunkState, s);
+    const cudaError_t le = launch_dependent(chunk_state_tc_kernel<N, HH>, grid, dim3(K::THREADS), K::SMEM, s, tx, tb, a);
+    const int r = launch_end(kKindChunkState, s);
+    return le != cudaSuccess ? SSD_ERR_CUDA : r;
 }
 
 // Heads per CTA: as many of one group as divide evenly, up to 4 (N <= 128) or 2 (N >= 256).

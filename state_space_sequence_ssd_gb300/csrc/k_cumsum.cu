@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
     __shared__ float tile[kHeads][Q + Q / 8];
     const int c = blockIdx.x, h0 = blockIdx.y * kHeads, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    grid_dep_launch_dependents();  // the next stage may set itself up while this one runs
     // this CTA's share of the B / C float16 copies (16-byte chunks); the first round of loads
     // is issued before the dt tile, so the two memory latencies overlap
     int64_t i = 0, hi = 0;

@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
                                                                  int64_t dec_step, int64_t dec_row,
                                                                  const float* __restrict__ init, Dims d,
                                                                  float* states, float* __restrict__ final_state) {
+    grid_dep_wait();  // the chunk or span states come from the previous launch
+    grid_dep_launch_dependents();
     const int64_t PN = (int64_t)d.headdim * d.dstate;
     const int64_t e = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * 4;
     const int h = blockIdx.y, b = blockIdx.z;
@@ -97,8 +99,11 @@ int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_ste
     const int64_t PN = (int64_t)d.headdim * d.dstate;
     dim3 grid((unsigned)ceil_div64(PN, (int64_t)kThreads * 4), d.nheads, d.batch);
     launch_begin(kKindStatePassing, s);
-    state_passing_kernel<<<grid, kThreads, 0, s>>>(S, dec, dec_step, dec_row, init, dd, states, final_state);
-    return launch_end(kKindStatePassing, s);
+    const cudaError_t le =
+        launch_dependent(state_passing_kernel, grid, dim3(kThreads), 0, s, S, dec, dec_step, dec_row, init, dd, states,
+                         final_state);
+    const int r = launch_end(kKindStatePassing, s);
+    return le != cudaSuccess ? SSD_ERR_CUDA : r;
 }
 
 }  // namespace ssd

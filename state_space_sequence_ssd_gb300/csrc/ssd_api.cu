@@ -19,7 +19,7 @@ struct EventPair {
 };
 
 std::mutex g_prof_mu;
-bool g_prof_enabled = false;
+unsigned g_prof_mask = 0;  // bit k: launches of kernel kind k record an event pair
 std::vector<EventPair> g_prof_open;   // recorded, not yet read
 std::vector<cudaEvent_t> g_prof_free; // reusable events
 double g_prof_ms[kNumKinds];
@@ -46,7 +46,7 @@ const char* const kKindNames[kNumKinds] = {"chunk_cumsum", "chunk_state", "state
 void launch_begin(int kind, cudaStream_t s) {
     std::lock_guard<std::mutex> lk(g_prof_mu);
     g_pending.kind = -1;
-    if (!g_prof_enabled) return;
+    if (kind < 0 || kind >= 32 || !((g_prof_mask >> kind) & 1u)) return;
     cudaEvent_t a = take_event(), b = take_event();
     if (a == nullptr || b == nullptr) return;
     cudaEventRecord(a, s);
@@ -467,9 +467,9 @@ int ssd_get_device_error(void) {
     return v == 0 ? SSD_OK : SSD_ERR_TIMEOUT;
 }
 
-int ssd_profile_enable(int enable) {
+int ssd_profile_enable(int kinds) {
     std::lock_guard<std::mutex> lk(g_prof_mu);
-    g_prof_enabled = enable != 0;
+    g_prof_mask = static_cast<unsigned>(kinds);
     return SSD_OK;
 }
 
