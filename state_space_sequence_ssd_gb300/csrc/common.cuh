@@ -114,10 +114,12 @@ int launch_state_passing(const float* S, const float* cs, const float* init, con
 int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_step, int64_t dec_row,
                                const float* init, const Dims& d, int nsteps, float* states, float* final_state,
                                cudaStream_t s);
+// span_states holds one state per span of `span_chunks` chunks; chunk_scan walks spans of
+// span_chunks * state_step chunks, each starting from every state_step-th of those states.
 int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C,
                            const float* dtt, const float* cs, const float* D, const float* span_states,
                            int span_chunks, const Dims& d, __nv_bfloat16* y, int* err, cudaStream_t s,
-                           const OutOpts& oo = OutOpts());
+                           const OutOpts& oo = OutOpts(), int state_step = 1);
 
 // one recurrent step for every (batch, head): state updated in place, y for the token (k_step.cu)
 int launch_step(const __nv_bfloat16* x, const float* dt, const float* A, const __nv_bfloat16* B,

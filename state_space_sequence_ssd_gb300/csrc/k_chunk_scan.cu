@@ -115,10 +115,12 @@ struct ScanArgs {
     Dims d;
     int span_chunks;  // chunks per span
     int nspans;
+    int state_step;    // span-start state of span s: entry s * state_step of the state array
+    int state_spans;   // entries per (batch) row of the state array
     const float* cs;    // (b, H, nc, Q)
     const float* dtt;   // (b, H, nc, Q)
     const float* D;     // (H) or null: the skip term on M's diagonal
-    const float* init;  // (b, nspans, H, P, N) span-start states
+    const float* init;  // (b, state_spans, H, P, N) span-start states
     __nv_bfloat16* y;   // (b, L, H, P)
     int* err;
     OutOpts oo;  // D per channel (then D is null: no diagonal skip) and the z gate
@@ -504,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = threadIdx.x - 128;  // TMEM lane (warp % 4 == warp - 4)
         const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
         const int64_t PN = (int64_t)d.headdim * N;
-        const float* init = a.init + (((int64_t)b * a.nspans + s) * H + h) * PN;
+        const float* init = a.init + (((int64_t)b * a.state_spans + (int64_t)s * a.state_step) * H + h) * PN;
         bool ok = true;
         float prev_raw = 0.f;  // raw dA_cumsum of the token before this sub-block (same chunk)
         for (int sb = 0; sb < nsb; ++sb) {
@@ -721,11 +723,13 @@ int launch_scan_n(const __nv_bfloat16* x, const __half* B, const __half* C, cons
 
 int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C, const float* dtt,
                            const float* cs, const float* D, const float* span_states, int span_chunks, const Dims& d,
-                           __nv_bfloat16* y, int* err, cudaStream_t s, const OutOpts& oo) {
+                           __nv_bfloat16* y, int* err, cudaStream_t s, const OutOpts& oo, int state_step) {
     ScanArgs a;
     a.d = d;
-    a.span_chunks = span_chunks;
-    a.nspans = ceil_div(d.nchunks, span_chunks);
+    a.span_chunks = span_chunks * state_step;
+    a.nspans = ceil_div(d.nchunks, a.span_chunks);
+    a.state_step = state_step;
+    a.state_spans = ceil_div(d.nchunks, span_chunks);
     a.cs = cs;
     a.dtt = dtt;
     a.D = D;

@@ -3,7 +3,13 @@
 // declared (and documented) in include/ssd.h.
 #include <stdint.h>
 
+#include <algorithm>
+#include <cmath>
+#include <array>
+#include <functional>
+#include <map>
 #include <mutex>
+#include <queue>
 #include <vector>
 
 #include "common.cuh"
@@ -206,6 +212,80 @@ int forward_span_chunks(const Dims& d) {
     return (int)k;
 }
 
+// Multiprocessor count of the current device (cached per device).
+int device_sms() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 152;
+        }
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Makespan, in 128-token sub-block times, of one chunk_scan launch over `sms` SMs (one CTA per
+// SM) when CTAs start in launch order (head fastest, then span, then batch) on the first free SM.
+// A CTA costs its sub-blocks plus a fixed pipeline fill and drain of about 1.2 sub-block times
+// (fitted to CUDA-event times of chunk_scan on GB300 at several span lengths).
+double scan_makespan(int64_t rows_per_batch, int batch, int nchunks, int chunk_size, int span2, int sms) {
+    const double fill = 1.2;
+    const int ns = ceil_div(nchunks, span2);
+    const double full = std::ceil((double)span2 * chunk_size / 128.0);
+    const double last = std::ceil((double)(nchunks - (ns - 1) * span2) * chunk_size / 128.0);
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int i = 0; i < sms; ++i) free_at.push(0.0);
+    double end = 0.0;
+    for (int b = 0; b < batch; ++b)
+        for (int sp = 0; sp < ns; ++sp)
+            for (int64_t r = 0; r < rows_per_batch; ++r) {
+                const double t = free_at.top() + fill + (sp == ns - 1 ? last : full);
+                free_at.pop();
+                free_at.push(t);
+                if (t > end) end = t;
+            }
+    return end;
+}
+
+// Span-start states per chunk_scan span: chunk_scan walks spans of `span` * step chunks
+// (step in {1, 2, 4}), each from every step-th span-start state, so there are fewer, longer
+// CTAs and less pipeline fill and drain per sub-block.  The step with the shortest estimated
+// makespan wins, among those that keep as many SMs busy as step 1; decided once per shape.
+int forward_scan_step(const Dims& d, int span) {
+    static std::mutex mu;
+    static std::map<std::array<int64_t, 5>, int> cache;
+    const int sms = device_sms();
+    const std::array<int64_t, 5> key = {d.batch, d.nheads, d.nchunks, span, sms};
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    const int64_t rows = d.nheads;
+    const int64_t cta1 = (int64_t)d.batch * rows * ceil_div(d.nchunks, span);
+    int best = 1;
+    double best_t = scan_makespan(rows, d.batch, d.nchunks, d.chunk_size, span, sms);
+    for (int m = 2; m <= 4; m *= 2) {
+        if ((int64_t)span * m > d.nchunks) break;
+        const int64_t cta = (int64_t)d.batch * rows * ceil_div(d.nchunks, span * m);
+        if (cta < std::min<int64_t>(sms, cta1)) break;
+        const double t = scan_makespan(rows, d.batch, d.nchunks, d.chunk_size, span * m, sms);
+        if (t < best_t * 0.995) {
+            best = m;
+            best_t = t;
+        }
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = best;
+    return best;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- fixed scratch
@@ -385,7 +465,7 @@ int ssd_forward_ex(const void* x, const float* dt, const float* A, const void* B
     if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
     if (r == SSD_OK)
         r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream,
-                                   oo);
+                                   oo, forward_scan_step(d, span));
     if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
     return r;
 }
@@ -430,7 +510,8 @@ int ssd_forward_noalloc(const void* x, const float* dt, const float* A, const vo
     if (r == SSD_OK) r = launch_chunk_state_span(xb, B16, dtt, cs, span, d, S, dec, err, stream);
     if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
     if (r == SSD_OK)
-        r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream);
+        r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream,
+                                   OutOpts(), forward_scan_step(d, span));
     return r;
 }
 

@@ -120,6 +120,30 @@ def test_forward_edge_cases(ssd, b, L, H, N, G, Q, init, with_D):
     assert_close("final", unit_states(fin, w, units), ref["final"])
 
 
+LONG_RAGGED = [
+    # (batch, L, H, N, G, Q): enough (batch, head, chunk) units that ssd_forward runs compute_out over
+    # spans of several span-start states, with a ragged tail (L % Q != 0) and a short last span
+    (1, 65536 - 100, 32, 64, 1, 256),
+    (2, 16384 + 64 + 7, 16, 128, 2, 128),
+    (1, 32768 - 1, 24, 256, 3, 64),
+]
+
+
+@pytest.mark.parametrize("b,L,H,N,G,Q", LONG_RAGGED)
+def test_forward_long_ragged(ssd, b, L, H, N, G, Q):
+    w = I.Workload("long_ragged", b, L, H, 64, N, G, Q, True)
+    inp = I.make_inputs(w, seed=5)
+    d = to_dev(inp)
+    y, fin = ssd.ssd_forward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"], Q)
+    torch.cuda.synchronize()
+    assert ssd.ssd_get_device_error() == 0
+    units = sample_units(w, 5, seed=b + H)
+    n = I.as_numpy(inp)
+    ref = oracle.forward(n["x"], n["dt"], n["A"], n["B"], n["C"], n["D"], n["init"], Q, units=units)
+    assert_close("y", unit_rows(y, w, units), ref["y"])
+    assert_close("final", unit_states(fin, w, units), ref["final"])
+
+
 @pytest.mark.parametrize("Q", [64, 128, 256])
 def test_chunk_size_invariance(ssd, Q):
     """The same sequence at every chunk size gives the recurrence's y (P4 on the GPU)."""
