@@ -277,7 +277,7 @@ def main():
     if dom_name is not None and dom_name in timed:
         name, st = dom_name, timed[dom_name]
         avg_ms = st["ms_total"] / max(1, st["launches"])
-        kb = kernel_alg_bytes(name, w)
+        kb = kernel_alg_bytes(name, w, torch.cuda.get_device_properties(dev).multi_processor_count)
         achieved = kb / (avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "peak_source": f"{peaks_src} hbm_gbs (copy)",
@@ -353,7 +353,40 @@ def forward_span_chunks(w: I.Workload) -> int:
     return max(1, min(64, -(-units // 1216), w.nchunks))
 
 
-def kernel_alg_bytes(name: str, w: I.Workload) -> float:
+def scan_state_step(w: I.Workload, sms: int = 152) -> int:
+    """Span-start states per compute_out run, as ssd_forward chooses it (ssd_api.cu): the step in
+    {1, 2, 4} with the shortest list-scheduling makespan of chunk_scan's CTAs in launch order, each
+    costing its 128-token sub-blocks plus 1.2 of fill, never leaving idle SMs that step 1 would use."""
+    import heapq
+    import math
+    span, nc, Q = forward_span_chunks(w), w.nchunks, w.chunk_size
+
+    def makespan(span2):
+        ns = -(-nc // span2)
+        full = math.ceil(span2 * Q / 128)
+        last = math.ceil((nc - (ns - 1) * span2) * Q / 128)
+        free = [0.0] * sms
+        end = 0.0
+        for _ in range(w.batch):
+            for sp in range(ns):
+                for _ in range(w.nheads):
+                    t = heapq.heappop(free) + 1.2 + (last if sp == ns - 1 else full)
+                    heapq.heappush(free, t)
+                    end = max(end, t)
+        return end
+
+    cta1 = w.batch * w.nheads * -(-nc // span)
+    best, best_t = 1, makespan(span)
+    for m in (2, 4):
+        if span * m > nc or w.batch * w.nheads * -(-nc // (span * m)) < min(sms, cta1):
+            break
+        t = makespan(span * m)
+        if t < best_t * 0.995:
+            best, best_t = m, t
+    return best
+
+
+def kernel_alg_bytes(name: str, w: I.Workload, sms: int = 152) -> float:
     """Algorithmic bytes one launch of `name` must move at ssd_forward's span tiling (per-unit figures in
     the design doc): every operand read once and every result written once, intermediates in float32."""
     b, L, H, P, N, G, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk_size
@@ -369,8 +402,9 @@ def kernel_alg_bytes(name: str, w: I.Workload) -> float:
         return float(xy + bc + 2 * ncq * 4 + st)
     if name == "state_passing":
         return float(2 * st + b * H * nspans * 4 + (2 if w.nonzero_init else 1) * b * H * P * N * 4)
-    if name == "chunk_scan":
-        return float(2 * xy + 2 * bc + 2 * ncq * 4 + st)
+    if name == "chunk_scan":  # reads the first span-start state of each run of scan_state_step spans
+        runs = -(-nc // (forward_span_chunks(w) * scan_state_step(w, sms)))
+        return float(2 * xy + 2 * bc + 2 * ncq * 4 + b * runs * H * P * N * 4)
     return float("nan")
 
 
