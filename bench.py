@@ -387,8 +387,11 @@ def scan_state_step(w: I.Workload, sms: int = 152) -> int:
 
 
 def kernel_alg_bytes(name: str, w: I.Workload, sms: int = 152) -> float:
-    """Algorithmic bytes one launch of `name` must move at ssd_forward's span tiling (per-unit figures in
-    the design doc): every operand read once and every result written once, intermediates in float32."""
+    """Algorithmic bytes one launch of `name` must move at ssd_forward's span tiling: every operand read
+    once and every result written once, intermediates in float32 (chunk_cumsum: dt in, dA_cumsum and dt
+    rows out, B and C in with their float16 copies out; chunk_state: x, the float16 B, the dA_cumsum and dt
+    rows, the span states out; state_passing: span states in and out, span decays, init and final;
+    chunk_scan: x in, y out, float16 B and C, dA_cumsum and dt rows, one state per run of spans)."""
     b, L, H, P, N, G, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk_size
     nc = w.nchunks
     nspans = -(-nc // forward_span_chunks(w))
