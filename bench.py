@@ -254,6 +254,8 @@ def main():
 
     # ---- the recurrent decode step on a serving batch of the workload's model
     decode = decode_measure(w, dev, stream, args, ssd, lib, flush)
+    # ---- several new tokens per sequence in one call (state read and written once per call)
+    decode_multi = [decode_multi_measure(w, dev, stream, args, ssd, lib, flush, K) for K in (4, 16)]
 
     # ---- the same forward with a whole layer's input-side options (dt bias/softplus/clamp, D per channel, z gate)
     layer = layer_options_measure(w, d, dev, stream, args, ssd, lib, flush)
@@ -313,6 +315,7 @@ def main():
         "gpu_launches": int(launches),
         "e2e": e2e,
         "decode_step": decode,
+        "decode_multi": decode_multi,
         "layer_options": layer,
         "clocks": clk,
         "device_error": int(err),
@@ -643,6 +646,53 @@ def decode_measure(w, dev, stream, args, ssd, lib, flush):
             "roofline": {"bound": "hbm", "kernel": "step", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(gbs / hbm, 4), "peak_source": f"{src} hbm_gbs (copy)",
                          "alg_bytes_per_launch": by, "traffic": kernel_traffic("step", dw)},
+            "steps": steps, "gpu_launches": int(launches)}
+
+
+def decode_multi_bytes(b: int, K: int, H: int, P: int, N: int, G: int) -> float:
+    """Algorithmic bytes of one ssd_step_multi over K tokens: the state read and written once (f32), and per
+    token x read and y written (bf16), dt (f32), B and C (bf16); A and D."""
+    return float(2 * b * H * P * N * 4 + K * (2 * b * H * P * 2 + b * H * 4 + 2 * b * G * N * 2) + 2 * H * 4)
+
+
+def decode_multi_measure(w, dev, stream, args, ssd, lib, flush, K: int):
+    """ssd_step_multi: K new tokens of each of DECODE_BATCH sequences of the workload's model per call,
+    state resident in HBM; L2 flushed between calls outside the events."""
+    import torch
+    dw = w.with_(name=f"decode_b{DECODE_BATCH}_k{K}_{w.name}", batch=DECODE_BATCH, seqlen=K, nonzero_init=True)
+    inp = I.make_inputs(dw, seed=2)
+    d = {k: v.to(dev) for k, v in inp.items()}
+    state = d["init"]
+    y = torch.empty_like(d["x"])
+
+    def call():
+        ssd.ssd_step_multi(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], state, y=y, stream=stream)
+
+    for _ in range(args.warmup):
+        call()
+        flush.zero_()
+    torch.cuda.synchronize()
+    steps = max(args.steps, 20)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    n0 = lib.ssd_launch_count()
+    for i in range(steps):
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    launches = lib.ssd_launch_count() - n0
+    us = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / steps * 1e3
+    by = decode_multi_bytes(dw.batch, K, dw.nheads, dw.headdim, dw.dstate, dw.ngroups)
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs = by / (us / 1e6) / 1e9
+    return {"workload": dw.name, "batch": dw.batch, "tokens_per_call": K, "us_per_call": round(us, 2),
+            "tokens_per_s": round(dw.batch * K / (us / 1e6), 1),
+            "roofline": {"bound": "hbm", "kernel": "step_multi", "achieved": round(gbs, 1), "peak": hbm,
+                         "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_source": f"{src} hbm_gbs (copy)",
+                         "alg_bytes_per_launch": by, "traffic": None},
             "steps": steps, "gpu_launches": int(launches)}
 
 

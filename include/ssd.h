@@ -228,6 +228,29 @@ SSD_API int ssd_step(const void* x, const float* dt, const float* A, const void*
                      void* y, cudaStream_t stream);
 
 /*
+ * ssd_step_multi -- ntokens consecutive new tokens of every sequence in one
+ * call: ssd_step applied ntokens times in order, with the state kept on chip
+ * between the tokens, so the state is read and written once per call rather
+ * than once per token.  Each token's arithmetic is that of ssd_step, so the
+ * results equal ntokens ssd_step calls exactly.  It is the recurrence
+ * itself (work linear in ntokens, no chunked matrix products): for short
+ * bursts such as speculative or multi-token decoding; long prompts belong in
+ * ssd_forward.  The readings are those of ssd_step (same pages):
+ *   x, y      (batch, ntokens, nheads, headdim)  bfloat16 (2-byte aligned)
+ *   dt        (batch, ntokens, nheads)           float32
+ *   A, D      (nheads)                           float32; D may be NULL
+ *   B, C      (batch, ntokens, ngroups, dstate)  bfloat16
+ *   state     (batch, nheads, headdim, dstate)   float32, 16-byte aligned;
+ *             read, then overwritten with the state after the last token.
+ * These are ssd_forward's layouts with seqlen = ntokens and
+ * init_state = final_state = state.  Errors as ssd_step, plus
+ * SSD_ERR_INVALID_ARG for ntokens <= 0.
+ */
+SSD_API int ssd_step_multi(const void* x, const float* dt, const float* A, const void* B, const void* C,
+                           const float* D, float* state, int batch, int ntokens, int nheads, int headdim,
+                           int ngroups, int dstate, void* y, cudaStream_t stream);
+
+/*
  * Input-side options of a whole Mamba-2 layer around the scan.  The pages
  * take dt as already positive and D as one weight per head; these are the
  * plainest reading of the steps a layer adds on either side, applied per

@@ -18,7 +18,7 @@ from __future__ import annotations
 from . import _ffi
 
 __all__ = ["ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_forward",
-           "ssd_forward_noalloc", "ssd_step", "ssd_forward_ex", "ssd_step_ex",
+           "ssd_forward_noalloc", "ssd_step", "ssd_step_multi", "ssd_forward_ex", "ssd_step_ex",
            "ssd_get_device_error", "SSDError", "library_path"]
 
 SSDError = _ffi.SSDError
@@ -290,6 +290,34 @@ def ssd_step(x, dt, A, B, C, D, state, y=None, stream=None):
             raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
     _ffi.check("ssd_step", _ffi.lib().ssd_step(
         _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(state), b, H, P, G, N, _ptr(y),
+        _stream(stream)))
+    return y
+
+
+def ssd_step_multi(x, dt, A, B, C, D, state, y=None, stream=None):
+    """K consecutive new tokens of every sequence in one call (ssd_step K times, the state kept on chip).
+
+    x (batch, K, H, P) bf16, dt (batch, K, H) f32, A (H,) f32, B, C (batch, K, G, N) bf16,
+    D (H,) f32 or None, state (batch, H, P, N) f32 updated in place.  Returns y (batch, K, H, P) bf16."""
+    torch = _torch()
+    _need(x, "x", torch.bfloat16, 4)
+    _need(dt, "dt", torch.float32, 3)
+    _need(A, "A", torch.float32, 1)
+    _need(B, "B", torch.bfloat16, 4)
+    _need(C, "C", torch.bfloat16, 4)
+    _opt(D, "D", torch.float32, 1)
+    _need(state, "state", torch.float32, 4)
+    b, K, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", torch.bfloat16, 4)
+    for name, t, shape in (("dt", dt, (b, K, H)), ("A", A, (H,)), ("B", B, (b, K, G, N)), ("C", C, (b, K, G, N)),
+                           ("D", D, (H,)), ("state", state, (b, H, P, N)), ("y", y, (b, K, H, P))):
+        if t is not None and tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+    _ffi.check("ssd_step_multi", _ffi.lib().ssd_step_multi(
+        _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(state), b, K, H, P, G, N, _ptr(y),
         _stream(stream)))
     return y
 

@@ -125,5 +125,9 @@ int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half
 int launch_step(const __nv_bfloat16* x, const float* dt, const float* A, const __nv_bfloat16* B,
                 const __nv_bfloat16* C, const float* D, float* state, int batch, int nheads, int ngroups, int dstate,
                 __nv_bfloat16* y, cudaStream_t s, const DtOpts& dto = DtOpts(), const OutOpts& oo = OutOpts());
+// ntok consecutive tokens of every sequence, the state in registers throughout (k_step.cu)
+int launch_step_multi(const __nv_bfloat16* x, const float* dt, const float* A, const __nv_bfloat16* B,
+                      const __nv_bfloat16* C, const float* D, float* state, int batch, int ntok, int nheads,
+                      int ngroups, int dstate, __nv_bfloat16* y, cudaStream_t s);
 
 }  // namespace ssd

@@ -179,7 +179,164 @@ __global__ void __launch_bounds__(kThreads) ssd_step_kernel_n64(const __nv_bfloa
     }
 }
 
+// ---------------------------------------------------------------- several tokens per launch
+// ssd_step_multi: K consecutive tokens of every sequence in one launch.  The state stays in
+// registers for all K tokens, so it is read and written once per launch instead of once per
+// token.  Each token's arithmetic (and the lanes' split of n and the reduction order) is that
+// of ssd_step, so K tokens here equal K ssd_step calls bit for bit.
+// Sums R per-row partial values over the lanes of a row group (xor offsets OFF, OFF/2, ..., 1).
+// While a lane holds more than one row it keeps half of them and trades the other half with its
+// partner, so R rows cost R - 1 + log2(lanes / R) + ... shuffles instead of R log2(lanes).  Each
+// row's sum is formed by the same butterfly pairings in the same order as a per-row xor reduction,
+// so the result is bitwise the same.  On return the lane holds the full sum of row `row`.
+template <int R, int OFF>
+__device__ __forceinline__ float fold_rows(const float (&v)[R], int lane, int& row) {
+    if constexpr (R == 1) {
+        float t = v[0];
+#pragma unroll
+        for (int o = OFF; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        return t;
+    } else {
+        constexpr int HALF = R / 2;
+        const bool up = (lane & OFF) != 0;
+        float w[HALF];
+#pragma unroll
+        for (int j = 0; j < HALF; ++j) {
+            const float mine = up ? v[j + HALF] : v[j];
+            const float other = up ? v[j] : v[j + HALF];
+            w[j] = mine + __shfl_xor_sync(0xffffffffu, other, OFF);
+        }
+        if (up) row += HALF;
+        return fold_rows<HALF, OFF / 2>(w, lane, row);
+    }
+}
+
+template <int N>
+struct MultiCfg {
+    static constexpr int THREADS = (N == 512) ? 512 : 256;
+    static constexpr int W = THREADS / 32;
+    static constexpr int LPR = (N == 64) ? 16 : 32;  // lanes per state row
+    static constexpr int RPS = 32 / LPR;             // rows of a warp per slot
+    static constexpr int NV = N / (4 * LPR);         // float4 per lane per row
+    static constexpr int SLOTS = 64 / (W * RPS);     // rows held by each lane
+};
+
+template <int N>
+__global__ void __launch_bounds__(MultiCfg<N>::THREADS) ssd_step_multi_kernel(
+    const __nv_bfloat16* __restrict__ x, const float* __restrict__ dt, const float* __restrict__ A,
+    const __nv_bfloat16* __restrict__ B, const __nv_bfloat16* __restrict__ C, const float* __restrict__ D,
+    float* __restrict__ state, int ntok, int nheads, int ngroups, __nv_bfloat16* __restrict__ y) {
+    using K = MultiCfg<N>;
+    constexpr int P = 64;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int g = h / (nheads / ngroups);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane / K::LPR, ln = lane % K::LPR;
+    const int64_t bh = (int64_t)b * nheads + h;
+    float* st = state + bh * (int64_t)P * N;
+    float4 s[K::SLOTS][K::NV];
+#pragma unroll
+    for (int i = 0; i < K::SLOTS; ++i)
+#pragma unroll
+        for (int v = 0; v < K::NV; ++v)
+            s[i][v] = *reinterpret_cast<const float4*>(st + (int64_t)((i * K::W + warp) * K::RPS + sub) * N +
+                                                       4 * ln + v * 4 * K::LPR);
+    const float Ah = A[h];
+    const float Dh = (D != nullptr) ? D[h] : 0.f;
+    const bool vec = ((reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 7) == 0;
+#pragma unroll 1
+    for (int k = 0; k < ntok; ++k) {
+        const int64_t bk = (int64_t)b * ntok + k;  // (batch, token) row of the (batch, K, ...) layouts
+        const float dtv = dt[bk * nheads + h];
+        const float a = expf(dtv * Ah);
+        const __nv_bfloat16* Bg = B + (bk * ngroups + g) * N;
+        const __nv_bfloat16* Cg = C + (bk * ngroups + g) * N;
+        float bv[K::NV][4], cv[K::NV][4];
+#pragma unroll
+        for (int v = 0; v < K::NV; ++v) {
+            const int n0 = 4 * ln + v * 4 * K::LPR;
+            if (vec) {  // four bf16 in one 8-byte load
+                const uint2 bq = *reinterpret_cast<const uint2*>(Bg + n0);
+                const uint2 cq = *reinterpret_cast<const uint2*>(Cg + n0);
+                const uint32_t bw[2] = {bq.x, bq.y}, cw[2] = {cq.x, cq.y};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    bv[v][e] = __uint_as_float((e & 1) ? (bw[e >> 1] & 0xffff0000u) : (bw[e >> 1] << 16)) * dtv;
+                    cv[v][e] = __uint_as_float((e & 1) ? (cw[e >> 1] & 0xffff0000u) : (cw[e >> 1] << 16));
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    bv[v][e] = __bfloat162float(Bg[n0 + e]) * dtv;
+                    cv[v][e] = __bfloat162float(Cg[n0 + e]);
+                }
+            }
+        }
+        const __nv_bfloat16* xr = x + (bk * nheads + h) * P;
+        __nv_bfloat16* yr = y + (bk * nheads + h) * P;
+        float xp[K::SLOTS], acc[K::SLOTS];
+#pragma unroll
+        for (int i = 0; i < K::SLOTS; ++i) {
+            xp[i] = __bfloat162float(xr[(i * K::W + warp) * K::RPS + sub]);
+            acc[i] = 0.f;
+#pragma unroll
+            for (int v = 0; v < K::NV; ++v) {
+                float4 q = s[i][v];
+                q.x = fmaf(a, q.x, bv[v][0] * xp[i]);
+                q.y = fmaf(a, q.y, bv[v][1] * xp[i]);
+                q.z = fmaf(a, q.z, bv[v][2] * xp[i]);
+                q.w = fmaf(a, q.w, bv[v][3] * xp[i]);
+                s[i][v] = q;
+                acc[i] = fmaf(cv[v][0], q.x, acc[i]);
+                acc[i] = fmaf(cv[v][1], q.y, acc[i]);
+                acc[i] = fmaf(cv[v][2], q.z, acc[i]);
+                acc[i] = fmaf(cv[v][3], q.w, acc[i]);
+            }
+        }
+        int i = 0;  // the row (slot) whose full sum this lane ends up holding
+        const float tot = fold_rows<K::SLOTS, K::LPR / 2>(acc, ln, i);
+        float xi = xp[0];
+#pragma unroll
+        for (int j = 1; j < K::SLOTS; ++j) xi = (i == j) ? xp[j] : xi;
+        if ((ln & (K::LPR / K::SLOTS - 1)) == 0)
+            yr[(i * K::W + warp) * K::RPS + sub] = __float2bfloat16_rn(step_output(tot, xi, Dh, 0, 0, OutOpts()));
+    }
+#pragma unroll
+    for (int i = 0; i < K::SLOTS; ++i)
+#pragma unroll
+        for (int v = 0; v < K::NV; ++v)
+            *reinterpret_cast<float4*>(st + (int64_t)((i * K::W + warp) * K::RPS + sub) * N + 4 * ln +
+                                       v * 4 * K::LPR) = s[i][v];
+}
+
 }  // namespace
+
+int launch_step_multi(const __nv_bfloat16* x, const float* dt, const float* A, const __nv_bfloat16* B,
+                      const __nv_bfloat16* C, const float* D, float* state, int batch, int ntok, int nheads,
+                      int ngroups, int dstate, __nv_bfloat16* y, cudaStream_t s) {
+    dim3 grid(nheads, batch);
+    launch_begin(kKindStep, s);
+    switch (dstate) {
+        case 64:
+            ssd_step_multi_kernel<64><<<grid, MultiCfg<64>::THREADS, 0, s>>>(x, dt, A, B, C, D, state, ntok, nheads,
+                                                                             ngroups, y);
+            break;
+        case 128:
+            ssd_step_multi_kernel<128><<<grid, MultiCfg<128>::THREADS, 0, s>>>(x, dt, A, B, C, D, state, ntok,
+                                                                               nheads, ngroups, y);
+            break;
+        case 256:
+            ssd_step_multi_kernel<256><<<grid, MultiCfg<256>::THREADS, 0, s>>>(x, dt, A, B, C, D, state, ntok,
+                                                                               nheads, ngroups, y);
+            break;
+        case 512:
+            ssd_step_multi_kernel<512><<<grid, MultiCfg<512>::THREADS, 0, s>>>(x, dt, A, B, C, D, state, ntok,
+                                                                               nheads, ngroups, y);
+            break;
+        default: return SSD_ERR_UNSUPPORTED;
+    }
+    return launch_end(kKindStep, s);
+}
 
 int launch_step(const __nv_bfloat16* x, const float* dt, const float* A, const __nv_bfloat16* B,
                 const __nv_bfloat16* C, const float* D, float* state, int batch, int nheads, int ngroups, int dstate,

@@ -541,6 +541,23 @@ int ssd_step_ex(const void* x, const float* dt, const float* A, const void* B, c
                        ngroups, dstate, static_cast<__nv_bfloat16*>(y), stream, dto, oo);
 }
 
+int ssd_step_multi(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,
+                   float* state, int batch, int ntokens, int nheads, int headdim, int ngroups, int dstate, void* y,
+                   cudaStream_t stream) {
+    if (!x || !dt || !A || !B || !C || !state || !y) return SSD_ERR_INVALID_ARG;
+    if (batch <= 0 || ntokens <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0)
+        return SSD_ERR_INVALID_ARG;
+    if (nheads % ngroups != 0) return SSD_ERR_INVALID_ARG;
+    if (headdim != 64 || !supported_dstate(dstate)) return SSD_ERR_UNSUPPORTED;
+    if (batch > 65535 || (int64_t)batch * ntokens * nheads > ((int64_t)1 << 40)) return SSD_ERR_UNSUPPORTED;
+    if (!aligned16(state) || ((uintptr_t)x & 1u) || ((uintptr_t)B & 1u) || ((uintptr_t)C & 1u) ||
+        ((uintptr_t)y & 1u) || ((uintptr_t)dt & 3u) || ((uintptr_t)A & 3u) || (D && ((uintptr_t)D & 3u)))
+        return SSD_ERR_INVALID_ARG;
+    return launch_step_multi(static_cast<const __nv_bfloat16*>(x), dt, A, static_cast<const __nv_bfloat16*>(B),
+                             static_cast<const __nv_bfloat16*>(C), D, state, batch, ntokens, nheads, ngroups, dstate,
+                             static_cast<__nv_bfloat16*>(y), stream);
+}
+
 int ssd_get_device_error(void) {
     int v = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&v, g_ssd_device_error, sizeof(int)) != cudaSuccess) return SSD_ERR_CUDA;

@@ -141,6 +141,24 @@ def test_step_validation(lib):
     assert step(dstate=96) == _ffi.SSD_ERR_UNSUPPORTED
 
 
+def test_step_multi_validation(lib):
+    def multi(**kw):
+        a = dict(x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, state=FAKE, batch=2, ntokens=8, nheads=4,
+                 headdim=64, ngroups=1, dstate=128, y=FAKE)
+        a.update(kw)
+        return lib.ssd_step_multi(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["state"], a["batch"],
+                                  a["ntokens"], a["nheads"], a["headdim"], a["ngroups"], a["dstate"], a["y"], None)
+    assert multi(x=None) == _ffi.SSD_ERR_INVALID_ARG
+    assert multi(state=None) == _ffi.SSD_ERR_INVALID_ARG
+    assert multi(ntokens=0) == _ffi.SSD_ERR_INVALID_ARG
+    assert multi(ntokens=-3) == _ffi.SSD_ERR_INVALID_ARG
+    assert multi(ngroups=3) == _ffi.SSD_ERR_INVALID_ARG
+    assert multi(state=FAKE + 8) == _ffi.SSD_ERR_INVALID_ARG
+    assert multi(dt=FAKE + 2) == _ffi.SSD_ERR_INVALID_ARG
+    assert multi(headdim=128) == _ffi.SSD_ERR_UNSUPPORTED
+    assert multi(dstate=32) == _ffi.SSD_ERR_UNSUPPORTED
+
+
 def test_options_validation(lib):
     """Bad input-side options are rejected before any launch (each case keeps every other argument valid)."""
     def fwd_ex(**kw):

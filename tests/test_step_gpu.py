@@ -110,3 +110,66 @@ def test_step_rejects_bad_arguments(ssd):
         ssd.ssd_step(x, torch.zeros((1, 4), device="cuda"), torch.zeros(4, device="cuda"),
                      torch.zeros((1, 3, 64), dtype=torch.bfloat16, device="cuda"),  # 3 groups do not divide 4 heads
                      torch.zeros((1, 3, 64), dtype=torch.bfloat16, device="cuda"), None, st)
+
+
+# ---------------------------------------------------------------- ssd_step_multi: K tokens per call
+
+MULTI = [(64, 1, True, 1), (64, 2, True, 9), (128, 1, True, 16), (128, 4, False, 5), (256, 2, True, 7),
+         (512, 1, True, 6), (512, 4, False, 3)]
+
+
+@pytest.mark.parametrize("N,G,with_D,K", MULTI)
+def test_step_multi_equals_repeated_steps(ssd, N, G, with_D, K):
+    """K tokens in one call give exactly (bit for bit) what K ssd_step calls give."""
+    w, inp = draw(3, K, 8, N, G, seed=21 + N + K, with_D=with_D)
+    A = inp["A"].cuda()
+    D = None if inp["D"] is None else inp["D"].cuda()
+    s_one = inp["init"].clone().cuda()
+    ys = []
+    for t in range(K):
+        x, dt, B, C = token(inp, t)
+        ys.append(ssd.ssd_step(x, dt, A, B, C, D, s_one))
+    s_multi = inp["init"].clone().cuda()
+    y_multi = ssd.ssd_step_multi(inp["x"].cuda(), inp["dt"].cuda(), A, inp["B"].cuda(), inp["C"].cuda(), D, s_multi)
+    torch.cuda.synchronize()
+    assert torch.equal(y_multi, torch.stack(ys, dim=1))
+    assert torch.equal(s_multi, s_one)
+
+
+@pytest.mark.parametrize("N,G,with_D,K", MULTI)
+def test_step_multi_matches_oracle(ssd, N, G, with_D, K):
+    w, inp = draw(3, K, 8, N, G, seed=31 + N + K, with_D=with_D)
+    ref = oracle_run(w, inp)
+    state = inp["init"].clone().cuda()
+    D = None if inp["D"] is None else inp["D"].cuda()
+    y = ssd.ssd_step_multi(inp["x"].cuda(), inp["dt"].cuda(), inp["A"].cuda(), inp["B"].cuda(), inp["C"].cuda(), D,
+                           state)
+    torch.cuda.synchronize()
+    got = y.float().cpu().numpy().transpose(0, 2, 1, 3).reshape(ref["y"].shape)
+    close("y", got, ref["y"])
+    close("state", state.cpu().numpy().reshape(ref["final"].shape), ref["final"])
+
+
+def test_step_multi_continues_forward(ssd):
+    """A forward over L tokens, then K more tokens in one multi-token step: the recurrence over L + K."""
+    L, K, N = 300, 12, 128
+    w, inp = draw(2, L + K, 4, N, 1, seed=13)
+    ref = oracle_run(w, inp)
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    _, fin = ssd.ssd_forward(d["x"][:, :L].contiguous(), d["dt"][:, :L].contiguous(), d["A"],
+                             d["B"][:, :L].contiguous(), d["C"][:, :L].contiguous(), d["D"], d["init"], 128)
+    y = ssd.ssd_step_multi(d["x"][:, L:].contiguous(), d["dt"][:, L:].contiguous(), d["A"],
+                           d["B"][:, L:].contiguous(), d["C"][:, L:].contiguous(), d["D"], fin)
+    torch.cuda.synchronize()
+    nunits = w.batch * w.nheads
+    got = y.float().cpu().numpy().transpose(0, 2, 1, 3).reshape(nunits, K, 64)
+    close("y[L:]", got, ref["y"][:, L:])
+    close("state", fin.cpu().numpy().reshape(ref["final"].shape), ref["final"])
+
+
+def test_step_multi_rejects_bad_arguments(ssd):
+    x = torch.zeros((1, 2, 4, 64), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros((1, 4, 64, 64), device="cuda")
+    bc = torch.zeros((1, 2, 3, 64), dtype=torch.bfloat16, device="cuda")  # 3 groups do not divide 4 heads
+    with pytest.raises(ssd.SSDError):
+        ssd.ssd_step_multi(x, torch.zeros((1, 2, 4), device="cuda"), torch.zeros(4, device="cuda"), bc, bc, None, st)
