@@ -11,8 +11,11 @@
 // conflicts avoided -- here by 128-byte swizzled tiles).
 //
 // One CTA per (head h, span s, batch b).  A span is a run of whole chunks
-// that starts from a known state (its chunk-start state).  The span is walked
-// in sub-blocks of 128 tokens.  With u_i the in-sub-block inclusive log2
+// that starts from a known state: entry s * state_step of the span-start
+// state array (state_step > 1 lets one CTA walk several of the state array's
+// spans, carrying the state across their boundaries, so fewer and longer CTAs
+// pay the pipeline fill and drain).  The span is walked in sub-blocks of 128
+// tokens.  With u_i the in-sub-block inclusive log2
 // decay (u_i = log2(e) * sum_{k<=i} dt_k A) and the state h at the
 // sub-block start:
 //
