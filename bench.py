@@ -279,7 +279,7 @@ def main():
     if dom_name is not None and dom_name in timed:
         name, st = dom_name, timed[dom_name]
         avg_ms = st["ms_total"] / max(1, st["launches"])
-        kb = kernel_alg_bytes(name, w, torch.cuda.get_device_properties(dev).multi_processor_count)
+        kb = kernel_alg_bytes(name, w, forward_plan(w))
         achieved = kb / (avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "peak_source": f"{peaks_src} hbm_gbs (copy)",
@@ -350,46 +350,14 @@ def default_oracle_tokens(w: I.Workload) -> int:
     return int(max(256, min(w.seqlen, 6.0e10 / per_tok)))
 
 
-def forward_span_chunks(w: I.Workload) -> int:
-    """Chunks per span that ssd_forward uses (about eight waves of 152 CTAs over batch x head x span)."""
-    units = w.batch * w.nheads * w.nchunks
-    return max(1, min(64, -(-units // 1216), w.nchunks))
+def forward_plan(w: I.Workload) -> dict:
+    """The library's own split of this workload (ssd_forward_plan): chunks per span and spans per
+    compute_out CTA, for the current device."""
+    import state_space_sequence_ssd_gb300 as ssd
+    return ssd.ssd_forward_plan(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk_size)
 
 
-def scan_state_step(w: I.Workload, sms: int = 152) -> int:
-    """Span-start states per compute_out run, as ssd_forward chooses it (ssd_api.cu): the step in
-    {1, 2, 4} with the shortest list-scheduling makespan of chunk_scan's CTAs in launch order, each
-    costing its 128-token sub-blocks plus 1.2 of fill, never leaving idle SMs that step 1 would use."""
-    import heapq
-    import math
-    span, nc, Q = forward_span_chunks(w), w.nchunks, w.chunk_size
-
-    def makespan(span2):
-        ns = -(-nc // span2)
-        full = math.ceil(span2 * Q / 128)
-        last = math.ceil((nc - (ns - 1) * span2) * Q / 128)
-        free = [0.0] * sms
-        end = 0.0
-        for _ in range(w.batch):
-            for sp in range(ns):
-                for _ in range(w.nheads):
-                    t = heapq.heappop(free) + 1.2 + (last if sp == ns - 1 else full)
-                    heapq.heappush(free, t)
-                    end = max(end, t)
-        return end
-
-    cta1 = w.batch * w.nheads * -(-nc // span)
-    best, best_t = 1, makespan(span)
-    for m in (2, 4):
-        if span * m > nc or w.batch * w.nheads * -(-nc // (span * m)) < min(sms, cta1):
-            break
-        t = makespan(span * m)
-        if t < best_t * 0.995:
-            best, best_t = m, t
-    return best
-
-
-def kernel_alg_bytes(name: str, w: I.Workload, sms: int = 152) -> float:
+def kernel_alg_bytes(name: str, w: I.Workload, plan: dict) -> float:
     """Algorithmic bytes one launch of `name` must move at ssd_forward's span tiling: every operand read
     once and every result written once, intermediates in float32 (chunk_cumsum: dt in, dA_cumsum and dt
     rows out, B and C in with their float16 copies out; chunk_state: x, the float16 B, the dA_cumsum and dt
@@ -397,7 +365,7 @@ def kernel_alg_bytes(name: str, w: I.Workload, sms: int = 152) -> float:
     chunk_scan: x in, y out, float16 B and C, dA_cumsum and dt rows, one state per run of spans)."""
     b, L, H, P, N, G, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk_size
     nc = w.nchunks
-    nspans = -(-nc // forward_span_chunks(w))
+    nspans = -(-nc // plan["span_chunks"])
     ncq = b * H * nc * Q
     st = b * nspans * H * P * N * 4           # span states, float32
     bc = b * L * G * N * 2                     # one of B / C, 16-bit
@@ -408,8 +376,8 @@ def kernel_alg_bytes(name: str, w: I.Workload, sms: int = 152) -> float:
         return float(xy + bc + 2 * ncq * 4 + st)
     if name == "state_passing":
         return float(2 * st + b * H * nspans * 4 + (2 if w.nonzero_init else 1) * b * H * P * N * 4)
-    if name == "chunk_scan":  # reads the first span-start state of each run of scan_state_step spans
-        runs = -(-nc // (forward_span_chunks(w) * scan_state_step(w, sms)))
+    if name == "chunk_scan":  # reads the first span-start state of each run of scan_step spans
+        runs = -(-nc // (plan["span_chunks"] * plan["scan_step"]))
         return float(2 * xy + 2 * bc + 2 * ncq * 4 + b * runs * H * P * N * 4)
     return float("nan")
 

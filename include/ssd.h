@@ -179,11 +179,13 @@ SSD_API int ssd_forward(const void* x, const float* dt, const float* A, const vo
  * this function is called.  The workspace of a call is about
  *     8 * batch * nheads * nchunks * chunk_size      (cumulative sums, dt)
  *   + 4 * batch * nspans * nheads * headdim * dstate (span states)
+ *   + 4 * batch * nheads * nspans                    (span decays)
  *   + 4 * batch * seqlen * ngroups * dstate          (float16 B and C)
  * bytes, each part rounded up to 256 bytes, where nspans is the number of
  * chunk groups the library forms (about 1216 (batch, head, group) units);
  * a call that would need more returns SSD_ERR_SCRATCH_TOO_SMALL and launches
- * nothing -- use ssd_forward for such sizes.  For example batch 2,
+ * nothing -- use ssd_forward for such sizes (ssd_forward_plan reports the
+ * exact figure beforehand).  For example batch 2,
  * seqlen 4096, nheads 64, dstate 128, chunk 256 needs 40 MiB and fits;
  * seqlen 65536, nheads 32, dstate 128 needs 85 MiB and does not.
  *
@@ -202,6 +204,26 @@ SSD_API int ssd_forward_noalloc(const void* x, const float* dt, const float* A, 
                         const void* C, const float* D, const float* init_state, int batch,
                         int seqlen, int nheads, int headdim, int ngroups, int dstate,
                         int chunk_size, void* y, float* final_state, cudaStream_t stream);
+
+/*
+ * ssd_forward_plan -- how ssd_forward and ssd_forward_noalloc split a
+ * workload of these sizes, without touching device memory or launching
+ * anything (a host-side query; no counterpart in the pages):
+ *   span_chunks    chunks per span of the state stages (chunk_state runs
+ *                  one CTA per span, state_passing hops over spans);
+ *   scan_step      spans per compute_out CTA (1, 2 or 4), chosen from the
+ *                  current device's multiprocessor count (152 when no
+ *                  device can be queried);
+ *   noalloc_bytes  the workspace ssd_forward_noalloc would place in its
+ *                  fixed scratch: the call fits when this is at most
+ *                  SSD_NOALLOC_SCRATCH_BYTES (ssd_forward allocates about
+ *                  as much from its pool).
+ * Any output pointer may be NULL.  Returns the errors of ssd_forward's
+ * shape checks (SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED), else SSD_OK.
+ */
+SSD_API int ssd_forward_plan(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                             int chunk_size, int* span_chunks, int* scan_step,
+                             unsigned long long* noalloc_bytes);
 
 /*
  * ssd_step -- one recurrent step of the selective state-space model for a

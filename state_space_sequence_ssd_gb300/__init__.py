@@ -18,7 +18,7 @@ from __future__ import annotations
 from . import _ffi
 
 __all__ = ["ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_forward",
-           "ssd_forward_noalloc", "ssd_step", "ssd_step_multi", "ssd_forward_ex", "ssd_step_ex",
+           "ssd_forward_noalloc", "ssd_forward_plan", "ssd_step", "ssd_step_multi", "ssd_forward_ex", "ssd_step_ex",
            "ssd_get_device_error", "SSDError", "library_path"]
 
 SSDError = _ffi.SSDError
@@ -320,6 +320,18 @@ def ssd_step_multi(x, dt, A, B, C, D, state, y=None, stream=None):
         _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(state), b, K, H, P, G, N, _ptr(y),
         _stream(stream)))
     return y
+
+
+def ssd_forward_plan(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size):
+    """How ssd_forward splits a workload of these sizes (host-side query, nothing allocated or launched):
+    {"span_chunks": chunks per span, "scan_step": spans per compute_out CTA,
+     "noalloc_bytes": workspace ssd_forward_noalloc needs in its fixed scratch}."""
+    import ctypes
+    span, step, nb = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_ulonglong(0)
+    _ffi.check("ssd_forward_plan", _ffi.lib().ssd_forward_plan(
+        batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, ctypes.addressof(span), ctypes.addressof(step),
+        ctypes.addressof(nb)))
+    return {"span_chunks": span.value, "scan_step": step.value, "noalloc_bytes": nb.value}
 
 
 def ssd_get_device_error():

@@ -33,6 +33,7 @@ SIGNATURES = {
     "ssd_forward_noalloc": (_i, [_p] * 7 + [_i] * 7 + [_p, _p, _p]),
     "ssd_step": (_i, [_p] * 7 + [_i] * 5 + [_p, _p]),
     "ssd_step_multi": (_i, [_p] * 7 + [_i] * 6 + [_p, _p]),
+    "ssd_forward_plan": (_i, [_i] * 7 + [_p, _p, _p]),
     "ssd_forward_ex": (_i, [_p] * 7 + [_i] * 7 + [_p, _p, _p, _p]),
     "ssd_step_ex": (_i, [_p] * 7 + [_i] * 5 + [_p, _p, _p]),
     "ssd_get_device_error": (_i, []),

@@ -217,7 +217,10 @@ int device_sms() {
     static std::mutex mu;
     static int cache[64] = {0};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 152;
+    }
     std::lock_guard<std::mutex> lk(mu);
     if (cache[dev] == 0) {
         int n = 0;
@@ -317,6 +320,28 @@ unsigned char* noalloc_scratch_ptr() {
 }
 
 size_t round256(size_t bytes) { return (bytes + 255) & ~(size_t)255; }
+
+// Byte offsets of ssd_forward_noalloc's workspace parts inside the fixed scratch (each part starts
+// on a 256-byte boundary): dA_cumsum, dt rows, span states, span decays, float16 B, float16 C.
+struct NoallocLayout {
+    size_t off_dtt, off_S, off_dec, off_B16, off_C16, need;
+};
+
+NoallocLayout noalloc_layout(const Dims& d, int span) {
+    const int nspans = ceil_div(d.nchunks, span);
+    const size_t ncq = (size_t)d.batch * d.nheads * d.nchunks * d.chunk_size;
+    const size_t nst = (size_t)d.batch * nspans * d.nheads * d.headdim * d.dstate;
+    const size_t ndec = (size_t)d.batch * d.nheads * nspans;
+    const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;
+    NoallocLayout l;
+    l.off_dtt = round256(ncq * sizeof(float));
+    l.off_S = l.off_dtt + round256(ncq * sizeof(float));
+    l.off_dec = l.off_S + round256(nst * sizeof(float));
+    l.off_B16 = l.off_dec + round256(ndec * sizeof(float));
+    l.off_C16 = l.off_B16 + round256(nbc * sizeof(__half));
+    l.need = l.off_C16 + round256(nbc * sizeof(__half));
+    return l;
+}
 
 }  // namespace
 
@@ -483,27 +508,18 @@ int ssd_forward_noalloc(const void* x, const float* dt, const float* A, const vo
     Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
     const int span = forward_span_chunks(d);
     const int nspans = ceil_div(d.nchunks, span);
-    const size_t ncq = (size_t)d.batch * d.nheads * d.nchunks * d.chunk_size;
-    const size_t nst = (size_t)d.batch * nspans * d.nheads * d.headdim * d.dstate;
-    const size_t ndec = (size_t)d.batch * d.nheads * nspans;
-    const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;
     // the same regions as ssd_forward, each starting on a 256-byte boundary
-    const size_t off_dtt = round256(ncq * sizeof(float));
-    const size_t off_S = off_dtt + round256(ncq * sizeof(float));
-    const size_t off_dec = off_S + round256(nst * sizeof(float));
-    const size_t off_B16 = off_dec + round256(ndec * sizeof(float));
-    const size_t off_C16 = off_B16 + round256(nbc * sizeof(__half));
-    const size_t need = off_C16 + round256(nbc * sizeof(__half));
-    if (need > (size_t)SSD_NOALLOC_SCRATCH_BYTES) return SSD_ERR_SCRATCH_TOO_SMALL;
+    const NoallocLayout l = noalloc_layout(d, span);
+    if (l.need > (size_t)SSD_NOALLOC_SCRATCH_BYTES) return SSD_ERR_SCRATCH_TOO_SMALL;
     int* err = device_error_ptr();
     unsigned char* ws = noalloc_scratch_ptr();
     if (err == nullptr || ws == nullptr) return SSD_ERR_CUDA;
     float* cs = reinterpret_cast<float*>(ws);
-    float* dtt = reinterpret_cast<float*>(ws + off_dtt);
-    float* S = reinterpret_cast<float*>(ws + off_S);
-    float* dec = reinterpret_cast<float*>(ws + off_dec);
-    __half* B16 = reinterpret_cast<__half*>(ws + off_B16);
-    __half* C16 = reinterpret_cast<__half*>(ws + off_C16);
+    float* dtt = reinterpret_cast<float*>(ws + l.off_dtt);
+    float* S = reinterpret_cast<float*>(ws + l.off_S);
+    float* dec = reinterpret_cast<float*>(ws + l.off_dec);
+    __half* B16 = reinterpret_cast<__half*>(ws + l.off_B16);
+    __half* C16 = reinterpret_cast<__half*>(ws + l.off_C16);
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     r = launch_chunk_cumsum_bc(dt, A, d, cs, dtt, static_cast<const __nv_bfloat16*>(B),
                                static_cast<const __nv_bfloat16*>(C), B16, C16, stream);
@@ -513,6 +529,18 @@ int ssd_forward_noalloc(const void* x, const float* dt, const float* A, const vo
         r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream,
                                    OutOpts(), forward_scan_step(d, span));
     return r;
+}
+
+int ssd_forward_plan(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk_size,
+                     int* span_chunks, int* scan_step, unsigned long long* noalloc_bytes) {
+    const int r = check_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    if (r != SSD_OK) return r;
+    const Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    const int span = forward_span_chunks(d);
+    if (span_chunks != nullptr) *span_chunks = span;
+    if (scan_step != nullptr) *scan_step = forward_scan_step(d, span);
+    if (noalloc_bytes != nullptr) *noalloc_bytes = (unsigned long long)noalloc_layout(d, span).need;
+    return SSD_OK;
 }
 
 int ssd_step(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,

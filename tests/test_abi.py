@@ -123,6 +123,46 @@ def test_noalloc_validates_before_the_device(lib):
     assert b"SCRATCH_TOO_SMALL" in lib.ssd_status_string(_ffi.SSD_ERR_SCRATCH_TOO_SMALL)
 
 
+def plan(lib, b, L, H, N, G, Q, P=64):
+    span, step, nb = ctypes.c_int(-1), ctypes.c_int(-1), ctypes.c_ulonglong(0)
+    r = lib.ssd_forward_plan(b, L, H, P, G, N, Q, ctypes.addressof(span), ctypes.addressof(step),
+                             ctypes.addressof(nb))
+    return r, span.value, step.value, nb.value
+
+
+@pytest.mark.parametrize("b,L,H,N,G,Q", [(1, 512, 4, 64, 1, 64), (2, 4096, 64, 128, 1, 256),
+                                         (1, 65536, 32, 128, 1, 256), (1, 16384, 32, 512, 1, 256),
+                                         (1, 262144, 32, 256, 8, 256), (3, 1000, 6, 128, 2, 128)])
+def test_forward_plan_is_consistent(lib, b, L, H, N, G, Q):
+    """The plan agrees with the workspace the no-allocation entry point accepts or refuses, and its
+    spans tile the sequence."""
+    r, span, step, nb = plan(lib, b, L, H, N, G, Q)
+    assert r == _ffi.SSD_OK
+    nc = -(-L // Q)
+    assert 1 <= span <= min(64, nc) and step in (1, 2, 4) and span * step <= max(nc, span)
+    nspans = -(-nc // span)
+    # the parts listed for ssd_forward_noalloc in include/ssd.h, each rounded up to 256 bytes
+    parts = 8 * b * H * nc * Q + 4 * b * nspans * H * 64 * N + 4 * b * H * nspans + 4 * b * L * G * N
+    assert parts <= nb <= parts + 6 * 256
+    fits = nb <= _ffi.SSD_NOALLOC_SCRATCH_BYTES
+    got = fwd_noalloc(lib, batch=b, seqlen=L, nheads=H, dstate=N, ngroups=G, chunk_size=Q, x=None)
+    assert got == _ffi.SSD_ERR_INVALID_ARG  # null x: refused before the size check either way
+    if not fits:
+        assert fwd_noalloc(lib, batch=b, seqlen=L, nheads=H, dstate=N, ngroups=G, chunk_size=Q) == \
+            _ffi.SSD_ERR_SCRATCH_TOO_SMALL
+
+
+def test_forward_plan_known_shapes(lib):
+    # ~1216 (batch, head, chunk) units per span wave: L 65536 x 32 heads -> 7-chunk spans
+    assert plan(lib, 1, 65536, 32, 128, 1, 256)[1] == 7
+    assert plan(lib, 1, 512, 4, 64, 1, 64)[1:3] == (1, 1)  # 32 CTAs: nothing to merge
+    assert plan(lib, 2, 4096, 64, 128, 1, 256)[3] <= _ffi.SSD_NOALLOC_SCRATCH_BYTES  # 40 MiB fits
+    assert plan(lib, 1, 65536, 32, 128, 1, 256)[3] > _ffi.SSD_NOALLOC_SCRATCH_BYTES  # 85 MiB does not
+    assert plan(lib, 1, 512, 4, 96, 1, 64)[0] == _ffi.SSD_ERR_UNSUPPORTED
+    assert plan(lib, 1, 512, 6, 64, 4, 64)[0] == _ffi.SSD_ERR_INVALID_ARG
+    assert lib.ssd_forward_plan(1, 512, 4, 64, 1, 64, 64, None, None, None) == _ffi.SSD_OK
+
+
 def test_step_validation(lib):
     def step(**kw):
         a = dict(x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, state=FAKE, batch=2, nheads=4, headdim=64,
