@@ -79,10 +79,15 @@ struct Cfg {
     static constexpr int NB = N < 128 ? N : 128;  // state rows per n-block
     static constexpr int NBLK = N / NB;
     static constexpr int BOXES = NB / 64;        // 64-column TMA boxes per n-block
-    static constexpr int NST = (N == 512) ? 1 : 2;
+    static constexpr int NST = 2;
     static constexpr bool S_FIRST = NBLK <= NST;  // all n-blocks resident: issue every S before YS/CB
     static constexpr int NBUF = (N == 512) ? 1 : 2;
-    static constexpr int NX = (N == 256) ? 2 : 3;  // x tiles in flight
+    static constexpr int NX = (N >= 256) ? 2 : 3;  // x tiles in flight
+    // RING (N = 512): the float16 copy of the state for C h lives in two 128-row slots, n-block nb
+    // in slot nb % 2, instead of all N rows at once; the shared memory this frees holds a second
+    // C/B stage, so an n-block's tiles load while the previous n-block's products run.
+    static constexpr bool RING = (N == 512);
+    static constexpr int SZ_HS = NB * 128;  // one slot
     // TMEM columns
     static constexpr int T_H = 0;
     static constexpr int HC = NBLK * 64;
@@ -94,7 +99,7 @@ struct Cfg {
     static constexpr int OFF_X = 0;  // NX x tiles
     static constexpr int OFF_XS = OFF_X + NX * kTile;
     static constexpr int OFF_H = OFF_XS + kTile;
-    static constexpr int SZ_H = N * 128;
+    static constexpr int SZ_H = RING ? 2 * SZ_HS : N * 128;
     static constexpr int OFF_BC = OFF_H + SZ_H;
     static constexpr int SZ_C = BOXES * kTile;
     static constexpr int SZ_STAGE = 2 * SZ_C;  // C then B
@@ -135,6 +140,7 @@ struct Bars {
     uint64_t uv_ready[3], u_free[3];
     uint64_t cb_full[2], m_ready[2], y_full[2], y_free[2];
     uint64_t xs_ready, xs_free, h_ready, state_done, final_mma;
+    uint64_t hs_ready[2], hs_free[2];  // RING: state-copy slot k filled (128 arrivals) / read by C h
 };
 
 static_assert(sizeof(Bars) <= 512, "barriers fit their shared-memory slot");
@@ -209,6 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar->h_ready, 128);
         mbar_init(&bar->state_done, 1);
         mbar_init(&bar->final_mma, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar->hs_ready[i], 128);
+            mbar_init(&bar->hs_free[i], 1);
+        }
         abort_sh = 0;
         fence_barrier_init();
     }
@@ -320,13 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ss(tm + K::T_H + nb * 64, desc_sw128(sB + kk * 2048, lbo, 1024),
                            desc_sw128(sXs + kk * 2048, 16, 1024), kIdescS, 1);
             };
-            // Yst += C_nb h_nb   (K = n, 16 per step)
+            // Yst += C_nb h_nb   (K = n, 16 per step); h_nb in its ring slot (RING) or at rows nb NB
             auto issue_ys = [&](int nb, uint32_t set, uint32_t sC) {
+                const uint32_t hb = K::RING ? sH + (uint32_t)((nb & 1) * K::SZ_HS) : sH + (uint32_t)(nb * K::NB * 128);
 #pragma unroll
                 for (int kk = 0; kk < K::NB / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kTile + (kk & 3) * 32;
-                    mma_ss(set + 128, desc_sw128(sC + off, 16, 1024),
-                           desc_sw128(sH + (nb * K::NB + kk * 16) * 128, 16, 1024), kIdescYS, (nb | kk) != 0);
+                    mma_ss(set + 128, desc_sw128(sC + off, 16, 1024), desc_sw128(hb + kk * 16 * 128, 16, 1024),
+                           kIdescYS, (nb | kk) != 0);
                 }
             };
             // CB += C_nb B_nb^T   (K = n, 16 per step)
@@ -388,14 +399,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // n-blocks streamed one stage at a time
                     for (int nb = 0; nb < K::NBLK; ++nb, ++it) {
                         const int st = it % K::NST;
+                        const int use = f * (K::NBLK / 2) + nb / 2;  // RING: use index of slot nb % 2
                         if (nb > 0) {
                             if (!mbar_wait_bounded(&bar->bc_full[st], (it / K::NST) & 1, abort_flag, a.err, 8,
                                                    kWaitNs))
+                                return false;
+                            if (K::RING &&
+                                !mbar_wait_bounded(&bar->hs_ready[nb & 1], use & 1, abort_flag, a.err, 9, kWaitNs))
                                 return false;
                             tc_fence_after();
                         }
                         if (need_S) issue_s(nb, stage_c(st) + K::SZ_C);
                         issue_ys(nb, set, stage_c(st));
+                        if (K::RING) mma_commit(&bar->hs_free[nb & 1]);
                         issue_cb(nb, set, stage_c(st), stage_c(st) + K::SZ_C);
                         mma_commit(&bar->bc_empty[st]);
                     }
@@ -406,7 +422,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             auto front_ready = [&](int f) -> bool {
-                if (!mbar_test_wait(&bar->xs_ready, f & 1) || !mbar_test_wait(&bar->h_ready, f & 1)) return false;
+                if (!mbar_test_wait(&bar->xs_ready, f & 1)) return false;
+                if (K::RING ? !mbar_test_wait(&bar->hs_ready[0], (f * (K::NBLK / 2)) & 1)
+                            : !mbar_test_wait(&bar->h_ready, f & 1))
+                    return false;
                 const int nres = K::S_FIRST ? K::NBLK : 1;  // stages that must be resident to start
                 for (int nb = 0; nb < nres; ++nb)
                     if (!mbar_test_wait(&bar->bc_full[(it + nb) % K::NST], ((it + nb) / K::NST) & 1)) return false;
@@ -603,8 +622,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int p = 0; p < 32; ++p) hv[32 + p] = __uint_as_float(v[p]);
                     }
+                    if (K::RING) {  // the slot's previous n-block has been read by its C h product
+                        const int use = sb * (K::NBLK / 2) + nb / 2;
+                        if (use >= 1)
+                            ok = mbar_wait_bounded(&bar->hs_free[nb & 1], (use - 1) & 1, abort_flag, a.err, 19,
+                                                   kWaitNs);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                    }
                     if (real) {
-                        const int hr = nb * K::NB + r;  // smem row (state index n)
+                        // smem row: state index n, or its row in the ring slot
+                        const int hr = K::RING ? r : nb * K::NB + r;
+                        uint8_t* hdst = K::RING ? hbase + (nb & 1) * K::SZ_HS : hbase;
 #pragma unroll
                         for (int ch = 0; ch < 8; ++ch) {
                             uint4 v;
@@ -612,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             v.y = pack_f16x2(hv[ch * 8 + 2], hv[ch * 8 + 3]);
                             v.z = pack_f16x2(hv[ch * 8 + 4], hv[ch * 8 + 5]);
                             v.w = pack_f16x2(hv[ch * 8 + 6], hv[ch * 8 + 7]);
-                            *reinterpret_cast<uint4*>(hbase + sw128_offset(hr, ch)) = v;
+                            *reinterpret_cast<uint4*>(hdst + sw128_offset(hr, ch)) = v;
                         }
                     }
                     uint32_t o[16];
@@ -621,6 +650,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int p = 0; p < 16; ++p) o[p] = __float_as_uint(hv[q4 * 16 + p] * dsb);
                         tmem_st16(tm + lane_base + K::T_H + nb * 64 + q4 * 16, o);
+                    }
+                    if (K::RING) {  // this n-block's copy and decayed state are ready for S, C h
+                        tmem_st_wait();
+                        fence_proxy_async_smem();
+                        tc_fence_before();
+                        mbar_arrive(&bar->hs_ready[nb & 1]);
                     }
                 }
                 tmem_st_wait();
