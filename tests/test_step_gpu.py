@@ -173,3 +173,34 @@ def test_step_multi_rejects_bad_arguments(ssd):
     bc = torch.zeros((1, 2, 3, 64), dtype=torch.bfloat16, device="cuda")  # 3 groups do not divide 4 heads
     with pytest.raises(ssd.SSDError):
         ssd.ssd_step_multi(x, torch.zeros((1, 2, 4), device="cuda"), torch.zeros(4, device="cuda"), bc, bc, None, st)
+
+
+def _misaligned(t):
+    """The same values at an address 2 bytes past an 8-byte boundary (the kernels' 2-byte load path)."""
+    n = t.numel()
+    buf = torch.empty(n + 4, dtype=t.dtype, device=t.device)
+    v = buf[1:1 + n].view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 8 == 2
+    return v
+
+
+@pytest.mark.parametrize("N", [64, 128, 256])
+def test_step_and_multi_bc_alignment_paths_agree(ssd, N):
+    """B and C read in 8-byte pieces (aligned) or element by element (2-byte aligned) give the same bits."""
+    K = 5
+    w, inp = draw(2, K, 4, N, 2, seed=41 + N)
+    A, D = inp["A"].cuda(), inp["D"].cuda()
+    x, dt = inp["x"].cuda(), inp["dt"].cuda()
+    B, C = inp["B"].cuda(), inp["C"].cuda()
+    s_a, s_u = inp["init"].clone().cuda(), inp["init"].clone().cuda()
+    y_a = ssd.ssd_step_multi(x, dt, A, B, C, D, s_a)
+    y_u = ssd.ssd_step_multi(x, dt, A, _misaligned(B), _misaligned(C), D, s_u)
+    torch.cuda.synchronize()
+    assert torch.equal(y_a, y_u) and torch.equal(s_a, s_u)
+    x0, dt0, B0, C0 = token(inp, 0)
+    s_a, s_u = inp["init"].clone().cuda(), inp["init"].clone().cuda()
+    y_a = ssd.ssd_step(x0, dt0, A, B0, C0, D, s_a)
+    y_u = ssd.ssd_step(x0, dt0, A, _misaligned(B0), _misaligned(C0), D, s_u)
+    torch.cuda.synchronize()
+    assert torch.equal(y_a, y_u) and torch.equal(s_a, s_u)
