@@ -295,3 +295,19 @@ def test_nonblocking_stream(ssd):
     n = I.as_numpy(inp)
     ref = oracle.forward(n["x"], n["dt"], n["A"], n["B"], n["C"], n["D"], n["init"], w.chunk_size)
     assert_close("y", unit_rows(y, w, np.arange(4)), ref["y"])
+
+
+@pytest.mark.parametrize("name", ["mamba2_1p3b_layer_2x4096_N128", "state_sweep_L16384_N512"])
+def test_forward_y_alignment_paths_agree(ssd, name):
+    """y rows stored in 32-byte pieces (y 32-byte aligned) or 16-byte pieces (y only 16-byte aligned):
+    the same bits either way."""
+    w = I.WORKLOADS[name]
+    d = to_dev(I.make_inputs(w, seed=2))
+    y_a, _ = ssd.ssd_forward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"], w.chunk_size)
+    buf = torch.empty(d["x"].numel() + 16, dtype=torch.bfloat16, device="cuda")
+    y_u = buf[8:8 + d["x"].numel()].view(d["x"].shape)
+    assert y_u.data_ptr() % 32 == 16
+    ssd.ssd_forward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"], w.chunk_size, y=y_u)
+    torch.cuda.synchronize()
+    assert ssd.ssd_get_device_error() == 0
+    assert torch.equal(y_a, y_u)
