@@ -131,6 +131,7 @@ struct ScanArgs {
     const float* init;  // (b, state_spans, H, P, N) span-start states
     __nv_bfloat16* y;   // (b, L, H, P)
     int y32;            // y is 32-byte aligned: rows are stored in 32-byte pieces
+    int z32;            // the gate z is 32-byte aligned: rows are loaded in 32-byte pieces
     int* err;
     OutOpts oo;  // D per channel (then D is null: no diagonal skip) and the z gate
 };
@@ -153,6 +154,24 @@ __device__ __forceinline__ void gate8(float (&o)[8], const uint4& zq) {
     for (int i = 0; i < 8; ++i) {
         const uint32_t w = zw[i >> 1];
         o[i] *= silu(__uint_as_float((i & 1) ? (w & 0xffff0000u) : (w << 16)));
+    }
+}
+
+// 32 bytes from a 32-byte-aligned read-only global address in one load (sm_100+ 256-bit vector load)
+__device__ __forceinline__ void ld_global_nc_32B(const void* p, uint4& lo, uint4& hi) {
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+                 : "l"(p));
+}
+
+// a thread's 128-byte z row: 32-byte loads when z is 32-byte aligned, else 16-byte loads
+__device__ __forceinline__ void load_z_row(const uint4* zr, bool z32, uint4 (&zq)[8]) {
+    if (z32) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ld_global_nc_32B(zr + 2 * i, zq[2 * i], zq[2 * i + 1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) zq[i] = __ldg(zr + i);
     }
 }
 
@@ -680,8 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint4 zq[8];                                 // this thread's z row of the coming sub-block
         if (gate && r < min((int64_t)128, te - ts)) {
             const uint4* zr = reinterpret_cast<const uint4*>(a.oo.z + (((int64_t)b * d.seqlen + ts + r) * H + h) * 64);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) zq[i] = __ldg(zr + i);
+            load_z_row(zr, a.z32, zq);
         }
         bool ok = true;
         for (int sb = 0; sb < nsb; ++sb) {
@@ -741,8 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (gate && t0 + 128 + r < te) {  // the next sub-block's z row, in flight during the next wait
                 const uint4* zr =
                     reinterpret_cast<const uint4*>(a.oo.z + (((int64_t)b * d.seqlen + t0 + 128 + r) * H + h) * 64);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) zq[i] = __ldg(zr + i);
+                load_z_row(zr, a.z32, zq);
             }
         }
     }
@@ -790,6 +807,7 @@ int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half
     a.init = span_states;
     a.y = y;
     a.y32 = (reinterpret_cast<uintptr_t>(y) & 31u) == 0;
+    a.z32 = (reinterpret_cast<uintptr_t>(oo.z) & 31u) == 0;
     a.err = err;
     a.oo = oo;
     if (oo.Dp != nullptr) a.D = nullptr;  // the skip moves from M's diagonal to the X diag(D) product

@@ -156,3 +156,30 @@ def test_step_ex_continues_forward_ex(ssd):
     close("y[:L]", rows(y_fw, w.with_(seqlen=L)), ref["y"][:, :L])
     close("y[L]", y_st.float().cpu().numpy().reshape(w.batch * w.nheads, 64), ref["y"][:, L])
     close("state", fin.cpu().numpy().reshape(ref["final"].shape), ref["final"])
+
+
+def _offset16(t):
+    """The same values at an address 16 bytes past a 32-byte boundary."""
+    n = t.numel()
+    buf = torch.empty(n + 16, dtype=t.dtype, device=t.device)
+    v = buf[8:8 + n].view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 32 == 16
+    return v
+
+
+def test_forward_ex_gate_and_y_alignment_paths_agree(ssd):
+    """z rows loaded and y rows stored in 32-byte pieces (32-byte aligned) or 16-byte pieces (16-byte
+    aligned only): the same bits."""
+    w = I.WORKLOADS["mamba2_1p3b_layer_2x4096_N128"]
+    inp, dt, D, kw = case(w, "all", seed=6)
+    dv = lambda t: None if t is None else t.cuda()
+    args = (dv(inp["x"]), dv(dt), dv(inp["A"]), dv(inp["B"]), dv(inp["C"]), dv(D), dv(inp["init"]), w.chunk_size)
+    z = dv(kw["z"])
+    opt = dict(dt_bias=dv(kw["dt_bias"]), dt_softplus=kw["dt_softplus"], dt_limit=kw["dt_limit"])
+    y_a, f_a = ssd.ssd_forward_ex(*args, z=z, **opt)
+    y_u = _offset16(torch.zeros_like(y_a))
+    _, f_u = ssd.ssd_forward_ex(*args, z=_offset16(z), y=y_u, **opt)
+    torch.cuda.synchronize()
+    assert ssd.ssd_get_device_error() == 0
+    assert torch.equal(y_a, y_u) and torch.equal(f_a, f_u)
