@@ -87,6 +87,27 @@ static __device__ __noinline__ bool mbar_wait_bounded_slow(uint64_t* bar, uint32
     }
 }
 
+// The same loop as mbar_wait_bounded_slow, compiled into the caller.  A kernel that waits at many
+// sites in its critical path can use it to avoid the call: around an out-of-line call the caller
+// saves live registers to local memory, and with most of L1 carved out as shared memory those
+// lines are often gone when the wait returns.
+__device__ __forceinline__ bool mbar_wait_bounded_inline(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
+                                                         int code, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort = 1;
+            if (err != nullptr) atomicExch(err, code);
+            return false;
+        }
+    }
+}
+
 // Bounded wait on phase `parity` of `bar`.  Gives up after `limit_ns` of
 // global time, or as soon as *abort becomes non-zero (another role already
 // gave up).  On giving up it sets *abort and records `code` in *err, and
