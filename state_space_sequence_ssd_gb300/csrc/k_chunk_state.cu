@@ -161,11 +161,10 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
     if (warp == K::WARP_TMA) {
         // TMA producer: per stage the HH x tiles, the B boxes and the heads' dA_cumsum / dt rows
         if (lane == 0) {
-            int issued[K::NST];
-            for (int i = 0; i < K::NST; ++i) issued[i] = 0;
+            int nissued = 0;  // stage loads issued; stage i took those with index % NST == i
             for (int kb = 0; kb < nblk; ++kb) {
                 const int st = kb % K::NST;
-                if (!mbar_wait_bounded(&empty[st], ((kb / K::NST) & 1) ^ 1, abort_flag, a.err, 21, kWaitNs)) break;
+                if (!mbar_wait_bounded_inline(&empty[st], ((kb / K::NST) & 1) ^ 1, abort_flag, a.err, 21, kWaitNs)) break;
                 uint8_t* sX = smem + st * K::SZ_STAGE;
                 const int t0 = (int)(ts + (int64_t)kb * K::TB);
                 const uint32_t cdb = (uint32_t)min((int64_t)K::TB, rowlen - t0) * 4u;
@@ -181,10 +180,13 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
 #pragma unroll
                 for (int bx = 0; bx < K::NBOX; ++bx)
                     tma_load_4d(sX + K::OFF_B + bx * K::BOX, &tm_B, &full[st], bx * 64, g, t0, b);
-                ++issued[st];
+                ++nissued;
             }
-            for (int i = 0; i < K::NST; ++i)
-                if (issued[i] > 0) mbar_wait_bounded(&full[i], (issued[i] - 1) & 1, abort_flag, a.err, 22, kWaitNs);
+#pragma unroll
+            for (int i = 0; i < K::NST; ++i) {
+                const int issued = (nissued + K::NST - 1 - i) / K::NST;
+                if (issued > 0) mbar_wait_bounded_inline(&full[i], (issued - 1) & 1, abort_flag, a.err, 22, kWaitNs);
+            }
         }
     } else if (warp == K::WARP_MMA) {
         // MMA issuer: acc[mb] (128 n x 64 HH) += B_mb^T (MN-major) * [X'_0 .. X'_HH-1] (MN-major)
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
             constexpr uint32_t idesc = idesc_fp16(128, 64 * HH, true, true);
             for (int kb = 0; kb < nblk; ++kb) {
                 const int st = kb % K::NST;
-                if (!mbar_wait_bounded(&xs_ready[st], (kb / K::NST) & 1, abort_flag, a.err, 23, kWaitNs)) break;
+                if (!mbar_wait_bounded_inline(&xs_ready[st], (kb / K::NST) & 1, abort_flag, a.err, 23, kWaitNs)) break;
                 tc_fence_after();
                 const uint32_t sX = smem_u32(smem + st * K::SZ_STAGE);
                 const uint32_t sB = sX + K::OFF_B;
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
         bool ok = true;
         for (int kb = 0; kb < nblk; ++kb) {
             const int st = kb % K::NST;
-            ok = ok && mbar_wait_bounded(&full[st], (kb / K::NST) & 1, abort_flag, a.err, 24, kWaitNs);
+            ok = ok && mbar_wait_bounded_inline(&full[st], (kb / K::NST) & 1, abort_flag, a.err, 24, kWaitNs);
             if (ok) {
                 const int64_t t = ts + (int64_t)kb * K::TB + rr;
                 uint8_t* stage = smem + st * K::SZ_STAGE;
@@ -251,7 +253,7 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
             }
             mbar_arrive(&xs_ready[st]);
         }
-        ok = ok && mbar_wait_bounded(acc_done, 0, abort_flag, a.err, 25, kWaitNs);
+        ok = ok && mbar_wait_bounded_inline(acc_done, 0, abort_flag, a.err, 25, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         if (ok) {
