@@ -400,14 +400,25 @@ def kernel_traffic(name: str, w: I.Workload):
     return ent.get("dram_bytes_per_launch") if ent.get("src_sha1") == kernel_source_sha1(name) else None
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments and with whitespace runs collapsed, so that a comment or layout
+    edit does not count as a change of the compiled kernel (no string literal in these sources holds
+    comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_sha1(name: str) -> str:
-    """SHA-1 over the kernel's source file and the shared device headers it is compiled with."""
+    """SHA-1 over the code (comments and layout stripped) of the kernel's source file and the shared
+    device headers it is compiled with."""
     import hashlib
     csrc = os.path.join(ROOT, "state_space_sequence_ssd_gb300", "csrc")
     h = hashlib.sha1()
     for fn in (KERNEL_SOURCES[name], "common.cuh", "sm100.cuh", "tmap.cuh"):
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, fn), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

@@ -186,7 +186,8 @@ __global__ void __launch_bounds__(kThreads) ssd_step_kernel_n64(const __nv_bfloa
 // of ssd_step, so K tokens here equal K ssd_step calls bit for bit.
 // Sums R per-row partial values over the lanes of a row group (xor offsets OFF, OFF/2, ..., 1).
 // While a lane holds more than one row it keeps half of them and trades the other half with its
-// partner, so R rows cost R - 1 + log2(lanes / R) + ... shuffles instead of R log2(lanes).  Each
+// partner, so R rows over 2^k lanes cost (R - 1) + (k - log2 R) shuffles instead of R k (9 instead of
+// 40 for 8 rows over 32 lanes).  Each
 // row's sum is formed by the same butterfly pairings in the same order as a per-row xor reduction,
 // so the result is bitwise the same.  On return the lane holds the full sum of row `row`.
 template <int R, int OFF>
