@@ -45,3 +45,24 @@ def test_max_over_ranks_world2():
 def test_max_over_ranks_single_process():
     import bench
     assert bench.max_over_ranks(2.0, None, torch.device("cpu")) == 2.0
+
+
+def test_algorithmic_bytes_of_the_headline_workload():
+    """bench.py's per-launch algorithmic bytes at L 65536, H 32, N 128 for the library's plan of that shape
+    (7-chunk spans, compute_out runs of four spans): the figures the roofline object reports."""
+    import bench
+    from state_space_sequence_ssd_gb300 import inputs as I
+    w = I.WORKLOADS["long_L65536_N128"]
+    plan = {"span_chunks": 7, "scan_step": 4}
+    mb = {k: bench.kernel_alg_bytes(k, w, plan) / 1e6 for k in ("chunk_cumsum", "chunk_state", "state_passing",
+                                                                  "chunk_scan")}
+    assert round(mb["chunk_scan"], 1) == 597.7
+    assert round(mb["chunk_state"], 1) == 340.8
+    assert round(mb["chunk_cumsum"], 1) == 92.3
+    assert round(mb["state_passing"], 1) == 79.7
+
+
+def test_source_key_ignores_comments_only():
+    import bench
+    assert bench._code_only("x = a; // note\n/* block\n comment */ y = b;") == bench._code_only("x = a;\ny = b;")
+    assert bench._code_only("x = a;") != bench._code_only("x = b;")
