@@ -153,6 +153,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--oracle-tokens", type=int, default=0, help="tokens per head for the CPU oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--forward-only", action="store_true",
+                    help="time the forward pass only: no end-to-end, decode or layer-options legs and no CPU "
+                         "baseline (for profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: --warmup raised to 3 (minimum)", file=sys.stderr)
@@ -249,16 +252,17 @@ def main():
 
     total_ms = max_over_ranks(total_ms, dist, dev)
 
-    # ---- end to end through the public call with host buffers
-    e2e = e2e_measure(w, inp, dev, stream, args, ssd, dist)
-
-    # ---- the recurrent decode step on a serving batch of the workload's model
-    decode = decode_measure(w, dev, stream, args, ssd, lib, flush)
-    # ---- several new tokens per sequence in one call (state read and written once per call)
-    decode_multi = [decode_multi_measure(w, dev, stream, args, ssd, lib, flush, K) for K in (4, 16)]
-
-    # ---- the same forward with a whole layer's input-side options (dt bias/softplus/clamp, D per channel, z gate)
-    layer = layer_options_measure(w, d, dev, stream, args, ssd, lib, flush)
+    e2e = decode = decode_multi = layer = None
+    if not args.forward_only:
+        # ---- end to end through the public call with host buffers
+        e2e = e2e_measure(w, inp, dev, stream, args, ssd, dist)
+        # ---- the recurrent decode step on a serving batch of the workload's model
+        decode = decode_measure(w, dev, stream, args, ssd, lib, flush)
+        # ---- several new tokens per sequence in one call (state read and written once per call)
+        decode_multi = [decode_multi_measure(w, dev, stream, args, ssd, lib, flush, K) for K in (4, 16)]
+        # ---- the same forward with a whole layer's input-side options (dt bias/softplus/clamp, D per channel,
+        #      z gate)
+        layer = layer_options_measure(w, d, dev, stream, args, ssd, lib, flush)
 
     if rank != 0:
         dist.destroy_process_group()
@@ -279,11 +283,13 @@ def main():
     if dom_name is not None and dom_name in timed:
         name, st = dom_name, timed[dom_name]
         avg_ms = st["ms_total"] / max(1, st["launches"])
-        kb = kernel_alg_bytes(name, w, forward_plan(w))
+        kbs = kernel_bytes(name, w, forward_plan(w))
+        kb = kbs["compulsory"]
         achieved = kb / (avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "peak_source": f"{peaks_src} hbm_gbs (copy)",
-                "alg_bytes_per_launch": kb, "avg_launch_us": round(avg_ms * 1e3, 2),
+                "alg_bytes_per_launch": kb, "alg_bytes": "compulsory only: x read, y written, B and C read",
+                "intermediate_bytes_per_launch": kbs["intermediate"], "avg_launch_us": round(avg_ms * 1e3, 2),
                 "traffic": kernel_traffic(name, w)}
 
     line = {
@@ -297,7 +303,9 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "fp16",
+        "precision": "x, B, C, y bfloat16 in HBM; tensor-core products on float16 operands with float32 "
+                     "accumulation; decays, scans and the state hop in float32",
         "data": "synthetic (seeded; x,B,C ~N(0,1) bf16, dt=softplus(N(0,1)-4), A=-exp(U(0,ln16)), D~N(0,1))",
         "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
                    "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk_size": w.chunk_size,
@@ -309,6 +317,7 @@ def main():
                           "alg_gflop": round(flops / 1e9, 3), "compulsory_mb": round(cbytes / 1e6, 2),
                           "peaks": f"{peaks_src}: {hbm} GB/s, {tflops_peak} TFLOP/s bf16"},
         "roofline": roof,
+        "pass_traffic": pass_traffic(w, kernels),
         "kernels": {k: {"ms_total": v["ms_total"], "launches": v["launches"]} for k, v in kernels.items()},
         "kernels_timing": "CUDA events around every launch, in a profiled pass over the same steps; the timed "
                           "steps bracket only the dominant kernel (roofline.avg_launch_us)",
@@ -320,7 +329,7 @@ def main():
         "clocks": clk,
         "device_error": int(err),
     }
-    if not args.no_cpu_baseline:
+    if not (args.no_cpu_baseline or args.forward_only):
         tok = args.oracle_tokens or default_oracle_tokens(w)
         # repeat the bounded sample until about 10 s of host work (at most 30 s)
         total_tok, total_s, reps = 0, 0.0, 0
@@ -357,12 +366,17 @@ def forward_plan(w: I.Workload) -> dict:
     return ssd.ssd_forward_plan(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk_size)
 
 
-def kernel_alg_bytes(name: str, w: I.Workload, plan: dict) -> float:
-    """Algorithmic bytes one launch of `name` must move at ssd_forward's span tiling: every operand read
-    once and every result written once, intermediates in float32 (chunk_cumsum: dt in, dA_cumsum and dt
-    rows out, B and C in with their float16 copies out; chunk_state: x, the float16 B, the dA_cumsum and dt
-    rows, the span states out; state_passing: span states in and out, span decays, init and final;
-    chunk_scan: x in, y out, float16 B and C, dA_cumsum and dt rows, one state per run of spans)."""
+def kernel_bytes(name: str, w: I.Workload, plan: dict) -> dict:
+    """Bytes one launch of `name` moves at ssd_forward's span tiling, split as the measurement rule of the
+    path counts them.  "compulsory": the method's own inputs read and outputs written by that launch (x, y,
+    B, C in bfloat16; dt; init and final state) -- the roofline credits only these.  "intermediate": the
+    method's intermediates it reads or writes once each (dA_cumsum and dt rows and span states in float32,
+    the float16 copies of B and C), reported beside it and never credited.
+      chunk_cumsum:  dt, B and C in | dA_cumsum and dt rows out, float16 B and C out;
+      chunk_state:   x in | float16 B, dA_cumsum and dt rows in, span states and decays out;
+      state_passing: init in, final out | span states in and out, span decays in;
+      chunk_scan:    x in, y out, B and C in (as their float16 copies) | dA_cumsum and dt rows, one
+                     state per run of spans."""
     b, L, H, P, N, G, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk_size
     nc = w.nchunks
     nspans = -(-nc // plan["span_chunks"])
@@ -370,16 +384,38 @@ def kernel_alg_bytes(name: str, w: I.Workload, plan: dict) -> float:
     st = b * nspans * H * P * N * 4           # span states, float32
     bc = b * L * G * N * 2                     # one of B / C, 16-bit
     xy = b * L * H * P * 2                     # x or y, bfloat16
+    fin = b * H * P * N * 4
     if name == "chunk_cumsum":
-        return float(b * L * H * 4 + 2 * ncq * 4 + 4 * bc)  # dt in; dA_cumsum, dt rows out; B, C in and f16 copies out
+        return {"compulsory": float(b * L * H * 4 + 2 * bc), "intermediate": float(2 * ncq * 4 + 2 * bc)}
     if name == "chunk_state":
-        return float(xy + bc + 2 * ncq * 4 + st)
+        return {"compulsory": float(xy), "intermediate": float(bc + 2 * ncq * 4 + st + b * H * nspans * 4)}
     if name == "state_passing":
-        return float(2 * st + b * H * nspans * 4 + (2 if w.nonzero_init else 1) * b * H * P * N * 4)
+        return {"compulsory": float((2 if w.nonzero_init else 1) * fin),
+                "intermediate": float(2 * st + b * H * nspans * 4)}
     if name == "chunk_scan":  # reads the first span-start state of each run of scan_step spans
         runs = -(-nc // (plan["span_chunks"] * plan["scan_step"]))
-        return float(2 * xy + 2 * bc + 2 * ncq * 4 + b * runs * H * P * N * 4)
-    return float("nan")
+        return {"compulsory": float(2 * xy + 2 * bc), "intermediate": float(2 * ncq * 4 + b * runs * H * P * N * 4)}
+    return {"compulsory": float("nan"), "intermediate": float("nan")}
+
+
+def kernel_alg_bytes(name: str, w: I.Workload, plan: dict) -> float:
+    """The roofline's algorithmic bytes of one launch: its compulsory bytes (kernel_bytes)."""
+    return kernel_bytes(name, w, plan)["compulsory"]
+
+
+def pass_traffic(w: I.Workload, kernels: dict):
+    """DRAM bytes of one whole forward from the committed ncu capture (sum over the kernels of their
+    per-launch dram__bytes read + write times launches per step) against its compulsory bytes; None when
+    a kernel has no capture for this workload or its code changed since."""
+    total = 0.0
+    for name, st in kernels.items():
+        t = kernel_traffic(name, w)
+        if t is None:
+            return None
+        total += t
+    cb = compulsory_bytes(w)
+    return {"dram_bytes_per_step": total, "compulsory_bytes": cb, "ratio": round(total / cb, 3),
+            "source": "profiles/traffic.json (ncu dram__bytes_read.sum + dram__bytes_write.sum per launch)"}
 
 
 KERNEL_SOURCES = {"chunk_cumsum": "k_cumsum.cu", "chunk_state": "k_chunk_state.cu",

@@ -55,8 +55,16 @@
  *    accumulation.  B and C are copied to float16 (exact for magnitudes in
  *    [2^-14, 65504]; larger magnitudes saturate), x is converted the same way
  *    on chip, and the derived operands (decayed masked C B^T, carried state,
- *    decay-scaled x) are rounded once to float16.  Inputs are expected to lie
- *    in float16's range.
+ *    decay-scaled x) are rounded once to float16.  Every such conversion is
+ *    checked on chip: if any converted value (an input element, or a derived
+ *    one: an entry of the masked matrix, of the carried state or of a
+ *    decay-scaled x row) exceeds float16's largest finite magnitude 65504,
+ *    the library's range flag is raised and ssd_get_device_error() reports
+ *    SSD_ERR_RANGE; the outputs of that call are then not reliable.  A
+ *    result is never wrong without one of these two reports.  Inputs of
+ *    magnitude ~1 with a few thousand tokens stay far inside the range;
+ *    inputs scaled by ~256 (or a state that grows without decay to ~65504)
+ *    leave it.
  *  * No C++ exception crosses this boundary.  The library keeps no state
  *    between calls other than the optional profiling counters below; calls
  *    on different streams may run concurrently, except ssd_forward_noalloc,
@@ -84,7 +92,8 @@ typedef enum {
     SSD_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
     SSD_ERR_NO_MEMORY = 4,   /* workspace allocation failed (ssd_forward) */
     SSD_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (see ssd_get_device_error) */
-    SSD_ERR_SCRATCH_TOO_SMALL = 6 /* ssd_forward_noalloc: workload larger than its fixed scratch */
+    SSD_ERR_SCRATCH_TOO_SMALL = 6, /* ssd_forward_noalloc: workload larger than its fixed scratch */
+    SSD_ERR_RANGE = 7        /* a float16 tensor-core operand left float16's range (see ssd_get_device_error) */
 } ssd_status;
 
 /* Size in bytes of the fixed device scratch array used by ssd_forward_noalloc. */
@@ -326,12 +335,34 @@ SSD_API int ssd_step_ex(const void* x, const float* dt, const float* A, const vo
                         int dstate, const ssd_input_options* options, void* y, cudaStream_t stream);
 
 /*
- * ssd_get_device_error -- reads and clears the library's device error word
- * on the current device (synchronizes with the device).  Returns SSD_OK, or
- * SSD_ERR_TIMEOUT if a kernel's bounded wait gave up since the last read, or
- * SSD_ERR_CUDA if the read itself failed.
+ * ssd_get_device_error -- reads and clears the library's device error words
+ * on the current device (synchronizes with the device).  Returns SSD_OK;
+ * SSD_ERR_TIMEOUT if a kernel's bounded wait gave up since the last read
+ * (the kernel then skipped the rest of its work and returned, so the outputs
+ * of that call are incomplete while the device stays usable); otherwise
+ * SSD_ERR_RANGE if a value converted to a float16 tensor-core operand was
+ * outside float16's finite range since the last read; or SSD_ERR_CUDA if the
+ * read itself failed.
  */
 SSD_API int ssd_get_device_error(void);
+
+/*
+ * Test hooks of the failure path (no counterpart in the pages; process-wide,
+ * they affect every later launch until reset).
+ * ssd_debug_set_wait_limit_ns(ns) sets the time after which a pipeline wait
+ * inside the tensor-core kernels (chunk_state, chunk_scan) gives up; 0
+ * restores the default of one second.  The teardown drains that let every
+ * copy and product already issued complete before a kernel releases shared
+ * memory and TMEM keep their own one-second limit.
+ * ssd_debug_stall(kinds) makes every later launch of the selected kernel
+ * kinds (bit k = kind k of ssd_kernel_name; 0 turns it off) first wait on a
+ * barrier that nothing completes: the wait runs out after the wait limit,
+ * the kernel abandons its work and returns, and ssd_get_device_error()
+ * reports SSD_ERR_TIMEOUT.  A stalled call's outputs are incomplete.
+ * Both return SSD_OK.
+ */
+SSD_API int ssd_debug_set_wait_limit_ns(unsigned long long ns);
+SSD_API int ssd_debug_stall(int kinds);
 
 /*
  * Profiling counters (host side, process-wide, not thread-safe).

@@ -19,6 +19,7 @@ SSD_ERR_CUDA = 3
 SSD_ERR_NO_MEMORY = 4
 SSD_ERR_TIMEOUT = 5
 SSD_ERR_SCRATCH_TOO_SMALL = 6
+SSD_ERR_RANGE = 7
 SSD_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 # name -> (restype, argtypes); the exported surface of include/ssd.h
@@ -37,6 +38,8 @@ SIGNATURES = {
     "ssd_forward_ex": (_i, [_p] * 7 + [_i] * 7 + [_p, _p, _p, _p]),
     "ssd_step_ex": (_i, [_p] * 7 + [_i] * 5 + [_p, _p, _p]),
     "ssd_get_device_error": (_i, []),
+    "ssd_debug_set_wait_limit_ns": (_i, [ctypes.c_ulonglong]),
+    "ssd_debug_stall": (_i, [_i]),
     "ssd_profile_enable": (_i, [_i]),
     "ssd_profile_reset": (_i, []),
     "ssd_profile_read": (_i, [_p, _p, _i, _p]),

@@ -12,6 +12,32 @@ namespace ssd {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Per-launch failure handling of the pipelined tensor-core kernels.
+//   err[0]   code of the first bounded wait that gave up (0: none) -- reported as SSD_ERR_TIMEOUT;
+//   err[1]   non-zero once a value converted to a float16 tensor-core operand fell outside
+//            float16's finite range (|v| > 65504) -- reported as SSD_ERR_RANGE.
+//   wait_ns  limit of every pipeline wait (drains at teardown use kDrainNs instead);
+//   stall    test hook: the kernel first waits on a barrier that nothing completes, so that the
+//            wait runs out and the abort path runs (see ssd_debug_stall in ssd.h).
+struct Ctl {
+    int* err = nullptr;
+    unsigned long long wait_ns = 1000000000ull;
+    int stall = 0;
+};
+
+// Limit of the teardown drains (copies and products already issued always complete).
+constexpr unsigned long long kDrainNs = 1000000000ull;
+
+// Largest finite float16 magnitude.
+constexpr float kF16Max = 65504.f;
+
+// Called by all 32 lanes of a warp: raises the float16 range flag if any lane saw a value whose
+// magnitude `mx` (the largest it converted to float16, or NaN) is not finite in float16.
+__device__ __forceinline__ void flag_f16_range(int* err, float mx) {
+    const bool bad = !(mx <= kF16Max);
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0 && err != nullptr) atomicOr(err + 1, 1);
+}
+
 // Problem dimensions shared by every launch.
 struct Dims {
     int batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nchunks;
@@ -99,15 +125,16 @@ int launch_end(int kind, cudaStream_t s);  // returns SSD_OK or SSD_ERR_CUDA
 int launch_chunk_cumsum(const float* dt, const float* A, const Dims& d, float* cs, float* dtt,
                         cudaStream_t s);
 // chunk_cumsum plus, in the same launch, the float16 copies of B and C
+// (the range flag of `err` is raised if a copied value exceeds float16's range)
 int launch_chunk_cumsum_bc(const float* dt, const float* A, const Dims& d, float* cs, float* dtt,
-                           const __nv_bfloat16* B, const __nv_bfloat16* C, __half* B16, __half* C16, cudaStream_t s,
-                           const DtOpts& dto = DtOpts());
+                           const __nv_bfloat16* B, const __nv_bfloat16* C, __half* B16, __half* C16, int* err,
+                           cudaStream_t s, const DtOpts& dto = DtOpts());
 // B, C (bf16) -> float16 copies for the tensor-core products (see k_convert.cu)
 int launch_bc_to_f16(const __nv_bfloat16* B, const __nv_bfloat16* C, const Dims& d, __half* B16, __half* C16,
-                     cudaStream_t s);
+                     int* err, cudaStream_t s);
 // B and C below are the float16 copies; x stays bfloat16.
 int launch_chunk_state_span(const __nv_bfloat16* x, const __half* B, const float* dtt, const float* cs,
-                            int span_chunks, const Dims& d, float* S, float* span_decay, int* err,
+                            int span_chunks, const Dims& d, float* S, float* span_decay, const Ctl& ctl,
                             cudaStream_t s);
 int launch_state_passing(const float* S, const float* cs, const float* init, const Dims& d,
                          float* states, float* final_state, cudaStream_t s);
@@ -118,7 +145,7 @@ int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_ste
 // span_chunks * state_step chunks, each starting from every state_step-th of those states.
 int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C,
                            const float* dtt, const float* cs, const float* D, const float* span_states,
-                           int span_chunks, const Dims& d, __nv_bfloat16* y, int* err, cudaStream_t s,
+                           int span_chunks, const Dims& d, __nv_bfloat16* y, const Ctl& ctl, cudaStream_t s,
                            const OutOpts& oo = OutOpts(), int state_step = 1);
 
 // one recurrent step for every (batch, head): state updated in place, y for the token (k_step.cu)

@@ -79,7 +79,6 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
     else return mbar_wait_bounded(bar, parity, abort, err, code, limit_ns);
 }
 
-constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr int kThreads = 480;
 constexpr int kTile = 16384;  // 128 rows x 128 B
 constexpr int kWarpTma = 12, kWarpMma = 13, kWarpTmaBC = 14;
@@ -142,7 +141,7 @@ struct ScanArgs {
     __nv_bfloat16* y;   // (b, L, H, P)
     int y32;            // y is 32-byte aligned: rows are stored in 32-byte pieces
     int z32;            // the gate z is 32-byte aligned: rows are loaded in 32-byte pieces
-    int* err;
+    Ctl ctl;            // error words, wait limit, stall hook
     OutOpts oo;  // D per channel (then D is null: no diagonal skip) and the z gate
 };
 
@@ -153,6 +152,7 @@ struct Bars {
     uint64_t cb_full[2], m_ready[2], y_full[2], y_free[2];
     uint64_t xs_ready, xs_free, h_ready, state_done, final_mma;
     uint64_t hs_ready[2], hs_free[2];  // RING: state-copy slot k filled (128 arrivals) / read by C h
+    uint64_t stall;                    // never completed: the test hook's wait runs out on it
 };
 
 static_assert(sizeof(Bars) <= 512, "barriers fit their shared-memory slot");
@@ -256,15 +256,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar->hs_ready[i], 128);
             mbar_init(&bar->hs_free[i], 1);
         }
+        mbar_init(&bar->stall, 1);
         abort_sh = 0;
         fence_barrier_init();
     }
+    int* const err = a.ctl.err;
+    const uint64_t wait_ns = a.ctl.wait_ns;
     if (K::SZ_ZERO > 0) {  // rows that pad the state-update A operand to 128 (N = 64)
         uint4* z = reinterpret_cast<uint4*>(smem + K::OFF_ZERO);
         for (int i = threadIdx.x; i < K::SZ_ZERO / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     if (OPT && a.oo.Dp != nullptr) {
+        float dmx = 0.f;
         // diag(D[h, :]) as the B operand of DX: row n (output channel) holds D[h][n] at column k = n.
         // 128B swizzle: row n at (n / 8) * 1024 + (n % 8) * 128, 16-byte chunk j stored at chunk j ^ (n % 8).
         for (int c = threadIdx.x; c < 512; c += kThreads) {
@@ -272,7 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = (c & 7) ^ (n & 7);  // logical chunk: columns 8j .. 8j+7
             uint32_t v = 0u;  // the diagonal element, placed in its 32-bit word of the chunk
             if (j == (n >> 3)) {
-                const __half dv = __float2half_rn(a.oo.Dp[h * 64 + n]);
+                const float df = a.oo.Dp[h * 64 + n];
+                dmx = fmaxf(dmx, fabsf(df));
+                const __half dv = __float2half_rn(df);
                 const uint32_t bits = *reinterpret_cast<const uint16_t*>(&dv);
                 v = (n & 1) ? (bits << 16) : bits;
             }
@@ -281,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_uint4(wi == 0 ? v : 0u, wi == 1 ? v : 0u, wi == 2 ? v : 0u, wi == 3 ? v : 0u);
         }
         fence_proxy_async_smem();
+        flag_f16_range(err, dmx);
     }
     if (warp == kWarpMma) {
         tmem_alloc(&tmem_base_sh, K::TCOLS);
@@ -301,12 +308,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpTma) {
         // ------------------------------------------------------ x / dA_cumsum / dt producer
         if (lane == 0) {
+            if (a.ctl.stall) wait_bounded<!OPT>(&bar->stall, 0, abort_flag, err, 30, wait_ns);
             int nissued = 0;  // loads issued; buffer i took those with index % NX == i
             const int64_t rowlen = (int64_t)d.nchunks * Q;
-            for (int sb = 0; sb < nsb; ++sb) {
+            for (int sb = 0; sb < nsb && !*abort_flag; ++sb) {
                 const int t0 = (int)(ts + sb * 128);
                 const int xb = sb % K::NX;
-                if (!wait_bounded<!OPT>(&bar->x_empty[xb], ((sb / K::NX) & 1) ^ 1, abort_flag, a.err, 1, kWaitNs))
+                if (!wait_bounded<!OPT>(&bar->x_empty[xb], ((sb / K::NX) & 1) ^ 1, abort_flag, err, 1, wait_ns))
                     break;
                 // this sub-block's rows of dA_cumsum and dt (contiguous per (b, h); at most 128)
                 const uint32_t cdb = (uint32_t)min((int64_t)128, rowlen - t0) * 4u;
@@ -321,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < K::NX; ++i) {
                 const int issued = (nissued + K::NX - 1 - i) / K::NX;
-                if (issued > 0) wait_bounded<!OPT>(&bar->x_full[i], (issued - 1) & 1, abort_flag, a.err, 3, kWaitNs);
+                if (issued > 0) mbar_wait_drain(&bar->x_full[i], (issued - 1) & 1, err, 103, kDrainNs);
             }
         }
     } else if (warp == kWarpTmaBC) {
@@ -330,12 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0;
             bool ok = true;
             int nissued = 0;  // stage loads issued; stage i took those with index % NST == i
-            for (int sb = 0; sb < nsb && ok; ++sb) {
+            for (int sb = 0; sb < nsb && ok && !*abort_flag; ++sb) {
                 const int t0 = (int)(ts + sb * 128);
                 for (int nb = 0; nb < K::NBLK && ok; ++nb, ++it) {
                     const int st = it % K::NST;
-                    ok = wait_bounded<!OPT>(&bar->bc_empty[st], ((it / K::NST) & 1) ^ 1, abort_flag, a.err, 2,
-                                           kWaitNs);
+                    ok = wait_bounded<!OPT>(&bar->bc_empty[st], ((it / K::NST) & 1) ^ 1, abort_flag, err, 2,
+                                           wait_ns);
                     if (!ok) break;
                     uint8_t* sC = smem + K::OFF_BC + st * K::SZ_STAGE;
                     uint8_t* sB = sC + K::SZ_C;
@@ -351,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < K::NST; ++i) {
                 const int issued = (nissued + K::NST - 1 - i) / K::NST;
-                if (issued > 0) wait_bounded<!OPT>(&bar->bc_full[i], (issued - 1) & 1, abort_flag, a.err, 3, kWaitNs);
+                if (issued > 0) mbar_wait_drain(&bar->bc_full[i], (issued - 1) & 1, err, 104, kDrainNs);
             }
         }
     } else if (warp == kWarpMma) {
@@ -442,11 +450,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int st = it % K::NST;
                         const int use = f * (K::NBLK / 2) + nb / 2;  // RING: use index of slot nb % 2
                         if (nb > 0) {
-                            if (!wait_bounded<!OPT>(&bar->bc_full[st], (it / K::NST) & 1, abort_flag, a.err, 8,
-                                                   kWaitNs))
+                            if (!wait_bounded<!OPT>(&bar->bc_full[st], (it / K::NST) & 1, abort_flag, err, 8,
+                                                   wait_ns))
                                 return false;
                             if (K::RING &&
-                                !wait_bounded<!OPT>(&bar->hs_ready[nb & 1], use & 1, abort_flag, a.err, 9, kWaitNs))
+                                !wait_bounded<!OPT>(&bar->hs_ready[nb & 1], use & 1, abort_flag, err, 9, wait_ns))
                                 return false;
                             tc_fence_after();
                         }
@@ -492,27 +500,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     __nanosleep(32);  // leave the issue slots to the math warps sharing this scheduler
                     if (*abort_flag) break;
-                    if (globaltimer_ns() - last > kWaitNs) {
+                    if (globaltimer_ns() - last > wait_ns) {
                         *abort_flag = 1;
-                        atomicExch(a.err, 4);
+                        atomicExch(err, 4);
                         break;
                     }
                 }
             }
             // every MMA retired before TMEM is released
             mma_commit(&bar->final_mma);
-            wait_bounded<!OPT>(&bar->final_mma, 0, abort_flag, a.err, 10, kWaitNs);
+            mbar_wait_drain(&bar->final_mma, 0, err, 110, kDrainNs);
         }
     } else if (warp < 4) {
         // ------------------------------------------------------ mask warpgroup: CB -> M
         const int r = threadIdx.x;  // TMEM lane == row
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const float Dh = (a.D != nullptr) ? a.D[h] : 0.f;  // the skip term rides on M's diagonal
+        float mx = 0.f;  // largest |M| converted to float16 (range flag)
         for (int sb = 0; sb < nsb; ++sb) {
             const int k = sb % K::NBUF;
             const int ub = sb % 3;
-            bool ok = wait_bounded<!OPT>(&bar->uv_ready[ub], (sb / 3) & 1, abort_flag, a.err, 11, kWaitNs) &&
-                      wait_bounded<!OPT>(&bar->cb_full[k], (sb / K::NBUF) & 1, abort_flag, a.err, 12, kWaitNs);
+            bool ok = wait_bounded<!OPT>(&bar->uv_ready[ub], (sb / 3) & 1, abort_flag, err, 11, wait_ns) &&
+                      wait_bounded<!OPT>(&bar->cb_full[k], (sb / K::NBUF) & 1, abort_flag, err, 12, wait_ns);
             ok = __all_sync(0xffffffffu, ok);  // TMEM loads/stores below are warp-collective
             if (!ok) break;
             tc_fence_after();
@@ -536,8 +545,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int jj = 0; jj < 32; jj += 2) {
                             const int j = q * 32 + jj;
-                            o[jj >> 1] = pack_f16x2(__uint_as_float(v[jj]) * (ar * sbc[j]),
-                                                    __uint_as_float(v[jj + 1]) * (ar * sbc[j + 1]));
+                            const float m0 = __uint_as_float(v[jj]) * (ar * sbc[j]);
+                            const float m1 = __uint_as_float(v[jj + 1]) * (ar * sbc[j + 1]);
+                            mx = fmaxf(mx, fmaxf(fabsf(m0), fabsf(m1)));
+                            o[jj >> 1] = pack_f16x2(m0, m1);
                         }
                     } else {
                         // diagonal block: exact per-element exponent, causal mask, D on the diagonal
@@ -552,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             m1 = (j1 <= r) ? m1 : 0.f;
                             m0 += (j0 == r) ? Dh : 0.f;
                             m1 += (j1 == r) ? Dh : 0.f;
+                            mx = fmaxf(mx, fmaxf(fabsf(m0), fabsf(m1)));
                             o[jj >> 1] = pack_f16x2(m0, m1);
                         }
                     }
@@ -563,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&bar->m_ready[k]);
             mbar_arrive(&bar->u_free[ub]);
         }
+        flag_f16_range(err, mx);
     } else if (warp < 8) {
         // ------------------------------------------------------ state warpgroup
         // A failed wait turns the remaining work into no-ops but keeps every arrival.
@@ -571,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t PN = (int64_t)d.headdim * N;
         const float* init = a.init + (((int64_t)b * a.state_spans + (int64_t)s * a.state_step) * H + h) * PN;
         bool ok = true;
+        float mx = 0.f;        // largest |value| converted to float16: x, w x, the state copy (range flag)
         float prev_raw = 0.f;  // raw dA_cumsum of the token before this sub-block (same chunk)
         for (int sb = 0; sb < nsb; ++sb) {
             const int64_t t0 = ts + sb * 128;
@@ -581,8 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 1. u, dt and the factorized column weights of this sub-block, each computed by its
             //    own thread from the dA_cumsum/dt rows that arrived with the x tile
             if (sb >= 3)
-                ok = ok && wait_bounded<!OPT>(&bar->u_free[ub], ((sb / 3) - 1) & 1, abort_flag, a.err, 17, kWaitNs);
-            ok = ok && wait_bounded<!OPT>(&bar->x_full[xb], (sb / K::NX) & 1, abort_flag, a.err, 13, kWaitNs);
+                ok = ok && wait_bounded<!OPT>(&bar->u_free[ub], ((sb / 3) - 1) & 1, abort_flag, err, 17, wait_ns);
+            ok = ok && wait_bounded<!OPT>(&bar->x_full[xb], (sb / K::NX) & 1, abort_flag, err, 13, wait_ns);
             ok = __all_sync(0xffffffffu, ok);
             const float* scs = reinterpret_cast<const float*>(smem + K::OFF_CD + xb * 1024);
             const int p0 = (int)(t0 % Q);
@@ -610,10 +624,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float dsb = exp2f(ulast);
             // 2. x tile -> float16 in place, and X' = w x into the single X' buffer once the
             //    previous sub-block's state update has read it
-            if (sb > 0) ok = ok && wait_bounded<!OPT>(&bar->xs_free, (sb - 1) & 1, abort_flag, a.err, 14, kWaitNs);
+            if (sb > 0) ok = ok && wait_bounded<!OPT>(&bar->xs_free, (sb - 1) & 1, abort_flag, err, 14, wait_ns);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 const float w = valid ? fast_exp2(fminf(ulast - u, 0.f)) * dtv : 0.f;
+                const float wr = fmaxf(w, 1.f);
                 uint8_t* xrow = smem + K::OFF_X + xb * kTile;
                 uint8_t* xsrow = smem + K::OFF_XS;
 #pragma unroll
@@ -627,6 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 fv = __bfloat1622float2(p2[e]);
+                        mx = fmaxf(mx, fmaxf(fabsf(fv.x), fabsf(fv.y)) * wr);  // x and w x
                         x4[e] = pack_f16x2(fv.x, fv.y);
                         w4[e] = pack_f16x2(fv.x * w, fv.y * w);
                     }
@@ -638,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&bar->xs_ready);
             // 3. state h_sb -> float16 copy for C h, and h <- 2^(u_last) h in TMEM
             if (sb > 0) {
-                ok = ok && wait_bounded<!OPT>(&bar->state_done, (sb - 1) & 1, abort_flag, a.err, 15, kWaitNs);
+                ok = ok && wait_bounded<!OPT>(&bar->state_done, (sb - 1) & 1, abort_flag, err, 15, wait_ns);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
             }
@@ -666,12 +682,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (K::RING) {  // the slot's previous n-block has been read by its C h product
                         const int use = sb * (K::NBLK / 2) + nb / 2;
                         if (use >= 1)
-                            ok = wait_bounded<!OPT>(&bar->hs_free[nb & 1], (use - 1) & 1, abort_flag, a.err, 19,
-                                                   kWaitNs);
+                            ok = wait_bounded<!OPT>(&bar->hs_free[nb & 1], (use - 1) & 1, abort_flag, err, 19,
+                                                   wait_ns);
                         ok = __all_sync(0xffffffffu, ok);
                         if (!ok) break;
                     }
                     if (real) {
+#pragma unroll
+                        for (int p = 0; p < 64; ++p) mx = fmaxf(mx, fabsf(hv[p]));
                         // smem row: state index n, or its row in the ring slot
                         const int hr = K::RING ? r : nb * K::NB + r;
                         uint8_t* hdst = K::RING ? hbase + (nb & 1) * K::SZ_HS : hbase;
@@ -705,6 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mbar_arrive(&bar->h_ready);
         }
+        flag_f16_range(err, mx);
     } else if (warp < 12) {
         // ------------------------------------------------------ epilogue warpgroup
         const int r = threadIdx.x - 256;  // TMEM lane (warp % 4 == warp - 8)
@@ -721,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nv = (int)min((int64_t)128, te - t0);
             const int k = sb % K::NBUF;
             const int ub = sb % 3;
-            ok = ok && wait_bounded<!OPT>(&bar->y_full[k], (sb / K::NBUF) & 1, abort_flag, a.err, 16, kWaitNs);
+            ok = ok && wait_bounded<!OPT>(&bar->y_full[k], (sb / K::NBUF) & 1, abort_flag, err, 16, wait_ns);
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             const float e = fast_exp2(fminf(sU[ub * 512 + r], 0.f));
@@ -808,7 +827,7 @@ int launch_scan_n(const __nv_bfloat16* x, const __half* B, const __half* C, cons
 
 int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C, const float* dtt,
                            const float* cs, const float* D, const float* span_states, int span_chunks, const Dims& d,
-                           __nv_bfloat16* y, int* err, cudaStream_t s, const OutOpts& oo, int state_step) {
+                           __nv_bfloat16* y, const Ctl& ctl, cudaStream_t s, const OutOpts& oo, int state_step) {
     ScanArgs a;
     a.d = d;
     a.span_chunks = span_chunks * state_step;
@@ -822,7 +841,7 @@ int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half
     a.y = y;
     a.y32 = (reinterpret_cast<uintptr_t>(y) & 31u) == 0;
     a.z32 = (reinterpret_cast<uintptr_t>(oo.z) & 31u) == 0;
-    a.err = err;
+    a.ctl = ctl;
     a.oo = oo;
     if (oo.Dp != nullptr) a.D = nullptr;  // the skip moves from M's diagonal to the X diag(D) product
     const bool opt = oo.Dp != nullptr || oo.z != nullptr;

@@ -36,7 +36,6 @@ namespace {
 
 using namespace sm100;
 
-constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr int kMaxSpanChunks = 256;
 
 // HH heads of one B group per CTA: they share the B tile, and one MMA per
@@ -77,7 +76,7 @@ struct StateArgs {
     const float* dtt;   // (b, H, nc, Q)
     float* S;           // (b, nspans, H, P, N)
     float* span_decay;  // (b, H, nspans) log2 units, or null
-    int* err;
+    Ctl ctl;            // error words, wait limit, stall hook
 };
 
 template <int N, int HH>
@@ -91,6 +90,7 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
     uint64_t* xs_ready = full + K::NST;
     uint64_t* empty = xs_ready + K::NST;
     uint64_t* acc_done = empty + K::NST;
+    uint64_t* stall_bar = acc_done + 1;  // never completed: the test hook's wait runs out on it
     float* Rs = reinterpret_cast<float*>(smem + K::OFF_R);  // head hh at hh * kMaxSpanChunks
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
             mbar_init(&empty[i], 1);
         }
         mbar_init(acc_done, 1);
+        mbar_init(stall_bar, 1);
         abort_sh = 0;
         fence_barrier_init();
     }
@@ -157,14 +158,17 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
     tc_fence_after();
     const uint32_t tm = tmem_base_sh;
     volatile int* abort_flag = &abort_sh;
+    int* const err = a.ctl.err;
+    const uint64_t wait_ns = a.ctl.wait_ns;
 
     if (warp == K::WARP_TMA) {
         // TMA producer: per stage the HH x tiles, the B boxes and the heads' dA_cumsum / dt rows
         if (lane == 0) {
+            if (a.ctl.stall) mbar_wait_bounded(stall_bar, 0, abort_flag, err, 20, wait_ns);
             int nissued = 0;  // stage loads issued; stage i took those with index % NST == i
-            for (int kb = 0; kb < nblk; ++kb) {
+            for (int kb = 0; kb < nblk && !*abort_flag; ++kb) {
                 const int st = kb % K::NST;
-                if (!mbar_wait_bounded_inline(&empty[st], ((kb / K::NST) & 1) ^ 1, abort_flag, a.err, 21, kWaitNs)) break;
+                if (!mbar_wait_bounded_inline(&empty[st], ((kb / K::NST) & 1) ^ 1, abort_flag, err, 21, wait_ns)) break;
                 uint8_t* sX = smem + st * K::SZ_STAGE;
                 const int t0 = (int)(ts + (int64_t)kb * K::TB);
                 const uint32_t cdb = (uint32_t)min((int64_t)K::TB, rowlen - t0) * 4u;
@@ -183,9 +187,9 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
                 ++nissued;
             }
 #pragma unroll
-            for (int i = 0; i < K::NST; ++i) {
+            for (int i = 0; i < K::NST; ++i) {  // every issued load has landed before teardown
                 const int issued = (nissued + K::NST - 1 - i) / K::NST;
-                if (issued > 0) mbar_wait_bounded_inline(&full[i], (issued - 1) & 1, abort_flag, a.err, 22, kWaitNs);
+                if (issued > 0) mbar_wait_drain(&full[i], (issued - 1) & 1, err, 122, kDrainNs);
             }
         }
     } else if (warp == K::WARP_MMA) {
@@ -194,7 +198,7 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
             constexpr uint32_t idesc = idesc_fp16(128, 64 * HH, true, true);
             for (int kb = 0; kb < nblk; ++kb) {
                 const int st = kb % K::NST;
-                if (!mbar_wait_bounded_inline(&xs_ready[st], (kb / K::NST) & 1, abort_flag, a.err, 23, kWaitNs)) break;
+                if (!mbar_wait_bounded_inline(&xs_ready[st], (kb / K::NST) & 1, abort_flag, err, 23, wait_ns)) break;
                 tc_fence_after();
                 const uint32_t sX = smem_u32(smem + st * K::SZ_STAGE);
                 const uint32_t sB = sX + K::OFF_B;
@@ -210,6 +214,7 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
                 mma_commit(&empty[st]);
             }
             mma_commit(acc_done);
+            mbar_wait_drain(acc_done, 0, err, 125, kDrainNs);  // every product retired before TMEM is freed
         }
     } else {
         // scaling warpgroup(s): thread t scales token row t % TB of the x tiles of heads
@@ -220,9 +225,10 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
         constexpr int kHeadStep = 128 * K::SW / K::TB;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         bool ok = true;
+        float mx = 0.f;  // largest |w x| converted to float16 (range flag)
         for (int kb = 0; kb < nblk; ++kb) {
             const int st = kb % K::NST;
-            ok = ok && mbar_wait_bounded_inline(&full[st], (kb / K::NST) & 1, abort_flag, a.err, 24, kWaitNs);
+            ok = ok && mbar_wait_bounded_inline(&full[st], (kb / K::NST) & 1, abort_flag, err, 24, wait_ns);
             if (ok) {
                 const int64_t t = ts + (int64_t)kb * K::TB + rr;
                 uint8_t* stage = smem + st * K::SZ_STAGE;
@@ -244,7 +250,9 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float2 f = __bfloat1622float2(p2[e]);
-                            o2[e] = __floats2half2_rn(f.x * w, f.y * w);
+                            const float a0 = f.x * w, a1 = f.y * w;
+                            mx = fmaxf(mx, fmaxf(fabsf(a0), fabsf(a1)));
+                            o2[e] = __floats2half2_rn(a0, a1);
                         }
                         *reinterpret_cast<uint4*>(xrow + sw128_offset(rr, ch)) = o;
                     }
@@ -253,7 +261,8 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
             }
             mbar_arrive(&xs_ready[st]);
         }
-        ok = ok && mbar_wait_bounded_inline(acc_done, 0, abort_flag, a.err, 25, kWaitNs);
+        flag_f16_range(err, mx);
+        ok = ok && mbar_wait_bounded_inline(acc_done, 0, abort_flag, err, 25, wait_ns);
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         if (ok) {
@@ -315,7 +324,8 @@ int launch_state_n(const __nv_bfloat16* x, const __half* B, const StateArgs& a, 
 }  // namespace
 
 int launch_chunk_state_span(const __nv_bfloat16* x, const __half* B, const float* dtt, const float* cs,
-                            int span_chunks, const Dims& d, float* S, float* span_decay, int* err, cudaStream_t s) {
+                            int span_chunks, const Dims& d, float* S, float* span_decay, const Ctl& ctl,
+                            cudaStream_t s) {
     if (span_chunks < 1 || span_chunks > kMaxSpanChunks) return SSD_ERR_UNSUPPORTED;
     StateArgs a;
     a.d = d;
@@ -325,7 +335,7 @@ int launch_chunk_state_span(const __nv_bfloat16* x, const __half* B, const float
     a.dtt = dtt;
     a.S = S;
     a.span_decay = span_decay;
-    a.err = err;
+    a.ctl = ctl;
     switch (d.dstate) {
         case 64: return launch_state_n<64>(x, B, a, s);
         case 128: return launch_state_n<128>(x, B, a, s);

@@ -25,11 +25,18 @@ namespace {
 constexpr int kHeads = 8;
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t v) {
+// two bfloat16 -> two float16, saturating; mx tracks the largest magnitude seen (for the range flag)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t v, float& mx) {
     const float lo = __uint_as_float(v << 16);
     const float hi = __uint_as_float(v & 0xffff0000u);
-    const __half2 h = __floats2half2_rn(fminf(fmaxf(lo, -65504.f), 65504.f), fminf(fmaxf(hi, -65504.f), 65504.f));
+    mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+    const __half2 h = __floats2half2_rn(fminf(fmaxf(lo, -kF16Max), kF16Max), fminf(fmaxf(hi, -kF16Max), kF16Max));
     return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 cvt16(const uint4& v, float& mx) {
+    return make_uint4(bf16x2_to_f16x2_sat(v.x, mx), bf16x2_to_f16x2_sat(v.y, mx), bf16x2_to_f16x2_sat(v.z, mx),
+                      bf16x2_to_f16x2_sat(v.w, mx));
 }
 
 template <int Q>
@@ -39,7 +46,7 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
                                                                 const uint4* __restrict__ bsrc,
                                                                 const uint4* __restrict__ csrc, uint4* __restrict__ bdst,
                                                                 uint4* __restrict__ cdst, int64_t bc16,
-                                                                DtOpts dto) {
+                                                                int* err, DtOpts dto) {
     // tile[h][i + i / 8]: one padding word per 8 positions, so that lanes reading runs of
     // consecutive positions spread over the banks
     __shared__ float tile[kHeads][Q + Q / 8];
@@ -96,6 +103,7 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
     }
     // the rest of the B / C share, independent of the scan
     if (bc16 > 0) {
+        float mx = 0.f;
         for (; i + 3 * kThreads < hi; i += 4 * kThreads) {  // four chunks of B and C in flight
             if (!first) {
 #pragma unroll
@@ -107,19 +115,16 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
             first = false;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                bdst[i + u * kThreads] = make_uint4(bf16x2_to_f16x2_sat(vb[u].x), bf16x2_to_f16x2_sat(vb[u].y),
-                                                    bf16x2_to_f16x2_sat(vb[u].z), bf16x2_to_f16x2_sat(vb[u].w));
-                cdst[i + u * kThreads] = make_uint4(bf16x2_to_f16x2_sat(vc[u].x), bf16x2_to_f16x2_sat(vc[u].y),
-                                                    bf16x2_to_f16x2_sat(vc[u].z), bf16x2_to_f16x2_sat(vc[u].w));
+                bdst[i + u * kThreads] = cvt16(vb[u], mx);
+                cdst[i + u * kThreads] = cvt16(vc[u], mx);
             }
         }
         for (; i < hi; i += kThreads) {
             const uint4 vb = __ldg(bsrc + i), vc = __ldg(csrc + i);
-            bdst[i] = make_uint4(bf16x2_to_f16x2_sat(vb.x), bf16x2_to_f16x2_sat(vb.y), bf16x2_to_f16x2_sat(vb.z),
-                                 bf16x2_to_f16x2_sat(vb.w));
-            cdst[i] = make_uint4(bf16x2_to_f16x2_sat(vc.x), bf16x2_to_f16x2_sat(vc.y), bf16x2_to_f16x2_sat(vc.z),
-                                 bf16x2_to_f16x2_sat(vc.w));
+            bdst[i] = cvt16(vb, mx);
+            cdst[i] = cvt16(vc, mx);
         }
+        flag_f16_range(err, mx);
     }
     __syncthreads();
     const int h = h0 + warp;
@@ -154,8 +159,8 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
 }  // namespace
 
 int launch_chunk_cumsum_bc(const float* dt, const float* A, const Dims& d, float* cs, float* dtt,
-                           const __nv_bfloat16* B, const __nv_bfloat16* C, __half* B16, __half* C16, cudaStream_t s,
-                           const DtOpts& dto) {
+                           const __nv_bfloat16* B, const __nv_bfloat16* C, __half* B16, __half* C16, int* err,
+                           cudaStream_t s, const DtOpts& dto) {
     dim3 grid(d.nchunks, ceil_div(d.nheads, kHeads), d.batch);
     const int64_t bc16 = (B != nullptr) ? (int64_t)d.batch * d.seqlen * d.ngroups * d.dstate / 8 : 0;
     const uint4* bs = reinterpret_cast<const uint4*>(B);
@@ -164,16 +169,16 @@ int launch_chunk_cumsum_bc(const float* dt, const float* A, const Dims& d, float
     uint4* cd = reinterpret_cast<uint4*>(C16);
     launch_begin(kKindCumsum, s);
     switch (d.chunk_size) {
-        case 64: chunk_cumsum_kernel<64><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, dto); break;
-        case 128: chunk_cumsum_kernel<128><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, dto); break;
-        case 256: chunk_cumsum_kernel<256><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, dto); break;
+        case 64: chunk_cumsum_kernel<64><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, err, dto); break;
+        case 128: chunk_cumsum_kernel<128><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, err, dto); break;
+        case 256: chunk_cumsum_kernel<256><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, err, dto); break;
         default: return SSD_ERR_UNSUPPORTED;
     }
     return launch_end(kKindCumsum, s);
 }
 
 int launch_chunk_cumsum(const float* dt, const float* A, const Dims& d, float* cs, float* dtt, cudaStream_t s) {
-    return launch_chunk_cumsum_bc(dt, A, d, cs, dtt, nullptr, nullptr, nullptr, nullptr, s);
+    return launch_chunk_cumsum_bc(dt, A, d, cs, dtt, nullptr, nullptr, nullptr, nullptr, nullptr, s);
 }
 
 }  // namespace ssd

@@ -108,6 +108,24 @@ __device__ __forceinline__ bool mbar_wait_bounded_inline(uint64_t* bar, uint32_t
     }
 }
 
+// Wait for the teardown drains: phase `parity` of `bar`, whatever the abort flag says, because a
+// CTA may not release shared memory or TMEM while a copy or a product it issued is still in
+// flight.  Bounded by `limit_ns` of global time only; on giving up it records `code` in *err.
+static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* err, int code,
+                                                    uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            if (err != nullptr) atomicExch(err, code);
+            return false;
+        }
+    }
+}
+
 // Bounded wait on phase `parity` of `bar`.  Gives up after `limit_ns` of
 // global time, or as soon as *abort becomes non-zero (another role already
 // gave up).  On giving up it sets *abort and records `code` in *err, and

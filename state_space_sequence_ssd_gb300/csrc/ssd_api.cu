@@ -4,6 +4,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <array>
 #include <functional>
@@ -146,10 +147,15 @@ Dims make_dims(int batch, int seqlen, int nheads, int headdim, int ngroups, int 
 
 }  // namespace
 
-// device error word (bounded waits that gave up set it)
-__device__ int g_ssd_device_error = 0;
+// device error words: [0] the code of a bounded wait that gave up, [1] the float16 range flag
+__device__ int g_ssd_device_error[2] = {0, 0};
 
 namespace {
+
+// Limit of the kernels' pipeline waits and the kernel kinds whose launches take the stall hook
+// (ssd_debug_set_wait_limit_ns, ssd_debug_stall).
+std::atomic<unsigned long long> g_wait_ns{1000000000ull};
+std::atomic<int> g_stall_kinds{0};
 
 // Device address of g_ssd_device_error on the current device (cached per device).
 int* device_error_ptr() {
@@ -189,6 +195,15 @@ cudaMemPool_t workspace_pool() {
         pools[dev] = p;
     }
     return pools[dev];
+}
+
+// Failure-handling arguments of one launch of kernel kind `kind`.
+Ctl make_ctl(int* err, int kind) {
+    Ctl c;
+    c.err = err;
+    c.wait_ns = g_wait_ns.load();
+    c.stall = (g_stall_kinds.load() >> kind) & 1;
+    return c;
 }
 
 int workspace_alloc(void** ptr, size_t bytes, cudaStream_t s) {
@@ -355,6 +370,9 @@ const char* ssd_status_string(int status) {
         case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA call or kernel launch failed";
         case SSD_ERR_NO_MEMORY: return "SSD_ERR_NO_MEMORY: workspace allocation failed";
         case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT: a bounded device-side wait gave up";
+        case SSD_ERR_RANGE:
+            return "SSD_ERR_RANGE: a value converted to a float16 tensor-core operand exceeded float16's range "
+                   "(|v| > 65504); that call's results are not reliable";
         case SSD_ERR_SCRATCH_TOO_SMALL:
             return "SSD_ERR_SCRATCH_TOO_SMALL: the workload needs more than the fixed scratch of ssd_forward_noalloc "
                    "(SSD_NOALLOC_SCRATCH_BYTES); use ssd_forward";
@@ -391,10 +409,10 @@ int ssd_chunk_state(const void* x, const void* B, const float* dt_t, const float
     void* ws = nullptr;
     if (workspace_alloc(&ws, nbc * sizeof(__half), stream) != SSD_OK) return SSD_ERR_NO_MEMORY;
     __half* B16 = static_cast<__half*>(ws);
-    r = launch_bc_to_f16(static_cast<const __nv_bfloat16*>(B), nullptr, d, B16, nullptr, stream);
+    r = launch_bc_to_f16(static_cast<const __nv_bfloat16*>(B), nullptr, d, B16, nullptr, err, stream);
     if (r == SSD_OK)
         r = launch_chunk_state_span(static_cast<const __nv_bfloat16*>(x), B16, dt_t, dA_cumsum, 1, d, chunk_states,
-                                    nullptr, err, stream);
+                                    nullptr, make_ctl(err, kKindChunkState), stream);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
     return r;
 }
@@ -434,10 +452,10 @@ int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_
     __half* B16 = static_cast<__half*>(ws);
     __half* C16 = B16 + nbc;
     r = launch_bc_to_f16(static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), d, B16, C16,
-                         stream);
+                         err, stream);
     if (r == SSD_OK)
         r = launch_chunk_scan_span(static_cast<const __nv_bfloat16*>(x), B16, C16, dt_t, dA_cumsum, D, states, 1, d,
-                                   static_cast<__nv_bfloat16*>(y), err, stream);
+                                   static_cast<__nv_bfloat16*>(y), make_ctl(err, kKindChunkScan), stream);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
     return r;
 }
@@ -484,13 +502,14 @@ int ssd_forward_ex(const void* x, const float* dt, const float* A, const void* B
     __half* C16 = B16 + nbc;
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     r = launch_chunk_cumsum_bc(dt, A, d, cs, dtt, static_cast<const __nv_bfloat16*>(B),
-                               static_cast<const __nv_bfloat16*>(C), B16, C16, stream, dto);
-    if (r == SSD_OK) r = launch_chunk_state_span(xb, B16, dtt, cs, span, d, S, dec, err, stream);
+                               static_cast<const __nv_bfloat16*>(C), B16, C16, err, stream, dto);
+    if (r == SSD_OK)
+        r = launch_chunk_state_span(xb, B16, dtt, cs, span, d, S, dec, make_ctl(err, kKindChunkState), stream);
     // span-level hop, in place: S becomes the span-start states
     if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
     if (r == SSD_OK)
-        r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream,
-                                   oo, forward_scan_step(d, span));
+        r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y),
+                                   make_ctl(err, kKindChunkScan), stream, oo, forward_scan_step(d, span));
     if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
     return r;
 }
@@ -522,12 +541,13 @@ int ssd_forward_noalloc(const void* x, const float* dt, const float* A, const vo
     __half* C16 = reinterpret_cast<__half*>(ws + l.off_C16);
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     r = launch_chunk_cumsum_bc(dt, A, d, cs, dtt, static_cast<const __nv_bfloat16*>(B),
-                               static_cast<const __nv_bfloat16*>(C), B16, C16, stream);
-    if (r == SSD_OK) r = launch_chunk_state_span(xb, B16, dtt, cs, span, d, S, dec, err, stream);
+                               static_cast<const __nv_bfloat16*>(C), B16, C16, err, stream);
+    if (r == SSD_OK)
+        r = launch_chunk_state_span(xb, B16, dtt, cs, span, d, S, dec, make_ctl(err, kKindChunkState), stream);
     if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
     if (r == SSD_OK)
-        r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y), err, stream,
-                                   OutOpts(), forward_scan_step(d, span));
+        r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y),
+                                   make_ctl(err, kKindChunkScan), stream, OutOpts(), forward_scan_step(d, span));
     return r;
 }
 
@@ -587,10 +607,23 @@ int ssd_step_multi(const void* x, const float* dt, const float* A, const void* B
 }
 
 int ssd_get_device_error(void) {
-    int v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, g_ssd_device_error, sizeof(int)) != cudaSuccess) return SSD_ERR_CUDA;
-    if (v != 0 && cudaMemcpyToSymbol(g_ssd_device_error, &zero, sizeof(int)) != cudaSuccess) return SSD_ERR_CUDA;
-    return v == 0 ? SSD_OK : SSD_ERR_TIMEOUT;
+    int v[2] = {0, 0};
+    const int zero[2] = {0, 0};
+    if (cudaMemcpyFromSymbol(v, g_ssd_device_error, sizeof(v)) != cudaSuccess) return SSD_ERR_CUDA;
+    if ((v[0] != 0 || v[1] != 0) && cudaMemcpyToSymbol(g_ssd_device_error, zero, sizeof(zero)) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (v[0] != 0) return SSD_ERR_TIMEOUT;
+    return v[1] != 0 ? SSD_ERR_RANGE : SSD_OK;
+}
+
+int ssd_debug_set_wait_limit_ns(unsigned long long ns) {
+    g_wait_ns.store(ns == 0 ? 1000000000ull : ns);
+    return SSD_OK;
+}
+
+int ssd_debug_stall(int kinds) {
+    g_stall_kinds.store(kinds);
+    return SSD_OK;
 }
 
 int ssd_profile_enable(int kinds) {

@@ -37,10 +37,19 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(0, 7):
+    for s in range(0, 8):
         msg = lib.ssd_status_string(s)
         assert msg is not None and len(msg) > 0
     assert b"INVALID_ARG" in lib.ssd_status_string(1)
+    assert b"RANGE" in lib.ssd_status_string(_ffi.SSD_ERR_RANGE)
+
+
+def test_debug_hooks_without_launches(lib):
+    """The failure-path hooks only set host state: they succeed and restore cleanly without a GPU."""
+    assert lib.ssd_debug_set_wait_limit_ns(2_000_000) == 0
+    assert lib.ssd_debug_stall(1 << 3) == 0
+    assert lib.ssd_debug_stall(0) == 0
+    assert lib.ssd_debug_set_wait_limit_ns(0) == 0
 
 
 FAKE = 4096  # a 16-byte aligned non-null address: validation must fail before it is used

@@ -48,18 +48,26 @@ def test_max_over_ranks_single_process():
 
 
 def test_algorithmic_bytes_of_the_headline_workload():
-    """bench.py's per-launch algorithmic bytes at L 65536, H 32, N 128 for the library's plan of that shape
-    (7-chunk spans, compute_out runs of four spans): the figures the roofline object reports."""
+    """bench.py's per-launch bytes at L 65536, H 32, N 128 for the library's plan of that shape (7-chunk
+    spans, compute_out runs of four spans).  The roofline credits compulsory bytes only: chunk_scan's are
+    x + y + B + C = 570.4 MB; the intermediates it also moves (dA_cumsum and dt rows, run-start states) are
+    reported apart."""
     import bench
     from state_space_sequence_ssd_gb300 import inputs as I
     w = I.WORKLOADS["long_L65536_N128"]
     plan = {"span_chunks": 7, "scan_step": 4}
-    mb = {k: bench.kernel_alg_bytes(k, w, plan) / 1e6 for k in ("chunk_cumsum", "chunk_state", "state_passing",
-                                                                  "chunk_scan")}
-    assert round(mb["chunk_scan"], 1) == 597.7
-    assert round(mb["chunk_state"], 1) == 340.8
-    assert round(mb["chunk_cumsum"], 1) == 92.3
-    assert round(mb["state_passing"], 1) == 79.7
+    kb = {k: bench.kernel_bytes(k, w, plan) for k in ("chunk_cumsum", "chunk_state", "state_passing", "chunk_scan")}
+    mb = {k: v["compulsory"] / 1e6 for k, v in kb.items()}
+    assert round(mb["chunk_scan"], 1) == 570.4
+    assert round(mb["chunk_state"], 1) == 268.4
+    assert round(mb["chunk_cumsum"], 1) == 41.9
+    assert round(mb["state_passing"], 1) == 2.1
+    tot = {k: (v["compulsory"] + v["intermediate"]) / 1e6 for k, v in kb.items()}
+    assert round(tot["chunk_scan"], 1) == 597.7
+    assert round(tot["chunk_cumsum"], 1) == 92.3
+    assert bench.kernel_alg_bytes("chunk_scan", w, plan) == kb["chunk_scan"]["compulsory"]
+    # the compulsory bytes of the kernels add up to the pass's (each input read and output written once)
+    assert sum(mb.values()) * 1e6 == pytest.approx(bench.compulsory_bytes(w) + 268435456 + 2 * 16777216, rel=1e-6)
 
 
 def test_source_key_ignores_comments_only():

@@ -3,7 +3,8 @@
 Tolerance (y, final_state, states): |gpu - ref| <= 1e-2 + 1e-2 * |ref|, element
 by element; dA_cumsum: |gpu - ref| <= 1e-5 * |ref| (+1e-30).  Full-size
 workloads compare every output of a sample of (batch, head) units, which the
-oracle computes one by one; small workloads compare everything.
+oracle computes one by one (the first and last unit, the first head of every
+B/C group, and random ones); small workloads compare everything.
 """
 import numpy as np
 import pytest
@@ -44,11 +45,14 @@ def to_dev(inp):
 
 
 def sample_units(w, k, seed=0):
+    """k (batch, head) units: the first and the last, the first head of every B/C group (so a
+    group-indexing slip in any group shows), and random ones for the rest."""
     n = w.batch * w.nheads
     if k >= n:
         return np.arange(n)
     rng = np.random.default_rng(seed)
-    u = set([0, n - 1])
+    hpg = w.nheads // w.ngroups
+    u = set([0, n - 1]) | {g * hpg for g in range(w.ngroups)}
     while len(u) < k:
         u.add(int(rng.integers(0, n)))
     return np.array(sorted(u))
