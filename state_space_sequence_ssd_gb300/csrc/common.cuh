@@ -148,6 +148,14 @@ int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half
                            int span_chunks, const Dims& d, __nv_bfloat16* y, const Ctl& ctl, cudaStream_t s,
                            const OutOpts& oo = OutOpts(), int state_step = 1);
 
+// compute_out for two heads of one group per CTA (k_chunk_scan_pair.cu): state sizes 64 and 128, an
+// even number of heads per group, no per-channel D or gate; launch_chunk_scan_span picks it when
+// chunk_scan_pair_supported says so
+bool chunk_scan_pair_supported(const Dims& d, const OutOpts& oo);
+int launch_chunk_scan_pair(const __nv_bfloat16* x, const __half* B, const __half* C, const float* dtt,
+                           const float* cs, const float* D, const float* span_states, int span_chunks, const Dims& d,
+                           __nv_bfloat16* y, const Ctl& ctl, cudaStream_t s, int state_step);
+
 // one recurrent step for every (batch, head): state updated in place, y for the token (k_step.cu)
 int launch_step(const __nv_bfloat16* x, const float* dt, const float* A, const __nv_bfloat16* B,
                 const __nv_bfloat16* C, const float* D, float* state, int batch, int nheads, int ngroups, int dstate,

@@ -63,21 +63,12 @@
 #include "common.cuh"
 #include "sm100.cuh"
 #include "tmap.cuh"
+#include "scan_util.cuh"
 
 namespace ssd {
 namespace {
 
 using namespace sm100;
-
-// The roles' waits.  INL: the whole loop inlined at every site (no call, so no register save and
-// restore through local memory around it), measured 3-4% faster for the plain kernel; the larger
-// instantiation with the layer's output options measured faster with the shared out-of-line loop.
-template <bool INL>
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort, int* err, int code,
-                                             uint64_t limit_ns) {
-    if constexpr (INL) return mbar_wait_bounded_inline(bar, parity, abort, err, code, limit_ns);
-    else return mbar_wait_bounded(bar, parity, abort, err, code, limit_ns);
-}
 
 constexpr int kThreads = 480;
 constexpr int kTile = 16384;  // 128 rows x 128 B
@@ -165,48 +156,6 @@ __device__ __forceinline__ void gate8(float (&o)[8], const uint4& zq) {
         const uint32_t w = zw[i >> 1];
         o[i] *= silu(__uint_as_float((i & 1) ? (w & 0xffff0000u) : (w << 16)));
     }
-}
-
-// 32 bytes from a 32-byte-aligned read-only global address in one load (sm_100+ 256-bit vector load)
-__device__ __forceinline__ void ld_global_nc_32B(const void* p, uint4& lo, uint4& hi) {
-    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
-                 : "l"(p));
-}
-
-// a thread's 128-byte z row: 32-byte loads when z is 32-byte aligned, else 16-byte loads
-__device__ __forceinline__ void load_z_row(const uint4* zr, bool z32, uint4 (&zq)[8]) {
-    if (z32) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ld_global_nc_32B(zr + 2 * i, zq[2 * i], zq[2 * i + 1]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) zq[i] = __ldg(zr + i);
-    }
-}
-
-// 32 bytes to a 32-byte-aligned global address in one store (sm_100+ 256-bit vector store)
-__device__ __forceinline__ void st_global_32B(void* p, const uint4& lo, const uint4& hi) {
-    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(lo.x), "r"(lo.y), "r"(lo.z),
-                 "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
-                 : "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// In-sub-block inclusive log2 decay of position i (raw per-chunk cumsums in
-// scs, the raw value before the sub-block in prev when it starts inside a
-// chunk; a 64-token chunk boundary may fall inside the sub-block).
-__device__ __forceinline__ float sub_block_decay(const float* scs, float prev, int p0, int Q, int i) {
-    return ((p0 + i) / Q == 0) ? (scs[i] - prev) : ((scs[Q - 1 - p0] - prev) + scs[i]);
 }
 
 // OPT: the layer's output options (D per channel, z gate) are compiled in; the plain
@@ -516,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = threadIdx.x;  // TMEM lane == row
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const float Dh = (a.D != nullptr) ? a.D[h] : 0.f;  // the skip term rides on M's diagonal
-        float mx = 0.f;  // largest |M| converted to float16 (range flag)
+        __half2 mx = __floats2half2_rn(0.f, 0.f);  // largest |M| after rounding to float16 (range flag)
         for (int sb = 0; sb < nsb; ++sb) {
             const int k = sb % K::NBUF;
             const int ub = sb % 3;
@@ -545,10 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int jj = 0; jj < 32; jj += 2) {
                             const int j = q * 32 + jj;
-                            const float m0 = __uint_as_float(v[jj]) * (ar * sbc[j]);
-                            const float m1 = __uint_as_float(v[jj + 1]) * (ar * sbc[j + 1]);
-                            mx = fmaxf(mx, fmaxf(fabsf(m0), fabsf(m1)));
-                            o[jj >> 1] = pack_f16x2(m0, m1);
+                            o[jj >> 1] = pack_f16x2(__uint_as_float(v[jj]) * (ar * sbc[j]),
+                                                    __uint_as_float(v[jj + 1]) * (ar * sbc[j + 1]));
+                            hmax_abs(mx, o[jj >> 1]);
                         }
                     } else {
                         // diagonal block: exact per-element exponent, causal mask, D on the diagonal
@@ -563,8 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             m1 = (j1 <= r) ? m1 : 0.f;
                             m0 += (j0 == r) ? Dh : 0.f;
                             m1 += (j1 == r) ? Dh : 0.f;
-                            mx = fmaxf(mx, fmaxf(fabsf(m0), fabsf(m1)));
                             o[jj >> 1] = pack_f16x2(m0, m1);
+                            hmax_abs(mx, o[jj >> 1]);
                         }
                     }
                 }
@@ -575,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&bar->m_ready[k]);
             mbar_arrive(&bar->u_free[ub]);
         }
-        flag_f16_range(err, mx);
+        flag_f16_range(err, hmax_to_float(mx));
     } else if (warp < 8) {
         // ------------------------------------------------------ state warpgroup
         // A failed wait turns the remaining work into no-ops but keeps every arrival.
@@ -584,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t PN = (int64_t)d.headdim * N;
         const float* init = a.init + (((int64_t)b * a.state_spans + (int64_t)s * a.state_step) * H + h) * PN;
         bool ok = true;
-        float mx = 0.f;        // largest |value| converted to float16: x, w x, the state copy (range flag)
+        __half2 mx = __floats2half2_rn(0.f, 0.f);  // largest |x|, |w x|, |state copy| in float16 (range flag)
         float prev_raw = 0.f;  // raw dA_cumsum of the token before this sub-block (same chunk)
         for (int sb = 0; sb < nsb; ++sb) {
             const int64_t t0 = ts + sb * 128;
@@ -628,7 +576,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 const float w = valid ? fast_exp2(fminf(ulast - u, 0.f)) * dtv : 0.f;
-                const float wr = fmaxf(w, 1.f);
                 uint8_t* xrow = smem + K::OFF_X + xb * kTile;
                 uint8_t* xsrow = smem + K::OFF_XS;
 #pragma unroll
@@ -642,9 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 fv = __bfloat1622float2(p2[e]);
-                        mx = fmaxf(mx, fmaxf(fabsf(fv.x), fabsf(fv.y)) * wr);  // x and w x
                         x4[e] = pack_f16x2(fv.x, fv.y);
                         w4[e] = pack_f16x2(fv.x * w, fv.y * w);
+                        hmax_abs(mx, x4[e]);
+                        hmax_abs(mx, w4[e]);
                     }
                     *reinterpret_cast<uint4*>(xrow + off) = xo;
                     *reinterpret_cast<uint4*>(xsrow + off) = wo;
@@ -688,8 +636,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!ok) break;
                     }
                     if (real) {
-#pragma unroll
-                        for (int p = 0; p < 64; ++p) mx = fmaxf(mx, fabsf(hv[p]));
                         // smem row: state index n, or its row in the ring slot
                         const int hr = K::RING ? r : nb * K::NB + r;
                         uint8_t* hdst = K::RING ? hbase + (nb & 1) * K::SZ_HS : hbase;
@@ -700,6 +646,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             v.y = pack_f16x2(hv[ch * 8 + 2], hv[ch * 8 + 3]);
                             v.z = pack_f16x2(hv[ch * 8 + 4], hv[ch * 8 + 5]);
                             v.w = pack_f16x2(hv[ch * 8 + 6], hv[ch * 8 + 7]);
+                            hmax_abs(mx, v.x);
+                            hmax_abs(mx, v.y);
+                            hmax_abs(mx, v.z);
+                            hmax_abs(mx, v.w);
                             *reinterpret_cast<uint4*>(hdst + sw128_offset(hr, ch)) = v;
                         }
                     }
@@ -723,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mbar_arrive(&bar->h_ready);
         }
-        flag_f16_range(err, mx);
+        flag_f16_range(err, hmax_to_float(mx));
     } else if (warp < 12) {
         // ------------------------------------------------------ epilogue warpgroup
         const int r = threadIdx.x - 256;  // TMEM lane (warp % 4 == warp - 8)
@@ -828,6 +778,8 @@ int launch_scan_n(const __nv_bfloat16* x, const __half* B, const __half* C, cons
 int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C, const float* dtt,
                            const float* cs, const float* D, const float* span_states, int span_chunks, const Dims& d,
                            __nv_bfloat16* y, const Ctl& ctl, cudaStream_t s, const OutOpts& oo, int state_step) {
+    if (chunk_scan_pair_supported(d, oo))
+        return launch_chunk_scan_pair(x, B, C, dtt, cs, D, span_states, span_chunks, d, y, ctl, s, state_step);
     ScanArgs a;
     a.d = d;
     a.span_chunks = span_chunks * state_step;

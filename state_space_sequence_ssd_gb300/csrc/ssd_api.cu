@@ -274,25 +274,25 @@ double scan_makespan(int64_t rows_per_batch, int batch, int nchunks, int chunk_s
 // Span-start states per chunk_scan span: chunk_scan walks spans of `span` * step chunks
 // (step in {1, 2, 4}), each from every step-th span-start state, so there are fewer, longer
 // CTAs and less pipeline fill and drain per sub-block.  The step with the shortest estimated
-// makespan wins, among those that keep as many SMs busy as step 1; decided once per shape.
-int forward_scan_step(const Dims& d, int span) {
+// makespan wins (by at least 0.5%); decided once per shape.
+// A CTA of the paired kernel covers two heads, so its rows are head pairs.
+int forward_scan_step(const Dims& d, int span, const OutOpts& oo) {
     static std::mutex mu;
-    static std::map<std::array<int64_t, 5>, int> cache;
+    static std::map<std::array<int64_t, 6>, int> cache;
     const int sms = device_sms();
-    const std::array<int64_t, 5> key = {d.batch, d.nheads, d.nchunks, span, sms};
+    const bool pair = chunk_scan_pair_supported(d, oo);
+    const std::array<int64_t, 6> key = {d.batch, d.nheads, d.nchunks, span, sms, pair ? 1 : 0};
     {
         std::lock_guard<std::mutex> lk(mu);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    const int64_t rows = d.nheads;
-    const int64_t cta1 = (int64_t)d.batch * rows * ceil_div(d.nchunks, span);
+    const int64_t rows = pair ? d.nheads / 2 : d.nheads;
     int best = 1;
     double best_t = scan_makespan(rows, d.batch, d.nchunks, d.chunk_size, span, sms);
     for (int m = 2; m <= 4; m *= 2) {
         if ((int64_t)span * m > d.nchunks) break;
-        const int64_t cta = (int64_t)d.batch * rows * ceil_div(d.nchunks, span * m);
-        if (cta < std::min<int64_t>(sms, cta1)) break;
+        // one wave that leaves SMs idle can still beat two fuller ones: the estimate decides
         const double t = scan_makespan(rows, d.batch, d.nchunks, d.chunk_size, span * m, sms);
         if (t < best_t * 0.995) {
             best = m;
@@ -509,7 +509,7 @@ int ssd_forward_ex(const void* x, const float* dt, const float* A, const void* B
     if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
     if (r == SSD_OK)
         r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y),
-                                   make_ctl(err, kKindChunkScan), stream, oo, forward_scan_step(d, span));
+                                   make_ctl(err, kKindChunkScan), stream, oo, forward_scan_step(d, span, oo));
     if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
     return r;
 }
@@ -547,7 +547,7 @@ int ssd_forward_noalloc(const void* x, const float* dt, const float* A, const vo
     if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
     if (r == SSD_OK)
         r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y),
-                                   make_ctl(err, kKindChunkScan), stream, OutOpts(), forward_scan_step(d, span));
+                                   make_ctl(err, kKindChunkScan), stream, OutOpts(), forward_scan_step(d, span, OutOpts()));
     return r;
 }
 
@@ -558,7 +558,7 @@ int ssd_forward_plan(int batch, int seqlen, int nheads, int headdim, int ngroups
     const Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
     const int span = forward_span_chunks(d);
     if (span_chunks != nullptr) *span_chunks = span;
-    if (scan_step != nullptr) *scan_step = forward_scan_step(d, span);
+    if (scan_step != nullptr) *scan_step = forward_scan_step(d, span, OutOpts());
     if (noalloc_bytes != nullptr) *noalloc_bytes = (unsigned long long)noalloc_layout(d, span).need;
     return SSD_OK;
 }
