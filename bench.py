@@ -1,4 +1,4 @@
-"""Benchmark of the SSD chunked forward pass on one GB300 (or N replicas).
+"""Benchmark of the SSD chunked forward pass on one GB300 (or N, heads split across them).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -190,10 +190,17 @@ def main():
     fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), device=dev, dtype=torch.float32)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    split = head_split(w, world, rank, d, dev, ssd) if world > 1 else None
 
     def step():
-        ssd.ssd_forward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"], w.chunk_size, y=y,
-                        final_state=fin, stream=stream)
+        if split is None:
+            ssd.ssd_forward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"], w.chunk_size, y=y,
+                            final_state=fin, stream=stream)
+        else:
+            g = split["t"]
+            ssd.ssd_forward_heads(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], g["init"], w.chunk_size,
+                                  split["head_begin"], split["head_count"], y=g["y"], final_state=g["fin"],
+                                  stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -310,7 +317,9 @@ def main():
         "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
                    "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk_size": w.chunk_size,
                    "nonzero_init": w.nonzero_init, "l2": "flushed between steps (256 MB memset, untimed)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": (f"heads: the problem has {world} x {w.nheads} heads in {world} x {w.ngroups} "
+                                   f"B/C groups, each rank computes its {w.nheads} heads (whole groups) with "
+                                   f"ssd_forward_heads; no exchange") if world > 1 else "single GPU"},
         "tflops": round(flops / (ms_per_step / 1e3) / 1e12, 2),
         "pass_roofline": {"t_roofline_us": round(t_roof_us, 2), "t_measured_us": round(ms_per_step * 1e3, 2),
                           "frac": round(t_roof_us / (ms_per_step * 1e3), 4),
@@ -351,6 +360,35 @@ def main():
         print("bench: the library's device error word was set (a bounded wait gave up)", file=sys.stderr)
         return 3
     return 0
+
+
+def head_split(w: I.Workload, world: int, rank: int, d: dict, dev, ssd) -> dict:
+    """The multi-GPU split: a problem of world x H heads (world x G groups, so every rank's heads are whole
+    groups), each rank computing its heads in place with ssd_forward_heads.  Each rank holds the full-size
+    tensors and fills only its own heads and groups with its seeded inputs; the call reads nothing else."""
+    import torch
+    Hg, Gg = w.nheads * world, w.ngroups * world
+    hb, hc = ssd.ssd_partition_heads(Hg, Gg, world, rank)
+    assert hc == w.nheads, (hb, hc)
+    g0 = hb // (Hg // Gg)
+    b, L, P, N = w.batch, w.seqlen, w.headdim, w.dstate
+    t = {"x": torch.empty((b, L, Hg, P), dtype=torch.bfloat16, device=dev),
+         "dt": torch.empty((b, L, Hg), device=dev), "A": torch.empty((Hg,), device=dev),
+         "B": torch.empty((b, L, Gg, N), dtype=torch.bfloat16, device=dev),
+         "C": torch.empty((b, L, Gg, N), dtype=torch.bfloat16, device=dev),
+         "D": torch.empty((Hg,), device=dev), "init": None,
+         "y": torch.empty((b, L, Hg, P), dtype=torch.bfloat16, device=dev),
+         "fin": torch.empty((b, Hg, P, N), device=dev)}
+    t["x"][:, :, hb:hb + hc] = d["x"]
+    t["dt"][:, :, hb:hb + hc] = d["dt"]
+    t["A"][hb:hb + hc] = d["A"]
+    t["D"][hb:hb + hc] = d["D"]
+    t["B"][:, :, g0:g0 + w.ngroups] = d["B"]
+    t["C"][:, :, g0:g0 + w.ngroups] = d["C"]
+    if d["init"] is not None:
+        t["init"] = torch.empty((b, Hg, P, N), device=dev)
+        t["init"][:, hb:hb + hc] = d["init"]
+    return {"t": t, "head_begin": hb, "head_count": hc}
 
 
 def default_oracle_tokens(w: I.Workload) -> int:

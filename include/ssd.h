@@ -173,6 +173,43 @@ SSD_API int ssd_forward(const void* x, const float* dt, const float* A, const vo
                 float* final_state, cudaStream_t stream);
 
 /*
+ * ssd_forward_heads -- ssd_forward over the contiguous range of heads
+ * [head_begin, head_begin + head_count) of full-size tensors, in place: the
+ * multi-GPU split of the pass.  Per batch row, (batch, head) units are
+ * independent -- each head reads its own x, dt, A, D and initial state and
+ * its group's B and C -- so N devices can each compute a range of heads of
+ * one problem with no exchange (devotd.net page on the Mamba-2 cuTile forward
+ * kernels, section 2: the state's independent parts are processed in
+ * parallel).  Every pointer and size is that of ssd_forward for the WHOLE
+ * problem (nheads heads); the call reads only the rows of its heads (and of
+ * the B/C groups they use) and writes only their rows of y and final_state,
+ * leaving the other heads' outputs untouched.  ssd_partition_heads gives a
+ * balanced range per device.  The workspace is allocated as in ssd_forward,
+ * sized for head_count heads.  Results equal ssd_forward's for those heads up
+ * to rounding (the work is tiled for the call's head count).
+ * Extra errors: SSD_ERR_INVALID_ARG if head_begin < 0, head_count < 1 or
+ * head_begin + head_count > nheads.
+ */
+SSD_API int ssd_forward_heads(const void* x, const float* dt, const float* A, const void* B, const void* C,
+                              const float* D, const float* init_state, int batch, int seqlen, int nheads,
+                              int headdim, int ngroups, int dstate, int chunk_size, int head_begin, int head_count,
+                              void* y, float* final_state, cudaStream_t stream);
+
+/*
+ * ssd_partition_heads -- the heads that part `part` of `nparts` (one per
+ * device) computes with ssd_forward_heads: a contiguous range, the ranges of
+ * all parts covering every head exactly once.  With at least as many B/C
+ * groups as parts the ranges are whole groups, so a device reads only its own
+ * groups' B and C; otherwise heads are split as evenly as possible in blocks
+ * of two (one block never straddling a group boundary), and a part may get
+ * no heads (*head_count == 0) when there are more parts than blocks.
+ * Host-only; touches no device.  Returns SSD_ERR_INVALID_ARG for
+ * non-positive sizes, nheads % ngroups != 0, part outside [0, nparts) or NULL
+ * outputs, else SSD_OK.
+ */
+SSD_API int ssd_partition_heads(int nheads, int ngroups, int nparts, int part, int* head_begin, int* head_count);
+
+/*
  * ssd_forward_noalloc -- ssd_forward with no memory allocation of any kind.
  * The pages describe no such variant; it exists for callers that must not
  * have the library allocate device memory during a call: code that has

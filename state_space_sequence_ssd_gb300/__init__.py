@@ -18,8 +18,8 @@ from __future__ import annotations
 from . import _ffi
 
 __all__ = ["ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_forward",
-           "ssd_forward_noalloc", "ssd_forward_plan", "ssd_step", "ssd_step_multi", "ssd_forward_ex", "ssd_step_ex",
-           "ssd_get_device_error", "SSDError", "library_path"]
+           "ssd_forward_noalloc", "ssd_forward_heads", "ssd_partition_heads", "ssd_forward_plan", "ssd_step",
+           "ssd_step_multi", "ssd_forward_ex", "ssd_step_ex", "ssd_get_device_error", "SSDError", "library_path"]
 
 SSDError = _ffi.SSDError
 library_path = _ffi.LIB_PATH
@@ -160,6 +160,41 @@ def ssd_forward(x, dt, A, B, C, D, init_state, chunk_size, y=None, final_state=N
         _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
         b, L, H, P, G, N, chunk_size, _ptr(y), _ptr(final_state), _stream(stream)))
     return y, final_state
+
+
+def ssd_forward_heads(x, dt, A, B, C, D, init_state, chunk_size, head_begin, head_count, y=None, final_state=None,
+                      want_final=True, stream=None):
+    """ssd_forward over heads [head_begin, head_begin + head_count) of the full-size tensors, in place:
+    only those heads' rows of y and final_state are written.  Returns (y, final_state or None)."""
+    torch = _torch()
+    _need(x, "x", torch.bfloat16, 4)
+    _need(dt, "dt", torch.float32, 3)
+    _need(A, "A", torch.float32, 1)
+    _need(B, "B", torch.bfloat16, 4)
+    _need(C, "C", torch.bfloat16, 4)
+    _opt(D, "D", torch.float32, 1)
+    _opt(init_state, "init_state", torch.float32, 4)
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and want_final:
+        final_state = torch.empty((b, H, P, N), device=x.device, dtype=torch.float32)
+    _need(y, "y", torch.bfloat16, 4)
+    _opt(final_state, "final_state", torch.float32, 4)
+    _ffi.check("ssd_forward_heads", _ffi.lib().ssd_forward_heads(
+        _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
+        b, L, H, P, G, N, chunk_size, int(head_begin), int(head_count), _ptr(y), _ptr(final_state), _stream(stream)))
+    return y, final_state
+
+
+def ssd_partition_heads(nheads, ngroups, nparts, part):
+    """(head_begin, head_count) of part `part` of `nparts` for ssd_forward_heads (host only)."""
+    import ctypes
+    hb, hc = ctypes.c_int(0), ctypes.c_int(0)
+    _ffi.check("ssd_partition_heads", _ffi.lib().ssd_partition_heads(
+        int(nheads), int(ngroups), int(nparts), int(part), ctypes.addressof(hb), ctypes.addressof(hc)))
+    return hb.value, hc.value
 
 
 def _options(x, D, dt_bias, dt_softplus, dt_limit, z, H, P):

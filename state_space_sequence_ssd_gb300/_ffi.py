@@ -32,6 +32,8 @@ SIGNATURES = {
     "ssd_chunk_scan": (_i, [_p] * 7 + [_i] * 7 + [_p, _p]),
     "ssd_forward": (_i, [_p] * 7 + [_i] * 7 + [_p, _p, _p]),
     "ssd_forward_noalloc": (_i, [_p] * 7 + [_i] * 7 + [_p, _p, _p]),
+    "ssd_forward_heads": (_i, [_p] * 7 + [_i] * 9 + [_p, _p, _p]),
+    "ssd_partition_heads": (_i, [_i] * 4 + [_p, _p]),
     "ssd_step": (_i, [_p] * 7 + [_i] * 5 + [_p, _p]),
     "ssd_step_multi": (_i, [_p] * 7 + [_i] * 6 + [_p, _p]),
     "ssd_forward_plan": (_i, [_i] * 7 + [_p, _p, _p]),

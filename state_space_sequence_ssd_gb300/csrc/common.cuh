@@ -38,9 +38,14 @@ __device__ __forceinline__ void flag_f16_range(int* err, float mx) {
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0 && err != nullptr) atomicOr(err + 1, 1);
 }
 
-// Problem dimensions shared by every launch.
+// Problem dimensions shared by every launch.  A call may cover a contiguous range of heads of
+// full-size tensors: heads head0 .. head0 + hcount - 1 of nheads.  Caller tensors (x, y, dt, A, D, z,
+// init and final states) are indexed by the global head h = head0 + local head; the library's own
+// intermediates (dA_cumsum and dt rows, chunk or span states and decays) hold the hcount heads of the
+// call only and are indexed by the local head.  A whole-problem call has head0 = 0, hcount = nheads.
 struct Dims {
     int batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nchunks;
+    int head0, hcount;
 };
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }

@@ -125,10 +125,10 @@ struct ScanArgs {
     int nspans;
     int state_step;    // span-start state of span s: entry s * state_step of the state array
     int state_spans;   // entries per (batch) row of the state array
-    const float* cs;    // (b, H, nc, Q)
-    const float* dtt;   // (b, H, nc, Q)
+    const float* cs;    // (b, hcount, nc, Q)
+    const float* dtt;   // (b, hcount, nc, Q)
     const float* D;     // (H) or null: the skip term on M's diagonal
-    const float* init;  // (b, state_spans, H, P, N) span-start states
+    const float* init;  // (b, state_spans, hcount, P, N) span-start states
     __nv_bfloat16* y;   // (b, L, H, P)
     int y32;            // y is 32-byte aligned: rows are stored in 32-byte pieces
     int z32;            // the gate z is 32-byte aligned: rows are loaded in 32-byte pieces
@@ -173,8 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int abort_sh;
 
     const Dims& d = a.d;
-    const int h = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
-    const int H = d.nheads, G = d.ngroups, Q = d.chunk_size;
+    // hl: local head (the call's intermediates); h = head0 + hl: its head in x, y, z, D and B / C
+    const int hl = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
+    const int H = d.nheads, HC = d.hcount, G = d.ngroups, Q = d.chunk_size;
+    const int h = d.head0 + hl;
     const int g = h / (H / G);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t ts = (int64_t)s * a.span_chunks * Q;
@@ -270,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* scd = reinterpret_cast<float*>(smem + K::OFF_CD + xb * 1024);
                 mbar_arrive_expect_tx(&bar->x_full[xb], kTile + 2 * cdb);
                 tma_load_4d(smem + K::OFF_X + xb * kTile, &tm_x, &bar->x_full[xb], 0, h, t0, b);
-                bulk_load(scd, a.cs + ((int64_t)b * H + h) * rowlen + t0, cdb, &bar->x_full[xb]);
-                bulk_load(scd + 128, a.dtt + ((int64_t)b * H + h) * rowlen + t0, cdb, &bar->x_full[xb]);
+                bulk_load(scd, a.cs + ((int64_t)b * HC + hl) * rowlen + t0, cdb, &bar->x_full[xb]);
+                bulk_load(scd + 128, a.dtt + ((int64_t)b * HC + hl) * rowlen + t0, cdb, &bar->x_full[xb]);
                 ++nissued;
             }
             // no load may still be landing in shared memory at teardown
@@ -530,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = threadIdx.x - 128;  // TMEM lane (warp % 4 == warp - 4)
         const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
         const int64_t PN = (int64_t)d.headdim * N;
-        const float* init = a.init + (((int64_t)b * a.state_spans + (int64_t)s * a.state_step) * H + h) * PN;
+        const float* init = a.init + (((int64_t)b * a.state_spans + (int64_t)s * a.state_step) * HC + hl) * PN;
         bool ok = true;
         __half2 mx = __floats2half2_rn(0.f, 0.f);  // largest |x|, |w x|, |state copy| in float16 (range flag)
         float prev_raw = 0.f;  // raw dA_cumsum of the token before this sub-block (same chunk)
@@ -766,7 +768,7 @@ int launch_scan_n(const __nv_bfloat16* x, const __half* B, const __half* C, cons
     const int smem = Cfg<N, OPT>::SMEM;
     if (ensure_smem_limit(reinterpret_cast<const void*>(chunk_scan_tc_kernel<N, OPT>), smem) != SSD_OK)
         return SSD_ERR_CUDA;
-    dim3 grid(d.nheads, a.nspans, d.batch);
+    dim3 grid(d.hcount, a.nspans, d.batch);
     launch_begin(kKindChunkScan, s);
     const cudaError_t le = launch_dependent(chunk_scan_tc_kernel<N, OPT>, grid, dim3(kThreads), smem, s, tx, tb, tc, a);
     const int r = launch_end(kKindChunkScan, s);

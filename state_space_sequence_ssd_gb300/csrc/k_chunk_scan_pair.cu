@@ -97,10 +97,10 @@ struct PairArgs {
     int nspans;
     int state_step;    // span-start state of span s: entry s * state_step of the state array
     int state_spans;   // entries per (batch) row of the state array
-    const float* cs;   // (b, H, nc, Q)
-    const float* dtt;  // (b, H, nc, Q)
+    const float* cs;   // (b, hcount, nc, Q)
+    const float* dtt;  // (b, hcount, nc, Q)
     const float* D;    // (H) or null
-    const float* init; // (b, state_spans, H, P, N) span-start states
+    const float* init; // (b, state_spans, hcount, P, N) span-start states
     __nv_bfloat16* y;  // (b, L, H, P)
     int y32;           // y is 32-byte aligned: rows are stored in 32-byte pieces
     Ctl ctl;
@@ -128,8 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int abort_sh;
 
     const Dims& d = a.d;
-    const int h0 = 2 * blockIdx.x, s = blockIdx.y, b = blockIdx.z;
-    const int H = d.nheads, G = d.ngroups, Q = d.chunk_size;
+    // hl0: first local head (the call's intermediates); h0 = head0 + hl0: its head in x, y, D and B / C
+    const int hl0 = 2 * blockIdx.x, s = blockIdx.y, b = blockIdx.z;
+    const int H = d.nheads, HC = d.hcount, G = d.ngroups, Q = d.chunk_size;
+    const int h0 = d.head0 + hl0;
     const int g = h0 / (H / G);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t ts = (int64_t)s * a.span_chunks * Q;
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     float* scd = reinterpret_cast<float*>(smem + K::OFF_CD + (2 * xs + hh) * 1024);
-                    const int64_t row = ((int64_t)b * H + h0 + hh) * rowlen + t0;
+                    const int64_t row = ((int64_t)b * HC + hl0 + hh) * rowlen + t0;
                     tma_load_4d(xtile(xs, hh), &tm_x, &bar->x_full[xs], 0, h0 + hh, t0, b);
                     bulk_load(scd, a.cs + row, cdb, &bar->x_full[xs]);
                     bulk_load(scd + 128, a.dtt + row, cdb, &bar->x_full[xs]);
@@ -389,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hs = r >> 6;  // head of the state row
         const uint32_t lane_base = (uint32_t)(((warp - 8) & 3) * 32) << 16;
         const int64_t PN = (int64_t)d.headdim * N;
-        const float* init = a.init + (((int64_t)b * a.state_spans + (int64_t)s * a.state_step) * H + h0 + hs) * PN +
+        const float* init = a.init + (((int64_t)b * a.state_spans + (int64_t)s * a.state_step) * HC + hl0 + hs) * PN +
                             (int64_t)(r & 63) * N;
         constexpr int NC = N / 64;  // 32-column chunks of the state row per warpgroup
         bool ok = true;
@@ -612,7 +614,7 @@ int launch_pair_n(const __nv_bfloat16* x, const __half* B, const __half* C, cons
         return SSD_ERR_CUDA;
     const int smem = PCfg<N>::SMEM;
     if (ensure_smem_limit(reinterpret_cast<const void*>(chunk_scan_pair_kernel<N>), smem) != SSD_OK) return SSD_ERR_CUDA;
-    dim3 grid(d.nheads / 2, a.nspans, d.batch);
+    dim3 grid(d.hcount / 2, a.nspans, d.batch);
     launch_begin(kKindChunkScan, s);
     const cudaError_t le = launch_dependent(chunk_scan_pair_kernel<N>, grid, dim3(kThreads), smem, s, tx, tb, tc, a);
     const int r = launch_end(kKindChunkScan, s);
@@ -622,8 +624,8 @@ int launch_pair_n(const __nv_bfloat16* x, const __half* B, const __half* C, cons
 }  // namespace
 
 bool chunk_scan_pair_supported(const Dims& d, const OutOpts& oo) {
-    return (d.dstate == 64 || d.dstate == 128) && ((d.nheads / d.ngroups) % 2 == 0) && oo.Dp == nullptr &&
-           oo.z == nullptr;
+    return (d.dstate == 64 || d.dstate == 128) && ((d.nheads / d.ngroups) % 2 == 0) && d.head0 % 2 == 0 &&
+           d.hcount % 2 == 0 && oo.Dp == nullptr && oo.z == nullptr;
 }
 
 int launch_chunk_scan_pair(const __nv_bfloat16* x, const __half* B, const __half* C, const float* dtt,

@@ -72,10 +72,10 @@ struct StateArgs {
     Dims d;
     int span_chunks;
     int nspans;
-    const float* cs;    // (b, H, nc, Q)
-    const float* dtt;   // (b, H, nc, Q)
-    float* S;           // (b, nspans, H, P, N)
-    float* span_decay;  // (b, H, nspans) log2 units, or null
+    const float* cs;    // (b, hcount, nc, Q)
+    const float* dtt;   // (b, hcount, nc, Q)
+    float* S;           // (b, nspans, hcount, P, N)
+    float* span_decay;  // (b, hcount, nspans) log2 units, or null
     Ctl ctl;            // error words, wait limit, stall hook
 };
 
@@ -96,9 +96,11 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
     __shared__ int abort_sh;
 
     const Dims& d = a.d;
+    // h0: first local head of the CTA (intermediates); hg0 = head0 + h0: its head in x and B
     const int h0 = blockIdx.x * HH, s = blockIdx.y, b = blockIdx.z;
-    const int H = d.nheads, G = d.ngroups, Q = d.chunk_size;
-    const int g = h0 / (H / G);
+    const int H = d.nheads, HC = d.hcount, G = d.ngroups, Q = d.chunk_size;
+    const int hg0 = d.head0 + h0;
+    const int g = hg0 / (H / G);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t ts = (int64_t)s * a.span_chunks * Q;
     const int64_t te = min((int64_t)d.seqlen, ts + (int64_t)a.span_chunks * Q);
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
     if (warp < HH) {
         // head h0 + warp: per chunk c of the span, R_c + cs[c][Q-1] = sum of the chunk totals
         // from c to the span end (an inclusive suffix sum), 32 chunks per round, one load per lane
-        const int64_t row = (int64_t)b * H + h0 + warp;
+        const int64_t row = (int64_t)b * HC + h0 + warp;
         const float* csr = a.cs + row * rowlen;
         float carry = 0.f;
         for (int base = nchk - 32; base > -32; base -= 32) {
@@ -176,8 +178,8 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
                 mbar_arrive_expect_tx(&full[st], HH * K::BOX + K::NBOX * K::BOX + HH * 2 * cdb);
 #pragma unroll
                 for (int hh = 0; hh < HH; ++hh) {
-                    const int64_t row = ((int64_t)b * H + h0 + hh) * rowlen + t0;
-                    tma_load_4d(sX + hh * K::BOX, &tm_x, &full[st], 0, h0 + hh, t0, b);
+                    const int64_t row = ((int64_t)b * HC + h0 + hh) * rowlen + t0;
+                    tma_load_4d(sX + hh * K::BOX, &tm_x, &full[st], 0, hg0 + hh, t0, b);
                     bulk_load(scd + hh * 2 * K::TB, a.cs + row, cdb, &full[st]);
                     bulk_load(scd + hh * 2 * K::TB + K::TB, a.dtt + row, cdb, &full[st]);
                 }
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
             const int64_t PN = (int64_t)d.headdim * N;
 #pragma unroll 1
             for (int hh = hsel; hh < HH; hh += K::SW) {
-                float* out = a.S + (((int64_t)b * a.nspans + s) * H + h0 + hh) * PN;
+                float* out = a.S + (((int64_t)b * a.nspans + s) * HC + h0 + hh) * PN;
 #pragma unroll 1
                 for (int mb = 0; mb < K::MB; ++mb) {
                     const int n = mb * 128 + r;
@@ -304,20 +306,22 @@ int launch_state_nh(const __nv_bfloat16* x, const __half* B, const StateArgs& a,
     if (!make_tmap_16b_4d(&tx, x, dx, box) || !make_tmap_16b_4d(&tb, B, db, box)) return SSD_ERR_CUDA;
     if (ensure_smem_limit(reinterpret_cast<const void*>(chunk_state_tc_kernel<N, HH>), K::SMEM) != SSD_OK)
         return SSD_ERR_CUDA;
-    dim3 grid(d.nheads / HH, a.nspans, d.batch);
+    dim3 grid(d.hcount / HH, a.nspans, d.batch);
     launch_begin(kKindChunkState, s);
     const cudaError_t le = launch_dependent(chunk_state_tc_kernel<N, HH>, grid, dim3(K::THREADS), K::SMEM, s, tx, tb, a);
     const int r = launch_end(kKindChunkState, s);
     return le != cudaSuccess ? SSD_ERR_CUDA : r;
 }
 
-// Heads per CTA: as many of one group as divide evenly, up to 4 (N <= 128) or 2 (N >= 256).
+// Heads per CTA: as many of one group as divide evenly, up to 4 (N <= 128) or 2 (N >= 256); with a
+// head range, the CTAs' head blocks must also tile the range and start on a multiple of the block.
 template <int N>
 int launch_state_n(const __nv_bfloat16* x, const __half* B, const StateArgs& a, cudaStream_t s) {
     const int hpg = a.d.nheads / a.d.ngroups;
+    auto fits = [&](int hh) { return hpg % hh == 0 && a.d.hcount % hh == 0 && a.d.head0 % hh == 0; };
     constexpr int HMAX = (N <= 128) ? 4 : 2;
-    if (HMAX >= 4 && hpg % 4 == 0) return launch_state_nh<N, (HMAX >= 4 ? 4 : 2)>(x, B, a, s);
-    if (hpg % 2 == 0) return launch_state_nh<N, 2>(x, B, a, s);
+    if (HMAX >= 4 && fits(4)) return launch_state_nh<N, (HMAX >= 4 ? 4 : 2)>(x, B, a, s);
+    if (fits(2)) return launch_state_nh<N, 2>(x, B, a, s);
     return launch_state_nh<N, 1>(x, B, a, s);
 }
 

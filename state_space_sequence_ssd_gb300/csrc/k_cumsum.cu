@@ -39,18 +39,34 @@ __device__ __forceinline__ uint4 cvt16(const uint4& v, float& mx) {
                       bf16x2_to_f16x2_sat(v.w, mx));
 }
 
+// The B / C rows (batch, token) the copy covers, in 16-byte chunks: columns [col0, col0 + ncol) of rows
+// of row16 chunks -- the groups of the call's heads (all of them for a whole-problem call: ncol == row16).
+struct BcSpan {
+    int64_t row16, col0, ncol;
+    __device__ __forceinline__ int64_t offset(int64_t i) const {
+        if (ncol == row16) return i;
+        if (i < 0xffffffffll) {  // 32-bit division where it fits
+            const uint32_t q = (uint32_t)i / (uint32_t)ncol;
+            return (int64_t)q * row16 + col0 + ((uint32_t)i - q * (uint32_t)ncol);
+        }
+        return (i / ncol) * row16 + col0 + i % ncol;
+    }
+};
+
 template <int Q>
 __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __restrict__ dt,
                                                                 const float* __restrict__ A, Dims d,
                                                                 float* __restrict__ cs, float* __restrict__ dtt,
                                                                 const uint4* __restrict__ bsrc,
                                                                 const uint4* __restrict__ csrc, uint4* __restrict__ bdst,
-                                                                uint4* __restrict__ cdst, int64_t bc16,
+                                                                uint4* __restrict__ cdst, int64_t bc16, BcSpan bsp,
                                                                 int* err, DtOpts dto) {
     // tile[h][i + i / 8]: one padding word per 8 positions, so that lanes reading runs of
     // consecutive positions spread over the banks
     __shared__ float tile[kHeads][Q + Q / 8];
+    // h0: first local head of this CTA (the call's intermediates); hg0 = h0 + head0 indexes dt, A, dt_bias
     const int c = blockIdx.x, h0 = blockIdx.y * kHeads, b = blockIdx.z;
+    const int hg0 = d.head0 + h0;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     grid_dep_launch_dependents();  // the next stage may set itself up while this one runs
     // this CTA's share of the B / C float16 copies (16-byte chunks); the first round of loads
@@ -69,8 +85,8 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
             first = true;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                vb[u] = __ldg(bsrc + i + u * kThreads);
-                vc[u] = __ldg(csrc + i + u * kThreads);
+                vb[u] = __ldg(bsrc + bsp.offset(i + u * kThreads));
+                vc[u] = __ldg(csrc + bsp.offset(i + u * kThreads));
             }
         }
     }
@@ -79,20 +95,20 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
         const int64_t t = (int64_t)c * Q + tid;
         float v[kHeads];
         if (t < d.seqlen) {
-            const float* src = dt + ((int64_t)b * d.seqlen + t) * d.nheads + h0;
-            if (h0 + kHeads <= d.nheads && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+            const float* src = dt + ((int64_t)b * d.seqlen + t) * d.nheads + hg0;
+            if (h0 + kHeads <= d.hcount && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
                 const float4 a0 = __ldg(reinterpret_cast<const float4*>(src));
                 const float4 a1 = __ldg(reinterpret_cast<const float4*>(src) + 1);
                 v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
                 v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
             } else {
 #pragma unroll
-                for (int k = 0; k < kHeads; ++k) v[k] = (h0 + k < d.nheads) ? __ldg(src + k) : 0.f;
+                for (int k = 0; k < kHeads; ++k) v[k] = (h0 + k < d.hcount) ? __ldg(src + k) : 0.f;
             }
             if (dto.active()) {  // the layer's dt transform, on real positions only (padding stays 0)
 #pragma unroll
                 for (int k = 0; k < kHeads; ++k)
-                    if (h0 + k < d.nheads) v[k] = effective_dt(v[k], h0 + k, dto);
+                    if (h0 + k < d.hcount) v[k] = effective_dt(v[k], hg0 + k, dto);
             }
         } else {
 #pragma unroll
@@ -108,29 +124,31 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
             if (!first) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    vb[u] = __ldg(bsrc + i + u * kThreads);
-                    vc[u] = __ldg(csrc + i + u * kThreads);
+                    vb[u] = __ldg(bsrc + bsp.offset(i + u * kThreads));
+                    vc[u] = __ldg(csrc + bsp.offset(i + u * kThreads));
                 }
             }
             first = false;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                bdst[i + u * kThreads] = cvt16(vb[u], mx);
-                cdst[i + u * kThreads] = cvt16(vc[u], mx);
+                const int64_t o = bsp.offset(i + u * kThreads);
+                bdst[o] = cvt16(vb[u], mx);
+                cdst[o] = cvt16(vc[u], mx);
             }
         }
         for (; i < hi; i += kThreads) {
-            const uint4 vb = __ldg(bsrc + i), vc = __ldg(csrc + i);
-            bdst[i] = cvt16(vb, mx);
-            cdst[i] = cvt16(vc, mx);
+            const int64_t o = bsp.offset(i);
+            const uint4 vb = __ldg(bsrc + o), vc = __ldg(csrc + o);
+            bdst[o] = cvt16(vb, mx);
+            cdst[o] = cvt16(vc, mx);
         }
         flag_f16_range(err, mx);
     }
     __syncthreads();
     const int h = h0 + warp;
-    if (h >= d.nheads) return;
+    if (h >= d.hcount) return;
     constexpr int kPer = Q / 32;  // positions per lane
-    const float a = __ldg(A + h);
+    const float a = __ldg(A + d.head0 + h);
     float v[kPer], run = 0.f;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
@@ -147,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
         if (lane >= off) tot += o;
     }
     const float excl = tot - run;
-    const int64_t row = (((int64_t)b * d.nheads + h) * d.nchunks + c) * Q + lane * kPer;
+    const int64_t row = (((int64_t)b * d.hcount + h) * d.nchunks + c) * Q + lane * kPer;
 #pragma unroll
     for (int k = 0; k < kPer; k += 2) {
         const int p0 = lane * kPer + k, p1 = p0 + 1;
@@ -161,17 +179,24 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
 int launch_chunk_cumsum_bc(const float* dt, const float* A, const Dims& d, float* cs, float* dtt,
                            const __nv_bfloat16* B, const __nv_bfloat16* C, __half* B16, __half* C16, int* err,
                            cudaStream_t s, const DtOpts& dto) {
-    dim3 grid(d.nchunks, ceil_div(d.nheads, kHeads), d.batch);
-    const int64_t bc16 = (B != nullptr) ? (int64_t)d.batch * d.seqlen * d.ngroups * d.dstate / 8 : 0;
+    dim3 grid(d.nchunks, ceil_div(d.hcount, kHeads), d.batch);
+    // the groups of the call's heads
+    const int hpg = d.nheads / d.ngroups;
+    const int g0 = d.head0 / hpg, g1 = (d.head0 + d.hcount - 1) / hpg + 1;
+    BcSpan bsp;
+    bsp.row16 = (int64_t)d.ngroups * d.dstate / 8;
+    bsp.col0 = (int64_t)g0 * d.dstate / 8;
+    bsp.ncol = (int64_t)(g1 - g0) * d.dstate / 8;
+    const int64_t bc16 = (B != nullptr) ? (int64_t)d.batch * d.seqlen * bsp.ncol : 0;
     const uint4* bs = reinterpret_cast<const uint4*>(B);
     const uint4* cs16 = reinterpret_cast<const uint4*>(C);
     uint4* bd = reinterpret_cast<uint4*>(B16);
     uint4* cd = reinterpret_cast<uint4*>(C16);
     launch_begin(kKindCumsum, s);
     switch (d.chunk_size) {
-        case 64: chunk_cumsum_kernel<64><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, err, dto); break;
-        case 128: chunk_cumsum_kernel<128><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, err, dto); break;
-        case 256: chunk_cumsum_kernel<256><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, err, dto); break;
+        case 64: chunk_cumsum_kernel<64><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, bsp, err, dto); break;
+        case 128: chunk_cumsum_kernel<128><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, bsp, err, dto); break;
+        case 256: chunk_cumsum_kernel<256><<<grid, kThreads, 0, s>>>(dt, A, d, cs, dtt, bs, cs16, bd, cd, bc16, bsp, err, dto); break;
         default: return SSD_ERR_UNSUPPORTED;
     }
     return launch_end(kKindCumsum, s);

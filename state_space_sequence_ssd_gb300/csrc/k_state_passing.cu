@@ -38,10 +38,12 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
     if (e >= PN) return;
     const int nc = d.nchunks;
     float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (init != nullptr) hv = *reinterpret_cast<const float4*>(init + ((int64_t)b * d.nheads + h) * PN + e);
-    const float* csl = dec + ((int64_t)b * d.nheads + h) * dec_row;
-    const int64_t cstride = (int64_t)d.nheads * PN;  // distance between consecutive chunks
-    const int64_t base = ((int64_t)b * nc * d.nheads + h) * PN + e;
+    // h: local head (S, states and dec hold the call's hcount heads); init and final are caller tensors
+    // indexed by the global head head0 + h
+    if (init != nullptr) hv = *reinterpret_cast<const float4*>(init + ((int64_t)b * d.nheads + d.head0 + h) * PN + e);
+    const float* csl = dec + ((int64_t)b * d.hcount + h) * dec_row;
+    const int64_t cstride = (int64_t)d.hcount * PN;  // distance between consecutive chunks
+    const int64_t base = ((int64_t)b * nc * d.hcount + h) * PN + e;
     // software pipeline: the next group of kUnroll steps is loaded before the current one is folded
     float4 sv[kUnroll], nv[kUnroll];
     float dk[kUnroll], nd[kUnroll];
@@ -79,7 +81,7 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
         }
     }
     if (final_state != nullptr)
-        *reinterpret_cast<float4*>(final_state + ((int64_t)b * d.nheads + h) * PN + e) = hv;
+        *reinterpret_cast<float4*>(final_state + ((int64_t)b * d.nheads + d.head0 + h) * PN + e) = hv;
 }
 
 }  // namespace
@@ -97,7 +99,7 @@ int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_ste
     Dims dd = d;
     dd.nchunks = nsteps;
     const int64_t PN = (int64_t)d.headdim * d.dstate;
-    dim3 grid((unsigned)ceil_div64(PN, (int64_t)kThreads * 4), d.nheads, d.batch);
+    dim3 grid((unsigned)ceil_div64(PN, (int64_t)kThreads * 4), d.hcount, d.batch);
     launch_begin(kKindStatePassing, s);
     const cudaError_t le =
         launch_dependent(state_passing_kernel, grid, dim3(kThreads), 0, s, S, dec, dec_step, dec_row, init, dd, states,

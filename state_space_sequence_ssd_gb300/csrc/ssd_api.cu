@@ -142,6 +142,8 @@ Dims make_dims(int batch, int seqlen, int nheads, int headdim, int ngroups, int 
     d.dstate = dstate;
     d.chunk_size = chunk_size;
     d.nchunks = (seqlen + chunk_size - 1) / chunk_size;
+    d.head0 = 0;
+    d.hcount = nheads;
     return d;
 }
 
@@ -219,7 +221,7 @@ int workspace_alloc(void** ptr, size_t bytes, cudaStream_t s) {
 // (batch, head, span), so the span-level intermediates stay small while
 // every SM stays busy.
 int forward_span_chunks(const Dims& d) {
-    const int64_t units = (int64_t)d.batch * d.nheads * d.nchunks;
+    const int64_t units = (int64_t)d.batch * d.hcount * d.nchunks;
     int64_t k = (units + 1215) / 1216;
     if (k < 1) k = 1;
     if (k > 64) k = 64;
@@ -281,13 +283,13 @@ int forward_scan_step(const Dims& d, int span, const OutOpts& oo) {
     static std::map<std::array<int64_t, 6>, int> cache;
     const int sms = device_sms();
     const bool pair = chunk_scan_pair_supported(d, oo);
-    const std::array<int64_t, 6> key = {d.batch, d.nheads, d.nchunks, span, sms, pair ? 1 : 0};
+    const std::array<int64_t, 6> key = {d.batch, d.hcount, d.nchunks, span, sms, pair ? 1 : 0};
     {
         std::lock_guard<std::mutex> lk(mu);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    const int64_t rows = pair ? d.nheads / 2 : d.nheads;
+    const int64_t rows = pair ? d.hcount / 2 : d.hcount;
     int best = 1;
     double best_t = scan_makespan(rows, d.batch, d.nchunks, d.chunk_size, span, sms);
     for (int m = 2; m <= 4; m *= 2) {
@@ -344,9 +346,9 @@ struct NoallocLayout {
 
 NoallocLayout noalloc_layout(const Dims& d, int span) {
     const int nspans = ceil_div(d.nchunks, span);
-    const size_t ncq = (size_t)d.batch * d.nheads * d.nchunks * d.chunk_size;
-    const size_t nst = (size_t)d.batch * nspans * d.nheads * d.headdim * d.dstate;
-    const size_t ndec = (size_t)d.batch * d.nheads * nspans;
+    const size_t ncq = (size_t)d.batch * d.hcount * d.nchunks * d.chunk_size;
+    const size_t nst = (size_t)d.batch * nspans * d.hcount * d.headdim * d.dstate;
+    const size_t ndec = (size_t)d.batch * d.hcount * nspans;
     const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;
     NoallocLayout l;
     l.off_dtt = round256(ncq * sizeof(float));
@@ -356,6 +358,69 @@ NoallocLayout noalloc_layout(const Dims& d, int span) {
     l.off_C16 = l.off_B16 + round256(nbc * sizeof(__half));
     l.need = l.off_C16 + round256(nbc * sizeof(__half));
     return l;
+}
+
+// The four stages of one forward over the call's heads (d.head0, d.hcount), with the workspace parts
+// given: dA_cumsum and dt rows (b, hcount, nc, Q), span states (b, nspans, hcount, P, N), span decays
+// (b, hcount, nspans), float16 B and C (the caller's layout; the groups of the call's heads written).
+int run_forward(const Dims& d, const void* x, const float* dt, const float* A, const void* B, const void* C,
+                const float* D, const float* init_state, void* y, float* final_state, float* cs, float* dtt, float* S,
+                float* dec, __half* B16, __half* C16, int* err, cudaStream_t stream, const DtOpts& dto,
+                const OutOpts& oo) {
+    const int span = forward_span_chunks(d);
+    const int nspans = ceil_div(d.nchunks, span);
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    int r = launch_chunk_cumsum_bc(dt, A, d, cs, dtt, static_cast<const __nv_bfloat16*>(B),
+                                   static_cast<const __nv_bfloat16*>(C), B16, C16, err, stream, dto);
+    if (r == SSD_OK)
+        r = launch_chunk_state_span(xb, B16, dtt, cs, span, d, S, dec, make_ctl(err, kKindChunkState), stream);
+    // span-level hop, in place: S becomes the span-start states
+    if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
+    if (r == SSD_OK)
+        r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y),
+                                   make_ctl(err, kKindChunkScan), stream, oo, forward_scan_step(d, span, oo));
+    return r;
+}
+
+// Validation shared by the forward entry points (pointers, shapes, alignment).
+int check_forward(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,
+                  const float* init_state, int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                  int chunk_size, const void* y, const float* final_state) {
+    if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    const int r = check_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    if (r != SSD_OK) return r;
+    if (!aligned16(x) || !aligned16(B) || !aligned16(C) || !aligned16(y) || ((uintptr_t)dt & 3u) ||
+        ((uintptr_t)A & 3u) || (D && ((uintptr_t)D & 3u)) || (init_state && !aligned16(init_state)) ||
+        (final_state && !aligned16(final_state)))
+        return SSD_ERR_INVALID_ARG;
+    return SSD_OK;
+}
+
+// Forward over the heads of d with a stream-ordered workspace from the library's pool.
+int forward_pooled(const Dims& d, const void* x, const float* dt, const float* A, const void* B, const void* C,
+                   const float* D, const float* init_state, void* y, float* final_state, cudaStream_t stream,
+                   const DtOpts& dto, const OutOpts& oo) {
+    int* err = device_error_ptr();
+    if (err == nullptr) return SSD_ERR_CUDA;
+    const int span = forward_span_chunks(d);
+    const int nspans = ceil_div(d.nchunks, span);
+    const size_t ncq = (size_t)d.batch * d.hcount * d.nchunks * d.chunk_size;
+    const size_t nst = (size_t)d.batch * nspans * d.hcount * d.headdim * d.dstate;
+    const size_t ndec = ((size_t)d.batch * d.hcount * nspans + 3) & ~(size_t)3;
+    const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;  // multiple of 64
+    const size_t bytes = (2 * ncq + nst + ndec) * sizeof(float) + 2 * nbc * sizeof(__half);
+    void* ws = nullptr;
+    if (workspace_alloc(&ws, bytes, stream) != SSD_OK) return SSD_ERR_NO_MEMORY;
+    float* cs = static_cast<float*>(ws);
+    float* dtt = cs + ncq;
+    float* S = dtt + ncq;
+    float* dec = S + nst;
+    __half* B16 = reinterpret_cast<__half*>(dec + ndec);
+    __half* C16 = B16 + nbc;
+    int r = run_forward(d, x, dt, A, B, C, D, init_state, y, final_state, cs, dtt, S, dec, B16, C16, err, stream, dto,
+                        oo);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
+    return r;
 }
 
 }  // namespace
@@ -471,84 +536,72 @@ int ssd_forward_ex(const void* x, const float* dt, const float* A, const void* B
                    const float* init_state, int batch, int seqlen, int nheads, int headdim, int ngroups,
                    int dstate, int chunk_size, const ssd_input_options* options, void* y, float* final_state,
                    cudaStream_t stream) {
-    if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
-    int r = check_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    int r = check_forward(x, dt, A, B, C, D, init_state, batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size,
+                          y, final_state);
     if (r != SSD_OK) return r;
-    if (!aligned16(x) || !aligned16(B) || !aligned16(C) || !aligned16(y) || ((uintptr_t)dt & 3u) ||
-        ((uintptr_t)A & 3u) || (D && ((uintptr_t)D & 3u)) || (init_state && !aligned16(init_state)) ||
-        (final_state && !aligned16(final_state)))
-        return SSD_ERR_INVALID_ARG;
     DtOpts dto;
     OutOpts oo;
     r = read_options(options, D, true, &dto, &oo);
     if (r != SSD_OK) return r;
+    const Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    return forward_pooled(d, x, dt, A, B, C, D, init_state, y, final_state, stream, dto, oo);
+}
+
+int ssd_forward_heads(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,
+                      const float* init_state, int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                      int chunk_size, int head_begin, int head_count, void* y, float* final_state,
+                      cudaStream_t stream) {
+    int r = check_forward(x, dt, A, B, C, D, init_state, batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size,
+                          y, final_state);
+    if (r != SSD_OK) return r;
+    if (head_begin < 0 || head_count < 1 || head_begin > nheads - head_count) return SSD_ERR_INVALID_ARG;
     Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
-    int* err = device_error_ptr();
-    if (err == nullptr) return SSD_ERR_CUDA;
-    const int span = forward_span_chunks(d);
-    const int nspans = ceil_div(d.nchunks, span);
-    const size_t ncq = (size_t)d.batch * d.nheads * d.nchunks * d.chunk_size;
-    const size_t nst = (size_t)d.batch * nspans * d.nheads * d.headdim * d.dstate;
-    const size_t ndec = ((size_t)d.batch * d.nheads * nspans + 3) & ~(size_t)3;
-    const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;  // multiple of 64
-    const size_t bytes = (2 * ncq + nst + ndec) * sizeof(float) + 2 * nbc * sizeof(__half);
-    void* ws = nullptr;
-    if (workspace_alloc(&ws, bytes, stream) != SSD_OK) return SSD_ERR_NO_MEMORY;
-    float* cs = static_cast<float*>(ws);
-    float* dtt = cs + ncq;
-    float* S = dtt + ncq;
-    float* dec = S + nst;
-    __half* B16 = reinterpret_cast<__half*>(dec + ndec);
-    __half* C16 = B16 + nbc;
-    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-    r = launch_chunk_cumsum_bc(dt, A, d, cs, dtt, static_cast<const __nv_bfloat16*>(B),
-                               static_cast<const __nv_bfloat16*>(C), B16, C16, err, stream, dto);
-    if (r == SSD_OK)
-        r = launch_chunk_state_span(xb, B16, dtt, cs, span, d, S, dec, make_ctl(err, kKindChunkState), stream);
-    // span-level hop, in place: S becomes the span-start states
-    if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
-    if (r == SSD_OK)
-        r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y),
-                                   make_ctl(err, kKindChunkScan), stream, oo, forward_scan_step(d, span, oo));
-    if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
-    return r;
+    d.head0 = head_begin;
+    d.hcount = head_count;
+    return forward_pooled(d, x, dt, A, B, C, D, init_state, y, final_state, stream, DtOpts(), OutOpts());
+}
+
+int ssd_partition_heads(int nheads, int ngroups, int nparts, int part, int* head_begin, int* head_count) {
+    if (nheads <= 0 || ngroups <= 0 || nheads % ngroups != 0 || nparts <= 0 || part < 0 || part >= nparts ||
+        !head_begin || !head_count)
+        return SSD_ERR_INVALID_ARG;
+    const int hpg = nheads / ngroups;
+    int b = 0, e = 0;
+    if (ngroups >= nparts) {
+        // whole groups: part p takes groups [floor(p G / n), floor((p + 1) G / n))
+        b = (int)((int64_t)part * ngroups / nparts) * hpg;
+        e = (int)((int64_t)(part + 1) * ngroups / nparts) * hpg;
+    } else {
+        // fewer groups than parts: split heads evenly, in blocks of two heads where the count allows
+        // (compute_out then keeps two heads per CTA), never a block across a group boundary
+        const int unit = (hpg % 2 == 0) ? 2 : 1;
+        const int nunits = nheads / unit;
+        b = (int)((int64_t)part * nunits / nparts) * unit;
+        e = (int)((int64_t)(part + 1) * nunits / nparts) * unit;
+    }
+    *head_begin = b;
+    *head_count = e - b;
+    return SSD_OK;
 }
 
 int ssd_forward_noalloc(const void* x, const float* dt, const float* A, const void* B, const void* C,
                         const float* D, const float* init_state, int batch, int seqlen, int nheads, int headdim,
                         int ngroups, int dstate, int chunk_size, void* y, float* final_state, cudaStream_t stream) {
-    if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
-    int r = check_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    int r = check_forward(x, dt, A, B, C, D, init_state, batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size,
+                          y, final_state);
     if (r != SSD_OK) return r;
-    if (!aligned16(x) || !aligned16(B) || !aligned16(C) || !aligned16(y) || ((uintptr_t)dt & 3u) ||
-        ((uintptr_t)A & 3u) || (D && ((uintptr_t)D & 3u)) || (init_state && !aligned16(init_state)) ||
-        (final_state && !aligned16(final_state)))
-        return SSD_ERR_INVALID_ARG;
-    Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    const Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
     const int span = forward_span_chunks(d);
-    const int nspans = ceil_div(d.nchunks, span);
     // the same regions as ssd_forward, each starting on a 256-byte boundary
     const NoallocLayout l = noalloc_layout(d, span);
     if (l.need > (size_t)SSD_NOALLOC_SCRATCH_BYTES) return SSD_ERR_SCRATCH_TOO_SMALL;
     int* err = device_error_ptr();
     unsigned char* ws = noalloc_scratch_ptr();
     if (err == nullptr || ws == nullptr) return SSD_ERR_CUDA;
-    float* cs = reinterpret_cast<float*>(ws);
-    float* dtt = reinterpret_cast<float*>(ws + l.off_dtt);
-    float* S = reinterpret_cast<float*>(ws + l.off_S);
-    float* dec = reinterpret_cast<float*>(ws + l.off_dec);
-    __half* B16 = reinterpret_cast<__half*>(ws + l.off_B16);
-    __half* C16 = reinterpret_cast<__half*>(ws + l.off_C16);
-    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-    r = launch_chunk_cumsum_bc(dt, A, d, cs, dtt, static_cast<const __nv_bfloat16*>(B),
-                               static_cast<const __nv_bfloat16*>(C), B16, C16, err, stream);
-    if (r == SSD_OK)
-        r = launch_chunk_state_span(xb, B16, dtt, cs, span, d, S, dec, make_ctl(err, kKindChunkState), stream);
-    if (r == SSD_OK) r = launch_state_passing_steps(S, dec, 1, nspans, init_state, d, nspans, S, final_state, stream);
-    if (r == SSD_OK)
-        r = launch_chunk_scan_span(xb, B16, C16, dtt, cs, D, S, span, d, static_cast<__nv_bfloat16*>(y),
-                                   make_ctl(err, kKindChunkScan), stream, OutOpts(), forward_scan_step(d, span, OutOpts()));
-    return r;
+    return run_forward(d, x, dt, A, B, C, D, init_state, y, final_state, reinterpret_cast<float*>(ws),
+                       reinterpret_cast<float*>(ws + l.off_dtt), reinterpret_cast<float*>(ws + l.off_S),
+                       reinterpret_cast<float*>(ws + l.off_dec), reinterpret_cast<__half*>(ws + l.off_B16),
+                       reinterpret_cast<__half*>(ws + l.off_C16), err, stream, DtOpts(), OutOpts());
 }
 
 int ssd_forward_plan(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk_size,

@@ -74,3 +74,25 @@ def test_source_key_ignores_comments_only():
     import bench
     assert bench._code_only("x = a; // note\n/* block\n comment */ y = b;") == bench._code_only("x = a;\ny = b;")
     assert bench._code_only("x = a;") != bench._code_only("x = b;")
+
+
+def test_head_split_places_each_ranks_inputs():
+    """bench.py's multi-GPU layout (on CPU tensors): world x H heads in world x G groups, rank r owning
+    heads [r H, (r + 1) H) and groups [r G, (r + 1) G), with its own seeded inputs in that slice."""
+    import bench
+    import state_space_sequence_ssd_gb300 as ssd
+    from state_space_sequence_ssd_gb300 import build, inputs as I
+    build.build()
+    w = I.Workload("split", 1, 96, 4, 64, 64, 2, 64, True)
+    for world in (2, 3):
+        for rank in range(world):
+            d = I.make_inputs(w, seed=rank)
+            sp = bench.head_split(w, world, rank, d, torch.device("cpu"), ssd)
+            t = sp["t"]
+            hb, hc = sp["head_begin"], sp["head_count"]
+            assert (hb, hc) == (rank * w.nheads, w.nheads)
+            assert t["x"].shape[2] == world * w.nheads and t["B"].shape[2] == world * w.ngroups
+            assert torch.equal(t["x"][:, :, hb:hb + hc], d["x"])
+            assert torch.equal(t["B"][:, :, rank * w.ngroups:(rank + 1) * w.ngroups], d["B"])
+            assert torch.equal(t["init"][:, hb:hb + hc], d["init"])
+            assert torch.equal(t["A"][hb:hb + hc], d["A"])
