@@ -21,17 +21,18 @@
 //                                            (M = 128 = both heads' p, N = dstate, K = tokens)
 //   CB  CB   = C B^T                         (128 x 128, once for both heads)
 //   YS  Yst  = C H^T                         (H = float16 copy of hT; N = both heads' p)
-//   mask M_h = CB * 2^(u_i - u_j) dt_j [j <= i] + D_h [j == i]   (float16, in place over CB)
-//   MX  Y_h  = M_h X_h                       (A from TMEM)
+//   mask M_h = CB * 2^(u_i - u_j) dt_j [j <= i]   (float16, in place over CB)
+//   MX  Y_h  = M_h X_h + X_h diag(D_h)       (A from TMEM; the skip term as one more small product on a
+//                                            float16 diag(D_h) tile built once per CTA)
 //   y_i = Y_i + 2^(u_i) Yst_i
 //
 // Roles (736 threads):
 //   warps 0-7   mask, two warpgroups MG = 0, 1, warpgroup MG taking 32-column
 //               blocks 2 MG and 2 MG + 1 of every row of CB (one row per
 //               thread); the two heads' masked rows are written back into the
-//               row's own CB columns, interleaved per block (M_0 in the first
-//               16 columns, M_1 in the last), so every block is read before it
-//               is overwritten
+//               row's own CB columns, interleaved per 16-column half-block (M_0
+//               of its 16 positions in 8 packed columns, then M_1), so every
+//               half is read before it is overwritten
 //   warps 8-15  state, two warpgroups SX = 0, 1 (the serial chain of the pass,
 //               split in halves): per sub-block (a) the decays of head SX for
 //               the thread's token row, (b) the float16 copy H of half SX of
@@ -83,12 +84,14 @@ struct PCfg {
     static constexpr int OFF_BC = OFF_H + NBOX * kTile;     // NSLOT tile slots
     static constexpr int OFF_U = OFF_BC + NSLOT * SLOT;     // 3 x 2 heads x {u, dt, bcol, -}[128] floats
     static constexpr int OFF_CD = OFF_U + 3 * 2 * 2048;     // NX x 2 heads x {cs, dt}[128] floats
-    static constexpr int OFF_BAR = OFF_CD + NX * 2 * 1024;
+    static constexpr int OFF_DG = OFF_CD + NX * 2 * 1024;   // 2 x diag(D_h) 64 x 64 float16, K-major, swizzled
+    static constexpr int OFF_BAR = OFF_DG + 2 * 8192;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;       // + alignment slack
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 constexpr uint32_t kIdescMX = idesc_fp16(128, 64, false, true);
+constexpr uint32_t kIdescDX = idesc_fp16(128, 64, false, false);  // X (K-major over channels) diag(D)
 constexpr uint32_t kIdescKK = idesc_fp16(128, 128, false, false);  // C B^T and C H^T: both operands K-major
 
 struct PairArgs {
@@ -166,6 +169,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int* const err = a.ctl.err;
     const uint64_t wait_ns = a.ctl.wait_ns;
+    if (a.D != nullptr) {
+        // diag(D_h) of each head as the B operand of Y_h += X_h diag(D_h): row n (output channel) holds D_h
+        // at column k = n.  128B swizzle: row n at (n / 8) * 1024 + (n % 8) * 128, 16-byte chunk j stored
+        // at chunk j ^ (n % 8).
+        for (int c = threadIdx.x; c < 1024; c += kThreads) {
+            const int hh = c >> 9, cc = c & 511;
+            const int n = (cc >> 6) * 8 + ((cc >> 3) & 7);
+            const int j = (cc & 7) ^ (n & 7);  // logical chunk: columns 8j .. 8j+7
+            uint32_t v = 0u;                   // the diagonal element, placed in its 32-bit word of the chunk
+            if (j == (n >> 3)) {
+                const __half dv = __float2half_rn(a.D[h0 + hh]);
+                const uint32_t bits = *reinterpret_cast<const uint16_t*>(&dv);
+                v = (n & 1) ? (bits << 16) : bits;
+            }
+            const int wi = (n & 7) >> 1;
+            reinterpret_cast<uint4*>(smem + K::OFF_DG)[c] =
+                make_uint4(wi == 0 ? v : 0u, wi == 1 ? v : 0u, wi == 2 ? v : 0u, wi == 3 ? v : 0u);
+        }
+        fence_proxy_async_smem();
+    }
     if (warp == kWarpMma) {
         tmem_alloc(&tmem_base_sh, K::TCOLS);
         tmem_relinquish();
@@ -282,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&bar->ys_done);
                 mma_commit(&bar->bc_empty[iC % K::NSLOT]);
-                // Y_h = M_h X_h: A = M_h from TMEM (32-column block q holds M_0 then M_1, 16 columns each),
-                // B = the float16 x tile of head hh (MN-major)
+                // Y_h = M_h X_h: A = M_h from TMEM (16-column half hf of block q holds M_0 then M_1 of its 16
+                // positions, 8 columns each), B = the float16 x tile of head hh (MN-major)
                 if (!wait_bounded<true>(&bar->m_ready, k & 1, abort_flag, err, 38, wait_ns) ||
                     !wait_bounded<true>(&bar->xf_ready, k & 1, abort_flag, err, 39, wait_ns))
                     break;
@@ -293,8 +316,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sX = smem_u32(xtile(k % K::NX, hh));
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tm + K::T_Y + 64 * hh, tm + K::T_CB + 32 * (kk >> 1) + 16 * hh + 8 * (kk & 1),
+                        mma_ts(tm + K::T_Y + 64 * hh, tm + K::T_CB + 32 * (kk >> 1) + 16 * (kk & 1) + 8 * hh,
                                desc_sw128(sX + kk * 2048, 16, 1024), kIdescMX, kk > 0);
+                    if (a.D != nullptr) {  // the skip term: Y_h += X_h diag(D_h) (the x tile read K-major)
+                        const uint32_t sDg = smem_u32(smem + K::OFF_DG + hh * 8192);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tm + K::T_Y + 64 * hh, desc_sw128(sX + kk * 32, 16, 1024),
+                                   desc_sw128(sDg + kk * 32, 16, 1024), kIdescDX, 1);
+                    }
                 }
                 mma_commit(&bar->y_full);
                 mma_commit(&bar->x_empty[k % K::NX]);
@@ -311,9 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wq = warp & 3;  // row block of this warp
         const int MG = warp >> 2;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-        float Dh[2];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) Dh[hh] = (a.D != nullptr) ? a.D[h0 + hh] : 0.f;
         __half2 mx = __floats2half2_rn(0.f, 0.f);
         for (int k = 0; k < nsb; ++k) {
             const int ub = k % 3;
@@ -335,44 +362,85 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(cb + 32 * q, z);
                     continue;
                 }
-                uint32_t v[32];
-                tmem_ld32(cb + 32 * q, v);
-                tmem_ld_wait(v);
-                // block q is read; it now receives M_0 (16 columns) then M_1 (16 columns)
-#pragma unroll 1
+                // the block in two halves of 16 columns; half hf of CB is read before its 16 columns receive
+                // M_0 then M_1 of the same 16 positions (8 packed columns each)
+                const float* su0 = sU + (2 * ub) * 512;
+                const float* su1 = su0 + 512;
+                const bool diag = q == wq;
+                bool fact[2] = {true, true};  // diagonal block: factorized when its decay is below 2^60
+                float ar[2];
+#pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    const float* su = sU + (2 * ub + hh) * 512;
+                    const float* su = hh ? su1 : su0;
                     const float uih = hh ? ui[1] : ui[0];  // selects: no local-memory array
-                    const float Dhh = hh ? Dh[1] : Dh[0];
-                    uint32_t o[16];
-                    if (q < wq) {  // strictly below: 2^(u_i - u_j) = 2^(u_i - u_r) 2^(u_r - u_j), r = block end
-                        const float ar = fast_exp2(fminf(uih - su[q * 32 + 31], 0.f));
-#pragma unroll
-                        for (int jj = 0; jj < 32; jj += 2) {
-                            const float2 bc = *reinterpret_cast<const float2*>(su + 256 + q * 32 + jj);
-                            const uint32_t pk = pack_f16x2(__uint_as_float(v[jj]) * (ar * bc.x),
-                                                           __uint_as_float(v[jj + 1]) * (ar * bc.y));
-                            hmax_abs(mx, pk);
-                            o[jj >> 1] = pk;
-                        }
-                    } else {  // diagonal block: exact exponent, causal mask, D on the diagonal
-#pragma unroll
-                        for (int jj = 0; jj < 32; jj += 2) {
-                            const int j0 = q * 32 + jj, j1 = j0 + 1;
-                            const float2 uj = *reinterpret_cast<const float2*>(su + j0);
-                            const float2 dj = *reinterpret_cast<const float2*>(su + 128 + j0);
-                            float m0 = __uint_as_float(v[jj]) * fast_exp2(fminf(uih - uj.x, 0.f)) * dj.x;
-                            float m1 = __uint_as_float(v[jj + 1]) * fast_exp2(fminf(uih - uj.y, 0.f)) * dj.y;
-                            m0 = (j0 <= r) ? m0 : 0.f;
-                            m1 = (j1 <= r) ? m1 : 0.f;
-                            m0 += (j0 == r) ? Dhh : 0.f;
-                            m1 += (j1 == r) ? Dhh : 0.f;
-                            const uint32_t pk = pack_f16x2(m0, m1);
-                            hmax_abs(mx, pk);
-                            o[jj >> 1] = pk;
-                        }
+                    const float ue = su[q * 32 + 31];       // u at the block end (its last valid position)
+                    if (diag) {
+                        // the block decays by less than 2^60: 2^(u_i - u_j) = 2^(u_i - u_e) 2^(u_e - u_j) with
+                        // a row factor in [1, 2^60] and column weights in [2^-60, 1] dt_j (warp-uniform)
+                        fact[hh] = su[q * 32] - ue < 60.f;
+                        ar[hh] = fast_exp2(uih - ue);
+                    } else {  // strictly below: both factors <= 1
+                        ar[hh] = fast_exp2(fminf(uih - ue, 0.f));
                     }
-                    tmem_st16(cb + 32 * q + 16 * hh, o);
+                }
+#pragma unroll 1
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t v[16];
+                    tmem_ld16(cb + 32 * q + 16 * hf, v);
+                    tmem_ld_wait16(v);
+                    uint32_t o[16];  // M_0 (o[0..7]) and M_1 (o[8..15]) of these 16 positions
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const float* su = hh ? su1 : su0;
+                        const float uih = hh ? ui[1] : ui[0];
+                        const float arh = hh ? ar[1] : ar[0];
+                        const bool fh = hh ? fact[1] : fact[0];
+                        const int jb = q * 32 + 16 * hf;  // first column of this half
+                        float m[16];
+                        if (!diag || fh) {
+                            // the 16 column weights first (four 16-byte loads, all issued before any use)
+                            float4 bc[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) bc[i] = *reinterpret_cast<const float4*>(su + 256 + jb + 4 * i);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                m[4 * i + 0] = __uint_as_float(v[4 * i + 0]) * (arh * bc[i].x);
+                                m[4 * i + 1] = __uint_as_float(v[4 * i + 1]) * (arh * bc[i].y);
+                                m[4 * i + 2] = __uint_as_float(v[4 * i + 2]) * (arh * bc[i].z);
+                                m[4 * i + 3] = __uint_as_float(v[4 * i + 3]) * (arh * bc[i].w);
+                            }
+                        } else {  // steep decay in the diagonal block: the exact exponent per element
+                            float4 uj[4], dj[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                uj[i] = *reinterpret_cast<const float4*>(su + jb + 4 * i);
+                                dj[i] = *reinterpret_cast<const float4*>(su + 128 + jb + 4 * i);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                m[4 * i + 0] = __uint_as_float(v[4 * i + 0]) * fast_exp2(fminf(uih - uj[i].x, 0.f)) * dj[i].x;
+                                m[4 * i + 1] = __uint_as_float(v[4 * i + 1]) * fast_exp2(fminf(uih - uj[i].y, 0.f)) * dj[i].y;
+                                m[4 * i + 2] = __uint_as_float(v[4 * i + 2]) * fast_exp2(fminf(uih - uj[i].z, 0.f)) * dj[i].z;
+                                m[4 * i + 3] = __uint_as_float(v[4 * i + 3]) * fast_exp2(fminf(uih - uj[i].w, 0.f)) * dj[i].w;
+                            }
+                        }
+                        if (diag) {  // causal mask: column jb + jj is kept for rows r >= it
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) m[jj] = (jb + jj <= r) ? m[jj] : 0.f;
+                        }
+                        // pack, and fold the magnitudes in a tree (short dependency chains)
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) pk[jj] = pack_f16x2(m[2 * jj], m[2 * jj + 1]);
+                        __half2 t0 = __hmax2(__habs2(*reinterpret_cast<__half2*>(&pk[0])), __habs2(*reinterpret_cast<__half2*>(&pk[1])));
+                        __half2 t1 = __hmax2(__habs2(*reinterpret_cast<__half2*>(&pk[2])), __habs2(*reinterpret_cast<__half2*>(&pk[3])));
+                        __half2 t2 = __hmax2(__habs2(*reinterpret_cast<__half2*>(&pk[4])), __habs2(*reinterpret_cast<__half2*>(&pk[5])));
+                        __half2 t3 = __hmax2(__habs2(*reinterpret_cast<__half2*>(&pk[6])), __habs2(*reinterpret_cast<__half2*>(&pk[7])));
+                        mx = __hmax2(mx, __hmax2(__hmax2(t0, t1), __hmax2(t2, t3)));
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) o[8 * hh + jj] = pk[jj];
+                    }
+                    tmem_st16(cb + 32 * q + 16 * hf, o);
                 }
             }
             tmem_st_wait();
@@ -414,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 4; ++e) {
                             const float2 f = __bfloat1622float2(p2[e]);
                             o4[e] = pack_f16x2(f.x, f.y);
-                            hmax_abs(mx, o4[e]);
                         }
+                        hmax_abs4(mx, o.x, o.y, o.z, o.w);
                         *reinterpret_cast<uint4*>(xrow + sw128_offset(r, ch)) = o;
                     }
                     fence_proxy_async_smem();
@@ -497,10 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         o.y = pack_f16x2(__uint_as_float(v[8 * q4 + 2]), __uint_as_float(v[8 * q4 + 3]));
                         o.z = pack_f16x2(__uint_as_float(v[8 * q4 + 4]), __uint_as_float(v[8 * q4 + 5]));
                         o.w = pack_f16x2(__uint_as_float(v[8 * q4 + 6]), __uint_as_float(v[8 * q4 + 7]));
-                        hmax_abs(mx, o.x);
-                        hmax_abs(mx, o.y);
-                        hmax_abs(mx, o.z);
-                        hmax_abs(mx, o.w);
+                        hmax_abs4(mx, o.x, o.y, o.z, o.w);
                         *reinterpret_cast<uint4*>(kb + sw128_offset(r, 4 * (c & 1) + q4)) = o;
                     }
 #pragma unroll
@@ -527,8 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 4; ++e) {
                         const float2 f = __bfloat1622float2(p2[e]);
                         o4[e] = pack_f16x2(f.x * w, f.y * w);
-                        hmax_abs(mx, o4[e]);
                     }
+                    hmax_abs4(mx, o.x, o.y, o.z, o.w);
                     *reinterpret_cast<uint4*>(xrow + sw128_offset(r, ch)) = o;
                 }
                 fence_proxy_async_smem();

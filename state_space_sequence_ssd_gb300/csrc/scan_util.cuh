@@ -70,6 +70,13 @@ __device__ __forceinline__ void hmax_abs(__half2& acc, uint32_t packed) {
     acc = __hmax2(acc, __habs2(v));
 }
 
+// Four packed pairs folded at once, as a tree: a chain of one dependent maximum per four pairs.
+__device__ __forceinline__ void hmax_abs4(__half2& acc, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    const __half2 ab = __hmax2(__habs2(*reinterpret_cast<const __half2*>(&a)), __habs2(*reinterpret_cast<const __half2*>(&b)));
+    const __half2 cd = __hmax2(__habs2(*reinterpret_cast<const __half2*>(&c)), __habs2(*reinterpret_cast<const __half2*>(&d)));
+    acc = __hmax2(acc, __hmax2(ab, cd));
+}
+
 __device__ __forceinline__ float hmax_to_float(__half2 acc) {
     return fmaxf(__low2float(acc), __high2float(acc));
 }

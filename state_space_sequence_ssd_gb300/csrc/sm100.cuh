@@ -136,6 +136,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return mbar_wait_bounded_slow(bar, parity, abort, err, code, limit_ns);
 }
 
+// Per-warpgroup register budgets (all four warps of a warpgroup execute the same one).  The budgets
+// of all warpgroups must add up to at most the registers the CTA was launched with, or an increase
+// waits for registers that are never released.
+template <int NREG>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(NREG));
+}
+template <int NREG>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(NREG));
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
