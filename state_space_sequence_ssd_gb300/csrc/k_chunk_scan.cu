@@ -491,32 +491,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t v[32];
                     tmem_ld32(set + q * 32, v);
                     tmem_ld_wait(v);
-                    if (q < warp) {  // strictly below: factorized decay
-                        const float ar = fast_exp2(fminf(ui - su[q * 32 + 31], 0.f));
+                    const float ue = su[q * 32 + 31];  // u at the block end (its last valid position)
+                    const bool diag = q == warp;
+                    float m[32];
+                    if (!diag || su[q * 32] - ue < 60.f) {
+                        // 2^(u_i - u_j) = 2^(u_i - u_e) 2^(u_e - u_j): below the diagonal both factors are <= 1;
+                        // on it the block decays by less than 2^60, so the row factor is in [1, 2^60] and
+                        // the column weights in [2^-60, 1] dt_j (a warp-uniform branch)
+                        const float ar = diag ? fast_exp2(ui - ue) : fast_exp2(fminf(ui - ue, 0.f));
+                        float4 bc[8];
 #pragma unroll
-                        for (int jj = 0; jj < 32; jj += 2) {
-                            const int j = q * 32 + jj;
-                            o[jj >> 1] = pack_f16x2(__uint_as_float(v[jj]) * (ar * sbc[j]),
-                                                    __uint_as_float(v[jj + 1]) * (ar * sbc[j + 1]));
-                            hmax_abs(mx, o[jj >> 1]);
+                        for (int i = 0; i < 8; ++i) bc[i] = *reinterpret_cast<const float4*>(sbc + q * 32 + 4 * i);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            m[4 * i + 0] = __uint_as_float(v[4 * i + 0]) * (ar * bc[i].x);
+                            m[4 * i + 1] = __uint_as_float(v[4 * i + 1]) * (ar * bc[i].y);
+                            m[4 * i + 2] = __uint_as_float(v[4 * i + 2]) * (ar * bc[i].z);
+                            m[4 * i + 3] = __uint_as_float(v[4 * i + 3]) * (ar * bc[i].w);
                         }
-                    } else {
-                        // diagonal block: exact per-element exponent, causal mask, D on the diagonal
+                    } else {  // steep decay in the diagonal block: the exact exponent per element
 #pragma unroll
-                        for (int jj = 0; jj < 32; jj += 2) {
-                            const int j0 = q * 32 + jj, j1 = j0 + 1;
-                            const float2 uj = *reinterpret_cast<const float2*>(su + j0);
-                            const float2 dj = *reinterpret_cast<const float2*>(sdt + j0);
-                            float m0 = __uint_as_float(v[jj]) * fast_exp2(fminf(ui - uj.x, 0.f)) * dj.x;
-                            float m1 = __uint_as_float(v[jj + 1]) * fast_exp2(fminf(ui - uj.y, 0.f)) * dj.y;
-                            m0 = (j0 <= r) ? m0 : 0.f;
-                            m1 = (j1 <= r) ? m1 : 0.f;
-                            m0 += (j0 == r) ? Dh : 0.f;
-                            m1 += (j1 == r) ? Dh : 0.f;
-                            o[jj >> 1] = pack_f16x2(m0, m1);
-                            hmax_abs(mx, o[jj >> 1]);
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 uj = *reinterpret_cast<const float4*>(su + q * 32 + 4 * i);
+                            const float4 dj = *reinterpret_cast<const float4*>(sdt + q * 32 + 4 * i);
+                            m[4 * i + 0] = __uint_as_float(v[4 * i + 0]) * fast_exp2(fminf(ui - uj.x, 0.f)) * dj.x;
+                            m[4 * i + 1] = __uint_as_float(v[4 * i + 1]) * fast_exp2(fminf(ui - uj.y, 0.f)) * dj.y;
+                            m[4 * i + 2] = __uint_as_float(v[4 * i + 2]) * fast_exp2(fminf(ui - uj.z, 0.f)) * dj.z;
+                            m[4 * i + 3] = __uint_as_float(v[4 * i + 3]) * fast_exp2(fminf(ui - uj.w, 0.f)) * dj.w;
                         }
                     }
+                    if (diag) {  // causal mask and the skip term D on the diagonal
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) {
+                            const int j = q * 32 + jj;
+                            m[jj] = (j <= r) ? m[jj] : 0.f;
+                            m[jj] += (j == r) ? Dh : 0.f;
+                        }
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) o[jj] = pack_f16x2(m[2 * jj], m[2 * jj + 1]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) hmax_abs4(mx, o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
                 }
                 tmem_st16(set + q * 16, o);
             }
@@ -593,9 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float2 fv = __bfloat1622float2(p2[e]);
                         x4[e] = pack_f16x2(fv.x, fv.y);
                         w4[e] = pack_f16x2(fv.x * w, fv.y * w);
-                        hmax_abs(mx, x4[e]);
-                        hmax_abs(mx, w4[e]);
                     }
+                    hmax_abs4(mx, x4[0], x4[1], x4[2], x4[3]);
+                    hmax_abs4(mx, w4[0], w4[1], w4[2], w4[3]);
                     *reinterpret_cast<uint4*>(xrow + off) = xo;
                     *reinterpret_cast<uint4*>(xsrow + off) = wo;
                 }
@@ -648,10 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             v.y = pack_f16x2(hv[ch * 8 + 2], hv[ch * 8 + 3]);
                             v.z = pack_f16x2(hv[ch * 8 + 4], hv[ch * 8 + 5]);
                             v.w = pack_f16x2(hv[ch * 8 + 6], hv[ch * 8 + 7]);
-                            hmax_abs(mx, v.x);
-                            hmax_abs(mx, v.y);
-                            hmax_abs(mx, v.z);
-                            hmax_abs(mx, v.w);
+                            hmax_abs4(mx, v.x, v.y, v.z, v.w);
                             *reinterpret_cast<uint4*>(hdst + sw128_offset(hr, ch)) = v;
                         }
                     }
