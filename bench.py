@@ -259,6 +259,19 @@ def main():
 
     total_ms = max_over_ranks(total_ms, dist, dev)
 
+    # the same steps once more with only the outer event pair (no event records between the launches,
+    # which chain through programmatic dependent launch): a check that the timed figure above is the
+    # forward callers get
+    plain = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for s0, s1 in plain:
+        s0.record(stream)
+        step()
+        s1.record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    plain_ms = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in plain)), dist, dev) / args.steps
+
     e2e = decode = decode_multi = layer = None
     if not args.forward_only:
         # ---- end to end through the public call with host buffers
@@ -307,6 +320,7 @@ def main():
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 4),
+        "ms_per_step_without_kernel_events": round(plain_ms, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -456,8 +470,10 @@ def pass_traffic(w: I.Workload, kernels: dict):
             "source": "profiles/traffic.json (ncu dram__bytes_read.sum + dram__bytes_write.sum per launch)"}
 
 
-KERNEL_SOURCES = {"chunk_cumsum": "k_cumsum.cu", "chunk_state": "k_chunk_state.cu",
-                  "state_passing": "k_state_passing.cu", "chunk_scan": "k_chunk_scan.cu", "step": "k_step.cu"}
+KERNEL_SOURCES = {"chunk_cumsum": ["k_cumsum.cu"], "chunk_state": ["k_chunk_state.cu"],
+                  "state_passing": ["k_state_passing.cu"],
+                  "chunk_scan": ["k_chunk_scan.cu", "k_chunk_scan_pair.cu", "scan_util.cuh"],
+                  "step": ["k_step.cu"]}
 
 
 def kernel_traffic(name: str, w: I.Workload):
@@ -490,7 +506,7 @@ def kernel_source_sha1(name: str) -> str:
     import hashlib
     csrc = os.path.join(ROOT, "state_space_sequence_ssd_gb300", "csrc")
     h = hashlib.sha1()
-    for fn in (KERNEL_SOURCES[name], "common.cuh", "sm100.cuh", "tmap.cuh"):
+    for fn in (*KERNEL_SOURCES[name], "common.cuh", "sm100.cuh", "tmap.cuh"):
         with open(os.path.join(csrc, fn), encoding="utf-8") as f:
             h.update(_code_only(f.read()).encode())
     return h.hexdigest()

@@ -210,11 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpTma) {
         // ------------------------------------------------------ x / dA_cumsum / dt producer
         if (lane == 0) {
-            if (a.ctl.stall) wait_bounded<true>(&bar->stall, 0, abort_flag, err, 30, wait_ns);
+            if (a.ctl.stall) wait_bounded<false>(&bar->stall, 0, abort_flag, err, 30, wait_ns);
             int nissued = 0;
             for (int k = 0; k < nsb && !*abort_flag; ++k) {
                 const int xs = k % K::NX;
-                if (!wait_bounded<true>(&bar->x_empty[xs], ((k / K::NX) & 1) ^ 1, abort_flag, err, 31, wait_ns))
+                if (!wait_bounded<false>(&bar->x_empty[xs], ((k / K::NX) & 1) ^ 1, abort_flag, err, 31, wait_ns))
                     break;
                 const int t0 = (int)(ts + (int64_t)k * 128);
                 const uint32_t cdb = (uint32_t)min((int64_t)128, rowlen - t0) * 4u;
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int which = 0; which < 2; ++which) {
                     const int i = 2 * k + which;
                     const int sl = i % K::NSLOT;
-                    ok = wait_bounded<true>(&bar->bc_empty[sl], ((i / K::NSLOT) & 1) ^ 1, abort_flag, err, 32, wait_ns);
+                    ok = wait_bounded<false>(&bar->bc_empty[sl], ((i / K::NSLOT) & 1) ^ 1, abort_flag, err, 32, wait_ns);
                     if (!ok) break;
                     mbar_arrive_expect_tx(&bar->bc_full[sl], K::SLOT);
 #pragma unroll
@@ -274,8 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // CB = C B^T (K = n, 16 per step) first, so that the mask can start while S waits for the
                 // state warpgroups; it writes the CB region, which the previous M X read (products run in
                 // issue order)
-                if (!wait_bounded<true>(&bar->bc_full[iB % K::NSLOT], (iB / K::NSLOT) & 1, abort_flag, err, 35, wait_ns) ||
-                    !wait_bounded<true>(&bar->bc_full[iC % K::NSLOT], (iC / K::NSLOT) & 1, abort_flag, err, 36, wait_ns))
+                if (!wait_bounded<false>(&bar->bc_full[iB % K::NSLOT], (iB / K::NSLOT) & 1, abort_flag, err, 35, wait_ns) ||
+                    !wait_bounded<false>(&bar->bc_full[iC % K::NSLOT], (iC / K::NSLOT) & 1, abort_flag, err, 36, wait_ns))
                     break;
                 tc_fence_after();
 #pragma unroll
@@ -285,8 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&bar->cb_full);
                 // S: hT (+)= X'^T B  -- A = both heads' X' (MN-major, heads kTile apart), B = the B tile (MN-major)
-                if (!wait_bounded<true>(&bar->xs_ready, k & 1, abort_flag, err, 33, wait_ns) ||
-                    !wait_bounded<true>(&bar->h_ready, k & 1, abort_flag, err, 34, wait_ns))
+                if (!wait_bounded<false>(&bar->xs_ready, k & 1, abort_flag, err, 33, wait_ns) ||
+                    !wait_bounded<false>(&bar->h_ready, k & 1, abort_flag, err, 34, wait_ns))
                     break;
                 tc_fence_after();
 #pragma unroll
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&bar->s_done);
                 mma_commit(&bar->bc_empty[iB % K::NSLOT]);
                 // Yst = C H^T once the epilogue has read the previous sub-block's Y and Yst
-                if (k > 0 && !wait_bounded<true>(&bar->y_free, (k - 1) & 1, abort_flag, err, 37, wait_ns)) break;
+                if (k > 0 && !wait_bounded<false>(&bar->y_free, (k - 1) & 1, abort_flag, err, 37, wait_ns)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < N / 16; ++kk) {
@@ -307,8 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&bar->bc_empty[iC % K::NSLOT]);
                 // Y_h = M_h X_h: A = M_h from TMEM (16-column half hf of block q holds M_0 then M_1 of its 16
                 // positions, 8 columns each), B = the float16 x tile of head hh (MN-major)
-                if (!wait_bounded<true>(&bar->m_ready, k & 1, abort_flag, err, 38, wait_ns) ||
-                    !wait_bounded<true>(&bar->xf_ready, k & 1, abort_flag, err, 39, wait_ns))
+                if (!wait_bounded<false>(&bar->m_ready, k & 1, abort_flag, err, 38, wait_ns) ||
+                    !wait_bounded<false>(&bar->xf_ready, k & 1, abort_flag, err, 39, wait_ns))
                     break;
                 tc_fence_after();
 #pragma unroll
@@ -344,8 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __half2 mx = __floats2half2_rn(0.f, 0.f);
         for (int k = 0; k < nsb; ++k) {
             const int ub = k % 3;
-            bool ok = wait_bounded<true>(&bar->uv_ready[ub], (k / 3) & 1, abort_flag, err, 41, wait_ns) &&
-                      wait_bounded<true>(&bar->cb_full, k & 1, abort_flag, err, 42, wait_ns);
+            bool ok = wait_bounded<false>(&bar->uv_ready[ub], (k / 3) & 1, abort_flag, err, 41, wait_ns) &&
+                      wait_bounded<false>(&bar->cb_full, k & 1, abort_flag, err, 42, wait_ns);
             ok = __all_sync(0xffffffffu, ok);  // TMEM loads/stores below are warp-collective
             if (!ok) break;
             tc_fence_after();
@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k <= nsb; ++k) {
             // (d) of the previous sub-block: once S has read X', the float16 x row for M X
             if (k >= 1) {
-                ok = ok && wait_bounded<true>(&bar->s_done, (k - 1) & 1, abort_flag, err, 51, wait_ns);
+                ok = ok && wait_bounded<false>(&bar->s_done, (k - 1) & 1, abort_flag, err, 51, wait_ns);
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok) {
                     uint8_t* xrow = xtile((k - 1) % K::NX, SX);
@@ -496,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int xs = k % K::NX;
             const int ub = k % 3;
             // (a) decays: u, dt and the column weight of head SX for token row r; u_last of both heads
-            if (k >= 3) ok = ok && wait_bounded<true>(&bar->u_free[ub], ((k / 3) - 1) & 1, abort_flag, err, 52, wait_ns);
-            ok = ok && wait_bounded<true>(&bar->x_full[xs], (k / K::NX) & 1, abort_flag, err, 53, wait_ns);
+            if (k >= 3) ok = ok && wait_bounded<false>(&bar->u_free[ub], ((k / 3) - 1) & 1, abort_flag, err, 52, wait_ns);
+            ok = ok && wait_bounded<false>(&bar->x_full[xs], (k / K::NX) & 1, abort_flag, err, 53, wait_ns);
             ok = __all_sync(0xffffffffu, ok);
             const int p0 = (int)(t0 % Q);
             const bool valid = r < nv;
@@ -532,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (b) columns of half SX of the state row r: the float16 copy for Yst = C H^T, and 2^(u_last)
             //     times them in TMEM
             if (k >= 1) {
-                ok = ok && wait_bounded<true>(&bar->ys_done, (k - 1) & 1, abort_flag, err, 54, wait_ns);
+                ok = ok && wait_bounded<false>(&bar->ys_done, (k - 1) & 1, abort_flag, err, 54, wait_ns);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
             }
@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t t0 = ts + (int64_t)k * 128;
             const int nv = (int)min((int64_t)128, te - t0);
             const int ub = k % 3;
-            ok = ok && wait_bounded<true>(&bar->y_full, k & 1, abort_flag, err, 61, wait_ns);
+            ok = ok && wait_bounded<false>(&bar->y_full, k & 1, abort_flag, err, 61, wait_ns);
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             float e[2];
