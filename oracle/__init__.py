@@ -1,4 +1,4 @@
-"""CPU oracle for the Mamba-2 SSD forward pass -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for the Mamba-2 SSD forward pass and its gradients -- TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
 ``bench.py`` may import this package.  The product path (the CUDA library and
@@ -65,8 +65,9 @@ def _load():
             lib.ssd_oracle_chunk_scan.argtypes = [p] * 7 + [i64] * 7 + [p, i64, p, i32]
             lib.ssd_oracle_dA_cumsum.argtypes = [p, p, i64, i64, i64, i64, p, p]
             lib.ssd_oracle_state_passing.argtypes = [p, p, p] + [i64] * 6 + [p, p]
+            lib.ssd_oracle_backward.argtypes = [p] * 9 + [i64] * 6 + [p, i64] + [p] * 7 + [i32]
             for f in ("ssd_oracle_forward", "ssd_oracle_forward_opts", "ssd_oracle_chunk_states", "ssd_oracle_chunk_scan",
-                      "ssd_oracle_dA_cumsum", "ssd_oracle_state_passing"):
+                      "ssd_oracle_dA_cumsum", "ssd_oracle_state_passing", "ssd_oracle_backward"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -212,3 +213,49 @@ def state_passing(S, cs, init, chunk_size):
     if r < 0:
         raise ValueError("ssd_oracle_state_passing: bad arguments")
     return states, fin
+
+
+def backward(x, dt, A, B, C, D, init, dy, dfinal=None, units=None, nthreads=0):
+    """Gradients of a scalar loss by the reverse-time recurrence (fp64).
+
+    ``dy`` (batch, L, H, P) bf16 bits is dLoss/dy, ``dfinal`` (batch, H, P, N)
+    f32 or None is dLoss/dfinal.  Per listed unit (b * H + h): ``dx`` (L, P),
+    ``dB`` and ``dC`` (L, N) -- this head's share (a group's gradient is the
+    sum over its heads) --, ``ddt`` (L,), ``dA`` and ``dD`` (this unit's share)
+    and ``dinit`` (P, N).
+    """
+    x, B, C, dy = _c(x, np.uint16), _c(B, np.uint16), _c(C, np.uint16), _c(dy, np.uint16)
+    dt, A = _c(dt, np.float32), _c(A, np.float32)
+    D, init, dfinal = _c(D, np.float32), _c(init, np.float32), _c(dfinal, np.float32)
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    if dy.shape != x.shape:
+        raise ValueError("dy must have x's shape")
+    if D is not None and D.shape != (H,):
+        raise ValueError("D must be (H,)")
+    u = _units(b, H, units)
+    out = {"dx": np.empty((u.size, L, P)), "dB": np.empty((u.size, L, N)), "dC": np.empty((u.size, L, N)),
+           "ddt": np.empty((u.size, L)), "dA": np.empty(u.size), "dD": np.empty(u.size),
+           "dinit": np.empty((u.size, P, N))}
+    r = _load().ssd_oracle_backward(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init), _ptr(dy),
+                                    _ptr(dfinal), b, L, H, P, G, N, _ptr(u), u.size,
+                                    *[_ptr(out[k]) for k in ("dx", "dB", "dC", "ddt", "dA", "dD", "dinit")], nthreads)
+    if r < 0:
+        raise ValueError("ssd_oracle_backward: bad arguments")
+    _last_threads[0] = r
+    return out
+
+
+def backward_full(x, dt, A, B, C, D, init, dy, dfinal=None, nthreads=0):
+    """``backward`` over every unit, assembled into the inputs' layouts: dx (b, L, H, P), ddt (b, L, H),
+    dB, dC (b, L, G, N) summed over each group's heads, dA, dD (H,) summed over the batch, dinit (b, H, P, N)."""
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    r = backward(x, dt, A, B, C, D, init, dy, dfinal, nthreads=nthreads)
+    hpg = H // G
+    dB = r["dB"].reshape(b, H, L, N).reshape(b, G, hpg, L, N).sum(axis=2).transpose(0, 2, 1, 3)
+    dC = r["dC"].reshape(b, H, L, N).reshape(b, G, hpg, L, N).sum(axis=2).transpose(0, 2, 1, 3)
+    return {"dx": r["dx"].reshape(b, H, L, P).transpose(0, 2, 1, 3), "ddt": r["ddt"].reshape(b, H, L).transpose(0, 2, 1),
+            "dB": np.ascontiguousarray(dB), "dC": np.ascontiguousarray(dC),
+            "dA": r["dA"].reshape(b, H).sum(axis=0), "dD": r["dD"].reshape(b, H).sum(axis=0),
+            "dinit": r["dinit"].reshape(b, H, P, N)}

@@ -152,3 +152,80 @@ def jump_formula_no_decay(x, dt, B, C, D, init):
             running = np.cumsum(outer, axis=0) + init[bi, h].T[None]
             y[bi, :, h] = np.einsum("tn,tnp->tp", C[bi, :, g], running) + D[h] * x[bi, :, h]
     return y, fin
+
+
+def backward_chunked(x, dt, A, B, C, D, init, dy, dfinal, block):
+    """Gradients by blocks of ``block`` tokens: the chunked reverse-mode algorithm, in numpy fp64.
+
+    Per (batch, head) and block (c the inclusive cumulative sum of dt*A inside the block, c_e its
+    last value, L[r, i] = exp(c_r - c_i) for r >= i, else 0; h0 the state before the block, mu the
+    gradient flowing into the state after the block from later tokens):
+        forward hop   h0_{k+1} = exp(c_e) h0_k + sum_j exp(c_e - c_j) dt_j B_j x_j^T
+        backward hop  mu_{k-1} = exp(c_e) mu_k + sum_r exp(c_r) C_r dy_r^T,  mu_last = dfinal,
+                      dinit = mu_{-1}
+        G   = (L o C B^T)^T dY + diag(exp(c_e - c)) B mu        (lam_i^T B_i, rows i)
+        dx  = diag(dt) G + D dY,   s_i = G_i . x_i
+        Wd  = L o (dY X^T) o dt_j (columns j)
+        dC  = diag(exp(c)) dY h0^T + Wd B      (this head's share)
+        dB  = diag(dt exp(c_e - c)) X mu^T + Wd^T C
+        q_t = B_t . dB_t - C_t . dC_t
+    and over the whole sequence the gradient of the step log-decay l_t = dt_t A is
+        dl_t = <dinit, init> + sum_{k<t} q_k,
+    so ddt_t = A dl_t + s_t and dA = sum_t dt_t dl_t.  Returns the layout of
+    ``oracle.backward_full``.  Independent of the C oracle (same mathematics, different route).
+    """
+    x, dt, A, B, C, D, init = _widen(x, dt, A, B, C, D, init)
+    dy = bf16_bits_to_f64(dy)
+    b, L, H, P = x.shape
+    G_, N = B.shape[2], B.shape[3]
+    hpg = H // G_
+    dfinal = np.zeros((b, H, P, N)) if dfinal is None else np.asarray(dfinal, np.float64)
+    nblk = -(-L // block)
+    out = {"dx": np.zeros((b, L, H, P)), "ddt": np.zeros((b, L, H)), "dB": np.zeros((b, L, G_, N)),
+           "dC": np.zeros((b, L, G_, N)), "dA": np.zeros(H), "dD": np.zeros(H), "dinit": np.zeros((b, H, P, N))}
+    for bb in range(b):
+        for h in range(H):
+            g = h // hpg
+            blocks = [(k * block, min(L, (k + 1) * block)) for k in range(nblk)]
+            cs = []
+            for t0, t1 in blocks:
+                cs.append(np.cumsum(dt[bb, t0:t1, h] * A[h]))
+            # forward hop: state before each block (N x P)
+            h0 = [init[bb, h].T.copy()]
+            for k, (t0, t1) in enumerate(blocks[:-1]):
+                c = cs[k]
+                w = np.exp(c[-1] - c) * dt[bb, t0:t1, h]
+                h0.append(np.exp(c[-1]) * h0[-1] + B[bb, t0:t1, g].T @ (w[:, None] * x[bb, t0:t1, h]))
+            # backward hop: gradient into each block's final state
+            mu = [None] * nblk
+            cur = dfinal[bb, h].T.copy()
+            for k in range(nblk - 1, -1, -1):
+                t0, t1 = blocks[k]
+                c = cs[k]
+                mu[k] = cur
+                cur = np.exp(c[-1]) * cur + C[bb, t0:t1, g].T @ (np.exp(c)[:, None] * dy[bb, t0:t1, h])
+            dinit = cur
+            out["dinit"][bb, h] = dinit.T
+            q = np.zeros(L)
+            for k, (t0, t1) in enumerate(blocks):
+                c = cs[k]
+                Lm = np.tril(np.exp(c[:, None] - c[None, :]))
+                Xb, Yb = x[bb, t0:t1, h], dy[bb, t0:t1, h]
+                Bb, Cb = B[bb, t0:t1, g], C[bb, t0:t1, g]
+                dtb = dt[bb, t0:t1, h]
+                ext = np.exp(c[-1] - c)
+                Gm = (Lm * (Cb @ Bb.T)).T @ Yb + ext[:, None] * (Bb @ mu[k])
+                out["dx"][bb, t0:t1, h] = dtb[:, None] * Gm + D[h] * Yb
+                s = np.sum(Gm * Xb, axis=1)
+                Wd = Lm * (Yb @ Xb.T) * dtb[None, :]
+                dC = np.exp(c)[:, None] * (Yb @ h0[k].T) + Wd @ Bb
+                dB = (dtb * ext)[:, None] * (Xb @ mu[k].T) + Wd.T @ Cb
+                out["dC"][bb, t0:t1, g] += dC
+                out["dB"][bb, t0:t1, g] += dB
+                q[t0:t1] = np.sum(Bb * dB, axis=1) - np.sum(Cb * dC, axis=1)
+                out["ddt"][bb, t0:t1, h] = s  # the direct term; the decay term is added below
+                out["dD"][h] += np.sum(Xb * Yb)
+            dl = np.sum(dinit * init[bb, h].T) + np.concatenate([[0.0], np.cumsum(q)[:-1]])
+            out["ddt"][bb, :, h] += A[h] * dl
+            out["dA"][h] += np.sum(dt[bb, :, h] * dl)
+    return out

@@ -1,5 +1,6 @@
 /*
- * ssd_oracle.c -- plain fp64 CPU oracle for the Mamba-2 SSD forward pass.
+ * ssd_oracle.c -- plain fp64 CPU oracle for the Mamba-2 SSD forward pass and
+ * its reverse mode (gradients, at the end of the file).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
  * call this file; only the tests, the smoke check and the benchmark's CPU
@@ -442,4 +443,148 @@ int ssd_oracle_state_passing(const float* S, const float* cs, const float* init,
         }
     free(hcur);
     return 0;
+}
+
+/* ------------------------------------------------------------ backward */
+
+/*
+ * Reverse mode of the recurrence (the pages describe no backward pass; this
+ * is the adjoint of the forward definition above, derived here).  For a
+ * scalar loss with dy = dLoss/dy (x's layout) and dfinal = dLoss/dfinal
+ * ((P, N) per unit, or zero), let lam_t = dLoss/dhs_t, the gradient with
+ * respect to the state after token t (N x P).  Going backward in time:
+ *
+ *     lam_{L-1} = dfinal + C_{L-1} dy_{L-1}^T
+ *     lam_t     = a_{t+1} lam_{t+1} + C_t dy_t^T,      a_t = exp(dt_t A)
+ *
+ * and, per token t (hs_{t-1} the state before token t, hs_{-1} = init):
+ *
+ *     dx_t[p]  = dt_t sum_n B_t[n] lam_t[n][p] + D dy_t[p]
+ *     dB_t[n] += dt_t sum_p lam_t[n][p] x_t[p]           (this head's share)
+ *     dC_t[n] += sum_p hs_t[n][p] dy_t[p]                 (this head's share)
+ *     ddt_t    = A a_t <lam_t, hs_{t-1}> + sum_{n,p} lam_t[n][p] B_t[n] x_t[p]
+ *     dA      += dt_t a_t <lam_t, hs_{t-1}>
+ *     dD      += sum_p x_t[p] dy_t[p]
+ *     dinit    = a_0 lam_0
+ *
+ * The states hs_t are recomputed segment by segment from checkpoints taken
+ * in a first forward sweep (a memory bound for the oracle, not part of the
+ * method).
+ */
+typedef struct {
+    inputs_t in;
+    const float* init;      /* (batch, H, P, N) or NULL */
+    const uint16_t* dy;     /* (batch, L, H, P) bf16 */
+    const float* dfinal;    /* (batch, H, P, N) or NULL */
+    const int64_t* units;
+    double *dx, *dB, *dC, *ddt, *dA, *dD, *dinit; /* per unit: (L,P) (L,N) (L,N) (L) (1) (1) (P,N) */
+} bwd_ctx_t;
+
+static void bwd_unit(void* vctx, int64_t u) {
+    bwd_ctx_t* c = (bwd_ctx_t*)vctx;
+    const dims_t* d = c->in.d;
+    const int64_t H = d->nheads, P = d->headdim, N = d->dstate, L = d->seqlen, G = d->ngroups;
+    const int64_t b = c->units[u] / H, h = c->units[u] % H, g = h / (H / G);
+    const double A = (double)c->in.A[h];
+    const double Dh = (c->in.D == NULL) ? 0.0 : (double)c->in.D[h];
+    int64_t K = 16;
+    while (K * K < L) ++K; /* checkpoint spacing about sqrt(L) */
+    const int64_t nseg = (L + K - 1) / K, NP = N * P;
+    double* ck = (double*)calloc((size_t)(nseg * NP), sizeof(double));   /* state before each segment */
+    double* seg = (double*)malloc(sizeof(double) * (size_t)((K + 1) * NP)); /* states through a segment */
+    double* lam = (double*)calloc((size_t)NP, sizeof(double));
+    double* xv = (double*)malloc(sizeof(double) * (size_t)P);
+    double* yv = (double*)malloc(sizeof(double) * (size_t)P);
+    double* bv = (double*)malloc(sizeof(double) * (size_t)N);
+    double* cv = (double*)malloc(sizeof(double) * (size_t)N);
+    /* forward sweep: checkpoints */
+    double* hs = seg;
+    memset(hs, 0, sizeof(double) * (size_t)NP);
+    if (c->init != NULL) load_state_f32(hs, c->init + (b * H + h) * P * N, P, N);
+    for (int64_t s = 0; s < nseg; ++s) {
+        const int64_t t0 = s * K, t1 = (t0 + K < L) ? t0 + K : L;
+        memcpy(ck + s * NP, hs, sizeof(double) * (size_t)NP);
+        recur_tokens(&c->in, b, h, t0, t1, hs, NULL);
+    }
+    /* backward sweep */
+    if (c->dfinal != NULL) load_state_f32(lam, c->dfinal + (b * H + h) * P * N, P, N);
+    double dA = 0.0, dD = 0.0;
+    double* dx = c->dx + u * L * P;
+    double* dB = c->dB + u * L * N;
+    double* dC = c->dC + u * L * N;
+    double* ddt = c->ddt + u * L;
+    for (int64_t s = nseg - 1; s >= 0; --s) {
+        const int64_t t0 = s * K, t1 = (t0 + K < L) ? t0 + K : L;
+        memcpy(seg, ck + s * NP, sizeof(double) * (size_t)NP);
+        for (int64_t t = t0; t < t1; ++t) { /* seg[i + 1] = state after token t0 + i */
+            memcpy(seg + (t - t0 + 1) * NP, seg + (t - t0) * NP, sizeof(double) * (size_t)NP);
+            recur_tokens(&c->in, b, h, t, t + 1, seg + (t - t0 + 1) * NP, NULL);
+        }
+        for (int64_t t = t1 - 1; t >= t0; --t) {
+            const double* hprev = seg + (t - t0) * NP;
+            const double* hcur = seg + (t - t0 + 1) * NP;
+            const double dtv = (double)c->in.dt[(b * L + t) * H + h];
+            const double a = exp(dtv * A);
+            const uint16_t* xr = c->in.x + ((b * L + t) * H + h) * P;
+            const uint16_t* dyr = c->dy + ((b * L + t) * H + h) * P;
+            const uint16_t* br = c->in.B + ((b * L + t) * G + g) * N;
+            const uint16_t* cr = c->in.C + ((b * L + t) * G + g) * N;
+            for (int64_t p = 0; p < P; ++p) { xv[p] = bf16_to_double(xr[p]); yv[p] = bf16_to_double(dyr[p]); }
+            for (int64_t n = 0; n < N; ++n) { bv[n] = bf16_to_double(br[n]); cv[n] = bf16_to_double(cr[n]); }
+            /* lam_t = (carried) + C_t dy_t^T */
+            for (int64_t n = 0; n < N; ++n)
+                for (int64_t p = 0; p < P; ++p) lam[n * P + p] += cv[n] * yv[p];
+            double xdy = 0.0;
+            for (int64_t p = 0; p < P; ++p) {
+                double acc = 0.0;
+                for (int64_t n = 0; n < N; ++n) acc += bv[n] * lam[n * P + p];
+                dx[t * P + p] = dtv * acc + Dh * yv[p];
+                xdy += xv[p] * yv[p];
+            }
+            double inner = 0.0, direct = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                double lx = 0.0, hy = 0.0;
+                for (int64_t p = 0; p < P; ++p) {
+                    lx += lam[n * P + p] * xv[p];
+                    hy += hcur[n * P + p] * yv[p];
+                    inner += lam[n * P + p] * hprev[n * P + p];
+                }
+                dB[t * N + n] = dtv * lx;
+                dC[t * N + n] = hy;
+                direct += bv[n] * lx;
+            }
+            ddt[t] = A * a * inner + direct;
+            dA += dtv * a * inner;
+            dD += xdy;
+            for (int64_t e = 0; e < NP; ++e) lam[e] *= a; /* carry to token t - 1 */
+        }
+    }
+    c->dA[u] = dA;
+    c->dD[u] = dD;
+    store_state(c->dinit + u * P * N, lam, P, N);
+    free(ck); free(seg); free(lam); free(xv); free(yv); free(bv); free(cv);
+}
+
+/*
+ * ssd_oracle_backward: per listed (batch, head) unit, the gradients of a
+ * scalar loss with respect to x (dx, (L, P)), this head's share of dB and dC
+ * ((L, N); a group's gradient is the sum over its heads), dt (ddt, (L)), A
+ * and D (this unit's share, one value each) and init (dinit, (P, N)), given
+ * dy (x's layout, bf16) and dfinal ((batch, H, P, N) f32, or NULL = 0).
+ * Returns the number of threads used, or -1 on bad arguments.
+ */
+int ssd_oracle_backward(const uint16_t* x, const float* dt, const float* A, const uint16_t* B,
+                        const uint16_t* C, const float* D, const float* init, const uint16_t* dy,
+                        const float* dfinal, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                        int64_t ngroups, int64_t dstate, const int64_t* units, int64_t nunits,
+                        double* dx, double* dB, double* dC, double* ddt, double* dA, double* dD,
+                        double* dinit, int nthreads) {
+    if (!x || !dt || !A || !B || !C || !dy || !units || !dx || !dB || !dC || !ddt || !dA || !dD || !dinit)
+        return -1;
+    if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0 ||
+        nheads % ngroups != 0 || nunits <= 0)
+        return -1;
+    dims_t d = {batch, seqlen, nheads, headdim, ngroups, dstate, seqlen};
+    bwd_ctx_t ctx = {{&d, x, B, C, dt, A, D, NULL}, init, dy, dfinal, units, dx, dB, dC, ddt, dA, dD, dinit};
+    return run_units(bwd_unit, &ctx, nunits, nthreads);
 }

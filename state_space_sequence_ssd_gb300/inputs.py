@@ -94,6 +94,19 @@ def make_layer_options(w: Workload, seed: int = 0) -> dict:
     return {"dt_raw": dt_raw, "dt_bias": dt_bias, "D_hp": D_hp, "z": z, "dt_limit": (0.001, 0.1)}
 
 
+def make_grad_inputs(w: Workload, seed: int = 0, dfinal: bool = True) -> dict:
+    """Seeded output gradients for workload ``w`` (CPU torch tensors), the inputs of the backward pass:
+        dy     ~ N(0, 1) rounded to bf16        (batch, L, H, P): dLoss/dy
+        dfinal ~ N(0, 1)                        float32 (batch, H, P, N): dLoss/dfinal (None if not asked for)
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(20_000 + seed)
+    b, L, H, P, N = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate
+    dy = torch.randn((b, L, H, P), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    df = torch.randn((b, H, P, N), generator=g, dtype=torch.float32) if dfinal else None
+    return {"dy": dy, "dfinal": df}
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """bfloat16 torch tensor -> numpy uint16 bit patterns (no copy of values' meaning)."""
     assert t.dtype == torch.bfloat16
