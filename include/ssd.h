@@ -252,6 +252,55 @@ SSD_API int ssd_forward_noalloc(const void* x, const float* dt, const float* A, 
                         int chunk_size, void* y, float* final_state, cudaStream_t stream);
 
 /*
+ * ssd_backward -- gradients of a scalar loss through ssd_forward, given
+ * dLoss/dy and dLoss/dfinal_state.  The pages describe no backward pass (they
+ * only note that training speed depends on one); this is the reverse mode of
+ * the recurrence ssd_forward computes, derived from it.  Per head h (group g),
+ * with lam_t = dLoss/dstate after token t:
+ *     lam_{L-1} = dfinal + C_{L-1} dy_{L-1}^T,   lam_t = exp(dt_{t+1} A) lam_{t+1} + C_t dy_t^T
+ *     dx_t  = dt_t lam_t^T B_t + D dy_t
+ *     dB_t  = sum over the group's heads of dt_t lam_t x_t
+ *     dC_t  = sum over the group's heads of state_t dy_t
+ *     ddt_t = A exp(dt_t A) <lam_t, state_{t-1}> + <lam_t, B_t x_t^T>
+ *     dA    = sum over batch and tokens of dt_t exp(dt_t A) <lam_t, state_{t-1}>
+ *     dD    = sum over batch, tokens and channels of x dy
+ *     dinit = exp(dt_0 A) lam_0
+ * computed in the forward's chunked form (blocks of 128 tokens, whatever
+ * chunk_size is: the result does not depend on the chunking): a forward hop
+ * for the state before every block, a reverse hop for the gradient flowing
+ * into every block's end, then per (block, group) one pass over the group's
+ * heads on tcgen05 tensor cores (every sum of the dt gradient kept inside a
+ * block), and a fixed-order reduction of the per-block parts of dA and dD.
+ * Operands of the products are float16 (as in ssd_forward), accumulation
+ * float32.
+ *
+ * Inputs: as ssd_forward (x, B, C bf16; dt, A, D, init_state f32; D and
+ * init_state nullable), dy (batch, seqlen, nheads, headdim) bf16, dfinal
+ * (batch, nheads, headdim, dstate) f32 or NULL (= 0).  Outputs, all
+ * caller-owned device memory, fully written:
+ *     dx    (batch, seqlen, nheads, headdim)  bf16
+ *     ddt   (batch, seqlen, nheads)           f32
+ *     dA    (nheads)                          f32
+ *     dB,dC (batch, seqlen, ngroups, dstate)  f32
+ *     dD    (nheads) f32, or NULL (not computed)
+ *     dinit (batch, nheads, headdim, dstate)  f32, or NULL (not computed)
+ * x, B, C, dy, dx, dB, dC, init_state, dfinal and dinit 16-byte aligned; the
+ * other pointers 4-byte aligned.  Supported: headdim 64, dstate 64 or 128,
+ * otherwise the shape limits of ssd_forward (SSD_ERR_UNSUPPORTED).  The
+ * workspace (about 2 x batch x nheads x headdim x dstate x 4 bytes per 128
+ * tokens, plus float16 copies of B and C) is allocated stream-ordered from
+ * the library's pool.  Deterministic: no atomics; dB and dC are summed over
+ * a group's heads in a fixed order.  Errors: SSD_ERR_INVALID_ARG,
+ * SSD_ERR_UNSUPPORTED, SSD_ERR_NO_MEMORY, SSD_ERR_CUDA; SSD_ERR_TIMEOUT and
+ * SSD_ERR_RANGE through ssd_get_device_error, as for ssd_forward.
+ */
+SSD_API int ssd_backward(const void* x, const float* dt, const float* A, const void* B, const void* C,
+                         const float* D, const float* init_state, const void* dy, const float* dfinal,
+                         int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                         int chunk_size, void* dx, float* ddt, float* dA, float* dB, float* dC, float* dD,
+                         float* dinit, cudaStream_t stream);
+
+/*
  * ssd_forward_plan -- how ssd_forward and ssd_forward_noalloc split a
  * workload of these sizes, without touching device memory or launching
  * anything (a host-side query; no counterpart in the pages):

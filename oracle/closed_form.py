@@ -168,10 +168,12 @@ def backward_chunked(x, dt, A, B, C, D, init, dy, dfinal, block):
         Wd  = L o (dY X^T) o dt_j (columns j)
         dC  = diag(exp(c)) dY h0^T + Wd B      (this head's share)
         dB  = diag(dt exp(c_e - c)) X mu^T + Wd^T C
-        q_t = B_t . dB_t - C_t . dC_t
-    and over the whole sequence the gradient of the step log-decay l_t = dt_t A is
-        dl_t = <dinit, init> + sum_{k<t} q_k,
-    so ddt_t = A dl_t + s_t and dA = sum_t dt_t dl_t.  Returns the layout of
+    and the gradient of the step log-decay l_t = dt_t A, split at the block's ends so that every sum
+    stays inside the block (h0 reaching forward, mu reaching back, pairs of tokens inside the block):
+        dl_t = exp(c_e) <mu, h0> + sum_{j<t} v_j + sum_{r>=t} (rho1_r + rho2_r - sigma_r),
+        v_j = dt_j exp(c_e - c_j) x_j . (B mu)_j,   rho2_r = exp(c_r) dy_r . (C h0)_r,
+        rho1_r = sum_j (Wd o C B^T)[r][j],          sigma_r = dt_r x_r . ((L o C B^T)^T dY)_r,
+    so ddt_t = A dl_t + G_t . x_t and dA = sum_t dt_t dl_t.  Returns the layout of
     ``oracle.backward_full``.  Independent of the C oracle (same mathematics, different route).
     """
     x, dt, A, B, C, D, init = _widen(x, dt, A, B, C, D, init)
@@ -206,7 +208,6 @@ def backward_chunked(x, dt, A, B, C, D, init, dy, dfinal, block):
                 cur = np.exp(c[-1]) * cur + C[bb, t0:t1, g].T @ (np.exp(c)[:, None] * dy[bb, t0:t1, h])
             dinit = cur
             out["dinit"][bb, h] = dinit.T
-            q = np.zeros(L)
             for k, (t0, t1) in enumerate(blocks):
                 c = cs[k]
                 Lm = np.tril(np.exp(c[:, None] - c[None, :]))
@@ -214,18 +215,22 @@ def backward_chunked(x, dt, A, B, C, D, init, dy, dfinal, block):
                 Bb, Cb = B[bb, t0:t1, g], C[bb, t0:t1, g]
                 dtb = dt[bb, t0:t1, h]
                 ext = np.exp(c[-1] - c)
-                Gm = (Lm * (Cb @ Bb.T)).T @ Yb + ext[:, None] * (Bb @ mu[k])
+                CB = Cb @ Bb.T
+                Gin = (Lm * CB).T @ Yb
+                Gmu = Bb @ mu[k]
+                Gm = Gin + ext[:, None] * Gmu
                 out["dx"][bb, t0:t1, h] = dtb[:, None] * Gm + D[h] * Yb
-                s = np.sum(Gm * Xb, axis=1)
                 Wd = Lm * (Yb @ Xb.T) * dtb[None, :]
-                dC = np.exp(c)[:, None] * (Yb @ h0[k].T) + Wd @ Bb
-                dB = (dtb * ext)[:, None] * (Xb @ mu[k].T) + Wd.T @ Cb
-                out["dC"][bb, t0:t1, g] += dC
-                out["dB"][bb, t0:t1, g] += dB
-                q[t0:t1] = np.sum(Bb * dB, axis=1) - np.sum(Cb * dC, axis=1)
-                out["ddt"][bb, t0:t1, h] = s  # the direct term; the decay term is added below
+                out["dC"][bb, t0:t1, g] += np.exp(c)[:, None] * (Yb @ h0[k].T) + Wd @ Bb
+                out["dB"][bb, t0:t1, g] += (dtb * ext)[:, None] * (Xb @ mu[k].T) + Wd.T @ Cb
+                v = dtb * ext * np.sum(Xb * Gmu, axis=1)
+                rho1 = np.sum(Wd * CB, axis=1)
+                rho2 = np.exp(c) * np.sum(Yb * (Cb @ h0[k]), axis=1)
+                sigma = dtb * np.sum(Xb * Gin, axis=1)
+                w = rho1 + rho2 - sigma
+                dl = (np.exp(c[-1]) * np.sum(mu[k] * h0[k]) + np.concatenate([[0.0], np.cumsum(v)[:-1]])
+                      + np.cumsum(w[::-1])[::-1])
+                out["ddt"][bb, t0:t1, h] = A[h] * dl + np.sum(Gm * Xb, axis=1)
+                out["dA"][h] += np.sum(dtb * dl)
                 out["dD"][h] += np.sum(Xb * Yb)
-            dl = np.sum(dinit * init[bb, h].T) + np.concatenate([[0.0], np.cumsum(q)[:-1]])
-            out["ddt"][bb, :, h] += A[h] * dl
-            out["dA"][h] += np.sum(dt[bb, :, h] * dl)
     return out

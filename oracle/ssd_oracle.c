@@ -478,6 +478,12 @@ typedef struct {
     const float* dfinal;    /* (batch, H, P, N) or NULL */
     const int64_t* units;
     double *dx, *dB, *dC, *ddt, *dA, *dD, *dinit; /* per unit: (L,P) (L,N) (L,N) (L) (1) (1) (P,N) */
+    double* ddt_direct; /* per unit (L) or NULL: the second term of ddt alone, <lam_t, B_t x_t^T> */
+    /* Scales, each NULL or per unit in the layout of its gradient: the sum of the magnitudes of the
+     * products the gradient adds up (dx: dt sum_n |B lam| + |D dy|; dB: dt sum_p |lam x|; dC:
+     * sum_p |hs dy|; ddt: |A| a sum |lam hs_prev| + sum |lam B x|; dA: sum_t dt a sum |lam hs_prev|;
+     * dD: sum_t sum_p |x dy|). */
+    double *dx_s, *dB_s, *dC_s, *ddt_s, *dA_s, *dD_s;
 } bwd_ctx_t;
 
 static void bwd_unit(void* vctx, int64_t u) {
@@ -508,7 +514,7 @@ static void bwd_unit(void* vctx, int64_t u) {
     }
     /* backward sweep */
     if (c->dfinal != NULL) load_state_f32(lam, c->dfinal + (b * H + h) * P * N, P, N);
-    double dA = 0.0, dD = 0.0;
+    double dA = 0.0, dD = 0.0, dA_abs = 0.0, dD_abs = 0.0;
     double* dx = c->dx + u * L * P;
     double* dB = c->dB + u * L * N;
     double* dC = c->dC + u * L * N;
@@ -534,33 +540,50 @@ static void bwd_unit(void* vctx, int64_t u) {
             /* lam_t = (carried) + C_t dy_t^T */
             for (int64_t n = 0; n < N; ++n)
                 for (int64_t p = 0; p < P; ++p) lam[n * P + p] += cv[n] * yv[p];
-            double xdy = 0.0;
+            double xdy = 0.0, xdy_abs = 0.0;
             for (int64_t p = 0; p < P; ++p) {
-                double acc = 0.0;
-                for (int64_t n = 0; n < N; ++n) acc += bv[n] * lam[n * P + p];
+                double acc = 0.0, acc_abs = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    acc += bv[n] * lam[n * P + p];
+                    acc_abs += fabs(bv[n] * lam[n * P + p]);
+                }
                 dx[t * P + p] = dtv * acc + Dh * yv[p];
+                if (c->dx_s != NULL) c->dx_s[(u * L + t) * P + p] = dtv * acc_abs + fabs(Dh * yv[p]);
                 xdy += xv[p] * yv[p];
+                xdy_abs += fabs(xv[p] * yv[p]);
             }
-            double inner = 0.0, direct = 0.0;
+            double inner = 0.0, direct = 0.0, inner_abs = 0.0, direct_abs = 0.0;
             for (int64_t n = 0; n < N; ++n) {
-                double lx = 0.0, hy = 0.0;
+                double lx = 0.0, hy = 0.0, lx_abs = 0.0, hy_abs = 0.0;
                 for (int64_t p = 0; p < P; ++p) {
                     lx += lam[n * P + p] * xv[p];
                     hy += hcur[n * P + p] * yv[p];
                     inner += lam[n * P + p] * hprev[n * P + p];
+                    lx_abs += fabs(lam[n * P + p] * xv[p]);
+                    hy_abs += fabs(hcur[n * P + p] * yv[p]);
+                    inner_abs += fabs(lam[n * P + p] * hprev[n * P + p]);
                 }
                 dB[t * N + n] = dtv * lx;
                 dC[t * N + n] = hy;
+                if (c->dB_s != NULL) c->dB_s[(u * L + t) * N + n] = dtv * lx_abs;
+                if (c->dC_s != NULL) c->dC_s[(u * L + t) * N + n] = hy_abs;
                 direct += bv[n] * lx;
+                direct_abs += fabs(bv[n]) * lx_abs;
             }
             ddt[t] = A * a * inner + direct;
+            if (c->ddt_direct != NULL) c->ddt_direct[u * L + t] = direct;
+            if (c->ddt_s != NULL) c->ddt_s[u * L + t] = fabs(A) * a * inner_abs + direct_abs;
             dA += dtv * a * inner;
+            dA_abs += dtv * a * inner_abs;
             dD += xdy;
+            dD_abs += xdy_abs;
             for (int64_t e = 0; e < NP; ++e) lam[e] *= a; /* carry to token t - 1 */
         }
     }
     c->dA[u] = dA;
     c->dD[u] = dD;
+    if (c->dA_s != NULL) c->dA_s[u] = dA_abs;
+    if (c->dD_s != NULL) c->dD_s[u] = dD_abs;
     store_state(c->dinit + u * P * N, lam, P, N);
     free(ck); free(seg); free(lam); free(xv); free(yv); free(bv); free(cv);
 }
@@ -571,6 +594,10 @@ static void bwd_unit(void* vctx, int64_t u) {
  * ((L, N); a group's gradient is the sum over its heads), dt (ddt, (L)), A
  * and D (this unit's share, one value each) and init (dinit, (P, N)), given
  * dy (x's layout, bf16) and dfinal ((batch, H, P, N) f32, or NULL = 0).
+ * ddt_direct (per unit (L), or NULL) receives ddt's second term alone; each
+ * of dx_s, dB_s, dC_s, ddt_s, dA_s, dD_s (NULL or the layout of its gradient)
+ * receives the sum of the magnitudes of the products that gradient adds up
+ * (the scale of its rounding error in any method that rounds the factors).
  * Returns the number of threads used, or -1 on bad arguments.
  */
 int ssd_oracle_backward(const uint16_t* x, const float* dt, const float* A, const uint16_t* B,
@@ -578,13 +605,15 @@ int ssd_oracle_backward(const uint16_t* x, const float* dt, const float* A, cons
                         const float* dfinal, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
                         int64_t ngroups, int64_t dstate, const int64_t* units, int64_t nunits,
                         double* dx, double* dB, double* dC, double* ddt, double* dA, double* dD,
-                        double* dinit, int nthreads) {
+                        double* dinit, double* ddt_direct, double* dx_s, double* dB_s, double* dC_s,
+                        double* ddt_s, double* dA_s, double* dD_s, int nthreads) {
     if (!x || !dt || !A || !B || !C || !dy || !units || !dx || !dB || !dC || !ddt || !dA || !dD || !dinit)
         return -1;
     if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0 ||
         nheads % ngroups != 0 || nunits <= 0)
         return -1;
     dims_t d = {batch, seqlen, nheads, headdim, ngroups, dstate, seqlen};
-    bwd_ctx_t ctx = {{&d, x, B, C, dt, A, D, NULL}, init, dy, dfinal, units, dx, dB, dC, ddt, dA, dD, dinit};
+    bwd_ctx_t ctx = {{&d, x, B, C, dt, A, D, NULL}, init, dy, dfinal, units, dx, dB, dC, ddt, dA, dD, dinit,
+                     ddt_direct, dx_s, dB_s, dC_s, ddt_s, dA_s, dD_s};
     return run_units(bwd_unit, &ctx, nunits, nthreads);
 }

@@ -19,7 +19,7 @@ from . import _ffi
 
 __all__ = ["ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan", "ssd_forward",
            "ssd_forward_noalloc", "ssd_forward_heads", "ssd_partition_heads", "ssd_forward_plan", "ssd_step",
-           "ssd_step_multi", "ssd_forward_ex", "ssd_step_ex", "ssd_get_device_error", "SSDError", "library_path"]
+           "ssd_step_multi", "ssd_forward_ex", "ssd_step_ex", "ssd_backward", "ssd_get_device_error", "SSDError", "library_path"]
 
 SSDError = _ffi.SSDError
 library_path = _ffi.LIB_PATH
@@ -160,6 +160,39 @@ def ssd_forward(x, dt, A, B, C, D, init_state, chunk_size, y=None, final_state=N
         _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
         b, L, H, P, G, N, chunk_size, _ptr(y), _ptr(final_state), _stream(stream)))
     return y, final_state
+
+
+def ssd_backward(x, dt, A, B, C, D, init_state, dy, dfinal=None, chunk_size=256, want_dD=True, want_dinit=True,
+                 stream=None):
+    """Gradients through ssd_forward given dy (x's layout, bf16) and dfinal ((batch, H, P, N) f32 or None).
+
+    Returns a dict: dx (batch, L, H, P) bf16, ddt (batch, L, H) f32, dA (H,) f32, dB and dC
+    (batch, L, G, N) f32 (summed over each group's heads), dD (H,) f32 or None, dinit
+    (batch, H, P, N) f32 or None."""
+    torch = _torch()
+    _need(x, "x", torch.bfloat16, 4)
+    _need(dt, "dt", torch.float32, 3)
+    _need(A, "A", torch.float32, 1)
+    _need(B, "B", torch.bfloat16, 4)
+    _need(C, "C", torch.bfloat16, 4)
+    _opt(D, "D", torch.float32, 1)
+    _opt(init_state, "init_state", torch.float32, 4)
+    _need(dy, "dy", torch.bfloat16, 4)
+    _opt(dfinal, "dfinal", torch.float32, 4)
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev = x.device
+    out = {"dx": torch.empty_like(x), "ddt": torch.empty((b, L, H), device=dev, dtype=torch.float32),
+           "dA": torch.empty((H,), device=dev, dtype=torch.float32),
+           "dB": torch.empty((b, L, G, N), device=dev, dtype=torch.float32),
+           "dC": torch.empty((b, L, G, N), device=dev, dtype=torch.float32),
+           "dD": torch.empty((H,), device=dev, dtype=torch.float32) if want_dD else None,
+           "dinit": torch.empty((b, H, P, N), device=dev, dtype=torch.float32) if want_dinit else None}
+    _ffi.check("ssd_backward", _ffi.lib().ssd_backward(
+        _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state), _ptr(dy), _ptr(dfinal),
+        b, L, H, P, G, N, chunk_size, _ptr(out["dx"]), _ptr(out["ddt"]), _ptr(out["dA"]), _ptr(out["dB"]),
+        _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dinit"]), _stream(stream)))
+    return out
 
 
 def ssd_forward_heads(x, dt, A, B, C, D, init_state, chunk_size, head_begin, head_count, y=None, final_state=None,

@@ -39,6 +39,7 @@ SIGNATURES = {
     "ssd_forward_plan": (_i, [_i] * 7 + [_p, _p, _p]),
     "ssd_forward_ex": (_i, [_p] * 7 + [_i] * 7 + [_p, _p, _p, _p]),
     "ssd_step_ex": (_i, [_p] * 7 + [_i] * 5 + [_p, _p, _p]),
+    "ssd_backward": (_i, [_p] * 9 + [_i] * 7 + [_p] * 8),
     "ssd_get_device_error": (_i, []),
     "ssd_debug_set_wait_limit_ns": (_i, [ctypes.c_ulonglong]),
     "ssd_debug_stall": (_i, [_i]),

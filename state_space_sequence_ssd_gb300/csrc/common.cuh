@@ -113,7 +113,9 @@ enum KernelKind {
     kKindChunkScan = 3,
     kKindConvert = 4,
     kKindStep = 5,
-    kNumKinds = 6
+    kKindBwdChunk = 6,
+    kKindBwdReduce = 7,
+    kNumKinds = 8
 };
 
 // Sets a kernel's dynamic shared-memory limit once per (kernel, device).
@@ -143,9 +145,13 @@ int launch_chunk_state_span(const __nv_bfloat16* x, const __half* B, const float
                             cudaStream_t s);
 int launch_state_passing(const float* S, const float* cs, const float* init, const Dims& d,
                          float* states, float* final_state, cudaStream_t s);
+// rev = 1: the steps run from the last to the first (the backward pass's hop, k_state_passing.cu)
 int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_step, int64_t dec_row,
                                const float* init, const Dims& d, int nsteps, float* states, float* final_state,
-                               cudaStream_t s);
+                               cudaStream_t s, int rev = 0);
+// reverse-time chunk states for the backward pass (one-chunk spans): Z[c] = sum_t C_t 2^(cs(t)) dy_t^T
+int launch_chunk_state_rev(const __nv_bfloat16* dy, const __half* C16, const float* dtt, const float* cs, const Dims& d,
+                           float* Z, const Ctl& ctl, cudaStream_t s);
 // span_states holds one state per span of `span_chunks` chunks; chunk_scan walks spans of
 // span_chunks * state_step chunks, each starting from every state_step-th of those states.
 int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C,
@@ -160,6 +166,20 @@ bool chunk_scan_pair_supported(const Dims& d, const OutOpts& oo);
 int launch_chunk_scan_pair(const __nv_bfloat16* x, const __half* B, const __half* C, const float* dtt,
                            const float* cs, const float* D, const float* span_states, int span_chunks, const Dims& d,
                            __nv_bfloat16* y, const Ctl& ctl, cudaStream_t s, int state_step);
+
+// Backward pass (k_bwd.cu), over blocks of kBwdBlock tokens (d.chunk_size == kBwdBlock, d.nchunks blocks):
+// per (block, group, batch) the gradients of every head of the group from the block-start states h0
+// and the block-end gradients mu (both (b, nblk, H, P, N) f32): dx, ddt, this block's rows of dB and
+// dC (summed over the group's heads), and per (b, h, block) the partial sums of dt dl (for dA) and of
+// x . dy (for dD), (b, H, nblk) f32 each.
+constexpr int kBwdBlock = 128;
+bool bwd_supported(const Dims& d);
+int launch_bwd_chunk(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __half* B16, const __half* C16,
+                     const float* cs, const float* dtt, const float* A, const float* D, const float* h0, const float* mu,
+                     const Dims& d, __nv_bfloat16* dx, float* ddt, float* dB, float* dC, float* dap, float* xdy,
+                     const Ctl& ctl, cudaStream_t s);
+// dA[h] and dD[h] (dD may be null): the partial sums over batch and blocks, in a fixed order
+int launch_bwd_reduce(const float* dap, const float* xdy, const Dims& d, float* dA, float* dD, cudaStream_t s);
 
 // one recurrent step for every (batch, head): state updated in place, y for the token (k_step.cu)
 int launch_step(const __nv_bfloat16* x, const float* dt, const float* A, const __nv_bfloat16* B,

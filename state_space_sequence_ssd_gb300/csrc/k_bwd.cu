@@ -1,0 +1,603 @@
+// k_bwd.cu -- backward pass of the chunked scan on tcgen05 tensor cores: the
+// gradients of a scalar loss with respect to x, dt, A, B, C, D and the initial
+// state, given dLoss/dy and dLoss/dfinal.
+//
+// The pages describe no backward pass; they only note that training speed
+// depends on one.  This is the reverse mode of the recurrence the forward
+// computes, in the forward's chunked shape (disconfirmai.com page "Jane Street
+// ML Engineers Map Mamba-2 Recurrent State Computation to Tensor Cores with
+// cuTile", three-kernel and jump-formula paragraphs; devotd.net page on the
+// Mamba-2 cuTile forward kernels, section 2).  Per (batch, head), over blocks
+// of T = 128 tokens, with c the inclusive cumulative log2 decay inside the
+// block, c_e its last value, L[r][i] = 2^(c_r - c_i) for r >= i (else 0), h0
+// the state before the block and mu the gradient flowing into the state after
+// the block from later tokens (h0 and mu come from the forward and the reverse
+// hops over blocks):
+//
+//   G   = (L o C B^T)^T dY + diag(2^(c_e - c)) B mu        row i: lam_i^T B_i
+//   dx  = diag(dt) G + D dY
+//   Wd  = L o (dY X^T) o dt_j                               (dt on the columns)
+//   dC += diag(2^c) dY h0^T + Wd B                          summed over the group's heads
+//   dB += diag(dt 2^(c_e - c)) X mu^T + Wd^T C
+//   ddt = A dl + s,   s_t = x_t . G_t
+//
+// where dl_t = exp(dt_t A) <lam_t, state_{t-1}> is the gradient of the step log-decay dt_t A.
+// Splitting lam_t and state_{t-1} at the block's ends keeps every sum inside the block:
+//   dl_t = 2^(c_e) <mu, h0> + sum_{j<t} v_j + sum_{r>=t} (rho1_r + rho2_r - sigma_r)
+//   v_j     = dt_j 2^(c_e - c_j) x_j . (B mu)_j          (mu reaching back to token j)
+//   rho2_r  = 2^(c_r) dy_r . (C h0)_r                    (h0 reaching token r: a fourth product C h0)
+//   rho1_r  = sum_j Wd[r][j] (C_r . B_j)                 (pairs inside the block, rows of Wd o C B^T)
+//   sigma_r = dt_r x_r . ((L o C B^T)^T dY)_r            (the same pairs by columns)
+// (a prefix over the whole sequence of the per-token differences would telescope to the same value
+// but accumulate the operands' rounding over every earlier token).  dA = sum of dt_t dl_t over
+// tokens and batch, dD = sum of x . dy: per (b, h, block) partial sums, added up in a fixed order
+// by bwd_reduce_kernel.
+//
+// One CTA per (block, group, batch) walks every head of the group, so dB and dC accumulate in
+// TMEM across the heads and are written once, without atomics and in a fixed order.  Per head
+// the phases run one after another: loads (x and dy to float16 tiles, the two scaled tiles
+// 2^c dy and dt 2^(c_e - c) x, h0 and mu to float16), the products C B^T and dY X^T, the mask
+// (one thread per row and column half: M' = L o C B^T and Wd to float16 tiles), the products
+// G, B mu, C h0 and the dC / dB accumulations, and the epilogue.  Operands are float16 (the
+// inputs exactly, the derived tiles rounded once), accumulation float32.
+#include "common.cuh"
+#include "scan_util.cuh"
+#include "sm100.cuh"
+
+namespace ssd {
+namespace {
+
+using namespace sm100;
+
+constexpr int T = kBwdBlock;     // tokens per block = the products' M
+constexpr int kP = 64;           // headdim
+constexpr int kThreads = 256;    // two warpgroups: warp w owns TMEM lanes 32 (w % 4) .. +31, column half w / 4
+constexpr int kPanel = T * 128;  // one 64-column float16 panel of a T-row tile (16 KB)
+constexpr int kPanelP = kP * 128;  // one 64-column float16 panel of a P-row tile (8 KB)
+
+template <int N>
+struct BwdCfg {
+    static constexpr int NP = N / 64;                    // 64-column panels of a B / C / state tile
+    static constexpr int OFF_C = 0;                      // C  [t][n]
+    static constexpr int OFF_B = OFF_C + NP * kPanel;    // B  [t][n]
+    static constexpr int OFF_X = OFF_B + NP * kPanel;    // x  [t][p]
+    static constexpr int OFF_DY = OFF_X + kPanel;        // dy [t][p]
+    static constexpr int OFF_DYS = OFF_DY + kPanel;      // 2^c dy
+    static constexpr int OFF_XS = OFF_DYS + kPanel;      // dt 2^(c_e - c) x
+    static constexpr int OFF_H0 = OFF_XS + kPanel;       // h0 [p][n]
+    static constexpr int OFF_MU = OFF_H0 + NP * kPanelP; // mu [p][n]
+    static constexpr int OFF_M = OFF_MU + NP * kPanelP;  // M' [r][i]; the epilogue's reductions after the products
+    static constexpr int OFF_W = OFF_M + 2 * kPanel;     // Wd [r][j]
+    static constexpr int OFF_CS = OFF_W + 2 * kPanel;    // cs[T], dt[T]
+    static constexpr int OFF_BAR = OFF_CS + 2 * T * 4;   // two mbarriers, TMEM base, abort flag, warp sums
+    static constexpr int SMEM = OFF_BAR + 128 + 1024;    // + slack to align the base to 1024 bytes
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+// TMEM columns (all 512): C B^T and dY X^T while the mask reads them, then G, B mu and C h0 in
+// their place; the dC and dB accumulators over the group's heads
+constexpr uint32_t T_CB = 0, T_DX = 128, T_G = 0, T_GMU = 64, T_YS = 128, T_DC = 256, T_DB = 384;
+
+constexpr uint32_t kIdescTT = idesc_fp16(128, 128, false, false);  // C B^T, dY X^T: both K-major
+constexpr uint32_t kIdescG = idesc_fp16(128, 64, true, true);      // M'^T dY: both MN-major
+constexpr uint32_t kIdescP = idesc_fp16(128, 64, false, false);    // B mu, C h0: both K-major over n
+
+struct BwdArgs {
+    const __nv_bfloat16 *x, *dy;
+    const __half *B16, *C16;
+    const float *cs, *dtt, *D, *h0, *mu;
+    const float* A;
+    __nv_bfloat16* dx;
+    float *ddt, *dB, *dC, *dap, *xdy;  // dap, xdy: per (b, h, block) partial sums of dt dl and x . dy
+    Dims d;
+    Ctl ctl;
+};
+
+// bfloat16 pair (low, high) -> float2
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+
+template <int N>
+__global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
+    using K = BwdCfg<N>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* scs = reinterpret_cast<float*>(smem + K::OFF_CS);
+    float* sdt = scs + T;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
+    uint64_t* stall_bar = bar + 1;  // never completed: the test hook's wait runs out on it
+    uint32_t* tmem_sh = reinterpret_cast<uint32_t*>(bar + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 3);
+    float* wsum = reinterpret_cast<float*>(bar + 4);  // per-warp partial sums of <mu, h0>
+
+    const Dims& d = a.d;
+    const int blk = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int H = d.nheads, G = d.ngroups, hpg = H / G;
+    const int64_t L = d.seqlen;
+    const int64_t t0 = (int64_t)blk * T;
+    const int64_t rowlen = (int64_t)d.nchunks * T;  // cs / dt / s / q row length per (b, h)
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qw = warp & 3, hf = warp >> 2;         // TMEM lane quarter, column half
+    const int r = 32 * qw + lane;                    // this thread's row in the mask and the epilogue
+    const uint32_t lane_base = (uint32_t)(32 * qw) << 16;
+    int* const err = a.ctl.err;
+    const uint64_t wait_ns = a.ctl.wait_ns;
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_init(stall_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_sh, 512);
+        tmem_relinquish();
+    }
+    // the block's B and C rows (float16 copies), once for all heads of the group
+    for (int c = tid; c < T * N / 8; c += kThreads) {
+        const int row = c / (N / 8), cc = c % (N / 8);
+        const int64_t tok = t0 + row;
+        uint4 vb = make_uint4(0, 0, 0, 0), vc = make_uint4(0, 0, 0, 0);
+        if (tok < L) {
+            const int64_t o = ((b * L + tok) * G + g) * (int64_t)N + cc * 8;
+            vb = __ldg(reinterpret_cast<const uint4*>(a.B16 + o));
+            vc = __ldg(reinterpret_cast<const uint4*>(a.C16 + o));
+        }
+        const uint32_t so = (cc >> 3) * kPanel + sw128_offset(row, cc & 7);
+        *reinterpret_cast<uint4*>(smem + K::OFF_B + so) = vb;
+        *reinterpret_cast<uint4*>(smem + K::OFF_C + so) = vc;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *tmem_sh;
+    const uint32_t sC = smem_u32(smem + K::OFF_C), sB = smem_u32(smem + K::OFF_B);
+    const uint32_t sX = smem_u32(smem + K::OFF_X), sDY = smem_u32(smem + K::OFF_DY);
+    const uint32_t sDYS = smem_u32(smem + K::OFF_DYS), sXS = smem_u32(smem + K::OFF_XS);
+    const uint32_t sH0 = smem_u32(smem + K::OFF_H0), sMU = smem_u32(smem + K::OFF_MU);
+    const uint32_t sM = smem_u32(smem + K::OFF_M), sW = smem_u32(smem + K::OFF_W);
+    constexpr uint32_t kIdescN = idesc_fp16(128, N, false, true);  // dY' h0^T, Wd B, X' mu^T
+    constexpr uint32_t kIdescNT = idesc_fp16(128, N, true, true);  // Wd^T C
+
+    bool ok = true;
+    if (a.ctl.stall && tid == 0) ok = mbar_wait_bounded(stall_bar, 0, abort_flag, err, 60, wait_ns);
+    ok = __syncthreads_and(ok);
+    uint32_t phase = 0;
+    bool pending = false;  // a commit of `bar` issued and not yet seen complete
+    __half2 mx = __floats2half2_rn(0.f, 0.f);  // largest |value| converted to float16 (range flag)
+
+#pragma unroll 1
+    for (int k = 0; k < hpg && ok; ++k) {
+        const int h = g * hpg + k;
+        const int64_t crow = ((int64_t)b * H + h) * rowlen + t0;
+        // ---- loads
+        if (tid < T) scs[tid] = a.cs[crow + tid];
+        else sdt[tid - T] = a.dtt[crow + tid - T];
+        __syncthreads();
+        const float ce = scs[T - 1];
+        {
+            const int rr = tid & (T - 1), hl = tid >> 7;  // row, half of the row's 64 channels
+            const int64_t tok = t0 + rr;
+            uint4 xv[4], yv[4];
+            if (tok < L) {
+                const int64_t o = ((b * L + tok) * H + h) * (int64_t)kP + 32 * hl;
+                const uint4* xs = reinterpret_cast<const uint4*>(a.x + o);
+                const uint4* ys = reinterpret_cast<const uint4*>(a.dy + o);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    xv[j] = __ldg(xs + j);
+                    yv[j] = __ldg(ys + j);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) xv[j] = yv[j] = make_uint4(0, 0, 0, 0);
+            }
+            const float wx = sdt[rr] * fast_exp2(ce - scs[rr]);
+            const float wy = fast_exp2(scs[rr]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv[j]);
+                const uint32_t* yw = reinterpret_cast<const uint32_t*>(&yv[j]);
+                uint32_t ox[4], oxs[4], oy[4], oys[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 xf = bf2_to_f2(xw[e]), yf = bf2_to_f2(yw[e]);
+                    ox[e] = pack_f16x2(xf.x, xf.y);
+                    oxs[e] = pack_f16x2(xf.x * wx, xf.y * wx);
+                    oy[e] = pack_f16x2(yf.x, yf.y);
+                    oys[e] = pack_f16x2(yf.x * wy, yf.y * wy);
+                }
+                hmax_abs4(mx, ox[0], ox[1], ox[2], ox[3]);
+                hmax_abs4(mx, oxs[0], oxs[1], oxs[2], oxs[3]);
+                hmax_abs4(mx, oy[0], oy[1], oy[2], oy[3]);
+                hmax_abs4(mx, oys[0], oys[1], oys[2], oys[3]);
+                const uint32_t so = sw128_offset(rr, 4 * hl + j);
+                *reinterpret_cast<uint4*>(smem + K::OFF_X + so) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
+                *reinterpret_cast<uint4*>(smem + K::OFF_XS + so) = make_uint4(oxs[0], oxs[1], oxs[2], oxs[3]);
+                *reinterpret_cast<uint4*>(smem + K::OFF_DY + so) = make_uint4(oy[0], oy[1], oy[2], oy[3]);
+                *reinterpret_cast<uint4*>(smem + K::OFF_DYS + so) = make_uint4(oys[0], oys[1], oys[2], oys[3]);
+            }
+        }
+        float hmu = 0.f;  // this thread's part of <mu, h0> (float32 values)
+        {
+            // h0 and mu of (b, blk, h): (P, N) float32 -> float16 [p][n] tiles
+            const int64_t srow = (((int64_t)b * d.nchunks + blk) * H + h) * (int64_t)kP * N;
+            for (int c = tid; c < kP * N / 8; c += kThreads) {
+                const int p = c / (N / 8), cc = c % (N / 8);
+                const float4* hs = reinterpret_cast<const float4*>(a.h0 + srow + (int64_t)p * N + cc * 8);
+                const float4* ms = reinterpret_cast<const float4*>(a.mu + srow + (int64_t)p * N + cc * 8);
+                const float4 h0a = __ldg(hs), h0b = __ldg(hs + 1), mua = __ldg(ms), mub = __ldg(ms + 1);
+                const uint4 oh = make_uint4(pack_f16x2(h0a.x, h0a.y), pack_f16x2(h0a.z, h0a.w), pack_f16x2(h0b.x, h0b.y),
+                                            pack_f16x2(h0b.z, h0b.w));
+                const uint4 om = make_uint4(pack_f16x2(mua.x, mua.y), pack_f16x2(mua.z, mua.w), pack_f16x2(mub.x, mub.y),
+                                            pack_f16x2(mub.z, mub.w));
+                hmu = fmaf(h0a.x, mua.x, fmaf(h0a.y, mua.y, fmaf(h0a.z, mua.z, fmaf(h0a.w, mua.w, hmu))));
+                hmu = fmaf(h0b.x, mub.x, fmaf(h0b.y, mub.y, fmaf(h0b.z, mub.z, fmaf(h0b.w, mub.w, hmu))));
+                hmax_abs4(mx, oh.x, oh.y, oh.z, oh.w);
+                hmax_abs4(mx, om.x, om.y, om.z, om.w);
+                const uint32_t so = (cc >> 3) * kPanelP + sw128_offset(p, cc & 7);
+                *reinterpret_cast<uint4*>(smem + K::OFF_H0 + so) = oh;
+                *reinterpret_cast<uint4*>(smem + K::OFF_MU + so) = om;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) hmu += __shfl_xor_sync(0xffffffffu, hmu, off);
+        if (lane == 0) wsum[warp] = hmu;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- C B^T (K = n) and dY X^T (K = p)
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < N / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+                mma_ss(tm + T_CB, desc_sw128(sC + off, 16, 1024), desc_sw128(sB + off, 16, 1024), kIdescTT, kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < kP / 16; ++kk)
+                mma_ss(tm + T_DX, desc_sw128(sDY + kk * 32, 16, 1024), desc_sw128(sX + kk * 32, 16, 1024), kIdescTT,
+                       kk > 0);
+            mma_commit(bar);
+        }
+        pending = true;
+        ok = mbar_wait_bounded(bar, phase, abort_flag, err, 61, wait_ns);
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+        phase ^= 1;
+        pending = false;
+        tc_fence_after();
+        // ---- mask: row r, columns [64 hf, 64 hf + 64) of M' = L o C B^T and Wd = L o dY X^T o dt_j
+        float rho1 = 0.f;  // sum_j Wd[r][j] (C_r . B_j) over this half
+        {
+            const float cr = scs[r];
+#pragma unroll 1
+            for (int c2 = 0; c2 < 2; ++c2) {
+                const int i0 = 64 * hf + 32 * c2;
+                uint32_t vcb[32], vdx[32];
+                tmem_ld32(tm + lane_base + T_CB + i0, vcb);
+                tmem_ld32(tm + lane_base + T_DX + i0, vdx);
+                tmem_ld_wait(vcb);
+                tmem_ld_wait(vdx);
+                uint32_t pm[16], pw[16];
+#pragma unroll
+                for (int jj = 0; jj < 32; jj += 2) {
+                    float mv[2], wv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int i = i0 + jj + e;
+                        const float dec = (i <= r) ? fast_exp2(cr - scs[i]) : 0.f;
+                        const float cb = __uint_as_float(vcb[jj + e]);
+                        mv[e] = dec * cb;
+                        wv[e] = dec * sdt[i] * __uint_as_float(vdx[jj + e]);
+                        rho1 = fmaf(wv[e], cb, rho1);
+                    }
+                    pm[jj / 2] = pack_f16x2(mv[0], mv[1]);
+                    pw[jj / 2] = pack_f16x2(wv[0], wv[1]);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    hmax_abs4(mx, pm[4 * j], pm[4 * j + 1], pm[4 * j + 2], pm[4 * j + 3]);
+                    hmax_abs4(mx, pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
+                    const uint32_t so = hf * kPanel + sw128_offset(r, 4 * c2 + j);
+                    *reinterpret_cast<uint4*>(smem + K::OFF_M + so) =
+                        make_uint4(pm[4 * j], pm[4 * j + 1], pm[4 * j + 2], pm[4 * j + 3]);
+                    *reinterpret_cast<uint4*>(smem + K::OFF_W + so) =
+                        make_uint4(pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- G = M'^T dY, B mu, C h0, dC (+)= dY' h0^T + Wd B, dB (+)= X' mu^T + Wd^T C
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < T / 16; ++kk)  // K = r
+                mma_ss(tm + T_G, desc_sw128(sM + kk * 2048, kPanel, 1024), desc_sw128(sDY + kk * 2048, kPanel, 1024),
+                       kIdescG, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < N / 16; ++kk) {  // K = n
+                const uint32_t offT = (kk >> 2) * kPanel + (kk & 3) * 32;
+                const uint32_t offP = (kk >> 2) * kPanelP + (kk & 3) * 32;
+                mma_ss(tm + T_GMU, desc_sw128(sB + offT, 16, 1024), desc_sw128(sMU + offP, 16, 1024), kIdescP, kk > 0);
+                mma_ss(tm + T_YS, desc_sw128(sC + offT, 16, 1024), desc_sw128(sH0 + offP, 16, 1024), kIdescP, kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < kP / 16; ++kk) {  // K = p
+                mma_ss(tm + T_DC, desc_sw128(sDYS + kk * 32, 16, 1024), desc_sw128(sH0 + kk * 2048, kPanelP, 1024),
+                       kIdescN, k > 0 || kk > 0);
+                mma_ss(tm + T_DB, desc_sw128(sXS + kk * 32, 16, 1024), desc_sw128(sMU + kk * 2048, kPanelP, 1024),
+                       kIdescN, k > 0 || kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < T / 16; ++kk) {  // K = tokens
+                const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+                mma_ss(tm + T_DC, desc_sw128(sW + off, 16, 1024), desc_sw128(sB + kk * 2048, kPanel, 1024), kIdescN, 1);
+                mma_ss(tm + T_DB, desc_sw128(sW + kk * 2048, kPanel, 1024), desc_sw128(sC + kk * 2048, kPanel, 1024),
+                       kIdescNT, 1);
+            }
+            mma_commit(bar);
+        }
+        pending = true;
+        ok = mbar_wait_bounded(bar, phase, abort_flag, err, 62, wait_ns);
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+        phase ^= 1;
+        pending = false;
+        tc_fence_after();
+        // ---- epilogue: row r, channels [32 hf, 32 hf + 32)
+        {
+            float* red = reinterpret_cast<float*>(smem + K::OFF_M);  // [quantity][half][T]; M' is consumed
+            const int64_t tok = t0 + r;
+            const float ext = fast_exp2(ce - scs[r]), dtr = sdt[r];
+            const float Dh = (a.D != nullptr) ? __ldg(a.D + h) : 0.f;
+            uint32_t vg[32], vm[32];
+            tmem_ld32(tm + lane_base + T_G + 32 * hf, vg);
+            tmem_ld32(tm + lane_base + T_GMU + 32 * hf, vm);
+            tmem_ld_wait(vg);
+            tmem_ld_wait(vm);
+            float sg = 0.f, sm = 0.f, xdy = 0.f;  // x . G (pairs in the block), x . B mu, x . dy
+            uint32_t ob[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 xq = *reinterpret_cast<const uint4*>(smem + K::OFF_X + sw128_offset(r, 4 * hf + j));
+                const uint4 yq = *reinterpret_cast<const uint4*>(smem + K::OFF_DY + sw128_offset(r, 4 * hf + j));
+                const __half2* xh = reinterpret_cast<const __half2*>(&xq);
+                const __half2* yh = reinterpret_cast<const __half2*>(&yq);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 8 * j + 2 * e;
+                    const float2 xf = __half22float2(xh[e]), yf = __half22float2(yh[e]);
+                    const float gi0 = __uint_as_float(vg[c]), gi1 = __uint_as_float(vg[c + 1]);
+                    const float gm0 = __uint_as_float(vm[c]), gm1 = __uint_as_float(vm[c + 1]);
+                    sg = fmaf(xf.x, gi0, fmaf(xf.y, gi1, sg));
+                    sm = fmaf(xf.x, gm0, fmaf(xf.y, gm1, sm));
+                    xdy = fmaf(xf.x, yf.x, fmaf(xf.y, yf.y, xdy));
+                    const float g0 = fmaf(ext, gm0, gi0), g1 = fmaf(ext, gm1, gi1);
+                    ob[4 * j + e] = pack_bf16x2(fmaf(dtr, g0, Dh * yf.x), fmaf(dtr, g1, Dh * yf.y));
+                }
+            }
+            if (tok < L) {
+                uint4* dst = reinterpret_cast<uint4*>(a.dx + ((b * L + tok) * H + h) * (int64_t)kP + 32 * hf);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) dst[j] = make_uint4(ob[4 * j], ob[4 * j + 1], ob[4 * j + 2], ob[4 * j + 3]);
+            }
+            uint32_t vy[32];
+            tmem_ld32(tm + lane_base + T_YS + 32 * hf, vy);
+            tmem_ld_wait(vy);
+            float rho2 = 0.f;  // dy_r . (C_r h0) over this half
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 yq = *reinterpret_cast<const uint4*>(smem + K::OFF_DY + sw128_offset(r, 4 * hf + j));
+                const __half2* yh = reinterpret_cast<const __half2*>(&yq);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 8 * j + 2 * e;
+                    const float2 yf = __half22float2(yh[e]);
+                    rho2 = fmaf(yf.x, __uint_as_float(vy[c]), fmaf(yf.y, __uint_as_float(vy[c + 1]), rho2));
+                }
+            }
+            red[(0 * 2 + hf) * T + r] = sg;
+            red[(1 * 2 + hf) * T + r] = sm;
+            red[(2 * 2 + hf) * T + r] = rho2;
+            red[(3 * 2 + hf) * T + r] = rho1;
+            red[(4 * 2 + hf) * T + r] = xdy;
+            tc_fence_before();
+            __syncthreads();
+            float* wtot = red + 10 * T;  // per-warp totals of the scans: [v or w][warp]
+            float v = 0.f, wv = 0.f, pv = 0.f, pw = 0.f, sfull = 0.f, dtl = 0.f, xd = 0.f;
+            if (tid < T) {
+                const int t = tid;
+                const float dtt = sdt[t], ex = fast_exp2(ce - scs[t]);
+                const float sgt = red[t] + red[T + t], smt = red[2 * T + t] + red[3 * T + t];
+                sfull = fmaf(ex, smt, sgt);                                   // x_t . G_t
+                v = dtt * ex * smt;                                           // mu's part, at token t
+                wv = fmaf(fast_exp2(scs[t]), red[4 * T + t] + red[5 * T + t],  // rho2 + rho1 - sigma
+                          red[6 * T + t] + red[7 * T + t]) - dtt * sgt;
+                dtl = dtt;
+                xd = red[8 * T + t] + red[9 * T + t];
+                // inclusive scans of v and w inside the warp
+                pv = v;
+                pw = wv;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float ov = __shfl_up_sync(0xffffffffu, pv, off);
+                    const float ow = __shfl_up_sync(0xffffffffu, pw, off);
+                    if (lane >= off) {
+                        pv += ov;
+                        pw += ow;
+                    }
+                }
+                if (lane == 31) {
+                    wtot[warp] = pv;
+                    wtot[4 + warp] = pw;
+                }
+            }
+            __syncthreads();
+            if (tid < T) {
+                const int t = tid;
+                float bv = 0.f, bw = 0.f, tw = 0.f;  // earlier warps' totals; all of w
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2) {
+                    if (k2 < warp) {
+                        bv += wtot[k2];
+                        bw += wtot[4 + k2];
+                    }
+                    tw += wtot[4 + k2];
+                }
+                const float hmu_all = (wsum[0] + wsum[1]) + (wsum[2] + wsum[3]) + ((wsum[4] + wsum[5]) + (wsum[6] + wsum[7]));
+                // dl_t = 2^(c_e) <mu, h0> + (v before t) + (w from t on)
+                const float excl_v = bv + pv - v;
+                const float from_t_w = tw - (bw + pw - wv);
+                const float dl = fmaf(fast_exp2(ce), hmu_all, excl_v + from_t_w);
+                if (t0 + t < L) a.ddt[((b * L + t0 + t) * H + h)] = fmaf(__ldg(a.A + h), dl, sfull);
+                float da = dtl * dl;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    da += __shfl_xor_sync(0xffffffffu, da, off);
+                    xd += __shfl_xor_sync(0xffffffffu, xd, off);
+                }
+                if (lane == 0) {
+                    wtot[8 + warp] = da;
+                    wtot[12 + warp] = xd;
+                }
+            }
+            __syncthreads();
+            if (tid == 0) {
+                const int64_t o = ((int64_t)b * H + h) * d.nchunks + blk;
+                a.dap[o] = (wtot[8] + wtot[9]) + (wtot[10] + wtot[11]);
+                a.xdy[o] = (wtot[12] + wtot[13]) + (wtot[14] + wtot[15]);
+            }
+        }
+    }
+    flag_f16_range(err, hmax_to_float(mx));
+    if (ok) {
+        // dC and dB rows of this block, summed over the group's heads
+        const int64_t tok = t0 + r;
+#pragma unroll 1
+        for (int c = 0; c < N / 64; ++c) {
+            const int n0 = hf * (N / 2) + 32 * c;
+            uint32_t vc[32], vb[32];
+            tmem_ld32(tm + lane_base + T_DC + n0, vc);
+            tmem_ld32(tm + lane_base + T_DB + n0, vb);
+            tmem_ld_wait(vc);
+            tmem_ld_wait(vb);
+            if (tok < L) {
+                float4* dc = reinterpret_cast<float4*>(a.dC + ((b * L + tok) * G + g) * (int64_t)N + n0);
+                float4* db = reinterpret_cast<float4*>(a.dB + ((b * L + tok) * G + g) * (int64_t)N + n0);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    dc[j] = make_float4(__uint_as_float(vc[4 * j]), __uint_as_float(vc[4 * j + 1]),
+                                        __uint_as_float(vc[4 * j + 2]), __uint_as_float(vc[4 * j + 3]));
+                    db[j] = make_float4(__uint_as_float(vb[4 * j]), __uint_as_float(vb[4 * j + 1]),
+                                        __uint_as_float(vb[4 * j + 2]), __uint_as_float(vb[4 * j + 3]));
+                }
+            }
+        }
+    } else if (tid == 0 && pending) {
+        mbar_wait_drain(bar, phase, err, 63, kDrainNs);  // the products issued have retired before TMEM is freed
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tm, 512);
+}
+
+// ---- dA and dD: one CTA per head adds the per-(batch, block) partial sums in a fixed order
+
+constexpr int kRedThreads = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* sh) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    __syncthreads();
+    if (lane == 0) sh[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        v = (lane < kRedThreads / 32) ? sh[lane] : 0.f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) sh[32] = v;
+    }
+    __syncthreads();
+    return sh[32];
+}
+
+__global__ void __launch_bounds__(kRedThreads) bwd_reduce_kernel(const float* __restrict__ dap,
+                                                                 const float* __restrict__ xdy, Dims d,
+                                                                 float* __restrict__ dA, float* __restrict__ dD) {
+    __shared__ float sh[33];
+    const int h = blockIdx.x, tid = threadIdx.x;
+    float sa = 0.f, sd = 0.f;
+    for (int b = 0; b < d.batch; ++b) {
+        const int64_t row = ((int64_t)b * d.nheads + h) * d.nchunks;
+        for (int64_t k = tid; k < d.nchunks; k += kRedThreads) {
+            sa += dap[row + k];
+            sd += xdy[row + k];
+        }
+    }
+    sa = block_sum(sa, sh);
+    sd = block_sum(sd, sh);
+    if (tid == 0) {
+        dA[h] = sa;
+        if (dD != nullptr) dD[h] = sd;
+    }
+}
+
+template <int N>
+int launch_bwd_n(const BwdArgs& a, cudaStream_t s) {
+    using K = BwdCfg<N>;
+    if (ensure_smem_limit(reinterpret_cast<const void*>(bwd_chunk_kernel<N>), K::SMEM) != SSD_OK) return SSD_ERR_CUDA;
+    dim3 grid(a.d.nchunks, a.d.ngroups, a.d.batch);
+    launch_begin(kKindBwdChunk, s);
+    bwd_chunk_kernel<N><<<grid, kThreads, K::SMEM, s>>>(a);
+    return launch_end(kKindBwdChunk, s);
+}
+
+}  // namespace
+
+bool bwd_supported(const Dims& d) {
+    return d.headdim == kP && (d.dstate == 64 || d.dstate == 128) && d.chunk_size == T && d.head0 == 0 &&
+           d.hcount == d.nheads;
+}
+
+int launch_bwd_chunk(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __half* B16, const __half* C16,
+                     const float* cs, const float* dtt, const float* A, const float* D, const float* h0, const float* mu,
+                     const Dims& d, __nv_bfloat16* dx, float* ddt, float* dB, float* dC, float* dap, float* xdy,
+                     const Ctl& ctl, cudaStream_t s) {
+    if (!bwd_supported(d) || d.nchunks > 2147483647 || d.ngroups > 65535 || d.batch > 65535)
+        return SSD_ERR_UNSUPPORTED;
+    BwdArgs a;
+    a.x = x;
+    a.dy = dy;
+    a.B16 = B16;
+    a.C16 = C16;
+    a.cs = cs;
+    a.dtt = dtt;
+    a.D = D;
+    a.h0 = h0;
+    a.mu = mu;
+    a.A = A;
+    a.dx = dx;
+    a.ddt = ddt;
+    a.dB = dB;
+    a.dC = dC;
+    a.dap = dap;
+    a.xdy = xdy;
+    a.d = d;
+    a.ctl = ctl;
+    return d.dstate == 64 ? launch_bwd_n<64>(a, s) : launch_bwd_n<128>(a, s);
+}
+
+int launch_bwd_reduce(const float* dap, const float* xdy, const Dims& d, float* dA, float* dD, cudaStream_t s) {
+    launch_begin(kKindBwdReduce, s);
+    bwd_reduce_kernel<<<d.nheads, kRedThreads, 0, s>>>(dap, xdy, d, dA, dD);
+    return launch_end(kKindBwdReduce, s);
+}
+
+}  // namespace ssd

@@ -24,6 +24,10 @@
 // warpgroups scale the X rows in shared memory (one token row per thread)
 // and store the result; one warp issues the TMA loads; one warp owns TMEM
 // and issues the MMAs.
+// Reverse-time mode (the backward pass, one-chunk spans): the same product with C in B's place,
+// dy in x's place and w_t = 2^(cs(t)) (the decay from the chunk start through token t, no dt
+// factor), which gives the chunk's contribution to the gradient flowing into the state before it:
+//   Z_c[p][n] = sum_{t in chunk} C[t, n] * 2^(cs(t)) * dy[t, p].
 // Operands are float16: B is the exact float16 copy of the input, and the
 // scaled rows w x (bfloat16 x times an f32 weight) are rounded once to
 // float16, whose 11 significant bits keep the state within tolerance.
@@ -77,6 +81,7 @@ struct StateArgs {
     float* S;           // (b, nspans, hcount, P, N)
     float* span_decay;  // (b, hcount, nspans) log2 units, or null
     Ctl ctl;            // error words, wait limit, stall hook
+    int rev;            // reverse-time weights (one-chunk spans): w_t = 2^(cs(t)), no dt factor
 };
 
 template <int N, int HH>
@@ -240,7 +245,9 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
                     uint8_t* xrow = stage + hh * K::BOX;
                     const float* cd = scd + hh * 2 * K::TB;
                     float w = 0.f;
-                    if (t < te) w = exp2f(Rs[hh * kMaxSpanChunks + (int)(t / Q - c_first)] - cd[rr]) * cd[K::TB + rr];
+                    if (t < te)
+                        w = a.rev ? exp2f(cd[rr])
+                                  : exp2f(Rs[hh * kMaxSpanChunks + (int)(t / Q - c_first)] - cd[rr]) * cd[K::TB + rr];
                     uint4 v[8];
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) v[ch] = *reinterpret_cast<const uint4*>(xrow + sw128_offset(rr, ch));
@@ -340,11 +347,33 @@ int launch_chunk_state_span(const __nv_bfloat16* x, const __half* B, const float
     a.S = S;
     a.span_decay = span_decay;
     a.ctl = ctl;
+    a.rev = 0;
     switch (d.dstate) {
         case 64: return launch_state_n<64>(x, B, a, s);
         case 128: return launch_state_n<128>(x, B, a, s);
         case 256: return launch_state_n<256>(x, B, a, s);
         case 512: return launch_state_n<512>(x, B, a, s);
+        default: return SSD_ERR_UNSUPPORTED;
+    }
+}
+
+int launch_chunk_state_rev(const __nv_bfloat16* dy, const __half* C16, const float* dtt, const float* cs, const Dims& d,
+                           float* Z, const Ctl& ctl, cudaStream_t s) {
+    StateArgs a;
+    a.d = d;
+    a.span_chunks = 1;
+    a.nspans = d.nchunks;
+    a.cs = cs;
+    a.dtt = dtt;
+    a.S = Z;
+    a.span_decay = nullptr;
+    a.ctl = ctl;
+    a.rev = 1;
+    switch (d.dstate) {
+        case 64: return launch_state_n<64>(dy, C16, a, s);
+        case 128: return launch_state_n<128>(dy, C16, a, s);
+        case 256: return launch_state_n<256>(dy, C16, a, s);
+        case 512: return launch_state_n<512>(dy, C16, a, s);
         default: return SSD_ERR_UNSUPPORTED;
     }
 }

@@ -10,6 +10,12 @@
 //
 //   h_0 = init;  states[c] = h_c;  h_{c+1} = 2^(cs[b,h,c,Q-1]) h_c + S[c];  final = h_nc
 //
+// Reverse mode (the backward pass): the steps run from the last chunk to the
+// first, so with the gradient into the final state as `init` the hop gives,
+// per chunk, the gradient flowing into the state after it from later tokens,
+// and as `final` the gradient with respect to the initial state:
+//   mu_{nc-1} = dfinal;  out[c] = mu_c;  mu_{c-1} = 2^(cs[b,h,c,Q-1]) mu_c + Z[c];  final = mu_{-1}
+//
 // Every (b, h, p, n) entry is an independent lane of a serial fp32 recurrence.
 // Each thread owns 4 consecutive entries (one float4); the loop over chunks
 // keeps two groups of kUnroll chunk-state loads in flight -- the next group
@@ -29,7 +35,8 @@ constexpr int kUnroll = 8;
 __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S, const float* __restrict__ dec,
                                                                  int64_t dec_step, int64_t dec_row,
                                                                  const float* __restrict__ init, Dims d,
-                                                                 float* states, float* __restrict__ final_state) {
+                                                                 float* states, float* __restrict__ final_state,
+                                                                 int rev) {
     grid_dep_wait();  // the chunk or span states come from the previous launch
     grid_dep_launch_dependents();
     const int64_t PN = (int64_t)d.headdim * d.dstate;
@@ -50,8 +57,9 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
 #pragma unroll
     for (int k = 0; k < kUnroll; ++k) {
         if (k < nc) {
-            nv[k] = *reinterpret_cast<const float4*>(S + base + (int64_t)k * cstride);
-            nd[k] = __ldg(csl + (int64_t)k * dec_step);
+            const int c = rev ? nc - 1 - k : k;
+            nv[k] = *reinterpret_cast<const float4*>(S + base + (int64_t)c * cstride);
+            nd[k] = __ldg(csl + (int64_t)c * dec_step);
         }
     }
     for (int c0 = 0; c0 < nc; c0 += kUnroll) {
@@ -64,15 +72,17 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
         for (int k = 0; k < kUnroll; ++k) {
             const int cn = c0 + kUnroll + k;
             if (cn < nc) {
-                nv[k] = *reinterpret_cast<const float4*>(S + base + (int64_t)cn * cstride);
-                nd[k] = __ldg(csl + (int64_t)cn * dec_step);
+                const int c = rev ? nc - 1 - cn : cn;
+                nv[k] = *reinterpret_cast<const float4*>(S + base + (int64_t)c * cstride);
+                nd[k] = __ldg(csl + (int64_t)c * dec_step);
             }
         }
 #pragma unroll
         for (int k = 0; k < kUnroll; ++k) {
             if (c0 + k < nc) {
                 const float dd = exp2f(dk[k]);
-                *reinterpret_cast<float4*>(states + base + (int64_t)(c0 + k) * cstride) = hv;
+                const int c = rev ? nc - 1 - (c0 + k) : c0 + k;
+                *reinterpret_cast<float4*>(states + base + (int64_t)c * cstride) = hv;
                 hv.x = fmaf(dd, hv.x, sv[k].x);
                 hv.y = fmaf(dd, hv.y, sv[k].y);
                 hv.z = fmaf(dd, hv.z, sv[k].z);
@@ -95,7 +105,7 @@ int launch_state_passing(const float* S, const float* cs, const float* init, con
 
 int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_step, int64_t dec_row,
                                const float* init, const Dims& d, int nsteps, float* states, float* final_state,
-                               cudaStream_t s) {
+                               cudaStream_t s, int rev) {
     Dims dd = d;
     dd.nchunks = nsteps;
     const int64_t PN = (int64_t)d.headdim * d.dstate;
@@ -103,7 +113,7 @@ int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_ste
     launch_begin(kKindStatePassing, s);
     const cudaError_t le =
         launch_dependent(state_passing_kernel, grid, dim3(kThreads), 0, s, S, dec, dec_step, dec_row, init, dd, states,
-                         final_state);
+                         final_state, rev);
     const int r = launch_end(kKindStatePassing, s);
     return le != cudaSuccess ? SSD_ERR_CUDA : r;
 }

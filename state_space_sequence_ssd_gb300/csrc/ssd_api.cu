@@ -46,7 +46,7 @@ cudaEvent_t take_event() {
 }
 
 const char* const kKindNames[kNumKinds] = {"chunk_cumsum", "chunk_state", "state_passing", "chunk_scan",
-                                           "bc_to_f16", "step"};
+                                           "bc_to_f16", "step", "bwd_chunk", "bwd_reduce"};
 
 }  // namespace
 
@@ -614,6 +614,60 @@ int ssd_forward_plan(int batch, int seqlen, int nheads, int headdim, int ngroups
     if (scan_step != nullptr) *scan_step = forward_scan_step(d, span, OutOpts());
     if (noalloc_bytes != nullptr) *noalloc_bytes = (unsigned long long)noalloc_layout(d, span).need;
     return SSD_OK;
+}
+
+int ssd_backward(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,
+                 const float* init_state, const void* dy, const float* dfinal, int batch, int seqlen, int nheads,
+                 int headdim, int ngroups, int dstate, int chunk_size, void* dx, float* ddt, float* dA, float* dB,
+                 float* dC, float* dD, float* dinit, cudaStream_t stream) {
+    if (!x || !dt || !A || !B || !C || !dy || !dx || !ddt || !dA || !dB || !dC) return SSD_ERR_INVALID_ARG;
+    int r = check_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size);
+    if (r != SSD_OK) return r;
+    if (!aligned16(x) || !aligned16(B) || !aligned16(C) || !aligned16(dy) || !aligned16(dx) || !aligned16(dB) ||
+        !aligned16(dC) || ((uintptr_t)dt & 3u) || ((uintptr_t)A & 3u) || ((uintptr_t)ddt & 3u) ||
+        ((uintptr_t)dA & 3u) || (D && ((uintptr_t)D & 3u)) || (dD && ((uintptr_t)dD & 3u)) ||
+        (init_state && !aligned16(init_state)) || (dfinal && !aligned16(dfinal)) || (dinit && !aligned16(dinit)))
+        return SSD_ERR_INVALID_ARG;
+    // the backward works in blocks of kBwdBlock tokens whatever chunk_size is (the result does not depend
+    // on the chunking)
+    const Dims d = make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, kBwdBlock);
+    if (!bwd_supported(d)) return SSD_ERR_UNSUPPORTED;
+    int* err = device_error_ptr();
+    if (err == nullptr) return SSD_ERR_CUDA;
+    const size_t nrow = (size_t)d.batch * d.nheads * d.nchunks * kBwdBlock;        // cs and dt rows
+    const size_t nst = (size_t)d.batch * d.nchunks * d.nheads * d.headdim * d.dstate;  // per-block states
+    const size_t npart = ((size_t)d.batch * d.nheads * d.nchunks + 3) & ~(size_t)3;  // per-block partial sums
+    const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;  // multiple of 64
+    const size_t bytes = (2 * nrow + 2 * nst + 2 * npart) * sizeof(float) + 2 * nbc * sizeof(__half);
+    void* ws = nullptr;
+    if (workspace_alloc(&ws, bytes, stream) != SSD_OK) return SSD_ERR_NO_MEMORY;
+    float* cs = static_cast<float*>(ws);
+    float* dtt = cs + nrow;
+    float* h0 = dtt + nrow;
+    float* mu = h0 + nst;
+    float* dap = mu + nst;
+    float* xdy = dap + npart;
+    __half* B16 = reinterpret_cast<__half*>(xdy + npart);
+    __half* C16 = B16 + nbc;
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    const __nv_bfloat16* dyb = static_cast<const __nv_bfloat16*>(dy);
+    // forward hop: the state before every block (in place over the blocks' own states)
+    r = launch_chunk_cumsum_bc(dt, A, d, cs, dtt, static_cast<const __nv_bfloat16*>(B),
+                               static_cast<const __nv_bfloat16*>(C), B16, C16, err, stream);
+    if (r == SSD_OK)
+        r = launch_chunk_state_span(xb, B16, dtt, cs, 1, d, h0, nullptr, make_ctl(err, kKindChunkState), stream);
+    if (r == SSD_OK) r = launch_state_passing(h0, cs, init_state, d, h0, nullptr, stream);
+    // reverse hop: the gradient flowing into the state after every block, and dinit
+    if (r == SSD_OK) r = launch_chunk_state_rev(dyb, C16, dtt, cs, d, mu, make_ctl(err, kKindChunkState), stream);
+    if (r == SSD_OK)
+        r = launch_state_passing_steps(mu, cs + (kBwdBlock - 1), kBwdBlock, (int64_t)d.nchunks * kBwdBlock, dfinal, d,
+                                       d.nchunks, mu, dinit, stream, 1);
+    if (r == SSD_OK)
+        r = launch_bwd_chunk(xb, dyb, B16, C16, cs, dtt, A, D, h0, mu, d, static_cast<__nv_bfloat16*>(dx), ddt, dB, dC,
+                             dap, xdy, make_ctl(err, kKindBwdChunk), stream);
+    if (r == SSD_OK) r = launch_bwd_reduce(dap, xdy, d, dA, dD, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
+    return r;
 }
 
 int ssd_step(const void* x, const float* dt, const float* A, const void* B, const void* C, const float* D,
