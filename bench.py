@@ -272,7 +272,7 @@ def main():
     torch.cuda.synchronize()
     plain_ms = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in plain)), dist, dev) / args.steps
 
-    e2e = decode = decode_multi = layer = None
+    e2e = decode = decode_multi = layer = backward = None
     if not args.forward_only:
         # ---- end to end through the public call with host buffers
         e2e = e2e_measure(w, inp, dev, stream, args, ssd, dist)
@@ -283,6 +283,9 @@ def main():
         # ---- the same forward with a whole layer's input-side options (dt bias/softplus/clamp, D per channel,
         #      z gate)
         layer = layer_options_measure(w, d, dev, stream, args, ssd, lib, flush)
+        # ---- the backward pass (gradients of a loss given dy and dfinal) on the same workload
+        if w.headdim == 64 and w.dstate in (64, 128):
+            backward = backward_measure(w, d, dev, stream, args, ssd, lib, flush)
 
     if rank != 0:
         dist.destroy_process_group()
@@ -349,6 +352,7 @@ def main():
         "decode_step": decode,
         "decode_multi": decode_multi,
         "layer_options": layer,
+        "backward": backward,
         "clocks": clk,
         "device_error": int(err),
     }
@@ -664,6 +668,115 @@ def layer_options_measure(w, d, dev, stream, args, ssd, lib, flush):
             "chunk_scan_us": None if scan_us is None else round(scan_us, 2),
             "extra_alg_bytes": float(w.batch * w.seqlen * w.nheads * w.headdim * 2 + w.nheads * 4 * (1 + w.headdim)),
             "steps": steps, "gpu_launches": int(launches)}
+
+
+BWD_BLOCK = 128  # the backward's token block (ssd_backward uses it whatever chunk_size is)
+
+
+def backward_alg_flops(w: I.Workload) -> dict:
+    """Algorithmic FLOPs of one ssd_backward, as its chunked form does them over 128-token blocks with the
+    masked products counted on their causal half (as the forward's count does): per block and head
+    T(T+1)P twice (dY X^T and (L o C B^T)^T dY), T(T+1)N twice (Wd B and Wd^T C) and 2TNP four times
+    (B mu, C h0, (2^c dY) h0^T, (dt 2^(c_e-c) X) mu^T); per block and group T(T+1)N (C B^T); and the two
+    hops' block states, 2TNP per block and head each.  Returns {"bwd_chunk": ..., "total": ...}."""
+    T, N, P, H, G = BWD_BLOCK, w.dstate, w.headdim, w.nheads, w.ngroups
+    nblk = -(-w.seqlen // T)
+    per_bh = 2 * T * (T + 1) * P + 2 * T * (T + 1) * N + 8 * T * N * P
+    chunk = w.batch * nblk * (H * per_bh + G * T * (T + 1) * N)
+    hops = w.batch * nblk * H * 2 * (2 * T * N * P)
+    return {"bwd_chunk": float(chunk), "total": float(chunk + hops)}
+
+
+def backward_compulsory_bytes(w: I.Workload) -> float:
+    """x, dy read and dx written (bf16); dt read, ddt written (f32); B, C read (bf16); dB, dC written (f32);
+    A, D read and dA, dD written; dfinal read, dinit written and init read when it is non-zero (f32)."""
+    b, L, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    by = 3 * b * L * H * P * 2 + 2 * b * L * H * 4 + 2 * b * L * G * N * 2 + 2 * b * L * G * N * 4 + 4 * H * 4
+    by += 2 * b * H * P * N * 4
+    if w.nonzero_init:
+        by += b * H * P * N * 4
+    return float(by)
+
+
+def backward_measure(w, d, dev, stream, args, ssd, lib, flush):
+    """ssd_backward on the workload (inputs, dy and dfinal resident, L2 flushed between steps outside the
+    events): ms per pass, per-kernel CUDA-event times from a profiled pass, the pass roofline and the
+    dominant kernel's tensor roofline."""
+    import ctypes
+    import torch
+    gi = I.make_grad_inputs(w, seed=0)
+    dy, dfin = gi["dy"].to(dev), gi["dfinal"].to(dev)
+    out = {"dx": torch.empty_like(d["x"]),
+           "ddt": torch.empty((w.batch, w.seqlen, w.nheads), device=dev, dtype=torch.float32),
+           "dA": torch.empty((w.nheads,), device=dev, dtype=torch.float32),
+           "dB": torch.empty((w.batch, w.seqlen, w.ngroups, w.dstate), device=dev, dtype=torch.float32),
+           "dC": torch.empty((w.batch, w.seqlen, w.ngroups, w.dstate), device=dev, dtype=torch.float32),
+           "dD": torch.empty((w.nheads,), device=dev, dtype=torch.float32),
+           "dinit": torch.empty((w.batch, w.nheads, w.headdim, w.dstate), device=dev, dtype=torch.float32)}
+    lp = ssd._ffi.lib()
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+
+    def step():
+        ssd._ffi.check("ssd_backward", lp.ssd_backward(
+            ptr(d["x"]), ptr(d["dt"]), ptr(d["A"]), ptr(d["B"]), ptr(d["C"]), ptr(d["D"]), ptr(d["init"]), ptr(dy),
+            ptr(dfin), w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk_size,
+            ptr(out["dx"]), ptr(out["ddt"]), ptr(out["dA"]), ptr(out["dB"]), ptr(out["dC"]), ptr(out["dD"]),
+            ptr(out["dinit"]), stream.cuda_stream))
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    steps = max(args.steps, 10)
+    # profiled pass: an event pair around every launch
+    lib.ssd_profile_reset()
+    lib.ssd_profile_enable(0xFFFF)
+    for _ in range(steps):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    lib.ssd_profile_enable(0)
+    kms = (ctypes.c_float * 16)()
+    kcnt = (ctypes.c_int * 16)()
+    nk = ctypes.c_int(0)
+    lib.ssd_profile_read(kms, kcnt, 16, ctypes.byref(nk))
+    kernels = {lib.ssd_kernel_name(k).decode(): {"us_per_launch": round(float(kms[k]) / kcnt[k] * 1e3, 2),
+                                                 "launches_per_pass": kcnt[k] // steps}
+               for k in range(nk.value) if kcnt[k] > 0}
+    # timed pass: only the outer event pair per step
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    n0 = lib.ssd_launch_count()
+    for i in range(steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    launches = lib.ssd_launch_count() - n0
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / steps
+    fl = backward_alg_flops(w)
+    cb = backward_compulsory_bytes(w)
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    t_roof = max(fl["total"] / (tf * 1e12), cb / (hbm * 1e9)) * 1e6
+    res = {"workload": w.name, "ms_per_step": round(ms, 4), "tokens_per_s": round(w.batch * w.seqlen / (ms / 1e3), 1),
+           "tflops": round(fl["total"] / (ms / 1e3) / 1e12, 2),
+           "pass_roofline": {"t_roofline_us": round(t_roof, 2), "t_measured_us": round(ms * 1e3, 2),
+                             "frac": round(t_roof / (ms * 1e3), 4), "alg_gflop": round(fl["total"] / 1e9, 3),
+                             "compulsory_mb": round(cb / 1e6, 2),
+                             "peaks": f"{src}: {hbm} GB/s, {tf} TFLOP/s bf16 (the kernels' products are fp16)"},
+           "kernels": kernels, "steps": steps, "gpu_launches": int(launches)}
+    bk = kernels.get("bwd_chunk")
+    if bk:
+        ach = fl["bwd_chunk"] / (bk["us_per_launch"] * 1e-6) / 1e12
+        res["roofline"] = {"bound": "tensor", "kernel": "bwd_chunk", "achieved": round(ach, 1), "peak": tf,
+                           "unit": "TFLOP/s", "frac": round(ach / tf, 4),
+                           "peak_source": "measured bf16_tflops (cuBLAS burst); fp16 has the same dense rate",
+                           "alg_flops_per_launch": fl["bwd_chunk"], "avg_launch_us": bk["us_per_launch"],
+                           "traffic": None}
+    return res
 
 
 DECODE_BATCH = 256

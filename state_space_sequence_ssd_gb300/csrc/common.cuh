@@ -168,7 +168,8 @@ int launch_chunk_scan_pair(const __nv_bfloat16* x, const __half* B, const __half
                            __nv_bfloat16* y, const Ctl& ctl, cudaStream_t s, int state_step);
 
 // Backward pass (k_bwd.cu), over blocks of kBwdBlock tokens (d.chunk_size == kBwdBlock, d.nchunks blocks):
-// per (block, group, batch) the gradients of every head of the group from the block-start states h0
+// per (block, group, batch) the gradients of every head of the group -- split over `slices` CTAs (a
+// cluster; 1, 2 or 4, dividing the heads per group) -- from the block-start states h0
 // and the block-end gradients mu (both (b, nblk, H, P, N) f32): dx, ddt, this block's rows of dB and
 // dC (summed over the group's heads), and per (b, h, block) the partial sums of dt dl (for dA) and of
 // x . dy (for dD), (b, H, nblk) f32 each.
@@ -177,7 +178,7 @@ bool bwd_supported(const Dims& d);
 int launch_bwd_chunk(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __half* B16, const __half* C16,
                      const float* cs, const float* dtt, const float* A, const float* D, const float* h0, const float* mu,
                      const Dims& d, __nv_bfloat16* dx, float* ddt, float* dB, float* dC, float* dap, float* xdy,
-                     const Ctl& ctl, cudaStream_t s);
+                     const Ctl& ctl, cudaStream_t s, int slices);
 // dA[h] and dD[h] (dD may be null): the partial sums over batch and blocks, in a fixed order
 int launch_bwd_reduce(const float* dap, const float* xdy, const Dims& d, float* dA, float* dD, cudaStream_t s);
 

@@ -33,8 +33,10 @@
 // tokens and batch, dD = sum of x . dy: per (b, h, block) partial sums, added up in a fixed order
 // by bwd_reduce_kernel.
 //
-// One CTA per (block, group, batch) walks every head of the group, so dB and dC accumulate in
-// TMEM across the heads and are written once, without atomics and in a fixed order.  Per head
+// One CTA per (block, group slice, batch) walks hpg / S heads of the group, with dB and dC
+// accumulated in TMEM across them; the S CTAs of a group form a thread-block cluster and add their
+// partial dB and dC through distributed shared memory in rank order, so the result is written once,
+// without atomics and in a fixed order (S = 1: no cluster).  Per head
 // the phases run one after another: loads (x and dy to float16 tiles, the two scaled tiles
 // 2^c dy and dt 2^(c_e - c) x, h0 and mu to float16), the products C B^T and dY X^T, the mask
 // (one thread per row and column half: M' = L o C B^T and Wd to float16 tiles), the products
@@ -91,6 +93,7 @@ struct BwdArgs {
     float *ddt, *dB, *dC, *dap, *xdy;  // dap, xdy: per (b, h, block) partial sums of dt dl and x . dy
     Dims d;
     Ctl ctl;
+    int slices;  // S: CTAs (a cluster) per (block, group), each with hpg / S heads
 };
 
 // bfloat16 pair (low, high) -> float2
@@ -112,8 +115,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     float* wsum = reinterpret_cast<float*>(bar + 4);  // per-warp partial sums of <mu, h0>
 
     const Dims& d = a.d;
-    const int blk = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const int H = d.nheads, G = d.ngroups, hpg = H / G;
+    const int S = a.slices;
+    const int blk = blockIdx.x, g = blockIdx.y / S, slice = blockIdx.y % S, b = blockIdx.z;
+    const int H = d.nheads, G = d.ngroups, hpg = H / G, hps = hpg / S;
     const int64_t L = d.seqlen;
     const int64_t t0 = (int64_t)blk * T;
     const int64_t rowlen = (int64_t)d.nchunks * T;  // cs / dt / s / q row length per (b, h)
@@ -169,8 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     __half2 mx = __floats2half2_rn(0.f, 0.f);  // largest |value| converted to float16 (range flag)
 
 #pragma unroll 1
-    for (int k = 0; k < hpg && ok; ++k) {
-        const int h = g * hpg + k;
+    for (int k = 0; k < hps && ok; ++k) {
+        const int h = g * hpg + slice * hps + k;
         const int64_t crow = ((int64_t)b * H + h) * rowlen + t0;
         // ---- loads
         if (tid < T) scs[tid] = a.cs[crow + tid];
@@ -224,7 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         {
             // h0 and mu of (b, blk, h): (P, N) float32 -> float16 [p][n] tiles
             const int64_t srow = (((int64_t)b * d.nchunks + blk) * H + h) * (int64_t)kP * N;
-            for (int c = tid; c < kP * N / 8; c += kThreads) {
+#pragma unroll
+            for (int i = 0; i < kP * N / 8 / kThreads; ++i) {  // every load of the loop in flight at once
+                const int c = tid + i * kThreads;
                 const int p = c / (N / 8), cc = c % (N / 8);
                 const float4* hs = reinterpret_cast<const float4*>(a.h0 + srow + (int64_t)p * N + cc * 8);
                 const float4* ms = reinterpret_cast<const float4*>(a.mu + srow + (int64_t)p * N + cc * 8);
@@ -475,31 +481,80 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         }
     }
     flag_f16_range(err, hmax_to_float(mx));
-    if (ok) {
-        // dC and dB rows of this block, summed over the group's heads
-        const int64_t tok = t0 + r;
+    if (!ok && tid == 0 && pending) mbar_wait_drain(bar, phase, err, 63, kDrainNs);  // products retired first
+    const int64_t tok = t0 + r;
+    if (S == 1) {
+        if (ok) {
+            // dC and dB rows of this block, summed over the group's heads
 #pragma unroll 1
-        for (int c = 0; c < N / 64; ++c) {
-            const int n0 = hf * (N / 2) + 32 * c;
-            uint32_t vc[32], vb[32];
-            tmem_ld32(tm + lane_base + T_DC + n0, vc);
-            tmem_ld32(tm + lane_base + T_DB + n0, vb);
-            tmem_ld_wait(vc);
-            tmem_ld_wait(vb);
-            if (tok < L) {
-                float4* dc = reinterpret_cast<float4*>(a.dC + ((b * L + tok) * G + g) * (int64_t)N + n0);
-                float4* db = reinterpret_cast<float4*>(a.dB + ((b * L + tok) * G + g) * (int64_t)N + n0);
+            for (int c = 0; c < N / 64; ++c) {
+                const int n0 = hf * (N / 2) + 32 * c;
+                uint32_t vc[32], vb[32];
+                tmem_ld32(tm + lane_base + T_DC + n0, vc);
+                tmem_ld32(tm + lane_base + T_DB + n0, vb);
+                tmem_ld_wait(vc);
+                tmem_ld_wait(vb);
+                if (tok < L) {
+                    float4* dc = reinterpret_cast<float4*>(a.dC + ((b * L + tok) * G + g) * (int64_t)N + n0);
+                    float4* db = reinterpret_cast<float4*>(a.dB + ((b * L + tok) * G + g) * (int64_t)N + n0);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        dc[j] = make_float4(__uint_as_float(vc[4 * j]), __uint_as_float(vc[4 * j + 1]),
+                                            __uint_as_float(vc[4 * j + 2]), __uint_as_float(vc[4 * j + 3]));
+                        db[j] = make_float4(__uint_as_float(vb[4 * j]), __uint_as_float(vb[4 * j + 1]),
+                                            __uint_as_float(vb[4 * j + 2]), __uint_as_float(vb[4 * j + 3]));
+                    }
+                }
+            }
+        }
+    } else {
+        // this CTA's partial dC and dB -> shared memory (the tiles are consumed), float32 [2][T][NS]
+        constexpr int NS = N + 4;  // padded rows: the float4 stores of a warp fall on different banks
+        float* acc = reinterpret_cast<float*>(smem);
+        if (ok) {
+#pragma unroll 1
+            for (int c = 0; c < N / 64; ++c) {
+                const int n0 = hf * (N / 2) + 32 * c;
+                uint32_t vc[32], vb[32];
+                tmem_ld32(tm + lane_base + T_DC + n0, vc);
+                tmem_ld32(tm + lane_base + T_DB + n0, vb);
+                tmem_ld_wait(vc);
+                tmem_ld_wait(vb);
+                float4* sc = reinterpret_cast<float4*>(acc + (int64_t)r * NS + n0);
+                float4* sb = reinterpret_cast<float4*>(acc + (int64_t)(T + r) * NS + n0);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    dc[j] = make_float4(__uint_as_float(vc[4 * j]), __uint_as_float(vc[4 * j + 1]),
+                    sc[j] = make_float4(__uint_as_float(vc[4 * j]), __uint_as_float(vc[4 * j + 1]),
                                         __uint_as_float(vc[4 * j + 2]), __uint_as_float(vc[4 * j + 3]));
-                    db[j] = make_float4(__uint_as_float(vb[4 * j]), __uint_as_float(vb[4 * j + 1]),
+                    sb[j] = make_float4(__uint_as_float(vb[4 * j]), __uint_as_float(vb[4 * j + 1]),
                                         __uint_as_float(vb[4 * j + 2]), __uint_as_float(vb[4 * j + 3]));
                 }
             }
         }
-    } else if (tid == 0 && pending) {
-        mbar_wait_drain(bar, phase, err, 63, kDrainNs);  // the products issued have retired before TMEM is freed
+        tc_fence_before();
+        cluster_sync();  // every CTA's partial sums are in its shared memory
+        // this CTA adds rows [slice T / S, (slice + 1) T / S) of both over the cluster, in rank order
+        const int rows = T / S, row0 = slice * rows;
+        const uint32_t acc_s = smem_u32(acc);
+        for (int it = tid; it < 2 * rows * (N / 4); it += kThreads) {
+            const int which = it / (rows * (N / 4)), rem = it % (rows * (N / 4));
+            const int row = row0 + rem / (N / 4), c4 = rem % (N / 4);
+            const uint32_t off = (uint32_t)(((which * T + row) * NS + 4 * c4) * 4);
+            float4 sum = ld_shared_cluster_f4(map_shared_rank(acc_s + off, 0));
+            for (int k2 = 1; k2 < S; ++k2) {
+                const float4 v = ld_shared_cluster_f4(map_shared_rank(acc_s + off, (uint32_t)k2));
+                sum.x += v.x;
+                sum.y += v.y;
+                sum.z += v.z;
+                sum.w += v.w;
+            }
+            const int64_t trow = t0 + row;
+            if (ok && trow < L) {
+                float* dst = (which == 0 ? a.dC : a.dB) + ((b * L + trow) * G + g) * (int64_t)N + 4 * c4;
+                *reinterpret_cast<float4*>(dst) = sum;
+            }
+        }
+        cluster_sync();  // no CTA leaves while another still reads its shared memory
     }
     tc_fence_before();
     __syncthreads();
@@ -550,13 +605,37 @@ __global__ void __launch_bounds__(kRedThreads) bwd_reduce_kernel(const float* __
 }
 
 template <int N>
-int launch_bwd_n(const BwdArgs& a, cudaStream_t s) {
+int launch_bwd_n(const BwdArgs& a0, cudaStream_t s) {
     using K = BwdCfg<N>;
     if (ensure_smem_limit(reinterpret_cast<const void*>(bwd_chunk_kernel<N>), K::SMEM) != SSD_OK) return SSD_ERR_CUDA;
-    dim3 grid(a.d.nchunks, a.d.ngroups, a.d.batch);
+    BwdArgs a = a0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = K::SMEM;
+    cfg.stream = s;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    for (;;) {
+        cfg.gridDim = dim3(a.d.nchunks, a.d.ngroups * a.slices, a.d.batch);
+        attr.val.clusterDim.x = 1;
+        attr.val.clusterDim.y = a.slices;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = a.slices > 1 ? 1 : 0;
+        if (a.slices == 1) break;
+        // a cluster of S CTAs at this shared-memory size must fit the device; else fewer slices
+        int nclusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&nclusters, reinterpret_cast<const void*>(bwd_chunk_kernel<N>), &cfg) ==
+                cudaSuccess &&
+            nclusters > 0)
+            break;
+        cudaGetLastError();
+        a.slices /= 2;
+    }
     launch_begin(kKindBwdChunk, s);
-    bwd_chunk_kernel<N><<<grid, kThreads, K::SMEM, s>>>(a);
-    return launch_end(kKindBwdChunk, s);
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, bwd_chunk_kernel<N>, a);
+    const int r = launch_end(kKindBwdChunk, s);
+    return le != cudaSuccess ? SSD_ERR_CUDA : r;
 }
 
 }  // namespace
@@ -569,8 +648,10 @@ bool bwd_supported(const Dims& d) {
 int launch_bwd_chunk(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __half* B16, const __half* C16,
                      const float* cs, const float* dtt, const float* A, const float* D, const float* h0, const float* mu,
                      const Dims& d, __nv_bfloat16* dx, float* ddt, float* dB, float* dC, float* dap, float* xdy,
-                     const Ctl& ctl, cudaStream_t s) {
-    if (!bwd_supported(d) || d.nchunks > 2147483647 || d.ngroups > 65535 || d.batch > 65535)
+                     const Ctl& ctl, cudaStream_t s, int slices) {
+    const int hpg = d.nheads / d.ngroups;
+    if (!bwd_supported(d) || d.nchunks > 2147483647 || (int64_t)d.ngroups * slices > 65535 || d.batch > 65535 ||
+        !(slices == 1 || slices == 2 || slices == 4) || hpg % slices != 0)
         return SSD_ERR_UNSUPPORTED;
     BwdArgs a;
     a.x = x;
@@ -591,6 +672,7 @@ int launch_bwd_chunk(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __ha
     a.xdy = xdy;
     a.d = d;
     a.ctl = ctl;
+    a.slices = slices;
     return d.dstate == 64 ? launch_bwd_n<64>(a, s) : launch_bwd_n<128>(a, s);
 }
 

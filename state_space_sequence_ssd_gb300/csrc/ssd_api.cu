@@ -306,6 +306,27 @@ int forward_scan_step(const Dims& d, int span, const OutOpts& oo) {
     return best;
 }
 
+// CTAs per (block, group) of the backward kernel: the heads of a group split into S slices (a cluster
+// whose partial dB / dC are added on chip).  With one CTA per SM, S is the value of 1, 2, 4 (dividing
+// the heads per group) with the smallest estimated makespan, waves x (heads per CTA + 1): the 1 is
+// the per-CTA setup and the cluster's final sum, about one head's time.
+int bwd_slices(const Dims& d) {
+    const int sms = device_sms();
+    const int hpg = d.nheads / d.ngroups;
+    int best = 1;
+    double best_t = 0.0;
+    for (int S = 1; S <= 4; S *= 2) {
+        if (hpg % S != 0) break;
+        const int64_t ctas = (int64_t)d.nchunks * d.ngroups * S * d.batch;
+        const double t = (double)((ctas + sms - 1) / sms) * (hpg / S + 1);
+        if (S == 1 || t < best_t) {
+            best = S;
+            best_t = t;
+        }
+    }
+    return best;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- fixed scratch
@@ -664,7 +685,7 @@ int ssd_backward(const void* x, const float* dt, const float* A, const void* B, 
                                        d.nchunks, mu, dinit, stream, 1);
     if (r == SSD_OK)
         r = launch_bwd_chunk(xb, dyb, B16, C16, cs, dtt, A, D, h0, mu, d, static_cast<__nv_bfloat16*>(dx), ddt, dB, dC,
-                             dap, xdy, make_ctl(err, kKindBwdChunk), stream);
+                             dap, xdy, make_ctl(err, kKindBwdChunk), stream, bwd_slices(d));
     if (r == SSD_OK) r = launch_bwd_reduce(dap, xdy, d, dA, dD, stream);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && r == SSD_OK) r = SSD_ERR_CUDA;
     return r;

@@ -94,6 +94,7 @@ CASES = [
     ("one_token", 1, 1, 2, 64, 64, 1, 64, True, True),
     ("ragged_N64_G4", 1, 700, 8, 64, 64, 4, 128, True, False),
     ("block_edge_N128", 1, 256, 4, 64, 128, 1, 128, False, True),
+    ("groups_eq_heads", 1, 600, 4, 64, 64, 4, 64, True, True),  # one head per group: no cluster split
 ]
 
 
