@@ -37,11 +37,13 @@
 // accumulated in TMEM across them; the S CTAs of a group form a thread-block cluster and add their
 // partial dB and dC through distributed shared memory in rank order, so the result is written once,
 // without atomics and in a fixed order (S = 1: no cluster).  Per head
-// the phases run one after another: loads (x and dy to float16 tiles, the two scaled tiles
+// the phases run one after another: the conversions (x and dy to float16 tiles, the two scaled tiles
 // 2^c dy and dt 2^(c_e - c) x, h0 and mu to float16), the products C B^T and dY X^T, the mask
 // (one thread per row and column half: M' = L o C B^T and Wd to float16 tiles), the products
-// G, B mu, C h0 and the dC / dB accumulations, and the epilogue.  Operands are float16 (the
-// inputs exactly, the derived tiles rounded once), accumulation float32.
+// G, B mu, C h0 and the dC / dB accumulations, and the epilogue.  The next head's raw inputs (x and
+// dy rows, h0 and mu in float32, its dA_cumsum and dt rows) are copied with cp.async into the tiles
+// the products have finished with as soon as they retire, so their loads overlap the epilogue.
+// Operands are float16 (the inputs exactly, the derived tiles rounded once), accumulation float32.
 #include "common.cuh"
 #include "scan_util.cuh"
 #include "sm100.cuh"
@@ -66,10 +68,10 @@ struct BwdCfg {
     static constexpr int OFF_DY = OFF_X + kPanel;        // dy [t][p]
     static constexpr int OFF_DYS = OFF_DY + kPanel;      // 2^c dy
     static constexpr int OFF_XS = OFF_DYS + kPanel;      // dt 2^(c_e - c) x
-    static constexpr int OFF_H0 = OFF_XS + kPanel;       // h0 [p][n]
+    static constexpr int OFF_H0 = OFF_XS + kPanel;       // h0 [p][n]; the epilogue's reductions after the products
     static constexpr int OFF_MU = OFF_H0 + NP * kPanelP; // mu [p][n]
-    static constexpr int OFF_M = OFF_MU + NP * kPanelP;  // M' [r][i]; the epilogue's reductions after the products
-    static constexpr int OFF_W = OFF_M + 2 * kPanel;     // Wd [r][j]
+    static constexpr int OFF_M = OFF_MU + NP * kPanelP;  // M' [r][i]; the next head's raw h0 after the products
+    static constexpr int OFF_W = OFF_M + 2 * kPanel;     // Wd [r][j]; the next head's raw mu after the products
     static constexpr int OFF_CS = OFF_W + 2 * kPanel;    // cs[T], dt[T]
     static constexpr int OFF_BAR = OFF_CS + 2 * T * 4;   // two mbarriers, TMEM base, abort flag, warp sums
     static constexpr int SMEM = OFF_BAR + 128 + 1024;    // + slack to align the base to 1024 bytes
@@ -168,6 +170,34 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     bool ok = true;
     if (a.ctl.stall && tid == 0) ok = mbar_wait_bounded(stall_bar, 0, abort_flag, err, 60, wait_ns);
     ok = __syncthreads_and(ok);
+
+    // Raw inputs of head hh: its x and dy rows (bfloat16) into the swizzled positions of the XS / DYS
+    // tiles (zeros past the sequence end), h0 and mu (float32, row-major) into the M' / Wd regions, and
+    // this thread's dA_cumsum (tid < T) or dt value of the block into `csdt`.
+    auto prefetch = [&](int hh, float& csdt) {
+        const int64_t crow = ((int64_t)b * H + hh) * rowlen + t0;
+        csdt = (tid < T) ? __ldg(a.cs + crow + tid) : __ldg(a.dtt + crow + tid - T);
+#pragma unroll
+        for (int i = 0; i < T * 8 / kThreads; ++i) {
+            const int c = tid + i * kThreads;
+            const int row = c >> 3, ch = c & 7;
+            const int64_t tok = t0 + row;
+            const int64_t o = ((b * L + (tok < L ? tok : 0)) * H + hh) * (int64_t)kP + ch * 8;
+            const uint32_t nb = tok < L ? 16u : 0u;
+            cp_async16(sXS + sw128_offset(row, ch), a.x + o, nb);
+            cp_async16(sDYS + sw128_offset(row, ch), a.dy + o, nb);
+        }
+        const int64_t srow = (((int64_t)b * d.nchunks + blk) * H + hh) * (int64_t)kP * N;
+#pragma unroll
+        for (int i = 0; i < kP * N / 4 / kThreads; ++i) {
+            const int c = tid + i * kThreads;
+            cp_async16(sM + c * 16, a.h0 + srow + c * 4, 16u);
+            cp_async16(sW + c * 16, a.mu + srow + c * 4, 16u);
+        }
+        cp_async_commit();
+    };
+    float csdt = 0.f;
+    if (ok) prefetch(g * hpg + slice * hps, csdt);
     uint32_t phase = 0;
     bool pending = false;  // a commit of `bar` issued and not yet seen complete
     __half2 mx = __floats2half2_rn(0.f, 0.f);  // largest |value| converted to float16 (range flag)
@@ -175,35 +205,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
 #pragma unroll 1
     for (int k = 0; k < hps && ok; ++k) {
         const int h = g * hpg + slice * hps + k;
-        const int64_t crow = ((int64_t)b * H + h) * rowlen + t0;
-        // ---- loads
-        if (tid < T) scs[tid] = a.cs[crow + tid];
-        else sdt[tid - T] = a.dtt[crow + tid - T];
+        // ---- this head's raw inputs (copied during the previous head's epilogue) -> float16 tiles
+        cp_async_wait_all();
+        if (tid < T) scs[tid] = csdt;
+        else sdt[tid - T] = csdt;
         __syncthreads();
         const float ce = scs[T - 1];
         {
             const int rr = tid & (T - 1), hl = tid >> 7;  // row, half of the row's 64 channels
-            const int64_t tok = t0 + rr;
-            uint4 xv[4], yv[4];
-            if (tok < L) {
-                const int64_t o = ((b * L + tok) * H + h) * (int64_t)kP + 32 * hl;
-                const uint4* xs = reinterpret_cast<const uint4*>(a.x + o);
-                const uint4* ys = reinterpret_cast<const uint4*>(a.dy + o);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    xv[j] = __ldg(xs + j);
-                    yv[j] = __ldg(ys + j);
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) xv[j] = yv[j] = make_uint4(0, 0, 0, 0);
-            }
             const float wx = sdt[rr] * fast_exp2(ce - scs[rr]);
             const float wy = fast_exp2(scs[rr]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv[j]);
-                const uint32_t* yw = reinterpret_cast<const uint32_t*>(&yv[j]);
+                const uint32_t so = sw128_offset(rr, 4 * hl + j);
+                const uint4 xv = *reinterpret_cast<const uint4*>(smem + K::OFF_XS + so);
+                const uint4 yv = *reinterpret_cast<const uint4*>(smem + K::OFF_DYS + so);
+                const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+                const uint32_t* yw = reinterpret_cast<const uint32_t*>(&yv);
                 uint32_t ox[4], oxs[4], oy[4], oys[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -217,7 +235,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                 hmax_abs4(mx, oxs[0], oxs[1], oxs[2], oxs[3]);
                 hmax_abs4(mx, oy[0], oy[1], oy[2], oy[3]);
                 hmax_abs4(mx, oys[0], oys[1], oys[2], oys[3]);
-                const uint32_t so = sw128_offset(rr, 4 * hl + j);
                 *reinterpret_cast<uint4*>(smem + K::OFF_X + so) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
                 *reinterpret_cast<uint4*>(smem + K::OFF_XS + so) = make_uint4(oxs[0], oxs[1], oxs[2], oxs[3]);
                 *reinterpret_cast<uint4*>(smem + K::OFF_DY + so) = make_uint4(oy[0], oy[1], oy[2], oy[3]);
@@ -225,28 +242,26 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
             }
         }
         float hmu = 0.f;  // this thread's part of <mu, h0> (float32 values)
-        {
-            // h0 and mu of (b, blk, h): (P, N) float32 -> float16 [p][n] tiles
-            const int64_t srow = (((int64_t)b * d.nchunks + blk) * H + h) * (int64_t)kP * N;
 #pragma unroll
-            for (int i = 0; i < kP * N / 8 / kThreads; ++i) {  // every load of the loop in flight at once
-                const int c = tid + i * kThreads;
-                const int p = c / (N / 8), cc = c % (N / 8);
-                const float4* hs = reinterpret_cast<const float4*>(a.h0 + srow + (int64_t)p * N + cc * 8);
-                const float4* ms = reinterpret_cast<const float4*>(a.mu + srow + (int64_t)p * N + cc * 8);
-                const float4 h0a = __ldg(hs), h0b = __ldg(hs + 1), mua = __ldg(ms), mub = __ldg(ms + 1);
-                const uint4 oh = make_uint4(pack_f16x2(h0a.x, h0a.y), pack_f16x2(h0a.z, h0a.w), pack_f16x2(h0b.x, h0b.y),
-                                            pack_f16x2(h0b.z, h0b.w));
-                const uint4 om = make_uint4(pack_f16x2(mua.x, mua.y), pack_f16x2(mua.z, mua.w), pack_f16x2(mub.x, mub.y),
-                                            pack_f16x2(mub.z, mub.w));
-                hmu = fmaf(h0a.x, mua.x, fmaf(h0a.y, mua.y, fmaf(h0a.z, mua.z, fmaf(h0a.w, mua.w, hmu))));
-                hmu = fmaf(h0b.x, mub.x, fmaf(h0b.y, mub.y, fmaf(h0b.z, mub.z, fmaf(h0b.w, mub.w, hmu))));
-                hmax_abs4(mx, oh.x, oh.y, oh.z, oh.w);
-                hmax_abs4(mx, om.x, om.y, om.z, om.w);
-                const uint32_t so = (cc >> 3) * kPanelP + sw128_offset(p, cc & 7);
-                *reinterpret_cast<uint4*>(smem + K::OFF_H0 + so) = oh;
-                *reinterpret_cast<uint4*>(smem + K::OFF_MU + so) = om;
-            }
+        for (int i = 0; i < kP * N / 8 / kThreads; ++i) {
+            // 8 consecutive float32 of h0 and of mu (row p, columns 8 cc ..) -> one float16 chunk each
+            const int c = tid + i * kThreads;
+            const int p = c / (N / 8), cc = c % (N / 8);
+            const float4 h0a = *reinterpret_cast<const float4*>(smem + K::OFF_M + c * 32);
+            const float4 h0b = *reinterpret_cast<const float4*>(smem + K::OFF_M + c * 32 + 16);
+            const float4 mua = *reinterpret_cast<const float4*>(smem + K::OFF_W + c * 32);
+            const float4 mub = *reinterpret_cast<const float4*>(smem + K::OFF_W + c * 32 + 16);
+            const uint4 oh = make_uint4(pack_f16x2(h0a.x, h0a.y), pack_f16x2(h0a.z, h0a.w), pack_f16x2(h0b.x, h0b.y),
+                                        pack_f16x2(h0b.z, h0b.w));
+            const uint4 om = make_uint4(pack_f16x2(mua.x, mua.y), pack_f16x2(mua.z, mua.w), pack_f16x2(mub.x, mub.y),
+                                        pack_f16x2(mub.z, mub.w));
+            hmu = fmaf(h0a.x, mua.x, fmaf(h0a.y, mua.y, fmaf(h0a.z, mua.z, fmaf(h0a.w, mua.w, hmu))));
+            hmu = fmaf(h0b.x, mub.x, fmaf(h0b.y, mub.y, fmaf(h0b.z, mub.z, fmaf(h0b.w, mub.w, hmu))));
+            hmax_abs4(mx, oh.x, oh.y, oh.z, oh.w);
+            hmax_abs4(mx, om.x, om.y, om.z, om.w);
+            const uint32_t so = (cc >> 3) * kPanelP + sw128_offset(p, cc & 7);
+            *reinterpret_cast<uint4*>(smem + K::OFF_H0 + so) = oh;
+            *reinterpret_cast<uint4*>(smem + K::OFF_MU + so) = om;
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) hmu += __shfl_xor_sync(0xffffffffu, hmu, off);
@@ -355,9 +370,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         phase ^= 1;
         pending = false;
         tc_fence_after();
+        // the products have read the XS, DYS, M' and Wd tiles: the next head's raw inputs go there
+        if (k + 1 < hps) prefetch(h + 1, csdt);
         // ---- epilogue: row r, channels [32 hf, 32 hf + 32)
         {
-            float* red = reinterpret_cast<float*>(smem + K::OFF_M);  // [quantity][half][T]; M' is consumed
+            float* red = reinterpret_cast<float*>(smem + K::OFF_H0);  // [quantity][half][T]; h0 is consumed
             const int64_t tok = t0 + r;
             const float ext = fast_exp2(ce - scs[r]), dtr = sdt[r];
             const float Dh = (a.D != nullptr) ? __ldg(a.D + h) : 0.f;
@@ -481,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         }
     }
     flag_f16_range(err, hmax_to_float(mx));
+    cp_async_wait_all();  // no copy is still landing when the shared memory is reused or released
     if (!ok && tid == 0 && pending) mbar_wait_drain(bar, phase, err, 63, kDrainNs);  // products retired first
     const int64_t tok = t0 + r;
     if (S == 1) {
