@@ -89,3 +89,41 @@ def test_short_limit_alone_does_not_break_a_normal_call(ssd):
     ref = oracle.forward(n["x"], n["dt"], n["A"], n["B"], n["C"], n["D"], n["init"], w.chunk_size)
     got = np.stack([y[0, :, h].float().cpu().numpy() for h in range(w.nheads)])
     assert (np.abs(got - ref["y"]) <= 1e-2 + 1e-2 * np.abs(ref["y"])).all()
+
+
+@pytest.mark.parametrize("name", ["tiny_L512_N64", "mamba2_1p3b_layer_2x4096_N128"])
+def test_backward_stall_times_out_and_the_device_recovers(ssd, name):
+    """The backward kernel (clusters of CTAs over a group's heads at these shapes) gives up on a stalled
+    wait: every CTA still meets the cluster barriers, the host sees SSD_ERR_TIMEOUT, and the next call is
+    right."""
+    lib = _ffi.lib()
+    w = I.WORKLOADS[name]
+    inp = I.make_inputs(w, seed=43)
+    gr = I.make_grad_inputs(w, seed=43)
+    d = {k: (None if v is None else v.cuda()) for k, v in {**inp, **gr}.items()}
+
+    def backward():
+        return ssd.ssd_backward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"], d["dy"], d["dfinal"],
+                                chunk_size=w.chunk_size)
+
+    assert lib.ssd_debug_set_wait_limit_ns(2_000_000) == 0
+    assert lib.ssd_debug_stall(1 << kind(lib, "bwd_chunk")) == 0
+    try:
+        backward()
+        torch.cuda.synchronize()
+        assert ssd.ssd_get_device_error() == _ffi.SSD_ERR_TIMEOUT
+    finally:
+        lib.ssd_debug_stall(0)
+        lib.ssd_debug_set_wait_limit_ns(0)
+    assert ssd.ssd_get_device_error() == 0
+    out = backward()
+    torch.cuda.synchronize()
+    assert ssd.ssd_get_device_error() == 0
+    units = np.array([0, w.batch * w.nheads - 1])
+    n = I.as_numpy(inp)
+    g = I.as_numpy(gr)
+    r = oracle.backward(n["x"], n["dt"], n["A"], n["B"], n["C"], n["D"], n["init"], g["dy"], g["dfinal"],
+                        units=units, scales=True)
+    got = np.stack([out["dx"][u // w.nheads, :, u % w.nheads].float().cpu().numpy() for u in units])
+    err = np.abs(got - r["dx"])
+    assert (err <= 1e-2 + 1e-2 * np.abs(r["dx"]) + 2.0 ** -9 * r["dx_s"]).all(), f"dx: max err {err.max()}"
