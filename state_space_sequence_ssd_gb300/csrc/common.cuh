@@ -145,10 +145,11 @@ int launch_chunk_state_span(const __nv_bfloat16* x, const __half* B, const float
                             cudaStream_t s);
 int launch_state_passing(const float* S, const float* cs, const float* init, const Dims& d,
                          float* states, float* final_state, cudaStream_t s);
-// rev = 1: the steps run from the last to the first (the backward pass's hop, k_state_passing.cu)
+// rev = 1: the steps run from the last to the first (the backward pass's hop, k_state_passing.cu);
+// states16: the per-step states written as float16 there instead of float32 to `states` (range flag in err)
 int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_step, int64_t dec_row,
                                const float* init, const Dims& d, int nsteps, float* states, float* final_state,
-                               cudaStream_t s, int rev = 0);
+                               cudaStream_t s, int rev = 0, __half* states16 = nullptr, int* err = nullptr);
 // reverse-time chunk states for the backward pass (one-chunk spans): Z[c] = sum_t C_t 2^(cs(t)) dy_t^T
 int launch_chunk_state_rev(const __nv_bfloat16* dy, const __half* C16, const float* dtt, const float* cs, const Dims& d,
                            float* Z, const Ctl& ctl, cudaStream_t s);
@@ -170,13 +171,13 @@ int launch_chunk_scan_pair(const __nv_bfloat16* x, const __half* B, const __half
 // Backward pass (k_bwd.cu), over blocks of kBwdBlock tokens (d.chunk_size == kBwdBlock, d.nchunks blocks):
 // per (block, group, batch) the gradients of every head of the group -- split over `slices` CTAs (a
 // cluster; 1, 2 or 4, dividing the heads per group) -- from the block-start states h0
-// and the block-end gradients mu (both (b, nblk, H, P, N) f32): dx, ddt, this block's rows of dB and
+// and the block-end gradients mu (both (b, nblk, H, P, N) float16): dx, ddt, this block's rows of dB and
 // dC (summed over the group's heads), and per (b, h, block) the partial sums of dt dl (for dA) and of
 // x . dy (for dD), (b, H, nblk) f32 each.
 constexpr int kBwdBlock = 128;
 bool bwd_supported(const Dims& d);
 int launch_bwd_chunk(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __half* B16, const __half* C16,
-                     const float* cs, const float* dtt, const float* A, const float* D, const float* h0, const float* mu,
+                     const float* cs, const float* dtt, const float* A, const float* D, const __half* h0, const __half* mu,
                      const Dims& d, __nv_bfloat16* dx, float* ddt, float* dB, float* dC, float* dap, float* xdy,
                      const Ctl& ctl, cudaStream_t s, int slices);
 // dA[h] and dD[h] (dD may be null): the partial sums over batch and blocks, in a fixed order

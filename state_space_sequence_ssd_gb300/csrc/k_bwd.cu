@@ -40,9 +40,10 @@
 // the phases run one after another: the conversions (x and dy to float16 tiles, the two scaled tiles
 // 2^c dy and dt 2^(c_e - c) x, h0 and mu to float16), the products C B^T and dY X^T, the mask
 // (one thread per row and column half: M' = L o C B^T and Wd to float16 tiles), the products
-// G, B mu, C h0 and the dC / dB accumulations, and the epilogue.  The next head's raw inputs (x and
-// dy rows, h0 and mu in float32, its dA_cumsum and dt rows) are copied with cp.async into the tiles
-// the products have finished with as soon as they retire, so their loads overlap the epilogue.
+// G, B mu, C h0 and the dC / dB accumulations, and the epilogue.  The next head's inputs (raw x and
+// dy rows, its h0 and mu -- already float16, in the tiles' swizzled order -- and its dA_cumsum and dt
+// rows) are copied with cp.async into the tiles the products have finished with as soon as they
+// retire, so their loads overlap the epilogue.
 // Operands are float16 (the inputs exactly, the derived tiles rounded once), accumulation float32.
 #include "common.cuh"
 #include "scan_util.cuh"
@@ -68,10 +69,10 @@ struct BwdCfg {
     static constexpr int OFF_DY = OFF_X + kPanel;        // dy [t][p]
     static constexpr int OFF_DYS = OFF_DY + kPanel;      // 2^c dy
     static constexpr int OFF_XS = OFF_DYS + kPanel;      // dt 2^(c_e - c) x
-    static constexpr int OFF_H0 = OFF_XS + kPanel;       // h0 [p][n]; the epilogue's reductions after the products
+    static constexpr int OFF_H0 = OFF_XS + kPanel;       // h0 [p][n]
     static constexpr int OFF_MU = OFF_H0 + NP * kPanelP; // mu [p][n]
-    static constexpr int OFF_M = OFF_MU + NP * kPanelP;  // M' [r][i]; the next head's raw h0 after the products
-    static constexpr int OFF_W = OFF_M + 2 * kPanel;     // Wd [r][j]; the next head's raw mu after the products
+    static constexpr int OFF_M = OFF_MU + NP * kPanelP;  // M' [r][i]; the epilogue's reductions after the products
+    static constexpr int OFF_W = OFF_M + 2 * kPanel;     // Wd [r][j]
     static constexpr int OFF_CS = OFF_W + 2 * kPanel;    // cs[T], dt[T]
     static constexpr int OFF_BAR = OFF_CS + 2 * T * 4;   // two mbarriers, TMEM base, abort flag, warp sums
     static constexpr int SMEM = OFF_BAR + 128 + 1024;    // + slack to align the base to 1024 bytes
@@ -89,7 +90,8 @@ constexpr uint32_t kIdescP = idesc_fp16(128, 64, false, false);    // B mu, C h0
 struct BwdArgs {
     const __nv_bfloat16 *x, *dy;
     const __half *B16, *C16;
-    const float *cs, *dtt, *D, *h0, *mu;
+    const float *cs, *dtt, *D;
+    const __half *h0, *mu;  // block-start states and block-end gradients, float16 (b, nblk, H, P, N)
     const float* A;
     __nv_bfloat16* dx;
     float *ddt, *dB, *dC, *dap, *xdy;  // dap, xdy: per (b, h, block) partial sums of dt dl and x . dy
@@ -171,9 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     if (a.ctl.stall && tid == 0) ok = mbar_wait_bounded(stall_bar, 0, abort_flag, err, 60, wait_ns);
     ok = __syncthreads_and(ok);
 
-    // Raw inputs of head hh: its x and dy rows (bfloat16) into the swizzled positions of the XS / DYS
-    // tiles (zeros past the sequence end), h0 and mu (float32, row-major) into the M' / Wd regions, and
-    // this thread's dA_cumsum (tid < T) or dt value of the block into `csdt`.
+    // Inputs of head hh: its x and dy rows (bfloat16) into the swizzled positions of the XS / DYS
+    // tiles (zeros past the sequence end), h0 and mu (float16 rows p) straight into the H0 / MU tiles,
+    // and this thread's dA_cumsum (tid < T) or dt value of the block into `csdt`.
     auto prefetch = [&](int hh, float& csdt) {
         const int64_t crow = ((int64_t)b * H + hh) * rowlen + t0;
         csdt = (tid < T) ? __ldg(a.cs + crow + tid) : __ldg(a.dtt + crow + tid - T);
@@ -189,10 +191,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         }
         const int64_t srow = (((int64_t)b * d.nchunks + blk) * H + hh) * (int64_t)kP * N;
 #pragma unroll
-        for (int i = 0; i < kP * N / 4 / kThreads; ++i) {
+        for (int i = 0; i < kP * N / 8 / kThreads; ++i) {  // 16-byte chunks: 8 columns n of row p
             const int c = tid + i * kThreads;
-            cp_async16(sM + c * 16, a.h0 + srow + c * 4, 16u);
-            cp_async16(sW + c * 16, a.mu + srow + c * 4, 16u);
+            const int p = c / (N / 8), cc = c % (N / 8);
+            const uint32_t so = (cc >> 3) * kPanelP + sw128_offset(p, cc & 7);
+            cp_async16(sH0 + so, a.h0 + srow + (int64_t)c * 8, 16u);
+            cp_async16(sMU + so, a.mu + srow + (int64_t)c * 8, 16u);
         }
         cp_async_commit();
     };
@@ -241,27 +245,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                 *reinterpret_cast<uint4*>(smem + K::OFF_DYS + so) = make_uint4(oys[0], oys[1], oys[2], oys[3]);
             }
         }
-        float hmu = 0.f;  // this thread's part of <mu, h0> (float32 values)
-#pragma unroll
+        float hmu = 0.f;  // this thread's part of <mu, h0> (over the float16 tiles)
+#pragma unroll 1
         for (int i = 0; i < kP * N / 8 / kThreads; ++i) {
-            // 8 consecutive float32 of h0 and of mu (row p, columns 8 cc ..) -> one float16 chunk each
             const int c = tid + i * kThreads;
             const int p = c / (N / 8), cc = c % (N / 8);
-            const float4 h0a = *reinterpret_cast<const float4*>(smem + K::OFF_M + c * 32);
-            const float4 h0b = *reinterpret_cast<const float4*>(smem + K::OFF_M + c * 32 + 16);
-            const float4 mua = *reinterpret_cast<const float4*>(smem + K::OFF_W + c * 32);
-            const float4 mub = *reinterpret_cast<const float4*>(smem + K::OFF_W + c * 32 + 16);
-            const uint4 oh = make_uint4(pack_f16x2(h0a.x, h0a.y), pack_f16x2(h0a.z, h0a.w), pack_f16x2(h0b.x, h0b.y),
-                                        pack_f16x2(h0b.z, h0b.w));
-            const uint4 om = make_uint4(pack_f16x2(mua.x, mua.y), pack_f16x2(mua.z, mua.w), pack_f16x2(mub.x, mub.y),
-                                        pack_f16x2(mub.z, mub.w));
-            hmu = fmaf(h0a.x, mua.x, fmaf(h0a.y, mua.y, fmaf(h0a.z, mua.z, fmaf(h0a.w, mua.w, hmu))));
-            hmu = fmaf(h0b.x, mub.x, fmaf(h0b.y, mub.y, fmaf(h0b.z, mub.z, fmaf(h0b.w, mub.w, hmu))));
-            hmax_abs4(mx, oh.x, oh.y, oh.z, oh.w);
-            hmax_abs4(mx, om.x, om.y, om.z, om.w);
             const uint32_t so = (cc >> 3) * kPanelP + sw128_offset(p, cc & 7);
-            *reinterpret_cast<uint4*>(smem + K::OFF_H0 + so) = oh;
-            *reinterpret_cast<uint4*>(smem + K::OFF_MU + so) = om;
+            const uint4 hq = *reinterpret_cast<const uint4*>(smem + K::OFF_H0 + so);
+            const uint4 mq = *reinterpret_cast<const uint4*>(smem + K::OFF_MU + so);
+            const __half2* hh2 = reinterpret_cast<const __half2*>(&hq);
+            const __half2* mh2 = reinterpret_cast<const __half2*>(&mq);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 hf2 = __half22float2(hh2[e]), mf2 = __half22float2(mh2[e]);
+                hmu = fmaf(hf2.x, mf2.x, fmaf(hf2.y, mf2.y, hmu));
+            }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) hmu += __shfl_xor_sync(0xffffffffu, hmu, off);
@@ -370,11 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         phase ^= 1;
         pending = false;
         tc_fence_after();
-        // the products have read the XS, DYS, M' and Wd tiles: the next head's raw inputs go there
+        // the products have read the XS, DYS, H0 and MU tiles: the next head's inputs go there
         if (k + 1 < hps) prefetch(h + 1, csdt);
         // ---- epilogue: row r, channels [32 hf, 32 hf + 32)
         {
-            float* red = reinterpret_cast<float*>(smem + K::OFF_H0);  // [quantity][half][T]; h0 is consumed
+            float* red = reinterpret_cast<float*>(smem + K::OFF_M);  // [quantity][half][T]; M' is consumed
             const int64_t tok = t0 + r;
             const float ext = fast_exp2(ce - scs[r]), dtr = sdt[r];
             const float Dh = (a.D != nullptr) ? __ldg(a.D + h) : 0.f;
@@ -664,7 +662,7 @@ bool bwd_supported(const Dims& d) {
 }
 
 int launch_bwd_chunk(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __half* B16, const __half* C16,
-                     const float* cs, const float* dtt, const float* A, const float* D, const float* h0, const float* mu,
+                     const float* cs, const float* dtt, const float* A, const float* D, const __half* h0, const __half* mu,
                      const Dims& d, __nv_bfloat16* dx, float* ddt, float* dB, float* dC, float* dap, float* xdy,
                      const Ctl& ctl, cudaStream_t s, int slices) {
     const int hpg = d.nheads / d.ngroups;

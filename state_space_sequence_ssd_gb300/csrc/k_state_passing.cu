@@ -16,6 +16,10 @@
 // and as `final` the gradient with respect to the initial state:
 //   mu_{nc-1} = dfinal;  out[c] = mu_c;  mu_{c-1} = 2^(cs[b,h,c,Q-1]) mu_c + Z[c];  final = mu_{-1}
 //
+// With `states16` given, the per-step states are written as float16 there
+// instead (the backward pass, whose kernel reads them as tensor-core operands);
+// a value past float16's range raises the range flag of `err`.
+//
 // Every (b, h, p, n) entry is an independent lane of a serial fp32 recurrence.
 // Each thread owns 4 consecutive entries (one float4); the loop over chunks
 // keeps two groups of kUnroll chunk-state loads in flight -- the next group
@@ -36,7 +40,7 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
                                                                  int64_t dec_step, int64_t dec_row,
                                                                  const float* __restrict__ init, Dims d,
                                                                  float* states, float* __restrict__ final_state,
-                                                                 int rev) {
+                                                                 int rev, __half* states16, int* err) {
     grid_dep_wait();  // the chunk or span states come from the previous launch
     grid_dep_launch_dependents();
     const int64_t PN = (int64_t)d.headdim * d.dstate;
@@ -52,6 +56,7 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
     const int64_t cstride = (int64_t)d.hcount * PN;  // distance between consecutive chunks
     const int64_t base = ((int64_t)b * nc * d.hcount + h) * PN + e;
     // software pipeline: the next group of kUnroll steps is loaded before the current one is folded
+    float mx = 0.f;  // largest |state| written as float16
     float4 sv[kUnroll], nv[kUnroll];
     float dk[kUnroll], nd[kUnroll];
 #pragma unroll
@@ -82,7 +87,16 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
             if (c0 + k < nc) {
                 const float dd = exp2f(dk[k]);
                 const int c = rev ? nc - 1 - (c0 + k) : c0 + k;
-                *reinterpret_cast<float4*>(states + base + (int64_t)c * cstride) = hv;
+                if (states16 != nullptr) {
+                    const __half2 lo = __floats2half2_rn(hv.x, hv.y), hi = __floats2half2_rn(hv.z, hv.w);
+                    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(hv.x), fabsf(hv.y)), fmaxf(fabsf(hv.z), fabsf(hv.w))));
+                    uint2 o16;
+                    o16.x = *reinterpret_cast<const uint32_t*>(&lo);
+                    o16.y = *reinterpret_cast<const uint32_t*>(&hi);
+                    *reinterpret_cast<uint2*>(states16 + base + (int64_t)c * cstride) = o16;
+                } else {
+                    *reinterpret_cast<float4*>(states + base + (int64_t)c * cstride) = hv;
+                }
                 hv.x = fmaf(dd, hv.x, sv[k].x);
                 hv.y = fmaf(dd, hv.y, sv[k].y);
                 hv.z = fmaf(dd, hv.z, sv[k].z);
@@ -92,6 +106,7 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
     }
     if (final_state != nullptr)
         *reinterpret_cast<float4*>(final_state + ((int64_t)b * d.nheads + d.head0 + h) * PN + e) = hv;
+    if (!(mx <= kF16Max) && err != nullptr) atomicOr(err + 1, 1);  // a float16 state out of range
 }
 
 }  // namespace
@@ -105,7 +120,7 @@ int launch_state_passing(const float* S, const float* cs, const float* init, con
 
 int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_step, int64_t dec_row,
                                const float* init, const Dims& d, int nsteps, float* states, float* final_state,
-                               cudaStream_t s, int rev) {
+                               cudaStream_t s, int rev, __half* states16, int* err) {
     Dims dd = d;
     dd.nchunks = nsteps;
     const int64_t PN = (int64_t)d.headdim * d.dstate;
@@ -113,7 +128,7 @@ int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_ste
     launch_begin(kKindStatePassing, s);
     const cudaError_t le =
         launch_dependent(state_passing_kernel, grid, dim3(kThreads), 0, s, S, dec, dec_step, dec_row, init, dd, states,
-                         final_state, rev);
+                         final_state, rev, states16, err);
     const int r = launch_end(kKindStatePassing, s);
     return le != cudaSuccess ? SSD_ERR_CUDA : r;
 }
