@@ -44,7 +44,7 @@
 //               its two 128-byte rows of y
 //   warp 20     x / dA_cumsum / dt producer (TMA and bulk copies)
 //   warp 21     TMEM owner and single-thread MMA issuer, in order per sub-block
-//               (C B^T first, then S, C H^T and M X)
+//               (C B^T first, then S, C H^T, the skip term X diag(D) and M X)
 //   warp 22     B / C producer: a ring of three tile slots (B of sub-block k,
 //               C of k, B of k + 1, ...); B is released after S and C B^T, C
 //               after YS, so two sub-blocks' tiles are in flight in three slots
@@ -305,11 +305,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&bar->ys_done);
                 mma_commit(&bar->bc_empty[iC % K::NSLOT]);
-                // Y_h = M_h X_h: A = M_h from TMEM (16-column half hf of block q holds M_0 then M_1 of its 16
+                // the skip term first, Y_h = X_h diag(D_h) (the x tile read K-major), as soon as the float16
+                // x tile is written: it needs no mask, so it runs while the mask warpgroups work
+                if (!wait_bounded<false>(&bar->xf_ready, k & 1, abort_flag, err, 39, wait_ns)) break;
+                tc_fence_after();
+                const bool skip = a.D != nullptr;
+                if (skip) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t sX = smem_u32(xtile(k % K::NX, hh));
+                        const uint32_t sDg = smem_u32(smem + K::OFF_DG + hh * 8192);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tm + K::T_Y + 64 * hh, desc_sw128(sX + kk * 32, 16, 1024),
+                                   desc_sw128(sDg + kk * 32, 16, 1024), kIdescDX, kk > 0);
+                    }
+                }
+                // Y_h (+)= M_h X_h: A = M_h from TMEM (16-column half hf of block q holds M_0 then M_1 of its 16
                 // positions, 8 columns each), B = the float16 x tile of head hh (MN-major)
-                if (!wait_bounded<false>(&bar->m_ready, k & 1, abort_flag, err, 38, wait_ns) ||
-                    !wait_bounded<false>(&bar->xf_ready, k & 1, abort_flag, err, 39, wait_ns))
-                    break;
+                if (!wait_bounded<false>(&bar->m_ready, k & 1, abort_flag, err, 38, wait_ns)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -317,14 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ts(tm + K::T_Y + 64 * hh, tm + K::T_CB + 32 * (kk >> 1) + 16 * (kk & 1) + 8 * hh,
-                               desc_sw128(sX + kk * 2048, 16, 1024), kIdescMX, kk > 0);
-                    if (a.D != nullptr) {  // the skip term: Y_h += X_h diag(D_h) (the x tile read K-major)
-                        const uint32_t sDg = smem_u32(smem + K::OFF_DG + hh * 8192);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tm + K::T_Y + 64 * hh, desc_sw128(sX + kk * 32, 16, 1024),
-                                   desc_sw128(sDg + kk * 32, 16, 1024), kIdescDX, 1);
-                    }
+                               desc_sw128(sX + kk * 2048, 16, 1024), kIdescMX, skip || kk > 0);
                 }
                 mma_commit(&bar->y_full);
                 mma_commit(&bar->x_empty[k % K::NX]);
