@@ -410,11 +410,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int i = 0; i < 4; ++i) bc[i] = *reinterpret_cast<const float4*>(su + 256 + jb + 4 * i);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                m[4 * i + 0] = __uint_as_float(v[4 * i + 0]) * (arh * bc[i].x);
-                                m[4 * i + 1] = __uint_as_float(v[4 * i + 1]) * (arh * bc[i].y);
-                                m[4 * i + 2] = __uint_as_float(v[4 * i + 2]) * (arh * bc[i].z);
-                                m[4 * i + 3] = __uint_as_float(v[4 * i + 3]) * (arh * bc[i].w);
+                            for (int i = 0; i < 4; ++i) {  // packed pairs: half the multiply instructions
+                                const float2 ar2 = make_float2(arh, arh);
+                                const float2 w01 = fmul2(ar2, make_float2(bc[i].x, bc[i].y));
+                                const float2 w23 = fmul2(ar2, make_float2(bc[i].z, bc[i].w));
+                                const float2 m01 = fmul2(make_float2(__uint_as_float(v[4 * i + 0]), __uint_as_float(v[4 * i + 1])), w01);
+                                const float2 m23 = fmul2(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])), w23);
+                                m[4 * i + 0] = m01.x;
+                                m[4 * i + 1] = m01.y;
+                                m[4 * i + 2] = m23.x;
+                                m[4 * i + 3] = m23.y;
                             }
                         } else {  // steep decay in the diagonal block: the exact exponent per element
                             float4 uj[4], dj[4];

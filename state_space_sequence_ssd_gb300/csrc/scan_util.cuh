@@ -77,6 +77,17 @@ __device__ __forceinline__ void hmax_abs4(__half2& acc, uint32_t a, uint32_t b, 
     acc = __hmax2(acc, __hmax2(ab, cd));
 }
 
+// Two float32 products in one instruction (sm_100's packed two-lane multiply, round to nearest even,
+// the same result as two separate multiplies).
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 __device__ __forceinline__ float hmax_to_float(__half2 acc) {
     return fmaxf(__low2float(acc), __high2float(acc));
 }
