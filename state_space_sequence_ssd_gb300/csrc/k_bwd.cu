@@ -100,6 +100,16 @@ struct BwdArgs {
     int slices;  // S: CTAs (a cluster) per (block, group), each with hpg / S heads
 };
 
+// C B^T (K = n) of the block into its TMEM columns; one thread issues it
+template <int N>
+__device__ __forceinline__ void issue_cb(uint32_t tm, uint32_t sC, uint32_t sB) {
+#pragma unroll
+    for (int kk = 0; kk < N / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+        mma_ss(tm + T_CB, desc_sw128(sC + off, 16, 1024), desc_sw128(sB + off, 16, 1024), kIdescTT, kk > 0);
+    }
+}
+
 // bfloat16 pair (low, high) -> float2
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
     return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
@@ -202,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     };
     float csdt = 0.f;
     if (ok) prefetch(g * hpg + slice * hps, csdt);
+
     uint32_t phase = 0;
     bool pending = false;  // a commit of `bar` issued and not yet seen complete
     __half2 mx = __floats2half2_rn(0.f, 0.f);  // largest |value| converted to float16 (range flag)
@@ -267,19 +278,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        // ---- C B^T (K = n) and dY X^T (K = p)
+        // ---- C B^T (K = n; the first head only -- later heads' was issued during the previous epilogue)
+        //      and dY X^T (K = p); then the dC / dB terms that need no mask, dY' h0^T and X' mu^T (K = p),
+        //      which run while the mask works (the phase's second commit covers them)
         if (tid == 0) {
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < N / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-                mma_ss(tm + T_CB, desc_sw128(sC + off, 16, 1024), desc_sw128(sB + off, 16, 1024), kIdescTT, kk > 0);
-            }
+            if (k == 0) issue_cb<N>(tm, sC, sB);
 #pragma unroll
             for (int kk = 0; kk < kP / 16; ++kk)
                 mma_ss(tm + T_DX, desc_sw128(sDY + kk * 32, 16, 1024), desc_sw128(sX + kk * 32, 16, 1024), kIdescTT,
                        kk > 0);
             mma_commit(bar);
+#pragma unroll
+            for (int kk = 0; kk < kP / 16; ++kk) {  // K = p
+                mma_ss(tm + T_DC, desc_sw128(sDYS + kk * 32, 16, 1024), desc_sw128(sH0 + kk * 2048, kPanelP, 1024),
+                       kIdescN, k > 0 || kk > 0);
+                mma_ss(tm + T_DB, desc_sw128(sXS + kk * 32, 16, 1024), desc_sw128(sMU + kk * 2048, kPanelP, 1024),
+                       kIdescN, k > 0 || kk > 0);
+            }
         }
         pending = true;
         ok = mbar_wait_bounded(bar, phase, abort_flag, err, 61, wait_ns);
@@ -344,13 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                 const uint32_t offP = (kk >> 2) * kPanelP + (kk & 3) * 32;
                 mma_ss(tm + T_GMU, desc_sw128(sB + offT, 16, 1024), desc_sw128(sMU + offP, 16, 1024), kIdescP, kk > 0);
                 mma_ss(tm + T_YS, desc_sw128(sC + offT, 16, 1024), desc_sw128(sH0 + offP, 16, 1024), kIdescP, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < kP / 16; ++kk) {  // K = p
-                mma_ss(tm + T_DC, desc_sw128(sDYS + kk * 32, 16, 1024), desc_sw128(sH0 + kk * 2048, kPanelP, 1024),
-                       kIdescN, k > 0 || kk > 0);
-                mma_ss(tm + T_DB, desc_sw128(sXS + kk * 32, 16, 1024), desc_sw128(sMU + kk * 2048, kPanelP, 1024),
-                       kIdescN, k > 0 || kk > 0);
             }
 #pragma unroll
             for (int kk = 0; kk < T / 16; ++kk) {  // K = tokens
@@ -429,6 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
             red[(4 * 2 + hf) * T + r] = xdy;
             tc_fence_before();
             __syncthreads();
+            // every TMEM read of this head is done: the next head's C B^T (it needs only the block's B / C)
+            // runs during the rest of this epilogue and the next head's conversions
+            if (tid == 0 && k + 1 < hps) {
+                tc_fence_after();
+                issue_cb<N>(tm, sC, sB);
+            }
             float* wtot = red + 10 * T;  // per-warp totals of the scans: [v or w][warp]
             float v = 0.f, wv = 0.f, pv = 0.f, pw = 0.f, sfull = 0.f, dtl = 0.f, xd = 0.f;
             if (tid < T) {
