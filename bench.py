@@ -474,7 +474,7 @@ def pass_traffic(w: I.Workload, kernels: dict):
 KERNEL_SOURCES = {"chunk_cumsum": ["k_cumsum.cu"], "chunk_state": ["k_chunk_state.cu"],
                   "state_passing": ["k_state_passing.cu"],
                   "chunk_scan": ["k_chunk_scan.cu", "k_chunk_scan_pair.cu", "scan_util.cuh"],
-                  "step": ["k_step.cu"]}
+                  "step": ["k_step.cu"], "bwd_chunk": ["k_bwd.cu", "scan_util.cuh"]}
 
 
 def kernel_traffic(name: str, w: I.Workload):
@@ -772,7 +772,7 @@ def backward_measure(w, d, dev, stream, args, ssd, lib, flush):
                            "unit": "TFLOP/s", "frac": round(ach / tf, 4),
                            "peak_source": "measured bf16_tflops (cuBLAS burst); fp16 has the same dense rate",
                            "alg_flops_per_launch": fl["bwd_chunk"], "avg_launch_us": bk["us_per_launch"],
-                           "traffic": None}
+                           "traffic": kernel_traffic("bwd_chunk", w)}
     return res
 
 
