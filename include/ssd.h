@@ -272,7 +272,8 @@ SSD_API int ssd_forward_noalloc(const void* x, const float* dt, const float* A, 
  * heads on tcgen05 tensor cores (every sum of the dt gradient kept inside a
  * block), and a fixed-order reduction of the per-block parts of dA and dD.
  * Operands of the products are float16 (as in ssd_forward), accumulation
- * float32.
+ * float32; the hops read each block's own term as float16 and carry the
+ * recurrence in float32.
  *
  * Inputs: as ssd_forward (x, B, C bf16; dt, A, D, init_state f32; D and
  * init_state nullable), dy (batch, seqlen, nheads, headdim) bf16, dfinal
@@ -287,7 +288,7 @@ SSD_API int ssd_forward_noalloc(const void* x, const float* dt, const float* A, 
  * x, B, C, dy, dx, dB, dC, init_state, dfinal and dinit 16-byte aligned; the
  * other pointers 4-byte aligned.  Supported: headdim 64, dstate 64 or 128,
  * otherwise the shape limits of ssd_forward (SSD_ERR_UNSUPPORTED).  The
- * workspace (about 2 x batch x nheads x headdim x dstate x 4 bytes per 128
+ * workspace (about 3 x batch x nheads x headdim x dstate x 2 bytes per 128
  * tokens, plus float16 copies of B and C) is allocated stream-ordered from
  * the library's pool.  Deterministic: no atomics; dB and dC are summed over
  * a group's heads in a fixed order.  Errors: SSD_ERR_INVALID_ARG,

@@ -140,19 +140,22 @@ int launch_chunk_cumsum_bc(const float* dt, const float* A, const Dims& d, float
 int launch_bc_to_f16(const __nv_bfloat16* B, const __nv_bfloat16* C, const Dims& d, __half* B16, __half* C16,
                      int* err, cudaStream_t s);
 // B and C below are the float16 copies; x stays bfloat16.
+// S16: the span states written as float16 there instead of float32 to S (range flag in ctl.err)
 int launch_chunk_state_span(const __nv_bfloat16* x, const __half* B, const float* dtt, const float* cs,
                             int span_chunks, const Dims& d, float* S, float* span_decay, const Ctl& ctl,
-                            cudaStream_t s);
+                            cudaStream_t s, __half* S16 = nullptr);
 int launch_state_passing(const float* S, const float* cs, const float* init, const Dims& d,
                          float* states, float* final_state, cudaStream_t s);
 // rev = 1: the steps run from the last to the first (the backward pass's hop, k_state_passing.cu);
-// states16: the per-step states written as float16 there instead of float32 to `states` (range flag in err)
+// states16: the per-step states written as float16 there instead of float32 to `states` (range flag in err);
+// S16: the per-step terms read as float16 from there instead of float32 from S
 int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_step, int64_t dec_row,
                                const float* init, const Dims& d, int nsteps, float* states, float* final_state,
-                               cudaStream_t s, int rev = 0, __half* states16 = nullptr, int* err = nullptr);
+                               cudaStream_t s, int rev = 0, __half* states16 = nullptr, int* err = nullptr,
+                               const __half* S16 = nullptr);
 // reverse-time chunk states for the backward pass (one-chunk spans): Z[c] = sum_t C_t 2^(cs(t)) dy_t^T
 int launch_chunk_state_rev(const __nv_bfloat16* dy, const __half* C16, const float* dtt, const float* cs, const Dims& d,
-                           float* Z, const Ctl& ctl, cudaStream_t s);
+                           float* Z, const Ctl& ctl, cudaStream_t s, __half* Z16 = nullptr);
 // span_states holds one state per span of `span_chunks` chunks; chunk_scan walks spans of
 // span_chunks * state_step chunks, each starting from every state_step-th of those states.
 int launch_chunk_scan_span(const __nv_bfloat16* x, const __half* B, const __half* C,

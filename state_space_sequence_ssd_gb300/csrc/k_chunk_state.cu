@@ -79,6 +79,7 @@ struct StateArgs {
     const float* cs;    // (b, hcount, nc, Q)
     const float* dtt;   // (b, hcount, nc, Q)
     float* S;           // (b, nspans, hcount, P, N)
+    __half* S16;        // the same as float16 instead, or null
     float* span_decay;  // (b, hcount, nspans) log2 units, or null
     Ctl ctl;            // error words, wait limit, stall hook
     int rev;            // reverse-time weights (one-chunk spans): w_t = 2^(cs(t)), no dt factor
@@ -276,9 +277,10 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
         tc_fence_after();
         if (ok) {
             const int64_t PN = (int64_t)d.headdim * N;
+            float smx = 0.f;  // largest |state| written as float16
 #pragma unroll 1
             for (int hh = hsel; hh < HH; hh += K::SW) {
-                float* out = a.S + (((int64_t)b * a.nspans + s) * HC + h0 + hh) * PN;
+                const int64_t o = (((int64_t)b * a.nspans + s) * HC + h0 + hh) * PN;
 #pragma unroll 1
                 for (int mb = 0; mb < K::MB; ++mb) {
                     const int n = mb * 128 + r;
@@ -288,12 +290,24 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
                         tmem_ld32(tm + lane_base + mb * 64 * HH + hh * 64 + half * 32, v);
                         tmem_ld_wait(v);
                         if (n < N) {
+                            if (a.S16 != nullptr) {
+                                __half* out = a.S16 + o;
 #pragma unroll
-                            for (int p = 0; p < 32; ++p) out[(int64_t)(half * 32 + p) * N + n] = __uint_as_float(v[p]);
+                                for (int p = 0; p < 32; ++p) {
+                                    const float f = __uint_as_float(v[p]);
+                                    smx = fmaxf(smx, fabsf(f));
+                                    out[(int64_t)(half * 32 + p) * N + n] = __float2half_rn(f);
+                                }
+                            } else {
+                                float* out = a.S + o;
+#pragma unroll
+                                for (int p = 0; p < 32; ++p) out[(int64_t)(half * 32 + p) * N + n] = __uint_as_float(v[p]);
+                            }
                         }
                     }
                 }
             }
+            flag_f16_range(err, smx);
         }
     }
     tc_fence_before();
@@ -336,7 +350,7 @@ int launch_state_n(const __nv_bfloat16* x, const __half* B, const StateArgs& a, 
 
 int launch_chunk_state_span(const __nv_bfloat16* x, const __half* B, const float* dtt, const float* cs,
                             int span_chunks, const Dims& d, float* S, float* span_decay, const Ctl& ctl,
-                            cudaStream_t s) {
+                            cudaStream_t s, __half* S16) {
     if (span_chunks < 1 || span_chunks > kMaxSpanChunks) return SSD_ERR_UNSUPPORTED;
     StateArgs a;
     a.d = d;
@@ -345,6 +359,7 @@ int launch_chunk_state_span(const __nv_bfloat16* x, const __half* B, const float
     a.cs = cs;
     a.dtt = dtt;
     a.S = S;
+    a.S16 = S16;
     a.span_decay = span_decay;
     a.ctl = ctl;
     a.rev = 0;
@@ -358,7 +373,7 @@ int launch_chunk_state_span(const __nv_bfloat16* x, const __half* B, const float
 }
 
 int launch_chunk_state_rev(const __nv_bfloat16* dy, const __half* C16, const float* dtt, const float* cs, const Dims& d,
-                           float* Z, const Ctl& ctl, cudaStream_t s) {
+                           float* Z, const Ctl& ctl, cudaStream_t s, __half* Z16) {
     StateArgs a;
     a.d = d;
     a.span_chunks = 1;
@@ -366,6 +381,7 @@ int launch_chunk_state_rev(const __nv_bfloat16* dy, const __half* C16, const flo
     a.cs = cs;
     a.dtt = dtt;
     a.S = Z;
+    a.S16 = Z16;
     a.span_decay = nullptr;
     a.ctl = ctl;
     a.rev = 1;

@@ -18,14 +18,17 @@
 //
 // With `states16` given, the per-step states are written as float16 there
 // instead (the backward pass, whose kernel reads them as tensor-core operands);
-// a value past float16's range raises the range flag of `err`.
+// a value past float16's range raises the range flag of `err`.  With `S16`
+// given, the per-step terms are read as float16 from there (the backward
+// pass's per-block terms; the recurrence itself stays float32).
 //
 // Every (b, h, p, n) entry is an independent lane of a serial fp32 recurrence.
 // Each thread owns 4 consecutive entries (one float4); the loop over chunks
-// keeps two groups of kUnroll chunk-state loads in flight -- the next group
-// is requested before the current one is folded -- so the memory system
-// always has independent requests outstanding (the loads of S do not depend
-// on the carried state).  `states` may alias `S`: every element is
+// keeps two groups of U chunk-state loads in flight -- the next group is
+// requested before the current one is folded -- so the memory system always
+// has independent requests outstanding (the loads of S do not depend on the
+// carried state).  U = 8 for float32 terms and 16 for float16 ones, so that
+// a thread keeps the same bytes in flight.  `states` may alias `S`: every element is
 // read before the same element is written.
 #include "common.cuh"
 
@@ -33,10 +36,33 @@ namespace ssd {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 8;
+
+// four consecutive per-step terms as loaded: float32, or float16 (H16) kept packed until they are folded
+template <bool H16>
+struct Term {
+    using T = float4;
+    static __device__ __forceinline__ T load(const float* S, const __half*, int64_t i) {
+        return *reinterpret_cast<const float4*>(S + i);
+    }
+    static __device__ __forceinline__ float4 widen(const T& v) { return v; }
+};
+template <>
+struct Term<true> {
+    using T = uint2;
+    static __device__ __forceinline__ T load(const float*, const __half* S16, int64_t i) {
+        return *reinterpret_cast<const uint2*>(S16 + i);
+    }
+    static __device__ __forceinline__ float4 widen(const T& u) {
+        const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        return make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+};
 
 // dec: log2 decay of step c for row (b, h) at dec[row * dec_row + c * dec_step]
-__global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S, const float* __restrict__ dec,
+template <bool H16>
+__global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S, const __half* S16,
+                                                                 const float* __restrict__ dec,
                                                                  int64_t dec_step, int64_t dec_row,
                                                                  const float* __restrict__ init, Dims d,
                                                                  float* states, float* __restrict__ final_state,
@@ -56,14 +82,15 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
     const int64_t cstride = (int64_t)d.hcount * PN;  // distance between consecutive chunks
     const int64_t base = ((int64_t)b * nc * d.hcount + h) * PN + e;
     // software pipeline: the next group of kUnroll steps is loaded before the current one is folded
+    constexpr int kUnroll = H16 ? 16 : 8;
     float mx = 0.f;  // largest |state| written as float16
-    float4 sv[kUnroll], nv[kUnroll];
+    typename Term<H16>::T sv[kUnroll], nv[kUnroll];
     float dk[kUnroll], nd[kUnroll];
 #pragma unroll
     for (int k = 0; k < kUnroll; ++k) {
         if (k < nc) {
             const int c = rev ? nc - 1 - k : k;
-            nv[k] = *reinterpret_cast<const float4*>(S + base + (int64_t)c * cstride);
+            nv[k] = Term<H16>::load(S, S16, base + (int64_t)c * cstride);
             nd[k] = __ldg(csl + (int64_t)c * dec_step);
         }
     }
@@ -78,7 +105,7 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
             const int cn = c0 + kUnroll + k;
             if (cn < nc) {
                 const int c = rev ? nc - 1 - cn : cn;
-                nv[k] = *reinterpret_cast<const float4*>(S + base + (int64_t)c * cstride);
+                nv[k] = Term<H16>::load(S, S16, base + (int64_t)c * cstride);
                 nd[k] = __ldg(csl + (int64_t)c * dec_step);
             }
         }
@@ -97,10 +124,11 @@ __global__ void __launch_bounds__(kThreads) state_passing_kernel(const float* S,
                 } else {
                     *reinterpret_cast<float4*>(states + base + (int64_t)c * cstride) = hv;
                 }
-                hv.x = fmaf(dd, hv.x, sv[k].x);
-                hv.y = fmaf(dd, hv.y, sv[k].y);
-                hv.z = fmaf(dd, hv.z, sv[k].z);
-                hv.w = fmaf(dd, hv.w, sv[k].w);
+                const float4 tv = Term<H16>::widen(sv[k]);
+                hv.x = fmaf(dd, hv.x, tv.x);
+                hv.y = fmaf(dd, hv.y, tv.y);
+                hv.z = fmaf(dd, hv.z, tv.z);
+                hv.w = fmaf(dd, hv.w, tv.w);
             }
         }
     }
@@ -120,15 +148,18 @@ int launch_state_passing(const float* S, const float* cs, const float* init, con
 
 int launch_state_passing_steps(const float* S, const float* dec, int64_t dec_step, int64_t dec_row,
                                const float* init, const Dims& d, int nsteps, float* states, float* final_state,
-                               cudaStream_t s, int rev, __half* states16, int* err) {
+                               cudaStream_t s, int rev, __half* states16, int* err, const __half* S16) {
     Dims dd = d;
     dd.nchunks = nsteps;
     const int64_t PN = (int64_t)d.headdim * d.dstate;
     dim3 grid((unsigned)ceil_div64(PN, (int64_t)kThreads * 4), d.hcount, d.batch);
     launch_begin(kKindStatePassing, s);
     const cudaError_t le =
-        launch_dependent(state_passing_kernel, grid, dim3(kThreads), 0, s, S, dec, dec_step, dec_row, init, dd, states,
-                         final_state, rev, states16, err);
+        S16 != nullptr
+            ? launch_dependent(state_passing_kernel<true>, grid, dim3(kThreads), 0, s, S, S16, dec, dec_step, dec_row,
+                               init, dd, states, final_state, rev, states16, err)
+            : launch_dependent(state_passing_kernel<false>, grid, dim3(kThreads), 0, s, S, S16, dec, dec_step, dec_row,
+                               init, dd, states, final_state, rev, states16, err);
     const int r = launch_end(kKindStatePassing, s);
     return le != cudaSuccess ? SSD_ERR_CUDA : r;
 }

@@ -659,17 +659,17 @@ int ssd_backward(const void* x, const float* dt, const float* A, const void* B, 
     const size_t nst = (size_t)d.batch * d.nchunks * d.nheads * d.headdim * d.dstate;  // per-block states
     const size_t npart = ((size_t)d.batch * d.nheads * d.nchunks + 3) & ~(size_t)3;  // per-block partial sums
     const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;  // multiple of 64
-    const size_t bytes = (2 * nrow + nst + 2 * npart) * sizeof(float) + (2 * nst + 2 * nbc) * sizeof(__half);
+    const size_t bytes = (2 * nrow + 2 * npart) * sizeof(float) + (3 * nst + 2 * nbc) * sizeof(__half);
     void* ws = nullptr;
     if (workspace_alloc(&ws, bytes, stream) != SSD_OK) return SSD_ERR_NO_MEMORY;
     float* cs = static_cast<float*>(ws);
     float* dtt = cs + nrow;
-    float* S = dtt + nrow;  // the blocks' own states, then the blocks' own reverse-time terms (float32)
-    float* dap = S + nst;
+    float* dap = dtt + nrow;
     float* xdy = dap + npart;
     __half* h0 = reinterpret_cast<__half*>(xdy + npart);  // block-start states (float16)
     __half* mu = h0 + nst;                                // block-end gradients (float16)
-    __half* B16 = mu + nst;
+    __half* S16 = mu + nst;  // the blocks' own states, then their own reverse-time terms (float16; the hops add in f32)
+    __half* B16 = S16 + nst;
     __half* C16 = B16 + nbc;
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     const __nv_bfloat16* dyb = static_cast<const __nv_bfloat16*>(dy);
@@ -677,15 +677,17 @@ int ssd_backward(const void* x, const float* dt, const float* A, const void* B, 
     r = launch_chunk_cumsum_bc(dt, A, d, cs, dtt, static_cast<const __nv_bfloat16*>(B),
                                static_cast<const __nv_bfloat16*>(C), B16, C16, err, stream);
     if (r == SSD_OK)
-        r = launch_chunk_state_span(xb, B16, dtt, cs, 1, d, S, nullptr, make_ctl(err, kKindChunkState), stream);
+        r = launch_chunk_state_span(xb, B16, dtt, cs, 1, d, nullptr, nullptr, make_ctl(err, kKindChunkState), stream,
+                                    S16);
     if (r == SSD_OK)
-        r = launch_state_passing_steps(S, cs + (kBwdBlock - 1), kBwdBlock, (int64_t)d.nchunks * kBwdBlock, init_state,
-                                       d, d.nchunks, nullptr, nullptr, stream, 0, h0, err);
+        r = launch_state_passing_steps(nullptr, cs + (kBwdBlock - 1), kBwdBlock, (int64_t)d.nchunks * kBwdBlock,
+                                       init_state, d, d.nchunks, nullptr, nullptr, stream, 0, h0, err, S16);
     // reverse hop: the gradient flowing into the state after every block, and dinit
-    if (r == SSD_OK) r = launch_chunk_state_rev(dyb, C16, dtt, cs, d, S, make_ctl(err, kKindChunkState), stream);
     if (r == SSD_OK)
-        r = launch_state_passing_steps(S, cs + (kBwdBlock - 1), kBwdBlock, (int64_t)d.nchunks * kBwdBlock, dfinal, d,
-                                       d.nchunks, nullptr, dinit, stream, 1, mu, err);
+        r = launch_chunk_state_rev(dyb, C16, dtt, cs, d, nullptr, make_ctl(err, kKindChunkState), stream, S16);
+    if (r == SSD_OK)
+        r = launch_state_passing_steps(nullptr, cs + (kBwdBlock - 1), kBwdBlock, (int64_t)d.nchunks * kBwdBlock,
+                                       dfinal, d, d.nchunks, nullptr, dinit, stream, 1, mu, err, S16);
     if (r == SSD_OK)
         r = launch_bwd_chunk(xb, dyb, B16, C16, cs, dtt, A, D, h0, mu, d, static_cast<__nv_bfloat16*>(dx), ddt, dB, dC,
                              dap, xdy, make_ctl(err, kKindBwdChunk), stream, bwd_slices(d));
