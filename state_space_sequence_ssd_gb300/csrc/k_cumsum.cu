@@ -9,7 +9,8 @@
 // one pair of 16-byte loads per token row into shared memory; each warp then
 // scans one head along the chunk (each lane owns Q/32 consecutive positions:
 // serial in-lane prefix + warp-shuffle scan of the lane totals) and writes
-// its (batch, H, nchunks, Q) rows with 16-byte stores.
+// its (batch, H, nchunks, Q) rows through its tile row, each store instruction
+// covering 512 contiguous bytes.
 //
 // With a layer's input-side options the dt tile is transformed as it is read
 // (bias, softplus, clamp), so dt_t and every later stage see the effective dt.
@@ -165,13 +166,26 @@ __global__ void __launch_bounds__(kThreads) chunk_cumsum_kernel(const float* __r
         if (lane >= off) tot += o;
     }
     const float excl = tot - run;
-    const int64_t row = (((int64_t)b * d.hcount + h) * d.nchunks + c) * Q + lane * kPer;
+    // both rows leave through the warp's tile row, so that each store instruction writes 512 whole
+    // bytes or the whole row (lane l: positions 4 l .. 4 l + 3 of every 128): first dt, then the cumsum
+    const int64_t row = (((int64_t)b * d.hcount + h) * d.nchunks + c) * Q;
+    float* trow = tile[warp];
+    auto store_row = [&](float* dst) {
 #pragma unroll
-    for (int k = 0; k < kPer; k += 2) {
-        const int p0 = lane * kPer + k, p1 = p0 + 1;
-        *reinterpret_cast<float2*>(cs + row + k) = make_float2((v[k] + excl) * kLog2e, (v[k + 1] + excl) * kLog2e);
-        *reinterpret_cast<float2*>(dtt + row + k) = make_float2(tile[warp][p0 + (p0 >> 3)], tile[warp][p1 + (p1 >> 3)]);
+        for (int p = 4 * lane; p < Q; p += 128) {  // p .. p + 3 share one padded group of 8
+            const float* t = trow + p + (p >> 3);
+            *reinterpret_cast<float4*>(dst + row + p) = make_float4(t[0], t[1], t[2], t[3]);
+        }
+    };
+    store_row(dtt);
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int pos = lane * kPer + k;
+        trow[pos + (pos >> 3)] = (v[k] + excl) * kLog2e;
     }
+    __syncwarp();
+    store_row(cs);
 }
 
 }  // namespace
