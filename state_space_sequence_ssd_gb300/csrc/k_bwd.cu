@@ -39,7 +39,7 @@
 // without atomics and in a fixed order (S = 1: no cluster).  Per head
 // the phases run one after another: the conversions (x and dy to float16 tiles, the two scaled tiles
 // 2^c dy and dt 2^(c_e - c) x, h0 and mu to float16), the products C B^T and dY X^T, the mask
-// (one thread per row and column half: M' = L o C B^T and Wd to float16 tiles), the products
+// (one thread per row and column quarter: M' = L o C B^T and Wd to float16 tiles), the products
 // G, B mu, C h0 and the dC / dB accumulations, and the epilogue.  The next head's inputs (raw x and
 // dy rows, its h0 and mu -- already float16, in the tiles' swizzled order -- and its dA_cumsum and dt
 // rows) are copied with cp.async into the tiles the products have finished with as soon as they
@@ -56,7 +56,8 @@ using namespace sm100;
 
 constexpr int T = kBwdBlock;     // tokens per block = the products' M
 constexpr int kP = 64;           // headdim
-constexpr int kThreads = 256;    // two warpgroups: warp w owns TMEM lanes 32 (w % 4) .. +31, column half w / 4
+constexpr int kThreads = 512;    // four warpgroups: warp w owns TMEM lanes 32 (w % 4) .. +31, column quarter w / 4
+constexpr int kNQ = kThreads / 128;  // column quarters of a row (mask, epilogue) and row parts (conversions)
 constexpr int kPanel = T * 128;  // one 64-column float16 panel of a T-row tile (16 KB)
 constexpr int kPanelP = kP * 128;  // one 64-column float16 panel of a P-row tile (8 KB)
 
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     uint64_t* stall_bar = bar + 1;  // never completed: the test hook's wait runs out on it
     uint32_t* tmem_sh = reinterpret_cast<uint32_t*>(bar + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 3);
-    float* wsum = reinterpret_cast<float*>(bar + 4);  // per-warp partial sums of <mu, h0>
+    float* wsum = reinterpret_cast<float*>(bar + 4);  // per-warp partial sums of <mu, h0> (16 floats)
 
     const Dims& d = a.d;
     const int S = a.slices;
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     const int64_t t0 = (int64_t)blk * T;
     const int64_t rowlen = (int64_t)d.nchunks * T;  // cs / dt / s / q row length per (b, h)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qw = warp & 3, hf = warp >> 2;         // TMEM lane quarter, column half
+    const int qw = warp & 3, qc = warp >> 2;         // TMEM lane quarter, column quarter
     const int r = 32 * qw + lane;                    // this thread's row in the mask and the epilogue
     const uint32_t lane_base = (uint32_t)(32 * qw) << 16;
     int* const err = a.ctl.err;
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     // and this thread's dA_cumsum (tid < T) or dt value of the block into `csdt`.
     auto prefetch = [&](int hh, float& csdt) {
         const int64_t crow = ((int64_t)b * H + hh) * rowlen + t0;
-        csdt = (tid < T) ? __ldg(a.cs + crow + tid) : __ldg(a.dtt + crow + tid - T);
+        if (tid < 2 * T) csdt = (tid < T) ? __ldg(a.cs + crow + tid) : __ldg(a.dtt + crow + tid - T);
 #pragma unroll
         for (int i = 0; i < T * 8 / kThreads; ++i) {
             const int c = tid + i * kThreads;
@@ -223,16 +224,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         // ---- this head's raw inputs (copied during the previous head's epilogue) -> float16 tiles
         cp_async_wait_all();
         if (tid < T) scs[tid] = csdt;
-        else sdt[tid - T] = csdt;
+        else if (tid < 2 * T) sdt[tid - T] = csdt;
         __syncthreads();
         const float ce = scs[T - 1];
         {
-            const int rr = tid & (T - 1), hl = tid >> 7;  // row, half of the row's 64 channels
+            const int rr = tid & (T - 1), hl = tid >> 7;  // row, quarter of the row's 64 channels
             const float wx = sdt[rr] * fast_exp2(ce - scs[rr]);
             const float wy = fast_exp2(scs[rr]);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t so = sw128_offset(rr, 4 * hl + j);
+            for (int j = 0; j < 8 / kNQ; ++j) {
+                const uint32_t so = sw128_offset(rr, (8 / kNQ) * hl + j);
                 const uint4 xv = *reinterpret_cast<const uint4*>(smem + K::OFF_XS + so);
                 const uint4 yv = *reinterpret_cast<const uint4*>(smem + K::OFF_DYS + so);
                 const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
@@ -304,21 +305,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         phase ^= 1;
         pending = false;
         tc_fence_after();
-        // ---- mask: row r, columns [64 hf, 64 hf + 64) of M' = L o C B^T and Wd = L o dY X^T o dt_j
-        float rho1 = 0.f;  // sum_j Wd[r][j] (C_r . B_j) over this half
+        // ---- mask: row r, columns [32 qc, 32 qc + 32) of M' = L o C B^T and Wd = L o dY X^T o dt_j,
+        //      16 at a time
+        float rho1 = 0.f;  // sum_j Wd[r][j] (C_r . B_j) over this quarter
         {
             const float cr = scs[r];
 #pragma unroll 1
             for (int c2 = 0; c2 < 2; ++c2) {
-                const int i0 = 64 * hf + 32 * c2;
-                uint32_t vcb[32], vdx[32];
-                tmem_ld32(tm + lane_base + T_CB + i0, vcb);
-                tmem_ld32(tm + lane_base + T_DX + i0, vdx);
-                tmem_ld_wait(vcb);
-                tmem_ld_wait(vdx);
-                uint32_t pm[16], pw[16];
+                const int i0 = 32 * qc + 16 * c2;
+                uint32_t vcb[16], vdx[16];
+                tmem_ld16(tm + lane_base + T_CB + i0, vcb);
+                tmem_ld16(tm + lane_base + T_DX + i0, vdx);
+                tmem_ld_wait16(vcb);
+                tmem_ld_wait16(vdx);
+                uint32_t pm[8], pw[8];
 #pragma unroll
-                for (int jj = 0; jj < 32; jj += 2) {
+                for (int jj = 0; jj < 16; jj += 2) {
                     float mv[2], wv[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
@@ -333,10 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                     pw[jj / 2] = pack_f16x2(wv[0], wv[1]);
                 }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < 2; ++j) {  // columns i0 .. i0 + 15: panel qc / 2, chunks 4 (qc % 2) + 2 c2 + j
                     hmax_abs4(mx, pm[4 * j], pm[4 * j + 1], pm[4 * j + 2], pm[4 * j + 3]);
                     hmax_abs4(mx, pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
-                    const uint32_t so = hf * kPanel + sw128_offset(r, 4 * c2 + j);
+                    const uint32_t so = (qc >> 1) * kPanel + sw128_offset(r, 4 * (qc & 1) + 2 * c2 + j);
                     *reinterpret_cast<uint4*>(smem + K::OFF_M + so) =
                         make_uint4(pm[4 * j], pm[4 * j + 1], pm[4 * j + 2], pm[4 * j + 3]);
                     *reinterpret_cast<uint4*>(smem + K::OFF_W + so) =
@@ -379,23 +381,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         tc_fence_after();
         // the products have read the XS, DYS, H0 and MU tiles: the next head's inputs go there
         if (k + 1 < hps) prefetch(h + 1, csdt);
-        // ---- epilogue: row r, channels [32 hf, 32 hf + 32)
+        // ---- epilogue: row r, channels [16 qc, 16 qc + 16)
         {
-            float* red = reinterpret_cast<float*>(smem + K::OFF_M);  // [quantity][half][T]; M' is consumed
+            float* red = reinterpret_cast<float*>(smem + K::OFF_M);  // [quantity][quarter][T]; M' is consumed
             const int64_t tok = t0 + r;
             const float ext = fast_exp2(ce - scs[r]), dtr = sdt[r];
             const float Dh = (a.D != nullptr) ? __ldg(a.D + h) : 0.f;
-            uint32_t vg[32], vm[32];
-            tmem_ld32(tm + lane_base + T_G + 32 * hf, vg);
-            tmem_ld32(tm + lane_base + T_GMU + 32 * hf, vm);
-            tmem_ld_wait(vg);
-            tmem_ld_wait(vm);
+            uint32_t vg[16], vm[16];
+            tmem_ld16(tm + lane_base + T_G + 16 * qc, vg);
+            tmem_ld16(tm + lane_base + T_GMU + 16 * qc, vm);
+            tmem_ld_wait16(vg);
+            tmem_ld_wait16(vm);
             float sg = 0.f, sm = 0.f, xdy = 0.f;  // x . G (pairs in the block), x . B mu, x . dy
-            uint32_t ob[16];
+            uint32_t ob[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint4 xq = *reinterpret_cast<const uint4*>(smem + K::OFF_X + sw128_offset(r, 4 * hf + j));
-                const uint4 yq = *reinterpret_cast<const uint4*>(smem + K::OFF_DY + sw128_offset(r, 4 * hf + j));
+            for (int j = 0; j < 2; ++j) {
+                const uint4 xq = *reinterpret_cast<const uint4*>(smem + K::OFF_X + sw128_offset(r, 2 * qc + j));
+                const uint4 yq = *reinterpret_cast<const uint4*>(smem + K::OFF_DY + sw128_offset(r, 2 * qc + j));
                 const __half2* xh = reinterpret_cast<const __half2*>(&xq);
                 const __half2* yh = reinterpret_cast<const __half2*>(&yq);
 #pragma unroll
@@ -412,17 +414,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                 }
             }
             if (tok < L) {
-                uint4* dst = reinterpret_cast<uint4*>(a.dx + ((b * L + tok) * H + h) * (int64_t)kP + 32 * hf);
+                uint4* dst = reinterpret_cast<uint4*>(a.dx + ((b * L + tok) * H + h) * (int64_t)kP + 16 * qc);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) dst[j] = make_uint4(ob[4 * j], ob[4 * j + 1], ob[4 * j + 2], ob[4 * j + 3]);
+                for (int j = 0; j < 2; ++j) dst[j] = make_uint4(ob[4 * j], ob[4 * j + 1], ob[4 * j + 2], ob[4 * j + 3]);
             }
-            uint32_t vy[32];
-            tmem_ld32(tm + lane_base + T_YS + 32 * hf, vy);
-            tmem_ld_wait(vy);
-            float rho2 = 0.f;  // dy_r . (C_r h0) over this half
+            uint32_t vy[16];
+            tmem_ld16(tm + lane_base + T_YS + 16 * qc, vy);
+            tmem_ld_wait16(vy);
+            float rho2 = 0.f;  // dy_r . (C_r h0) over this quarter
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint4 yq = *reinterpret_cast<const uint4*>(smem + K::OFF_DY + sw128_offset(r, 4 * hf + j));
+            for (int j = 0; j < 2; ++j) {
+                const uint4 yq = *reinterpret_cast<const uint4*>(smem + K::OFF_DY + sw128_offset(r, 2 * qc + j));
                 const __half2* yh = reinterpret_cast<const __half2*>(&yq);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -431,11 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                     rho2 = fmaf(yf.x, __uint_as_float(vy[c]), fmaf(yf.y, __uint_as_float(vy[c + 1]), rho2));
                 }
             }
-            red[(0 * 2 + hf) * T + r] = sg;
-            red[(1 * 2 + hf) * T + r] = sm;
-            red[(2 * 2 + hf) * T + r] = rho2;
-            red[(3 * 2 + hf) * T + r] = rho1;
-            red[(4 * 2 + hf) * T + r] = xdy;
+            red[(0 * kNQ + qc) * T + r] = sg;
+            red[(1 * kNQ + qc) * T + r] = sm;
+            red[(2 * kNQ + qc) * T + r] = rho2;
+            red[(3 * kNQ + qc) * T + r] = rho1;
+            red[(4 * kNQ + qc) * T + r] = xdy;
             tc_fence_before();
             __syncthreads();
             // every TMEM read of this head is done: the next head's C B^T (it needs only the block's B / C)
@@ -444,18 +446,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                 tc_fence_after();
                 issue_cb<N>(tm, sC, sB);
             }
-            float* wtot = red + 10 * T;  // per-warp totals of the scans: [v or w][warp]
+            float* wtot = red + 5 * kNQ * T;  // per-warp totals of the scans: [v or w][warp]
+            // quantity q of row t summed over the quarters, in a fixed order
+            auto qsum = [&](int q, int t) {
+                const float* rq = red + q * kNQ * T + t;
+                return (rq[0] + rq[T]) + (rq[2 * T] + rq[3 * T]);
+            };
             float v = 0.f, wv = 0.f, pv = 0.f, pw = 0.f, sfull = 0.f, dtl = 0.f, xd = 0.f;
             if (tid < T) {
                 const int t = tid;
                 const float dtt = sdt[t], ex = fast_exp2(ce - scs[t]);
-                const float sgt = red[t] + red[T + t], smt = red[2 * T + t] + red[3 * T + t];
-                sfull = fmaf(ex, smt, sgt);                                   // x_t . G_t
-                v = dtt * ex * smt;                                           // mu's part, at token t
-                wv = fmaf(fast_exp2(scs[t]), red[4 * T + t] + red[5 * T + t],  // rho2 + rho1 - sigma
-                          red[6 * T + t] + red[7 * T + t]) - dtt * sgt;
+                const float sgt = qsum(0, t), smt = qsum(1, t);
+                sfull = fmaf(ex, smt, sgt);                      // x_t . G_t
+                v = dtt * ex * smt;                              // mu's part, at token t
+                wv = fmaf(fast_exp2(scs[t]), qsum(2, t),         // rho2 + rho1 - sigma
+                          qsum(3, t)) - dtt * sgt;
                 dtl = dtt;
-                xd = red[8 * T + t] + red[9 * T + t];
+                xd = qsum(4, t);
                 // inclusive scans of v and w inside the warp
                 pv = v;
                 pw = wv;
@@ -485,7 +492,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                     }
                     tw += wtot[4 + k2];
                 }
-                const float hmu_all = (wsum[0] + wsum[1]) + (wsum[2] + wsum[3]) + ((wsum[4] + wsum[5]) + (wsum[6] + wsum[7]));
+                float hmu_all = 0.f;
+#pragma unroll
+                for (int w4 = 0; w4 < kThreads / 32; w4 += 4)
+                    hmu_all += (wsum[w4] + wsum[w4 + 1]) + (wsum[w4 + 2] + wsum[w4 + 3]);
                 // dl_t = 2^(c_e) <mu, h0> + (v before t) + (w from t on)
                 const float excl_v = bv + pv - v;
                 const float from_t_w = tw - (bw + pw - wv);
@@ -518,18 +528,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         if (ok) {
             // dC and dB rows of this block, summed over the group's heads
 #pragma unroll 1
-            for (int c = 0; c < N / 64; ++c) {
-                const int n0 = hf * (N / 2) + 32 * c;
-                uint32_t vc[32], vb[32];
-                tmem_ld32(tm + lane_base + T_DC + n0, vc);
-                tmem_ld32(tm + lane_base + T_DB + n0, vb);
-                tmem_ld_wait(vc);
-                tmem_ld_wait(vb);
+            for (int c = 0; c < N / 64; ++c) {  // this warp's quarter of the columns, 16 at a time
+                const int n0 = qc * (N / 4) + 16 * c;
+                uint32_t vc[16], vb[16];
+                tmem_ld16(tm + lane_base + T_DC + n0, vc);
+                tmem_ld16(tm + lane_base + T_DB + n0, vb);
+                tmem_ld_wait16(vc);
+                tmem_ld_wait16(vb);
                 if (tok < L) {
                     float4* dc = reinterpret_cast<float4*>(a.dC + ((b * L + tok) * G + g) * (int64_t)N + n0);
                     float4* db = reinterpret_cast<float4*>(a.dB + ((b * L + tok) * G + g) * (int64_t)N + n0);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < 4; ++j) {
                         dc[j] = make_float4(__uint_as_float(vc[4 * j]), __uint_as_float(vc[4 * j + 1]),
                                             __uint_as_float(vc[4 * j + 2]), __uint_as_float(vc[4 * j + 3]));
                         db[j] = make_float4(__uint_as_float(vb[4 * j]), __uint_as_float(vb[4 * j + 1]),
@@ -544,17 +554,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         float* acc = reinterpret_cast<float*>(smem);
         if (ok) {
 #pragma unroll 1
-            for (int c = 0; c < N / 64; ++c) {
-                const int n0 = hf * (N / 2) + 32 * c;
-                uint32_t vc[32], vb[32];
-                tmem_ld32(tm + lane_base + T_DC + n0, vc);
-                tmem_ld32(tm + lane_base + T_DB + n0, vb);
-                tmem_ld_wait(vc);
-                tmem_ld_wait(vb);
+            for (int c = 0; c < N / 64; ++c) {  // this warp's quarter of the columns, 16 at a time
+                const int n0 = qc * (N / 4) + 16 * c;
+                uint32_t vc[16], vb[16];
+                tmem_ld16(tm + lane_base + T_DC + n0, vc);
+                tmem_ld16(tm + lane_base + T_DB + n0, vb);
+                tmem_ld_wait16(vc);
+                tmem_ld_wait16(vb);
                 float4* sc = reinterpret_cast<float4*>(acc + (int64_t)r * NS + n0);
                 float4* sb = reinterpret_cast<float4*>(acc + (int64_t)(T + r) * NS + n0);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 4; ++j) {
                     sc[j] = make_float4(__uint_as_float(vc[4 * j]), __uint_as_float(vc[4 * j + 1]),
                                         __uint_as_float(vc[4 * j + 2]), __uint_as_float(vc[4 * j + 3]));
                     sb[j] = make_float4(__uint_as_float(vb[4 * j]), __uint_as_float(vb[4 * j + 1]),
