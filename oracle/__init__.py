@@ -65,7 +65,7 @@ def _load():
             lib.ssd_oracle_chunk_scan.argtypes = [p] * 7 + [i64] * 7 + [p, i64, p, i32]
             lib.ssd_oracle_dA_cumsum.argtypes = [p, p, i64, i64, i64, i64, p, p]
             lib.ssd_oracle_state_passing.argtypes = [p, p, p] + [i64] * 6 + [p, p]
-            lib.ssd_oracle_backward.argtypes = [p] * 9 + [i64] * 6 + [p, i64] + [p] * 14 + [i32]
+            lib.ssd_oracle_backward.argtypes = [p] * 9 + [i64] * 6 + [p, i64] + [p] * 15 + [i32]
             for f in ("ssd_oracle_forward", "ssd_oracle_forward_opts", "ssd_oracle_chunk_states", "ssd_oracle_chunk_scan",
                       "ssd_oracle_dA_cumsum", "ssd_oracle_state_passing", "ssd_oracle_backward"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -225,10 +225,11 @@ def backward(x, dt, A, B, C, D, init, dy, dfinal=None, units=None, nthreads=0, s
     ``dinit`` (P, N), and ``ddt_direct`` (L,): ddt's term <lam_t, B_t x_t^T> alone (the rest,
     ddt - ddt_direct, is A exp(dt_t A) <lam_t, state_{t-1}>).
 
-    With ``scales``, also ``dx_s``, ``dB_s``, ``dC_s``, ``ddt_s``, ``dA_s``, ``dD_s`` in the same
-    layouts: the sum of the magnitudes of the products each gradient adds up (dx: dt sum_n |B lam|
+    With ``scales``, also ``dx_s``, ``dB_s``, ``dC_s``, ``ddt_s``, ``dA_s``, ``dD_s``, ``dinit_s`` in the
+    same layouts: the sum of the magnitudes of the products each gradient adds up (dx: dt sum_n |B lam|
     + |D dy|; dB: dt sum_p |lam x|; dC: sum_p |state dy|; ddt: |A| exp(dt A) sum |lam state_prev| +
-    sum |lam B x|; dA: the sum over tokens of dt exp(dt A) sum |lam state_prev|; dD: sum |x dy|).
+    sum |lam B x|; dA: the sum over tokens of dt exp(dt A) sum |lam state_prev|; dD: sum |x dy|;
+    dinit: the adjoint's terms |C_t dy_t^T| and |dfinal|, each decayed to the start as lam is).
     """
     x, B, C, dy = _c(x, np.uint16), _c(B, np.uint16), _c(C, np.uint16), _c(dy, np.uint16)
     dt, A = _c(dt, np.float32), _c(A, np.float32)
@@ -244,7 +245,7 @@ def backward(x, dt, A, B, C, D, init, dy, dfinal=None, units=None, nthreads=0, s
            "ddt": np.empty((u.size, L)), "dA": np.empty(u.size), "dD": np.empty(u.size),
            "dinit": np.empty((u.size, P, N)), "ddt_direct": np.empty((u.size, L))}
     names = ("dx", "dB", "dC", "ddt", "dA", "dD", "dinit", "ddt_direct")
-    snames = ("dx_s", "dB_s", "dC_s", "ddt_s", "dA_s", "dD_s")
+    snames = ("dx_s", "dB_s", "dC_s", "ddt_s", "dA_s", "dD_s", "dinit_s")
     if scales:
         for k in snames:
             out[k] = np.empty_like(out[k[:-2]])
@@ -276,7 +277,7 @@ def backward_full(x, dt, A, B, C, D, init, dy, dfinal=None, nthreads=0):
 def backward_terms(x, dt, A, B, C, D, init, dy, dfinal=None, nthreads=0):
     """``backward_full`` plus ``scales``: for every gradient, in its layout, the sum of the magnitudes of
     the products it adds up (see ``backward``), summed like the gradient itself (over a group's heads
-    for dB and dC, over the batch for dA and dD); dinit's scale is |dinit|."""
+    for dB and dC, over the batch for dA and dD)."""
     b, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     r = backward(x, dt, A, B, C, D, init, dy, dfinal, nthreads=nthreads, scales=True)
@@ -293,5 +294,5 @@ def backward_terms(x, dt, A, B, C, D, init, dy, dfinal=None, nthreads=0):
                      "ddt": r["ddt_s"].reshape(b, H, L).transpose(0, 2, 1),
                      "dB": group_sum(r["dB_s"]), "dC": group_sum(r["dC_s"]),
                      "dA": r["dA_s"].reshape(b, H).sum(axis=0), "dD": r["dD_s"].reshape(b, H).sum(axis=0),
-                     "dinit": np.abs(out["dinit"])}
+                     "dinit": r["dinit_s"].reshape(b, H, P, N)}
     return out

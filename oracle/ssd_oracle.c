@@ -482,8 +482,9 @@ typedef struct {
     /* Scales, each NULL or per unit in the layout of its gradient: the sum of the magnitudes of the
      * products the gradient adds up (dx: dt sum_n |B lam| + |D dy|; dB: dt sum_p |lam x|; dC:
      * sum_p |hs dy|; ddt: |A| a sum |lam hs_prev| + sum |lam B x|; dA: sum_t dt a sum |lam hs_prev|;
-     * dD: sum_t sum_p |x dy|). */
-    double *dx_s, *dB_s, *dC_s, *ddt_s, *dA_s, *dD_s;
+     * dD: sum_t sum_p |x dy|; dinit: the adjoint's terms |C_t dy_t^T| and |dfinal|, each decayed to
+     * the start as lam is). */
+    double *dx_s, *dB_s, *dC_s, *ddt_s, *dA_s, *dD_s, *dinit_s;
 } bwd_ctx_t;
 
 static void bwd_unit(void* vctx, int64_t u) {
@@ -499,6 +500,7 @@ static void bwd_unit(void* vctx, int64_t u) {
     double* ck = (double*)calloc((size_t)(nseg * NP), sizeof(double));   /* state before each segment */
     double* seg = (double*)malloc(sizeof(double) * (size_t)((K + 1) * NP)); /* states through a segment */
     double* lam = (double*)calloc((size_t)NP, sizeof(double));
+    double* lam_abs = (double*)calloc((size_t)NP, sizeof(double)); /* the same over |terms| (dinit's scale) */
     double* xv = (double*)malloc(sizeof(double) * (size_t)P);
     double* yv = (double*)malloc(sizeof(double) * (size_t)P);
     double* bv = (double*)malloc(sizeof(double) * (size_t)N);
@@ -513,7 +515,10 @@ static void bwd_unit(void* vctx, int64_t u) {
         recur_tokens(&c->in, b, h, t0, t1, hs, NULL);
     }
     /* backward sweep */
-    if (c->dfinal != NULL) load_state_f32(lam, c->dfinal + (b * H + h) * P * N, P, N);
+    if (c->dfinal != NULL) {
+        load_state_f32(lam, c->dfinal + (b * H + h) * P * N, P, N);
+        for (int64_t e = 0; e < NP; ++e) lam_abs[e] = fabs(lam[e]);
+    }
     double dA = 0.0, dD = 0.0, dA_abs = 0.0, dD_abs = 0.0;
     double* dx = c->dx + u * L * P;
     double* dB = c->dB + u * L * N;
@@ -539,7 +544,10 @@ static void bwd_unit(void* vctx, int64_t u) {
             for (int64_t n = 0; n < N; ++n) { bv[n] = bf16_to_double(br[n]); cv[n] = bf16_to_double(cr[n]); }
             /* lam_t = (carried) + C_t dy_t^T */
             for (int64_t n = 0; n < N; ++n)
-                for (int64_t p = 0; p < P; ++p) lam[n * P + p] += cv[n] * yv[p];
+                for (int64_t p = 0; p < P; ++p) {
+                    lam[n * P + p] += cv[n] * yv[p];
+                    lam_abs[n * P + p] += fabs(cv[n] * yv[p]);
+                }
             double xdy = 0.0, xdy_abs = 0.0;
             for (int64_t p = 0; p < P; ++p) {
                 double acc = 0.0, acc_abs = 0.0;
@@ -577,7 +585,10 @@ static void bwd_unit(void* vctx, int64_t u) {
             dA_abs += dtv * a * inner_abs;
             dD += xdy;
             dD_abs += xdy_abs;
-            for (int64_t e = 0; e < NP; ++e) lam[e] *= a; /* carry to token t - 1 */
+            for (int64_t e = 0; e < NP; ++e) { /* carry to token t - 1 */
+                lam[e] *= a;
+                lam_abs[e] *= a;
+            }
         }
     }
     c->dA[u] = dA;
@@ -585,7 +596,8 @@ static void bwd_unit(void* vctx, int64_t u) {
     if (c->dA_s != NULL) c->dA_s[u] = dA_abs;
     if (c->dD_s != NULL) c->dD_s[u] = dD_abs;
     store_state(c->dinit + u * P * N, lam, P, N);
-    free(ck); free(seg); free(lam); free(xv); free(yv); free(bv); free(cv);
+    if (c->dinit_s != NULL) store_state(c->dinit_s + u * P * N, lam_abs, P, N);
+    free(ck); free(seg); free(lam); free(lam_abs); free(xv); free(yv); free(bv); free(cv);
 }
 
 /*
@@ -595,7 +607,7 @@ static void bwd_unit(void* vctx, int64_t u) {
  * and D (this unit's share, one value each) and init (dinit, (P, N)), given
  * dy (x's layout, bf16) and dfinal ((batch, H, P, N) f32, or NULL = 0).
  * ddt_direct (per unit (L), or NULL) receives ddt's second term alone; each
- * of dx_s, dB_s, dC_s, ddt_s, dA_s, dD_s (NULL or the layout of its gradient)
+ * of dx_s, dB_s, dC_s, ddt_s, dA_s, dD_s, dinit_s (NULL or the layout of its gradient)
  * receives the sum of the magnitudes of the products that gradient adds up
  * (the scale of its rounding error in any method that rounds the factors).
  * Returns the number of threads used, or -1 on bad arguments.
@@ -606,7 +618,7 @@ int ssd_oracle_backward(const uint16_t* x, const float* dt, const float* A, cons
                         int64_t ngroups, int64_t dstate, const int64_t* units, int64_t nunits,
                         double* dx, double* dB, double* dC, double* ddt, double* dA, double* dD,
                         double* dinit, double* ddt_direct, double* dx_s, double* dB_s, double* dC_s,
-                        double* ddt_s, double* dA_s, double* dD_s, int nthreads) {
+                        double* ddt_s, double* dA_s, double* dD_s, double* dinit_s, int nthreads) {
     if (!x || !dt || !A || !B || !C || !dy || !units || !dx || !dB || !dC || !ddt || !dA || !dD || !dinit)
         return -1;
     if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0 ||
@@ -614,6 +626,6 @@ int ssd_oracle_backward(const uint16_t* x, const float* dt, const float* A, cons
         return -1;
     dims_t d = {batch, seqlen, nheads, headdim, ngroups, dstate, seqlen};
     bwd_ctx_t ctx = {{&d, x, B, C, dt, A, D, NULL}, init, dy, dfinal, units, dx, dB, dC, ddt, dA, dD, dinit,
-                     ddt_direct, dx_s, dB_s, dC_s, ddt_s, dA_s, dD_s};
+                     ddt_direct, dx_s, dB_s, dC_s, ddt_s, dA_s, dD_s, dinit_s};
     return run_units(bwd_unit, &ctx, nunits, nthreads);
 }

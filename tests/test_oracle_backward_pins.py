@@ -15,7 +15,8 @@ for the scalar loss
 * dt and A enter through exp(dt A): central differences on values chosen
   exactly representable in float32 together with their perturbations, so
   the step is exact and only the O(step^2) truncation error remains.
-* dy = 0: closed forms for dinit and dx (pure decay of dfinal).
+* dy = 0: closed forms for dinit and dx (pure decay of dfinal), and for dinit's
+  scale; with non-negative terms that scale equals dinit.
 * The chunked algorithm (``closed_form.backward_chunked``), another route to
   the same numbers, agrees with the token recurrence for several blocks.
 """
@@ -144,6 +145,38 @@ def test_zero_dy_is_pure_decay_of_dfinal():
             want = (dt[bb, :, h] * after)[:, None] * (B[bb, :, h // hpg] @ g["dfinal"][bb, h].astype(np.float64).T)
             np.testing.assert_allclose(gr["dx"][bb, :, h], want, rtol=1e-11, atol=1e-14)
     assert np.all(gr["dC"] == 0) and gr["dD"].any() == False  # noqa: E712  (x . dy = 0 with dy = 0)
+
+
+def terms(n, g):
+    return oracle.backward_terms(n["x"], n["dt"], n["A"], n["B"], n["C"], n["D"], n["init"], g["dy"], g["dfinal"])
+
+
+def test_dinit_scale_closed_forms():
+    """dinit's scale (the magnitudes of the adjoint's terms C_t dy_t^T and dfinal, each decayed to the
+    start):
+    * dy = 0: one term, so it is exp(A sum dt) |dfinal|;
+    * C, dy and dfinal >= 0: no term cancels, so it equals dinit (pinned above by exact differences);
+    * otherwise it bounds |dinit| (triangle inequality) and exceeds it where the terms cancel."""
+    n, g = draw()
+    g0 = dict(g)
+    g0["dy"] = np.zeros_like(g["dy"])
+    r = terms(n, g0)
+    dt = n["dt"].astype(np.float64)
+    A = n["A"].astype(np.float64)
+    for bb in range(W.batch):
+        for h in range(W.nheads):
+            tot = np.exp(A[h] * dt[bb, :, h].sum())
+            np.testing.assert_allclose(r["scales"]["dinit"][bb, h], tot * np.abs(g["dfinal"][bb, h]), rtol=1e-12,
+                                       atol=1e-15)
+    npos, gpos = dict(n), dict(g)
+    npos["C"] = n["C"] & np.uint16(0x7FFF)   # bf16 sign bit cleared: |C|
+    gpos["dy"] = g["dy"] & np.uint16(0x7FFF)
+    gpos["dfinal"] = np.abs(g["dfinal"])
+    rp = terms(npos, gpos)
+    np.testing.assert_allclose(rp["scales"]["dinit"], rp["dinit"], rtol=1e-12, atol=1e-15)
+    r = terms(n, g)
+    assert np.all(r["scales"]["dinit"] >= np.abs(r["dinit"]) * (1 - 1e-12))
+    assert np.any(r["scales"]["dinit"] > 2 * np.abs(r["dinit"]))
 
 
 def test_no_gradient_in_gives_zero():
