@@ -186,10 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
 
     // Inputs of head hh: its x and dy rows (bfloat16) into the swizzled positions of the XS / DYS
     // tiles (zeros past the sequence end), h0 and mu (float16 rows p) straight into the H0 / MU tiles,
-    // and this thread's dA_cumsum (tid < T) or dt value of the block into `csdt`.
+    // this thread's dA_cumsum (tid < T) or dt value of the block into `csdt`, and the head's D and A into
+    // `dnext` and `anext` (loads in flight while the current head finishes).
+    float dnext = 0.f, anext = 0.f;
     auto prefetch = [&](int hh, float& csdt) {
         const int64_t crow = ((int64_t)b * H + hh) * rowlen + t0;
         if (tid < 2 * T) csdt = (tid < T) ? __ldg(a.cs + crow + tid) : __ldg(a.dtt + crow + tid - T);
+        dnext = (a.D != nullptr) ? __ldg(a.D + hh) : 0.f;
+        anext = __ldg(a.A + hh);
 #pragma unroll
         for (int i = 0; i < T * 8 / kThreads; ++i) {
             const int c = tid + i * kThreads;
@@ -221,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
 #pragma unroll 1
     for (int k = 0; k < hps && ok; ++k) {
         const int h = g * hpg + slice * hps + k;
+        const float Dh = dnext, Ah = anext;  // this head's D and A (loaded with its inputs)
         // ---- this head's raw inputs (copied during the previous head's epilogue) -> float16 tiles
         cp_async_wait_all();
         if (tid < T) scs[tid] = csdt;
@@ -386,7 +391,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
             float* red = reinterpret_cast<float*>(smem + K::OFF_M);  // [quantity][quarter][T]; M' is consumed
             const int64_t tok = t0 + r;
             const float ext = fast_exp2(ce - scs[r]), dtr = sdt[r];
-            const float Dh = (a.D != nullptr) ? __ldg(a.D + h) : 0.f;
             uint32_t vg[16], vm[16];
             tmem_ld16(tm + lane_base + T_G + 16 * qc, vg);
             tmem_ld16(tm + lane_base + T_GMU + 16 * qc, vm);
@@ -446,15 +450,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                 tc_fence_after();
                 issue_cb<N>(tm, sC, sB);
             }
-            float* wtot = red + 5 * kNQ * T;  // per-warp totals of the scans: [v or w][warp]
+            // the scans over the block's tokens run on warps 1-4 (token t = tid - 32, scan warp sw = warp - 1),
+            // so that warp 0, whose thread 0 issues the products, does not delay them
+            const int sw = warp - 1;
+            const bool scan = tid >= 32 && tid < 32 + T;
+            float* wtot = red + 5 * kNQ * T;  // per-warp totals of the scans: [v or w][scan warp]
             // quantity q of row t summed over the quarters, in a fixed order
             auto qsum = [&](int q, int t) {
                 const float* rq = red + q * kNQ * T + t;
                 return (rq[0] + rq[T]) + (rq[2 * T] + rq[3 * T]);
             };
             float v = 0.f, wv = 0.f, pv = 0.f, pw = 0.f, sfull = 0.f, dtl = 0.f, xd = 0.f;
-            if (tid < T) {
-                const int t = tid;
+            if (scan) {
+                const int t = tid - 32;
                 const float dtt = sdt[t], ex = fast_exp2(ce - scs[t]);
                 const float sgt = qsum(0, t), smt = qsum(1, t);
                 sfull = fmaf(ex, smt, sgt);                      // x_t . G_t
@@ -476,17 +484,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                     }
                 }
                 if (lane == 31) {
-                    wtot[warp] = pv;
-                    wtot[4 + warp] = pw;
+                    wtot[sw] = pv;
+                    wtot[4 + sw] = pw;
                 }
             }
             __syncthreads();
-            if (tid < T) {
-                const int t = tid;
+            if (scan) {
+                const int t = tid - 32;
                 float bv = 0.f, bw = 0.f, tw = 0.f;  // earlier warps' totals; all of w
 #pragma unroll
                 for (int k2 = 0; k2 < 4; ++k2) {
-                    if (k2 < warp) {
+                    if (k2 < sw) {
                         bv += wtot[k2];
                         bw += wtot[4 + k2];
                     }
@@ -500,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                 const float excl_v = bv + pv - v;
                 const float from_t_w = tw - (bw + pw - wv);
                 const float dl = fmaf(fast_exp2(ce), hmu_all, excl_v + from_t_w);
-                if (t0 + t < L) a.ddt[((b * L + t0 + t) * H + h)] = fmaf(__ldg(a.A + h), dl, sfull);
+                if (t0 + t < L) a.ddt[((b * L + t0 + t) * H + h)] = fmaf(Ah, dl, sfull);
                 float da = dtl * dl;
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {
@@ -508,8 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                     xd += __shfl_xor_sync(0xffffffffu, xd, off);
                 }
                 if (lane == 0) {
-                    wtot[8 + warp] = da;
-                    wtot[12 + warp] = xd;
+                    wtot[8 + sw] = da;
+                    wtot[12 + sw] = xd;
                 }
             }
             __syncthreads();
