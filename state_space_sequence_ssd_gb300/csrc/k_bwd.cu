@@ -285,8 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         tc_fence_before();
         __syncthreads();
         // ---- C B^T (K = n; the first head only -- later heads' was issued during the previous epilogue)
-        //      and dY X^T (K = p); then the dC / dB terms that need no mask, dY' h0^T and X' mu^T (K = p),
-        //      which run while the mask works (the phase's second commit covers them)
+        //      and dY X^T (K = p)
         if (tid == 0) {
             tc_fence_after();
             if (k == 0) issue_cb<N>(tm, sC, sB);
@@ -295,13 +294,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                 mma_ss(tm + T_DX, desc_sw128(sDY + kk * 32, 16, 1024), desc_sw128(sX + kk * 32, 16, 1024), kIdescTT,
                        kk > 0);
             mma_commit(bar);
-#pragma unroll
-            for (int kk = 0; kk < kP / 16; ++kk) {  // K = p
-                mma_ss(tm + T_DC, desc_sw128(sDYS + kk * 32, 16, 1024), desc_sw128(sH0 + kk * 2048, kPanelP, 1024),
-                       kIdescN, k > 0 || kk > 0);
-                mma_ss(tm + T_DB, desc_sw128(sXS + kk * 32, 16, 1024), desc_sw128(sMU + kk * 2048, kPanelP, 1024),
-                       kIdescN, k > 0 || kk > 0);
-            }
         }
         pending = true;
         ok = mbar_wait_bounded(bar, phase, abort_flag, err, 61, wait_ns);
@@ -349,6 +341,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                     *reinterpret_cast<uint4*>(smem + K::OFF_W + so) =
                         make_uint4(pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
                 }
+            }
+        }
+        // the dC / dB terms that need no mask, dY' h0^T and X' mu^T (K = p): issued once this thread's own
+        // mask rows are written, so that they run while the other warps finish theirs (the next commit
+        // covers them)
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < kP / 16; ++kk) {
+                mma_ss(tm + T_DC, desc_sw128(sDYS + kk * 32, 16, 1024), desc_sw128(sH0 + kk * 2048, kPanelP, 1024),
+                       kIdescN, k > 0 || kk > 0);
+                mma_ss(tm + T_DB, desc_sw128(sXS + kk * 32, 16, 1024), desc_sw128(sMU + kk * 2048, kPanelP, 1024),
+                       kIdescN, k > 0 || kk > 0);
             }
         }
         fence_proxy_async_smem();
