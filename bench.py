@@ -156,6 +156,9 @@ def main():
     ap.add_argument("--forward-only", action="store_true",
                     help="time the forward pass only: no end-to-end, decode or layer-options legs and no CPU "
                          "baseline (for profiler runs)")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time the backward pass only and print its JSON object alone (for profiler runs; one "
+                         "GPU)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: --warmup raised to 3 (minimum)", file=sys.stderr)
@@ -190,6 +193,12 @@ def main():
     fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), device=dev, dtype=torch.float32)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    if args.backward_only:
+        if not (w.headdim == 64 and w.dstate in (64, 128)):
+            print(json.dumps({"backward": None, "unsupported": "ssd_backward covers P 64, N 64 or 128"}))
+            return 0
+        print(json.dumps({"backward": backward_measure(w, d, dev, stream, args, ssd, lib, flush)}))
+        return 0
     split = head_split(w, world, rank, d, dev, ssd) if world > 1 else None
 
     def step():
