@@ -22,12 +22,47 @@
 // With a layer's input-side options, dt is transformed first (bias, softplus,
 // clamp), the skip weight may be one per channel (D is (H, P)) and y is gated
 // by z sigmoid(z); the state itself is never gated.
+//
+// The arithmetic runs two state entries per instruction (sm_100's packed two-lane float32 multiply
+// and fma, each lane rounded as a separate instruction would be), and a lane's share of C.state is
+// kept as two partial sums, of its even and of its odd entries, added at the end: the same order in
+// every kernel here, so that K single steps and one K-token step agree bit for bit.
 #include "common.cuh"
 
 namespace ssd {
 namespace {
 
 constexpr int kThreads = 256;
+
+// two float32 products, and two fused multiply-adds a * b + c, each in one instruction
+__device__ __forceinline__ float2 pmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 pfma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// One state row's four entries of this lane: q <- a q + (dt B) x, then their terms of C.state added to
+// the even / odd partial sums in acc
+__device__ __forceinline__ void step4(float4& q, float a, float xp, const float (&bv)[4], const float (&cv)[4],
+                                      float2& acc) {
+    const float2 a2 = make_float2(a, a), x2 = make_float2(xp, xp);
+    const float2 q01 = pfma2(a2, make_float2(q.x, q.y), pmul2(make_float2(bv[0], bv[1]), x2));
+    const float2 q23 = pfma2(a2, make_float2(q.z, q.w), pmul2(make_float2(bv[2], bv[3]), x2));
+    q = make_float4(q01.x, q01.y, q23.x, q23.y);
+    acc = pfma2(make_float2(cv[0], cv[1]), q01, acc);
+    acc = pfma2(make_float2(cv[2], cv[3]), q23, acc);
+}
 
 // y = C.state + D x, then the optional gate; hp indexes (H, P) weights, i the (batch, H, P) rows
 __device__ __forceinline__ float step_output(float acc, float xp, float Dh, int64_t hp, int64_t i, const OutOpts& oo) {
@@ -104,20 +139,14 @@ __global__ void __launch_bounds__(kThreads) ssd_step_kernel(const __nv_bfloat16*
         for (int i = 0; i < RG; ++i) {
             const int p = warp + 8 * (r0 + i);
             const float xp = __bfloat162float(xr[p]);
-            float acc = 0.f;
+            float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int v = 0; v < NV; ++v) {
                 float4 q = s4[i][v];
-                q.x = fmaf(a, q.x, bv[v][0] * xp);
-                q.y = fmaf(a, q.y, bv[v][1] * xp);
-                q.z = fmaf(a, q.z, bv[v][2] * xp);
-                q.w = fmaf(a, q.w, bv[v][3] * xp);
+                step4(q, a, xp, bv[v], cv[v], acc2);
                 *reinterpret_cast<float4*>(st + (int64_t)p * N + 128 * v + 4 * lane) = q;
-                acc = fmaf(cv[v][0], q.x, acc);
-                acc = fmaf(cv[v][1], q.y, acc);
-                acc = fmaf(cv[v][2], q.z, acc);
-                acc = fmaf(cv[v][3], q.w, acc);
             }
+            float acc = acc2.x + acc2.y;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (lane == 0) y[bh * P + p] = __float2bfloat16_rn(step_output(acc, xp, Dh, h * P + p, bh * P + p, oo));
@@ -164,15 +193,10 @@ __global__ void __launch_bounds__(kThreads) ssd_step_kernel_n64(const __nv_bfloa
         const int p = 2 * warp + 16 * i + half;
         const float xp = __bfloat162float(xr[p]);
         float4 q = s4[i];
-        q.x = fmaf(a, q.x, bv[0] * xp);
-        q.y = fmaf(a, q.y, bv[1] * xp);
-        q.z = fmaf(a, q.z, bv[2] * xp);
-        q.w = fmaf(a, q.w, bv[3] * xp);
+        float2 acc2 = make_float2(0.f, 0.f);
+        step4(q, a, xp, bv, cv, acc2);
         *reinterpret_cast<float4*>(st + (int64_t)p * N + 4 * l16) = q;
-        float acc = cv[0] * q.x;
-        acc = fmaf(cv[1], q.y, acc);
-        acc = fmaf(cv[2], q.z, acc);
-        acc = fmaf(cv[3], q.w, acc);
+        float acc = acc2.x + acc2.y;
 #pragma unroll
         for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (l16 == 0) y[bh * P + p] = __float2bfloat16_rn(step_output(acc, xp, Dh, h * P + p, bh * P + p, oo));
@@ -182,8 +206,9 @@ __global__ void __launch_bounds__(kThreads) ssd_step_kernel_n64(const __nv_bfloa
 // ---------------------------------------------------------------- several tokens per launch
 // ssd_step_multi: K consecutive tokens of every sequence in one launch.  The state stays in
 // registers for all K tokens, so it is read and written once per launch instead of once per
-// token.  Each token's arithmetic (and the lanes' split of n and the reduction order) is that
-// of ssd_step, so K tokens here equal K ssd_step calls bit for bit.
+// token.  Each token's arithmetic (the lanes' split of n, the packed state update, the two partial
+// sums and the reduction order) is that of ssd_step, so K tokens here equal K ssd_step calls bit for
+// bit.
 // Sums R per-row partial values over the lanes of a row group (xor offsets OFF, OFF/2, ..., 1).
 // While a lane holds more than one row it keeps half of them and trades the other half with its
 // partner, so R rows over 2^k lanes cost (R - 1) + (k - log2 R) shuffles instead of R k (9 instead of
@@ -279,20 +304,10 @@ __global__ void __launch_bounds__(MultiCfg<N>::THREADS) ssd_step_multi_kernel(
 #pragma unroll
         for (int i = 0; i < K::SLOTS; ++i) {
             xp[i] = __bfloat162float(xr[(i * K::W + warp) * K::RPS + sub]);
-            acc[i] = 0.f;
+            float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int v = 0; v < K::NV; ++v) {
-                float4 q = s[i][v];
-                q.x = fmaf(a, q.x, bv[v][0] * xp[i]);
-                q.y = fmaf(a, q.y, bv[v][1] * xp[i]);
-                q.z = fmaf(a, q.z, bv[v][2] * xp[i]);
-                q.w = fmaf(a, q.w, bv[v][3] * xp[i]);
-                s[i][v] = q;
-                acc[i] = fmaf(cv[v][0], q.x, acc[i]);
-                acc[i] = fmaf(cv[v][1], q.y, acc[i]);
-                acc[i] = fmaf(cv[v][2], q.z, acc[i]);
-                acc[i] = fmaf(cv[v][3], q.w, acc[i]);
-            }
+            for (int v = 0; v < K::NV; ++v) step4(s[i][v], a, xp[i], bv[v], cv[v], acc2);
+            acc[i] = acc2.x + acc2.y;
         }
         int i = 0;  // the row (slot) whose full sum this lane ends up holding
         const float tot = fold_rows<K::SLOTS, K::LPR / 2>(acc, ln, i);
