@@ -580,8 +580,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         hmax_abs4(mx, o.x, o.y, o.z, o.w);
                         *reinterpret_cast<uint4*>(kb + sw128_offset(r, 4 * (c & 1) + q4)) = o;
                     }
+                    const float2 dsb2 = make_float2(dsb, dsb);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * dsb);
+                    for (int i = 0; i < 16; ++i) {  // packed pairs
+                        const float2 f = fmul2(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), dsb2);
+                        v[2 * i] = __float_as_uint(f.x);
+                        v[2 * i + 1] = __float_as_uint(f.y);
+                    }
                     tmem_st32(tm + lane_base + K::T_H + 32 * c, v);
                 }
                 tmem_st_wait();
@@ -602,8 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t* o4 = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 f = __bfloat1622float2(p2[e]);
-                        o4[e] = pack_f16x2(f.x * w, f.y * w);
+                        const float2 f = fmul2(__bfloat1622float2(p2[e]), make_float2(w, w));
+                        o4[e] = pack_f16x2(f.x, f.y);
                     }
                     hmax_abs4(mx, o.x, o.y, o.z, o.w);
                     *reinterpret_cast<uint4*>(xrow + sw128_offset(r, ch)) = o;
@@ -654,8 +659,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                 for (int e2 = 0; e2 < 4; ++e2) {
                                     const int i = ch * 8 + 2 * e2;
-                                    o4[e2] = pack_bf16x2(__uint_as_float(yv[i]) + eh * __uint_as_float(sv[i]),
-                                                         __uint_as_float(yv[i + 1]) + eh * __uint_as_float(sv[i + 1]));
+                                    const float2 f = ffma2(make_float2(eh, eh),
+                                                           make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])),
+                                                           make_float2(__uint_as_float(yv[i]), __uint_as_float(yv[i + 1])));
+                                    o4[e2] = pack_bf16x2(f.x, f.y);
                                 }
                             }
                             if (a.y32) {
