@@ -248,9 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                 for (int e = 0; e < 4; ++e) {
                     const float2 xf = bf2_to_f2(xw[e]), yf = bf2_to_f2(yw[e]);
                     ox[e] = pack_f16x2(xf.x, xf.y);
-                    oxs[e] = pack_f16x2(xf.x * wx, xf.y * wx);
+                    const float2 xs = fmul2(xf, make_float2(wx, wx));
+                    oxs[e] = pack_f16x2(xs.x, xs.y);
                     oy[e] = pack_f16x2(yf.x, yf.y);
-                    oys[e] = pack_f16x2(yf.x * wy, yf.y * wy);
+                    const float2 ys = fmul2(yf, make_float2(wy, wy));
+                    oys[e] = pack_f16x2(ys.x, ys.y);
                 }
                 hmax_abs4(mx, ox[0], ox[1], ox[2], ox[3]);
                 hmax_abs4(mx, oxs[0], oxs[1], oxs[2], oxs[3]);
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         tc_fence_after();
         // ---- mask: row r, columns [32 qc, 32 qc + 32) of M' = L o C B^T and Wd = L o dY X^T o dt_j,
         //      16 at a time
-        float rho1 = 0.f;  // sum_j Wd[r][j] (C_r . B_j) over this quarter
+        float2 rho1p = make_float2(0.f, 0.f);  // sum_j Wd[r][j] (C_r . B_j) over this quarter: even / odd j
         {
             const float cr = scs[r];
 #pragma unroll 1
@@ -317,19 +319,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                 tmem_ld_wait16(vdx);
                 uint32_t pm[8], pw[8];
 #pragma unroll
-                for (int jj = 0; jj < 16; jj += 2) {
-                    float mv[2], wv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int i = i0 + jj + e;
-                        const float dec = (i <= r) ? fast_exp2(cr - scs[i]) : 0.f;
-                        const float cb = __uint_as_float(vcb[jj + e]);
-                        mv[e] = dec * cb;
-                        wv[e] = dec * sdt[i] * __uint_as_float(vdx[jj + e]);
-                        rho1 = fmaf(wv[e], cb, rho1);
-                    }
-                    pm[jj / 2] = pack_f16x2(mv[0], mv[1]);
-                    pw[jj / 2] = pack_f16x2(wv[0], wv[1]);
+                for (int jj = 0; jj < 16; jj += 2) {  // packed pairs of columns
+                    const int i = i0 + jj;
+                    const float2 dec = make_float2((i <= r) ? fast_exp2(cr - scs[i]) : 0.f,
+                                                   (i + 1 <= r) ? fast_exp2(cr - scs[i + 1]) : 0.f);
+                    const float2 cb = make_float2(__uint_as_float(vcb[jj]), __uint_as_float(vcb[jj + 1]));
+                    const float2 mv = fmul2(dec, cb);
+                    const float2 wv = fmul2(fmul2(dec, make_float2(sdt[i], sdt[i + 1])),
+                                            make_float2(__uint_as_float(vdx[jj]), __uint_as_float(vdx[jj + 1])));
+                    rho1p = ffma2(wv, cb, rho1p);
+                    pm[jj / 2] = pack_f16x2(mv.x, mv.y);
+                    pw[jj / 2] = pack_f16x2(wv.x, wv.y);
                 }
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {  // columns i0 .. i0 + 15: panel qc / 2, chunks 4 (qc % 2) + 2 c2 + j
@@ -400,7 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
             tmem_ld16(tm + lane_base + T_GMU + 16 * qc, vm);
             tmem_ld_wait16(vg);
             tmem_ld_wait16(vm);
-            float sg = 0.f, sm = 0.f, xdy = 0.f;  // x . G (pairs in the block), x . B mu, x . dy
+            // x . G (pairs in the block), x . B mu, x . dy: even / odd channel partial sums
+            float2 sg2 = make_float2(0.f, 0.f), sm2 = make_float2(0.f, 0.f), xdy2 = make_float2(0.f, 0.f);
             uint32_t ob[8];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
@@ -409,15 +410,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                 const __half2* xh = reinterpret_cast<const __half2*>(&xq);
                 const __half2* yh = reinterpret_cast<const __half2*>(&yq);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
+                for (int e = 0; e < 4; ++e) {  // packed pairs of channels
                     const int c = 8 * j + 2 * e;
                     const float2 xf = __half22float2(xh[e]), yf = __half22float2(yh[e]);
-                    const float gi0 = __uint_as_float(vg[c]), gi1 = __uint_as_float(vg[c + 1]);
-                    const float gm0 = __uint_as_float(vm[c]), gm1 = __uint_as_float(vm[c + 1]);
-                    sg = fmaf(xf.x, gi0, fmaf(xf.y, gi1, sg));
-                    sm = fmaf(xf.x, gm0, fmaf(xf.y, gm1, sm));
-                    xdy = fmaf(xf.x, yf.x, fmaf(xf.y, yf.y, xdy));
-                    const float g0 = fmaf(ext, gm0, gi0), g1 = fmaf(ext, gm1, gi1);
+                    const float2 gi = make_float2(__uint_as_float(vg[c]), __uint_as_float(vg[c + 1]));
+                    const float2 gm = make_float2(__uint_as_float(vm[c]), __uint_as_float(vm[c + 1]));
+                    sg2 = ffma2(xf, gi, sg2);
+                    sm2 = ffma2(xf, gm, sm2);
+                    xdy2 = ffma2(xf, yf, xdy2);
+                    const float g0 = fmaf(ext, gm.x, gi.x), g1 = fmaf(ext, gm.y, gi.y);
                     ob[4 * j + e] = pack_bf16x2(fmaf(dtr, g0, Dh * yf.x), fmaf(dtr, g1, Dh * yf.y));
                 }
             }
@@ -429,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
             uint32_t vy[16];
             tmem_ld16(tm + lane_base + T_YS + 16 * qc, vy);
             tmem_ld_wait16(vy);
-            float rho2 = 0.f;  // dy_r . (C_r h0) over this quarter
+            float2 rho22 = make_float2(0.f, 0.f);  // dy_r . (C_r h0) over this quarter: even / odd channels
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const uint4 yq = *reinterpret_cast<const uint4*>(smem + K::OFF_DY + sw128_offset(r, 2 * qc + j));
@@ -437,15 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int c = 8 * j + 2 * e;
-                    const float2 yf = __half22float2(yh[e]);
-                    rho2 = fmaf(yf.x, __uint_as_float(vy[c]), fmaf(yf.y, __uint_as_float(vy[c + 1]), rho2));
+                    rho22 = ffma2(__half22float2(yh[e]), make_float2(__uint_as_float(vy[c]), __uint_as_float(vy[c + 1])),
+                                  rho22);
                 }
             }
-            red[(0 * kNQ + qc) * T + r] = sg;
-            red[(1 * kNQ + qc) * T + r] = sm;
-            red[(2 * kNQ + qc) * T + r] = rho2;
-            red[(3 * kNQ + qc) * T + r] = rho1;
-            red[(4 * kNQ + qc) * T + r] = xdy;
+            red[(0 * kNQ + qc) * T + r] = sg2.x + sg2.y;
+            red[(1 * kNQ + qc) * T + r] = sm2.x + sm2.y;
+            red[(2 * kNQ + qc) * T + r] = rho22.x + rho22.y;
+            red[(3 * kNQ + qc) * T + r] = rho1p.x + rho1p.y;
+            red[(4 * kNQ + qc) * T + r] = xdy2.x + xdy2.y;
             tc_fence_before();
             __syncthreads();
             // every TMEM read of this head is done: the next head's C B^T (it needs only the block's B / C)
