@@ -502,12 +502,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float4 bc[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) bc[i] = *reinterpret_cast<const float4*>(sbc + q * 32 + 4 * i);
+                        const float2 ar2 = make_float2(ar, ar);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            m[4 * i + 0] = __uint_as_float(v[4 * i + 0]) * (ar * bc[i].x);
-                            m[4 * i + 1] = __uint_as_float(v[4 * i + 1]) * (ar * bc[i].y);
-                            m[4 * i + 2] = __uint_as_float(v[4 * i + 2]) * (ar * bc[i].z);
-                            m[4 * i + 3] = __uint_as_float(v[4 * i + 3]) * (ar * bc[i].w);
+                        for (int i = 0; i < 8; ++i) {  // packed pairs: half the multiply instructions
+                            const float2 w01 = fmul2(ar2, make_float2(bc[i].x, bc[i].y));
+                            const float2 w23 = fmul2(ar2, make_float2(bc[i].z, bc[i].w));
+                            const float2 m01 = fmul2(make_float2(__uint_as_float(v[4 * i + 0]), __uint_as_float(v[4 * i + 1])), w01);
+                            const float2 m23 = fmul2(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])), w23);
+                            m[4 * i + 0] = m01.x;
+                            m[4 * i + 1] = m01.y;
+                            m[4 * i + 2] = m23.x;
+                            m[4 * i + 3] = m23.y;
                         }
                     } else {  // steep decay in the diagonal block: the exact exponent per element
 #pragma unroll
@@ -607,7 +612,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 4; ++e) {
                         const float2 fv = __bfloat1622float2(p2[e]);
                         x4[e] = pack_f16x2(fv.x, fv.y);
-                        w4[e] = pack_f16x2(fv.x * w, fv.y * w);
+                        const float2 fw = fmul2(fv, make_float2(w, w));
+                        w4[e] = pack_f16x2(fw.x, fw.y);
                     }
                     hmax_abs4(mx, x4[0], x4[1], x4[2], x4[3]);
                     hmax_abs4(mx, w4[0], w4[1], w4[2], w4[3]);
