@@ -677,7 +677,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
 #pragma unroll
-                        for (int p = 0; p < 16; ++p) o[p] = __float_as_uint(hv[q4 * 16 + p] * dsb);
+                        for (int p = 0; p < 16; p += 2) {  // packed pairs
+                            const float2 f = fmul2(make_float2(hv[q4 * 16 + p], hv[q4 * 16 + p + 1]), make_float2(dsb, dsb));
+                            o[p] = __float_as_uint(f.x);
+                            o[p + 1] = __float_as_uint(f.y);
+                        }
                         tmem_st16(tm + lane_base + K::T_H + nb * 64 + q4 * 16, o);
                     }
                     if (K::RING) {  // this n-block's copy and decayed state are ready for S, C h
@@ -736,8 +740,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int ch = 0; ch < 4; ++ch) {
                             float o[8];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                o[i] = __uint_as_float(yv[ch * 8 + i]) + e * __uint_as_float(sv[ch * 8 + i]);
+                            for (int i = 0; i < 8; i += 2) {  // packed pairs
+                                const float2 f = ffma2(make_float2(e, e),
+                                                       make_float2(__uint_as_float(sv[ch * 8 + i]), __uint_as_float(sv[ch * 8 + i + 1])),
+                                                       make_float2(__uint_as_float(yv[ch * 8 + i]), __uint_as_float(yv[ch * 8 + i + 1])));
+                                o[i] = f.x;
+                                o[i + 1] = f.y;
+                            }
                             if (gate) gate8(o, zq[ch]);
                             uint32_t* o4 = reinterpret_cast<uint32_t*>(&ov[ch]);
 #pragma unroll
