@@ -36,14 +36,16 @@
 // One CTA per (block, group slice, batch) walks hpg / S heads of the group, with dB and dC
 // accumulated in TMEM across them; the S CTAs of a group form a thread-block cluster and add their
 // partial dB and dC through distributed shared memory in rank order, so the result is written once,
-// without atomics and in a fixed order (S = 1: no cluster).  Per head
-// the phases run one after another: the conversions (x and dy to float16 tiles, the two scaled tiles
-// 2^c dy and dt 2^(c_e - c) x, h0 and mu to float16), the products C B^T and dY X^T, the mask
-// (one thread per row and column quarter: M' = L o C B^T and Wd to float16 tiles), the products
-// G, B mu, C h0 and the dC / dB accumulations, and the epilogue.  The next head's inputs (raw x and
-// dy rows, its h0 and mu -- already float16, in the tiles' swizzled order -- and its dA_cumsum and dt
-// rows) are copied with cp.async into the tiles the products have finished with as soon as they
-// retire, so their loads overlap the epilogue.
+// without atomics and in a fixed order (S = 1: no cluster).  Per head the 512 worker threads run
+// the conversions (x and dy to float16 tiles, the two scaled tiles 2^c dy and dt 2^(c_e - c) x, h0 and
+// mu to float16), the mask (one thread per row and column quarter: M' = L o C B^T and Wd to float16
+// tiles) and the epilogue, one after another.  One more warp issues the products, each as soon as the
+// phase that writes its operands has signalled (mbarriers both ways): C B^T and dY X^T before the mask,
+// the unmasked dC / dB terms during it, G, B mu and C h0 after it, then the masked dC / dB terms and
+// the next head's C B^T while the workers run the epilogue and the next head's conversions.  The next
+// head's inputs (raw x and dy rows, its h0 and mu -- already float16, in the tiles' swizzled order --
+// its dA_cumsum and dt rows, D and A) are copied with cp.async into tiles the products have finished
+// with as soon as they retire, so their loads overlap the epilogue.
 // Operands are float16 (the inputs exactly, the derived tiles rounded once), accumulation float32.
 #include "common.cuh"
 #include "scan_util.cuh"
@@ -56,8 +58,10 @@ using namespace sm100;
 
 constexpr int T = kBwdBlock;     // tokens per block = the products' M
 constexpr int kP = 64;           // headdim
-constexpr int kThreads = 512;    // four warpgroups: warp w owns TMEM lanes 32 (w % 4) .. +31, column quarter w / 4
-constexpr int kNQ = kThreads / 128;  // column quarters of a row (mask, epilogue) and row parts (conversions)
+constexpr int kWorkers = 512;    // four warpgroups: warp w owns TMEM lanes 32 (w % 4) .. +31, column quarter w / 4
+constexpr int kIssuerWarp = kWorkers / 32;  // one more warp: its first thread issues the products
+constexpr int kThreads = kWorkers + 32;
+constexpr int kNQ = kWorkers / 128;  // column quarters of a row (mask, epilogue) and row parts (conversions)
 constexpr int kPanel = T * 128;  // one 64-column float16 panel of a T-row tile (16 KB)
 constexpr int kPanelP = kP * 128;  // one 64-column float16 panel of a P-row tile (8 KB)
 
@@ -75,8 +79,8 @@ struct BwdCfg {
     static constexpr int OFF_M = OFF_MU + NP * kPanelP;  // M' [r][i]; the epilogue's reductions after the products
     static constexpr int OFF_W = OFF_M + 2 * kPanel;     // Wd [r][j]
     static constexpr int OFF_CS = OFF_W + 2 * kPanel;    // cs[T], dt[T]
-    static constexpr int OFF_BAR = OFF_CS + 2 * T * 4;   // two mbarriers, TMEM base, abort flag, warp sums
-    static constexpr int SMEM = OFF_BAR + 128 + 1024;    // + slack to align the base to 1024 bytes
+    static constexpr int OFF_BAR = OFF_CS + 2 * T * 4;   // seven mbarriers, TMEM base, abort flag, warp sums
+    static constexpr int SMEM = OFF_BAR + 192 + 1024;    // + slack to align the base to 1024 bytes
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -95,7 +99,7 @@ struct BwdArgs {
     const __half *h0, *mu;  // block-start states and block-end gradients, float16 (b, nblk, H, P, N)
     const float* A;
     __nv_bfloat16* dx;
-    float *ddt, *dB, *dC, *dap, *xdy;  // dap, xdy: per (b, h, block) partial sums of dt dl and x . dy
+    float *ddt, *dB, *dC, *dap, *xdy;  // dap, xdy: per (b, h, block) four partial sums of dt dl and x . dy
     Dims d;
     Ctl ctl;
     int slices;  // S: CTAs (a cluster) per (block, group), each with hpg / S heads
@@ -116,6 +120,35 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
     return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
+// 4-byte asynchronous copy global -> shared (visible to the issuing thread after cp_async_wait_all)
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Barrier of the kWorkers worker threads only (named barrier 1; the issuer warp does not take part).
+__device__ __forceinline__ void worker_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory"); }
+
+// The same barrier, returning whether `p` holds on every worker thread.
+__device__ __forceinline__ bool worker_and(bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred a, q;\n\t"
+        "setp.ne.u32 a, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, a;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)p), "n"(kWorkers)
+        : "memory");
+    return r != 0;
+}
+
+// One arrival per warp on `bar` (initialised with one arrival per worker warp), after every lane's
+// writes: __syncwarp orders them before the first lane's release.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 template <int N>
 __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     using K = BwdCfg<N>;
@@ -124,10 +157,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     float* scs = reinterpret_cast<float*>(smem + K::OFF_CS);
     float* sdt = scs + T;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
-    uint64_t* stall_bar = bar + 1;  // never completed: the test hook's wait runs out on it
-    uint32_t* tmem_sh = reinterpret_cast<uint32_t*>(bar + 2);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 3);
-    float* wsum = reinterpret_cast<float*>(bar + 4);  // per-warp partial sums of <mu, h0> (16 floats)
+    uint64_t* stall_bar = bar;  // never completed: the test hook's wait runs out on it
+    // workers -> issuer, one arrival per worker warp and head: the float16 input tiles are written; M' and Wd
+    // are written (and C B^T, dY X^T read); G, B mu and C h0 are read
+    uint64_t *ev_in = bar + 1, *ev_mask = bar + 2, *ev_epi = bar + 3;
+    // issuer -> workers, one commit per head: C B^T and dY X^T; G, B mu and C h0; and, once, every product
+    uint64_t *mm1 = bar + 4, *mm2 = bar + 5, *mm_done = bar + 6;
+    uint32_t* tmem_sh = reinterpret_cast<uint32_t*>(bar + 7);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 8);
+    float* wsum = reinterpret_cast<float*>(bar + 9);  // per-warp partial sums of <mu, h0> (16 floats)
+    float* hconst = wsum + 16;                        // the current head's D and A
+    // the next head's dA_cumsum and dt rows, D and A, copied during the epilogue into the upper half of the
+    // M' tile (free from the products' reading it until the next head's mask)
+    float* stg = reinterpret_cast<float*>(smem + K::OFF_M + kPanel);
 
     const Dims& d = a.d;
     const int S = a.slices;
@@ -144,8 +186,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     const uint64_t wait_ns = a.ctl.wait_ns;
 
     if (tid == 0) {
-        mbar_init(bar, 1);
         mbar_init(stall_bar, 1);
+        mbar_init(ev_in, kWorkers / 32);
+        mbar_init(ev_mask, kWorkers / 32);
+        mbar_init(ev_epi, kWorkers / 32);
+        mbar_init(mm1, 1);
+        mbar_init(mm2, 1);
+        mbar_init(mm_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -153,25 +200,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         tmem_alloc(tmem_sh, 512);
         tmem_relinquish();
     }
-    // the block's B and C rows (float16 copies), once for all heads of the group
-    for (int c = tid; c < T * N / 8; c += kThreads) {
-        const int row = c / (N / 8), cc = c % (N / 8);
-        const int64_t tok = t0 + row;
-        uint4 vb = make_uint4(0, 0, 0, 0), vc = make_uint4(0, 0, 0, 0);
-        if (tok < L) {
-            const int64_t o = ((b * L + tok) * G + g) * (int64_t)N + cc * 8;
-            vb = __ldg(reinterpret_cast<const uint4*>(a.B16 + o));
-            vc = __ldg(reinterpret_cast<const uint4*>(a.C16 + o));
-        }
-        const uint32_t so = (cc >> 3) * kPanel + sw128_offset(row, cc & 7);
-        *reinterpret_cast<uint4*>(smem + K::OFF_B + so) = vb;
-        *reinterpret_cast<uint4*>(smem + K::OFF_C + so) = vc;
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tm = *tmem_sh;
     const uint32_t sC = smem_u32(smem + K::OFF_C), sB = smem_u32(smem + K::OFF_B);
     const uint32_t sX = smem_u32(smem + K::OFF_X), sDY = smem_u32(smem + K::OFF_DY);
     const uint32_t sDYS = smem_u32(smem + K::OFF_DYS), sXS = smem_u32(smem + K::OFF_XS);
@@ -180,23 +208,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     constexpr uint32_t kIdescN = idesc_fp16(128, N, false, true);  // dY' h0^T, Wd B, X' mu^T
     constexpr uint32_t kIdescNT = idesc_fp16(128, N, true, true);  // Wd^T C
 
-    bool ok = true;
-    if (a.ctl.stall && tid == 0) ok = mbar_wait_bounded(stall_bar, 0, abort_flag, err, 60, wait_ns);
-    ok = __syncthreads_and(ok);
-
     // Inputs of head hh: its x and dy rows (bfloat16) into the swizzled positions of the XS / DYS
     // tiles (zeros past the sequence end), h0 and mu (float16 rows p) straight into the H0 / MU tiles,
-    // this thread's dA_cumsum (tid < T) or dt value of the block into `csdt`, and the head's D and A into
-    // `dnext` and `anext` (loads in flight while the current head finishes).
-    float dnext = 0.f, anext = 0.f;
-    auto prefetch = [&](int hh, float& csdt) {
+    // this thread's dA_cumsum (tid < T) or dt value (T <= tid < 2 T) of the block and (thread 0) the head's
+    // D and A into `stg`: copies in flight while the current head finishes, none held in registers.
+    const uint32_t stg_s = smem_u32(stg);
+    auto prefetch = [&](int hh) {
         const int64_t crow = ((int64_t)b * H + hh) * rowlen + t0;
-        if (tid < 2 * T) csdt = (tid < T) ? __ldg(a.cs + crow + tid) : __ldg(a.dtt + crow + tid - T);
-        dnext = (a.D != nullptr) ? __ldg(a.D + hh) : 0.f;
-        anext = __ldg(a.A + hh);
+        if (tid < 2 * T) cp_async4(stg_s + 4 * tid, tid < T ? a.cs + crow + tid : a.dtt + crow + tid - T);
+        if (tid == 0) {
+            if (a.D != nullptr) cp_async4(stg_s + 8 * T, a.D + hh);
+            else stg[2 * T] = 0.f;
+            cp_async4(stg_s + 8 * T + 4, a.A + hh);
+        }
 #pragma unroll
-        for (int i = 0; i < T * 8 / kThreads; ++i) {
-            const int c = tid + i * kThreads;
+        for (int i = 0; i < T * 8 / kWorkers; ++i) {
+            const int c = tid + i * kWorkers;
             const int row = c >> 3, ch = c & 7;
             const int64_t tok = t0 + row;
             const int64_t o = ((b * L + (tok < L ? tok : 0)) * H + hh) * (int64_t)kP + ch * 8;
@@ -206,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         }
         const int64_t srow = (((int64_t)b * d.nchunks + blk) * H + hh) * (int64_t)kP * N;
 #pragma unroll
-        for (int i = 0; i < kP * N / 8 / kThreads; ++i) {  // 16-byte chunks: 8 columns n of row p
-            const int c = tid + i * kThreads;
+        for (int i = 0; i < kP * N / 8 / kWorkers; ++i) {  // 16-byte chunks: 8 columns n of row p
+            const int c = tid + i * kWorkers;
             const int p = c / (N / 8), cc = c % (N / 8);
             const uint32_t so = (cc >> 3) * kPanelP + sw128_offset(p, cc & 7);
             cp_async16(sH0 + so, a.h0 + srow + (int64_t)c * 8, 16u);
@@ -215,330 +242,377 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         }
         cp_async_commit();
     };
-    float csdt = 0.f;
-    if (ok) prefetch(g * hpg + slice * hps, csdt);
-
-    uint32_t phase = 0;
-    bool pending = false;  // a commit of `bar` issued and not yet seen complete
-    __half2 mx = __floats2half2_rn(0.f, 0.f);  // largest |value| converted to float16 (range flag)
-
-#pragma unroll 1
-    for (int k = 0; k < hps && ok; ++k) {
-        const int h = g * hpg + slice * hps + k;
-        const float Dh = dnext, Ah = anext;  // this head's D and A (loaded with its inputs)
-        // ---- this head's raw inputs (copied during the previous head's epilogue) -> float16 tiles
+    // the block's B and C rows (float16 copies), once for all heads of the group, and the first head's
+    // inputs: all copies in flight together
+    for (int c = tid; c < T * N / 8; c += kThreads) {
+        const int row = c / (N / 8), cc = c % (N / 8);
+        const int64_t tok = t0 + row;
+        const int64_t o = ((b * L + (tok < L ? tok : 0)) * G + g) * (int64_t)N + cc * 8;
+        const uint32_t nb = tok < L ? 16u : 0u;  // zeros past the sequence end
+        const uint32_t so = (cc >> 3) * kPanel + sw128_offset(row, cc & 7);
+        cp_async16(sB + so, a.B16 + o, nb);
+        cp_async16(sC + so, a.C16 + o, nb);
+    }
+    cp_async_commit();
+    if (warp != kIssuerWarp) {
+        prefetch(g * hpg + slice * hps);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");  // B and C landed; the head's inputs may not have
+    } else {
         cp_async_wait_all();
-        if (tid < T) scs[tid] = csdt;
-        else if (tid < 2 * T) sdt[tid - T] = csdt;
-        __syncthreads();
-        const float ce = scs[T - 1];
-        {
-            const int rr = tid & (T - 1), hl = tid >> 7;  // row, quarter of the row's 64 channels
-            const float wx = sdt[rr] * fast_exp2(ce - scs[rr]);
-            const float wy = fast_exp2(scs[rr]);
-#pragma unroll
-            for (int j = 0; j < 8 / kNQ; ++j) {
-                const uint32_t so = sw128_offset(rr, (8 / kNQ) * hl + j);
-                const uint4 xv = *reinterpret_cast<const uint4*>(smem + K::OFF_XS + so);
-                const uint4 yv = *reinterpret_cast<const uint4*>(smem + K::OFF_DYS + so);
-                const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
-                const uint32_t* yw = reinterpret_cast<const uint32_t*>(&yv);
-                uint32_t ox[4], oxs[4], oy[4], oys[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 xf = bf2_to_f2(xw[e]), yf = bf2_to_f2(yw[e]);
-                    ox[e] = pack_f16x2(xf.x, xf.y);
-                    const float2 xs = fmul2(xf, make_float2(wx, wx));
-                    oxs[e] = pack_f16x2(xs.x, xs.y);
-                    oy[e] = pack_f16x2(yf.x, yf.y);
-                    const float2 ys = fmul2(yf, make_float2(wy, wy));
-                    oys[e] = pack_f16x2(ys.x, ys.y);
-                }
-                hmax_abs4(mx, ox[0], ox[1], ox[2], ox[3]);
-                hmax_abs4(mx, oxs[0], oxs[1], oxs[2], oxs[3]);
-                hmax_abs4(mx, oy[0], oy[1], oy[2], oy[3]);
-                hmax_abs4(mx, oys[0], oys[1], oys[2], oys[3]);
-                *reinterpret_cast<uint4*>(smem + K::OFF_X + so) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
-                *reinterpret_cast<uint4*>(smem + K::OFF_XS + so) = make_uint4(oxs[0], oxs[1], oxs[2], oxs[3]);
-                *reinterpret_cast<uint4*>(smem + K::OFF_DY + so) = make_uint4(oy[0], oy[1], oy[2], oy[3]);
-                *reinterpret_cast<uint4*>(smem + K::OFF_DYS + so) = make_uint4(oys[0], oys[1], oys[2], oys[3]);
-            }
-        }
-        float hmu = 0.f;  // this thread's part of <mu, h0> (over the float16 tiles)
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *tmem_sh;
+    bool ok = true;
+    if (a.ctl.stall && tid == 0) ok = mbar_wait_bounded(stall_bar, 0, abort_flag, err, 60, wait_ns);
+    ok = __syncthreads_and(ok);
+
+
+    __half2 mx = __floats2half2_rn(0.f, 0.f);  // largest |value| converted to float16 (range flag)
+    bool fin = true;                           // the issuer's final drain
+
+    if (warp == kIssuerWarp) {
+        // ---- the products, issued by one thread in the order the workers' phases need them; each waits only
+        //      for the phase that writes its operands, so the tensor pipe works while the workers convert,
+        //      mask and run the epilogue
+        if (lane == 0) {
 #pragma unroll 1
-        for (int i = 0; i < kP * N / 8 / kThreads; ++i) {
-            const int c = tid + i * kThreads;
-            const int p = c / (N / 8), cc = c % (N / 8);
-            const uint32_t so = (cc >> 3) * kPanelP + sw128_offset(p, cc & 7);
-            const uint4 hq = *reinterpret_cast<const uint4*>(smem + K::OFF_H0 + so);
-            const uint4 mq = *reinterpret_cast<const uint4*>(smem + K::OFF_MU + so);
-            const __half2* hh2 = reinterpret_cast<const __half2*>(&hq);
-            const __half2* mh2 = reinterpret_cast<const __half2*>(&mq);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 hf2 = __half22float2(hh2[e]), mf2 = __half22float2(mh2[e]);
-                hmu = fmaf(hf2.x, mf2.x, fmaf(hf2.y, mf2.y, hmu));
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) hmu += __shfl_xor_sync(0xffffffffu, hmu, off);
-        if (lane == 0) wsum[warp] = hmu;
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // ---- C B^T (K = n; the first head only -- later heads' was issued during the previous epilogue)
-        //      and dY X^T (K = p)
-        if (tid == 0) {
-            tc_fence_after();
-            if (k == 0) issue_cb<N>(tm, sC, sB);
-#pragma unroll
-            for (int kk = 0; kk < kP / 16; ++kk)
-                mma_ss(tm + T_DX, desc_sw128(sDY + kk * 32, 16, 1024), desc_sw128(sX + kk * 32, 16, 1024), kIdescTT,
-                       kk > 0);
-            mma_commit(bar);
-        }
-        pending = true;
-        ok = mbar_wait_bounded(bar, phase, abort_flag, err, 61, wait_ns);
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-        phase ^= 1;
-        pending = false;
-        tc_fence_after();
-        // ---- mask: row r, columns [32 qc, 32 qc + 32) of M' = L o C B^T and Wd = L o dY X^T o dt_j,
-        //      16 at a time
-        float2 rho1p = make_float2(0.f, 0.f);  // sum_j Wd[r][j] (C_r . B_j) over this quarter: even / odd j
-        {
-            const float cr = scs[r];
-#pragma unroll 1
-            for (int c2 = 0; c2 < 2; ++c2) {
-                const int i0 = 32 * qc + 16 * c2;
-                uint32_t vcb[16], vdx[16];
-                tmem_ld16(tm + lane_base + T_CB + i0, vcb);
-                tmem_ld16(tm + lane_base + T_DX + i0, vdx);
-                tmem_ld_wait16(vcb);
-                tmem_ld_wait16(vdx);
-                uint32_t pm[8], pw[8];
-#pragma unroll
-                for (int jj = 0; jj < 16; jj += 2) {  // packed pairs of columns
-                    const int i = i0 + jj;
-                    const float2 dec = make_float2((i <= r) ? fast_exp2(cr - scs[i]) : 0.f,
-                                                   (i + 1 <= r) ? fast_exp2(cr - scs[i + 1]) : 0.f);
-                    const float2 cb = make_float2(__uint_as_float(vcb[jj]), __uint_as_float(vcb[jj + 1]));
-                    const float2 mv = fmul2(dec, cb);
-                    const float2 wv = fmul2(fmul2(dec, make_float2(sdt[i], sdt[i + 1])),
-                                            make_float2(__uint_as_float(vdx[jj]), __uint_as_float(vdx[jj + 1])));
-                    rho1p = ffma2(wv, cb, rho1p);
-                    pm[jj / 2] = pack_f16x2(mv.x, mv.y);
-                    pw[jj / 2] = pack_f16x2(wv.x, wv.y);
-                }
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {  // columns i0 .. i0 + 15: panel qc / 2, chunks 4 (qc % 2) + 2 c2 + j
-                    hmax_abs4(mx, pm[4 * j], pm[4 * j + 1], pm[4 * j + 2], pm[4 * j + 3]);
-                    hmax_abs4(mx, pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
-                    const uint32_t so = (qc >> 1) * kPanel + sw128_offset(r, 4 * (qc & 1) + 2 * c2 + j);
-                    *reinterpret_cast<uint4*>(smem + K::OFF_M + so) =
-                        make_uint4(pm[4 * j], pm[4 * j + 1], pm[4 * j + 2], pm[4 * j + 3]);
-                    *reinterpret_cast<uint4*>(smem + K::OFF_W + so) =
-                        make_uint4(pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
-                }
-            }
-        }
-        // the dC / dB terms that need no mask, dY' h0^T and X' mu^T (K = p): issued once this thread's own
-        // mask rows are written, so that they run while the other warps finish theirs (the next commit
-        // covers them)
-        if (tid == 0) {
-#pragma unroll
-            for (int kk = 0; kk < kP / 16; ++kk) {
-                mma_ss(tm + T_DC, desc_sw128(sDYS + kk * 32, 16, 1024), desc_sw128(sH0 + kk * 2048, kPanelP, 1024),
-                       kIdescN, k > 0 || kk > 0);
-                mma_ss(tm + T_DB, desc_sw128(sXS + kk * 32, 16, 1024), desc_sw128(sMU + kk * 2048, kPanelP, 1024),
-                       kIdescN, k > 0 || kk > 0);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // ---- G = M'^T dY, B mu, C h0, dC (+)= dY' h0^T + Wd B, dB (+)= X' mu^T + Wd^T C
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < T / 16; ++kk)  // K = r
-                mma_ss(tm + T_G, desc_sw128(sM + kk * 2048, kPanel, 1024), desc_sw128(sDY + kk * 2048, kPanel, 1024),
-                       kIdescG, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < N / 16; ++kk) {  // K = n
-                const uint32_t offT = (kk >> 2) * kPanel + (kk & 3) * 32;
-                const uint32_t offP = (kk >> 2) * kPanelP + (kk & 3) * 32;
-                mma_ss(tm + T_GMU, desc_sw128(sB + offT, 16, 1024), desc_sw128(sMU + offP, 16, 1024), kIdescP, kk > 0);
-                mma_ss(tm + T_YS, desc_sw128(sC + offT, 16, 1024), desc_sw128(sH0 + offP, 16, 1024), kIdescP, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < T / 16; ++kk) {  // K = tokens
-                const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-                mma_ss(tm + T_DC, desc_sw128(sW + off, 16, 1024), desc_sw128(sB + kk * 2048, kPanel, 1024), kIdescN, 1);
-                mma_ss(tm + T_DB, desc_sw128(sW + kk * 2048, kPanel, 1024), desc_sw128(sC + kk * 2048, kPanel, 1024),
-                       kIdescNT, 1);
-            }
-            mma_commit(bar);
-        }
-        pending = true;
-        ok = mbar_wait_bounded(bar, phase, abort_flag, err, 62, wait_ns);
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-        phase ^= 1;
-        pending = false;
-        tc_fence_after();
-        // the products have read the XS, DYS, H0 and MU tiles: the next head's inputs go there
-        if (k + 1 < hps) prefetch(h + 1, csdt);
-        // ---- epilogue: row r, channels [16 qc, 16 qc + 16)
-        {
-            float* red = reinterpret_cast<float*>(smem + K::OFF_M);  // [quantity][quarter][T]; M' is consumed
-            const int64_t tok = t0 + r;
-            const float ext = fast_exp2(ce - scs[r]), dtr = sdt[r];
-            uint32_t vg[16], vm[16];
-            tmem_ld16(tm + lane_base + T_G + 16 * qc, vg);
-            tmem_ld16(tm + lane_base + T_GMU + 16 * qc, vm);
-            tmem_ld_wait16(vg);
-            tmem_ld_wait16(vm);
-            // x . G (pairs in the block), x . B mu, x . dy: even / odd channel partial sums
-            float2 sg2 = make_float2(0.f, 0.f), sm2 = make_float2(0.f, 0.f), xdy2 = make_float2(0.f, 0.f);
-            uint32_t ob[8];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const uint4 xq = *reinterpret_cast<const uint4*>(smem + K::OFF_X + sw128_offset(r, 2 * qc + j));
-                const uint4 yq = *reinterpret_cast<const uint4*>(smem + K::OFF_DY + sw128_offset(r, 2 * qc + j));
-                const __half2* xh = reinterpret_cast<const __half2*>(&xq);
-                const __half2* yh = reinterpret_cast<const __half2*>(&yq);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {  // packed pairs of channels
-                    const int c = 8 * j + 2 * e;
-                    const float2 xf = __half22float2(xh[e]), yf = __half22float2(yh[e]);
-                    const float2 gi = make_float2(__uint_as_float(vg[c]), __uint_as_float(vg[c + 1]));
-                    const float2 gm = make_float2(__uint_as_float(vm[c]), __uint_as_float(vm[c + 1]));
-                    sg2 = ffma2(xf, gi, sg2);
-                    sm2 = ffma2(xf, gm, sm2);
-                    xdy2 = ffma2(xf, yf, xdy2);
-                    const float g0 = fmaf(ext, gm.x, gi.x), g1 = fmaf(ext, gm.y, gi.y);
-                    ob[4 * j + e] = pack_bf16x2(fmaf(dtr, g0, Dh * yf.x), fmaf(dtr, g1, Dh * yf.y));
-                }
-            }
-            if (tok < L) {
-                uint4* dst = reinterpret_cast<uint4*>(a.dx + ((b * L + tok) * H + h) * (int64_t)kP + 16 * qc);
-#pragma unroll
-                for (int j = 0; j < 2; ++j) dst[j] = make_uint4(ob[4 * j], ob[4 * j + 1], ob[4 * j + 2], ob[4 * j + 3]);
-            }
-            uint32_t vy[16];
-            tmem_ld16(tm + lane_base + T_YS + 16 * qc, vy);
-            tmem_ld_wait16(vy);
-            float2 rho22 = make_float2(0.f, 0.f);  // dy_r . (C_r h0) over this quarter: even / odd channels
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const uint4 yq = *reinterpret_cast<const uint4*>(smem + K::OFF_DY + sw128_offset(r, 2 * qc + j));
-                const __half2* yh = reinterpret_cast<const __half2*>(&yq);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = 8 * j + 2 * e;
-                    rho22 = ffma2(__half22float2(yh[e]), make_float2(__uint_as_float(vy[c]), __uint_as_float(vy[c + 1])),
-                                  rho22);
-                }
-            }
-            red[(0 * kNQ + qc) * T + r] = sg2.x + sg2.y;
-            red[(1 * kNQ + qc) * T + r] = sm2.x + sm2.y;
-            red[(2 * kNQ + qc) * T + r] = rho22.x + rho22.y;
-            red[(3 * kNQ + qc) * T + r] = rho1p.x + rho1p.y;
-            red[(4 * kNQ + qc) * T + r] = xdy2.x + xdy2.y;
-            tc_fence_before();
-            __syncthreads();
-            // every TMEM read of this head is done: the next head's C B^T (it needs only the block's B / C)
-            // runs during the rest of this epilogue and the next head's conversions
-            if (tid == 0 && k + 1 < hps) {
+            for (int k = 0; k < hps && ok; ++k) {
+                const uint32_t par = k & 1;
+                // this head's float16 tiles (x, dy, the scaled x and dy, h0, mu) are written
+                if (!(ok = mbar_wait_bounded(ev_in, par, abort_flag, err, 64, wait_ns))) break;
                 tc_fence_after();
-                issue_cb<N>(tm, sC, sB);
-            }
-            // the scans over the block's tokens run on warps 1-4 (token t = tid - 32, scan warp sw = warp - 1),
-            // so that warp 0, whose thread 0 issues the products, does not delay them
-            const int sw = warp - 1;
-            const bool scan = tid >= 32 && tid < 32 + T;
-            float* wtot = red + 5 * kNQ * T;  // per-warp totals of the scans: [v or w][scan warp]
-            // quantity q of row t summed over the quarters, in a fixed order
-            auto qsum = [&](int q, int t) {
-                const float* rq = red + q * kNQ * T + t;
-                return (rq[0] + rq[T]) + (rq[2 * T] + rq[3 * T]);
-            };
-            float v = 0.f, wv = 0.f, pv = 0.f, pw = 0.f, sfull = 0.f, dtl = 0.f, xd = 0.f;
-            if (scan) {
-                const int t = tid - 32;
-                const float dtt = sdt[t], ex = fast_exp2(ce - scs[t]);
-                const float sgt = qsum(0, t), smt = qsum(1, t);
-                sfull = fmaf(ex, smt, sgt);                      // x_t . G_t
-                v = dtt * ex * smt;                              // mu's part, at token t
-                wv = fmaf(fast_exp2(scs[t]), qsum(2, t),         // rho2 + rho1 - sigma
-                          qsum(3, t)) - dtt * sgt;
-                dtl = dtt;
-                xd = qsum(4, t);
-                // inclusive scans of v and w inside the warp
-                pv = v;
-                pw = wv;
+                if (k == 0) issue_cb<N>(tm, sC, sB);  // later heads': issued after the previous epilogue's reads
 #pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float ov = __shfl_up_sync(0xffffffffu, pv, off);
-                    const float ow = __shfl_up_sync(0xffffffffu, pw, off);
-                    if (lane >= off) {
-                        pv += ov;
-                        pw += ow;
-                    }
-                }
-                if (lane == 31) {
-                    wtot[sw] = pv;
-                    wtot[4 + sw] = pw;
-                }
-            }
-            __syncthreads();
-            if (scan) {
-                const int t = tid - 32;
-                float bv = 0.f, bw = 0.f, tw = 0.f;  // earlier warps' totals; all of w
+                for (int kk = 0; kk < kP / 16; ++kk)  // dY X^T (K = p)
+                    mma_ss(tm + T_DX, desc_sw128(sDY + kk * 32, 16, 1024), desc_sw128(sX + kk * 32, 16, 1024),
+                           kIdescTT, kk > 0);
+                mma_commit(mm1);
+                // the dC / dB terms that need no mask, dY' h0^T and X' mu^T (K = p): they run during the mask
 #pragma unroll
-                for (int k2 = 0; k2 < 4; ++k2) {
-                    if (k2 < sw) {
-                        bv += wtot[k2];
-                        bw += wtot[4 + k2];
-                    }
-                    tw += wtot[4 + k2];
+                for (int kk = 0; kk < kP / 16; ++kk) {
+                    mma_ss(tm + T_DC, desc_sw128(sDYS + kk * 32, 16, 1024), desc_sw128(sH0 + kk * 2048, kPanelP, 1024),
+                           kIdescN, k > 0 || kk > 0);
+                    mma_ss(tm + T_DB, desc_sw128(sXS + kk * 32, 16, 1024), desc_sw128(sMU + kk * 2048, kPanelP, 1024),
+                           kIdescN, k > 0 || kk > 0);
                 }
-                float hmu_all = 0.f;
+                // M' and Wd are written and the mask's reads of C B^T and dY X^T are done
+                if (!(ok = mbar_wait_bounded(ev_mask, par, abort_flag, err, 65, wait_ns))) break;
+                tc_fence_after();
+                // G = M'^T dY, B mu, C h0: the epilogue's operands
 #pragma unroll
-                for (int w4 = 0; w4 < kThreads / 32; w4 += 4)
-                    hmu_all += (wsum[w4] + wsum[w4 + 1]) + (wsum[w4 + 2] + wsum[w4 + 3]);
-                // dl_t = 2^(c_e) <mu, h0> + (v before t) + (w from t on)
-                const float excl_v = bv + pv - v;
-                const float from_t_w = tw - (bw + pw - wv);
-                const float dl = fmaf(fast_exp2(ce), hmu_all, excl_v + from_t_w);
-                if (t0 + t < L) a.ddt[((b * L + t0 + t) * H + h)] = fmaf(Ah, dl, sfull);
-                float da = dtl * dl;
+                for (int kk = 0; kk < T / 16; ++kk)  // K = r
+                    mma_ss(tm + T_G, desc_sw128(sM + kk * 2048, kPanel, 1024), desc_sw128(sDY + kk * 2048, kPanel, 1024),
+                           kIdescG, kk > 0);
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    da += __shfl_xor_sync(0xffffffffu, da, off);
-                    xd += __shfl_xor_sync(0xffffffffu, xd, off);
+                for (int kk = 0; kk < N / 16; ++kk) {  // K = n
+                    const uint32_t offT = (kk >> 2) * kPanel + (kk & 3) * 32;
+                    const uint32_t offP = (kk >> 2) * kPanelP + (kk & 3) * 32;
+                    mma_ss(tm + T_GMU, desc_sw128(sB + offT, 16, 1024), desc_sw128(sMU + offP, 16, 1024), kIdescP,
+                           kk > 0);
+                    mma_ss(tm + T_YS, desc_sw128(sC + offT, 16, 1024), desc_sw128(sH0 + offP, 16, 1024), kIdescP,
+                           kk > 0);
                 }
-                if (lane == 0) {
-                    wtot[8 + sw] = da;
-                    wtot[12 + sw] = xd;
+                mma_commit(mm2);
+                // dC += Wd B, dB += Wd^T C (K = tokens): they read only the Wd, B and C tiles, which neither the
+                // epilogue nor the next head's copies and conversions write; the next head's mask writes Wd only
+                // after mm1 of the next head, whose commit covers them
+#pragma unroll
+                for (int kk = 0; kk < T / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+                    mma_ss(tm + T_DC, desc_sw128(sW + off, 16, 1024), desc_sw128(sB + kk * 2048, kPanel, 1024), kIdescN,
+                           1);
+                    mma_ss(tm + T_DB, desc_sw128(sW + kk * 2048, kPanel, 1024), desc_sw128(sC + kk * 2048, kPanel, 1024),
+                           kIdescNT, 1);
+                }
+                if (k + 1 < hps) {
+                    // the epilogue has read G, B mu and C h0: the next head's C B^T (only the block's B / C) goes
+                    // into their columns
+                    if (!(ok = mbar_wait_bounded(ev_epi, par, abort_flag, err, 66, wait_ns))) break;
+                    tc_fence_after();
+                    issue_cb<N>(tm, sC, sB);
                 }
             }
-            __syncthreads();
+            // everything issued retires before TMEM is read or released, whatever happened above
+            mma_commit(mm_done);
+            fin = mbar_wait_drain(mm_done, 0, err, 63, kDrainNs);
+        }
+        __syncwarp();
+    } else {
+#pragma unroll 1
+        for (int k = 0; k < hps && ok; ++k) {
+            const int h = g * hpg + slice * hps + k;
+            const uint32_t par = k & 1;
+            // ---- this head's raw inputs (copied during the previous head's epilogue) -> float16 tiles
+            cp_async_wait_all();
+            if (tid < 2 * T) scs[tid] = stg[tid];  // dA_cumsum then dt: `sdt` follows `scs`
             if (tid == 0) {
-                const int64_t o = ((int64_t)b * H + h) * d.nchunks + blk;
-                a.dap[o] = (wtot[8] + wtot[9]) + (wtot[10] + wtot[11]);
-                a.xdy[o] = (wtot[12] + wtot[13]) + (wtot[14] + wtot[15]);
+                hconst[0] = stg[2 * T];
+                hconst[1] = stg[2 * T + 1];
+            }
+            worker_sync();
+            const float ce = scs[T - 1];
+            {
+                const int rr = tid & (T - 1), hl = tid >> 7;  // row, quarter of the row's 64 channels
+                const float wx = sdt[rr] * fast_exp2(ce - scs[rr]);
+                const float wy = fast_exp2(scs[rr]);
+#pragma unroll
+                for (int j = 0; j < 8 / kNQ; ++j) {
+                    const uint32_t so = sw128_offset(rr, (8 / kNQ) * hl + j);
+                    const uint4 xv = *reinterpret_cast<const uint4*>(smem + K::OFF_XS + so);
+                    const uint4 yv = *reinterpret_cast<const uint4*>(smem + K::OFF_DYS + so);
+                    const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+                    const uint32_t* yw = reinterpret_cast<const uint32_t*>(&yv);
+                    uint32_t ox[4], oxs[4], oy[4], oys[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 xf = bf2_to_f2(xw[e]), yf = bf2_to_f2(yw[e]);
+                        ox[e] = pack_f16x2(xf.x, xf.y);
+                        const float2 xs = fmul2(xf, make_float2(wx, wx));
+                        oxs[e] = pack_f16x2(xs.x, xs.y);
+                        oy[e] = pack_f16x2(yf.x, yf.y);
+                        const float2 ys = fmul2(yf, make_float2(wy, wy));
+                        oys[e] = pack_f16x2(ys.x, ys.y);
+                    }
+                    hmax_abs4(mx, ox[0], ox[1], ox[2], ox[3]);
+                    hmax_abs4(mx, oxs[0], oxs[1], oxs[2], oxs[3]);
+                    hmax_abs4(mx, oy[0], oy[1], oy[2], oy[3]);
+                    hmax_abs4(mx, oys[0], oys[1], oys[2], oys[3]);
+                    *reinterpret_cast<uint4*>(smem + K::OFF_X + so) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
+                    *reinterpret_cast<uint4*>(smem + K::OFF_XS + so) = make_uint4(oxs[0], oxs[1], oxs[2], oxs[3]);
+                    *reinterpret_cast<uint4*>(smem + K::OFF_DY + so) = make_uint4(oy[0], oy[1], oy[2], oy[3]);
+                    *reinterpret_cast<uint4*>(smem + K::OFF_DYS + so) = make_uint4(oys[0], oys[1], oys[2], oys[3]);
+                }
+            }
+            float hmu = 0.f;  // this thread's part of <mu, h0> (over the float16 tiles)
+#pragma unroll 1
+            for (int i = 0; i < kP * N / 8 / kWorkers; ++i) {
+                const int c = tid + i * kWorkers;
+                const int p = c / (N / 8), cc = c % (N / 8);
+                const uint32_t so = (cc >> 3) * kPanelP + sw128_offset(p, cc & 7);
+                const uint4 hq = *reinterpret_cast<const uint4*>(smem + K::OFF_H0 + so);
+                const uint4 mq = *reinterpret_cast<const uint4*>(smem + K::OFF_MU + so);
+                const __half2* hh2 = reinterpret_cast<const __half2*>(&hq);
+                const __half2* mh2 = reinterpret_cast<const __half2*>(&mq);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 hf2 = __half22float2(hh2[e]), mf2 = __half22float2(mh2[e]);
+                    hmu = fmaf(hf2.x, mf2.x, fmaf(hf2.y, mf2.y, hmu));
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) hmu += __shfl_xor_sync(0xffffffffu, hmu, off);
+            if (lane == 0) wsum[warp] = hmu;
+            fence_proxy_async_smem();  // the tiles written here (and the copies landed) are read by the products
+            warp_arrive(ev_in);
+            // ---- C B^T and dY X^T
+            ok = mbar_wait_bounded(mm1, par, abort_flag, err, 61, wait_ns);
+            ok = worker_and(ok);
+            if (!ok) break;
+            tc_fence_after();
+            // ---- mask: row r, columns [32 qc, 32 qc + 32) of M' = L o C B^T and Wd = L o dY X^T o dt_j,
+            //      16 at a time
+            float2 rho1p = make_float2(0.f, 0.f);  // sum_j Wd[r][j] (C_r . B_j) over this quarter: even / odd j
+            {
+                const float cr = scs[r];
+#pragma unroll 1
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int i0 = 32 * qc + 16 * c2;
+                    uint32_t vcb[16], vdx[16];
+                    tmem_ld16(tm + lane_base + T_CB + i0, vcb);
+                    tmem_ld16(tm + lane_base + T_DX + i0, vdx);
+                    tmem_ld_wait16(vcb);
+                    tmem_ld_wait16(vdx);
+                    uint32_t pm[8], pw[8];
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj += 2) {  // packed pairs of columns
+                        const int i = i0 + jj;
+                        const float2 dec = make_float2((i <= r) ? fast_exp2(cr - scs[i]) : 0.f,
+                                                       (i + 1 <= r) ? fast_exp2(cr - scs[i + 1]) : 0.f);
+                        const float2 cb = make_float2(__uint_as_float(vcb[jj]), __uint_as_float(vcb[jj + 1]));
+                        const float2 mv = fmul2(dec, cb);
+                        const float2 wv = fmul2(fmul2(dec, make_float2(sdt[i], sdt[i + 1])),
+                                                make_float2(__uint_as_float(vdx[jj]), __uint_as_float(vdx[jj + 1])));
+                        rho1p = ffma2(wv, cb, rho1p);
+                        pm[jj / 2] = pack_f16x2(mv.x, mv.y);
+                        pw[jj / 2] = pack_f16x2(wv.x, wv.y);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {  // columns i0 .. i0 + 15: panel qc / 2, chunks 4 (qc % 2) + 2 c2 + j
+                        hmax_abs4(mx, pm[4 * j], pm[4 * j + 1], pm[4 * j + 2], pm[4 * j + 3]);
+                        hmax_abs4(mx, pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
+                        const uint32_t so = (qc >> 1) * kPanel + sw128_offset(r, 4 * (qc & 1) + 2 * c2 + j);
+                        *reinterpret_cast<uint4*>(smem + K::OFF_M + so) =
+                            make_uint4(pm[4 * j], pm[4 * j + 1], pm[4 * j + 2], pm[4 * j + 3]);
+                        *reinterpret_cast<uint4*>(smem + K::OFF_W + so) =
+                            make_uint4(pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            warp_arrive(ev_mask);
+            // ---- G, B mu, C h0
+            ok = mbar_wait_bounded(mm2, par, abort_flag, err, 62, wait_ns);
+            ok = worker_and(ok);
+            if (!ok) break;
+            tc_fence_after();
+            // the committed products have read the XS, DYS, H0 and MU tiles: the next head's inputs go there
+            if (k + 1 < hps) prefetch(h + 1);
+            // ---- epilogue: row r, channels [16 qc, 16 qc + 16)
+            {
+                float* red = reinterpret_cast<float*>(smem + K::OFF_M);  // [quantity][quarter][T]; M' is consumed
+                const int64_t tok = t0 + r;
+                const float ext = fast_exp2(ce - scs[r]), dtr = sdt[r], Dh = hconst[0];
+                uint32_t vg[16], vm[16];
+                tmem_ld16(tm + lane_base + T_G + 16 * qc, vg);
+                tmem_ld16(tm + lane_base + T_GMU + 16 * qc, vm);
+                tmem_ld_wait16(vg);
+                tmem_ld_wait16(vm);
+                // x . G (pairs in the block), x . B mu, x . dy: even / odd channel partial sums
+                float2 sg2 = make_float2(0.f, 0.f), sm2 = make_float2(0.f, 0.f), xdy2 = make_float2(0.f, 0.f);
+                uint32_t ob[8];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint4 xq = *reinterpret_cast<const uint4*>(smem + K::OFF_X + sw128_offset(r, 2 * qc + j));
+                    const uint4 yq = *reinterpret_cast<const uint4*>(smem + K::OFF_DY + sw128_offset(r, 2 * qc + j));
+                    const __half2* xh = reinterpret_cast<const __half2*>(&xq);
+                    const __half2* yh = reinterpret_cast<const __half2*>(&yq);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {  // packed pairs of channels
+                        const int c = 8 * j + 2 * e;
+                        const float2 xf = __half22float2(xh[e]), yf = __half22float2(yh[e]);
+                        const float2 gi = make_float2(__uint_as_float(vg[c]), __uint_as_float(vg[c + 1]));
+                        const float2 gm = make_float2(__uint_as_float(vm[c]), __uint_as_float(vm[c + 1]));
+                        sg2 = ffma2(xf, gi, sg2);
+                        sm2 = ffma2(xf, gm, sm2);
+                        xdy2 = ffma2(xf, yf, xdy2);
+                        const float g0 = fmaf(ext, gm.x, gi.x), g1 = fmaf(ext, gm.y, gi.y);
+                        ob[4 * j + e] = pack_bf16x2(fmaf(dtr, g0, Dh * yf.x), fmaf(dtr, g1, Dh * yf.y));
+                    }
+                }
+                if (tok < L) {
+                    uint4* dst = reinterpret_cast<uint4*>(a.dx + ((b * L + tok) * H + h) * (int64_t)kP + 16 * qc);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        dst[j] = make_uint4(ob[4 * j], ob[4 * j + 1], ob[4 * j + 2], ob[4 * j + 3]);
+                }
+                uint32_t vy[16];
+                tmem_ld16(tm + lane_base + T_YS + 16 * qc, vy);
+                tmem_ld_wait16(vy);
+                // every TMEM read of this head is done: the next head's C B^T may overwrite these columns
+                if (k + 1 < hps) {
+                    tc_fence_before();
+                    warp_arrive(ev_epi);
+                }
+                float2 rho22 = make_float2(0.f, 0.f);  // dy_r . (C_r h0) over this quarter: even / odd channels
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint4 yq = *reinterpret_cast<const uint4*>(smem + K::OFF_DY + sw128_offset(r, 2 * qc + j));
+                    const __half2* yh = reinterpret_cast<const __half2*>(&yq);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 8 * j + 2 * e;
+                        rho22 = ffma2(__half22float2(yh[e]),
+                                      make_float2(__uint_as_float(vy[c]), __uint_as_float(vy[c + 1])), rho22);
+                    }
+                }
+                red[(0 * kNQ + qc) * T + r] = sg2.x + sg2.y;
+                red[(1 * kNQ + qc) * T + r] = sm2.x + sm2.y;
+                red[(2 * kNQ + qc) * T + r] = rho22.x + rho22.y;
+                red[(3 * kNQ + qc) * T + r] = rho1p.x + rho1p.y;
+                red[(4 * kNQ + qc) * T + r] = xdy2.x + xdy2.y;
+                worker_sync();
+                // the scans over the block's tokens run on warps 1-4 (token t = tid - 32, scan warp sw = warp - 1)
+                const int sw = warp - 1;
+                const bool scan = tid >= 32 && tid < 32 + T;
+                float* wtot = red + 5 * kNQ * T;  // per-warp totals of the scans: [v or w][scan warp]
+                // quantity q of row t summed over the quarters, in a fixed order
+                auto qsum = [&](int q, int t) {
+                    const float* rq = red + q * kNQ * T + t;
+                    return (rq[0] + rq[T]) + (rq[2 * T] + rq[3 * T]);
+                };
+                float v = 0.f, wv = 0.f, pv = 0.f, pw = 0.f, sfull = 0.f, dtl = 0.f, xd = 0.f;
+                float Ah = 0.f;  // read before the barrier below: thread 0 sets the next head's once past it
+                if (scan) {
+                    const int t = tid - 32;
+                    Ah = hconst[1];
+                    const float dtt = sdt[t], ex = fast_exp2(ce - scs[t]);
+                    const float sgt = qsum(0, t), smt = qsum(1, t);
+                    sfull = fmaf(ex, smt, sgt);                      // x_t . G_t
+                    v = dtt * ex * smt;                              // mu's part, at token t
+                    wv = fmaf(fast_exp2(scs[t]), qsum(2, t),         // rho2 + rho1 - sigma
+                              qsum(3, t)) - dtt * sgt;
+                    dtl = dtt;
+                    xd = qsum(4, t);
+                    // inclusive scans of v and w inside the warp
+                    pv = v;
+                    pw = wv;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const float ov = __shfl_up_sync(0xffffffffu, pv, off);
+                        const float ow = __shfl_up_sync(0xffffffffu, pw, off);
+                        if (lane >= off) {
+                            pv += ov;
+                            pw += ow;
+                        }
+                    }
+                    if (lane == 31) {
+                        wtot[sw] = pv;
+                        wtot[4 + sw] = pw;
+                    }
+                }
+                worker_sync();
+                if (scan) {
+                    const int t = tid - 32;
+                    float bv = 0.f, bw = 0.f, tw = 0.f;  // earlier warps' totals; all of w
+#pragma unroll
+                    for (int k2 = 0; k2 < 4; ++k2) {
+                        if (k2 < sw) {
+                            bv += wtot[k2];
+                            bw += wtot[4 + k2];
+                        }
+                        tw += wtot[4 + k2];
+                    }
+                    float hmu_all = 0.f;
+#pragma unroll
+                    for (int w4 = 0; w4 < kWorkers / 32; w4 += 4)
+                        hmu_all += (wsum[w4] + wsum[w4 + 1]) + (wsum[w4 + 2] + wsum[w4 + 3]);
+                    // dl_t = 2^(c_e) <mu, h0> + (v before t) + (w from t on)
+                    const float excl_v = bv + pv - v;
+                    const float from_t_w = tw - (bw + pw - wv);
+                    const float dl = fmaf(fast_exp2(ce), hmu_all, excl_v + from_t_w);
+                    if (t0 + t < L) a.ddt[((b * L + t0 + t) * H + h)] = fmaf(Ah, dl, sfull);
+                    float da = dtl * dl;
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        da += __shfl_xor_sync(0xffffffffu, da, off);
+                        xd += __shfl_xor_sync(0xffffffffu, xd, off);
+                    }
+                    // this scan warp's part of the block's sums: four per (b, h, block), added in order by
+                    // bwd_reduce_kernel
+                    if (lane == 0) {
+                        const int64_t o = (((int64_t)b * H + h) * d.nchunks + blk) * 4 + sw;
+                        a.dap[o] = da;
+                        a.xdy[o] = xd;
+                    }
+                }
+                // no barrier here: the next head's first writes that these reads could see (its D and A,
+                // its dA_cumsum and dt rows, the <mu, h0> partials) come after values read above, or after
+                // that head's first barrier
             }
         }
+        cp_async_wait_all();  // no copy is still landing when the shared memory is reused or released
     }
     flag_f16_range(err, hmax_to_float(mx));
-    cp_async_wait_all();  // no copy is still landing when the shared memory is reused or released
-    if (!ok && tid == 0 && pending) mbar_wait_drain(bar, phase, err, 63, kDrainNs);  // products retired first
+    // the issuer's drain has seen every product retire (or given up): TMEM may be read, then released
+    ok = __syncthreads_and(ok && fin);
+    tc_fence_after();
     const int64_t tok = t0 + r;
     if (S == 1) {
-        if (ok) {
+        if (ok && warp != kIssuerWarp) {
             // dC and dB rows of this block, summed over the group's heads
 #pragma unroll 1
             for (int c = 0; c < N / 64; ++c) {  // this warp's quarter of the columns, 16 at a time
@@ -565,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         // this CTA's partial dC and dB -> shared memory (the tiles are consumed), float32 [2][T][NS]
         constexpr int NS = N + 4;  // padded rows: the float4 stores of a warp fall on different banks
         float* acc = reinterpret_cast<float*>(smem);
-        if (ok) {
+        if (ok && warp != kIssuerWarp) {
 #pragma unroll 1
             for (int c = 0; c < N / 64; ++c) {  // this warp's quarter of the columns, 16 at a time
                 const int n0 = qc * (N / 4) + 16 * c;
@@ -644,8 +718,8 @@ __global__ void __launch_bounds__(kRedThreads) bwd_reduce_kernel(const float* __
     const int h = blockIdx.x, tid = threadIdx.x;
     float sa = 0.f, sd = 0.f;
     for (int b = 0; b < d.batch; ++b) {
-        const int64_t row = ((int64_t)b * d.nheads + h) * d.nchunks;
-        for (int64_t k = tid; k < d.nchunks; k += kRedThreads) {
+        const int64_t row = ((int64_t)b * d.nheads + h) * d.nchunks * 4;
+        for (int64_t k = tid; k < (int64_t)d.nchunks * 4; k += kRedThreads) {
             sa += dap[row + k];
             sd += xdy[row + k];
         }
