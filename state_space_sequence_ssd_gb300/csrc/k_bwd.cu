@@ -79,7 +79,7 @@ struct BwdCfg {
     static constexpr int OFF_M = OFF_MU + NP * kPanelP;  // M' [r][i]; the epilogue's reductions after the products
     static constexpr int OFF_W = OFF_M + 2 * kPanel;     // Wd [r][j]
     static constexpr int OFF_CS = OFF_W + 2 * kPanel;    // cs[T], dt[T]
-    static constexpr int OFF_BAR = OFF_CS + 2 * T * 4;   // seven mbarriers, TMEM base, abort flag, warp sums
+    static constexpr int OFF_BAR = OFF_CS + 2 * T * 4;   // eight mbarriers, TMEM base, abort flag, warp sums
     static constexpr int SMEM = OFF_BAR + 192 + 1024;    // + slack to align the base to 1024 bytes
     static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -158,14 +158,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     float* sdt = scs + T;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
     uint64_t* stall_bar = bar;  // never completed: the test hook's wait runs out on it
-    // workers -> issuer, one arrival per worker warp and head: the float16 input tiles are written; M' and Wd
-    // are written (and C B^T, dY X^T read); G, B mu and C h0 are read
-    uint64_t *ev_in = bar + 1, *ev_mask = bar + 2, *ev_epi = bar + 3;
+    // workers -> issuer, one arrival per worker warp and head: the float16 input tiles are written; the mask
+    // has read C B^T and dY X^T; M' and Wd are written; G, B mu and C h0 are read
+    uint64_t *ev_in = bar + 1, *ev_tfree = bar + 7, *ev_mask = bar + 2, *ev_epi = bar + 3;
     // issuer -> workers, one commit per head: C B^T and dY X^T; G, B mu and C h0; and, once, every product
     uint64_t *mm1 = bar + 4, *mm2 = bar + 5, *mm_done = bar + 6;
-    uint32_t* tmem_sh = reinterpret_cast<uint32_t*>(bar + 7);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 8);
-    float* wsum = reinterpret_cast<float*>(bar + 9);  // per-warp partial sums of <mu, h0> (16 floats)
+    uint32_t* tmem_sh = reinterpret_cast<uint32_t*>(bar + 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 9);
+    float* wsum = reinterpret_cast<float*>(bar + 10);  // per-warp partial sums of <mu, h0> (16 floats)
     float* hconst = wsum + 16;                        // the current head's D and A
     // the next head's dA_cumsum and dt rows, D and A, copied during the epilogue into the upper half of the
     // M' tile (free from the products' reading it until the next head's mask)
@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     if (tid == 0) {
         mbar_init(stall_bar, 1);
         mbar_init(ev_in, kWorkers / 32);
+        mbar_init(ev_tfree, kWorkers / 32);
         mbar_init(ev_mask, kWorkers / 32);
         mbar_init(ev_epi, kWorkers / 32);
         mbar_init(mm1, 1);
@@ -298,14 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                     mma_ss(tm + T_DB, desc_sw128(sXS + kk * 32, 16, 1024), desc_sw128(sMU + kk * 2048, kPanelP, 1024),
                            kIdescN, k > 0 || kk > 0);
                 }
-                // M' and Wd are written and the mask's reads of C B^T and dY X^T are done
-                if (!(ok = mbar_wait_bounded(ev_mask, par, abort_flag, err, 65, wait_ns))) break;
+                // the mask has read C B^T and dY X^T (it is still writing M' and Wd): B mu and C h0, the
+                // epilogue's operands that need no mask, go into their columns
+                if (!(ok = mbar_wait_bounded(ev_tfree, par, abort_flag, err, 67, wait_ns))) break;
                 tc_fence_after();
-                // G = M'^T dY, B mu, C h0: the epilogue's operands
-#pragma unroll
-                for (int kk = 0; kk < T / 16; ++kk)  // K = r
-                    mma_ss(tm + T_G, desc_sw128(sM + kk * 2048, kPanel, 1024), desc_sw128(sDY + kk * 2048, kPanel, 1024),
-                           kIdescG, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < N / 16; ++kk) {  // K = n
                     const uint32_t offT = (kk >> 2) * kPanel + (kk & 3) * 32;
@@ -315,6 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                     mma_ss(tm + T_YS, desc_sw128(sC + offT, 16, 1024), desc_sw128(sH0 + offP, 16, 1024), kIdescP,
                            kk > 0);
                 }
+                // M' and Wd are written: G = M'^T dY
+                if (!(ok = mbar_wait_bounded(ev_mask, par, abort_flag, err, 65, wait_ns))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < T / 16; ++kk)  // K = r
+                    mma_ss(tm + T_G, desc_sw128(sM + kk * 2048, kPanel, 1024), desc_sw128(sDY + kk * 2048, kPanel, 1024),
+                           kIdescG, kk > 0);
                 mma_commit(mm2);
                 // dC += Wd B, dB += Wd^T C (K = tokens): they read only the Wd, B and C tiles, which neither the
                 // epilogue nor the next head's copies and conversions write; the next head's mask writes Wd only
@@ -425,6 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                     tmem_ld16(tm + lane_base + T_DX + i0, vdx);
                     tmem_ld_wait16(vcb);
                     tmem_ld_wait16(vdx);
+                    if (c2 == 1) {  // this warp's last reads of C B^T and dY X^T
+                        tc_fence_before();
+                        warp_arrive(ev_tfree);
+                    }
                     uint32_t pm[8], pw[8];
 #pragma unroll
                     for (int jj = 0; jj < 16; jj += 2) {  // packed pairs of columns
