@@ -79,7 +79,7 @@ struct BwdCfg {
     static constexpr int OFF_M = OFF_MU + NP * kPanelP;  // M' [r][i]; the epilogue's reductions after the products
     static constexpr int OFF_W = OFF_M + 2 * kPanel;     // Wd [r][j]
     static constexpr int OFF_CS = OFF_W + 2 * kPanel;    // cs[T], dt[T]
-    static constexpr int OFF_BAR = OFF_CS + 2 * T * 4;   // eight mbarriers, TMEM base, abort flag, warp sums
+    static constexpr int OFF_BAR = OFF_CS + 2 * T * 4;   // nine mbarriers, TMEM base, abort flag, warp sums
     static constexpr int SMEM = OFF_BAR + 192 + 1024;    // + slack to align the base to 1024 bytes
     static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -158,9 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     float* sdt = scs + T;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
     uint64_t* stall_bar = bar;  // never completed: the test hook's wait runs out on it
-    // workers -> issuer, one arrival per worker warp and head: the float16 input tiles are written; the mask
+    // workers -> issuer, one arrival per worker warp and head: the float16 x and dy tiles are written; all
+    // float16 input tiles are written; the mask
     // has read C B^T and dY X^T; M' and Wd are written; G, B mu and C h0 are read
-    uint64_t *ev_in = bar + 1, *ev_tfree = bar + 7, *ev_mask = bar + 2, *ev_epi = bar + 3;
+    uint64_t *ev_xd = bar + 19, *ev_in = bar + 1, *ev_tfree = bar + 7, *ev_mask = bar + 2, *ev_epi = bar + 3;
     // issuer -> workers, one commit per head: C B^T and dY X^T; G, B mu and C h0; and, once, every product
     uint64_t *mm1 = bar + 4, *mm2 = bar + 5, *mm_done = bar + 6;
     uint32_t* tmem_sh = reinterpret_cast<uint32_t*>(bar + 8);
@@ -187,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
 
     if (tid == 0) {
         mbar_init(stall_bar, 1);
+        mbar_init(ev_xd, kWorkers / 32);
         mbar_init(ev_in, kWorkers / 32);
         mbar_init(ev_tfree, kWorkers / 32);
         mbar_init(ev_mask, kWorkers / 32);
@@ -282,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
 #pragma unroll 1
             for (int k = 0; k < hps && ok; ++k) {
                 const uint32_t par = k & 1;
-                // this head's float16 tiles (x, dy, the scaled x and dy, h0, mu) are written
-                if (!(ok = mbar_wait_bounded(ev_in, par, abort_flag, err, 64, wait_ns))) break;
+                // this head's float16 x and dy tiles are written
+                if (!(ok = mbar_wait_bounded(ev_xd, par, abort_flag, err, 68, wait_ns))) break;
                 tc_fence_after();
                 if (k == 0) issue_cb<N>(tm, sC, sB);  // later heads': issued after the previous epilogue's reads
 #pragma unroll
@@ -291,6 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                     mma_ss(tm + T_DX, desc_sw128(sDY + kk * 32, 16, 1024), desc_sw128(sX + kk * 32, 16, 1024),
                            kIdescTT, kk > 0);
                 mma_commit(mm1);
+                // the scaled x and dy, h0 and mu are in place too
+                if (!(ok = mbar_wait_bounded(ev_in, par, abort_flag, err, 64, wait_ns))) break;
+                tc_fence_after();
                 // the dC / dB terms that need no mask, dY' h0^T and X' mu^T (K = p): they run during the mask
 #pragma unroll
                 for (int kk = 0; kk < kP / 16; ++kk) {
@@ -358,10 +363,36 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
             }
             worker_sync();
             const float ce = scs[T - 1];
+            // N = 64: x and dy to float16 first, so that dY X^T starts while the scaled rows are written (a
+            // second read of the raw rows).  N = 128: one pass, both signals after it -- the split costs more
+            // registers than that kernel has at this thread count, and the spills it causes are slower.
             {
                 const int rr = tid & (T - 1), hl = tid >> 7;  // row, quarter of the row's 64 channels
                 const float wx = sdt[rr] * fast_exp2(ce - scs[rr]);
                 const float wy = fast_exp2(scs[rr]);
+                if constexpr (N == 64) {
+#pragma unroll
+                    for (int j = 0; j < 8 / kNQ; ++j) {
+                        const uint32_t so = sw128_offset(rr, (8 / kNQ) * hl + j);
+                        const uint4 xv = *reinterpret_cast<const uint4*>(smem + K::OFF_XS + so);
+                        const uint4 yv = *reinterpret_cast<const uint4*>(smem + K::OFF_DYS + so);
+                        const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+                        const uint32_t* yw = reinterpret_cast<const uint32_t*>(&yv);
+                        uint32_t ox[4], oy[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 xf = bf2_to_f2(xw[e]), yf = bf2_to_f2(yw[e]);
+                            ox[e] = pack_f16x2(xf.x, xf.y);
+                            oy[e] = pack_f16x2(yf.x, yf.y);
+                        }
+                        hmax_abs4(mx, ox[0], ox[1], ox[2], ox[3]);
+                        hmax_abs4(mx, oy[0], oy[1], oy[2], oy[3]);
+                        *reinterpret_cast<uint4*>(smem + K::OFF_X + so) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
+                        *reinterpret_cast<uint4*>(smem + K::OFF_DY + so) = make_uint4(oy[0], oy[1], oy[2], oy[3]);
+                    }
+                    fence_proxy_async_smem();
+                    warp_arrive(ev_xd);
+                }
 #pragma unroll
                 for (int j = 0; j < 8 / kNQ; ++j) {
                     const uint32_t so = sw128_offset(rr, (8 / kNQ) * hl + j);
@@ -369,24 +400,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                     const uint4 yv = *reinterpret_cast<const uint4*>(smem + K::OFF_DYS + so);
                     const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
                     const uint32_t* yw = reinterpret_cast<const uint32_t*>(&yv);
-                    uint32_t ox[4], oxs[4], oy[4], oys[4];
+                    uint32_t oxs[4], oys[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 xf = bf2_to_f2(xw[e]), yf = bf2_to_f2(yw[e]);
-                        ox[e] = pack_f16x2(xf.x, xf.y);
                         const float2 xs = fmul2(xf, make_float2(wx, wx));
                         oxs[e] = pack_f16x2(xs.x, xs.y);
-                        oy[e] = pack_f16x2(yf.x, yf.y);
                         const float2 ys = fmul2(yf, make_float2(wy, wy));
                         oys[e] = pack_f16x2(ys.x, ys.y);
                     }
-                    hmax_abs4(mx, ox[0], ox[1], ox[2], ox[3]);
                     hmax_abs4(mx, oxs[0], oxs[1], oxs[2], oxs[3]);
-                    hmax_abs4(mx, oy[0], oy[1], oy[2], oy[3]);
                     hmax_abs4(mx, oys[0], oys[1], oys[2], oys[3]);
-                    *reinterpret_cast<uint4*>(smem + K::OFF_X + so) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
+                    if constexpr (N != 64) {
+                        uint32_t ox[4], oy[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 xf = bf2_to_f2(xw[e]), yf = bf2_to_f2(yw[e]);
+                            ox[e] = pack_f16x2(xf.x, xf.y);
+                            oy[e] = pack_f16x2(yf.x, yf.y);
+                        }
+                        hmax_abs4(mx, ox[0], ox[1], ox[2], ox[3]);
+                        hmax_abs4(mx, oy[0], oy[1], oy[2], oy[3]);
+                        *reinterpret_cast<uint4*>(smem + K::OFF_X + so) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
+                        *reinterpret_cast<uint4*>(smem + K::OFF_DY + so) = make_uint4(oy[0], oy[1], oy[2], oy[3]);
+                    }
                     *reinterpret_cast<uint4*>(smem + K::OFF_XS + so) = make_uint4(oxs[0], oxs[1], oxs[2], oxs[3]);
-                    *reinterpret_cast<uint4*>(smem + K::OFF_DY + so) = make_uint4(oy[0], oy[1], oy[2], oy[3]);
                     *reinterpret_cast<uint4*>(smem + K::OFF_DYS + so) = make_uint4(oys[0], oys[1], oys[2], oys[3]);
                 }
             }
@@ -410,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
             for (int off = 16; off > 0; off >>= 1) hmu += __shfl_xor_sync(0xffffffffu, hmu, off);
             if (lane == 0) wsum[warp] = hmu;
             fence_proxy_async_smem();  // the tiles written here (and the copies landed) are read by the products
+            if constexpr (N != 64) warp_arrive(ev_xd);
             warp_arrive(ev_in);
             // ---- C B^T and dY X^T
             ok = mbar_wait_bounded(mm1, par, abort_flag, err, 61, wait_ns);
