@@ -141,6 +141,8 @@ int launch_bc_to_f16(const __nv_bfloat16* B, const __nv_bfloat16* C, const Dims&
                      int* err, cudaStream_t s);
 // B and C below are the float16 copies; x stays bfloat16.
 // S16: the span states written as float16 there instead of float32 to S (range flag in ctl.err)
+// Heads of one B group that a chunk_state CTA covers (they share its B tile): 4, 2 or 1.
+int chunk_state_heads_per_cta(const Dims& d);
 int launch_chunk_state_span(const __nv_bfloat16* x, const __half* B, const float* dtt, const float* cs,
                             int span_chunks, const Dims& d, float* S, float* span_decay, const Ctl& ctl,
                             cudaStream_t s, __half* S16 = nullptr);

@@ -44,7 +44,8 @@ constexpr int kMaxSpanChunks = 256;
 
 // HH heads of one B group per CTA: they share the B tile, and one MMA per
 // k-step covers all of them (N = 64 HH).  2 scaling warpgroups when HH > 1.
-template <int N, int HH>
+// ONE: a grid of at most one CTA per SM, which then takes twice the shared memory for stages.
+template <int N, int HH, bool ONE>
 struct StCfg {
     static constexpr int TB = 64;                      // tokens per stage
     static constexpr int BOX = TB * 128;               // one 64-column box, TB rows
@@ -57,16 +58,16 @@ struct StCfg {
     static constexpr int OFF_B = HH * BOX;
     static constexpr int OFF_CD = OFF_B + NBOX * BOX;
     static constexpr int SZ_STAGE = (OFF_CD + HH * 2 * TB * 4 + 1023) / 1024 * 1024;
-    // as many stages as fit about 200 KB (2 to 4): a stage refills only after its MMAs retire,
-    // so more, smaller stages keep more of the x stream in flight
-    static constexpr int NST_FIT = (100 * 1024) / SZ_STAGE;
+    // as many stages as fit about 100 KB (two CTAs per SM) or 208 KB (one), 2 to 4: a stage refills
+    // only after its MMAs retire, so more stages keep more of the x stream in flight
+    static constexpr int NST_FIT = ((ONE ? 208 : 100) * 1024) / SZ_STAGE;
     static constexpr int NST = NST_FIT < 2 ? 2 : (NST_FIT > 4 ? 4 : NST_FIT);
     static constexpr int OFF_ZERO = NST * SZ_STAGE;
     static constexpr int SZ_ZERO = (N == 64) ? BOX : 0;  // zero rows padding the A operand to 128
     static constexpr int OFF_R = OFF_ZERO + SZ_ZERO;     // HH x per chunk of the span: R_c + cs[c][Q-1]
     static constexpr int OFF_BAR = OFF_R + HH * kMaxSpanChunks * 4;
     static constexpr int SMEM = OFF_BAR + 256 + 1024;
-    static constexpr int CTAS_PER_SM = (SMEM <= 113 * 1024) ? 2 : 1;
+    static constexpr int CTAS_PER_SM = (!ONE && SMEM <= 113 * 1024) ? 2 : 1;
     static constexpr int TCOLS = MB * HH * 64 <= 32 ? 32 : (MB * HH * 64 <= 64 ? 64 : (MB * HH * 64 <= 128 ? 128 : (MB * HH * 64 <= 256 ? 256 : 512)));
     static_assert(MB * HH * 64 <= 512, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -85,11 +86,11 @@ struct StateArgs {
     int rev;            // reverse-time weights (one-chunk spans): w_t = 2^(cs(t)), no dt factor
 };
 
-template <int N, int HH>
-__global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_SM)
+template <int N, int HH, bool ONE>
+__global__ void __launch_bounds__(StCfg<N, HH, ONE>::THREADS, StCfg<N, HH, ONE>::CTAS_PER_SM)
     chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
                           StateArgs a) {
-    using K = StCfg<N, HH>;
+    using K = StCfg<N, HH, ONE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + K::OFF_BAR);
@@ -316,37 +317,73 @@ __global__ void __launch_bounds__(StCfg<N, HH>::THREADS, StCfg<N, HH>::CTAS_PER_
     if (warp == K::WARP_MMA) tmem_dealloc(tm, K::TCOLS);
 }
 
-template <int N, int HH>
-int launch_state_nh(const __nv_bfloat16* x, const __half* B, const StateArgs& a, cudaStream_t s) {
-    using K = StCfg<N, HH>;
+template <int N, int HH, bool ONE>
+int launch_state_nho(const __nv_bfloat16* x, const __half* B, const StateArgs& a, cudaStream_t s) {
+    using K = StCfg<N, HH, ONE>;
     const Dims& d = a.d;
     CUtensorMap tx, tb;
     const uint64_t dx[4] = {(uint64_t)d.headdim, (uint64_t)d.nheads, (uint64_t)d.seqlen, (uint64_t)d.batch};
     const uint64_t db[4] = {(uint64_t)d.dstate, (uint64_t)d.ngroups, (uint64_t)d.seqlen, (uint64_t)d.batch};
     const uint32_t box[4] = {64, 1, (uint32_t)K::TB, 1};
     if (!make_tmap_16b_4d(&tx, x, dx, box) || !make_tmap_16b_4d(&tb, B, db, box)) return SSD_ERR_CUDA;
-    if (ensure_smem_limit(reinterpret_cast<const void*>(chunk_state_tc_kernel<N, HH>), K::SMEM) != SSD_OK)
+    if (ensure_smem_limit(reinterpret_cast<const void*>(chunk_state_tc_kernel<N, HH, ONE>), K::SMEM) != SSD_OK)
         return SSD_ERR_CUDA;
     dim3 grid(d.hcount / HH, a.nspans, d.batch);
     launch_begin(kKindChunkState, s);
-    const cudaError_t le = launch_dependent(chunk_state_tc_kernel<N, HH>, grid, dim3(K::THREADS), K::SMEM, s, tx, tb, a);
+    const cudaError_t le =
+        launch_dependent(chunk_state_tc_kernel<N, HH, ONE>, grid, dim3(K::THREADS), K::SMEM, s, tx, tb, a);
     const int r = launch_end(kKindChunkState, s);
     return le != cudaSuccess ? SSD_ERR_CUDA : r;
+}
+
+// Multiprocessor count of the current device (cached per device).
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 152;
+    }
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 152;
+        }
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// A grid that fits one CTA per SM gets the configuration with twice the stages.
+template <int N, int HH>
+int launch_state_nh(const __nv_bfloat16* x, const __half* B, const StateArgs& a, cudaStream_t s) {
+    const int64_t ctas = (int64_t)(a.d.hcount / HH) * a.nspans * a.d.batch;
+    if (ctas <= sm_count()) return launch_state_nho<N, HH, true>(x, B, a, s);
+    return launch_state_nho<N, HH, false>(x, B, a, s);
 }
 
 // Heads per CTA: as many of one group as divide evenly, up to 4 (N <= 128) or 2 (N >= 256); with a
 // head range, the CTAs' head blocks must also tile the range and start on a multiple of the block.
 template <int N>
 int launch_state_n(const __nv_bfloat16* x, const __half* B, const StateArgs& a, cudaStream_t s) {
-    const int hpg = a.d.nheads / a.d.ngroups;
-    auto fits = [&](int hh) { return hpg % hh == 0 && a.d.hcount % hh == 0 && a.d.head0 % hh == 0; };
-    constexpr int HMAX = (N <= 128) ? 4 : 2;
-    if (HMAX >= 4 && fits(4)) return launch_state_nh<N, (HMAX >= 4 ? 4 : 2)>(x, B, a, s);
-    if (fits(2)) return launch_state_nh<N, 2>(x, B, a, s);
-    return launch_state_nh<N, 1>(x, B, a, s);
+    switch (chunk_state_heads_per_cta(a.d)) {
+        case 4: return launch_state_nh<N, (N <= 128 ? 4 : 2)>(x, B, a, s);
+        case 2: return launch_state_nh<N, 2>(x, B, a, s);
+        default: return launch_state_nh<N, 1>(x, B, a, s);
+    }
 }
 
 }  // namespace
+
+int chunk_state_heads_per_cta(const Dims& d) {
+    const int hpg = d.nheads / d.ngroups;
+    auto fits = [&](int hh) { return hpg % hh == 0 && d.hcount % hh == 0 && d.head0 % hh == 0; };
+    const int hmax = (d.dstate <= 128) ? 4 : 2;
+    if (hmax >= 4 && fits(4)) return 4;
+    if (fits(2)) return 2;
+    return 1;
+}
 
 int launch_chunk_state_span(const __nv_bfloat16* x, const __half* B, const float* dtt, const float* cs,
                             int span_chunks, const Dims& d, float* S, float* span_decay, const Ctl& ctl,

@@ -206,9 +206,11 @@ __global__ void __launch_bounds__(kThreads) ssd_step_kernel_n64(const __nv_bfloa
 // ---------------------------------------------------------------- several tokens per launch
 // ssd_step_multi: K consecutive tokens of every sequence in one launch.  The state stays in
 // registers for all K tokens, so it is read and written once per launch instead of once per
-// token.  Each token's arithmetic (the lanes' split of n, the packed state update, the two partial
-// sums and the reduction order) is that of ssd_step, so K tokens here equal K ssd_step calls bit for
-// bit.
+// token.  The tokens' inputs (dt, the B, C and x rows) come through shared memory in groups of KT
+// tokens, copied asynchronously one group ahead, so one memory latency covers a group instead of
+// each token paying its own.  Each token's arithmetic (the lanes' split of n, the packed state
+// update, the two partial sums and the reduction order) is that of ssd_step, so K tokens here equal
+// K ssd_step calls bit for bit.
 // Sums R per-row partial values over the lanes of a row group (xor offsets OFF, OFF/2, ..., 1).
 // While a lane holds more than one row it keeps half of them and trades the other half with its
 // partner, so R rows over 2^k lanes cost (R - 1) + (k - log2 R) shuffles instead of R k (9 instead of
@@ -245,7 +247,27 @@ struct MultiCfg {
     static constexpr int RPS = 32 / LPR;             // rows of a warp per slot
     static constexpr int NV = N / (4 * LPR);         // float4 per lane per row
     static constexpr int SLOTS = 64 / (W * RPS);     // rows held by each lane
+    static constexpr int XW = SLOTS * RPS;           // a warp's rows (consecutive): 8, or 4 for N = 512
+    // tokens per staged group: their B, C and x rows and dt go to shared memory together (two groups,
+    // one filling while the other is used), so one memory latency covers KT tokens
+    static constexpr int KT = (N <= 128) ? 16 : (N == 256 ? 8 : 4);
+    static constexpr int OFF_C = KT * N * 2, OFF_X = 2 * KT * N * 2, OFF_DT = OFF_X + KT * 64 * 2;
+    static constexpr int SZ = OFF_DT + KT * 4;  // bytes per group buffer (a multiple of 16)
+    static_assert(SZ % 16 == 0, "group buffer alignment");
 };
+
+// 4-byte asynchronous copy global -> shared
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int NPEND>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(NPEND) : "memory");
+}
 
 template <int N>
 __global__ void __launch_bounds__(MultiCfg<N>::THREADS) ssd_step_multi_kernel(
@@ -254,35 +276,82 @@ __global__ void __launch_bounds__(MultiCfg<N>::THREADS) ssd_step_multi_kernel(
     float* __restrict__ state, int ntok, int nheads, int ngroups, __nv_bfloat16* __restrict__ y) {
     using K = MultiCfg<N>;
     constexpr int P = 64;
+    extern __shared__ __align__(16) uint8_t sbuf[];
     const int h = blockIdx.x, b = blockIdx.y;
     const int g = h / (nheads / ngroups);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sub = lane / K::LPR, ln = lane % K::LPR;
     const int64_t bh = (int64_t)b * nheads + h;
     float* st = state + bh * (int64_t)P * N;
+    // this lane's rows: slot i is row (warp SLOTS + i) RPS + sub, so a warp's rows are consecutive
+    auto row = [&](int i) { return (warp * K::SLOTS + i) * K::RPS + sub; };
+    // the rows of tokens k0 .. k0 + cnt - 1 into group buffer `buf`: 16-byte asynchronous copies when
+    // every row starts on 16 bytes, else element by element
+    const bool al = ((reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C) |
+                      reinterpret_cast<uintptr_t>(x)) & 15) == 0;
+    auto stage = [&](int buf, int k0, int cnt) {
+        uint8_t* sb = sbuf + buf * K::SZ;
+        const uint32_t ss = (uint32_t)__cvta_generic_to_shared(sb);
+        constexpr int RB = N / 8;                 // 16-byte pieces of a B or C row
+        const int total = cnt * (2 * RB + 8);     // B, C and x pieces
+        for (int c = tid; c < total; c += K::THREADS) {
+            const int t = c / (2 * RB + 8), q = c % (2 * RB + 8);
+            const int64_t bk = (int64_t)b * ntok + k0 + t;
+            const __nv_bfloat16* src;
+            uint32_t dst;
+            if (q < RB) {
+                src = B + (bk * ngroups + g) * N + q * 8;
+                dst = t * N * 2 + q * 16;
+            } else if (q < 2 * RB) {
+                src = C + (bk * ngroups + g) * N + (q - RB) * 8;
+                dst = K::OFF_C + t * N * 2 + (q - RB) * 16;
+            } else {
+                src = x + (bk * nheads + h) * P + (q - 2 * RB) * 8;
+                dst = K::OFF_X + t * P * 2 + (q - 2 * RB) * 16;
+            }
+            if (al) {
+                cp_async16(ss + dst, src);
+            } else {
+                __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(sb + dst);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) d[e] = src[e];
+            }
+        }
+        if (tid < cnt) cp_async4(ss + K::OFF_DT + 4 * tid, dt + ((int64_t)b * ntok + k0 + tid) * nheads + h);
+        cp_async_commit();
+    };
+    stage(0, 0, ntok < K::KT ? ntok : K::KT);
     float4 s[K::SLOTS][K::NV];
 #pragma unroll
     for (int i = 0; i < K::SLOTS; ++i)
 #pragma unroll
         for (int v = 0; v < K::NV; ++v)
-            s[i][v] = *reinterpret_cast<const float4*>(st + (int64_t)((i * K::W + warp) * K::RPS + sub) * N +
-                                                       4 * ln + v * 4 * K::LPR);
+            s[i][v] = *reinterpret_cast<const float4*>(st + (int64_t)row(i) * N + 4 * ln + v * 4 * K::LPR);
     const float Ah = A[h];
     const float Dh = (D != nullptr) ? D[h] : 0.f;
-    const bool vec = ((reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 7) == 0;
 #pragma unroll 1
-    for (int k = 0; k < ntok; ++k) {
-        const int64_t bk = (int64_t)b * ntok + k;  // (batch, token) row of the (batch, K, ...) layouts
-        const float dtv = dt[bk * nheads + h];
-        const float a = expf(dtv * Ah);
-        const __nv_bfloat16* Bg = B + (bk * ngroups + g) * N;
-        const __nv_bfloat16* Cg = C + (bk * ngroups + g) * N;
-        float bv[K::NV][4], cv[K::NV][4];
+    for (int k0 = 0, j = 0; k0 < ntok; k0 += K::KT, ++j) {
+        const int cnt = (ntok - k0 < K::KT) ? ntok - k0 : K::KT;
+        if (k0 + K::KT < ntok) {  // the next group fills the other buffer while this one is used
+            stage((j + 1) & 1, k0 + K::KT, (ntok - k0 - K::KT < K::KT) ? ntok - k0 - K::KT : K::KT);
+            cp_async_wait_group<1>();
+        } else {
+            cp_async_wait_group<0>();
+        }
+        __syncthreads();  // every thread's copies of this group have landed
+        const uint8_t* sb = sbuf + (j & 1) * K::SZ;
+#pragma unroll 1
+        for (int kk = 0; kk < cnt; ++kk) {
+            const int64_t bk = (int64_t)b * ntok + k0 + kk;  // (batch, token) row of the (batch, K, ...) layouts
+            const float dtv = reinterpret_cast<const float*>(sb + K::OFF_DT)[kk];
+            const float a = expf(dtv * Ah);
+            const __nv_bfloat16* Bg = reinterpret_cast<const __nv_bfloat16*>(sb + kk * N * 2);
+            const __nv_bfloat16* Cg = reinterpret_cast<const __nv_bfloat16*>(sb + K::OFF_C + kk * N * 2);
+            float bv[K::NV][4], cv[K::NV][4];
 #pragma unroll
-        for (int v = 0; v < K::NV; ++v) {
-            const int n0 = 4 * ln + v * 4 * K::LPR;
-            if (vec) {  // four bf16 in one 8-byte load
-                const uint2 bq = *reinterpret_cast<const uint2*>(Bg + n0);
+            for (int v = 0; v < K::NV; ++v) {
+                const int n0 = 4 * ln + v * 4 * K::LPR;
+                const uint2 bq = *reinterpret_cast<const uint2*>(Bg + n0);  // four bf16 in one 8-byte load
                 const uint2 cq = *reinterpret_cast<const uint2*>(Cg + n0);
                 const uint32_t bw[2] = {bq.x, bq.y}, cw[2] = {cq.x, cq.y};
 #pragma unroll
@@ -290,39 +359,41 @@ __global__ void __launch_bounds__(MultiCfg<N>::THREADS) ssd_step_multi_kernel(
                     bv[v][e] = __uint_as_float((e & 1) ? (bw[e >> 1] & 0xffff0000u) : (bw[e >> 1] << 16)) * dtv;
                     cv[v][e] = __uint_as_float((e & 1) ? (cw[e >> 1] & 0xffff0000u) : (cw[e >> 1] << 16));
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    bv[v][e] = __bfloat162float(Bg[n0 + e]) * dtv;
-                    cv[v][e] = __bfloat162float(Cg[n0 + e]);
-                }
             }
+            // the warp's consecutive x values in one load (the same for all its lanes)
+            const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(sb + K::OFF_X + kk * P * 2) +
+                                      warp * K::XW;
+            __nv_bfloat16 xw[K::XW];
+            if constexpr (K::XW == 8) {
+                *reinterpret_cast<uint4*>(xw) = *reinterpret_cast<const uint4*>(xs);
+            } else {
+                *reinterpret_cast<uint2*>(xw) = *reinterpret_cast<const uint2*>(xs);
+            }
+            __nv_bfloat16* yr = y + (bk * nheads + h) * P;
+            float xp[K::SLOTS], acc[K::SLOTS];
+#pragma unroll
+            for (int i = 0; i < K::SLOTS; ++i) {
+                xp[i] = __bfloat162float(xw[i * K::RPS + sub]);
+                float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int v = 0; v < K::NV; ++v) step4(s[i][v], a, xp[i], bv[v], cv[v], acc2);
+                acc[i] = acc2.x + acc2.y;
+            }
+            int i = 0;  // the row (slot) whose full sum this lane ends up holding
+            const float tot = fold_rows<K::SLOTS, K::LPR / 2>(acc, ln, i);
+            float xi = xp[0];
+#pragma unroll
+            for (int j2 = 1; j2 < K::SLOTS; ++j2) xi = (i == j2) ? xp[j2] : xi;
+            if ((ln & (K::LPR / K::SLOTS - 1)) == 0)
+                yr[row(i)] = __float2bfloat16_rn(step_output(tot, xi, Dh, 0, 0, OutOpts()));
         }
-        const __nv_bfloat16* xr = x + (bk * nheads + h) * P;
-        __nv_bfloat16* yr = y + (bk * nheads + h) * P;
-        float xp[K::SLOTS], acc[K::SLOTS];
-#pragma unroll
-        for (int i = 0; i < K::SLOTS; ++i) {
-            xp[i] = __bfloat162float(xr[(i * K::W + warp) * K::RPS + sub]);
-            float2 acc2 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int v = 0; v < K::NV; ++v) step4(s[i][v], a, xp[i], bv[v], cv[v], acc2);
-            acc[i] = acc2.x + acc2.y;
-        }
-        int i = 0;  // the row (slot) whose full sum this lane ends up holding
-        const float tot = fold_rows<K::SLOTS, K::LPR / 2>(acc, ln, i);
-        float xi = xp[0];
-#pragma unroll
-        for (int j = 1; j < K::SLOTS; ++j) xi = (i == j) ? xp[j] : xi;
-        if ((ln & (K::LPR / K::SLOTS - 1)) == 0)
-            yr[(i * K::W + warp) * K::RPS + sub] = __float2bfloat16_rn(step_output(tot, xi, Dh, 0, 0, OutOpts()));
+        __syncthreads();  // this buffer is refilled two groups on
     }
 #pragma unroll
     for (int i = 0; i < K::SLOTS; ++i)
 #pragma unroll
         for (int v = 0; v < K::NV; ++v)
-            *reinterpret_cast<float4*>(st + (int64_t)((i * K::W + warp) * K::RPS + sub) * N + 4 * ln +
-                                       v * 4 * K::LPR) = s[i][v];
+            *reinterpret_cast<float4*>(st + (int64_t)row(i) * N + 4 * ln + v * 4 * K::LPR) = s[i][v];
 }
 
 }  // namespace
@@ -330,23 +401,25 @@ __global__ void __launch_bounds__(MultiCfg<N>::THREADS) ssd_step_multi_kernel(
 int launch_step_multi(const __nv_bfloat16* x, const float* dt, const float* A, const __nv_bfloat16* B,
                       const __nv_bfloat16* C, const float* D, float* state, int batch, int ntok, int nheads,
                       int ngroups, int dstate, __nv_bfloat16* y, cudaStream_t s) {
+    // one token: the one-token kernel (the same arithmetic and bits; nothing to stage)
+    if (ntok == 1) return launch_step(x, dt, A, B, C, D, state, batch, nheads, ngroups, dstate, y, s, DtOpts(), OutOpts());
     dim3 grid(nheads, batch);
     launch_begin(kKindStep, s);
     switch (dstate) {
         case 64:
-            ssd_step_multi_kernel<64><<<grid, MultiCfg<64>::THREADS, 0, s>>>(x, dt, A, B, C, D, state, ntok, nheads,
+            ssd_step_multi_kernel<64><<<grid, MultiCfg<64>::THREADS, 2 * MultiCfg<64>::SZ, s>>>(x, dt, A, B, C, D, state, ntok, nheads,
                                                                              ngroups, y);
             break;
         case 128:
-            ssd_step_multi_kernel<128><<<grid, MultiCfg<128>::THREADS, 0, s>>>(x, dt, A, B, C, D, state, ntok,
+            ssd_step_multi_kernel<128><<<grid, MultiCfg<128>::THREADS, 2 * MultiCfg<128>::SZ, s>>>(x, dt, A, B, C, D, state, ntok,
                                                                                nheads, ngroups, y);
             break;
         case 256:
-            ssd_step_multi_kernel<256><<<grid, MultiCfg<256>::THREADS, 0, s>>>(x, dt, A, B, C, D, state, ntok,
+            ssd_step_multi_kernel<256><<<grid, MultiCfg<256>::THREADS, 2 * MultiCfg<256>::SZ, s>>>(x, dt, A, B, C, D, state, ntok,
                                                                                nheads, ngroups, y);
             break;
         case 512:
-            ssd_step_multi_kernel<512><<<grid, MultiCfg<512>::THREADS, 0, s>>>(x, dt, A, B, C, D, state, ntok,
+            ssd_step_multi_kernel<512><<<grid, MultiCfg<512>::THREADS, 2 * MultiCfg<512>::SZ, s>>>(x, dt, A, B, C, D, state, ntok,
                                                                                nheads, ngroups, y);
             break;
         default: return SSD_ERR_UNSUPPORTED;

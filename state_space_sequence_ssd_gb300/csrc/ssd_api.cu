@@ -217,15 +217,23 @@ int workspace_alloc(void** ptr, size_t bytes, cudaStream_t s) {
     return SSD_OK;
 }
 
+int device_sms();
+
 // Chunks per span for ssd_forward: about eight waves of 152 CTAs over
 // (batch, head, span), so the span-level intermediates stay small while
-// every SM stays busy.
+// every SM stays busy -- or, when a span of at most 64 chunks makes chunk_state's grid
+// (batch, heads / heads per CTA, spans) fit one CTA per SM, the shortest such span: chunk_state then
+// runs its CTAs all at once with twice the stages in flight, and the hop has fewer spans to cross.
 int forward_span_chunks(const Dims& d) {
     const int64_t units = (int64_t)d.batch * d.hcount * d.nchunks;
     int64_t k = (units + 1215) / 1216;
     if (k < 1) k = 1;
     if (k > 64) k = 64;
     if (k > d.nchunks) k = d.nchunks;
+    const int64_t rows = (int64_t)d.batch * (d.hcount / chunk_state_heads_per_cta(d));
+    const int sms = device_sms();
+    for (int64_t k1 = k; k1 <= 64 && k1 <= d.nchunks; ++k1)
+        if (rows * ceil_div64(d.nchunks, k1) <= sms) return (int)k1;
     return (int)k;
 }
 
