@@ -162,8 +162,14 @@ def test_forward_plan_is_consistent(lib, b, L, H, N, G, Q):
 
 
 def test_forward_plan_known_shapes(lib):
-    # ~1216 (batch, head, chunk) units per span wave: L 65536 x 32 heads -> 7-chunk spans
-    assert plan(lib, 1, 65536, 32, 128, 1, 256)[1] == 7
+    # the shortest span whose chunk_state grid (batch, heads / 4, spans) fits one CTA per SM of a 152-SM
+    # device: L 65536 x 32 heads -> 8 x 19 = 152 CTAs of 14 chunks
+    assert plan(lib, 1, 65536, 32, 128, 1, 256)[1] == 14
+    assert plan(lib, 2, 4096, 64, 128, 1, 256)[1] == 4      # 2 x 16 x 4 = 128 CTAs
+    assert plan(lib, 1, 16384, 32, 256, 1, 256)[1] == 8     # two heads per CTA at N 256: 16 x 8 = 128
+    # no span of at most 64 chunks fits: ~1216 (batch, head, chunk) units per span wave
+    assert plan(lib, 8, 65536, 32, 128, 1, 256)[1] == 54
+    assert plan(lib, 1, 262144, 32, 256, 8, 256)[1] == 27
     assert plan(lib, 1, 512, 4, 64, 1, 64)[1:3] == (1, 1)  # 32 CTAs: nothing to merge
     assert plan(lib, 2, 4096, 64, 128, 1, 256)[3] <= _ffi.SSD_NOALLOC_SCRATCH_BYTES  # 40 MiB fits
     assert plan(lib, 1, 65536, 32, 128, 1, 256)[3] > _ffi.SSD_NOALLOC_SCRATCH_BYTES  # 85 MiB does not
@@ -173,14 +179,17 @@ def test_forward_plan_known_shapes(lib):
 
 
 def test_forward_plan_run_lengths(lib):
-    """compute_out's run length on a 152-SM device (the value used when no device can be queried): runs
-    of four spans where the waves are few and a longer run saves pipeline fills -- even when the longer
-    runs leave SMs idle in one wave (2 x 4096, 64 heads: 128 CTAs of two heads in one wave beat 256 in
-    two, 88.0 against 94.7 us measured on GB300); one span when the batch is large enough that the fills
-    are spread over many waves anyway."""
-    assert plan(lib, 1, 65536, 32, 128, 1, 256)[2] == 4       # 37 spans of 7 chunks -> 10 runs per head
-    assert plan(lib, 2, 4096, 64, 128, 1, 256)[2] == 4
-    assert plan(lib, 1, 16384, 32, 64, 1, 256)[2] == 4
+    """compute_out's run length (span x step, in chunks) on a 152-SM device (the value used when no device
+    can be queried): long runs where the waves are few and a longer run saves pipeline fills -- even when
+    the longer runs leave SMs idle in one wave (2 x 4096, 64 heads: 128 CTAs of two heads in one wave beat
+    256 in two, 88.0 against 94.7 us measured on GB300); one span when the batch is large enough that the
+    fills are spread over many waves anyway."""
+    def run(*a):
+        r = plan(lib, *a)
+        return r[1] * r[2]
+    assert run(1, 65536, 32, 128, 1, 256) == 28   # 10 runs per head pair: 9 of 28 chunks and one of 4
+    assert run(2, 4096, 64, 128, 1, 256) == 8
+    assert run(1, 16384, 32, 64, 1, 256) == 8
     assert plan(lib, 8, 65536, 32, 128, 1, 256)[2] == 1       # 54-chunk spans, eight waves of CTAs
     assert plan(lib, 1, 512, 4, 64, 1, 64)[2] == 1            # 16 one-chunk CTAs: longer runs only serialize them
 
