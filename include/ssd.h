@@ -306,7 +306,10 @@ SSD_API int ssd_backward(const void* x, const float* dt, const float* A, const v
  * workload of these sizes, without touching device memory or launching
  * anything (a host-side query; no counterpart in the pages):
  *   span_chunks    chunks per span of the state stages (chunk_state runs
- *                  one CTA per span, state_passing hops over spans);
+ *                  one CTA per span and few heads, state_passing hops over
+ *                  spans): the shortest span of at most 64 chunks whose
+ *                  chunk_state grid fits one CTA per multiprocessor, else
+ *                  about eight waves of (batch, head, span) units;
  *   scan_step      spans per compute_out CTA (1, 2 or 4), chosen from the
  *                  current device's multiprocessor count (152 when no
  *                  device can be queried);
