@@ -129,26 +129,6 @@ __global__ void __launch_bounds__(StCfg<N, HH, ONE>::THREADS, StCfg<N, HH, ONE>:
     }
     grid_dep_wait();  // dA_cumsum, dt and the float16 B come from the previous launch
     grid_dep_launch_dependents();
-    if (warp < HH) {
-        // head h0 + warp: per chunk c of the span, R_c + cs[c][Q-1] = sum of the chunk totals
-        // from c to the span end (an inclusive suffix sum), 32 chunks per round, one load per lane
-        const int64_t row = (int64_t)b * HC + h0 + warp;
-        const float* csr = a.cs + row * rowlen;
-        float carry = 0.f;
-        for (int base = nchk - 32; base > -32; base -= 32) {
-            const int c = base + lane;
-            float v = (c >= 0) ? csr[(c_first + c) * Q + Q - 1] : 0.f;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {  // suffix scan: add the lanes above
-                const float o = __shfl_down_sync(0xffffffffu, v, off);
-                if (lane + off < 32) v += o;
-            }
-            v += carry;
-            if (c >= 0) Rs[warp * kMaxSpanChunks + c] = v;
-            carry = __shfl_sync(0xffffffffu, v, 0);
-        }
-        if (lane == 0 && a.span_decay != nullptr) a.span_decay[row * a.nspans + s] = carry;
-    }
     if (K::SZ_ZERO > 0) {
         uint4* z = reinterpret_cast<uint4*>(smem + K::OFF_ZERO);
         for (int i = threadIdx.x; i < K::SZ_ZERO / 16; i += K::THREADS) z[i] = make_uint4(0, 0, 0, 0);
@@ -227,7 +207,30 @@ __global__ void __launch_bounds__(StCfg<N, HH, ONE>::THREADS, StCfg<N, HH, ONE>:
         }
     } else {
         // scaling warpgroup(s): thread t scales token row t % TB of the x tiles of heads
-        // hh = t / TB, t / TB + 128 SW / TB, ... in place; afterwards thread t stores TMEM lane t % 128
+        // hh = t / TB, t / TB + 128 SW / TB, ... in place; afterwards thread t stores TMEM lane t % 128.
+        // First (not in reverse-time mode, which weights by 2^(cs) alone): warp hh < HH forms head
+        // h0 + hh's R_c + cs[c][Q-1] per chunk c of the span -- the sum of the chunk totals from c to the
+        // span end (an inclusive suffix sum), 32 chunks per round, one load per lane -- while the first
+        // stages load.
+        if (warp < HH && (!a.rev || a.span_decay != nullptr)) {
+            const int64_t row = (int64_t)b * HC + h0 + warp;
+            const float* csr = a.cs + row * rowlen;
+            float carry = 0.f;
+            for (int base = nchk - 32; base > -32; base -= 32) {
+                const int c = base + lane;
+                float v = (c >= 0) ? csr[(c_first + c) * Q + Q - 1] : 0.f;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {  // suffix scan: add the lanes above
+                    const float o = __shfl_down_sync(0xffffffffu, v, off);
+                    if (lane + off < 32) v += o;
+                }
+                v += carry;
+                if (c >= 0) Rs[warp * kMaxSpanChunks + c] = v;
+                carry = __shfl_sync(0xffffffffu, v, 0);
+            }
+            if (lane == 0 && a.span_decay != nullptr) a.span_decay[row * a.nspans + s] = carry;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(128 * K::SW) : "memory");  // the scaling warps only
         const int r = threadIdx.x & 127;
         const int hsel = threadIdx.x >> 7;
         const int rr = threadIdx.x % K::TB;
