@@ -40,9 +40,12 @@
 // the conversions (x and dy to float16 tiles, the two scaled tiles 2^c dy and dt 2^(c_e - c) x, h0 and
 // mu to float16), the mask (one thread per row and column quarter: M' = L o C B^T and Wd to float16
 // tiles) and the epilogue, one after another.  One more warp issues the products, each as soon as the
-// phase that writes its operands has signalled (mbarriers both ways): C B^T and dY X^T before the mask,
-// the unmasked dC / dB terms during it, G, B mu and C h0 after it, then the masked dC / dB terms and
-// the next head's C B^T while the workers run the epilogue and the next head's conversions.  The next
+// phase that writes its operands has signalled (mbarriers both ways): dY X^T once x and dy are in
+// float16 (before the scaled rows), the unmasked dC / dB terms during the mask, B mu and C h0 once the
+// mask has read C B^T and dY X^T, G after it, then the masked dC / dB terms and the next head's C B^T
+// while the workers run the epilogue and the next head's conversions.  Another warp runs the
+// dt-gradient scans of each head from the epilogue's per-row partial sums, while the workers go on
+// to the next head (they wait for it only before the next mask overwrites those sums).  The next
 // head's inputs (raw x and dy rows, its h0 and mu -- already float16, in the tiles' swizzled order --
 // its dA_cumsum and dt rows, D and A) are copied with cp.async into tiles the products have finished
 // with as soon as they retire, so their loads overlap the epilogue.
@@ -60,7 +63,8 @@ constexpr int T = kBwdBlock;     // tokens per block = the products' M
 constexpr int kP = 64;           // headdim
 constexpr int kWorkers = 512;    // four warpgroups: warp w owns TMEM lanes 32 (w % 4) .. +31, column quarter w / 4
 constexpr int kIssuerWarp = kWorkers / 32;  // one more warp: its first thread issues the products
-constexpr int kThreads = kWorkers + 32;
+constexpr int kScanWarp = kIssuerWarp + 1;  // and another: the dt-gradient scans of each head
+constexpr int kThreads = kWorkers + 64;
 constexpr int kNQ = kWorkers / 128;  // column quarters of a row (mask, epilogue) and row parts (conversions)
 constexpr int kPanel = T * 128;  // one 64-column float16 panel of a T-row tile (16 KB)
 constexpr int kPanelP = kP * 128;  // one 64-column float16 panel of a P-row tile (8 KB)
@@ -79,7 +83,7 @@ struct BwdCfg {
     static constexpr int OFF_M = OFF_MU + NP * kPanelP;  // M' [r][i]; the epilogue's reductions after the products
     static constexpr int OFF_W = OFF_M + 2 * kPanel;     // Wd [r][j]
     static constexpr int OFF_CS = OFF_W + 2 * kPanel;    // cs[T], dt[T]
-    static constexpr int OFF_BAR = OFF_CS + 2 * T * 4;   // nine mbarriers, TMEM base, abort flag, warp sums
+    static constexpr int OFF_BAR = OFF_CS + 2 * T * 4;   // eleven mbarriers, TMEM base, abort flag, warp sums
     static constexpr int SMEM = OFF_BAR + 192 + 1024;    // + slack to align the base to 1024 bytes
     static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -99,7 +103,7 @@ struct BwdArgs {
     const __half *h0, *mu;  // block-start states and block-end gradients, float16 (b, nblk, H, P, N)
     const float* A;
     __nv_bfloat16* dx;
-    float *ddt, *dB, *dC, *dap, *xdy;  // dap, xdy: per (b, h, block) four partial sums of dt dl and x . dy
+    float *ddt, *dB, *dC, *dap, *xdy;  // dap, xdy: per (b, h, block) partial sums of dt dl and x . dy
     Dims d;
     Ctl ctl;
     int slices;  // S: CTAs (a cluster) per (block, group), each with hpg / S heads
@@ -161,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     // workers -> issuer, one arrival per worker warp and head: the float16 x and dy tiles are written; all
     // float16 input tiles are written; the mask
     // has read C B^T and dY X^T; M' and Wd are written; G, B mu and C h0 are read
+    uint64_t *ev_red = bar + 20, *ev_scanned = bar + 21;  // the epilogue's partial sums are in place; scanned
     uint64_t *ev_xd = bar + 19, *ev_in = bar + 1, *ev_tfree = bar + 7, *ev_mask = bar + 2, *ev_epi = bar + 3;
     // issuer -> workers, one commit per head: C B^T and dY X^T; G, B mu and C h0; and, once, every product
     uint64_t *mm1 = bar + 4, *mm2 = bar + 5, *mm_done = bar + 6;
@@ -189,6 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     if (tid == 0) {
         mbar_init(stall_bar, 1);
         mbar_init(ev_xd, kWorkers / 32);
+        mbar_init(ev_red, kWorkers / 32);
+        mbar_init(ev_scanned, 1);
         mbar_init(ev_in, kWorkers / 32);
         mbar_init(ev_tfree, kWorkers / 32);
         mbar_init(ev_mask, kWorkers / 32);
@@ -257,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         cp_async16(sC + so, a.C16 + o, nb);
     }
     cp_async_commit();
-    if (warp != kIssuerWarp) {
+    if (warp < kIssuerWarp) {
         prefetch(g * hpg + slice * hps);
         asm volatile("cp.async.wait_group 1;" ::: "memory");  // B and C landed; the head's inputs may not have
     } else {
@@ -349,6 +356,74 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
             fin = mbar_wait_drain(mm_done, 0, err, 63, kDrainNs);
         }
         __syncwarp();
+    } else if (warp == kScanWarp) {
+        // ---- per head, the dt-gradient scans over the block's tokens (lane l: tokens 4 l .. 4 l + 3), from
+        // the partial sums the workers' epilogue leaves in the M' tile: quantity q of token t, quarter qc at
+        // red[(q kNQ + qc) T + t] (x . G, x . B mu, dy . C h0, the rho1 pairs, x . dy), then c_e, 2^(c_e),
+        // <mu, h0> and A.  dl_t = 2^(c_e) <mu, h0> + (v before t) + (w from t on).
+        const float* red = reinterpret_cast<const float*>(smem + K::OFF_M);
+#pragma unroll 1
+        for (int k = 0; k < hps && ok; ++k) {
+            const int h = g * hpg + slice * hps + k;
+            if (!(ok = mbar_wait_bounded(ev_red, k & 1, abort_flag, err, 69, wait_ns))) break;
+            const float* tail = red + 5 * kNQ * T;
+            const float ce = tail[0], ece = tail[1], hmu_all = tail[2], Ah = tail[3];
+            const int64_t crow = ((int64_t)b * H + h) * rowlen + t0;
+            auto qsum = [&](int q, int t) {  // over the quarters, in a fixed order
+                const float* rq = red + q * kNQ * T + t;
+                return (rq[0] + rq[T]) + (rq[2 * T] + rq[3 * T]);
+            };
+            float sfull[4], v[4], w[4], dtl[4], epv[4], epw[4];
+            float pv = 0.f, pw = 0.f, xd = 0.f;  // this lane's running sums
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = 4 * lane + j;
+                const float cst = __ldg(a.cs + crow + t), dtt = __ldg(a.dtt + crow + t);
+                const float ex = fast_exp2(ce - cst);
+                const float sgt = qsum(0, t), smt = qsum(1, t);
+                sfull[j] = fmaf(ex, smt, sgt);                                     // x_t . G_t
+                v[j] = dtt * ex * smt;                                             // mu's part, at token t
+                w[j] = fmaf(fast_exp2(cst), qsum(2, t), qsum(3, t)) - dtt * sgt;  // rho2 + rho1 - sigma
+                dtl[j] = dtt;
+                xd += qsum(4, t);
+                epv[j] = pv;
+                epw[j] = pw;
+                pv += v[j];
+                pw += w[j];
+            }
+            float iv = pv, iw = pw;  // inclusive scans of the lanes' totals
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float ov = __shfl_up_sync(0xffffffffu, iv, off);
+                const float ow = __shfl_up_sync(0xffffffffu, iw, off);
+                if (lane >= off) {
+                    iv += ov;
+                    iw += ow;
+                }
+            }
+            const float bv = iv - pv, bw = iw - pw;           // the lanes before this one
+            const float tw = __shfl_sync(0xffffffffu, iw, 31);  // all of w
+            float da = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = 4 * lane + j;
+                const float dl = fmaf(ece, hmu_all, (bv + epv[j]) + (tw - (bw + epw[j])));
+                if (t0 + t < L) a.ddt[((b * L + t0 + t) * H + h)] = fmaf(Ah, dl, sfull[j]);
+                da = fmaf(dtl[j], dl, da);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                da += __shfl_xor_sync(0xffffffffu, da, off);
+                xd += __shfl_xor_sync(0xffffffffu, xd, off);
+            }
+            __syncwarp();  // every lane's reads of the partial sums are done
+            if (lane == 0) {
+                const int64_t o = ((int64_t)b * H + h) * d.nchunks + blk;
+                a.dap[o] = da;
+                a.xdy[o] = xd;
+                mbar_arrive(ev_scanned);
+            }
+        }
     } else {
 #pragma unroll 1
         for (int k = 0; k < hps && ok; ++k) {
@@ -363,36 +438,33 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
             }
             worker_sync();
             const float ce = scs[T - 1];
-            // N = 64: x and dy to float16 first, so that dY X^T starts while the scaled rows are written (a
-            // second read of the raw rows).  N = 128: one pass, both signals after it -- the split costs more
-            // registers than that kernel has at this thread count, and the spills it causes are slower.
+            // x and dy to float16 first, so that dY X^T starts while the scaled rows are written (a second
+            // read of the raw rows)
             {
                 const int rr = tid & (T - 1), hl = tid >> 7;  // row, quarter of the row's 64 channels
+#pragma unroll
+                for (int j = 0; j < 8 / kNQ; ++j) {
+                    const uint32_t so = sw128_offset(rr, (8 / kNQ) * hl + j);
+                    const uint4 xv = *reinterpret_cast<const uint4*>(smem + K::OFF_XS + so);
+                    const uint4 yv = *reinterpret_cast<const uint4*>(smem + K::OFF_DYS + so);
+                    const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+                    const uint32_t* yw = reinterpret_cast<const uint32_t*>(&yv);
+                    uint32_t ox[4], oy[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 xf = bf2_to_f2(xw[e]), yf = bf2_to_f2(yw[e]);
+                        ox[e] = pack_f16x2(xf.x, xf.y);
+                        oy[e] = pack_f16x2(yf.x, yf.y);
+                    }
+                    hmax_abs4(mx, ox[0], ox[1], ox[2], ox[3]);
+                    hmax_abs4(mx, oy[0], oy[1], oy[2], oy[3]);
+                    *reinterpret_cast<uint4*>(smem + K::OFF_X + so) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
+                    *reinterpret_cast<uint4*>(smem + K::OFF_DY + so) = make_uint4(oy[0], oy[1], oy[2], oy[3]);
+                }
+                fence_proxy_async_smem();
+                warp_arrive(ev_xd);
                 const float wx = sdt[rr] * fast_exp2(ce - scs[rr]);
                 const float wy = fast_exp2(scs[rr]);
-                if constexpr (N == 64) {
-#pragma unroll
-                    for (int j = 0; j < 8 / kNQ; ++j) {
-                        const uint32_t so = sw128_offset(rr, (8 / kNQ) * hl + j);
-                        const uint4 xv = *reinterpret_cast<const uint4*>(smem + K::OFF_XS + so);
-                        const uint4 yv = *reinterpret_cast<const uint4*>(smem + K::OFF_DYS + so);
-                        const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
-                        const uint32_t* yw = reinterpret_cast<const uint32_t*>(&yv);
-                        uint32_t ox[4], oy[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 xf = bf2_to_f2(xw[e]), yf = bf2_to_f2(yw[e]);
-                            ox[e] = pack_f16x2(xf.x, xf.y);
-                            oy[e] = pack_f16x2(yf.x, yf.y);
-                        }
-                        hmax_abs4(mx, ox[0], ox[1], ox[2], ox[3]);
-                        hmax_abs4(mx, oy[0], oy[1], oy[2], oy[3]);
-                        *reinterpret_cast<uint4*>(smem + K::OFF_X + so) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
-                        *reinterpret_cast<uint4*>(smem + K::OFF_DY + so) = make_uint4(oy[0], oy[1], oy[2], oy[3]);
-                    }
-                    fence_proxy_async_smem();
-                    warp_arrive(ev_xd);
-                }
 #pragma unroll
                 for (int j = 0; j < 8 / kNQ; ++j) {
                     const uint32_t so = sw128_offset(rr, (8 / kNQ) * hl + j);
@@ -403,27 +475,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                     uint32_t oxs[4], oys[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 xf = bf2_to_f2(xw[e]), yf = bf2_to_f2(yw[e]);
-                        const float2 xs = fmul2(xf, make_float2(wx, wx));
+                        const float2 xs = fmul2(bf2_to_f2(xw[e]), make_float2(wx, wx));
                         oxs[e] = pack_f16x2(xs.x, xs.y);
-                        const float2 ys = fmul2(yf, make_float2(wy, wy));
+                        const float2 ys = fmul2(bf2_to_f2(yw[e]), make_float2(wy, wy));
                         oys[e] = pack_f16x2(ys.x, ys.y);
                     }
                     hmax_abs4(mx, oxs[0], oxs[1], oxs[2], oxs[3]);
                     hmax_abs4(mx, oys[0], oys[1], oys[2], oys[3]);
-                    if constexpr (N != 64) {
-                        uint32_t ox[4], oy[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 xf = bf2_to_f2(xw[e]), yf = bf2_to_f2(yw[e]);
-                            ox[e] = pack_f16x2(xf.x, xf.y);
-                            oy[e] = pack_f16x2(yf.x, yf.y);
-                        }
-                        hmax_abs4(mx, ox[0], ox[1], ox[2], ox[3]);
-                        hmax_abs4(mx, oy[0], oy[1], oy[2], oy[3]);
-                        *reinterpret_cast<uint4*>(smem + K::OFF_X + so) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
-                        *reinterpret_cast<uint4*>(smem + K::OFF_DY + so) = make_uint4(oy[0], oy[1], oy[2], oy[3]);
-                    }
                     *reinterpret_cast<uint4*>(smem + K::OFF_XS + so) = make_uint4(oxs[0], oxs[1], oxs[2], oxs[3]);
                     *reinterpret_cast<uint4*>(smem + K::OFF_DYS + so) = make_uint4(oys[0], oys[1], oys[2], oys[3]);
                 }
@@ -448,10 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
             for (int off = 16; off > 0; off >>= 1) hmu += __shfl_xor_sync(0xffffffffu, hmu, off);
             if (lane == 0) wsum[warp] = hmu;
             fence_proxy_async_smem();  // the tiles written here (and the copies landed) are read by the products
-            if constexpr (N != 64) warp_arrive(ev_xd);
             warp_arrive(ev_in);
-            // ---- C B^T and dY X^T
+            // ---- C B^T and dY X^T; and the previous head's scans have read the partial sums in the M' tile
             ok = mbar_wait_bounded(mm1, par, abort_flag, err, 61, wait_ns);
+            if (k > 0) ok = ok && mbar_wait_bounded(ev_scanned, par ^ 1, abort_flag, err, 70, wait_ns);
             ok = worker_and(ok);
             if (!ok) break;
             tc_fence_after();
@@ -571,84 +629,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                 red[(2 * kNQ + qc) * T + r] = rho22.x + rho22.y;
                 red[(3 * kNQ + qc) * T + r] = rho1p.x + rho1p.y;
                 red[(4 * kNQ + qc) * T + r] = xdy2.x + xdy2.y;
-                worker_sync();
-                // the scans over the block's tokens run on warps 1-4 (token t = tid - 32, scan warp sw = warp - 1)
-                const int sw = warp - 1;
-                const bool scan = tid >= 32 && tid < 32 + T;
-                float* wtot = red + 5 * kNQ * T;  // per-warp totals of the scans: [v or w][scan warp]
-                // quantity q of row t summed over the quarters, in a fixed order
-                auto qsum = [&](int q, int t) {
-                    const float* rq = red + q * kNQ * T + t;
-                    return (rq[0] + rq[T]) + (rq[2 * T] + rq[3 * T]);
-                };
-                float v = 0.f, wv = 0.f, pv = 0.f, pw = 0.f, sfull = 0.f, dtl = 0.f, xd = 0.f;
-                float Ah = 0.f;  // read before the barrier below: thread 0 sets the next head's once past it
-                if (scan) {
-                    const int t = tid - 32;
-                    Ah = hconst[1];
-                    const float dtt = sdt[t], ex = fast_exp2(ce - scs[t]);
-                    const float sgt = qsum(0, t), smt = qsum(1, t);
-                    sfull = fmaf(ex, smt, sgt);                      // x_t . G_t
-                    v = dtt * ex * smt;                              // mu's part, at token t
-                    wv = fmaf(fast_exp2(scs[t]), qsum(2, t),         // rho2 + rho1 - sigma
-                              qsum(3, t)) - dtt * sgt;
-                    dtl = dtt;
-                    xd = qsum(4, t);
-                    // inclusive scans of v and w inside the warp
-                    pv = v;
-                    pw = wv;
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const float ov = __shfl_up_sync(0xffffffffu, pv, off);
-                        const float ow = __shfl_up_sync(0xffffffffu, pw, off);
-                        if (lane >= off) {
-                            pv += ov;
-                            pw += ow;
-                        }
-                    }
-                    if (lane == 31) {
-                        wtot[sw] = pv;
-                        wtot[4 + sw] = pw;
-                    }
-                }
-                worker_sync();
-                if (scan) {
-                    const int t = tid - 32;
-                    float bv = 0.f, bw = 0.f, tw = 0.f;  // earlier warps' totals; all of w
-#pragma unroll
-                    for (int k2 = 0; k2 < 4; ++k2) {
-                        if (k2 < sw) {
-                            bv += wtot[k2];
-                            bw += wtot[4 + k2];
-                        }
-                        tw += wtot[4 + k2];
-                    }
+                if (tid == 0) {  // what the scans need besides the partial sums
                     float hmu_all = 0.f;
 #pragma unroll
                     for (int w4 = 0; w4 < kWorkers / 32; w4 += 4)
                         hmu_all += (wsum[w4] + wsum[w4 + 1]) + (wsum[w4 + 2] + wsum[w4 + 3]);
-                    // dl_t = 2^(c_e) <mu, h0> + (v before t) + (w from t on)
-                    const float excl_v = bv + pv - v;
-                    const float from_t_w = tw - (bw + pw - wv);
-                    const float dl = fmaf(fast_exp2(ce), hmu_all, excl_v + from_t_w);
-                    if (t0 + t < L) a.ddt[((b * L + t0 + t) * H + h)] = fmaf(Ah, dl, sfull);
-                    float da = dtl * dl;
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        da += __shfl_xor_sync(0xffffffffu, da, off);
-                        xd += __shfl_xor_sync(0xffffffffu, xd, off);
-                    }
-                    // this scan warp's part of the block's sums: four per (b, h, block), added in order by
-                    // bwd_reduce_kernel
-                    if (lane == 0) {
-                        const int64_t o = (((int64_t)b * H + h) * d.nchunks + blk) * 4 + sw;
-                        a.dap[o] = da;
-                        a.xdy[o] = xd;
-                    }
+                    float* tail = red + 5 * kNQ * T;
+                    tail[0] = ce;
+                    tail[1] = fast_exp2(ce);
+                    tail[2] = hmu_all;
+                    tail[3] = hconst[1];
                 }
-                // no barrier here: the next head's first writes that these reads could see (its D and A,
-                // its dA_cumsum and dt rows, the <mu, h0> partials) come after values read above, or after
-                // that head's first barrier
+                warp_arrive(ev_red);  // the scan warp takes it from here; the workers go on to the next head
+                // once every worker is past its reads of this head's dA_cumsum, dt, D and A (the next head's
+                // first step writes them)
+                worker_sync();
             }
         }
         cp_async_wait_all();  // no copy is still landing when the shared memory is reused or released
@@ -659,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
     tc_fence_after();
     const int64_t tok = t0 + r;
     if (S == 1) {
-        if (ok && warp != kIssuerWarp) {
+        if (ok && warp < kIssuerWarp) {
             // dC and dB rows of this block, summed over the group's heads
 #pragma unroll 1
             for (int c = 0; c < N / 64; ++c) {  // this warp's quarter of the columns, 16 at a time
@@ -686,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
         // this CTA's partial dC and dB -> shared memory (the tiles are consumed), float32 [2][T][NS]
         constexpr int NS = N + 4;  // padded rows: the float4 stores of a warp fall on different banks
         float* acc = reinterpret_cast<float*>(smem);
-        if (ok && warp != kIssuerWarp) {
+        if (ok && warp < kIssuerWarp) {
 #pragma unroll 1
             for (int c = 0; c < N / 64; ++c) {  // this warp's quarter of the columns, 16 at a time
                 const int n0 = qc * (N / 4) + 16 * c;
@@ -765,8 +760,8 @@ __global__ void __launch_bounds__(kRedThreads) bwd_reduce_kernel(const float* __
     const int h = blockIdx.x, tid = threadIdx.x;
     float sa = 0.f, sd = 0.f;
     for (int b = 0; b < d.batch; ++b) {
-        const int64_t row = ((int64_t)b * d.nheads + h) * d.nchunks * 4;
-        for (int64_t k = tid; k < (int64_t)d.nchunks * 4; k += kRedThreads) {
+        const int64_t row = ((int64_t)b * d.nheads + h) * d.nchunks;
+        for (int64_t k = tid; k < d.nchunks; k += kRedThreads) {
             sa += dap[row + k];
             sd += xdy[row + k];
         }

@@ -665,7 +665,7 @@ int ssd_backward(const void* x, const float* dt, const float* A, const void* B, 
     if (err == nullptr) return SSD_ERR_CUDA;
     const size_t nrow = (size_t)d.batch * d.nheads * d.nchunks * kBwdBlock;        // cs and dt rows
     const size_t nst = (size_t)d.batch * d.nchunks * d.nheads * d.headdim * d.dstate;  // per-block states
-    const size_t npart = (size_t)d.batch * d.nheads * d.nchunks * 4;  // per-block partial sums, four each
+    const size_t npart = ((size_t)d.batch * d.nheads * d.nchunks + 3) & ~(size_t)3;  // per-block partial sums
     const size_t nbc = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;  // multiple of 64
     const size_t bytes = (2 * nrow + 2 * npart) * sizeof(float) + (3 * nst + 2 * nbc) * sizeof(__half);
     void* ws = nullptr;
