@@ -89,8 +89,9 @@ struct BwdCfg {
 };
 
 // TMEM columns (all 512): C B^T and dY X^T while the mask reads them, then G, B mu and C h0 in
-// their place; the dC and dB accumulators over the group's heads
-constexpr uint32_t T_CB = 0, T_DX = 128, T_G = 0, T_GMU = 64, T_YS = 128, T_DC = 256, T_DB = 384;
+// their place (B mu and C h0 over the columns the mask reads first, G over the rest); the dC and dB
+// accumulators over the group's heads
+constexpr uint32_t T_CB = 0, T_DX = 128, T_GMU = 0, T_G = 64, T_YS = 128, T_DC = 256, T_DB = 384;
 
 constexpr uint32_t kIdescTT = idesc_fp16(128, 128, false, false);  // C B^T, dY X^T: both K-major
 constexpr uint32_t kIdescG = idesc_fp16(128, 64, true, true);      // M'^T dY: both MN-major
@@ -513,20 +514,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
             ok = worker_and(ok);
             if (!ok) break;
             tc_fence_after();
-            // ---- mask: row r, columns [32 qc, 32 qc + 32) of M' = L o C B^T and Wd = L o dY X^T o dt_j,
-            //      16 at a time
+            // ---- mask: row r, columns [16 qc, 16 qc + 16) and [64 + 16 qc, 64 + 16 qc + 16) of M' = L o C B^T
+            //      and Wd = L o dY X^T o dt_j, the first 64 columns first (all warps' first pieces free the
+            //      TMEM columns of B mu and C h0)
             float2 rho1p = make_float2(0.f, 0.f);  // sum_j Wd[r][j] (C_r . B_j) over this quarter: even / odd j
             {
                 const float cr = scs[r];
-#pragma unroll 1
+#pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
-                    const int i0 = 32 * qc + 16 * c2;
+                    const int i0 = 16 * qc + 64 * c2;
                     uint32_t vcb[16], vdx[16];
                     tmem_ld16(tm + lane_base + T_CB + i0, vcb);
                     tmem_ld16(tm + lane_base + T_DX + i0, vdx);
                     tmem_ld_wait16(vcb);
                     tmem_ld_wait16(vdx);
-                    if (c2 == 1) {  // this warp's last reads of C B^T and dY X^T
+                    if (c2 == 0) {  // this warp's reads of columns 0-63 of C B^T and dY X^T
                         tc_fence_before();
                         warp_arrive(ev_tfree);
                     }
@@ -545,10 +547,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_kernel(BwdArgs a) {
                         pw[jj / 2] = pack_f16x2(wv.x, wv.y);
                     }
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {  // columns i0 .. i0 + 15: panel qc / 2, chunks 4 (qc % 2) + 2 c2 + j
+                    for (int j = 0; j < 2; ++j) {  // columns i0 .. i0 + 15: panel c2, chunks 2 qc + j
                         hmax_abs4(mx, pm[4 * j], pm[4 * j + 1], pm[4 * j + 2], pm[4 * j + 3]);
                         hmax_abs4(mx, pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
-                        const uint32_t so = (qc >> 1) * kPanel + sw128_offset(r, 4 * (qc & 1) + 2 * c2 + j);
+                        const uint32_t so = c2 * kPanel + sw128_offset(r, 2 * qc + j);
                         *reinterpret_cast<uint4*>(smem + K::OFF_M + so) =
                             make_uint4(pm[4 * j], pm[4 * j + 1], pm[4 * j + 2], pm[4 * j + 3]);
                         *reinterpret_cast<uint4*>(smem + K::OFF_W + so) =
